@@ -1,0 +1,118 @@
+"""Seeded synthetic inputs for GroupNorm forward/backward.
+
+This module only draws random numbers and lays them out in memory; it holds
+none of the normalisation arithmetic, so both the CUDA path and the fp64 oracle
+can be fed from it.  Shapes and distributions are the five workloads the
+library is measured on (activations [N, C, H, W]; N(mu, sigma) means mean mu
+and standard deviation sigma).
+
+Every tensor is returned FLAT, in its memory layout: ``"nchw"`` is
+``[(n*C + c)*HW + hw]`` and ``"nhwc"`` (channels_last) is
+``[(n*HW + hw)*C + c]``.  gamma and beta are fp32 ``[C]``.
+"""
+from __future__ import annotations
+
+import dataclasses
+
+import torch
+
+DTYPES = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
+LAYOUTS = {"nchw": 0, "nhwc": 1}
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    dtype: str          # "f32" | "f16" | "bf16"  (x, y, dy, dx)
+    layout: str         # "nchw" | "nhwc"
+    N: int
+    C: int
+    G: int
+    H: int
+    W: int
+    eps: float
+    x: tuple            # ("normal", mu, sigma)
+    dy: tuple
+    gamma: tuple        # ("normal", mu, sigma) or ("const", v)
+    beta: tuple
+    channel_offset: tuple | None = None   # ("uniform", lo, hi): one draw per channel
+
+    @property
+    def HW(self) -> int:
+        return self.H * self.W
+
+    @property
+    def E(self) -> int:
+        return self.N * self.C * self.H * self.W
+
+    def scaled(self, **kw) -> "Workload":
+        """The same distributions on another shape (for small parity cases)."""
+        return dataclasses.replace(self, **kw)
+
+
+WORKLOADS = [
+    Workload("fp32_nchw_2x32x16x16_g8", "f32", "nchw", 2, 32, 8, 16, 16, 1e-5,
+             ("normal", 0.0, 1.0), ("normal", 0.0, 1.0),
+             ("normal", 1.0, 0.1), ("normal", 0.0, 0.1)),
+    Workload("fp16_nhwc_1x128x1024x2048_g16", "f16", "nhwc", 1, 128, 16, 1024, 2048,
+             1e-5, ("normal", 0.0, 1.0), ("normal", 0.0, 1.0),
+             ("normal", 0.0, 1.0), ("normal", 0.0, 1.0)),
+    Workload("bf16_nhwc_8x320x64x64_g32", "bf16", "nhwc", 8, 320, 32, 64, 64, 1e-6,
+             ("normal", 0.5, 2.0), ("normal", 0.0, 1e-2),
+             ("normal", 1.0, 0.1), ("normal", 0.0, 0.1)),
+    Workload("fp32_nchw_112x64x512x512_g8", "f32", "nchw", 112, 64, 8, 512, 512, 1e-5,
+             ("normal", 0.0, 1.0), ("normal", 0.0, 1.0),
+             ("const", 1.0), ("const", 0.0)),
+    Workload("bf16_nhwc_32x512x32x32_g32", "bf16", "nhwc", 32, 512, 32, 32, 32, 1e-5,
+             ("normal", 0.0, 1.0), ("normal", 0.0, 1.0),
+             ("normal", 1.0, 0.1), ("normal", 0.0, 0.1),
+             channel_offset=("uniform", -4.0, 4.0)),
+]
+BY_NAME = {w.name: w for w in WORKLOADS}
+
+
+def _draw(spec, n, gen, device):
+    kind = spec[0]
+    if kind == "normal":
+        t = torch.randn(n, generator=gen, device=device, dtype=torch.float32)
+        return t.mul_(spec[2]).add_(spec[1])
+    if kind == "uniform":
+        t = torch.rand(n, generator=gen, device=device, dtype=torch.float32)
+        return t.mul_(spec[2] - spec[1]).add_(spec[1])
+    if kind == "const":
+        return torch.full((n,), float(spec[1]), device=device, dtype=torch.float32)
+    raise ValueError(spec)
+
+
+def _activation(w: Workload, spec, gen, device, offset):
+    t = _draw(spec, w.E, gen, device)
+    if offset is not None:
+        # one value per channel, shared by every n and every spatial position
+        if w.layout == "nchw":
+            t.view(w.N, w.C, w.HW).add_(offset.view(1, w.C, 1))
+        else:
+            t.view(w.N, w.HW, w.C).add_(offset.view(1, 1, w.C))
+    return t.to(DTYPES[w.dtype])
+
+
+def make_inputs(w: Workload, device="cpu", seed: int = 0, need_dy: bool = True):
+    """dict(x, dy, gamma, beta): x/dy flat in w.layout and w.dtype.
+
+    Draw order: channel offsets (if any), x, dy, gamma, beta."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    offset = None
+    if w.channel_offset is not None:
+        offset = _draw(w.channel_offset, w.C, gen, device)
+    x = _activation(w, w.x, gen, device, offset)
+    dy = _activation(w, w.dy, gen, device, None) if need_dy else None
+    gamma = _draw(w.gamma, w.C, gen, device)
+    beta = _draw(w.beta, w.C, gen, device)
+    return {"x": x, "dy": dy, "gamma": gamma, "beta": beta}
+
+
+def to_nchw_view(flat: torch.Tensor, w: Workload) -> torch.Tensor:
+    """A [N, C, HW] view of a flat tensor stored in w.layout (data movement only)."""
+    if w.layout == "nchw":
+        return flat.view(w.N, w.C, w.HW)
+    return flat.view(w.N, w.HW, w.C).permute(0, 2, 1)
