@@ -1,0 +1,211 @@
+// gn_api.cu -- the C ABI declared in include/gn.h: argument validation
+// (before anything is enqueued), planning and kernel dispatch.
+#include <atomic>
+#include <cstring>
+
+#include "../../include/gn.h"
+#include "gn_internal.h"
+
+namespace {
+
+thread_local int t_last_cuda_error = 0;
+thread_local gn::TimingEvents t_events = {nullptr, nullptr, nullptr};
+std::atomic<unsigned> g_epoch{0};
+
+unsigned next_epoch() {
+  unsigned e = g_epoch.fetch_add(1u, std::memory_order_relaxed) + 1u;
+  if (e == 0u) e = g_epoch.fetch_add(1u, std::memory_order_relaxed) + 1u;
+  return e;
+}
+
+int elem_size(int dtype) { return dtype == gn::kF32 ? 4 : 2; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// [a, a+na) and [b, b+nb) share a byte.
+bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+  if (!a || !b || na == 0 || nb == 0) return false;
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+int check_problem(int64_t N, int64_t C, int64_t HW, int64_t G, int layout, int dtype) {
+  if (layout != GN_LAYOUT_NCHW && layout != GN_LAYOUT_NHWC) return GN_ERR_UNSUPPORTED;
+  if (dtype != GN_DTYPE_F32 && dtype != GN_DTYPE_F16 && dtype != GN_DTYPE_BF16)
+    return GN_ERR_UNSUPPORTED;
+  if (N < 0 || C < 0 || HW < 0 || G <= 0) return GN_ERR_INVALID;
+  if (C % G != 0) return GN_ERR_INVALID;
+  // element offsets and per-call counts must stay far from int64 overflow
+  if (N > 0 && C > 0 && HW > 0) {
+    const double e = (double)N * (double)C * (double)HW;
+    if (e > 4.0e18) return GN_ERR_UNSUPPORTED;
+  }
+  return GN_OK;
+}
+
+int cuda_fail(cudaError_t e) {
+  t_last_cuda_error = (int)e;
+  return GN_ERR_CUDA;
+}
+
+// Plan + workspace check shared by both ops.
+int prepare(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout, int dtype,
+            bool aligned, void* workspace, size_t workspace_bytes, gn::KParams* p) {
+  std::memset(p, 0, sizeof(*p));
+  p->g = gn::make_geom(op, N, C, HW, G, layout, dtype, aligned, gn::device_sm_count());
+  if (p->g.items <= 0 || p->g.items > 0x7fffffffLL) return GN_ERR_UNSUPPORTED;
+  const gn::WsLayout w = gn::ws_layout(op, p->g);
+  if (!workspace || workspace_bytes < w.total || !aligned16(workspace)) return GN_ERR_WORKSPACE;
+  char* ws = static_cast<char*>(workspace);
+  p->tickets = reinterpret_cast<unsigned long long*>(ws + w.tickets);
+  p->err = reinterpret_cast<unsigned*>(ws + w.err);
+  p->part = reinterpret_cast<float2*>(ws + w.part);
+  p->chst = reinterpret_cast<float2*>(ws + w.chst);
+  p->coef = reinterpret_cast<float2*>(ws + w.coef);
+  p->epoch = next_epoch();
+  return GN_OK;
+}
+
+size_t ws_size_any_alignment(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout,
+                             int dtype) {
+  const int sms = gn::device_sm_count();
+  size_t best = 0;
+  for (int a = 0; a < 2; ++a) {
+    const gn::Geom g = gn::make_geom(op, N, C, HW, G, layout, dtype, a != 0, sms);
+    const size_t t = gn::ws_layout(op, g).total;
+    if (t > best) best = t;
+  }
+  return best;
+}
+
+}  // namespace
+
+namespace gn {
+const TimingEvents& timing_events() { return t_events; }
+}  // namespace gn
+
+extern "C" {
+
+size_t gn_workspace_size(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout,
+                         int dtype) {
+  if (op != GN_OP_FWD && op != GN_OP_BWD) return 0;
+  if (check_problem(N, C, HW, G, layout, dtype) != GN_OK) return 0;
+  if (N == 0 || C == 0 || HW == 0) return 0;
+  return ws_size_any_alignment(op, N, C, HW, G, layout, dtype);
+}
+
+int gn_fwd(const void* x, int64_t N, int64_t C, int64_t HW, int64_t G, int layout, int dtype,
+           const float* gamma, const float* beta, float eps, void* y, float* mean, float* rstd,
+           void* workspace, size_t workspace_bytes, void* stream) {
+  int rc = check_problem(N, C, HW, G, layout, dtype);
+  if (rc != GN_OK) return rc;
+  if (N == 0 || C == 0 || HW == 0) return GN_OK;
+  if (!x || !y || !mean || !rstd) return GN_ERR_INVALID;
+  if (!(eps >= 0.0f)) return GN_ERR_INVALID;  // rejects NaN and negative eps
+  const size_t bytes = (size_t)(N * C * HW) * (size_t)elem_size(dtype);
+  const size_t sbytes = sizeof(float) * (size_t)(N * G);
+  if (y != x && overlap(y, bytes, x, bytes)) return GN_ERR_INVALID;
+  if (overlap(mean, sbytes, x, bytes) || overlap(mean, sbytes, y, bytes) ||
+      overlap(rstd, sbytes, x, bytes) || overlap(rstd, sbytes, y, bytes) ||
+      overlap(mean, sbytes, rstd, sbytes))
+    return GN_ERR_INVALID;
+  gn::KParams p;
+  rc = prepare(GN_OP_FWD, N, C, HW, G, layout, dtype, aligned16(x) && aligned16(y), workspace,
+               workspace_bytes, &p);
+  if (rc != GN_OK) return rc;
+  p.x = x;
+  p.out = y;
+  p.gamma = gamma;
+  p.beta = beta;
+  p.mean = mean;
+  p.rstd = rstd;
+  p.eps = eps;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = layout == GN_LAYOUT_NHWC ? gn::launch_nhwc_fwd(p, s) : gn::launch_nchw_fwd(p, s);
+  return e == cudaSuccess ? GN_OK : cuda_fail(e);
+}
+
+int gn_bwd(const void* dy, const void* x, const float* mean, const float* rstd,
+           const float* gamma, int64_t N, int64_t C, int64_t HW, int64_t G, int layout,
+           int dtype, void* dx, float* dgamma, float* dbeta, void* workspace,
+           size_t workspace_bytes, void* stream) {
+  int rc = check_problem(N, C, HW, G, layout, dtype);
+  if (rc != GN_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (C == 0) return GN_OK;
+  if (N == 0 || HW == 0) {
+    // empty sums: the parameter gradients are zero
+    if (dgamma) {
+      const cudaError_t e = cudaMemsetAsync(dgamma, 0, sizeof(float) * (size_t)C, s);
+      if (e != cudaSuccess) return cuda_fail(e);
+    }
+    if (dbeta) {
+      const cudaError_t e = cudaMemsetAsync(dbeta, 0, sizeof(float) * (size_t)C, s);
+      if (e != cudaSuccess) return cuda_fail(e);
+    }
+    return GN_OK;
+  }
+  if (!dy || !x || !mean || !rstd || !dx) return GN_ERR_INVALID;
+  const size_t bytes = (size_t)(N * C * HW) * (size_t)elem_size(dtype);
+  const size_t cbytes = sizeof(float) * (size_t)C;
+  if (dx != dy && dx != x && (overlap(dx, bytes, dy, bytes) || overlap(dx, bytes, x, bytes)))
+    return GN_ERR_INVALID;
+  if (overlap(dgamma, cbytes, dx, bytes) || overlap(dbeta, cbytes, dx, bytes) ||
+      overlap(dgamma, cbytes, dbeta, cbytes))
+    return GN_ERR_INVALID;
+  gn::KParams p;
+  rc = prepare(GN_OP_BWD, N, C, HW, G, layout, dtype,
+               aligned16(x) && aligned16(dy) && aligned16(dx), workspace, workspace_bytes, &p);
+  if (rc != GN_OK) return rc;
+  p.x = x;
+  p.dy = dy;
+  p.out = dx;
+  p.gamma = gamma;
+  p.mean = const_cast<float*>(mean);
+  p.rstd = const_cast<float*>(rstd);
+  p.dgamma = dgamma;
+  p.dbeta = dbeta;
+  const cudaError_t e = layout == GN_LAYOUT_NHWC ? gn::launch_nhwc_bwd(p, s) : gn::launch_nchw_bwd(p, s);
+  return e == cudaSuccess ? GN_OK : cuda_fail(e);
+}
+
+const char* gn_status_string(int status) {
+  switch (status) {
+    case GN_OK: return "GN_OK";
+    case GN_ERR_INVALID: return "GN_ERR_INVALID: invalid problem or buffers";
+    case GN_ERR_UNSUPPORTED: return "GN_ERR_UNSUPPORTED: unsupported layout, dtype or size";
+    case GN_ERR_WORKSPACE: return "GN_ERR_WORKSPACE: workspace missing, misaligned or too small";
+    case GN_ERR_CUDA: return "GN_ERR_CUDA: a CUDA call failed";
+    default: return "unknown gn_status";
+  }
+}
+
+int gn_last_cuda_error(void) { return t_last_cuda_error; }
+
+int gn_set_timing_events(void* ev_begin, void* ev_mid, void* ev_end) {
+  t_events.begin = static_cast<cudaEvent_t>(ev_begin);
+  t_events.mid = static_cast<cudaEvent_t>(ev_mid);
+  t_events.end = static_cast<cudaEvent_t>(ev_end);
+  return GN_OK;
+}
+
+int gn_plan_info(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout, int dtype,
+                 int aligned, gn_plan_desc* out) {
+  if (!out) return GN_ERR_INVALID;
+  if (op != GN_OP_FWD && op != GN_OP_BWD) return GN_ERR_INVALID;
+  const int rc = check_problem(N, C, HW, G, layout, dtype);
+  if (rc != GN_OK) return rc;
+  std::memset(out, 0, sizeof(*out));
+  if (N == 0 || C == 0 || HW == 0) return GN_OK;
+  const gn::Geom g = gn::make_geom(op, N, C, HW, G, layout, dtype, aligned != 0, gn::device_sm_count());
+  out->regime = gn::kRegimeGeneric;
+  out->launches = 2;
+  out->vector_width = g.vw;
+  out->threads = g.tpb;
+  out->ctas = g.items;
+  out->partials = g.N * g.C * g.T;
+  out->workspace_bytes = gn::ws_layout(op, g).total;
+  return GN_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,230 @@
+// gn_device.cuh -- device-side building blocks shared by the GroupNorm kernels:
+// 16-byte vector loads/stores with L2 cache-policy hints, fp16/bf16/fp32
+// conversion, deterministic block reductions and the per-unit arrival ticket
+// used by the "last CTA finalises" reductions.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "gn_internal.h"
+
+namespace gn {
+
+// ------------------------------------------------------------ cache policies
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t pol;
+  asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t pol;
+  asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ uint64_t policy_evict_normal() {
+  uint64_t pol;
+  asm("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// Read-only 16-byte load through the non-coherent path, not kept in L1, with
+// an L2 eviction policy.  Inputs are never written while a kernel runs.
+__device__ __forceinline__ uint4 ld16(const void* p, uint64_t pol) {
+  uint4 r;
+  asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "l"(p), "l"(pol));
+  return r;
+}
+__device__ __forceinline__ void st16(void* p, const uint4& v, uint64_t pol) {
+  asm volatile("st.global.L1::no_allocate.L2::cache_hint.v4.u32 [%0], {%1,%2,%3,%4}, %5;"
+               :
+               : "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "l"(pol)
+               : "memory");
+}
+
+// ----------------------------------------------------------- element access
+template <typename T>
+struct Elem;
+template <>
+struct Elem<float> {
+  static constexpr int VEC = 4;  // elements per 16 bytes
+  __device__ static float to_f(float v) { return v; }
+  __device__ static float from_f(float v) { return v; }
+};
+template <>
+struct Elem<__half> {
+  static constexpr int VEC = 8;
+  __device__ static float to_f(__half v) { return __half2float(v); }
+  __device__ static __half from_f(float v) { return __float2half_rn(v); }
+};
+template <>
+struct Elem<__nv_bfloat16> {
+  static constexpr int VEC = 8;
+  __device__ static float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+  __device__ static __nv_bfloat16 from_f(float v) { return __float2bfloat16_rn(v); }
+};
+
+__device__ __forceinline__ void unpack16(const uint4& u, float (&f)[4], float) {
+  f[0] = __uint_as_float(u.x);
+  f[1] = __uint_as_float(u.y);
+  f[2] = __uint_as_float(u.z);
+  f[3] = __uint_as_float(u.w);
+}
+__device__ __forceinline__ float2 h2f(uint32_t w) {
+  __half2 h;
+  *reinterpret_cast<uint32_t*>(&h) = w;
+  return __half22float2(h);
+}
+__device__ __forceinline__ float2 b2f(uint32_t w) {
+  __nv_bfloat162 h;
+  *reinterpret_cast<uint32_t*>(&h) = w;
+  return __bfloat1622float2(h);
+}
+__device__ __forceinline__ uint32_t f2h(float a, float b) {
+  __half2 h = __floats2half2_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ uint32_t f2b(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Load VW consecutive elements starting at p as floats.  VW is either the
+// 16-byte vector width of T (p 16-byte aligned) or 1 (scalar path).
+template <typename T, int VW>
+struct Access;
+
+template <typename T>
+struct Access<T, 1> {
+  __device__ static void load(const T* p, float (&f)[1], uint64_t) {
+    f[0] = Elem<T>::to_f(__ldg(p));
+  }
+  __device__ static void store(T* p, const float (&f)[1], uint64_t) {
+    *p = Elem<T>::from_f(f[0]);
+  }
+};
+template <>
+struct Access<float, 4> {
+  __device__ static void load(const float* p, float (&f)[4], uint64_t pol) {
+    const uint4 u = ld16(p, pol);
+    f[0] = __uint_as_float(u.x);
+    f[1] = __uint_as_float(u.y);
+    f[2] = __uint_as_float(u.z);
+    f[3] = __uint_as_float(u.w);
+  }
+  __device__ static void store(float* p, const float (&f)[4], uint64_t pol) {
+    uint4 u;
+    u.x = __float_as_uint(f[0]);
+    u.y = __float_as_uint(f[1]);
+    u.z = __float_as_uint(f[2]);
+    u.w = __float_as_uint(f[3]);
+    st16(p, u, pol);
+  }
+};
+template <>
+struct Access<__half, 8> {
+  __device__ static void load(const __half* p, float (&f)[8], uint64_t pol) {
+    const uint4 u = ld16(p, pol);
+    float2 a = h2f(u.x), b = h2f(u.y), c = h2f(u.z), d = h2f(u.w);
+    f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+    f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
+  }
+  __device__ static void store(__half* p, const float (&f)[8], uint64_t pol) {
+    uint4 u;
+    u.x = f2h(f[0], f[1]);
+    u.y = f2h(f[2], f[3]);
+    u.z = f2h(f[4], f[5]);
+    u.w = f2h(f[6], f[7]);
+    st16(p, u, pol);
+  }
+};
+template <>
+struct Access<__nv_bfloat16, 8> {
+  __device__ static void load(const __nv_bfloat16* p, float (&f)[8], uint64_t pol) {
+    const uint4 u = ld16(p, pol);
+    float2 a = b2f(u.x), b = b2f(u.y), c = b2f(u.z), d = b2f(u.w);
+    f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+    f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
+  }
+  __device__ static void store(__nv_bfloat16* p, const float (&f)[8], uint64_t pol) {
+    uint4 u;
+    u.x = f2b(f[0], f[1]);
+    u.y = f2b(f[2], f[3]);
+    u.z = f2b(f[4], f[5]);
+    u.w = f2b(f[6], f[7]);
+    st16(p, u, pol);
+  }
+};
+
+// ------------------------------------------------------------- reductions
+// Warp sum with a fixed association; the result is meaningful in lane 0 only.
+__device__ __forceinline__ float warp_sum_lane0(float v) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v += __shfl_down_sync(0xffffffffu, v, off);
+  return v;
+}
+
+// Block sum of two values with a fixed tree (shuffle within warps, then the
+// warp results in warp order).  Returns the totals in thread 0.
+// `scratch` holds at least 2 * 32 floats.
+__device__ __forceinline__ float2 block_sum2_t0(float a, float b, float* scratch) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nw = (blockDim.x + 31) >> 5;
+  a = warp_sum_lane0(a);
+  b = warp_sum_lane0(b);
+  if (lane == 0) {
+    scratch[2 * warp] = a;
+    scratch[2 * warp + 1] = b;
+  }
+  __syncthreads();
+  float2 r = make_float2(0.f, 0.f);
+  if (threadIdx.x == 0) {
+    for (int w = 0; w < nw; ++w) {
+      r.x += scratch[2 * w];
+      r.y += scratch[2 * w + 1];
+    }
+  }
+  __syncthreads();
+  return r;
+}
+
+// --------------------------------------------------------------- tickets
+// A ticket word counts the CTAs of one reduction unit that have published
+// their partial results.  The high 32 bits carry the call's epoch and the low
+// 32 bits the count, so a word left over from another call (or never
+// initialised) reads as count 0: no zero-filled workspace is needed.  The CTA
+// whose arrival completes the unit returns true; it resets the word to 0 once
+// it has finished.  The CAS loop always makes progress (a retry means another
+// CTA's CAS succeeded); the iteration bound is only a safety net and, when hit,
+// raises the error word instead of looping.
+__device__ __forceinline__ bool ticket_arrive(unsigned long long* t, unsigned epoch,
+                                              unsigned long long total, unsigned* err) {
+  unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(t);
+  for (int it = 0; it < (1 << 24); ++it) {
+    const unsigned long long cnt =
+        ((unsigned)(old >> 32) == epoch) ? (old & 0xffffffffull) : 0ull;
+    const unsigned long long nw = ((unsigned long long)epoch << 32) | (cnt + 1ull);
+    const unsigned long long prev = atomicCAS(t, old, nw);
+    if (prev == old) return cnt + 1ull == total;
+    old = prev;
+  }
+  atomicOr(err, 1u);
+  return false;
+}
+
+// Called by thread 0 after the CTA's partial stores (and a __syncthreads()).
+// Makes the stores visible device-wide before arriving; when this CTA is the
+// last one, the trailing fence orders the following reads of other CTAs'
+// partials after the arrival.
+__device__ __forceinline__ bool publish_and_arrive(unsigned long long* t, unsigned epoch,
+                                                   unsigned long long total, unsigned* err) {
+  __threadfence();
+  const bool last = ticket_arrive(t, epoch, total, err);
+  if (last) __threadfence();
+  return last;
+}
+
+}  // namespace gn

@@ -1,0 +1,96 @@
+// gn_internal.h -- plan (work decomposition) and kernel parameter block shared
+// by the C-ABI layer and the kernels.  Not part of the public interface.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace gn {
+
+enum Layout { kNCHW = 0, kNHWC = 1 };
+enum DType { kF32 = 0, kF16 = 1, kBF16 = 2 };
+enum Op { kFwd = 0, kBwd = 1 };
+
+// Regimes (which kernel family runs a call).
+enum Regime {
+  kRegimeAuto = -1,
+  kRegimeGeneric = 0,  // stats/reduce kernel + apply/dx kernel, any shape
+};
+
+// How one call is cut into "items" (one CTA each).  Both kernels of an op use
+// the same items; the second kernel walks them in reverse so that the data the
+// first kernel read last is still in L2 when it is needed again.
+struct Geom {
+  int64_t N, C, HW, G, Cg;
+  int layout, dtype;
+  int vw;    // elements per access: the 16-byte vector width, or 1 (scalar path)
+  int tpb;   // threads per CTA
+  // NHWC: a row is one (n, hw) position holding C channels; a thread owns a
+  // fixed column of vw channels and walks rows.
+  int64_t V;     // columns per row (C / vw)
+  int Wv;        // columns per column block
+  int ncb;       // column blocks per row
+  int rpi;       // rows handled concurrently by one CTA (row lanes)
+  int64_t rb;    // rows per item
+  // NCHW: a row is one (n, c) channel plane of HW elements.
+  int mode;      // 0: item = (row, chunk) walked by the whole CTA; 1: item = block of rows, one warp per row
+  int64_t L;     // mode 0: chunk length (multiple of vw)
+  int64_t RB;    // mode 1: rows per item
+  // common
+  int64_t T;            // partial records per (n, c): row blocks (NHWC) or chunks (NCHW)
+  int64_t cstride, tstride;  // partial index = n*C*T + c*cstride + t*tstride
+  int64_t items_per_n;
+  int64_t items;
+};
+
+// Workspace layout (byte offsets, each 256-byte aligned).
+struct WsLayout {
+  size_t tickets;  // (N + 1) ticket words (uint64): one per sample, one global
+  size_t err;      // one uint32 error word
+  size_t part;     // N*C*T float2 partial sums
+  size_t chst;     // N*C float2 per-channel results of the finalisation
+  size_t coef;     // N*G float2 dx coefficients (backward only)
+  size_t total;
+};
+
+struct KParams {
+  Geom g;
+  const void* x;
+  const void* dy;
+  void* out;  // y (forward) or dx (backward)
+  const float* gamma;
+  const float* beta;
+  float* mean;   // forward: written; backward: read
+  float* rstd;
+  float* dgamma;
+  float* dbeta;
+  float eps;
+  unsigned epoch;
+  unsigned long long* tickets;
+  unsigned* err;
+  float2* part;
+  float2* chst;
+  float2* coef;
+};
+
+// plan.cpp
+int device_sm_count();
+Geom make_geom(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout,
+               int dtype, bool aligned, int sm_count);
+WsLayout ws_layout(int op, const Geom& g);
+
+// Events recorded around/between the kernels of a call (benchmark hook; the
+// launchers record the non-null ones on the call's stream).
+struct TimingEvents {
+  cudaEvent_t begin, mid, end;
+};
+const TimingEvents& timing_events();
+
+// kernels (gn_nhwc.cu / gn_nchw.cu): enqueue the two kernels of an op.
+cudaError_t launch_nhwc_fwd(const KParams& p, cudaStream_t s);
+cudaError_t launch_nhwc_bwd(const KParams& p, cudaStream_t s);
+cudaError_t launch_nchw_fwd(const KParams& p, cudaStream_t s);
+cudaError_t launch_nchw_bwd(const KParams& p, cudaStream_t s);
+
+}  // namespace gn

@@ -1,0 +1,321 @@
+// gn_nhwc.cu -- GroupNorm kernels for channels_last activations.
+//
+// Memory: element (n, c, hw) sits at (n*HW + hw)*C + c, so one spatial
+// position ("row") holds the C channels contiguously and a group is a run of
+// Cg channels inside every row.  A CTA owns an item = (sample n, block of rb
+// consecutive rows, block of Wv column vectors); each thread owns one column
+// of vw channels (one 16-byte vector) and walks the item's rows with stride
+// rpi, so every warp issues fully coalesced 16-byte loads and each thread's
+// channels (and their group constants) never change.
+//
+// Forward : nhwc_fwd_stats  -> per-(item, channel) shifted sums, last CTA of a
+//                              sample merges them into mean/rstd per group
+//           nhwc_fwd_apply  -> y = (x - mean) * rstd*gamma + beta
+// Backward: nhwc_bwd_reduce -> per-(item, channel) sum(dy), sum(dy*(x-mean)),
+//                              last CTA of a sample forms the dx
+//                              coefficients, last sample forms dgamma/dbeta
+//           nhwc_bwd_dx     -> dx = rstd*gamma*dy + B*(x - mean) + D
+#include "gn_finalize.cuh"
+
+namespace gn {
+namespace {
+
+struct NhwcItem {
+  int64_t n, t, col, row0, row1;
+  int j, r;
+  bool active;
+};
+
+__device__ __forceinline__ NhwcItem nhwc_item(const Geom& g, int64_t item) {
+  NhwcItem it;
+  const int tid = threadIdx.x;
+  it.j = tid % g.Wv;
+  it.r = tid / g.Wv;
+  const int cb = (int)(item % g.ncb);
+  item /= g.ncb;
+  it.t = item % g.T;
+  it.n = item / g.T;
+  it.col = (int64_t)cb * g.Wv + it.j;
+  it.active = (it.r < g.rpi) && (it.col < g.V);
+  it.row0 = it.t * g.rb;
+  it.row1 = (it.row0 + g.rb < g.HW) ? it.row0 + g.rb : g.HW;
+  return it;
+}
+
+// Fixed-order tree over the rpi row lanes of each column, in shared memory.
+// On return thread (r = 0, j) holds the CTA totals in red[q*tpb + tid].
+template <int NQ>
+__device__ __forceinline__ void reduce_row_lanes(const Geom& g, float* red, const float (&v)[NQ],
+                                                 int r) {
+  const int tid = threadIdx.x, tpb = blockDim.x;
+#pragma unroll
+  for (int q = 0; q < NQ; ++q) red[q * tpb + tid] = v[q];
+  __syncthreads();
+  for (int s = 1; s < g.rpi; s <<= 1) {
+    if (r < g.rpi && (r % (2 * s)) == 0 && r + s < g.rpi) {
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) red[q * tpb + tid] += red[q * tpb + tid + s * g.Wv];
+    }
+    __syncthreads();
+  }
+}
+
+template <typename T, int VW>
+__global__ void __launch_bounds__(512) nhwc_fwd_stats(const __grid_constant__ KParams p) {
+  extern __shared__ float red[];
+  const Geom& g = p.g;
+  const NhwcItem it = nhwc_item(g, blockIdx.x);
+  float acc[2 * VW];
+#pragma unroll
+  for (int q = 0; q < 2 * VW; ++q) acc[q] = 0.f;
+  if (it.active) {
+    const T* xn = static_cast<const T*>(p.x) + it.n * g.HW * g.C + it.col * VW;
+    const uint64_t pol = policy_evict_last();
+    float K[VW];
+    Access<T, VW>::load(xn, K, pol);  // row 0 of the sample: the per-channel shift
+    const int64_t step = g.rpi;
+    int64_t row = it.row0 + it.r;
+    for (; row + 3 * step < it.row1; row += 4 * step) {
+      float v[4][VW];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) Access<T, VW>::load(xn + (row + u * step) * g.C, v[u], pol);
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int k = 0; k < VW; ++k) {
+          const float d = v[u][k] - K[k];
+          acc[2 * k] += d;
+          acc[2 * k + 1] = fmaf(d, d, acc[2 * k + 1]);
+        }
+    }
+    for (; row < it.row1; row += step) {
+      float v[VW];
+      Access<T, VW>::load(xn + row * g.C, v, pol);
+#pragma unroll
+      for (int k = 0; k < VW; ++k) {
+        const float d = v[k] - K[k];
+        acc[2 * k] += d;
+        acc[2 * k + 1] = fmaf(d, d, acc[2 * k + 1]);
+      }
+    }
+  }
+  reduce_row_lanes<2 * VW>(g, red, acc, it.r);
+  if (it.r == 0 && it.active) {
+    float2* out = p.part + it.n * g.C * g.T + it.t * g.C + it.col * VW;
+#pragma unroll
+    for (int k = 0; k < VW; ++k)
+      out[k] = make_float2(red[(2 * k) * blockDim.x + threadIdx.x],
+                           red[(2 * k + 1) * blockDim.x + threadIdx.x]);
+  }
+  arrive_and_finalize<T, false>(p, it.n, red);
+}
+
+template <typename T, int VW>
+__global__ void __launch_bounds__(512) nhwc_fwd_apply(const __grid_constant__ KParams p) {
+  const Geom& g = p.g;
+  const NhwcItem it = nhwc_item(g, g.items - 1 - (int64_t)blockIdx.x);
+  if (!it.active) return;
+  float a[VW], mu[VW], b[VW];
+#pragma unroll
+  for (int k = 0; k < VW; ++k) {
+    const int64_t c = it.col * VW + k;
+    const int64_t ng = it.n * g.G + c / g.Cg;
+    const float r = __ldg(p.rstd + ng);
+    mu[k] = __ldg(p.mean + ng);
+    a[k] = p.gamma ? r * __ldg(p.gamma + c) : r;
+    b[k] = p.beta ? __ldg(p.beta + c) : 0.f;
+  }
+  const int64_t off = it.n * g.HW * g.C + it.col * VW;
+  const T* xn = static_cast<const T*>(p.x) + off;
+  T* yn = static_cast<T*>(p.out) + off;
+  const uint64_t pin = policy_evict_first();
+  const uint64_t pout = policy_evict_first();
+  const int64_t step = g.rpi;
+  const int64_t cnt = it.row1 - it.row0 - it.r;  // rows of this lane: r, r+step, ...
+  if (cnt <= 0) return;
+  int64_t row = it.row0 + it.r + ((cnt - 1) / step) * step;  // last row of the lane
+  for (; row - 3 * step >= it.row0; row -= 4 * step) {
+    float v[4][VW];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) Access<T, VW>::load(xn + (row - u * step) * g.C, v[u], pin);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+#pragma unroll
+      for (int k = 0; k < VW; ++k) v[u][k] = fmaf(v[u][k] - mu[k], a[k], b[k]);
+      Access<T, VW>::store(yn + (row - u * step) * g.C, v[u], pout);
+    }
+  }
+  for (; row >= it.row0; row -= step) {
+    float v[VW];
+    Access<T, VW>::load(xn + row * g.C, v, pin);
+#pragma unroll
+    for (int k = 0; k < VW; ++k) v[k] = fmaf(v[k] - mu[k], a[k], b[k]);
+    Access<T, VW>::store(yn + row * g.C, v, pout);
+  }
+}
+
+template <typename T, int VW>
+__global__ void __launch_bounds__(512) nhwc_bwd_reduce(const __grid_constant__ KParams p) {
+  extern __shared__ float red[];
+  const Geom& g = p.g;
+  const NhwcItem it = nhwc_item(g, blockIdx.x);
+  float acc[2 * VW];
+#pragma unroll
+  for (int q = 0; q < 2 * VW; ++q) acc[q] = 0.f;
+  if (it.active) {
+    float mu[VW];
+#pragma unroll
+    for (int k = 0; k < VW; ++k) mu[k] = __ldg(p.mean + it.n * g.G + (it.col * VW + k) / g.Cg);
+    const int64_t off = it.n * g.HW * g.C + it.col * VW;
+    const T* xn = static_cast<const T*>(p.x) + off;
+    const T* dyn = static_cast<const T*>(p.dy) + off;
+    const uint64_t pol = policy_evict_last();
+    const int64_t step = g.rpi;
+    int64_t row = it.row0 + it.r;
+    for (; row + step < it.row1; row += 2 * step) {
+      float xv[2][VW], dv[2][VW];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        Access<T, VW>::load(xn + (row + u * step) * g.C, xv[u], pol);
+        Access<T, VW>::load(dyn + (row + u * step) * g.C, dv[u], pol);
+      }
+#pragma unroll
+      for (int u = 0; u < 2; ++u)
+#pragma unroll
+        for (int k = 0; k < VW; ++k) {
+          acc[2 * k] += dv[u][k];
+          acc[2 * k + 1] = fmaf(dv[u][k], xv[u][k] - mu[k], acc[2 * k + 1]);
+        }
+    }
+    for (; row < it.row1; row += step) {
+      float xv[VW], dv[VW];
+      Access<T, VW>::load(xn + row * g.C, xv, pol);
+      Access<T, VW>::load(dyn + row * g.C, dv, pol);
+#pragma unroll
+      for (int k = 0; k < VW; ++k) {
+        acc[2 * k] += dv[k];
+        acc[2 * k + 1] = fmaf(dv[k], xv[k] - mu[k], acc[2 * k + 1]);
+      }
+    }
+  }
+  reduce_row_lanes<2 * VW>(g, red, acc, it.r);
+  if (it.r == 0 && it.active) {
+    float2* out = p.part + it.n * g.C * g.T + it.t * g.C + it.col * VW;
+#pragma unroll
+    for (int k = 0; k < VW; ++k)
+      out[k] = make_float2(red[(2 * k) * blockDim.x + threadIdx.x],
+                           red[(2 * k + 1) * blockDim.x + threadIdx.x]);
+  }
+  arrive_and_finalize<T, true>(p, it.n, red);
+}
+
+template <typename T, int VW>
+__global__ void __launch_bounds__(512) nhwc_bwd_dx(const __grid_constant__ KParams p) {
+  const Geom& g = p.g;
+  const NhwcItem it = nhwc_item(g, g.items - 1 - (int64_t)blockIdx.x);
+  if (!it.active) return;
+  float A[VW], mu[VW], B[VW], D[VW];
+#pragma unroll
+  for (int k = 0; k < VW; ++k) {
+    const int64_t c = it.col * VW + k;
+    const int64_t ng = it.n * g.G + c / g.Cg;
+    const float r = __ldg(p.rstd + ng);
+    const float2 cf = __ldcg(p.coef + ng);
+    mu[k] = __ldg(p.mean + ng);
+    A[k] = p.gamma ? r * __ldg(p.gamma + c) : r;
+    B[k] = cf.x;
+    D[k] = cf.y;
+  }
+  const int64_t off = it.n * g.HW * g.C + it.col * VW;
+  const T* xn = static_cast<const T*>(p.x) + off;
+  const T* dyn = static_cast<const T*>(p.dy) + off;
+  T* dxn = static_cast<T*>(p.out) + off;
+  const uint64_t pin = policy_evict_first();
+  const int64_t step = g.rpi;
+  const int64_t cnt = it.row1 - it.row0 - it.r;
+  if (cnt <= 0) return;
+  int64_t row = it.row0 + it.r + ((cnt - 1) / step) * step;
+  for (; row - step >= it.row0; row -= 2 * step) {
+    float xv[2][VW], dv[2][VW];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      Access<T, VW>::load(xn + (row - u * step) * g.C, xv[u], pin);
+      Access<T, VW>::load(dyn + (row - u * step) * g.C, dv[u], pin);
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+#pragma unroll
+      for (int k = 0; k < VW; ++k) xv[u][k] = fmaf(A[k], dv[u][k], fmaf(B[k], xv[u][k] - mu[k], D[k]));
+      Access<T, VW>::store(dxn + (row - u * step) * g.C, xv[u], pin);
+    }
+  }
+  for (; row >= it.row0; row -= step) {
+    float xv[VW], dv[VW];
+    Access<T, VW>::load(xn + row * g.C, xv, pin);
+    Access<T, VW>::load(dyn + row * g.C, dv, pin);
+#pragma unroll
+    for (int k = 0; k < VW; ++k) xv[k] = fmaf(A[k], dv[k], fmaf(B[k], xv[k] - mu[k], D[k]));
+    Access<T, VW>::store(dxn + row * g.C, xv, pin);
+  }
+}
+
+template <typename T, int VW>
+cudaError_t fwd_t(const KParams& p, cudaStream_t s) {
+  const Geom& g = p.g;
+  const size_t sm1 = sizeof(float) * 2 * VW * g.tpb;
+  const TimingEvents& ev = timing_events();
+  if (ev.begin) cudaEventRecord(ev.begin, s);
+  nhwc_fwd_stats<T, VW><<<(unsigned)g.items, g.tpb, sm1, s>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (ev.mid) cudaEventRecord(ev.mid, s);
+  nhwc_fwd_apply<T, VW><<<(unsigned)g.items, g.tpb, 0, s>>>(p);
+  e = cudaGetLastError();
+  if (ev.end) cudaEventRecord(ev.end, s);
+  return e;
+}
+
+template <typename T, int VW>
+cudaError_t bwd_t(const KParams& p, cudaStream_t s) {
+  const Geom& g = p.g;
+  const size_t sm1 = sizeof(float) * 2 * VW * g.tpb;
+  const TimingEvents& ev = timing_events();
+  if (ev.begin) cudaEventRecord(ev.begin, s);
+  nhwc_bwd_reduce<T, VW><<<(unsigned)g.items, g.tpb, sm1, s>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (ev.mid) cudaEventRecord(ev.mid, s);
+  nhwc_bwd_dx<T, VW><<<(unsigned)g.items, g.tpb, 0, s>>>(p);
+  e = cudaGetLastError();
+  if (ev.end) cudaEventRecord(ev.end, s);
+  return e;
+}
+
+template <typename T>
+cudaError_t fwd_dispatch_vw(const KParams& p, cudaStream_t s) {
+  return p.g.vw == 1 ? fwd_t<T, 1>(p, s) : fwd_t<T, Elem<T>::VEC>(p, s);
+}
+template <typename T>
+cudaError_t bwd_dispatch_vw(const KParams& p, cudaStream_t s) {
+  return p.g.vw == 1 ? bwd_t<T, 1>(p, s) : bwd_t<T, Elem<T>::VEC>(p, s);
+}
+
+}  // namespace
+
+cudaError_t launch_nhwc_fwd(const KParams& p, cudaStream_t s) {
+  switch (p.g.dtype) {
+    case kF32: return fwd_dispatch_vw<float>(p, s);
+    case kF16: return fwd_dispatch_vw<__half>(p, s);
+    default: return fwd_dispatch_vw<__nv_bfloat16>(p, s);
+  }
+}
+
+cudaError_t launch_nhwc_bwd(const KParams& p, cudaStream_t s) {
+  switch (p.g.dtype) {
+    case kF32: return bwd_dispatch_vw<float>(p, s);
+    case kF16: return bwd_dispatch_vw<__half>(p, s);
+    default: return bwd_dispatch_vw<__nv_bfloat16>(p, s);
+  }
+}
+
+}  // namespace gn

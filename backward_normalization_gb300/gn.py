@@ -1,0 +1,171 @@
+"""Thin Python binding of libgn.so (include/gn.h): argument marshalling only.
+
+Every function here hands raw device pointers, sizes and a stream to the C
+ABI; all GroupNorm arithmetic runs in the CUDA kernels of ``csrc/``.  Loading
+fails loudly (ImportError / RuntimeError) when the library has not been built;
+there is no fallback implementation.
+
+Tensors are torch tensors holding the data flat in the chosen layout
+(``"nchw"`` or ``"nhwc"``); torch is used for device memory and streams only.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libgn.so")
+
+GN_OK, GN_ERR_INVALID, GN_ERR_UNSUPPORTED, GN_ERR_WORKSPACE, GN_ERR_CUDA = range(5)
+OP_FWD, OP_BWD = 0, 1
+LAYOUT = {"nchw": 0, "nhwc": 1}
+DTYPE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
+DTYPE_NAME = {"f32": 0, "f16": 1, "bf16": 2}
+
+_I64 = ctypes.c_int64
+_VP = ctypes.c_void_p
+
+
+class GnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+
+
+class PlanDesc(ctypes.Structure):
+    _fields_ = [("regime", ctypes.c_int), ("launches", ctypes.c_int),
+                ("vector_width", ctypes.c_int), ("threads", ctypes.c_int),
+                ("ctas", ctypes.c_int64), ("partials", ctypes.c_int64),
+                ("workspace_bytes", ctypes.c_size_t)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libgn.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is missing: build it with "
+                              "`python -c 'import __graft_entry__ as g; g.build()'`")
+        L = ctypes.CDLL(LIB_PATH)
+        L.gn_workspace_size.argtypes = [ctypes.c_int, _I64, _I64, _I64, _I64, ctypes.c_int, ctypes.c_int]
+        L.gn_workspace_size.restype = ctypes.c_size_t
+        L.gn_fwd.argtypes = [_VP, _I64, _I64, _I64, _I64, ctypes.c_int, ctypes.c_int, _VP, _VP,
+                             ctypes.c_float, _VP, _VP, _VP, _VP, ctypes.c_size_t, _VP]
+        L.gn_fwd.restype = ctypes.c_int
+        L.gn_bwd.argtypes = [_VP, _VP, _VP, _VP, _VP, _I64, _I64, _I64, _I64, ctypes.c_int,
+                             ctypes.c_int, _VP, _VP, _VP, _VP, ctypes.c_size_t, _VP]
+        L.gn_bwd.restype = ctypes.c_int
+        L.gn_status_string.argtypes = [ctypes.c_int]
+        L.gn_status_string.restype = ctypes.c_char_p
+        L.gn_last_cuda_error.argtypes = []
+        L.gn_last_cuda_error.restype = ctypes.c_int
+        L.gn_plan_info.argtypes = [ctypes.c_int, _I64, _I64, _I64, _I64, ctypes.c_int, ctypes.c_int,
+                                   ctypes.c_int, ctypes.POINTER(PlanDesc)]
+        L.gn_plan_info.restype = ctypes.c_int
+        L.gn_set_timing_events.argtypes = [_VP, _VP, _VP]
+        L.gn_set_timing_events.restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().gn_status_string(int(status)).decode()
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def workspace_size(op, N, C, HW, G, layout, dtype) -> int:
+    lay = LAYOUT[layout] if isinstance(layout, str) else int(layout)
+    dt = DTYPE[dtype] if isinstance(dtype, torch.dtype) else (
+        DTYPE_NAME[dtype] if isinstance(dtype, str) else int(dtype))
+    return int(lib().gn_workspace_size(op, N, C, HW, G, lay, dt))
+
+
+def plan_info(op, N, C, HW, G, layout, dtype, aligned=True) -> PlanDesc:
+    lay = LAYOUT[layout] if isinstance(layout, str) else int(layout)
+    dt = DTYPE[dtype] if isinstance(dtype, torch.dtype) else (
+        DTYPE_NAME[dtype] if isinstance(dtype, str) else int(dtype))
+    d = PlanDesc()
+    rc = lib().gn_plan_info(op, N, C, HW, G, lay, dt, int(bool(aligned)), ctypes.byref(d))
+    if rc != GN_OK:
+        raise GnError(rc, "gn_plan_info")
+    return d
+
+
+def fwd_raw(x, N, C, HW, G, layout, gamma, beta, eps, y, mean, rstd, workspace,
+            stream=None) -> int:
+    """gn_fwd on torch tensors; returns the gn_status."""
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    return lib().gn_fwd(_ptr(x), N, C, HW, G, LAYOUT[layout], DTYPE[x.dtype], _ptr(gamma),
+                        _ptr(beta), float(eps), _ptr(y), _ptr(mean), _ptr(rstd),
+                        _ptr(workspace), ws_bytes, _stream(stream))
+
+
+def bwd_raw(dy, x, mean, rstd, gamma, N, C, HW, G, layout, dx, dgamma, dbeta, workspace,
+            stream=None) -> int:
+    """gn_bwd on torch tensors; returns the gn_status."""
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    return lib().gn_bwd(_ptr(dy), _ptr(x), _ptr(mean), _ptr(rstd), _ptr(gamma), N, C, HW, G,
+                        LAYOUT[layout], DTYPE[x.dtype], _ptr(dx), _ptr(dgamma), _ptr(dbeta),
+                        _ptr(workspace), ws_bytes, _stream(stream))
+
+
+def set_timing_events(ev_begin=None, ev_mid=None, ev_end=None) -> None:
+    """Make the following calls of this thread record torch.cuda.Event objects
+    before, between and after their two kernels (None: no record)."""
+    def h(e):
+        return None if e is None else e.cuda_event
+    lib().gn_set_timing_events(h(ev_begin), h(ev_mid), h(ev_end))
+
+
+def alloc_workspace(op, N, C, HW, G, layout, dtype, device="cuda"):
+    n = workspace_size(op, N, C, HW, G, layout, dtype)
+    return torch.empty(max(n, 16), dtype=torch.uint8, device=device)
+
+
+def forward(x, N, C, HW, G, layout, gamma=None, beta=None, eps=1e-5, workspace=None,
+            stream=None):
+    """Allocates y/mean/rstd (and a workspace if none is given), calls gn_fwd.
+    Returns (y, mean, rstd)."""
+    y = torch.empty_like(x)
+    mean = torch.empty(N * G, dtype=torch.float32, device=x.device)
+    rstd = torch.empty(N * G, dtype=torch.float32, device=x.device)
+    if workspace is None:
+        workspace = alloc_workspace(OP_FWD, N, C, HW, G, layout, x.dtype, x.device)
+    rc = fwd_raw(x, N, C, HW, G, layout, gamma, beta, eps, y, mean, rstd, workspace, stream)
+    if rc != GN_OK:
+        raise GnError(rc, "gn_fwd")
+    return y, mean, rstd
+
+
+def backward(dy, x, mean, rstd, N, C, HW, G, layout, gamma=None, workspace=None,
+             need_params=True, stream=None):
+    """Allocates dx (and dgamma/dbeta, a workspace), calls gn_bwd.
+    Returns (dx, dgamma, dbeta)."""
+    dx = torch.empty_like(x)
+    dgamma = dbeta = None
+    if need_params:
+        dgamma = torch.empty(C, dtype=torch.float32, device=x.device)
+        dbeta = torch.empty(C, dtype=torch.float32, device=x.device)
+    if workspace is None:
+        workspace = alloc_workspace(OP_BWD, N, C, HW, G, layout, x.dtype, x.device)
+    rc = bwd_raw(dy, x, mean, rstd, gamma, N, C, HW, G, layout, dx, dgamma, dbeta, workspace,
+                 stream)
+    if rc != GN_OK:
+        raise GnError(rc, "gn_bwd")
+    return dx, dgamma, dbeta

@@ -1,0 +1,470 @@
+"""GroupNorm forward + backward benchmark on GB300.
+
+One step = gn_fwd + gn_bwd (stats, normalize/affine, backward group
+reduction, dx, dgamma/dbeta) over the fp16 channels_last workload
+N=1, C=128, G=16, H=1024, W=2048 with inputs resident in HBM.  The metric is
+achieved HBM bandwidth over the minimal traffic of the two ops
+(forward: read x + write y; backward: read x, dy + write dx).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  Under torchrun every rank runs its own copy of
+the workload (weak scaling) and the per-channel dgamma/dbeta are summed across
+ranks, in rank order, inside each step.  `--impl reference` times the fp64
+CPU oracle on a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "fp16_nhwc_1x128x1024x2048_g16"
+METRIC = "GroupNorm fwd+bwd achieved HBM GB/s (% of GB300 roofline), us/call per config"
+UNIT = "GB/s"
+L2_FLUSH_BYTES = 512 << 20
+
+
+def esize(dtype: str) -> int:
+    return 4 if dtype == "f32" else 2
+
+
+def min_bytes(w):
+    """Minimal traffic per op: forward reads x and writes y; backward reads x
+    and dy and writes dx."""
+    e = w.E * esize(w.dtype)
+    return {"fwd": 2 * e, "bwd": 3 * e}
+
+
+def kernel_bytes(w):
+    """Algorithmic bytes of each kernel (what it must move at least)."""
+    e = w.E * esize(w.dtype)
+    return {"fwd_stats": e, "fwd_apply": 2 * e, "bwd_reduce": 2 * e, "bwd_dx": 3 * e}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def config_of(w, extra=None):
+    c = {"workload": w.name, "N": w.N, "C": w.C, "G": w.G, "H": w.H, "W": w.W,
+         "layout": w.layout, "io_dtype": w.dtype, "eps": w.eps}
+    if extra:
+        c.update(extra)
+    return c
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            import tempfile
+
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [s.strip() for s in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[4:]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        busy = [r for r in rows if r[2] > 200.0] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in busy for i, v in enumerate(r[3][1:5])
+                          if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[0] for r in busy),
+                "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons,
+                "samples": len(busy), "power_w_max": max(r[2] for r in rows)}
+
+
+# --------------------------------------------------------------- oracle leg
+def oracle_sample(H):
+    """Times the fp64 CPU oracle (fwd + bwd) on a bounded slice of the
+    workload: the first H rows of the image (all channels and groups).
+    Returns (GB/s over the slice's minimal traffic, seconds, description)."""
+    import oracle
+    from backward_normalization_gb300 import synth
+
+    o = oracle.get()
+    w = synth.BY_NAME[WORKLOAD]
+    ws = w.scaled(H=H)
+    inp = synth.make_inputs(ws, "cpu", seed=0)
+    x = inp["x"].double().numpy()
+    dy = inp["dy"].double().numpy()
+    g = inp["gamma"].double().numpy()
+    b = inp["beta"].double().numpy()
+    t0 = time.perf_counter()
+    o.forward(x, ws.N, ws.C, ws.HW, ws.G, 1, g, b, ws.eps)
+    o.backward(dy, x, ws.N, ws.C, ws.HW, ws.G, 1, g, ws.eps)
+    dt = time.perf_counter() - t0
+    mb = min_bytes(ws)
+    gbs = (mb["fwd"] + mb["bwd"]) / dt / 1e9
+    desc = (f"fp64 oracle fwd+bwd on rows 0..{H - 1} of the image (N=1, C=128, G=16, "
+            f"H={H}, W=2048: {ws.E} elements, {H / w.H:.4f} of the workload), 1 thread")
+    return gbs, dt, desc
+
+
+def rows_for_seconds(target_s):
+    """Image rows whose oracle fwd+bwd takes about target_s seconds here."""
+    _, dt, _ = oracle_sample(2)
+    return int(max(1, min(1024, round(2 * target_s / max(dt, 1e-6)))))
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    from backward_normalization_gb300 import synth
+
+    w = synth.BY_NAME[WORKLOAD]
+    # the whole run stays within about two minutes of CPU time
+    H = rows_for_seconds(min(2.0, 120.0 / (args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample(H)
+    times = []
+    desc = ""
+    for _ in range(args.steps):
+        _, dt, desc = oracle_sample(H)
+        times.append(dt)
+    mb = min_bytes(w.scaled(H=H))
+    ms = 1e3 * sum(times) / len(times)
+    value = (mb["fwd"] + mb["bwd"]) / (ms * 1e-3) / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_of(w, {"sample": desc}),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ our arm
+def traffic_from_profiles(kernel_key):
+    """Per-launch DRAM bytes of a kernel from the committed ncu summary, if the
+    kernel sources are unchanged since the capture."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    if d.get("src_sha") != source_sha():
+        return None
+    k = d.get("kernels", {}).get(kernel_key)
+    return None if k is None else k.get("dram_bytes_per_launch")
+
+
+def source_sha():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "backward_normalization_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h", ".cpp")):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def time_configs(gn, synth, torch, flush, reps=20):
+    """Per-workload fwd and bwd times (median of reps, L2 flushed before each
+    call) for the four large workloads."""
+    out = {}
+    peak, _ = load_peaks()
+    stream = torch.cuda.current_stream()
+    for w in synth.WORKLOADS[1:]:
+        inp = synth.make_inputs(w, "cuda", seed=0)
+        x, dy, gm, bt = inp["x"], inp["dy"], inp["gamma"], inp["beta"]
+        y = torch.empty_like(x)
+        dx = torch.empty_like(x)
+        mean = torch.empty(w.N * w.G, device="cuda")
+        rstd = torch.empty(w.N * w.G, device="cuda")
+        dg = torch.empty(w.C, device="cuda")
+        db = torch.empty(w.C, device="cuda")
+        ws = gn.alloc_workspace(gn.OP_BWD, w.N, w.C, w.HW, w.G, w.layout, x.dtype)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+        rec = {"fwd": [], "bwd": [], "fwd_stats": [], "fwd_apply": [], "bwd_reduce": [], "bwd_dx": []}
+        for it in range(reps + 3):
+            flush()
+            gn.set_timing_events(ev[0], ev[1], ev[2])
+            assert gn.fwd_raw(x, w.N, w.C, w.HW, w.G, w.layout, gm, bt, w.eps, y, mean, rstd, ws, stream) == 0
+            flush()
+            gn.set_timing_events(ev[3], ev[4], ev[5])
+            assert gn.bwd_raw(dy, x, mean, rstd, gm, w.N, w.C, w.HW, w.G, w.layout, dx, dg, db, ws, stream) == 0
+            gn.set_timing_events()
+            torch.cuda.synchronize()
+            if it >= 3:
+                rec["fwd"].append(ev[0].elapsed_time(ev[2]))
+                rec["fwd_stats"].append(ev[0].elapsed_time(ev[1]))
+                rec["fwd_apply"].append(ev[1].elapsed_time(ev[2]))
+                rec["bwd"].append(ev[3].elapsed_time(ev[5]))
+                rec["bwd_reduce"].append(ev[3].elapsed_time(ev[4]))
+                rec["bwd_dx"].append(ev[4].elapsed_time(ev[5]))
+        mb = min_bytes(w)
+        med = {k: statistics.median(v) for k, v in rec.items()}
+        fwd_gbs = mb["fwd"] / (med["fwd"] * 1e-3) / 1e9
+        bwd_gbs = mb["bwd"] / (med["bwd"] * 1e-3) / 1e9
+        kb = kernel_bytes(w)
+        out[w.name] = {
+            "fwd_us": round(med["fwd"] * 1e3, 2), "bwd_us": round(med["bwd"] * 1e3, 2),
+            "fwd_gbs": round(fwd_gbs, 1), "bwd_gbs": round(bwd_gbs, 1),
+            "fwd_frac": round(fwd_gbs / peak, 4), "bwd_frac": round(bwd_gbs / peak, 4),
+            "fwd_frac_of_8tbs": round(fwd_gbs / 8000.0, 4), "bwd_frac_of_8tbs": round(bwd_gbs / 8000.0, 4),
+            "kernels_us": {k: round(med[k] * 1e3, 2) for k in kb},
+            "kernels_frac": {k: round(kb[k] / (med[k] * 1e-3) / 1e9 / peak, 4) for k in kb},
+        }
+        del x, dy, y, dx, inp, ws
+        torch.cuda.empty_cache()
+    return out
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    from backward_normalization_gb300 import gn, synth
+
+    gn.lib()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    w = synth.BY_NAME[WORKLOAD]
+    inp = synth.make_inputs(w, dev, seed=rank)
+    x, dy, gm, bt = inp["x"], inp["dy"], inp["gamma"], inp["beta"]
+    y = torch.empty_like(x)
+    dx = torch.empty_like(x)
+    mean = torch.empty(w.N * w.G, device=dev)
+    rstd = torch.empty(w.N * w.G, device=dev)
+    dg = torch.empty(w.C, device=dev)
+    db = torch.empty(w.C, device=dev)
+    ws = gn.alloc_workspace(gn.OP_BWD, w.N, w.C, w.HW, w.G, w.layout, x.dtype, dev)
+    gathered = torch.empty(world, 2 * w.C, device=dev) if world > 1 else None
+    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def flush():
+        flush_buf.add_(1)
+
+    def step(evs=None):
+        if evs:
+            gn.set_timing_events(evs[0], evs[1], evs[2])
+        rc = gn.fwd_raw(x, w.N, w.C, w.HW, w.G, w.layout, gm, bt, w.eps, y, mean, rstd, ws, stream)
+        if evs:
+            gn.set_timing_events(evs[3], evs[4], evs[5])
+        rc |= gn.bwd_raw(dy, x, mean, rstd, gm, w.N, w.C, w.HW, w.G, w.layout, dx, dg, db, ws, stream)
+        if evs:
+            gn.set_timing_events()
+        if rc:
+            raise RuntimeError(f"gn call failed: {rc}")
+        if world > 1:
+            # dgamma/dbeta summed over ranks in rank order (deterministic)
+            dist.all_gather_into_tensor(gathered.view(-1), torch.cat([dg, db]))
+            tot = gathered[0].clone()
+            for r in range(1, world):
+                tot += gathered[r]
+            dg.copy_(tot[:w.C])
+            db.copy_(tot[w.C:])
+
+    for _ in range(args.warmup):
+        step()
+        flush()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    clocks = ClockSampler(local_rank)
+    if rank == 0:
+        clocks.start()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for k in range(K):
+        step(evs[k])
+        flush()  # L2 flushed between steps (outside the per-step event windows)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop() if rank == 0 else None
+
+    per_step = [e[0].elapsed_time(e[5]) for e in evs]          # ms, fwd start -> bwd end
+    kern = {
+        "fwd_stats": [e[0].elapsed_time(e[1]) for e in evs],
+        "fwd_apply": [e[1].elapsed_time(e[2]) for e in evs],
+        "bwd_reduce": [e[3].elapsed_time(e[4]) for e in evs],
+        "bwd_dx": [e[4].elapsed_time(e[5]) for e in evs],
+    }
+    step_sum = torch.tensor([sum(per_step)], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(step_sum, op=dist.ReduceOp.MAX)
+    ms_per_step = float(step_sum.item()) / K
+    mb = min_bytes(w)
+    bytes_step = mb["fwd"] + mb["bwd"]
+    value = world * bytes_step / (ms_per_step * 1e-3) / 1e9
+
+    # ---- e2e through the C ABI with host buffers (pinned), copies timed
+    hx = x.cpu().pin_memory()
+    hdy = dy.cpu().pin_memory()
+    hg, hb = gm.cpu().pin_memory(), bt.cpu().pin_memory()
+    hy = torch.empty_like(hx).pin_memory()
+    hdx = torch.empty_like(hx).pin_memory()
+    hst = torch.empty(2 * w.N * w.G + 2 * w.C, dtype=torch.float32).pin_memory()
+    h2d = (hx.numel() + hdy.numel()) * hx.element_size() + (hg.numel() + hb.numel()) * 4
+    d2h = (hy.numel() + hdx.numel()) * hy.element_size() + hst.numel() * 4
+    Ke = max(3, min(10, K))
+    e2e_times = []
+    for k in range(Ke + 2):
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        x.copy_(hx, non_blocking=True)
+        dy.copy_(hdy, non_blocking=True)
+        gm.copy_(hg, non_blocking=True)
+        bt.copy_(hb, non_blocking=True)
+        step()
+        hy.copy_(y, non_blocking=True)
+        hdx.copy_(dx, non_blocking=True)
+        hst.copy_(torch.cat([mean, rstd, dg, db]), non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize()
+        if k >= 2:
+            e2e_times.append(a.elapsed_time(b))
+        flush()
+    e2e_ms = torch.tensor([statistics.mean(e2e_times)], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(e2e_ms, op=dist.ReduceOp.MAX)
+    e2e_value = world * bytes_step / (float(e2e_ms.item()) * 1e-3) / 1e9
+    del hx, hdy, hy, hdx
+
+    if rank != 0:
+        return 0
+
+    peak, peak_kind = load_peaks()
+    kb = kernel_bytes(w)
+    totals = {k: sum(v) for k, v in kern.items()}
+    dom = max(totals, key=totals.get)
+    avg_ms = totals[dom] / K
+    achieved = kb[dom] / (avg_ms * 1e-3) / 1e9
+    plan_f = gn.plan_info(0, w.N, w.C, w.HW, w.G, w.layout, w.dtype)
+    plan_b = gn.plan_info(1, w.N, w.C, w.HW, w.G, w.layout, w.dtype)
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": traffic_from_profiles(dom),
+                "kernel": dom, "peak_kind": peak_kind,
+                "algorithmic_bytes_per_launch": kb[dom], "avg_launch_us": round(avg_ms * 1e3, 2),
+                "kernels": {k: {"avg_us": round(totals[k] / K * 1e3, 2),
+                                "frac": round(kb[k] / (totals[k] / K * 1e-3) / 1e9 / peak, 4)}
+                            for k in kb}}
+
+    per_config = None
+    if not args.no_per_config and world == 1:
+        del x, dy, y, dx, inp
+        torch.cuda.empty_cache()
+        per_config = time_configs(gn, synth, torch, flush)
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        gbs, dt, desc = oracle_sample(rows_for_seconds(10.0))
+        cpu = {"value": round(gbs, 4), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc,
+               "seconds": round(dt, 2)}
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": config_of(w, {
+            "l2": "inputs larger than L2 (512 MiB per tensor); L2 also flushed between steps",
+            "parallelism": f"replicas x{world}, dgamma/dbeta summed across ranks",
+            "frac_of_measured_peak": round(value / world / peak, 4),
+            "frac_of_8tbs": round(value / world / 8000.0, 4)}),
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": (plan_f.launches + plan_b.launches) * K,
+        "clocks": clk,
+        "per_config": per_config,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-per-config", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    rc = run_ours(args, rank, world, local_rank)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return rc
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,139 @@
+/*
+ * gn.h -- C ABI of libgn.so: GroupNorm forward and backward on NVIDIA GB300
+ * (sm_103a), hand-written CUDA kernels behind plain pointers and sizes.
+ *
+ * The operation ("Kimi-K2.6 l1_p35" POPCORNBENCH transcript, opening problem
+ * analysis; "baracuda-kernels src/norm/group_norm_backward.rs", module comment
+ * and GroupNormBackwardArgs): an activation [N, C, *spatial] is viewed as
+ * [N, C, HW] with HW = product of the spatial extents.  The C channels form G
+ * groups of Cg = C/G consecutive channels.  For every sample n and group g,
+ *     mean = average of x over the Cg*HW elements of (n, g)
+ *     var  = biased variance over the same elements (divisor Cg*HW)
+ *     rstd = 1 / sqrt(var + eps)
+ *     y    = (x - mean) * rstd * gamma[c] + beta[c]
+ * and the backward, with g_i = gamma[c] * dy_i and xhat = (x - mean) * rstd,
+ *     dx     = rstd * (g - avg_(n,g)(g) - xhat * avg_(n,g)(g * xhat))
+ *     dgamma[c] = sum over n, hw of dy * xhat
+ *     dbeta[c]  = sum over n, hw of dy
+ *
+ * Memory layouts ("Fix GroupNorm NHWC one-pass backward execution",
+ * NVIDIA/apex PR #2018, reproducer: channels_last activations):
+ *     GN_LAYOUT_NCHW: element (n, c, hw) at offset (n*C + c)*HW + hw
+ *     GN_LAYOUT_NHWC: element (n, c, hw) at offset (n*HW + hw)*C + c
+ * Tensors are densely packed in one of these layouts; strided views are not
+ * accepted.
+ *
+ * Types: x, y, dy, dx are all of `dtype` (fp32, fp16 or bf16); every
+ * reduction and every intermediate is fp32.  gamma, beta, dgamma, dbeta are
+ * fp32 [C]; mean and rstd are fp32 [N*G] indexed n*G + g.  y and dx are
+ * rounded once, to nearest even, from fp32.
+ *
+ * Ownership and execution: every pointer except `workspace_bytes`-sized
+ * scalars is a DEVICE pointer owned by the caller.  The library allocates
+ * nothing; each call validates its arguments on the host and then enqueues its
+ * kernels asynchronously on `stream` (a cudaStream_t; NULL = legacy default
+ * stream) of the current device.  Results are bit-identical from run to run
+ * for the same arguments on the same device.
+ *
+ * Workspace: a caller-provided device buffer of at least gn_workspace_size()
+ * bytes, 16-byte aligned.  Its contents on entry are ignored and on return are
+ * unspecified (no zero-fill is needed).  Two calls that are in flight at the
+ * same time must not share one workspace.
+ */
+#ifndef GN_H_
+#define GN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define GN_API __attribute__((visibility("default")))
+#else
+#define GN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum gn_layout { GN_LAYOUT_NCHW = 0, GN_LAYOUT_NHWC = 1 } gn_layout;
+typedef enum gn_dtype { GN_DTYPE_F32 = 0, GN_DTYPE_F16 = 1, GN_DTYPE_BF16 = 2 } gn_dtype;
+typedef enum gn_op { GN_OP_FWD = 0, GN_OP_BWD = 1 } gn_op;
+
+/* Status codes ("baracuda-kernels src/norm/group_norm_backward.rs",
+ * GroupNormBackwardPlan::select / can_implement / run: invalid problems,
+ * unsupported element types, a workspace that is too small). */
+typedef enum gn_status {
+  GN_OK = 0,
+  GN_ERR_INVALID = 1,     /* bad sizes, G not dividing C, missing or overlapping buffers */
+  GN_ERR_UNSUPPORTED = 2, /* unknown layout or dtype, or a problem too large to launch */
+  GN_ERR_WORKSPACE = 3,   /* workspace NULL, misaligned or smaller than gn_workspace_size() */
+  GN_ERR_CUDA = 4         /* a CUDA call or kernel launch failed (see gn_last_cuda_error) */
+} gn_status;
+
+/* Bytes of workspace that gn_fwd (op = GN_OP_FWD) or gn_bwd (op = GN_OP_BWD)
+ * needs for this problem on the current device; 0 for invalid or empty
+ * problems.  Host-only: launches nothing.  ("baracuda-kernels
+ * src/norm/group_norm_backward.rs", workspace_size.) */
+GN_API size_t gn_workspace_size(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout,
+                         int dtype);
+
+/* Forward.  Reads x [N, C, HW] (layout, dtype), gamma [C] and beta [C]
+ * (either may be NULL: weight 1 / bias 0).  Writes y (same shape, layout and
+ * dtype as x), mean [N*G] and rstd [N*G].  y may be the same buffer as x
+ * (in place); any other overlap between y, x, mean and rstd is rejected.
+ * N, C or HW equal to 0: returns GN_OK and launches nothing.
+ * Errors are reported before anything is enqueued, except GN_ERR_CUDA from a
+ * failed launch. */
+GN_API int gn_fwd(const void* x, int64_t N, int64_t C, int64_t HW, int64_t G, int layout, int dtype,
+           const float* gamma, const float* beta, float eps, void* y, float* mean, float* rstd,
+           void* workspace, size_t workspace_bytes, void* stream);
+
+/* Backward ("baracuda-kernels src/norm/group_norm_backward.rs",
+ * GroupNormBackwardArgs: dy, x, gamma, saved mean, saved rstd -> dx, dgamma,
+ * dbeta).  mean and rstd are the forward's outputs for the same x.  gamma may
+ * be NULL (weight 1).  dgamma and dbeta may each be NULL (not computed).
+ * dx may be the same buffer as dy (in place); any other overlap is rejected.
+ * N or C equal to 0: GN_OK, nothing launched.  HW equal to 0 (or N == 0 with
+ * C > 0): dgamma and dbeta, when given, are set to 0 (an empty sum) with
+ * cudaMemsetAsync and no kernel is launched. */
+GN_API int gn_bwd(const void* dy, const void* x, const float* mean, const float* rstd,
+           const float* gamma, int64_t N, int64_t C, int64_t HW, int64_t G, int layout,
+           int dtype, void* dx, float* dgamma, float* dbeta, void* workspace,
+           size_t workspace_bytes, void* stream);
+
+/* Static, human-readable name of a status code. */
+GN_API const char* gn_status_string(int status);
+
+/* The cudaError_t behind the last GN_ERR_CUDA returned on this thread. */
+GN_API int gn_last_cuda_error(void);
+
+/* Timing hook for benchmarks.  After this call, every gn_fwd/gn_bwd made by
+ * the same host thread records, on its stream, ev_begin before its first
+ * kernel, ev_mid between its two kernels and ev_end after its last kernel
+ * (each a cudaEvent_t created by the caller; NULL skips that record).  Pass
+ * three NULLs to stop.  Returns a gn_status. */
+GN_API int gn_set_timing_events(void* ev_begin, void* ev_mid, void* ev_end);
+
+/* What a call would run, for tests and reports (host-only, no launch). */
+typedef struct gn_plan_desc {
+  int regime;            /* 0 = two-kernel path (reduce, then elementwise) */
+  int launches;          /* kernels one call enqueues */
+  int vector_width;      /* elements per access: 16-byte vectors, or 1 (scalar path) */
+  int threads;           /* threads per CTA */
+  int64_t ctas;          /* CTAs per kernel */
+  int64_t partials;      /* fp32 partial-sum records written per call */
+  size_t workspace_bytes;
+} gn_plan_desc;
+
+/* Fills *out with the plan of gn_fwd/gn_bwd for this problem, assuming every
+ * data pointer is 16-byte aligned when `aligned` is nonzero.  Returns a
+ * gn_status. */
+GN_API int gn_plan_info(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout, int dtype,
+                 int aligned, gn_plan_desc* out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GN_H_ */

@@ -1,0 +1,136 @@
+"""C-ABI checks that need no GPU: the library loads, exports every symbol the
+header declares, validates arguments before touching the device, sizes
+workspaces and plans consistently.  No compute call is made here."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from backward_normalization_gb300 import build as lib_build
+from backward_normalization_gb300 import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def gn():
+    lib_build.build()
+    from backward_normalization_gb300 import gn as mod
+
+    mod.lib()
+    return mod
+
+
+def _declared_symbols():
+    names = []
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if h.endswith(".h"):
+            txt = open(os.path.join(ROOT, "include", h)).read()
+            names += re.findall(r"GN_API[^;{(]*?\b(gn_\w+)\s*\(", txt)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(gn):
+    names = _declared_symbols()
+    assert "gn_fwd" in names and "gn_bwd" in names and "gn_workspace_size" in names
+    L = gn.lib()
+    for n in names:
+        assert hasattr(L, n), f"{n} declared in include/ but not exported"
+
+
+def test_status_strings(gn):
+    for s in range(5):
+        assert gn.status_string(s).startswith("GN_")
+    assert "unknown" in gn.status_string(99)
+
+
+def test_workspace_size(gn):
+    for w in synth.WORKLOADS:
+        for op in (0, 1):
+            n = gn.workspace_size(op, w.N, w.C, w.HW, w.G, w.layout, w.dtype)
+            assert n > 0 and n % 256 == 0
+            d = gn.plan_info(op, w.N, w.C, w.HW, w.G, w.layout, w.dtype, aligned=True)
+            assert d.workspace_bytes <= n
+            d1 = gn.plan_info(op, w.N, w.C, w.HW, w.G, w.layout, w.dtype, aligned=False)
+            assert d1.workspace_bytes <= n
+    # invalid or empty problems need no workspace
+    assert gn.workspace_size(0, 2, 6, 4, 4, "nchw", "f32") == 0   # G does not divide C
+    assert gn.workspace_size(0, 0, 8, 4, 2, "nhwc", "f16") == 0
+    assert gn.workspace_size(1, 2, 8, 0, 2, "nhwc", "f16") == 0
+    assert gn.workspace_size(7, 2, 8, 4, 2, "nhwc", "f16") == 0
+    assert gn.lib().gn_workspace_size(0, 2, 8, 4, 2, 5, 0) == 0
+
+
+FAKE = 1 << 20  # a 16-byte aligned address that is never dereferenced
+
+
+def _fwd(gn, **kw):
+    a = dict(x=FAKE, N=2, C=8, HW=16, G=2, layout=0, dtype=0, gamma=None, beta=None, eps=1e-5,
+             y=FAKE * 2, mean=FAKE * 3, rstd=FAKE * 4, ws=FAKE * 5, ws_bytes=1 << 30, stream=None)
+    a.update(kw)
+    return gn.lib().gn_fwd(a["x"], a["N"], a["C"], a["HW"], a["G"], a["layout"], a["dtype"],
+                           a["gamma"], a["beta"], a["eps"], a["y"], a["mean"], a["rstd"], a["ws"],
+                           a["ws_bytes"], a["stream"])
+
+
+def _bwd(gn, **kw):
+    a = dict(dy=FAKE, x=FAKE * 2, mean=FAKE * 3, rstd=FAKE * 4, gamma=None, N=2, C=8, HW=16, G=2,
+             layout=1, dtype=1, dx=FAKE * 5, dgamma=None, dbeta=None, ws=FAKE * 6,
+             ws_bytes=1 << 30, stream=None)
+    a.update(kw)
+    return gn.lib().gn_bwd(a["dy"], a["x"], a["mean"], a["rstd"], a["gamma"], a["N"], a["C"],
+                           a["HW"], a["G"], a["layout"], a["dtype"], a["dx"], a["dgamma"],
+                           a["dbeta"], a["ws"], a["ws_bytes"], a["stream"])
+
+
+def test_validation_before_any_launch(gn):
+    INV, UNS, WS = gn.GN_ERR_INVALID, gn.GN_ERR_UNSUPPORTED, gn.GN_ERR_WORKSPACE
+    assert _fwd(gn, G=3) == INV                 # 3 does not divide 8
+    assert _fwd(gn, G=0) == INV
+    assert _fwd(gn, N=-1) == INV
+    assert _fwd(gn, layout=2) == UNS
+    assert _fwd(gn, dtype=5) == UNS
+    assert _fwd(gn, x=None) == INV
+    assert _fwd(gn, mean=None) == INV
+    assert _fwd(gn, eps=-1.0) == INV
+    assert _fwd(gn, eps=float("nan")) == INV
+    assert _fwd(gn, y=FAKE + 4) == INV           # y overlaps x without being x
+    assert _fwd(gn, mean=FAKE + 8) == INV        # stats inside x
+    assert _fwd(gn, ws=None) == WS
+    assert _fwd(gn, ws_bytes=8) == WS
+    assert _fwd(gn, ws=FAKE * 5 + 8) == WS       # misaligned workspace
+    assert _fwd(gn, N=0) == 0                    # empty: nothing to do
+    assert _fwd(gn, HW=0, x=None) == 0
+    assert _bwd(gn, G=5) == INV
+    assert _bwd(gn, dy=None) == INV
+    assert _bwd(gn, dx=FAKE * 2 + 2) == INV      # dx overlaps x without being x
+    assert _bwd(gn, dgamma=FAKE * 7, dbeta=FAKE * 7) == INV
+    assert _bwd(gn, ws_bytes=0) == WS
+    assert _bwd(gn, C=0) == 0
+    ws_need = gn.workspace_size(1, 2, 8, 16, 2, "nhwc", "f16")
+    assert _bwd(gn, ws_bytes=ws_need - 1) == WS
+
+
+def test_plan_vector_width_and_modes(gn):
+    d = gn.plan_info(0, 1, 128, 2048 * 1024, 16, "nhwc", "f16")
+    assert d.vector_width == 8 and d.launches == 2
+    assert gn.plan_info(0, 2, 6, 77, 3, "nhwc", "f16").vector_width == 1       # C*2 % 16 != 0
+    assert gn.plan_info(0, 2, 64, 2303, 8, "nchw", "f32").vector_width == 1    # HW*4 % 16 != 0
+    assert gn.plan_info(0, 2, 64, 2304, 8, "nchw", "f32").vector_width == 4
+    assert gn.plan_info(0, 2, 32, 256, 8, "nchw", "f32").threads == 256         # small planes: warp per plane
+    assert gn.plan_info(0, 2, 64, 4096, 8, "nchw", "f32").threads == 512        # large planes: CTA per chunk
+    for w in synth.WORKLOADS:
+        d = gn.plan_info(1, w.N, w.C, w.HW, w.G, w.layout, w.dtype)
+        assert 0 < d.ctas < 2 ** 31
+        assert d.threads % 32 == 0 or w.layout == "nhwc"
+
+
+def test_configs_cover_both_layouts_and_vector_paths(gn):
+    seen = set()
+    for w in synth.WORKLOADS:
+        d = gn.plan_info(0, w.N, w.C, w.HW, w.G, w.layout, w.dtype)
+        seen.add((w.layout, d.vector_width > 1, d.threads))
+    assert {s[0] for s in seen} == {"nchw", "nhwc"}

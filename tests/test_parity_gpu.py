@@ -1,0 +1,306 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle.
+
+Small cases (the oracle runs in well under a second) are compared element by
+element; they span several CTAs, ragged row/chunk tails, both layouts, all
+three dtypes, the 16-byte vector path and the scalar path.  The full-size
+workloads are compared on sampled outputs plus the complete dgamma/dbeta.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from backward_normalization_gb300 import gn, synth
+from tests import checks
+
+pytestmark = pytest.mark.gpu
+
+W = synth.BY_NAME
+
+
+def _small_cases():
+    c0, c1, c2, c3, c4 = synth.WORKLOADS
+    return [
+        ("fp32_nchw_2x32x16x16_g8", c0),
+        ("fp16_nhwc_1x128x61x97_g16", c1.scaled(name="s1", H=61, W=97)),
+        ("bf16_nhwc_3x320x17x17_g32", c2.scaled(name="s2", N=3, H=17, W=17)),
+        ("fp32_nchw_3x64x48x48_g8", c3.scaled(name="s3", N=3, H=48, W=48)),
+        ("fp32_nchw_2x64x47x49_g8_scalar", c3.scaled(name="s3b", N=2, H=47, W=49)),
+        ("bf16_nhwc_4x512x12x12_g32_offsets", c4.scaled(name="s4", N=4, H=12, W=12)),
+        ("fp16_nchw_2x24x20x20_g1_layernorm", c1.scaled(name="ln", layout="nchw", N=2, C=24, G=1, H=20, W=20)),
+        ("bf16_nhwc_2x48x5x10_g48_instancenorm", c2.scaled(name="in", N=2, C=48, G=48, H=5, W=10)),
+        ("fp16_nhwc_3x6x7x11_g3_scalar", c1.scaled(name="sc", N=3, C=6, G=3, H=7, W=11)),
+        ("fp32_nchw_5x12x1x1_g4", c0.scaled(name="hw1", N=5, C=12, G=4, H=1, W=1)),
+        ("bf16_nhwc_7x16x1x1_g4", c2.scaled(name="hw1b", N=7, C=16, G=4, H=1, W=1)),
+        ("fp32_nchw_1x1x1x3_g1", c0.scaled(name="tiny", N=1, C=1, G=1, H=1, W=3)),
+        ("fp16_nhwc_2x4096x5x8_g32_wide", c1.scaled(name="wide", N=2, C=4096, G=32, H=5, W=8)),
+        ("fp32_nhwc_2x64x15x20_g8", c0.scaled(name="f32nhwc", layout="nhwc", C=64, H=15, W=20)),
+        ("fp16_nchw_2x16x64x64_g4", c1.scaled(name="f16nchw", layout="nchw", N=2, C=16, G=4, H=64, W=64)),
+        ("bf16_nchw_2x8x3x683_g2_scalar", c2.scaled(name="b16nchw", layout="nchw", N=2, C=8, G=2, H=3, W=683)),
+        ("bf16_nhwc_1x32x300x300_g8_many_rows", c2.scaled(name="rows", N=1, C=32, G=8, H=300, W=300)),
+    ]
+
+
+SMALL = _small_cases()
+
+
+def _oracle_full(inp, w):
+    o = oracle.get()
+    L = synth.LAYOUTS[w.layout]
+    x = inp["x"].double().numpy()
+    dy = inp["dy"].double().numpy()
+    g = inp["gamma"].double().numpy()
+    b = inp["beta"].double().numpy()
+    y, mean, rstd = o.forward(x, w.N, w.C, w.HW, w.G, L, g, b, w.eps)
+    dx, dg, db = o.backward(dy, x, w.N, w.C, w.HW, w.G, L, g, w.eps)
+    return dict(y=y, mean=mean, rstd=rstd, dx=dx, dgamma=dg, dbeta=db)
+
+
+def _gpu_run(inp, w, dev="cuda", gamma=True, beta=True, params=True):
+    x = inp["x"].to(dev)
+    dy = inp["dy"].to(dev)
+    gm = inp["gamma"].to(dev) if gamma else None
+    bt = inp["beta"].to(dev) if beta else None
+    y, mean, rstd = gn.forward(x, w.N, w.C, w.HW, w.G, w.layout, gm, bt, w.eps)
+    dx, dg, db = gn.backward(dy, x, mean, rstd, w.N, w.C, w.HW, w.G, w.layout, gm,
+                             need_params=params)
+    torch.cuda.synchronize()
+    return dict(y=y, mean=mean, rstd=rstd, dx=dx, dgamma=dg, dbeta=db)
+
+
+def _compare(got, ref, w):
+    checks.assert_out("y", got["y"], ref["y"], w.dtype)
+    checks.assert_out("dx", got["dx"], ref["dx"], w.dtype)
+    checks.assert_stat("mean", got["mean"], ref["mean"])
+    checks.assert_stat("rstd", got["rstd"], ref["rstd"])
+    if got["dgamma"] is not None:
+        checks.assert_param("dgamma", got["dgamma"], ref["dgamma"])
+        checks.assert_param("dbeta", got["dbeta"], ref["dbeta"])
+
+
+@pytest.mark.parametrize("name,w", SMALL, ids=[c[0] for c in SMALL])
+def test_small_parity(name, w):
+    inp = synth.make_inputs(w, "cpu", seed=0)
+    got = _gpu_run(inp, w)
+    _compare(got, _oracle_full(inp, w), w)
+
+
+@pytest.mark.parametrize("name,w", SMALL[:6], ids=[c[0] for c in SMALL[:6]])
+def test_bit_identical_runs(name, w):
+    inp = synth.make_inputs(w, "cpu", seed=1)
+    a = _gpu_run(inp, w)
+    b = _gpu_run(inp, w)
+    for k in a:
+        assert torch.equal(a[k].view(torch.uint8) if a[k].dtype != torch.float32 else a[k],
+                           b[k].view(torch.uint8) if b[k].dtype != torch.float32 else b[k]), k
+
+
+@pytest.mark.parametrize("name,w", [SMALL[1], SMALL[3], SMALL[0]], ids=["nhwc", "nchw_m0", "nchw_m1"])
+def test_no_affine_and_output_mask(name, w):
+    inp = synth.make_inputs(w, "cpu", seed=2)
+    got = _gpu_run(inp, w, gamma=False, beta=False, params=False)
+    o = oracle.get()
+    L = synth.LAYOUTS[w.layout]
+    x, dy = inp["x"].double().numpy(), inp["dy"].double().numpy()
+    y, mean, rstd = o.forward(x, w.N, w.C, w.HW, w.G, L, None, None, w.eps)
+    dx, dg, db = o.backward(dy, x, w.N, w.C, w.HW, w.G, L, None, w.eps)
+    checks.assert_out("y", got["y"], y, w.dtype)
+    checks.assert_out("dx", got["dx"], dx, w.dtype)
+    checks.assert_stat("rstd", got["rstd"], rstd)
+    # gamma given but beta absent: beta = 0
+    inp2 = dict(inp)
+    got2 = _gpu_run(inp2, w, gamma=True, beta=False)
+    y2, _, _ = o.forward(x, w.N, w.C, w.HW, w.G, L, inp["gamma"].double().numpy(), None, w.eps)
+    checks.assert_out("y(no beta)", got2["y"], y2, w.dtype)
+
+
+@pytest.mark.parametrize("name,w", [SMALL[1], SMALL[3]], ids=["nhwc", "nchw"])
+def test_misaligned_pointers_take_scalar_path(name, w):
+    """Buffers offset by one element (not 16-byte aligned) still give the
+    right answer (the scalar path)."""
+    inp = synth.make_inputs(w, "cpu", seed=3)
+    dev = "cuda"
+    E = w.E
+    dt = synth.DTYPES[w.dtype]
+    xb = torch.empty(E + 1, dtype=dt, device=dev)
+    dyb = torch.empty(E + 1, dtype=dt, device=dev)
+    yb = torch.empty(E + 1, dtype=dt, device=dev)
+    dxb = torch.empty(E + 1, dtype=dt, device=dev)
+    x, dy, y, dx = xb[1:], dyb[1:], yb[1:], dxb[1:]
+    x.copy_(inp["x"])
+    dy.copy_(inp["dy"])
+    gm, bt = inp["gamma"].to(dev), inp["beta"].to(dev)
+    mean = torch.empty(w.N * w.G, device=dev)
+    rstd = torch.empty(w.N * w.G, device=dev)
+    ws = gn.alloc_workspace(gn.OP_BWD, w.N, w.C, w.HW, w.G, w.layout, dt)
+    assert gn.fwd_raw(x, w.N, w.C, w.HW, w.G, w.layout, gm, bt, w.eps, y, mean, rstd, ws) == 0
+    dg = torch.empty(w.C, device=dev)
+    db = torch.empty(w.C, device=dev)
+    assert gn.bwd_raw(dy, x, mean, rstd, gm, w.N, w.C, w.HW, w.G, w.layout, dx, dg, db, ws) == 0
+    torch.cuda.synchronize()
+    assert gn.plan_info(0, w.N, w.C, w.HW, w.G, w.layout, dt, aligned=False).vector_width == 1
+    _compare(dict(y=y, mean=mean, rstd=rstd, dx=dx, dgamma=dg, dbeta=db), _oracle_full(inp, w), w)
+
+
+@pytest.mark.parametrize("name,w", [SMALL[2], SMALL[3]], ids=["nhwc", "nchw"])
+def test_in_place(name, w):
+    """y may overwrite x, and dx may overwrite dy."""
+    inp = synth.make_inputs(w, "cpu", seed=4)
+    ref = _oracle_full(inp, w)
+    dev = "cuda"
+    x = inp["x"].to(dev)
+    gm, bt = inp["gamma"].to(dev), inp["beta"].to(dev)
+    mean = torch.empty(w.N * w.G, device=dev)
+    rstd = torch.empty(w.N * w.G, device=dev)
+    ws = gn.alloc_workspace(gn.OP_BWD, w.N, w.C, w.HW, w.G, w.layout, x.dtype)
+    x_keep = x.clone()
+    assert gn.fwd_raw(x, w.N, w.C, w.HW, w.G, w.layout, gm, bt, w.eps, x, mean, rstd, ws) == 0
+    torch.cuda.synchronize()
+    checks.assert_out("y(in place)", x, ref["y"], w.dtype)
+    dy = inp["dy"].to(dev)
+    dg = torch.empty(w.C, device=dev)
+    db = torch.empty(w.C, device=dev)
+    assert gn.bwd_raw(dy, x_keep, mean, rstd, gm, w.N, w.C, w.HW, w.G, w.layout, dy, dg, db, ws) == 0
+    torch.cuda.synchronize()
+    checks.assert_out("dx(in place)", dy, ref["dx"], w.dtype)
+    checks.assert_param("dgamma", dg, ref["dgamma"])
+
+
+def test_garbage_workspace_and_canaries():
+    """The workspace needs no zero-fill, and nothing is written past the end of
+    the workspace or of any output."""
+    w = SMALL[5][1]
+    inp = synth.make_inputs(w, "cpu", seed=5)
+    ref = _oracle_full(inp, w)
+    dev = "cuda"
+    dt = synth.DTYPES[w.dtype]
+    pad = 64
+    n_ws = gn.workspace_size(gn.OP_BWD, w.N, w.C, w.HW, w.G, w.layout, dt)
+    n_ws = max(n_ws, gn.workspace_size(gn.OP_FWD, w.N, w.C, w.HW, w.G, w.layout, dt))
+    wsb = torch.randint(0, 256, (n_ws + 256,), dtype=torch.uint8, device=dev)
+    canary_ws = wsb[n_ws:].clone()
+    ws = wsb[:n_ws]
+
+    def padded(n, dtype):
+        b = torch.full((n + 2 * pad,), 7.0, dtype=dtype, device=dev)
+        return b, b[pad:pad + n]
+
+    yb, y = padded(w.E, dt)
+    dxb, dx = padded(w.E, dt)
+    mb, mean = padded(w.N * w.G, torch.float32)
+    rb, rstd = padded(w.N * w.G, torch.float32)
+    gb, dg = padded(w.C, torch.float32)
+    bb, db = padded(w.C, torch.float32)
+    x, dy = inp["x"].to(dev), inp["dy"].to(dev)
+    gm, bt = inp["gamma"].to(dev), inp["beta"].to(dev)
+    for _ in range(2):
+        assert gn.fwd_raw(x, w.N, w.C, w.HW, w.G, w.layout, gm, bt, w.eps, y, mean, rstd, ws) == 0
+        assert gn.bwd_raw(dy, x, mean, rstd, gm, w.N, w.C, w.HW, w.G, w.layout, dx, dg, db, ws) == 0
+    torch.cuda.synchronize()
+    assert torch.equal(wsb[n_ws:], canary_ws)
+    for b in (yb, dxb, mb, rb, gb, bb):
+        assert torch.all(b[:pad] == 7.0) and torch.all(b[-pad:] == 7.0)
+    _compare(dict(y=y, mean=mean, rstd=rstd, dx=dx, dgamma=dg, dbeta=db), ref, w)
+
+
+def test_shared_workspace_across_shapes():
+    """Calls of different shapes in a row on one workspace stay correct."""
+    dev = "cuda"
+    cases = [SMALL[0][1], SMALL[2][1], SMALL[3][1], SMALL[2][1]]
+    n_ws = max(gn.workspace_size(op, w.N, w.C, w.HW, w.G, w.layout, w.dtype)
+               for w in cases for op in (0, 1))
+    ws = torch.full((n_ws,), 255, dtype=torch.uint8, device=dev)
+    for i, w in enumerate(cases):
+        inp = synth.make_inputs(w, "cpu", seed=10 + i)
+        x, dy = inp["x"].to(dev), inp["dy"].to(dev)
+        gm, bt = inp["gamma"].to(dev), inp["beta"].to(dev)
+        y, mean, rstd = gn.forward(x, w.N, w.C, w.HW, w.G, w.layout, gm, bt, w.eps, workspace=ws)
+        dx, dg, db = gn.backward(dy, x, mean, rstd, w.N, w.C, w.HW, w.G, w.layout, gm, workspace=ws)
+        torch.cuda.synchronize()
+        _compare(dict(y=y, mean=mean, rstd=rstd, dx=dx, dgamma=dg, dbeta=db), _oracle_full(inp, w), w)
+
+
+def test_zero_extents():
+    dev = "cuda"
+    x = torch.empty(0, device=dev)
+    mean = torch.empty(0, device=dev)
+    assert gn.fwd_raw(x, 0, 8, 16, 2, "nchw", None, None, 1e-5, x, mean, mean, None) == 0
+    dg = torch.full((8,), 3.0, device=dev)
+    db = torch.full((8,), 3.0, device=dev)
+    assert gn.bwd_raw(x, x, mean, mean, None, 4, 8, 0, 2, "nhwc", x, dg, db, None) == 0
+    torch.cuda.synchronize()
+    assert torch.all(dg == 0) and torch.all(db == 0)
+
+
+def test_constant_group_gives_beta():
+    """A constant group: xhat = 0, so y = beta and rstd = 1/sqrt(eps)."""
+    w = SMALL[0][1]
+    inp = synth.make_inputs(w, "cpu", seed=6)
+    inp["x"] = torch.full_like(inp["x"], 1.5)
+    got = _gpu_run(inp, w)
+    ref = _oracle_full(inp, w)
+    checks.assert_out("y", got["y"], ref["y"], w.dtype)
+    checks.assert_stat("rstd", got["rstd"], ref["rstd"])
+    checks.assert_out("dx", got["dx"], ref["dx"], w.dtype)
+
+
+# ------------------------------------------------------------- full sizes
+def _sample_offsets(w, k=4096, seed=0):
+    rng = np.random.default_rng(seed)
+    idx = rng.integers(0, w.E, k)
+    edge = [0, w.E - 1, w.E // 2]
+    return np.unique(np.concatenate([idx, edge])).astype(np.int64)
+
+
+@pytest.mark.parametrize("w", synth.WORKLOADS[1:], ids=[w.name for w in synth.WORKLOADS[1:]])
+def test_full_size_sampled(w):
+    """The benchmarked workloads at full size: y and dx at sampled offsets and
+    mean/rstd/dgamma/dbeta in full, against the oracle; plus a bit-identical
+    rerun.  Large NCHW inputs are handed to the oracle one sample at a time
+    (the statistics of sample n depend on sample n only)."""
+    dev = "cuda"
+    inp = synth.make_inputs(w, dev, seed=0)
+    got = _gpu_run(inp, w)
+    again = _gpu_run(inp, w)
+    for k in ("y", "dx"):
+        assert torch.equal(got[k].view(torch.uint8) if got[k].dtype != torch.float32 else got[k],
+                           again[k].view(torch.uint8) if again[k].dtype != torch.float32 else again[k]), k
+    for k in ("mean", "rstd", "dgamma", "dbeta"):
+        assert torch.equal(got[k], again[k]), k
+    del again
+    o = oracle.get()
+    L = synth.LAYOUTS[w.layout]
+    gm = inp["gamma"].double().cpu().numpy()
+    bt = inp["beta"].double().cpu().numpy()
+    idx = _sample_offsets(w)
+    per_n = w.C * w.HW
+    chunk_n = max(1, min(w.N, (1 << 27) // per_n))  # at most ~128M elements per oracle call
+    mean_ref = np.zeros(w.N * w.G)
+    rstd_ref = np.zeros(w.N * w.G)
+    dg_ref = np.zeros(w.C)
+    db_ref = np.zeros(w.C)
+    y_ref = np.zeros(idx.size)
+    dx_ref = np.zeros(idx.size)
+    for n0 in range(0, w.N, chunk_n):
+        n1 = min(w.N, n0 + chunk_n)
+        lo, hi = n0 * per_n, n1 * per_n
+        sel = (idx >= lo) & (idx < hi)
+        xs = inp["x"][lo:hi].double().cpu().numpy()
+        dys = inp["dy"][lo:hi].double().cpu().numpy()
+        ya, m, r = o.forward_at(xs, n1 - n0, w.C, w.HW, w.G, L, gm, bt, w.eps, idx[sel] - lo)
+        dxa, dg, db = o.backward_at(dys, xs, n1 - n0, w.C, w.HW, w.G, L, gm, w.eps, idx[sel] - lo)
+        y_ref[sel] = ya
+        dx_ref[sel] = dxa
+        mean_ref[n0 * w.G:n1 * w.G] = m
+        rstd_ref[n0 * w.G:n1 * w.G] = r
+        dg_ref += dg
+        db_ref += db
+    it = torch.from_numpy(idx).to(dev)
+    checks.assert_out("y", got["y"][it], y_ref, w.dtype)
+    checks.assert_out("dx", got["dx"][it], dx_ref, w.dtype)
+    checks.assert_stat("mean", got["mean"], mean_ref)
+    checks.assert_stat("rstd", got["rstd"], rstd_ref)
+    checks.assert_param("dgamma", got["dgamma"], dg_ref)
+    checks.assert_param("dbeta", got["dbeta"], db_ref)
