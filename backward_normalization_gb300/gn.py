@@ -129,7 +129,11 @@ def set_timing_events(ev_begin=None, ev_mid=None, ev_end=None) -> None:
     """Make the following calls of this thread record torch.cuda.Event objects
     before, between and after their two kernels (None: no record)."""
     def h(e):
-        return None if e is None else e.cuda_event
+        if e is None:
+            return None
+        if not e.cuda_event:  # torch creates the CUDA event on first record
+            e.record()
+        return e.cuda_event
     lib().gn_set_timing_events(h(ev_begin), h(ev_mid), h(ev_end))
 
 

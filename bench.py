@@ -259,6 +259,51 @@ def time_configs(gn, synth, torch, flush, reps=20):
     return out
 
 
+def run_e2e(args, torch, dist, world, stream, x, dy, gm, bt, y, dx, mean, rstd, dg, db, step,
+            flush, bytes_step):
+    """The same metric through the C ABI with pinned host buffers: every step
+    copies x, dy, gamma, beta in and y, dx, mean, rstd, dgamma, dbeta out."""
+    w_numel = x.numel()
+    hx = x.cpu().pin_memory()
+    hdy = dy.cpu().pin_memory()
+    hg, hb = gm.cpu().pin_memory(), bt.cpu().pin_memory()
+    hy = torch.empty_like(hx).pin_memory()
+    hdx = torch.empty_like(hx).pin_memory()
+    hst = torch.empty(mean.numel() + rstd.numel() + dg.numel() + db.numel(),
+                      dtype=torch.float32).pin_memory()
+    h2d = (hx.numel() + hdy.numel()) * hx.element_size() + (hg.numel() + hb.numel()) * 4
+    d2h = (hy.numel() + hdx.numel()) * hy.element_size() + hst.numel() * 4
+    assert hx.numel() == w_numel
+    Ke = max(3, min(10, args.steps))
+    times = []
+    for k in range(Ke + 2):
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        x.copy_(hx, non_blocking=True)
+        dy.copy_(hdy, non_blocking=True)
+        gm.copy_(hg, non_blocking=True)
+        bt.copy_(hb, non_blocking=True)
+        step()
+        hy.copy_(y, non_blocking=True)
+        hdx.copy_(dx, non_blocking=True)
+        hst.copy_(torch.cat([mean, rstd, dg, db]), non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize()
+        if k >= 2:
+            times.append(a.elapsed_time(b))
+        flush()
+    ms = torch.tensor([statistics.mean(times)], dtype=torch.float64, device=x.device)
+    if world > 1:
+        dist.all_reduce(ms, op=dist.ReduceOp.MAX)
+    value = world * bytes_step / (float(ms.item()) * 1e-3) / 1e9
+    return {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(float(ms.item()), 3)}
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -348,41 +393,10 @@ def run_ours(args, rank, world, local_rank):
     value = world * bytes_step / (ms_per_step * 1e-3) / 1e9
 
     # ---- e2e through the C ABI with host buffers (pinned), copies timed
-    hx = x.cpu().pin_memory()
-    hdy = dy.cpu().pin_memory()
-    hg, hb = gm.cpu().pin_memory(), bt.cpu().pin_memory()
-    hy = torch.empty_like(hx).pin_memory()
-    hdx = torch.empty_like(hx).pin_memory()
-    hst = torch.empty(2 * w.N * w.G + 2 * w.C, dtype=torch.float32).pin_memory()
-    h2d = (hx.numel() + hdy.numel()) * hx.element_size() + (hg.numel() + hb.numel()) * 4
-    d2h = (hy.numel() + hdx.numel()) * hy.element_size() + hst.numel() * 4
-    Ke = max(3, min(10, K))
-    e2e_times = []
-    for k in range(Ke + 2):
-        torch.cuda.synchronize()
-        if world > 1:
-            dist.barrier()
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        x.copy_(hx, non_blocking=True)
-        dy.copy_(hdy, non_blocking=True)
-        gm.copy_(hg, non_blocking=True)
-        bt.copy_(hb, non_blocking=True)
-        step()
-        hy.copy_(y, non_blocking=True)
-        hdx.copy_(dx, non_blocking=True)
-        hst.copy_(torch.cat([mean, rstd, dg, db]), non_blocking=True)
-        b.record(stream)
-        torch.cuda.synchronize()
-        if k >= 2:
-            e2e_times.append(a.elapsed_time(b))
-        flush()
-    e2e_ms = torch.tensor([statistics.mean(e2e_times)], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(e2e_ms, op=dist.ReduceOp.MAX)
-    e2e_value = world * bytes_step / (float(e2e_ms.item()) * 1e-3) / 1e9
-    del hx, hdy, hy, hdx
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, torch, dist, world, stream, x, dy, gm, bt, y, dx, mean, rstd, dg, db,
+                      step, flush, bytes_step)
 
     if rank != 0:
         return 0
@@ -426,8 +440,7 @@ def run_ours(args, rank, world, local_rank):
             "frac_of_8tbs": round(value / world / 8000.0, 4)}),
         "roofline": roofline,
         "cpu_baseline": cpu,
-        "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+        "e2e": e2e,
         "gpu_launches": (plan_f.launches + plan_b.launches) * K,
         "clocks": clk,
         "per_config": per_config,
@@ -444,6 +457,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-per-config", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
