@@ -1,6 +1,5 @@
 // gn_api.cu -- the C ABI declared in include/gn.h: argument validation
 // (before anything is enqueued), planning and kernel dispatch.
-#include <atomic>
 #include <cstring>
 
 #include "../../include/gn.h"
@@ -10,13 +9,6 @@ namespace {
 
 thread_local int t_last_cuda_error = 0;
 thread_local gn::TimingEvents t_events = {nullptr, nullptr, nullptr};
-std::atomic<unsigned> g_epoch{0};
-
-unsigned next_epoch() {
-  unsigned e = g_epoch.fetch_add(1u, std::memory_order_relaxed) + 1u;
-  if (e == 0u) e = g_epoch.fetch_add(1u, std::memory_order_relaxed) + 1u;
-  return e;
-}
 
 int elem_size(int dtype) { return dtype == gn::kF32 ? 4 : 2; }
 
@@ -57,12 +49,10 @@ int prepare(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout, int
   const gn::WsLayout w = gn::ws_layout(op, p->g);
   if (!workspace || workspace_bytes < w.total || !aligned16(workspace)) return GN_ERR_WORKSPACE;
   char* ws = static_cast<char*>(workspace);
-  p->tickets = reinterpret_cast<unsigned long long*>(ws + w.tickets);
-  p->err = reinterpret_cast<unsigned*>(ws + w.err);
+  p->tickets = reinterpret_cast<unsigned*>(ws + w.tickets);
   p->part = reinterpret_cast<float2*>(ws + w.part);
   p->chst = reinterpret_cast<float2*>(ws + w.chst);
   p->coef = reinterpret_cast<float2*>(ws + w.coef);
-  p->epoch = next_epoch();
   return GN_OK;
 }
 
@@ -121,7 +111,7 @@ int gn_fwd(const void* x, int64_t N, int64_t C, int64_t HW, int64_t G, int layou
   p.rstd = rstd;
   p.eps = eps;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const cudaError_t e = layout == GN_LAYOUT_NHWC ? gn::launch_nhwc_fwd(p, s) : gn::launch_nchw_fwd(p, s);
+  const cudaError_t e = layout == GN_LAYOUT_NHWC ? gn::launch_nhwc(p, s, false) : gn::launch_nchw(p, s, false);
   return e == cudaSuccess ? GN_OK : cuda_fail(e);
 }
 
@@ -165,7 +155,7 @@ int gn_bwd(const void* dy, const void* x, const float* mean, const float* rstd,
   p.rstd = const_cast<float*>(rstd);
   p.dgamma = dgamma;
   p.dbeta = dbeta;
-  const cudaError_t e = layout == GN_LAYOUT_NHWC ? gn::launch_nhwc_bwd(p, s) : gn::launch_nchw_bwd(p, s);
+  const cudaError_t e = layout == GN_LAYOUT_NHWC ? gn::launch_nhwc(p, s, true) : gn::launch_nchw(p, s, true);
   return e == cudaSuccess ? GN_OK : cuda_fail(e);
 }
 
@@ -203,7 +193,7 @@ int gn_plan_info(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout
   out->vector_width = g.vw;
   out->threads = g.tpb;
   out->ctas = g.items;
-  out->partials = g.N * g.C * g.T;
+  out->partials = g.N * g.C * g.Tp;
   out->workspace_bytes = gn::ws_layout(op, g).total;
   return GN_OK;
 }

@@ -1,9 +1,10 @@
 // gn_device.cuh -- device-side building blocks shared by the GroupNorm kernels:
 // 16-byte vector loads/stores with L2 cache-policy hints, fp16/bf16/fp32
-// conversion, deterministic block reductions and the per-unit arrival ticket
-// used by the "last CTA finalises" reductions.
+// conversion, deterministic block and cluster reductions and the per-unit
+// arrival counter used by the "last CTA finalises" reductions.
 #pragma once
 
+#include <cooperative_groups.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
@@ -11,6 +12,8 @@
 #include "gn_internal.h"
 
 namespace gn {
+
+namespace cg = cooperative_groups;
 
 // ------------------------------------------------------------ cache policies
 __device__ __forceinline__ uint64_t policy_evict_last() {
@@ -67,12 +70,6 @@ struct Elem<__nv_bfloat16> {
   __device__ static __nv_bfloat16 from_f(float v) { return __float2bfloat16_rn(v); }
 };
 
-__device__ __forceinline__ void unpack16(const uint4& u, float (&f)[4], float) {
-  f[0] = __uint_as_float(u.x);
-  f[1] = __uint_as_float(u.y);
-  f[2] = __uint_as_float(u.z);
-  f[3] = __uint_as_float(u.w);
-}
 __device__ __forceinline__ float2 h2f(uint32_t w) {
   __half2 h;
   *reinterpret_cast<uint32_t*>(&h) = w;
@@ -192,39 +189,52 @@ __device__ __forceinline__ float2 block_sum2_t0(float a, float b, float* scratch
 }
 
 // --------------------------------------------------------------- tickets
-// A ticket word counts the CTAs of one reduction unit that have published
-// their partial results.  The high 32 bits carry the call's epoch and the low
-// 32 bits the count, so a word left over from another call (or never
-// initialised) reads as count 0: no zero-filled workspace is needed.  The CTA
-// whose arrival completes the unit returns true; it resets the word to 0 once
-// it has finished.  The CAS loop always makes progress (a retry means another
-// CTA's CAS succeeded); the iteration bound is only a safety net and, when hit,
-// raises the error word instead of looping.
-__device__ __forceinline__ bool ticket_arrive(unsigned long long* t, unsigned epoch,
-                                              unsigned long long total, unsigned* err) {
-  unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(t);
-  for (int it = 0; it < (1 << 24); ++it) {
-    const unsigned long long cnt =
-        ((unsigned)(old >> 32) == epoch) ? (old & 0xffffffffull) : 0ull;
-    const unsigned long long nw = ((unsigned long long)epoch << 32) | (cnt + 1ull);
-    const unsigned long long prev = atomicCAS(t, old, nw);
-    if (prev == old) return cnt + 1ull == total;
-    old = prev;
-  }
-  atomicOr(err, 1u);
-  return false;
-}
-
-// Called by thread 0 after the CTA's partial stores (and a __syncthreads()).
-// Makes the stores visible device-wide before arriving; when this CTA is the
-// last one, the trailing fence orders the following reads of other CTAs'
-// partials after the arrival.
-__device__ __forceinline__ bool publish_and_arrive(unsigned long long* t, unsigned epoch,
-                                                   unsigned long long total, unsigned* err) {
+// An arrival counter per reduction unit.  Every CTA that publishes a partial
+// result increments it once; the CTA that brings it to `total` is the last one
+// and finalises the unit, then sets the counter back to 0, so every completed
+// call leaves its counters at 0 for the next call.  (The workspace therefore
+// has to be zero-filled once, before its first use.)  atomicAdd never retries,
+// so arrivals cost one atomic each however many CTAs arrive together.
+//
+// Called by one thread after the CTA's partial stores and a __syncthreads():
+// the first fence makes this CTA's stores visible device-wide before its
+// arrival; the last CTA's fence orders its reads of the other CTAs' partials
+// after the arrival.
+__device__ __forceinline__ bool publish_and_arrive(unsigned* t, unsigned total) {
   __threadfence();
-  const bool last = ticket_arrive(t, epoch, total, err);
+  const unsigned old = atomicAdd(t, 1u);
+  const bool last = (old == total - 1u);
   if (last) __threadfence();
   return last;
+}
+
+// ------------------------------------------------------ cluster reduction
+// Adds, for every q < NQ, red[q*stride + slot] of all CTAs of the cluster into
+// the copy of cluster rank 0, in rank order.  Every thread of every CTA of the
+// cluster must call it.  The second cluster barrier keeps each CTA's shared
+// memory alive until rank 0 has read it.
+template <int NQ>
+__device__ __forceinline__ void cluster_sum_to_rank0(float* red, int stride, int slot, bool active) {
+  cg::cluster_group cluster = cg::this_cluster();
+  cluster.sync();
+  if (cluster.block_rank() == 0 && active) {
+    float acc[NQ];
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) acc[q] = red[q * stride + slot];
+    const unsigned nb = cluster.num_blocks();
+    for (unsigned r = 1; r < nb; ++r) {
+      const float* rem = cluster.map_shared_rank(red, r);
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) acc[q] += rem[q * stride + slot];
+    }
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) red[q * stride + slot] = acc[q];
+  }
+  cluster.sync();
+}
+
+__device__ __forceinline__ unsigned cluster_rank() {
+  return cg::this_cluster().block_rank();
 }
 
 }  // namespace gn

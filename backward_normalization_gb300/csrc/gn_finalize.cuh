@@ -8,10 +8,11 @@
 
 namespace gn {
 
-// For every channel c of sample n, sums the g.T partial records of (n, c) in
-// index order and calls fn(c, total) from one thread.  The T records of a
-// channel are split into up to blockDim.x / C contiguous slices summed in
-// parallel, and the slice sums are then added in slice order.
+// For every channel c of sample n, sums the g.Tp partial records of (n, c)
+// and calls fn(c, total) from one thread.  Threads are laid out as
+// (slice, channel) with consecutive threads on consecutive channels; slice s
+// adds records s, s + nsl, s + 2*nsl, ... (issued eight at a time so that the
+// loads overlap), then the slice sums are added in slice order.
 // `sm` holds at least 2 * blockDim.x floats.  Ends with __syncthreads().
 template <typename Fn>
 __device__ __forceinline__ void sum_channel_partials(const KParams& p, int64_t n, float* sm,
@@ -20,30 +21,28 @@ __device__ __forceinline__ void sum_channel_partials(const KParams& p, int64_t n
   const int tid = threadIdx.x, nt = blockDim.x;
   const int cpb = (int)(g.C < nt ? g.C : nt);
   int64_t nsl64 = nt / cpb;
-  if (nsl64 > g.T) nsl64 = g.T;
+  if (nsl64 > g.Tp) nsl64 = g.Tp;
   const int nsl = nsl64 < 1 ? 1 : (int)nsl64;
-  const int64_t Ts = (g.T + nsl - 1) / nsl;
   const int cl = tid % cpb, sl = tid / cpb;
-  const float2* base = p.part + n * g.C * g.T;
+  const float2* base = p.part + n * g.C * g.Tp;
   for (int64_t c0 = 0; c0 < g.C; c0 += cpb) {
     const int64_t c = c0 + cl;
     float ax = 0.f, ay = 0.f;
     if (sl < nsl && c < g.C) {
       const float2* pc = base + c * g.cstride;
-      const int64_t t0 = sl * Ts;
-      const int64_t t1 = (t0 + Ts < g.T) ? t0 + Ts : g.T;
-      int64_t t = t0;
-      for (; t + 4 <= t1; t += 4) {
-        const float2 v0 = __ldcg(pc + (t + 0) * g.tstride);
-        const float2 v1 = __ldcg(pc + (t + 1) * g.tstride);
-        const float2 v2 = __ldcg(pc + (t + 2) * g.tstride);
-        const float2 v3 = __ldcg(pc + (t + 3) * g.tstride);
-        ax += v0.x; ay += v0.y;
-        ax += v1.x; ay += v1.y;
-        ax += v2.x; ay += v2.y;
-        ax += v3.x; ay += v3.y;
+      const int64_t st = (int64_t)nsl * g.tstride;
+      int64_t t = sl;
+      for (; t + 7 * nsl < g.Tp; t += 8 * nsl) {
+        float2 v[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) v[k] = __ldcg(pc + t * g.tstride + k * st);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          ax += v[k].x;
+          ay += v[k].y;
+        }
       }
-      for (; t < t1; ++t) {
+      for (; t < g.Tp; t += nsl) {
         const float2 v = __ldcg(pc + t * g.tstride);
         ax += v.x;
         ay += v.y;
@@ -148,15 +147,15 @@ __device__ __forceinline__ void finalize_params(const KParams& p) {
   }
 }
 
-// Tail of every first-kernel CTA: publish this CTA's partials, and if the
-// sample is now complete run its finalisation (and, in the backward, the
-// parameter-gradient step once every sample is complete).
+// Tail of every CTA that published a cluster-level partial: arrive on the
+// sample's counter and, if the sample is now complete, run its finalisation
+// (and, in the backward, the parameter-gradient step once every sample is
+// complete).  Must be reached by all threads of the CTA.
 template <typename T, bool kBwd>
 __device__ __forceinline__ void arrive_and_finalize(const KParams& p, int64_t n, float* sm) {
   __shared__ int s_last;
   __syncthreads();
-  if (threadIdx.x == 0)
-    s_last = publish_and_arrive(p.tickets + n, p.epoch, (unsigned long long)p.g.items_per_n, p.err);
+  if (threadIdx.x == 0) s_last = publish_and_arrive(p.tickets + n, (unsigned)p.g.arrivals_per_n);
   __syncthreads();
   if (!s_last) return;
   if (kBwd)
@@ -164,15 +163,14 @@ __device__ __forceinline__ void arrive_and_finalize(const KParams& p, int64_t n,
   else
     finalize_fwd<T>(p, n, sm);
   __syncthreads();
-  if (threadIdx.x == 0) atomicExch(p.tickets + n, 0ull);
+  if (threadIdx.x == 0) atomicExch(p.tickets + n, 0u);
   if (!kBwd) return;
-  if (threadIdx.x == 0)
-    s_last = publish_and_arrive(p.tickets + p.g.N, p.epoch, (unsigned long long)p.g.N, p.err);
+  if (threadIdx.x == 0) s_last = publish_and_arrive(p.tickets + p.g.N, (unsigned)p.g.N);
   __syncthreads();
   if (!s_last) return;
   finalize_params(p);
   __syncthreads();
-  if (threadIdx.x == 0) atomicExch(p.tickets + p.g.N, 0ull);
+  if (threadIdx.x == 0) atomicExch(p.tickets + p.g.N, 0u);
 }
 
 }  // namespace gn

@@ -38,17 +38,22 @@ struct Geom {
   int64_t L;     // mode 0: chunk length (multiple of vw)
   int64_t RB;    // mode 1: rows per item
   // common
-  int64_t T;            // partial records per (n, c): row blocks (NHWC) or chunks (NCHW)
-  int64_t cstride, tstride;  // partial index = n*C*T + c*cstride + t*tstride
-  int64_t items_per_n;
+  int64_t T;     // items per (n, column block) (NHWC) or per row (NCHW)
+  int cl;        // CTAs per thread-block cluster of the first kernel (1 or 8);
+                 // a cluster = cl consecutive items that merge their partials through DSMEM
+  int64_t Tp;    // partial records per (n, c) = T / cl
+  int64_t cstride, tstride;  // partial index = n*C*Tp + c*cstride + t'*tstride
+  int64_t arrivals_per_n;    // cluster-level partials that complete sample n
+  int64_t items_per_n;       // NCHW mode 1: items per sample
   int64_t items;
+  int64_t keep_from;  // item-relative row/element index from which the first kernel
+                      // loads with the L2 evict_last policy (the part read again first)
 };
 
 // Workspace layout (byte offsets, each 256-byte aligned).
 struct WsLayout {
-  size_t tickets;  // (N + 1) ticket words (uint64): one per sample, one global
-  size_t err;      // one uint32 error word
-  size_t part;     // N*C*T float2 partial sums
+  size_t tickets;  // (N + 1) uint32 arrival counters: one per sample, one global
+  size_t part;     // N*C*Tp float2 partial sums
   size_t chst;     // N*C float2 per-channel results of the finalisation
   size_t coef;     // N*G float2 dx coefficients (backward only)
   size_t total;
@@ -66,9 +71,7 @@ struct KParams {
   float* dgamma;
   float* dbeta;
   float eps;
-  unsigned epoch;
-  unsigned long long* tickets;
-  unsigned* err;
+  unsigned* tickets;
   float2* part;
   float2* chst;
   float2* coef;
@@ -87,10 +90,11 @@ struct TimingEvents {
 };
 const TimingEvents& timing_events();
 
+// Launches the first kernel of an op (one CTA per item, clusters of g.cl CTAs).
+cudaError_t launch_first(const void* kernel, const KParams& p, size_t smem, cudaStream_t s);
+
 // kernels (gn_nhwc.cu / gn_nchw.cu): enqueue the two kernels of an op.
-cudaError_t launch_nhwc_fwd(const KParams& p, cudaStream_t s);
-cudaError_t launch_nhwc_bwd(const KParams& p, cudaStream_t s);
-cudaError_t launch_nchw_fwd(const KParams& p, cudaStream_t s);
-cudaError_t launch_nchw_bwd(const KParams& p, cudaStream_t s);
+cudaError_t launch_nhwc(const KParams& p, cudaStream_t s, bool bwd);
+cudaError_t launch_nchw(const KParams& p, cudaStream_t s, bool bwd);
 
 }  // namespace gn

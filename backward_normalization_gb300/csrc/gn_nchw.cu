@@ -3,19 +3,21 @@
 // Memory: element (n, c, hw) sits at (n*C + c)*HW + hw, so each (n, c)
 // channel plane ("row") is HW contiguous elements and a group is Cg
 // consecutive planes.  Two item shapes:
-//   mode 0 (large planes): item = (row, chunk of L elements); the whole CTA
-//          strides the chunk with 16-byte loads; one partial per item.
+//   mode 0 (large planes): item = (row, chunk of L elements), numbered
+//          row*T + chunk; the whole CTA strides the chunk with 16-byte loads.
+//          When a plane has T >= 8 chunks, 8 consecutive chunks form a
+//          thread-block cluster that merges its sums through DSMEM.
 //   mode 1 (small planes): item = RB consecutive rows of one sample; each warp
 //          takes whole rows; one partial per row.
-// The kernels mirror gn_nhwc.cu: stats/reduce kernels publish per-(n, c,
-// chunk) partial sums and the last CTA of a sample finalises it; apply/dx
-// kernels walk the items in reverse order.
+// The kernels mirror gn_nhwc.cu: stats/reduce kernels publish partial sums and
+// the last CTA of a sample finalises it; apply/dx kernels walk the items (and
+// the elements of a chunk) in reverse order.
 #include "gn_finalize.cuh"
 
 namespace gn {
 namespace {
 
-template <typename T, int VW>
+template <int VW>
 __device__ __forceinline__ void acc_shifted(const float (&v)[VW], float K, float& s, float& q) {
 #pragma unroll
   for (int k = 0; k < VW; ++k) {
@@ -25,7 +27,7 @@ __device__ __forceinline__ void acc_shifted(const float (&v)[VW], float K, float
   }
 }
 
-template <typename T, int VW>
+template <int VW>
 __device__ __forceinline__ void acc_grad(const float (&xv)[VW], const float (&dv)[VW], float mu,
                                          float& s1, float& s2) {
 #pragma unroll
@@ -35,6 +37,39 @@ __device__ __forceinline__ void acc_grad(const float (&xv)[VW], const float (&dv
   }
 }
 
+// Mode-0 tail of the first kernels: CTA sum (thread 0), cluster merge, publish.
+// Returns false in the CTAs that do not publish (cluster ranks other than 0).
+__device__ __forceinline__ bool publish_chunk(const KParams& p, int64_t row, int64_t ch, float a,
+                                              float b, float* sm) {
+  const Geom& g = p.g;
+  const float2 tot = block_sum2_t0(a, b, sm);
+  if (g.cl > 1) {
+    if (threadIdx.x == 0) {
+      sm[0] = tot.x;
+      sm[1] = tot.y;
+    }
+    cluster_sum_to_rank0<2>(sm, 1, 0, threadIdx.x == 0);
+    if (cluster_rank() != 0) return false;
+    if (threadIdx.x == 0) p.part[row * g.Tp + ch / g.cl] = make_float2(sm[0], sm[1]);
+  } else if (threadIdx.x == 0) {
+    p.part[row * g.Tp + ch] = tot;
+  }
+  return true;
+}
+
+struct Chunk {
+  int64_t row, ch, h0, h1;
+};
+
+__device__ __forceinline__ Chunk chunk_of(const Geom& g, int64_t item) {
+  Chunk c;
+  c.row = item / g.T;
+  c.ch = item % g.T;
+  c.h0 = c.ch * g.L;
+  c.h1 = (c.h0 + g.L < g.HW) ? c.h0 + g.L : g.HW;  // may be <= h0: empty chunk
+  return c;
+}
+
 // ------------------------------------------------------------------ forward
 template <typename T, int VW>
 __global__ void __launch_bounds__(512) nchw_fwd_stats(const __grid_constant__ KParams p) {
@@ -42,39 +77,38 @@ __global__ void __launch_bounds__(512) nchw_fwd_stats(const __grid_constant__ KP
   const Geom& g = p.g;
   const int tid = threadIdx.x;
   const T* x = static_cast<const T*>(p.x);
-  const uint64_t pol = policy_evict_last();
+  const uint64_t pfirst = policy_evict_first(), plast = policy_evict_last();
   int64_t n;
   if (g.mode == 0) {
-    const int64_t item = blockIdx.x;
-    const int64_t row = item / g.T, ch = item % g.T;
-    n = row / g.C;
-    const T* xr = x + row * g.HW;
-    const int64_t h0 = ch * g.L;
-    const int64_t h1 = (h0 + g.L < g.HW) ? h0 + g.L : g.HW;
+    const Chunk k = chunk_of(g, blockIdx.x);
+    n = k.row / g.C;
+    const T* xr = x + k.row * g.HW;
     const float K = Elem<T>::to_f(xr[0]);
+    const int64_t keep = k.h0 + g.keep_from;
     float s = 0.f, q = 0.f;
     const int64_t st = (int64_t)blockDim.x * VW;
-    int64_t h = h0 + (int64_t)tid * VW;
-    for (; h + 3 * st < h1; h += 4 * st) {
+    int64_t h = k.h0 + (int64_t)tid * VW;
+    for (; h + 3 * st < k.h1; h += 4 * st) {
+      const uint64_t pol = h >= keep ? plast : pfirst;
       float v[4][VW];
 #pragma unroll
       for (int u = 0; u < 4; ++u) Access<T, VW>::load(xr + h + u * st, v[u], pol);
 #pragma unroll
-      for (int u = 0; u < 4; ++u) acc_shifted<T, VW>(v[u], K, s, q);
+      for (int u = 0; u < 4; ++u) acc_shifted<VW>(v[u], K, s, q);
     }
-    for (; h < h1; h += st) {
+    for (; h < k.h1; h += st) {
       float v[VW];
-      Access<T, VW>::load(xr + h, v, pol);
-      acc_shifted<T, VW>(v, K, s, q);
+      Access<T, VW>::load(xr + h, v, h >= keep ? plast : pfirst);
+      acc_shifted<VW>(v, K, s, q);
     }
-    const float2 tot = block_sum2_t0(s, q, sm);
-    if (tid == 0) p.part[row * g.T + ch] = tot;
+    if (!publish_chunk(p, k.row, k.ch, s, q, sm)) return;
   } else {
     const int64_t item = blockIdx.x;
     n = item / g.items_per_n;
     const int64_t c0 = (item % g.items_per_n) * g.RB;
     const int64_t c1 = (c0 + g.RB < g.C) ? c0 + g.RB : g.C;
     const int lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+    const uint64_t pol = g.keep_from == 0 ? plast : pfirst;
     for (int64_t c = c0 + warp; c < c1; c += nwarps) {
       const int64_t row = n * g.C + c;
       const T* xr = x + row * g.HW;
@@ -83,7 +117,7 @@ __global__ void __launch_bounds__(512) nchw_fwd_stats(const __grid_constant__ KP
       for (int64_t h = (int64_t)lane * VW; h < g.HW; h += 32 * VW) {
         float v[VW];
         Access<T, VW>::load(xr + h, v, pol);
-        acc_shifted<T, VW>(v, K, s, q);
+        acc_shifted<VW>(v, K, s, q);
       }
       s = warp_sum_lane0(s);
       q = warp_sum_lane0(q);
@@ -102,35 +136,34 @@ __global__ void __launch_bounds__(512) nchw_fwd_apply(const __grid_constant__ KP
   const uint64_t pol = policy_evict_first();
   const int64_t item = g.items - 1 - (int64_t)blockIdx.x;
   if (g.mode == 0) {
-    const int64_t row = item / g.T, ch = item % g.T;
-    const int64_t n = row / g.C, c = row % g.C, ng = n * g.G + c / g.Cg;
+    const Chunk k = chunk_of(g, item);
+    if (k.h0 >= k.h1) return;
+    const int64_t n = k.row / g.C, c = k.row % g.C, ng = n * g.G + c / g.Cg;
     const float r = __ldg(p.rstd + ng), mu = __ldg(p.mean + ng);
     const float a = p.gamma ? r * __ldg(p.gamma + c) : r;
     const float b = p.beta ? __ldg(p.beta + c) : 0.f;
-    const T* xr = x + row * g.HW;
-    T* yr = y + row * g.HW;
-    const int64_t h0 = ch * g.L;
-    const int64_t h1 = (h0 + g.L < g.HW) ? h0 + g.L : g.HW;
-    const int64_t nv = (h1 - h0) / VW;
+    const T* xr = x + k.row * g.HW + k.h0;
+    T* yr = y + k.row * g.HW + k.h0;
+    const int64_t nv = (k.h1 - k.h0) / VW;
     const int64_t st = blockDim.x;
-    int64_t k = nv - 1 - tid;
-    for (; k - 3 * st >= 0; k -= 4 * st) {
+    int64_t i = nv - 1 - tid;
+    for (; i - 3 * st >= 0; i -= 4 * st) {
       float v[4][VW];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) Access<T, VW>::load(xr + h0 + (k - u * st) * VW, v[u], pol);
+      for (int u = 0; u < 4; ++u) Access<T, VW>::load(xr + (i - u * st) * VW, v[u], pol);
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
 #pragma unroll
         for (int e = 0; e < VW; ++e) v[u][e] = fmaf(v[u][e] - mu, a, b);
-        Access<T, VW>::store(yr + h0 + (k - u * st) * VW, v[u], pol);
+        Access<T, VW>::store(yr + (i - u * st) * VW, v[u], pol);
       }
     }
-    for (; k >= 0; k -= st) {
+    for (; i >= 0; i -= st) {
       float v[VW];
-      Access<T, VW>::load(xr + h0 + k * VW, v, pol);
+      Access<T, VW>::load(xr + i * VW, v, pol);
 #pragma unroll
       for (int e = 0; e < VW; ++e) v[e] = fmaf(v[e] - mu, a, b);
-      Access<T, VW>::store(yr + h0 + k * VW, v, pol);
+      Access<T, VW>::store(yr + i * VW, v, pol);
     }
   } else {
     const int64_t n = item / g.items_per_n;
@@ -163,21 +196,20 @@ __global__ void __launch_bounds__(512) nchw_bwd_reduce(const __grid_constant__ K
   const int tid = threadIdx.x;
   const T* x = static_cast<const T*>(p.x);
   const T* dy = static_cast<const T*>(p.dy);
-  const uint64_t pol = policy_evict_last();
+  const uint64_t pfirst = policy_evict_first(), plast = policy_evict_last();
   int64_t n;
   if (g.mode == 0) {
-    const int64_t item = blockIdx.x;
-    const int64_t row = item / g.T, ch = item % g.T;
-    n = row / g.C;
-    const float mu = __ldg(p.mean + n * g.G + (row % g.C) / g.Cg);
-    const T* xr = x + row * g.HW;
-    const T* dr = dy + row * g.HW;
-    const int64_t h0 = ch * g.L;
-    const int64_t h1 = (h0 + g.L < g.HW) ? h0 + g.L : g.HW;
+    const Chunk k = chunk_of(g, blockIdx.x);
+    n = k.row / g.C;
+    const float mu = __ldg(p.mean + n * g.G + (k.row % g.C) / g.Cg);
+    const T* xr = x + k.row * g.HW;
+    const T* dr = dy + k.row * g.HW;
+    const int64_t keep = k.h0 + g.keep_from;
     float s1 = 0.f, s2 = 0.f;
     const int64_t st = (int64_t)blockDim.x * VW;
-    int64_t h = h0 + (int64_t)tid * VW;
-    for (; h + st < h1; h += 2 * st) {
+    int64_t h = k.h0 + (int64_t)tid * VW;
+    for (; h + st < k.h1; h += 2 * st) {
+      const uint64_t pol = h >= keep ? plast : pfirst;
       float xv[2][VW], dv[2][VW];
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
@@ -185,22 +217,23 @@ __global__ void __launch_bounds__(512) nchw_bwd_reduce(const __grid_constant__ K
         Access<T, VW>::load(dr + h + u * st, dv[u], pol);
       }
 #pragma unroll
-      for (int u = 0; u < 2; ++u) acc_grad<T, VW>(xv[u], dv[u], mu, s1, s2);
+      for (int u = 0; u < 2; ++u) acc_grad<VW>(xv[u], dv[u], mu, s1, s2);
     }
-    for (; h < h1; h += st) {
+    for (; h < k.h1; h += st) {
+      const uint64_t pol = h >= keep ? plast : pfirst;
       float xv[VW], dv[VW];
       Access<T, VW>::load(xr + h, xv, pol);
       Access<T, VW>::load(dr + h, dv, pol);
-      acc_grad<T, VW>(xv, dv, mu, s1, s2);
+      acc_grad<VW>(xv, dv, mu, s1, s2);
     }
-    const float2 tot = block_sum2_t0(s1, s2, sm);
-    if (tid == 0) p.part[row * g.T + ch] = tot;
+    if (!publish_chunk(p, k.row, k.ch, s1, s2, sm)) return;
   } else {
     const int64_t item = blockIdx.x;
     n = item / g.items_per_n;
     const int64_t c0 = (item % g.items_per_n) * g.RB;
     const int64_t c1 = (c0 + g.RB < g.C) ? c0 + g.RB : g.C;
     const int lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+    const uint64_t pol = g.keep_from == 0 ? plast : pfirst;
     for (int64_t c = c0 + warp; c < c1; c += nwarps) {
       const int64_t row = n * g.C + c;
       const float mu = __ldg(p.mean + n * g.G + c / g.Cg);
@@ -211,7 +244,7 @@ __global__ void __launch_bounds__(512) nchw_bwd_reduce(const __grid_constant__ K
         float xv[VW], dv[VW];
         Access<T, VW>::load(xr + h, xv, pol);
         Access<T, VW>::load(dr + h, dv, pol);
-        acc_grad<T, VW>(xv, dv, mu, s1, s2);
+        acc_grad<VW>(xv, dv, mu, s1, s2);
       }
       s1 = warp_sum_lane0(s1);
       s2 = warp_sum_lane0(s2);
@@ -231,40 +264,39 @@ __global__ void __launch_bounds__(512) nchw_bwd_dx(const __grid_constant__ KPara
   const uint64_t pol = policy_evict_first();
   const int64_t item = g.items - 1 - (int64_t)blockIdx.x;
   if (g.mode == 0) {
-    const int64_t row = item / g.T, ch = item % g.T;
-    const int64_t n = row / g.C, c = row % g.C, ng = n * g.G + c / g.Cg;
+    const Chunk k = chunk_of(g, item);
+    if (k.h0 >= k.h1) return;
+    const int64_t n = k.row / g.C, c = k.row % g.C, ng = n * g.G + c / g.Cg;
     const float r = __ldg(p.rstd + ng), mu = __ldg(p.mean + ng);
     const float A = p.gamma ? r * __ldg(p.gamma + c) : r;
     const float2 cf = __ldcg(p.coef + ng);
-    const T* xr = x + row * g.HW;
-    const T* dr = dy + row * g.HW;
-    T* outr = dx + row * g.HW;
-    const int64_t h0 = ch * g.L;
-    const int64_t h1 = (h0 + g.L < g.HW) ? h0 + g.L : g.HW;
-    const int64_t nv = (h1 - h0) / VW;
+    const T* xr = x + k.row * g.HW + k.h0;
+    const T* dr = dy + k.row * g.HW + k.h0;
+    T* outr = dx + k.row * g.HW + k.h0;
+    const int64_t nv = (k.h1 - k.h0) / VW;
     const int64_t st = blockDim.x;
-    int64_t k = nv - 1 - tid;
-    for (; k - st >= 0; k -= 2 * st) {
+    int64_t i = nv - 1 - tid;
+    for (; i - st >= 0; i -= 2 * st) {
       float xv[2][VW], dv[2][VW];
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
-        Access<T, VW>::load(xr + h0 + (k - u * st) * VW, xv[u], pol);
-        Access<T, VW>::load(dr + h0 + (k - u * st) * VW, dv[u], pol);
+        Access<T, VW>::load(xr + (i - u * st) * VW, xv[u], pol);
+        Access<T, VW>::load(dr + (i - u * st) * VW, dv[u], pol);
       }
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
 #pragma unroll
         for (int e = 0; e < VW; ++e) xv[u][e] = fmaf(A, dv[u][e], fmaf(cf.x, xv[u][e] - mu, cf.y));
-        Access<T, VW>::store(outr + h0 + (k - u * st) * VW, xv[u], pol);
+        Access<T, VW>::store(outr + (i - u * st) * VW, xv[u], pol);
       }
     }
-    for (; k >= 0; k -= st) {
+    for (; i >= 0; i -= st) {
       float xv[VW], dv[VW];
-      Access<T, VW>::load(xr + h0 + k * VW, xv, pol);
-      Access<T, VW>::load(dr + h0 + k * VW, dv, pol);
+      Access<T, VW>::load(xr + i * VW, xv, pol);
+      Access<T, VW>::load(dr + i * VW, dv, pol);
 #pragma unroll
       for (int e = 0; e < VW; ++e) xv[e] = fmaf(A, dv[e], fmaf(cf.x, xv[e] - mu, cf.y));
-      Access<T, VW>::store(outr + h0 + k * VW, xv, pol);
+      Access<T, VW>::store(outr + i * VW, xv, pol);
     }
   } else {
     const int64_t n = item / g.items_per_n;
@@ -292,61 +324,36 @@ __global__ void __launch_bounds__(512) nchw_bwd_dx(const __grid_constant__ KPara
 }
 
 template <typename T, int VW>
-cudaError_t fwd_t(const KParams& p, cudaStream_t s) {
+cudaError_t run_op(const KParams& p, cudaStream_t s, bool bwd) {
   const Geom& g = p.g;
   const size_t sm1 = sizeof(float) * 2 * g.tpb;
   const TimingEvents& ev = timing_events();
   if (ev.begin) cudaEventRecord(ev.begin, s);
-  nchw_fwd_stats<T, VW><<<(unsigned)g.items, g.tpb, sm1, s>>>(p);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_first(bwd ? (const void*)nchw_bwd_reduce<T, VW> : (const void*)nchw_fwd_stats<T, VW>,
+                               p, sm1, s);
   if (e != cudaSuccess) return e;
   if (ev.mid) cudaEventRecord(ev.mid, s);
-  nchw_fwd_apply<T, VW><<<(unsigned)g.items, g.tpb, 0, s>>>(p);
-  e = cudaGetLastError();
-  if (ev.end) cudaEventRecord(ev.end, s);
-  return e;
-}
-
-template <typename T, int VW>
-cudaError_t bwd_t(const KParams& p, cudaStream_t s) {
-  const Geom& g = p.g;
-  const size_t sm1 = sizeof(float) * 2 * g.tpb;
-  const TimingEvents& ev = timing_events();
-  if (ev.begin) cudaEventRecord(ev.begin, s);
-  nchw_bwd_reduce<T, VW><<<(unsigned)g.items, g.tpb, sm1, s>>>(p);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  if (ev.mid) cudaEventRecord(ev.mid, s);
-  nchw_bwd_dx<T, VW><<<(unsigned)g.items, g.tpb, 0, s>>>(p);
+  if (bwd)
+    nchw_bwd_dx<T, VW><<<(unsigned)g.items, g.tpb, 0, s>>>(p);
+  else
+    nchw_fwd_apply<T, VW><<<(unsigned)g.items, g.tpb, 0, s>>>(p);
   e = cudaGetLastError();
   if (ev.end) cudaEventRecord(ev.end, s);
   return e;
 }
 
 template <typename T>
-cudaError_t fwd_dispatch_vw(const KParams& p, cudaStream_t s) {
-  return p.g.vw == 1 ? fwd_t<T, 1>(p, s) : fwd_t<T, Elem<T>::VEC>(p, s);
-}
-template <typename T>
-cudaError_t bwd_dispatch_vw(const KParams& p, cudaStream_t s) {
-  return p.g.vw == 1 ? bwd_t<T, 1>(p, s) : bwd_t<T, Elem<T>::VEC>(p, s);
+cudaError_t dispatch_vw(const KParams& p, cudaStream_t s, bool bwd) {
+  return p.g.vw == 1 ? run_op<T, 1>(p, s, bwd) : run_op<T, Elem<T>::VEC>(p, s, bwd);
 }
 
 }  // namespace
 
-cudaError_t launch_nchw_fwd(const KParams& p, cudaStream_t s) {
+cudaError_t launch_nchw(const KParams& p, cudaStream_t s, bool bwd) {
   switch (p.g.dtype) {
-    case kF32: return fwd_dispatch_vw<float>(p, s);
-    case kF16: return fwd_dispatch_vw<__half>(p, s);
-    default: return fwd_dispatch_vw<__nv_bfloat16>(p, s);
-  }
-}
-
-cudaError_t launch_nchw_bwd(const KParams& p, cudaStream_t s) {
-  switch (p.g.dtype) {
-    case kF32: return bwd_dispatch_vw<float>(p, s);
-    case kF16: return bwd_dispatch_vw<__half>(p, s);
-    default: return bwd_dispatch_vw<__nv_bfloat16>(p, s);
+    case kF32: return dispatch_vw<float>(p, s, bwd);
+    case kF16: return dispatch_vw<__half>(p, s, bwd);
+    default: return dispatch_vw<__nv_bfloat16>(p, s, bwd);
   }
 }
 

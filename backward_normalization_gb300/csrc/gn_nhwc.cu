@@ -2,19 +2,23 @@
 //
 // Memory: element (n, c, hw) sits at (n*HW + hw)*C + c, so one spatial
 // position ("row") holds the C channels contiguously and a group is a run of
-// Cg channels inside every row.  A CTA owns an item = (sample n, block of rb
-// consecutive rows, block of Wv column vectors); each thread owns one column
-// of vw channels (one 16-byte vector) and walks the item's rows with stride
-// rpi, so every warp issues fully coalesced 16-byte loads and each thread's
-// channels (and their group constants) never change.
+// Cg channels inside every row.  A CTA owns an item = (sample n, column block
+// cb, block t of rb consecutive rows); each thread owns one column of vw
+// channels (one 16-byte vector) and walks the item's rows with stride rpi, so
+// every warp issues fully coalesced 16-byte loads and each thread's channels
+// (and their group constants) never change.  Items are numbered
+// ((n*ncb + cb)*T + t), so the cl CTAs of a thread-block cluster hold cl
+// consecutive row blocks of the same (n, cb).
 //
-// Forward : nhwc_fwd_stats  -> per-(item, channel) shifted sums, last CTA of a
-//                              sample merges them into mean/rstd per group
+// Forward : nhwc_fwd_stats  -> per-(cluster, channel) shifted sums; the last
+//                              cluster of a sample merges them into mean/rstd
 //           nhwc_fwd_apply  -> y = (x - mean) * rstd*gamma + beta
-// Backward: nhwc_bwd_reduce -> per-(item, channel) sum(dy), sum(dy*(x-mean)),
-//                              last CTA of a sample forms the dx
-//                              coefficients, last sample forms dgamma/dbeta
+// Backward: nhwc_bwd_reduce -> per-(cluster, channel) sum(dy), sum(dy*(x-mean));
+//                              the last cluster of a sample forms the dx
+//                              coefficients, the last sample dgamma/dbeta
 //           nhwc_bwd_dx     -> dx = rstd*gamma*dy + B*(x - mean) + D
+// The second kernel of each op walks items and rows in the reverse order of
+// the first, so it starts on the data the first kernel left in L2.
 #include "gn_finalize.cuh"
 
 namespace gn {
@@ -31,14 +35,14 @@ __device__ __forceinline__ NhwcItem nhwc_item(const Geom& g, int64_t item) {
   const int tid = threadIdx.x;
   it.j = tid % g.Wv;
   it.r = tid / g.Wv;
-  const int cb = (int)(item % g.ncb);
-  item /= g.ncb;
   it.t = item % g.T;
-  it.n = item / g.T;
+  item /= g.T;
+  const int cb = (int)(item % g.ncb);
+  it.n = item / g.ncb;
   it.col = (int64_t)cb * g.Wv + it.j;
   it.active = (it.r < g.rpi) && (it.col < g.V);
   it.row0 = it.t * g.rb;
-  it.row1 = (it.row0 + g.rb < g.HW) ? it.row0 + g.rb : g.HW;
+  it.row1 = (it.row0 + g.rb < g.HW) ? it.row0 + g.rb : g.HW;  // may be <= row0: empty item
   return it;
 }
 
@@ -52,12 +56,33 @@ __device__ __forceinline__ void reduce_row_lanes(const Geom& g, float* red, cons
   for (int q = 0; q < NQ; ++q) red[q * tpb + tid] = v[q];
   __syncthreads();
   for (int s = 1; s < g.rpi; s <<= 1) {
-    if (r < g.rpi && (r % (2 * s)) == 0 && r + s < g.rpi) {
+    if ((r % (2 * s)) == 0 && r + s < g.rpi) {
 #pragma unroll
       for (int q = 0; q < NQ; ++q) red[q * tpb + tid] += red[q * tpb + tid + s * g.Wv];
     }
     __syncthreads();
   }
+}
+
+// Shared tail of the two first kernels: CTA tree, cluster merge, publish the
+// cluster partial, arrive.
+template <typename T, int VW, bool kBwd>
+__device__ __forceinline__ void publish_nhwc(const KParams& p, const NhwcItem& it, float* red,
+                                             const float (&acc)[2 * VW]) {
+  const Geom& g = p.g;
+  reduce_row_lanes<2 * VW>(g, red, acc, it.r);
+  if (g.cl > 1) {
+    cluster_sum_to_rank0<2 * VW>(red, blockDim.x, threadIdx.x, it.r == 0 && it.active);
+    if (cluster_rank() != 0) return;
+  }
+  if (it.r == 0 && it.active) {
+    float2* out = p.part + it.n * g.C * g.Tp + (it.t / g.cl) * g.C + it.col * VW;
+#pragma unroll
+    for (int k = 0; k < VW; ++k)
+      out[k] = make_float2(red[(2 * k) * blockDim.x + threadIdx.x],
+                           red[(2 * k + 1) * blockDim.x + threadIdx.x]);
+  }
+  arrive_and_finalize<T, kBwd>(p, it.n, red);
 }
 
 template <typename T, int VW>
@@ -68,14 +93,16 @@ __global__ void __launch_bounds__(512) nhwc_fwd_stats(const __grid_constant__ KP
   float acc[2 * VW];
 #pragma unroll
   for (int q = 0; q < 2 * VW; ++q) acc[q] = 0.f;
-  if (it.active) {
+  if (it.active && it.row0 < it.row1) {
     const T* xn = static_cast<const T*>(p.x) + it.n * g.HW * g.C + it.col * VW;
-    const uint64_t pol = policy_evict_last();
+    const uint64_t pfirst = policy_evict_first(), plast = policy_evict_last();
+    const int64_t keep = it.row0 + g.keep_from;  // rows from here on are read again first
     float K[VW];
-    Access<T, VW>::load(xn, K, pol);  // row 0 of the sample: the per-channel shift
+    Access<T, VW>::load(xn, K, pfirst);  // row 0 of the sample: the per-channel shift
     const int64_t step = g.rpi;
     int64_t row = it.row0 + it.r;
     for (; row + 3 * step < it.row1; row += 4 * step) {
+      const uint64_t pol = row >= keep ? plast : pfirst;
       float v[4][VW];
 #pragma unroll
       for (int u = 0; u < 4; ++u) Access<T, VW>::load(xn + (row + u * step) * g.C, v[u], pol);
@@ -90,7 +117,7 @@ __global__ void __launch_bounds__(512) nhwc_fwd_stats(const __grid_constant__ KP
     }
     for (; row < it.row1; row += step) {
       float v[VW];
-      Access<T, VW>::load(xn + row * g.C, v, pol);
+      Access<T, VW>::load(xn + row * g.C, v, row >= keep ? plast : pfirst);
 #pragma unroll
       for (int k = 0; k < VW; ++k) {
         const float d = v[k] - K[k];
@@ -99,15 +126,7 @@ __global__ void __launch_bounds__(512) nhwc_fwd_stats(const __grid_constant__ KP
       }
     }
   }
-  reduce_row_lanes<2 * VW>(g, red, acc, it.r);
-  if (it.r == 0 && it.active) {
-    float2* out = p.part + it.n * g.C * g.T + it.t * g.C + it.col * VW;
-#pragma unroll
-    for (int k = 0; k < VW; ++k)
-      out[k] = make_float2(red[(2 * k) * blockDim.x + threadIdx.x],
-                           red[(2 * k + 1) * blockDim.x + threadIdx.x]);
-  }
-  arrive_and_finalize<T, false>(p, it.n, red);
+  publish_nhwc<T, VW, false>(p, it, red, acc);
 }
 
 template <typename T, int VW>
@@ -115,6 +134,8 @@ __global__ void __launch_bounds__(512) nhwc_fwd_apply(const __grid_constant__ KP
   const Geom& g = p.g;
   const NhwcItem it = nhwc_item(g, g.items - 1 - (int64_t)blockIdx.x);
   if (!it.active) return;
+  const int64_t cnt = it.row1 - it.row0 - it.r;  // rows of this lane: r, r+step, ...
+  if (cnt <= 0) return;
   float a[VW], mu[VW], b[VW];
 #pragma unroll
   for (int k = 0; k < VW; ++k) {
@@ -128,29 +149,26 @@ __global__ void __launch_bounds__(512) nhwc_fwd_apply(const __grid_constant__ KP
   const int64_t off = it.n * g.HW * g.C + it.col * VW;
   const T* xn = static_cast<const T*>(p.x) + off;
   T* yn = static_cast<T*>(p.out) + off;
-  const uint64_t pin = policy_evict_first();
-  const uint64_t pout = policy_evict_first();
+  const uint64_t pol = policy_evict_first();
   const int64_t step = g.rpi;
-  const int64_t cnt = it.row1 - it.row0 - it.r;  // rows of this lane: r, r+step, ...
-  if (cnt <= 0) return;
   int64_t row = it.row0 + it.r + ((cnt - 1) / step) * step;  // last row of the lane
   for (; row - 3 * step >= it.row0; row -= 4 * step) {
     float v[4][VW];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) Access<T, VW>::load(xn + (row - u * step) * g.C, v[u], pin);
+    for (int u = 0; u < 4; ++u) Access<T, VW>::load(xn + (row - u * step) * g.C, v[u], pol);
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
 #pragma unroll
       for (int k = 0; k < VW; ++k) v[u][k] = fmaf(v[u][k] - mu[k], a[k], b[k]);
-      Access<T, VW>::store(yn + (row - u * step) * g.C, v[u], pout);
+      Access<T, VW>::store(yn + (row - u * step) * g.C, v[u], pol);
     }
   }
   for (; row >= it.row0; row -= step) {
     float v[VW];
-    Access<T, VW>::load(xn + row * g.C, v, pin);
+    Access<T, VW>::load(xn + row * g.C, v, pol);
 #pragma unroll
     for (int k = 0; k < VW; ++k) v[k] = fmaf(v[k] - mu[k], a[k], b[k]);
-    Access<T, VW>::store(yn + row * g.C, v, pout);
+    Access<T, VW>::store(yn + row * g.C, v, pol);
   }
 }
 
@@ -162,17 +180,19 @@ __global__ void __launch_bounds__(512) nhwc_bwd_reduce(const __grid_constant__ K
   float acc[2 * VW];
 #pragma unroll
   for (int q = 0; q < 2 * VW; ++q) acc[q] = 0.f;
-  if (it.active) {
+  if (it.active && it.row0 < it.row1) {
     float mu[VW];
 #pragma unroll
     for (int k = 0; k < VW; ++k) mu[k] = __ldg(p.mean + it.n * g.G + (it.col * VW + k) / g.Cg);
     const int64_t off = it.n * g.HW * g.C + it.col * VW;
     const T* xn = static_cast<const T*>(p.x) + off;
     const T* dyn = static_cast<const T*>(p.dy) + off;
-    const uint64_t pol = policy_evict_last();
+    const uint64_t pfirst = policy_evict_first(), plast = policy_evict_last();
+    const int64_t keep = it.row0 + g.keep_from;
     const int64_t step = g.rpi;
     int64_t row = it.row0 + it.r;
     for (; row + step < it.row1; row += 2 * step) {
+      const uint64_t pol = row >= keep ? plast : pfirst;
       float xv[2][VW], dv[2][VW];
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
@@ -188,6 +208,7 @@ __global__ void __launch_bounds__(512) nhwc_bwd_reduce(const __grid_constant__ K
         }
     }
     for (; row < it.row1; row += step) {
+      const uint64_t pol = row >= keep ? plast : pfirst;
       float xv[VW], dv[VW];
       Access<T, VW>::load(xn + row * g.C, xv, pol);
       Access<T, VW>::load(dyn + row * g.C, dv, pol);
@@ -198,15 +219,7 @@ __global__ void __launch_bounds__(512) nhwc_bwd_reduce(const __grid_constant__ K
       }
     }
   }
-  reduce_row_lanes<2 * VW>(g, red, acc, it.r);
-  if (it.r == 0 && it.active) {
-    float2* out = p.part + it.n * g.C * g.T + it.t * g.C + it.col * VW;
-#pragma unroll
-    for (int k = 0; k < VW; ++k)
-      out[k] = make_float2(red[(2 * k) * blockDim.x + threadIdx.x],
-                           red[(2 * k + 1) * blockDim.x + threadIdx.x]);
-  }
-  arrive_and_finalize<T, true>(p, it.n, red);
+  publish_nhwc<T, VW, true>(p, it, red, acc);
 }
 
 template <typename T, int VW>
@@ -214,6 +227,8 @@ __global__ void __launch_bounds__(512) nhwc_bwd_dx(const __grid_constant__ KPara
   const Geom& g = p.g;
   const NhwcItem it = nhwc_item(g, g.items - 1 - (int64_t)blockIdx.x);
   if (!it.active) return;
+  const int64_t cnt = it.row1 - it.row0 - it.r;
+  if (cnt <= 0) return;
   float A[VW], mu[VW], B[VW], D[VW];
 #pragma unroll
   for (int k = 0; k < VW; ++k) {
@@ -230,91 +245,64 @@ __global__ void __launch_bounds__(512) nhwc_bwd_dx(const __grid_constant__ KPara
   const T* xn = static_cast<const T*>(p.x) + off;
   const T* dyn = static_cast<const T*>(p.dy) + off;
   T* dxn = static_cast<T*>(p.out) + off;
-  const uint64_t pin = policy_evict_first();
+  const uint64_t pol = policy_evict_first();
   const int64_t step = g.rpi;
-  const int64_t cnt = it.row1 - it.row0 - it.r;
-  if (cnt <= 0) return;
   int64_t row = it.row0 + it.r + ((cnt - 1) / step) * step;
   for (; row - step >= it.row0; row -= 2 * step) {
     float xv[2][VW], dv[2][VW];
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
-      Access<T, VW>::load(xn + (row - u * step) * g.C, xv[u], pin);
-      Access<T, VW>::load(dyn + (row - u * step) * g.C, dv[u], pin);
+      Access<T, VW>::load(xn + (row - u * step) * g.C, xv[u], pol);
+      Access<T, VW>::load(dyn + (row - u * step) * g.C, dv[u], pol);
     }
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
 #pragma unroll
       for (int k = 0; k < VW; ++k) xv[u][k] = fmaf(A[k], dv[u][k], fmaf(B[k], xv[u][k] - mu[k], D[k]));
-      Access<T, VW>::store(dxn + (row - u * step) * g.C, xv[u], pin);
+      Access<T, VW>::store(dxn + (row - u * step) * g.C, xv[u], pol);
     }
   }
   for (; row >= it.row0; row -= step) {
     float xv[VW], dv[VW];
-    Access<T, VW>::load(xn + row * g.C, xv, pin);
-    Access<T, VW>::load(dyn + row * g.C, dv, pin);
+    Access<T, VW>::load(xn + row * g.C, xv, pol);
+    Access<T, VW>::load(dyn + row * g.C, dv, pol);
 #pragma unroll
     for (int k = 0; k < VW; ++k) xv[k] = fmaf(A[k], dv[k], fmaf(B[k], xv[k] - mu[k], D[k]));
-    Access<T, VW>::store(dxn + row * g.C, xv, pin);
+    Access<T, VW>::store(dxn + row * g.C, xv, pol);
   }
 }
 
 template <typename T, int VW>
-cudaError_t fwd_t(const KParams& p, cudaStream_t s) {
+cudaError_t run_op(const KParams& p, cudaStream_t s, bool bwd) {
   const Geom& g = p.g;
   const size_t sm1 = sizeof(float) * 2 * VW * g.tpb;
   const TimingEvents& ev = timing_events();
   if (ev.begin) cudaEventRecord(ev.begin, s);
-  nhwc_fwd_stats<T, VW><<<(unsigned)g.items, g.tpb, sm1, s>>>(p);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_first(bwd ? (const void*)nhwc_bwd_reduce<T, VW> : (const void*)nhwc_fwd_stats<T, VW>,
+                               p, sm1, s);
   if (e != cudaSuccess) return e;
   if (ev.mid) cudaEventRecord(ev.mid, s);
-  nhwc_fwd_apply<T, VW><<<(unsigned)g.items, g.tpb, 0, s>>>(p);
-  e = cudaGetLastError();
-  if (ev.end) cudaEventRecord(ev.end, s);
-  return e;
-}
-
-template <typename T, int VW>
-cudaError_t bwd_t(const KParams& p, cudaStream_t s) {
-  const Geom& g = p.g;
-  const size_t sm1 = sizeof(float) * 2 * VW * g.tpb;
-  const TimingEvents& ev = timing_events();
-  if (ev.begin) cudaEventRecord(ev.begin, s);
-  nhwc_bwd_reduce<T, VW><<<(unsigned)g.items, g.tpb, sm1, s>>>(p);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  if (ev.mid) cudaEventRecord(ev.mid, s);
-  nhwc_bwd_dx<T, VW><<<(unsigned)g.items, g.tpb, 0, s>>>(p);
+  if (bwd)
+    nhwc_bwd_dx<T, VW><<<(unsigned)g.items, g.tpb, 0, s>>>(p);
+  else
+    nhwc_fwd_apply<T, VW><<<(unsigned)g.items, g.tpb, 0, s>>>(p);
   e = cudaGetLastError();
   if (ev.end) cudaEventRecord(ev.end, s);
   return e;
 }
 
 template <typename T>
-cudaError_t fwd_dispatch_vw(const KParams& p, cudaStream_t s) {
-  return p.g.vw == 1 ? fwd_t<T, 1>(p, s) : fwd_t<T, Elem<T>::VEC>(p, s);
-}
-template <typename T>
-cudaError_t bwd_dispatch_vw(const KParams& p, cudaStream_t s) {
-  return p.g.vw == 1 ? bwd_t<T, 1>(p, s) : bwd_t<T, Elem<T>::VEC>(p, s);
+cudaError_t dispatch_vw(const KParams& p, cudaStream_t s, bool bwd) {
+  return p.g.vw == 1 ? run_op<T, 1>(p, s, bwd) : run_op<T, Elem<T>::VEC>(p, s, bwd);
 }
 
 }  // namespace
 
-cudaError_t launch_nhwc_fwd(const KParams& p, cudaStream_t s) {
+cudaError_t launch_nhwc(const KParams& p, cudaStream_t s, bool bwd) {
   switch (p.g.dtype) {
-    case kF32: return fwd_dispatch_vw<float>(p, s);
-    case kF16: return fwd_dispatch_vw<__half>(p, s);
-    default: return fwd_dispatch_vw<__nv_bfloat16>(p, s);
-  }
-}
-
-cudaError_t launch_nhwc_bwd(const KParams& p, cudaStream_t s) {
-  switch (p.g.dtype) {
-    case kF32: return bwd_dispatch_vw<float>(p, s);
-    case kF16: return bwd_dispatch_vw<__half>(p, s);
-    default: return bwd_dispatch_vw<__nv_bfloat16>(p, s);
+    case kF32: return dispatch_vw<float>(p, s, bwd);
+    case kF16: return dispatch_vw<__half>(p, s, bwd);
+    default: return dispatch_vw<__nv_bfloat16>(p, s, bwd);
   }
 }
 

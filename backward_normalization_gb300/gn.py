@@ -138,8 +138,9 @@ def set_timing_events(ev_begin=None, ev_mid=None, ev_end=None) -> None:
 
 
 def alloc_workspace(op, N, C, HW, G, layout, dtype, device="cuda"):
+    """A zero-filled workspace (the library requires zeros before first use)."""
     n = workspace_size(op, N, C, HW, G, layout, dtype)
-    return torch.empty(max(n, 16), dtype=torch.uint8, device=device)
+    return torch.zeros(max(n, 16), dtype=torch.uint8, device=device)
 
 
 def forward(x, N, C, HW, G, layout, gamma=None, beta=None, eps=1e-5, workspace=None,

@@ -36,9 +36,12 @@
  * for the same arguments on the same device.
  *
  * Workspace: a caller-provided device buffer of at least gn_workspace_size()
- * bytes, 16-byte aligned.  Its contents on entry are ignored and on return are
- * unspecified (no zero-fill is needed).  Two calls that are in flight at the
- * same time must not share one workspace.
+ * bytes, 16-byte aligned, ZERO-FILLED before its first use (for example with
+ * cudaMemsetAsync).  Its first bytes hold the arrival counters of the
+ * cross-CTA reductions; every call that runs to completion leaves them at zero
+ * again, so one workspace can serve any sequence of later calls, of any shape
+ * and either op, without being cleared again.  The rest is scratch.  Two calls
+ * that are in flight at the same time must not share one workspace.
  */
 #ifndef GN_H_
 #define GN_H_
@@ -67,7 +70,7 @@ typedef enum gn_status {
   GN_OK = 0,
   GN_ERR_INVALID = 1,     /* bad sizes, G not dividing C, missing or overlapping buffers */
   GN_ERR_UNSUPPORTED = 2, /* unknown layout or dtype, or a problem too large to launch */
-  GN_ERR_WORKSPACE = 3,   /* workspace NULL, misaligned or smaller than gn_workspace_size() */
+  GN_ERR_WORKSPACE = 3,   /* workspace NULL, not 16-byte aligned or smaller than gn_workspace_size() */
   GN_ERR_CUDA = 4         /* a CUDA call or kernel launch failed (see gn_last_cuda_error) */
 } gn_status;
 

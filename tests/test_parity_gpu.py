@@ -168,9 +168,10 @@ def test_in_place(name, w):
     checks.assert_param("dgamma", dg, ref["dgamma"])
 
 
-def test_garbage_workspace_and_canaries():
-    """The workspace needs no zero-fill, and nothing is written past the end of
-    the workspace or of any output."""
+def test_workspace_reuse_and_canaries():
+    """A workspace zero-filled once serves repeated calls of both ops, its
+    scratch part may hold anything, and nothing is written past the end of the
+    workspace or of any output."""
     w = SMALL[5][1]
     inp = synth.make_inputs(w, "cpu", seed=5)
     ref = _oracle_full(inp, w)
@@ -182,6 +183,7 @@ def test_garbage_workspace_and_canaries():
     wsb = torch.randint(0, 256, (n_ws + 256,), dtype=torch.uint8, device=dev)
     canary_ws = wsb[n_ws:].clone()
     ws = wsb[:n_ws]
+    ws[:256].zero_()  # the arrival counters (the rest is scratch)
 
     def padded(n, dtype):
         b = torch.full((n + 2 * pad,), 7.0, dtype=dtype, device=dev)
@@ -195,11 +197,12 @@ def test_garbage_workspace_and_canaries():
     bb, db = padded(w.C, torch.float32)
     x, dy = inp["x"].to(dev), inp["dy"].to(dev)
     gm, bt = inp["gamma"].to(dev), inp["beta"].to(dev)
-    for _ in range(2):
+    for _ in range(3):
         assert gn.fwd_raw(x, w.N, w.C, w.HW, w.G, w.layout, gm, bt, w.eps, y, mean, rstd, ws) == 0
         assert gn.bwd_raw(dy, x, mean, rstd, gm, w.N, w.C, w.HW, w.G, w.layout, dx, dg, db, ws) == 0
     torch.cuda.synchronize()
     assert torch.equal(wsb[n_ws:], canary_ws)
+    assert torch.all(ws[:4 * (w.N + 1)] == 0), "arrival counters not returned to zero"
     for b in (yb, dxb, mb, rb, gb, bb):
         assert torch.all(b[:pad] == 7.0) and torch.all(b[-pad:] == 7.0)
     _compare(dict(y=y, mean=mean, rstd=rstd, dx=dx, dgamma=dg, dbeta=db), ref, w)
@@ -211,7 +214,7 @@ def test_shared_workspace_across_shapes():
     cases = [SMALL[0][1], SMALL[2][1], SMALL[3][1], SMALL[2][1]]
     n_ws = max(gn.workspace_size(op, w.N, w.C, w.HW, w.G, w.layout, w.dtype)
                for w in cases for op in (0, 1))
-    ws = torch.full((n_ws,), 255, dtype=torch.uint8, device=dev)
+    ws = torch.zeros((n_ws,), dtype=torch.uint8, device=dev)
     for i, w in enumerate(cases):
         inp = synth.make_inputs(w, "cpu", seed=10 + i)
         x, dy = inp["x"].to(dev), inp["dy"].to(dev)
