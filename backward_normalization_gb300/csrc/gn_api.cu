@@ -44,7 +44,7 @@ int cuda_fail(cudaError_t e) {
 int prepare(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout, int dtype,
             bool aligned, void* workspace, size_t workspace_bytes, gn::KParams* p) {
   std::memset(p, 0, sizeof(*p));
-  p->g = gn::make_geom(op, N, C, HW, G, layout, dtype, aligned, gn::device_sm_count());
+  p->g = gn::make_geom(op, N, C, HW, G, layout, dtype, aligned);
   if (p->g.items <= 0 || p->g.items > 0x7fffffffLL) return GN_ERR_UNSUPPORTED;
   const gn::WsLayout w = gn::ws_layout(op, p->g);
   if (!workspace || workspace_bytes < w.total || !aligned16(workspace)) return GN_ERR_WORKSPACE;
@@ -58,10 +58,9 @@ int prepare(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout, int
 
 size_t ws_size_any_alignment(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout,
                              int dtype) {
-  const int sms = gn::device_sm_count();
   size_t best = 0;
   for (int a = 0; a < 2; ++a) {
-    const gn::Geom g = gn::make_geom(op, N, C, HW, G, layout, dtype, a != 0, sms);
+    const gn::Geom g = gn::make_geom(op, N, C, HW, G, layout, dtype, a != 0);
     const size_t t = gn::ws_layout(op, g).total;
     if (t > best) best = t;
   }
@@ -187,7 +186,7 @@ int gn_plan_info(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout
   if (rc != GN_OK) return rc;
   std::memset(out, 0, sizeof(*out));
   if (N == 0 || C == 0 || HW == 0) return GN_OK;
-  const gn::Geom g = gn::make_geom(op, N, C, HW, G, layout, dtype, aligned != 0, gn::device_sm_count());
+  const gn::Geom g = gn::make_geom(op, N, C, HW, G, layout, dtype, aligned != 0);
   out->regime = gn::kRegimeGeneric;
   out->launches = 2;
   out->vector_width = g.vw;

@@ -94,8 +94,14 @@ __device__ __forceinline__ uint32_t f2b(float a, float b) {
 template <typename T, int VW>
 struct Access;
 
+// Besides load/store, each access type exposes load_raw (the bits, kept packed
+// while loads are in flight) and unpack (bits -> floats), so that deep unrolls
+// hold 4 registers per 16-byte vector instead of VW floats.
 template <typename T>
 struct Access<T, 1> {
+  using Raw = T;
+  __device__ static Raw load_raw(const T* p, uint64_t) { return __ldg(p); }
+  __device__ static void unpack(const Raw& r, float (&f)[1]) { f[0] = Elem<T>::to_f(r); }
   __device__ static void load(const T* p, float (&f)[1], uint64_t) {
     f[0] = Elem<T>::to_f(__ldg(p));
   }
@@ -105,6 +111,14 @@ struct Access<T, 1> {
 };
 template <>
 struct Access<float, 4> {
+  using Raw = uint4;
+  __device__ static Raw load_raw(const float* p, uint64_t pol) { return ld16(p, pol); }
+  __device__ static void unpack(const Raw& u, float (&f)[4]) {
+    f[0] = __uint_as_float(u.x);
+    f[1] = __uint_as_float(u.y);
+    f[2] = __uint_as_float(u.z);
+    f[3] = __uint_as_float(u.w);
+  }
   __device__ static void load(const float* p, float (&f)[4], uint64_t pol) {
     const uint4 u = ld16(p, pol);
     f[0] = __uint_as_float(u.x);
@@ -123,6 +137,13 @@ struct Access<float, 4> {
 };
 template <>
 struct Access<__half, 8> {
+  using Raw = uint4;
+  __device__ static Raw load_raw(const __half* p, uint64_t pol) { return ld16(p, pol); }
+  __device__ static void unpack(const Raw& u, float (&f)[8]) {
+    float2 a = h2f(u.x), b = h2f(u.y), c = h2f(u.z), d = h2f(u.w);
+    f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+    f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
+  }
   __device__ static void load(const __half* p, float (&f)[8], uint64_t pol) {
     const uint4 u = ld16(p, pol);
     float2 a = h2f(u.x), b = h2f(u.y), c = h2f(u.z), d = h2f(u.w);
@@ -140,6 +161,13 @@ struct Access<__half, 8> {
 };
 template <>
 struct Access<__nv_bfloat16, 8> {
+  using Raw = uint4;
+  __device__ static Raw load_raw(const __nv_bfloat16* p, uint64_t pol) { return ld16(p, pol); }
+  __device__ static void unpack(const Raw& u, float (&f)[8]) {
+    float2 a = b2f(u.x), b = b2f(u.y), c = b2f(u.z), d = b2f(u.w);
+    f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+    f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
+  }
   __device__ static void load(const __nv_bfloat16* p, float (&f)[8], uint64_t pol) {
     const uint4 u = ld16(p, pol);
     float2 a = b2f(u.x), b = b2f(u.y), c = b2f(u.z), d = b2f(u.w);

@@ -79,8 +79,11 @@ struct KParams {
 
 // plan.cpp
 int device_sm_count();
+// CTAs of the op's first kernel that fit on the current device at once when
+// launched with g.tpb threads in clusters of `cl` CTAs (0: no device).
+int64_t resident_first_ctas(const Geom& g, int op, int cl);
 Geom make_geom(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout,
-               int dtype, bool aligned, int sm_count);
+               int dtype, bool aligned);
 WsLayout ws_layout(int op, const Geom& g);
 
 // Events recorded around/between the kernels of a call (benchmark hook; the
@@ -96,5 +99,8 @@ cudaError_t launch_first(const void* kernel, const KParams& p, size_t smem, cuda
 // kernels (gn_nhwc.cu / gn_nchw.cu): enqueue the two kernels of an op.
 cudaError_t launch_nhwc(const KParams& p, cudaStream_t s, bool bwd);
 cudaError_t launch_nchw(const KParams& p, cudaStream_t s, bool bwd);
+// The first kernel's function and dynamic shared memory for a plan.
+const void* nhwc_first_kernel(const Geom& g, bool bwd, size_t* smem);
+const void* nchw_first_kernel(const Geom& g, bool bwd, size_t* smem);
 
 }  // namespace gn

@@ -347,7 +347,27 @@ cudaError_t dispatch_vw(const KParams& p, cudaStream_t s, bool bwd) {
   return p.g.vw == 1 ? run_op<T, 1>(p, s, bwd) : run_op<T, Elem<T>::VEC>(p, s, bwd);
 }
 
+
+template <typename T, int VW>
+const void* first_t(const Geom& g, bool bwd, size_t* smem) {
+  *smem = sizeof(float) * 2 * g.tpb;
+  return bwd ? (const void*)nchw_bwd_reduce<T, VW> : (const void*)nchw_fwd_stats<T, VW>;
+}
+
+template <typename T>
+const void* first_vw(const Geom& g, bool bwd, size_t* smem) {
+  return g.vw == 1 ? first_t<T, 1>(g, bwd, smem) : first_t<T, Elem<T>::VEC>(g, bwd, smem);
+}
+
 }  // namespace
+
+const void* nchw_first_kernel(const Geom& g, bool bwd, size_t* smem) {
+  switch (g.dtype) {
+    case kF32: return first_vw<float>(g, bwd, smem);
+    case kF16: return first_vw<__half>(g, bwd, smem);
+    default: return first_vw<__nv_bfloat16>(g, bwd, smem);
+  }
+}
 
 cudaError_t launch_nchw(const KParams& p, cudaStream_t s, bool bwd) {
   switch (p.g.dtype) {

@@ -86,7 +86,7 @@ __device__ __forceinline__ void publish_nhwc(const KParams& p, const NhwcItem& i
 }
 
 template <typename T, int VW>
-__global__ void __launch_bounds__(512) nhwc_fwd_stats(const __grid_constant__ KParams p) {
+__global__ void __launch_bounds__(512, 2) nhwc_fwd_stats(const __grid_constant__ KParams p) {
   extern __shared__ float red[];
   const Geom& g = p.g;
   const NhwcItem it = nhwc_item(g, blockIdx.x);
@@ -101,19 +101,24 @@ __global__ void __launch_bounds__(512) nhwc_fwd_stats(const __grid_constant__ KP
     Access<T, VW>::load(xn, K, pfirst);  // row 0 of the sample: the per-channel shift
     const int64_t step = g.rpi;
     int64_t row = it.row0 + it.r;
-    for (; row + 3 * step < it.row1; row += 4 * step) {
+    using Raw = typename Access<T, VW>::Raw;
+    constexpr int U = 8;  // rows in flight per thread
+    for (; row + (U - 1) * step < it.row1; row += U * step) {
       const uint64_t pol = row >= keep ? plast : pfirst;
-      float v[4][VW];
+      Raw raw[U];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) Access<T, VW>::load(xn + (row + u * step) * g.C, v[u], pol);
+      for (int u = 0; u < U; ++u) raw[u] = Access<T, VW>::load_raw(xn + (row + u * step) * g.C, pol);
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
+      for (int u = 0; u < U; ++u) {
+        float v[VW];
+        Access<T, VW>::unpack(raw[u], v);
 #pragma unroll
         for (int k = 0; k < VW; ++k) {
-          const float d = v[u][k] - K[k];
+          const float d = v[k] - K[k];
           acc[2 * k] += d;
           acc[2 * k + 1] = fmaf(d, d, acc[2 * k + 1]);
         }
+      }
     }
     for (; row < it.row1; row += step) {
       float v[VW];
@@ -173,7 +178,7 @@ __global__ void __launch_bounds__(512) nhwc_fwd_apply(const __grid_constant__ KP
 }
 
 template <typename T, int VW>
-__global__ void __launch_bounds__(512) nhwc_bwd_reduce(const __grid_constant__ KParams p) {
+__global__ void __launch_bounds__(512, 2) nhwc_bwd_reduce(const __grid_constant__ KParams p) {
   extern __shared__ float red[];
   const Geom& g = p.g;
   const NhwcItem it = nhwc_item(g, blockIdx.x);
@@ -191,21 +196,27 @@ __global__ void __launch_bounds__(512) nhwc_bwd_reduce(const __grid_constant__ K
     const int64_t keep = it.row0 + g.keep_from;
     const int64_t step = g.rpi;
     int64_t row = it.row0 + it.r;
-    for (; row + step < it.row1; row += 2 * step) {
+    using Raw = typename Access<T, VW>::Raw;
+    constexpr int U = 4;  // rows in flight per thread (x and dy each)
+    for (; row + (U - 1) * step < it.row1; row += U * step) {
       const uint64_t pol = row >= keep ? plast : pfirst;
-      float xv[2][VW], dv[2][VW];
+      Raw rx[U], rd[U];
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        Access<T, VW>::load(xn + (row + u * step) * g.C, xv[u], pol);
-        Access<T, VW>::load(dyn + (row + u * step) * g.C, dv[u], pol);
+      for (int u = 0; u < U; ++u) {
+        rx[u] = Access<T, VW>::load_raw(xn + (row + u * step) * g.C, pol);
+        rd[u] = Access<T, VW>::load_raw(dyn + (row + u * step) * g.C, pol);
       }
 #pragma unroll
-      for (int u = 0; u < 2; ++u)
+      for (int u = 0; u < U; ++u) {
+        float xv[VW], dv[VW];
+        Access<T, VW>::unpack(rx[u], xv);
+        Access<T, VW>::unpack(rd[u], dv);
 #pragma unroll
         for (int k = 0; k < VW; ++k) {
-          acc[2 * k] += dv[u][k];
-          acc[2 * k + 1] = fmaf(dv[u][k], xv[u][k] - mu[k], acc[2 * k + 1]);
+          acc[2 * k] += dv[k];
+          acc[2 * k + 1] = fmaf(dv[k], xv[k] - mu[k], acc[2 * k + 1]);
         }
+      }
     }
     for (; row < it.row1; row += step) {
       const uint64_t pol = row >= keep ? plast : pfirst;
@@ -296,7 +307,27 @@ cudaError_t dispatch_vw(const KParams& p, cudaStream_t s, bool bwd) {
   return p.g.vw == 1 ? run_op<T, 1>(p, s, bwd) : run_op<T, Elem<T>::VEC>(p, s, bwd);
 }
 
+
+template <typename T, int VW>
+const void* first_t(const Geom& g, bool bwd, size_t* smem) {
+  *smem = sizeof(float) * 2 * VW * g.tpb;
+  return bwd ? (const void*)nhwc_bwd_reduce<T, VW> : (const void*)nhwc_fwd_stats<T, VW>;
+}
+
+template <typename T>
+const void* first_vw(const Geom& g, bool bwd, size_t* smem) {
+  return g.vw == 1 ? first_t<T, 1>(g, bwd, smem) : first_t<T, Elem<T>::VEC>(g, bwd, smem);
+}
+
 }  // namespace
+
+const void* nhwc_first_kernel(const Geom& g, bool bwd, size_t* smem) {
+  switch (g.dtype) {
+    case kF32: return first_vw<float>(g, bwd, smem);
+    case kF16: return first_vw<__half>(g, bwd, smem);
+    default: return first_vw<__nv_bfloat16>(g, bwd, smem);
+  }
+}
 
 cudaError_t launch_nhwc(const KParams& p, cudaStream_t s, bool bwd) {
   switch (p.g.dtype) {

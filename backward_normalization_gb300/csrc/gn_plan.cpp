@@ -5,6 +5,9 @@
 // so the same call on the same device always runs the same reduction tree and
 // gives bit-identical results.
 #include <atomic>
+#include <map>
+#include <mutex>
+#include <tuple>
 
 #include "gn_internal.h"
 
@@ -21,6 +24,17 @@ constexpr int64_t kCluster = 8;           // CTAs per cluster in the first kerne
 constexpr double kKeepBytes = 64.0 * (1 << 20);  // input kept in L2 for the second kernel
 std::atomic<int> g_sm_cache[kMaxDevices];
 
+}  // namespace
+
+namespace {
+// Resident CTAs of the first kernel, or an estimate when no device is visible
+// (two 512-thread CTAs per SM, clusters fitting 4 per 19-SM GPC).
+int64_t resident_or(const Geom& g, int op, int cl, int sm_count) {
+  const int64_t r = resident_first_ctas(g, op, cl);
+  if (r > 0) return r;
+  const int64_t per_sm = g.tpb > 256 ? 2 : 4;
+  return cl > 1 ? (int64_t)sm_count * per_sm * 16 / 19 : (int64_t)sm_count * per_sm;
+}
 }  // namespace
 
 int device_sm_count() {
@@ -42,8 +56,53 @@ int device_sm_count() {
   return sms;
 }
 
+int64_t resident_first_ctas(const Geom& g, int op, int cl) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  size_t smem = 0;
+  const void* fn = g.layout == kNHWC ? nhwc_first_kernel(g, op == kBwd, &smem)
+                                     : nchw_first_kernel(g, op == kBwd, &smem);
+  using Key = std::tuple<int, const void*, int, size_t, int>;
+  static std::mutex mu;
+  static std::map<Key, int64_t> cache;
+  const Key key{dev, fn, g.tpb, smem, cl};
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+  }
+  int64_t r = 0;
+  if (cl > 1) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)cl, 1, 1);
+    cfg.blockDim = dim3((unsigned)g.tpb, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)cl;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int nc = 0;
+    if (cudaOccupancyMaxActiveClusters(&nc, fn, &cfg) == cudaSuccess) r = (int64_t)nc * cl;
+  } else {
+    int nb = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fn, g.tpb, smem) == cudaSuccess)
+      r = (int64_t)nb * device_sm_count();
+  }
+  cudaGetLastError();
+  std::lock_guard<std::mutex> lock(mu);
+  cache[key] = r;
+  return r;
+}
+
 Geom make_geom(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout, int dtype,
-               bool aligned, int sm_count) {
+               bool aligned) {
+  const int sm_count = device_sm_count();
   Geom g{};
   g.N = N;
   g.C = C;
@@ -54,9 +113,8 @@ Geom make_geom(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout, 
   g.dtype = dtype;
   const int esz = dtype == kF32 ? 4 : 2;
   const int vec = 16 / esz;
-  // Two 512-thread CTAs are resident per SM; one item per CTA, one wave when
-  // the problem is large enough to fill the device.
-  const int64_t target = (int64_t)sm_count * 2;
+  // One item per CTA of the first kernel, and as many items as fit on the
+  // device at once (one wave) unless the problem needs more.
   int64_t item_len = 0;  // rows (NHWC) or elements (NCHW mode 0) per item
   if (layout == kNHWC) {
     g.vw = (aligned && C % vec == 0) ? vec : 1;
@@ -66,8 +124,17 @@ Geom make_geom(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout, 
     g.rpi = 512 / g.Wv;
     if (g.rpi < 1) g.rpi = 1;
     g.tpb = g.Wv * g.rpi;
-    int64_t T = clamp64(cdiv(target, N * g.ncb), 1, cdiv(HW, g.rpi));
-    if (T >= kCluster) T = rup(T, kCluster);
+    // One wave: as many row blocks per (n, cb) as the resident clusters allow.
+    const int64_t units = N * g.ncb;
+    const int64_t r8 = resident_or(g, op, kCluster, sm_count);
+    int64_t T = (r8 / units) / kCluster * kCluster;
+    if (T >= kCluster) {
+      T = (T < rup(cdiv(HW, g.rpi), kCluster)) ? T : rup(cdiv(HW, g.rpi), kCluster);
+    } else {
+      const int64_t r1 = resident_or(g, op, 1, sm_count);
+      T = clamp64(r1 / units, 1, cdiv(HW, g.rpi));
+      if (T >= kCluster) T = T / kCluster * kCluster;
+    }
     g.rb = rup(cdiv(HW, T), g.rpi);
     g.T = T;  // trailing items may be empty when rb*T > HW
     g.cl = T % kCluster == 0 ? kCluster : 1;
@@ -82,8 +149,15 @@ Geom make_geom(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout, 
     if (HW >= 2048) {
       g.mode = 0;
       g.tpb = 512;
-      int64_t P = clamp64(cdiv(target, N * C), 1, cdiv(HW, (int64_t)g.tpb * g.vw));
-      if (P >= kCluster) P = rup(P, kCluster);
+      const int64_t pmax = cdiv(HW, (int64_t)g.tpb * g.vw);
+      const int64_t r8 = resident_or(g, op, kCluster, sm_count);
+      int64_t P = (r8 / (N * C)) / kCluster * kCluster;
+      if (P >= kCluster) {
+        P = (P < rup(pmax, kCluster)) ? P : rup(pmax, kCluster);
+      } else {
+        P = clamp64(resident_or(g, op, 1, sm_count) / (N * C), 1, pmax);
+        if (P >= kCluster) P = P / kCluster * kCluster;
+      }
       g.L = rup(cdiv(HW, P), g.vw);
       g.T = P;  // trailing chunks may be empty when L*P > HW
       g.cl = P % kCluster == 0 ? kCluster : 1;
@@ -96,7 +170,7 @@ Geom make_geom(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout, 
     } else {
       g.mode = 1;
       g.tpb = 256;
-      g.RB = clamp64(cdiv(N * C, target), 8, C);
+      g.RB = clamp64(cdiv(N * C, resident_or(g, op, 1, sm_count)), 8, C);
       g.T = 1;
       g.cl = 1;
       g.Tp = 1;
