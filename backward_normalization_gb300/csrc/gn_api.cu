@@ -58,12 +58,16 @@ int prepare(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout, int
 
 size_t ws_size_any_alignment(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout,
                              int dtype) {
+  // Large enough for either op and either alignment, so that one workspace can
+  // serve a forward and the following backward.
+  (void)op;
   size_t best = 0;
-  for (int a = 0; a < 2; ++a) {
-    const gn::Geom g = gn::make_geom(op, N, C, HW, G, layout, dtype, a != 0);
-    const size_t t = gn::ws_layout(op, g).total;
-    if (t > best) best = t;
-  }
+  for (int o = 0; o < 2; ++o)
+    for (int a = 0; a < 2; ++a) {
+      const gn::Geom g = gn::make_geom(o, N, C, HW, G, layout, dtype, a != 0);
+      const size_t t = gn::ws_layout(o, g).total;
+      if (t > best) best = t;
+    }
   return best;
 }
 

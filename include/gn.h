@@ -75,8 +75,9 @@ typedef enum gn_status {
 } gn_status;
 
 /* Bytes of workspace that gn_fwd (op = GN_OP_FWD) or gn_bwd (op = GN_OP_BWD)
- * needs for this problem on the current device; 0 for invalid or empty
- * problems.  Host-only: launches nothing.  ("baracuda-kernels
+ * needs for this problem on the current device; the value is the same for
+ * both ops, so one workspace serves a forward and its backward.  0 for
+ * invalid or empty problems.  Host-only: launches nothing.  ("baracuda-kernels
  * src/norm/group_norm_backward.rs", workspace_size.) */
 GN_API size_t gn_workspace_size(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout,
                          int dtype);
