@@ -8,60 +8,82 @@
 
 namespace gn {
 
+// Sums a strided run of float2 records into (ax, ay) in index order:
+// records base[i*stride] for i = first, first + step, ... < count.  Loads are
+// issued eight at a time (predicated), so a short run costs one round trip.
+__device__ __forceinline__ void sum_records(const float2* base, int64_t stride, int64_t first,
+                                            int64_t step, int64_t count, float& ax, float& ay) {
+  for (int64_t i = first; i < count; i += 8 * step) {
+    float2 v[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int64_t j = i + k * step;
+      v[k] = j < count ? __ldcg(base + j * stride) : make_float2(0.f, 0.f);
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      ax += v[k].x;
+      ay += v[k].y;
+    }
+  }
+}
+
+// Threads as (slice, channel): consecutive threads on consecutive channels,
+// nsl slices per channel block.
+struct SliceLayout {
+  int cpb, nsl, cl, sl;
+};
+__device__ __forceinline__ SliceLayout slice_layout(int64_t C, int64_t count) {
+  SliceLayout L;
+  const int nt = blockDim.x;
+  L.cpb = (int)(C < nt ? C : nt);
+  int64_t nsl = nt / L.cpb;
+  if (nsl > count) nsl = count;
+  L.nsl = nsl < 1 ? 1 : (int)nsl;
+  L.cl = threadIdx.x % L.cpb;
+  L.sl = threadIdx.x / L.cpb;
+  return L;
+}
+
 // For every channel c of sample n, sums the g.Tp partial records of (n, c)
-// and calls fn(c, total) from one thread.  Threads are laid out as
-// (slice, channel) with consecutive threads on consecutive channels; slice s
-// adds records s, s + nsl, s + 2*nsl, ... (issued eight at a time so that the
-// loads overlap), then the slice sums are added in slice order.
+// and calls fn(c, total) from one thread.  Slice s adds records s, s + nsl,
+// ... in order, then the slice sums are added in slice order.
 // `sm` holds at least 2 * blockDim.x floats.  Ends with __syncthreads().
 template <typename Fn>
 __device__ __forceinline__ void sum_channel_partials(const KParams& p, int64_t n, float* sm,
                                                      Fn fn) {
   const Geom& g = p.g;
-  const int tid = threadIdx.x, nt = blockDim.x;
-  const int cpb = (int)(g.C < nt ? g.C : nt);
-  int64_t nsl64 = nt / cpb;
-  if (nsl64 > g.Tp) nsl64 = g.Tp;
-  const int nsl = nsl64 < 1 ? 1 : (int)nsl64;
-  const int cl = tid % cpb, sl = tid / cpb;
+  const SliceLayout L = slice_layout(g.C, g.Tp);
   const float2* base = p.part + n * g.C * g.Tp;
-  for (int64_t c0 = 0; c0 < g.C; c0 += cpb) {
-    const int64_t c = c0 + cl;
+  for (int64_t c0 = 0; c0 < g.C; c0 += L.cpb) {
+    const int64_t c = c0 + L.cl;
     float ax = 0.f, ay = 0.f;
-    if (sl < nsl && c < g.C) {
-      const float2* pc = base + c * g.cstride;
-      const int64_t st = (int64_t)nsl * g.tstride;
-      int64_t t = sl;
-      for (; t + 7 * nsl < g.Tp; t += 8 * nsl) {
-        float2 v[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) v[k] = __ldcg(pc + t * g.tstride + k * st);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          ax += v[k].x;
-          ay += v[k].y;
-        }
-      }
-      for (; t < g.Tp; t += nsl) {
-        const float2 v = __ldcg(pc + t * g.tstride);
-        ax += v.x;
-        ay += v.y;
-      }
-    }
-    if (sl < nsl) {
-      sm[2 * (sl * cpb + cl)] = ax;
-      sm[2 * (sl * cpb + cl) + 1] = ay;
+    if (L.sl < L.nsl && c < g.C)
+      sum_records(base + c * g.cstride, g.tstride, L.sl, L.nsl, g.Tp, ax, ay);
+    if (L.sl < L.nsl) {
+      sm[2 * (L.sl * L.cpb + L.cl)] = ax;
+      sm[2 * (L.sl * L.cpb + L.cl) + 1] = ay;
     }
     __syncthreads();
-    if (sl == 0 && c < g.C) {
-      for (int s = 1; s < nsl; ++s) {
-        ax += sm[2 * (s * cpb + cl)];
-        ay += sm[2 * (s * cpb + cl) + 1];
+    if (L.sl == 0 && c < g.C) {
+      for (int s = 1; s < L.nsl; ++s) {
+        ax += sm[2 * (s * L.cpb + L.cl)];
+        ay += sm[2 * (s * L.cpb + L.cl) + 1];
       }
       fn(c, make_float2(ax, ay));
     }
     __syncthreads();
   }
+}
+
+// Where the finalising CTA keeps its per-channel results for the group step:
+// in shared memory after the 2*blockDim.x floats used by the partial sums when
+// the C records fit (sm_floats is the CTA's dynamic shared memory), else in
+// the workspace.
+__device__ __forceinline__ float2* channel_stage(const KParams& p, int64_t n, float* sm,
+                                                 int64_t sm_floats) {
+  const int64_t need = 2 * (int64_t)blockDim.x + 2 * p.g.C;
+  return need <= sm_floats ? reinterpret_cast<float2*>(sm + 2 * blockDim.x) : p.chst + n * p.g.C;
 }
 
 // Offset of element (n, c, hw = 0): the per-channel shift of the forward sums.
@@ -75,26 +97,27 @@ __device__ __forceinline__ int64_t first_elem_offset(const Geom& g, int64_t n, i
 //   mean_g = avg_c(mean_c),  M2_g = sum_c M2_c + HW * sum_c (mean_c - mean_g)^2,
 // and var = M2_g / (Cg*HW) (biased), rstd = 1/sqrt(var + eps).
 template <typename T>
-__device__ void finalize_fwd(const KParams& p, int64_t n, float* sm) {
+__device__ void finalize_fwd(const KParams& p, int64_t n, float* sm, int64_t sm_floats) {
   const Geom& g = p.g;
   const T* x = static_cast<const T*>(p.x);
   const float hw = (float)g.HW;
+  float2* stage = channel_stage(p, n, sm, sm_floats);
   sum_channel_partials(p, n, sm, [&](int64_t c, float2 s) {
     const float K = Elem<T>::to_f(x[first_elem_offset(g, n, c)]);
     const float q = s.x / hw;
     const float m2 = fmaxf(fmaf(-s.x, q, s.y), 0.f);
-    p.chst[n * g.C + c] = make_float2(K + q, m2);
+    stage[c] = make_float2(K + q, m2);
   });
   const float cgf = (float)g.Cg;
   const float mf = (float)(g.Cg * g.HW);
   for (int64_t gi = threadIdx.x; gi < g.G; gi += blockDim.x) {
-    const float2* cs = p.chst + n * g.C + gi * g.Cg;
+    const float2* cs = stage + gi * g.Cg;
     float s = 0.f;
-    for (int64_t k = 0; k < g.Cg; ++k) s += __ldcg(cs + k).x;
+    for (int64_t k = 0; k < g.Cg; ++k) s += cs[k].x;
     const float mg = s / cgf;
     float m2 = 0.f;
     for (int64_t k = 0; k < g.Cg; ++k) {
-      const float2 v = __ldcg(cs + k);
+      const float2 v = cs[k];
       const float d = v.x - mg;
       m2 += fmaf(hw * d, d, v.y);
     }
@@ -111,15 +134,21 @@ __device__ void finalize_fwd(const KParams& p, int64_t n, float* sm) {
 // and dx = rstd*gamma_c*dy + B*(x - mean) + D with
 //   B = -rstd^3 * c2 / M,  D = -rstd * c1 / M,  M = Cg*HW.
 // The per-channel (S1, S2) stay in chst for the dgamma/dbeta step.
-__device__ __forceinline__ void finalize_bwd(const KParams& p, int64_t n, float* sm) {
+__device__ __forceinline__ void finalize_bwd(const KParams& p, int64_t n, float* sm,
+                                             int64_t sm_floats) {
   const Geom& g = p.g;
-  sum_channel_partials(p, n, sm, [&](int64_t c, float2 s) { p.chst[n * g.C + c] = s; });
+  float2* stage = channel_stage(p, n, sm, sm_floats);
+  float2* chst = p.chst + n * g.C;
+  sum_channel_partials(p, n, sm, [&](int64_t c, float2 s) {
+    chst[c] = s;  // kept for the dgamma/dbeta step
+    stage[c] = s;
+  });
   const float mf = (float)(g.Cg * g.HW);
   for (int64_t gi = threadIdx.x; gi < g.G; gi += blockDim.x) {
-    const float2* cs = p.chst + n * g.C + gi * g.Cg;
+    const float2* cs = stage + gi * g.Cg;
     float c1 = 0.f, c2 = 0.f;
     for (int64_t k = 0; k < g.Cg; ++k) {
-      const float2 v = __ldcg(cs + k);
+      const float2 v = cs[k];
       const float gm = p.gamma ? __ldg(p.gamma + gi * g.Cg + k) : 1.0f;
       c1 = fmaf(gm, v.x, c1);
       c2 = fmaf(gm, v.y, c2);
@@ -129,21 +158,49 @@ __device__ __forceinline__ void finalize_bwd(const KParams& p, int64_t n, float*
   }
 }
 
-// Level 2 of the parameter gradients, over samples in index order:
-//   dbeta_c = sum_n S1[n, c],   dgamma_c = sum_n rstd[n, g(c)] * S2[n, c].
-__device__ __forceinline__ void finalize_params(const KParams& p) {
+// Level 2 of the parameter gradients:
+//   dbeta_c = sum_n S1[n, c],   dgamma_c = sum_n rstd[n, g(c)] * S2[n, c],
+// with the samples split into fixed slices (summed in order, then the slice
+// sums in slice order).
+__device__ __forceinline__ void finalize_params(const KParams& p, float* sm) {
   const Geom& g = p.g;
   if (!p.dgamma && !p.dbeta) return;
-  for (int64_t c = threadIdx.x; c < g.C; c += blockDim.x) {
-    const int64_t gi = c / g.Cg;
+  const SliceLayout L = slice_layout(g.C, g.N);
+  for (int64_t c0 = 0; c0 < g.C; c0 += L.cpb) {
+    const int64_t c = c0 + L.cl;
     float db = 0.f, dg = 0.f;
-    for (int64_t n = 0; n < g.N; ++n) {
-      const float2 v = __ldcg(p.chst + n * g.C + c);
-      db += v.x;
-      dg = fmaf(__ldg(p.rstd + n * g.G + gi), v.y, dg);
+    if (L.sl < L.nsl && c < g.C) {
+      const int64_t gi = c / g.Cg;
+      for (int64_t n = L.sl; n < g.N; n += 8 * L.nsl) {
+        float2 v[8];
+        float r[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int64_t j = n + k * L.nsl;
+          v[k] = j < g.N ? __ldcg(p.chst + j * g.C + c) : make_float2(0.f, 0.f);
+          r[k] = j < g.N ? __ldg(p.rstd + j * g.G + gi) : 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          db += v[k].x;
+          dg = fmaf(r[k], v[k].y, dg);
+        }
+      }
     }
-    if (p.dbeta) p.dbeta[c] = db;
-    if (p.dgamma) p.dgamma[c] = dg;
+    if (L.sl < L.nsl) {
+      sm[2 * (L.sl * L.cpb + L.cl)] = db;
+      sm[2 * (L.sl * L.cpb + L.cl) + 1] = dg;
+    }
+    __syncthreads();
+    if (L.sl == 0 && c < g.C) {
+      for (int s = 1; s < L.nsl; ++s) {
+        db += sm[2 * (s * L.cpb + L.cl)];
+        dg += sm[2 * (s * L.cpb + L.cl) + 1];
+      }
+      if (p.dbeta) p.dbeta[c] = db;
+      if (p.dgamma) p.dgamma[c] = dg;
+    }
+    __syncthreads();
   }
 }
 
@@ -152,24 +209,24 @@ __device__ __forceinline__ void finalize_params(const KParams& p) {
 // (and, in the backward, the parameter-gradient step once every sample is
 // complete).  Must be reached by all threads of the CTA.
 template <typename T, bool kBwd>
-__device__ __forceinline__ void arrive_and_finalize(const KParams& p, int64_t n, float* sm) {
+__device__ __forceinline__ void arrive_and_finalize(const KParams& p, int64_t n, float* sm,
+                                                    int64_t sm_floats) {
   __shared__ int s_last;
   __syncthreads();
   if (threadIdx.x == 0) s_last = publish_and_arrive(p.tickets + n, (unsigned)p.g.arrivals_per_n);
   __syncthreads();
   if (!s_last) return;
   if (kBwd)
-    finalize_bwd(p, n, sm);
+    finalize_bwd(p, n, sm, sm_floats);
   else
-    finalize_fwd<T>(p, n, sm);
+    finalize_fwd<T>(p, n, sm, sm_floats);
   __syncthreads();
   if (threadIdx.x == 0) atomicExch(p.tickets + n, 0u);
   if (!kBwd) return;
   if (threadIdx.x == 0) s_last = publish_and_arrive(p.tickets + p.g.N, (unsigned)p.g.N);
   __syncthreads();
   if (!s_last) return;
-  finalize_params(p);
-  __syncthreads();
+  finalize_params(p, sm);
   if (threadIdx.x == 0) atomicExch(p.tickets + p.g.N, 0u);
 }
 

@@ -17,6 +17,13 @@
 namespace gn {
 namespace {
 
+// Dynamic shared memory of the first kernels, in floats: reduction scratch
+// plus room to stage the per-channel results of the finalisation.
+__host__ __device__ __forceinline__ int64_t nchw_smem_floats(const Geom& g) {
+  const int64_t stage = 2 * g.C <= 8192 ? 2 * g.C : 0;
+  return 2 * (int64_t)g.tpb + stage;
+}
+
 template <int VW>
 __device__ __forceinline__ void acc_shifted(const float (&v)[VW], float K, float& s, float& q) {
 #pragma unroll
@@ -124,7 +131,7 @@ __global__ void __launch_bounds__(512) nchw_fwd_stats(const __grid_constant__ KP
       if (lane == 0) p.part[row] = make_float2(s, q);
     }
   }
-  arrive_and_finalize<T, false>(p, n, sm);
+  arrive_and_finalize<T, false>(p, n, sm, nchw_smem_floats(g));
 }
 
 template <typename T, int VW>
@@ -251,7 +258,7 @@ __global__ void __launch_bounds__(512) nchw_bwd_reduce(const __grid_constant__ K
       if (lane == 0) p.part[row] = make_float2(s1, s2);
     }
   }
-  arrive_and_finalize<T, true>(p, n, sm);
+  arrive_and_finalize<T, true>(p, n, sm, nchw_smem_floats(g));
 }
 
 template <typename T, int VW>
@@ -326,7 +333,7 @@ __global__ void __launch_bounds__(512) nchw_bwd_dx(const __grid_constant__ KPara
 template <typename T, int VW>
 cudaError_t run_op(const KParams& p, cudaStream_t s, bool bwd) {
   const Geom& g = p.g;
-  const size_t sm1 = sizeof(float) * 2 * g.tpb;
+  const size_t sm1 = sizeof(float) * nchw_smem_floats(g);
   const TimingEvents& ev = timing_events();
   if (ev.begin) cudaEventRecord(ev.begin, s);
   cudaError_t e = launch_first(bwd ? (const void*)nchw_bwd_reduce<T, VW> : (const void*)nchw_fwd_stats<T, VW>,
@@ -350,7 +357,7 @@ cudaError_t dispatch_vw(const KParams& p, cudaStream_t s, bool bwd) {
 
 template <typename T, int VW>
 const void* first_t(const Geom& g, bool bwd, size_t* smem) {
-  *smem = sizeof(float) * 2 * g.tpb;
+  *smem = sizeof(float) * nchw_smem_floats(g);
   return bwd ? (const void*)nchw_bwd_reduce<T, VW> : (const void*)nchw_fwd_stats<T, VW>;
 }
 

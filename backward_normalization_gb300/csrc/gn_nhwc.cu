@@ -82,7 +82,7 @@ __device__ __forceinline__ void publish_nhwc(const KParams& p, const NhwcItem& i
       out[k] = make_float2(red[(2 * k) * blockDim.x + threadIdx.x],
                            red[(2 * k + 1) * blockDim.x + threadIdx.x]);
   }
-  arrive_and_finalize<T, kBwd>(p, it.n, red);
+  arrive_and_finalize<T, kBwd>(p, it.n, red, (int64_t)2 * VW * blockDim.x);
 }
 
 template <typename T, int VW>
