@@ -207,13 +207,16 @@ def source_sha():
     return h.hexdigest()[:16]
 
 
-def time_configs(gn, synth, torch, flush, reps=20):
+def time_configs(gn, synth, torch, flush, names=None, reps=20):
     """Per-workload fwd and bwd times (median of reps, L2 flushed before each
-    call) for the four large workloads."""
+    call) for the large workloads.  All reps are queued before the first
+    synchronisation, so the GPU never waits for the host between calls."""
     out = {}
     peak, _ = load_peaks()
     stream = torch.cuda.current_stream()
     for w in synth.WORKLOADS[1:]:
+        if names and w.name not in names:
+            continue
         inp = synth.make_inputs(w, "cuda", seed=0)
         x, dy, gm, bt = inp["x"], inp["dy"], inp["gamma"], inp["beta"]
         y = torch.empty_like(x)
@@ -223,9 +226,10 @@ def time_configs(gn, synth, torch, flush, reps=20):
         dg = torch.empty(w.C, device="cuda")
         db = torch.empty(w.C, device="cuda")
         ws = gn.alloc_workspace(gn.OP_BWD, w.N, w.C, w.HW, w.G, w.layout, x.dtype)
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
-        rec = {"fwd": [], "bwd": [], "fwd_stats": [], "fwd_apply": [], "bwd_reduce": [], "bwd_dx": []}
-        for it in range(reps + 3):
+        n_it = reps + 3
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(n_it)]
+        for it in range(n_it):
+            ev = evs[it]
             flush()
             gn.set_timing_events(ev[0], ev[1], ev[2])
             assert gn.fwd_raw(x, w.N, w.C, w.HW, w.G, w.layout, gm, bt, w.eps, y, mean, rstd, ws, stream) == 0
@@ -233,14 +237,15 @@ def time_configs(gn, synth, torch, flush, reps=20):
             gn.set_timing_events(ev[3], ev[4], ev[5])
             assert gn.bwd_raw(dy, x, mean, rstd, gm, w.N, w.C, w.HW, w.G, w.layout, dx, dg, db, ws, stream) == 0
             gn.set_timing_events()
-            torch.cuda.synchronize()
-            if it >= 3:
-                rec["fwd"].append(ev[0].elapsed_time(ev[2]))
-                rec["fwd_stats"].append(ev[0].elapsed_time(ev[1]))
-                rec["fwd_apply"].append(ev[1].elapsed_time(ev[2]))
-                rec["bwd"].append(ev[3].elapsed_time(ev[5]))
-                rec["bwd_reduce"].append(ev[3].elapsed_time(ev[4]))
-                rec["bwd_dx"].append(ev[4].elapsed_time(ev[5]))
+        torch.cuda.synchronize()
+        rec = {"fwd": [], "bwd": [], "fwd_stats": [], "fwd_apply": [], "bwd_reduce": [], "bwd_dx": []}
+        for ev in evs[3:]:
+            rec["fwd"].append(ev[0].elapsed_time(ev[2]))
+            rec["fwd_stats"].append(ev[0].elapsed_time(ev[1]))
+            rec["fwd_apply"].append(ev[1].elapsed_time(ev[2]))
+            rec["bwd"].append(ev[3].elapsed_time(ev[5]))
+            rec["bwd_reduce"].append(ev[3].elapsed_time(ev[4]))
+            rec["bwd_dx"].append(ev[4].elapsed_time(ev[5]))
         mb = min_bytes(w)
         med = {k: statistics.median(v) for k, v in rec.items()}
         fwd_gbs = mb["fwd"] / (med["fwd"] * 1e-3) / 1e9
@@ -424,7 +429,9 @@ def run_ours(args, rank, world, local_rank):
     if not args.no_per_config and world == 1:
         del x, dy, y, dx, inp
         torch.cuda.empty_cache()
-        per_config = time_configs(gn, synth, torch, flush)
+        per_config = time_configs(gn, synth, torch, flush,
+                                  names=args.configs.split(",") if args.configs else None,
+                                  reps=args.reps)
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
@@ -461,6 +468,8 @@ def main():
     ap.add_argument("--no-per-config", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--configs", default="", help="comma-separated workload names for the per-workload leg")
+    ap.add_argument("--reps", type=int, default=20, help="timed calls per workload in the per-workload leg")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
