@@ -45,11 +45,13 @@ int prepare(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout, int
             bool aligned, void* workspace, size_t workspace_bytes, gn::KParams* p) {
   std::memset(p, 0, sizeof(*p));
   p->g = gn::make_geom(op, N, C, HW, G, layout, dtype, aligned);
-  if (p->g.items <= 0 || p->g.items > 0x7fffffffLL) return GN_ERR_UNSUPPORTED;
+  if (p->g.regime != gn::kRegimeResident && (p->g.items <= 0 || p->g.items > 0x7fffffffLL))
+    return GN_ERR_UNSUPPORTED;
   const gn::WsLayout w = gn::ws_layout(op, p->g);
   if (!workspace || workspace_bytes < w.total || !aligned16(workspace)) return GN_ERR_WORKSPACE;
   char* ws = static_cast<char*>(workspace);
   p->tickets = reinterpret_cast<unsigned*>(ws + w.tickets);
+  p->err = reinterpret_cast<unsigned*>(ws + w.err);
   p->part = reinterpret_cast<float2*>(ws + w.part);
   p->chst = reinterpret_cast<float2*>(ws + w.chst);
   p->coef = reinterpret_cast<float2*>(ws + w.coef);
@@ -114,7 +116,9 @@ int gn_fwd(const void* x, int64_t N, int64_t C, int64_t HW, int64_t G, int layou
   p.rstd = rstd;
   p.eps = eps;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const cudaError_t e = layout == GN_LAYOUT_NHWC ? gn::launch_nhwc(p, s, false) : gn::launch_nchw(p, s, false);
+  const cudaError_t e = p.g.regime == gn::kRegimeResident ? gn::launch_resident(p, s, false)
+                        : layout == GN_LAYOUT_NHWC       ? gn::launch_nhwc(p, s, false)
+                                                         : gn::launch_nchw(p, s, false);
   return e == cudaSuccess ? GN_OK : cuda_fail(e);
 }
 
@@ -158,7 +162,9 @@ int gn_bwd(const void* dy, const void* x, const float* mean, const float* rstd,
   p.rstd = const_cast<float*>(rstd);
   p.dgamma = dgamma;
   p.dbeta = dbeta;
-  const cudaError_t e = layout == GN_LAYOUT_NHWC ? gn::launch_nhwc(p, s, true) : gn::launch_nchw(p, s, true);
+  const cudaError_t e = p.g.regime == gn::kRegimeResident ? gn::launch_resident(p, s, true)
+                        : layout == GN_LAYOUT_NHWC       ? gn::launch_nhwc(p, s, true)
+                                                         : gn::launch_nchw(p, s, true);
   return e == cudaSuccess ? GN_OK : cuda_fail(e);
 }
 
@@ -174,6 +180,13 @@ const char* gn_status_string(int status) {
 }
 
 int gn_last_cuda_error(void) { return t_last_cuda_error; }
+
+int gn_set_regime(int regime) {
+  if (regime != GN_REGIME_AUTO && regime != GN_REGIME_TWO_KERNEL && regime != GN_REGIME_RESIDENT)
+    return GN_ERR_INVALID;
+  gn::set_regime_override(regime);
+  return GN_OK;
+}
 
 int gn_set_timing_events(void* ev_begin, void* ev_mid, void* ev_end) {
   t_events.begin = static_cast<cudaEvent_t>(ev_begin);
@@ -191,11 +204,11 @@ int gn_plan_info(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout
   std::memset(out, 0, sizeof(*out));
   if (N == 0 || C == 0 || HW == 0) return GN_OK;
   const gn::Geom g = gn::make_geom(op, N, C, HW, G, layout, dtype, aligned != 0);
-  out->regime = gn::kRegimeGeneric;
-  out->launches = 2;
+  out->regime = g.regime;
+  out->launches = g.regime == gn::kRegimeResident ? 1 : 2;
   out->vector_width = g.vw;
   out->threads = g.tpb;
-  out->ctas = g.items;
+  out->ctas = g.regime == gn::kRegimeResident ? g.units * g.K : g.items;
   out->partials = g.N * g.C * g.Tp;
   out->workspace_bytes = gn::ws_layout(op, g).total;
   return GN_OK;

@@ -15,7 +15,8 @@ enum Op { kFwd = 0, kBwd = 1 };
 // Regimes (which kernel family runs a call).
 enum Regime {
   kRegimeAuto = -1,
-  kRegimeGeneric = 0,  // stats/reduce kernel + apply/dx kernel, any shape
+  kRegimeGeneric = 0,   // stats/reduce kernel + apply/dx kernel, any shape
+  kRegimeResident = 1,  // one kernel: a cluster holds a unit in shared memory
 };
 
 // How one call is cut into "items" (one CTA each).  Both kernels of an op use
@@ -48,11 +49,23 @@ struct Geom {
   int64_t items;
   int64_t keep_from;  // item-relative row/element index from which the first kernel
                       // loads with the L2 evict_last policy (the part read again first)
+  // resident regime (gn_resident.cu)
+  int regime;
+  int K;               // CTAs per unit (cluster size)
+  int64_t m;           // NCHW: pieces per channel plane (K = Cg*m)
+  int64_t units;       // clusters: N*G (NCHW) or N (NHWC)
+  int64_t slice;       // NCHW: elements per piece; NHWC: rows per CTA
+  int64_t chunk;       // NCHW: elements per chunk; NHWC: rows per chunk
+  int64_t chunk_bytes; // bytes of one tensor's chunk
+  int nres, S;         // resident chunk slots, ring slots
+  size_t smem;         // dynamic shared memory bytes
+  size_t off_ring, off_red, off_xch, off_tot, off_grp, off_bar;
 };
 
 // Workspace layout (byte offsets, each 256-byte aligned).
 struct WsLayout {
   size_t tickets;  // (N + 1) uint32 arrival counters: one per sample, one global
+  size_t err;      // uint32 error word (a bounded wait ran out)
   size_t part;     // N*C*Tp float2 partial sums
   size_t chst;     // N*C float2 per-channel results of the finalisation
   size_t coef;     // N*G float2 dx coefficients (backward only)
@@ -72,6 +85,7 @@ struct KParams {
   float* dbeta;
   float eps;
   unsigned* tickets;
+  unsigned* err;
   float2* part;
   float2* chst;
   float2* coef;
@@ -79,6 +93,8 @@ struct KParams {
 
 // plan.cpp
 int device_sm_count();
+// Test hook: force a regime (kRegimeAuto = automatic choice).
+void set_regime_override(int regime);
 // CTAs of the op's first kernel that fit on the current device at once when
 // launched with g.tpb threads in clusters of `cl` CTAs (0: no device).
 int64_t resident_first_ctas(const Geom& g, int op, int cl);
@@ -102,5 +118,11 @@ cudaError_t launch_nchw(const KParams& p, cudaStream_t s, bool bwd);
 // The first kernel's function and dynamic shared memory for a plan.
 const void* nhwc_first_kernel(const Geom& g, bool bwd, size_t* smem);
 const void* nchw_first_kernel(const Geom& g, bool bwd, size_t* smem);
+// gn_resident.cu
+const void* resident_kernel_ptr(const Geom& g, bool bwd);
+cudaError_t launch_resident(const KParams& p, cudaStream_t s, bool bwd);
+// Sets the kernel attributes a resident launch needs (large shared memory,
+// 16-CTA clusters); idempotent.
+cudaError_t prepare_resident_kernel(const void* kernel, const Geom& g);
 
 }  // namespace gn

@@ -20,6 +20,7 @@ int64_t clamp64(int64_t v, int64_t lo, int64_t hi) { return v < lo ? lo : (v > h
 size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
 constexpr int kMaxDevices = 64;
+std::atomic<int> g_regime_override{kRegimeAuto};
 constexpr int64_t kCluster = 8;           // CTAs per cluster in the first kernels
 constexpr double kKeepBytes = 64.0 * (1 << 20);  // input kept in L2 for the second kernel
 std::atomic<int> g_sm_cache[kMaxDevices];
@@ -34,6 +35,158 @@ int64_t resident_or(const Geom& g, int op, int cl, int sm_count) {
   if (r > 0) return r;
   const int64_t per_sm = g.tpb > 256 ? 2 : 4;
   return cl > 1 ? (int64_t)sm_count * per_sm * 16 / 19 : (int64_t)sm_count * per_sm;
+}
+}  // namespace
+
+void set_regime_override(int regime) { g_regime_override.store(regime); }
+
+cudaError_t prepare_resident_kernel(const void* kernel, const Geom& g) {
+  static std::mutex mu;
+  static std::map<std::pair<int, const void*>, size_t> done;  // (device, kernel) -> smem set
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = done.find({dev, kernel});
+  if (it != done.end() && it->second >= g.smem) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)g.smem);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e != cudaSuccess) return e;
+  done[{dev, kernel}] = g.smem;
+  return cudaSuccess;
+}
+
+namespace {
+constexpr size_t kSmemPerCta = 227 * 1024 - 1024;  // dynamic smem budget (static use ~1 KB)
+constexpr int64_t kMaxUnitBytes = 32ll << 20;       // per-unit input (x, or x + dy)
+constexpr int64_t kChunkBytes = 16 * 1024;
+
+size_t a128(size_t v) { return (v + 127) & ~size_t(127); }
+
+// Clusters of the resident kernel that fit on the device at once (0 if none,
+// -1 when no device is visible).
+int64_t resident_clusters(const Geom& g, int op) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return -1;
+  }
+  const void* fn = resident_kernel_ptr(g, op == kBwd);
+  if (prepare_resident_kernel(fn, g) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)g.K, 1, 1);
+  cfg.blockDim = dim3((unsigned)g.tpb, 1, 1);
+  cfg.dynamicSmemBytes = g.smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)g.K;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int nc = 0;
+  if (cudaOccupancyMaxActiveClusters(&nc, fn, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return nc;
+}
+
+// Fills the resident-regime fields of g; false when the problem does not fit
+// the regime (the two-kernel path then runs).
+bool plan_resident(Geom& g, int op) {
+  const int esz = g.dtype == kF32 ? 4 : 2;
+  const int vec = 16 / esz;
+  const int nten = op == kBwd ? 2 : 1;
+  if (g.vw != vec) return false;
+  Geom r = g;
+  size_t red_f, xch_f, tot_f, grp_f;
+  int64_t slice_elems, chunk_elems;
+  if (g.layout == kNCHW) {
+    if (g.Cg > 16) return false;
+    const int64_t unit_bytes = g.Cg * g.HW * esz * nten;
+    if (unit_bytes > kMaxUnitBytes) return false;
+    int64_t m = 16 / g.Cg;
+    while (m > 1 && g.HW * esz / m < 2 * kChunkBytes) m /= 2;
+    r.m = m;
+    r.K = (int)(g.Cg * m);
+    r.tpb = 512;
+    r.slice = rup(cdiv(g.HW, m), vec);
+    r.chunk = kChunkBytes / esz;
+    r.chunk_bytes = kChunkBytes;
+    r.units = g.N * g.G;
+    slice_elems = r.slice;
+    chunk_elems = r.chunk;
+    red_f = 2 * (size_t)r.tpb;
+    xch_f = 2;
+    tot_f = 0;
+    grp_f = 2;
+  } else {
+    const int64_t V = g.C / vec;
+    if (V > 512) return false;
+    const int64_t unit_bytes = g.HW * g.C * esz * nten;
+    if (unit_bytes > kMaxUnitBytes) return false;
+    r.ncb = 1;
+    r.Wv = (int)V;
+    r.rpi = (int)(512 / V);
+    r.tpb = r.Wv * r.rpi;
+    const int64_t row_bytes = g.C * esz;
+    r.chunk = kChunkBytes / row_bytes > 0 ? kChunkBytes / row_bytes : 1;
+    r.chunk_bytes = r.chunk * row_bytes;
+    r.units = g.N;
+    red_f = 2 * (size_t)vec * r.tpb;
+    xch_f = 2 * (size_t)g.C;
+    tot_f = 2 * (size_t)g.C;
+    grp_f = 2 * (size_t)g.G;
+    chunk_elems = r.chunk * g.C;
+    // smallest power-of-two K whose slices fit the chunk budget (at most 16)
+    const size_t fixed = a128(red_f * 4) + a128(xch_f * 4) + a128(tot_f * 4) + a128(grp_f * 4) + 1024;
+    const size_t budget = kSmemPerCta > fixed ? kSmemPerCta - fixed : 0;
+    r.K = 1;
+    while (r.K < 16 && (size_t)(cdiv(cdiv(g.HW, r.K), r.chunk) * r.chunk_bytes * nten) > budget) r.K *= 2;
+    r.slice = cdiv(g.HW, r.K);
+    slice_elems = r.slice * g.C;
+  }
+  const size_t fixed = a128(red_f * 4) + a128(xch_f * 4) + a128(tot_f * 4) + a128(grp_f * 4);
+  const size_t slot = (size_t)r.chunk_bytes * nten;
+  const int64_t nch = cdiv(slice_elems, chunk_elems);
+  if (kSmemPerCta < fixed + 512) return false;
+  // slots left after the fixed areas and one mbarrier per slot
+  int64_t slots = (int64_t)((kSmemPerCta - fixed - 512) / (slot + 8));
+  if (nch <= slots) {
+    r.nres = (int)nch;
+    r.S = 0;
+  } else {
+    if (slots < 3) return false;
+    r.S = 2;
+    r.nres = (int)(slots - r.S);
+  }
+  size_t off = 0;
+  off += a128((size_t)r.nres * slot);
+  r.off_ring = off;
+  off += a128((size_t)r.S * slot);
+  r.off_red = off;
+  off += a128(red_f * 4);
+  r.off_xch = off;
+  off += a128(xch_f * 4);
+  r.off_tot = off;
+  off += a128(tot_f * 4);
+  r.off_grp = off;
+  off += a128(grp_f * 4);
+  r.off_bar = off;
+  off += a128(8 * (size_t)(r.nres + r.S));
+  r.smem = off;
+  if (r.smem > kSmemPerCta) return false;
+  if (r.units * r.K > 0x7fffffffLL) return false;
+  r.regime = kRegimeResident;
+  r.Tp = 0;
+  if (resident_clusters(r, op) == 0) return false;
+  g = r;
+  return true;
 }
 }  // namespace
 
@@ -190,6 +343,9 @@ Geom make_geom(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout, 
     g.keep_from = keep_frac >= 1.0 ? 0 : 1;  // whole rows: all or nothing
   else
     g.keep_from = item_len - (int64_t)((double)item_len * keep_frac);
+  g.regime = kRegimeGeneric;
+  const int ov = g_regime_override.load();
+  if (ov != kRegimeGeneric) plan_resident(g, op);
   return g;
 }
 
@@ -198,6 +354,8 @@ WsLayout ws_layout(int op, const Geom& g) {
   size_t off = 0;
   w.tickets = off;
   off = align256(off + sizeof(unsigned) * (size_t)(g.N + 1));
+  w.err = off;
+  off = align256(off + sizeof(unsigned));
   w.part = off;
   off = align256(off + 2 * sizeof(float) * (size_t)(g.N * g.C * g.Tp));
   w.chst = off;

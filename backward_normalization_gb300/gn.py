@@ -67,6 +67,8 @@ def lib() -> ctypes.CDLL:
         L.gn_plan_info.argtypes = [ctypes.c_int, _I64, _I64, _I64, _I64, ctypes.c_int, ctypes.c_int,
                                    ctypes.c_int, ctypes.POINTER(PlanDesc)]
         L.gn_plan_info.restype = ctypes.c_int
+        L.gn_set_regime.argtypes = [ctypes.c_int]
+        L.gn_set_regime.restype = ctypes.c_int
         L.gn_set_timing_events.argtypes = [_VP, _VP, _VP]
         L.gn_set_timing_events.restype = ctypes.c_int
         _lib = L
@@ -123,6 +125,16 @@ def bwd_raw(dy, x, mean, rstd, gamma, N, C, HW, G, layout, dx, dgamma, dbeta, wo
     return lib().gn_bwd(_ptr(dy), _ptr(x), _ptr(mean), _ptr(rstd), _ptr(gamma), N, C, HW, G,
                         LAYOUT[layout], DTYPE[x.dtype], _ptr(dx), _ptr(dgamma), _ptr(dbeta),
                         _ptr(workspace), ws_bytes, _stream(stream))
+
+
+REGIME_AUTO, REGIME_TWO_KERNEL, REGIME_RESIDENT = -1, 0, 1
+
+
+def set_regime(regime: int) -> None:
+    """Test hook: force the kernel family (REGIME_AUTO restores the default)."""
+    rc = lib().gn_set_regime(int(regime))
+    if rc != GN_OK:
+        raise GnError(rc, "gn_set_regime")
 
 
 def set_timing_events(ev_begin=None, ev_mid=None, ev_end=None) -> None:

@@ -119,9 +119,26 @@ GN_API int gn_last_cuda_error(void);
  * three NULLs to stop.  Returns a gn_status. */
 GN_API int gn_set_timing_events(void* ev_begin, void* ev_mid, void* ev_end);
 
+/* Kernel families ("regimes").  GN_REGIME_TWO_KERNEL runs any shape: a
+ * reduction kernel (statistics, or the backward group sums) and an
+ * elementwise kernel (y, or dx).  GN_REGIME_RESIDENT runs one kernel in which
+ * a thread-block cluster holds a whole reduction unit -- one (n, group) span
+ * for NCHW, one sample for NHWC -- in shared memory; it is taken for 16-byte
+ * aligned inputs whose unit is at most 32 MiB. */
+#define GN_REGIME_AUTO (-1)
+#define GN_REGIME_TWO_KERNEL 0
+#define GN_REGIME_RESIDENT 1
+
+/* Test hook, process-wide: GN_REGIME_AUTO (default) lets each call choose;
+ * GN_REGIME_TWO_KERNEL forces the two-kernel path; GN_REGIME_RESIDENT is the
+ * same as automatic (the resident regime wherever it applies).  Not
+ * thread-safe with respect to calls in flight on other threads.  Returns a
+ * gn_status. */
+GN_API int gn_set_regime(int regime);
+
 /* What a call would run, for tests and reports (host-only, no launch). */
 typedef struct gn_plan_desc {
-  int regime;            /* 0 = two-kernel path (reduce, then elementwise) */
+  int regime;            /* GN_REGIME_TWO_KERNEL or GN_REGIME_RESIDENT */
   int launches;          /* kernels one call enqueues */
   int vector_width;      /* elements per access: 16-byte vectors, or 1 (scalar path) */
   int threads;           /* threads per CTA */

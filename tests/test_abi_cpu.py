@@ -110,8 +110,9 @@ def test_validation_before_any_launch(gn):
     assert _bwd(gn, dgamma=FAKE * 7, dbeta=FAKE * 7) == INV
     assert _bwd(gn, ws_bytes=0) == WS
     assert _bwd(gn, C=0) == 0
-    ws_need = gn.workspace_size(1, 2, 8, 16, 2, "nhwc", "f16")
-    assert _bwd(gn, ws_bytes=ws_need - 1) == WS
+    need = gn.plan_info(1, 2, 8, 16, 2, "nhwc", "f16", aligned=True).workspace_bytes
+    assert need <= gn.workspace_size(1, 2, 8, 16, 2, "nhwc", "f16")
+    assert _bwd(gn, ws_bytes=need - 1) == WS
 
 
 def test_plan_vector_width_and_modes(gn):
@@ -126,6 +127,21 @@ def test_plan_vector_width_and_modes(gn):
         d = gn.plan_info(1, w.N, w.C, w.HW, w.G, w.layout, w.dtype)
         assert 0 < d.ctas < 2 ** 31
         assert d.threads % 32 == 0 or w.layout == "nhwc"
+
+
+def test_regime_choice(gn):
+    # the 512 MiB single-sample workload is too large for a cluster to hold
+    assert gn.plan_info(0, 1, 128, 2048 * 1024, 16, "nhwc", "f16").regime == 0
+    # misaligned inputs (scalar path) always take the two-kernel path
+    assert gn.plan_info(0, 2, 64, 2304, 8, "nchw", "f32", aligned=False).regime == 0
+    gn.set_regime(gn.REGIME_TWO_KERNEL)
+    try:
+        d = gn.plan_info(1, 8, 320, 4096, 32, "nhwc", "bf16")
+        assert d.regime == 0 and d.launches == 2
+    finally:
+        gn.set_regime(gn.REGIME_AUTO)
+    with pytest.raises(gn.GnError):
+        gn.set_regime(7)
 
 
 def test_configs_cover_both_layouts_and_vector_paths(gn):

@@ -45,6 +45,23 @@ def _small_cases():
 
 SMALL = _small_cases()
 
+# Slices larger than shared memory: the resident regime streams part of each
+# slice through its ring and reads it again in the second pass.
+STREAMING = [
+    ("fp32_nchw_1x16x512x512_g2_stream", synth.WORKLOADS[3].scaled(name="st3", N=1, C=16, G=2)),
+    ("bf16_nhwc_2x320x64x64_g32_stream_bwd", synth.WORKLOADS[2].scaled(name="st2", N=2)),
+    ("fp16_nchw_2x8x300x300_g1_stream", synth.WORKLOADS[1].scaled(name="st1", layout="nchw", N=2, C=8, G=1, H=300, W=300)),
+]
+
+
+@pytest.fixture(params=["auto", "two_kernel"])
+def regime(request):
+    """Runs a test with the automatic kernel choice and with the two-kernel
+    path forced, so both families see every case."""
+    gn.set_regime(gn.REGIME_AUTO if request.param == "auto" else gn.REGIME_TWO_KERNEL)
+    yield request.param
+    gn.set_regime(gn.REGIME_AUTO)
+
 
 def _oracle_full(inp, w):
     o = oracle.get()
@@ -80,15 +97,15 @@ def _compare(got, ref, w):
         checks.assert_param("dbeta", got["dbeta"], ref["dbeta"])
 
 
-@pytest.mark.parametrize("name,w", SMALL, ids=[c[0] for c in SMALL])
-def test_small_parity(name, w):
+@pytest.mark.parametrize("name,w", SMALL + STREAMING, ids=[c[0] for c in SMALL + STREAMING])
+def test_small_parity(name, w, regime):
     inp = synth.make_inputs(w, "cpu", seed=0)
     got = _gpu_run(inp, w)
     _compare(got, _oracle_full(inp, w), w)
 
 
-@pytest.mark.parametrize("name,w", SMALL[:6], ids=[c[0] for c in SMALL[:6]])
-def test_bit_identical_runs(name, w):
+@pytest.mark.parametrize("name,w", SMALL[:6] + STREAMING[:2], ids=[c[0] for c in SMALL[:6] + STREAMING[:2]])
+def test_bit_identical_runs(name, w, regime):
     inp = synth.make_inputs(w, "cpu", seed=1)
     a = _gpu_run(inp, w)
     b = _gpu_run(inp, w)
@@ -98,7 +115,7 @@ def test_bit_identical_runs(name, w):
 
 
 @pytest.mark.parametrize("name,w", [SMALL[1], SMALL[3], SMALL[0]], ids=["nhwc", "nchw_m0", "nchw_m1"])
-def test_no_affine_and_output_mask(name, w):
+def test_no_affine_and_output_mask(name, w, regime):
     inp = synth.make_inputs(w, "cpu", seed=2)
     got = _gpu_run(inp, w, gamma=False, beta=False, params=False)
     o = oracle.get()
@@ -145,7 +162,7 @@ def test_misaligned_pointers_take_scalar_path(name, w):
 
 
 @pytest.mark.parametrize("name,w", [SMALL[2], SMALL[3]], ids=["nhwc", "nchw"])
-def test_in_place(name, w):
+def test_in_place(name, w, regime):
     """y may overwrite x, and dx may overwrite dy."""
     inp = synth.make_inputs(w, "cpu", seed=4)
     ref = _oracle_full(inp, w)
@@ -168,7 +185,7 @@ def test_in_place(name, w):
     checks.assert_param("dgamma", dg, ref["dgamma"])
 
 
-def test_workspace_reuse_and_canaries():
+def test_workspace_reuse_and_canaries(regime):
     """A workspace zero-filled once serves repeated calls of both ops, its
     scratch part may hold anything, and nothing is written past the end of the
     workspace or of any output."""
@@ -203,12 +220,14 @@ def test_workspace_reuse_and_canaries():
     torch.cuda.synchronize()
     assert torch.equal(wsb[n_ws:], canary_ws)
     assert torch.all(ws[:4 * (w.N + 1)] == 0), "arrival counters not returned to zero"
+    err_off = (4 * (w.N + 1) + 255) // 256 * 256
+    assert int(ws[err_off:err_off + 4].view(torch.int32).item()) == 0, "a bounded wait ran out"
     for b in (yb, dxb, mb, rb, gb, bb):
         assert torch.all(b[:pad] == 7.0) and torch.all(b[-pad:] == 7.0)
     _compare(dict(y=y, mean=mean, rstd=rstd, dx=dx, dgamma=dg, dbeta=db), ref, w)
 
 
-def test_shared_workspace_across_shapes():
+def test_shared_workspace_across_shapes(regime):
     """Calls of different shapes in a row on one workspace stay correct."""
     dev = "cuda"
     cases = [SMALL[0][1], SMALL[2][1], SMALL[3][1], SMALL[2][1]]
@@ -237,7 +256,7 @@ def test_zero_extents():
     assert torch.all(dg == 0) and torch.all(db == 0)
 
 
-def test_constant_group_gives_beta():
+def test_constant_group_gives_beta(regime):
     """A constant group: xhat = 0, so y = beta and rstd = 1/sqrt(eps)."""
     w = SMALL[0][1]
     inp = synth.make_inputs(w, "cpu", seed=6)
@@ -257,16 +276,23 @@ def _sample_offsets(w, k=4096, seed=0):
     return np.unique(np.concatenate([idx, edge])).astype(np.int64)
 
 
-@pytest.mark.parametrize("w", synth.WORKLOADS[1:], ids=[w.name for w in synth.WORKLOADS[1:]])
-def test_full_size_sampled(w):
+FULL = [(w, "auto") for w in synth.WORKLOADS[1:]] + [(synth.WORKLOADS[3], "two_kernel")]
+
+
+@pytest.mark.parametrize("w,reg", FULL, ids=[f"{w.name}-{r}" for w, r in FULL])
+def test_full_size_sampled(w, reg):
     """The benchmarked workloads at full size: y and dx at sampled offsets and
     mean/rstd/dgamma/dbeta in full, against the oracle; plus a bit-identical
     rerun.  Large NCHW inputs are handed to the oracle one sample at a time
     (the statistics of sample n depend on sample n only)."""
     dev = "cuda"
-    inp = synth.make_inputs(w, dev, seed=0)
-    got = _gpu_run(inp, w)
-    again = _gpu_run(inp, w)
+    gn.set_regime(gn.REGIME_AUTO if reg == "auto" else gn.REGIME_TWO_KERNEL)
+    try:
+        inp = synth.make_inputs(w, dev, seed=0)
+        got = _gpu_run(inp, w)
+        again = _gpu_run(inp, w)
+    finally:
+        gn.set_regime(gn.REGIME_AUTO)
     for k in ("y", "dx"):
         assert torch.equal(got[k].view(torch.uint8) if got[k].dtype != torch.float32 else got[k],
                            again[k].view(torch.uint8) if again[k].dtype != torch.float32 else again[k]), k
