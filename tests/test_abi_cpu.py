@@ -121,8 +121,13 @@ def test_plan_vector_width_and_modes(gn):
     assert gn.plan_info(0, 2, 6, 77, 3, "nhwc", "f16").vector_width == 1       # C*2 % 16 != 0
     assert gn.plan_info(0, 2, 64, 2303, 8, "nchw", "f32").vector_width == 1    # HW*4 % 16 != 0
     assert gn.plan_info(0, 2, 64, 2304, 8, "nchw", "f32").vector_width == 4
-    assert gn.plan_info(0, 2, 32, 256, 8, "nchw", "f32").threads == 256         # small planes: warp per plane
-    assert gn.plan_info(0, 2, 64, 4096, 8, "nchw", "f32").threads == 512        # large planes: CTA per chunk
+    gn.set_regime(gn.REGIME_TWO_KERNEL)
+    try:
+        # two-kernel path: small planes get a warp each, large planes a CTA per chunk
+        assert gn.plan_info(0, 2, 32, 256, 8, "nchw", "f32").threads == 256
+        assert gn.plan_info(0, 2, 64, 4096, 8, "nchw", "f32").threads == 512
+    finally:
+        gn.set_regime(gn.REGIME_AUTO)
     for w in synth.WORKLOADS:
         d = gn.plan_info(1, w.N, w.C, w.HW, w.G, w.layout, w.dtype)
         assert 0 < d.ctas < 2 ** 31
