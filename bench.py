@@ -44,10 +44,37 @@ def min_bytes(w):
     return {"fwd": 2 * e, "bwd": 3 * e}
 
 
-def kernel_bytes(w):
-    """Algorithmic bytes of each kernel (what it must move at least)."""
+def kernel_bytes(w, fwd_launches=2, bwd_launches=2):
+    """Algorithmic bytes of each kernel (what it must move at least).  The
+    two-kernel path reads its input twice by construction; the resident path
+    runs one kernel per op that moves the op's minimal traffic."""
     e = w.E * esize(w.dtype)
-    return {"fwd_stats": e, "fwd_apply": 2 * e, "bwd_reduce": 2 * e, "bwd_dx": 3 * e}
+    kb = {}
+    if fwd_launches == 2:
+        kb.update({"fwd_stats": e, "fwd_apply": 2 * e})
+    else:
+        kb["fwd_resident"] = 2 * e
+    if bwd_launches == 2:
+        kb.update({"bwd_reduce": 2 * e, "bwd_dx": 3 * e})
+    else:
+        kb["bwd_resident"] = 3 * e
+    return kb
+
+
+def kernel_times(kb, ev):
+    """Per-kernel ms from the six events of one step (fwd: 0-2, bwd: 3-5)."""
+    t = {}
+    if "fwd_stats" in kb:
+        t["fwd_stats"] = ev[0].elapsed_time(ev[1])
+        t["fwd_apply"] = ev[1].elapsed_time(ev[2])
+    else:
+        t["fwd_resident"] = ev[0].elapsed_time(ev[2])
+    if "bwd_reduce" in kb:
+        t["bwd_reduce"] = ev[3].elapsed_time(ev[4])
+        t["bwd_dx"] = ev[4].elapsed_time(ev[5])
+    else:
+        t["bwd_resident"] = ev[3].elapsed_time(ev[5])
+    return t
 
 
 def load_peaks():
@@ -238,20 +265,22 @@ def time_configs(gn, synth, torch, flush, names=None, reps=20):
             assert gn.bwd_raw(dy, x, mean, rstd, gm, w.N, w.C, w.HW, w.G, w.layout, dx, dg, db, ws, stream) == 0
             gn.set_timing_events()
         torch.cuda.synchronize()
-        rec = {"fwd": [], "bwd": [], "fwd_stats": [], "fwd_apply": [], "bwd_reduce": [], "bwd_dx": []}
+        pf = gn.plan_info(0, w.N, w.C, w.HW, w.G, w.layout, w.dtype)
+        pb = gn.plan_info(1, w.N, w.C, w.HW, w.G, w.layout, w.dtype)
+        kb = kernel_bytes(w, pf.launches, pb.launches)
+        rec = {"fwd": [], "bwd": []}
         for ev in evs[3:]:
             rec["fwd"].append(ev[0].elapsed_time(ev[2]))
-            rec["fwd_stats"].append(ev[0].elapsed_time(ev[1]))
-            rec["fwd_apply"].append(ev[1].elapsed_time(ev[2]))
             rec["bwd"].append(ev[3].elapsed_time(ev[5]))
-            rec["bwd_reduce"].append(ev[3].elapsed_time(ev[4]))
-            rec["bwd_dx"].append(ev[4].elapsed_time(ev[5]))
+            for k, v in kernel_times(kb, ev).items():
+                rec.setdefault(k, []).append(v)
         mb = min_bytes(w)
         med = {k: statistics.median(v) for k, v in rec.items()}
         fwd_gbs = mb["fwd"] / (med["fwd"] * 1e-3) / 1e9
         bwd_gbs = mb["bwd"] / (med["bwd"] * 1e-3) / 1e9
-        kb = kernel_bytes(w)
         out[w.name] = {
+            "regime": {"fwd": "resident" if pf.launches == 1 else "two-kernel",
+                       "bwd": "resident" if pb.launches == 1 else "two-kernel"},
             "fwd_us": round(med["fwd"] * 1e3, 2), "bwd_us": round(med["bwd"] * 1e3, 2),
             "fwd_gbs": round(fwd_gbs, 1), "bwd_gbs": round(bwd_gbs, 1),
             "fwd_frac": round(fwd_gbs / peak, 4), "bwd_frac": round(bwd_gbs / peak, 4),
@@ -386,12 +415,13 @@ def run_ours(args, rank, world, local_rank):
     clk = clocks.stop() if rank == 0 else None
 
     per_step = [e[0].elapsed_time(e[5]) for e in evs]          # ms, fwd start -> bwd end
-    kern = {
-        "fwd_stats": [e[0].elapsed_time(e[1]) for e in evs],
-        "fwd_apply": [e[1].elapsed_time(e[2]) for e in evs],
-        "bwd_reduce": [e[3].elapsed_time(e[4]) for e in evs],
-        "bwd_dx": [e[4].elapsed_time(e[5]) for e in evs],
-    }
+    plan_f = gn.plan_info(0, w.N, w.C, w.HW, w.G, w.layout, w.dtype)
+    plan_b = gn.plan_info(1, w.N, w.C, w.HW, w.G, w.layout, w.dtype)
+    kb = kernel_bytes(w, plan_f.launches, plan_b.launches)
+    kern = {}
+    for e in evs:
+        for k, v in kernel_times(kb, e).items():
+            kern.setdefault(k, []).append(v)
     step_sum = torch.tensor([sum(per_step)], dtype=torch.float64, device=dev)
     if world > 1:
         dist.all_reduce(step_sum, op=dist.ReduceOp.MAX)
@@ -410,13 +440,10 @@ def run_ours(args, rank, world, local_rank):
         return 0
 
     peak, peak_kind = load_peaks()
-    kb = kernel_bytes(w)
     totals = {k: sum(v) for k, v in kern.items()}
     dom = max(totals, key=totals.get)
     avg_ms = totals[dom] / K
     achieved = kb[dom] / (avg_ms * 1e-3) / 1e9
-    plan_f = gn.plan_info(0, w.N, w.C, w.HW, w.G, w.layout, w.dtype)
-    plan_b = gn.plan_info(1, w.N, w.C, w.HW, w.G, w.layout, w.dtype)
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": traffic_from_profiles(dom),
                 "kernel": dom, "peak_kind": peak_kind,

@@ -200,7 +200,8 @@ def test_workspace_reuse_and_canaries(regime):
     wsb = torch.randint(0, 256, (n_ws + 256,), dtype=torch.uint8, device=dev)
     canary_ws = wsb[n_ws:].clone()
     ws = wsb[:n_ws]
-    ws[:256].zero_()  # the arrival counters (the rest is scratch)
+    err_off = (4 * (w.N + 1) + 255) // 256 * 256
+    ws[:err_off + 4].zero_()  # arrival counters and error word (the rest is scratch)
 
     def padded(n, dtype):
         b = torch.full((n + 2 * pad,), 7.0, dtype=dtype, device=dev)
@@ -220,7 +221,6 @@ def test_workspace_reuse_and_canaries(regime):
     torch.cuda.synchronize()
     assert torch.equal(wsb[n_ws:], canary_ws)
     assert torch.all(ws[:4 * (w.N + 1)] == 0), "arrival counters not returned to zero"
-    err_off = (4 * (w.N + 1) + 255) // 256 * 256
     assert int(ws[err_off:err_off + 4].view(torch.int32).item()) == 0, "a bounded wait ran out"
     for b in (yb, dxb, mb, rb, gb, bb):
         assert torch.all(b[:pad] == 7.0) and torch.all(b[-pad:] == 7.0)
