@@ -211,6 +211,19 @@ int gn_plan_info(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout
   out->ctas = g.regime == gn::kRegimeResident ? g.units * g.K : g.items;
   out->partials = g.N * g.C * g.Tp;
   out->workspace_bytes = gn::ws_layout(op, g).total;
+  out->cluster_ctas = g.regime == gn::kRegimeResident ? g.K : g.cl;
+  const int64_t mc = gn::plan_max_clusters(g, op);
+  out->max_clusters = mc > 0 ? (int)mc : 0;
+  if (g.regime == gn::kRegimeResident) {
+    out->smem_bytes = g.smem;
+  } else {
+    size_t sm = 0;
+    if (g.layout == GN_LAYOUT_NHWC)
+      gn::nhwc_first_kernel(g, op == GN_OP_BWD, &sm);
+    else
+      gn::nchw_first_kernel(g, op == GN_OP_BWD, &sm);
+    out->smem_bytes = sm;
+  }
   return GN_OK;
 }
 

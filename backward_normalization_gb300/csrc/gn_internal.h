@@ -93,6 +93,8 @@ struct KParams {
 
 // plan.cpp
 int device_sm_count();
+// Co-resident clusters of the plan's first (or only) kernel (-1: no device).
+int64_t plan_max_clusters(const Geom& g, int op);
 // Test hook: force a regime (kRegimeAuto = automatic choice).
 void set_regime_override(int regime);
 // CTAs of the op's first kernel that fit on the current device at once when

@@ -190,6 +190,12 @@ bool plan_resident(Geom& g, int op) {
 }
 }  // namespace
 
+int64_t plan_max_clusters(const Geom& g, int op) {
+  if (g.regime == kRegimeResident) return resident_clusters(g, op);
+  const int64_t r = resident_first_ctas(g, op, g.cl);
+  return r > 0 ? r / g.cl : -1;
+}
+
 int device_sm_count() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) {

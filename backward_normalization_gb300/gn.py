@@ -38,7 +38,8 @@ class PlanDesc(ctypes.Structure):
     _fields_ = [("regime", ctypes.c_int), ("launches", ctypes.c_int),
                 ("vector_width", ctypes.c_int), ("threads", ctypes.c_int),
                 ("ctas", ctypes.c_int64), ("partials", ctypes.c_int64),
-                ("workspace_bytes", ctypes.c_size_t)]
+                ("workspace_bytes", ctypes.c_size_t), ("cluster_ctas", ctypes.c_int),
+                ("max_clusters", ctypes.c_int), ("smem_bytes", ctypes.c_size_t)]
 
 
 _lib = None

@@ -145,6 +145,9 @@ typedef struct gn_plan_desc {
   int64_t ctas;          /* CTAs per kernel */
   int64_t partials;      /* fp32 partial-sum records written per call */
   size_t workspace_bytes;
+  int cluster_ctas;      /* CTAs per thread-block cluster of the first (or only) kernel */
+  int max_clusters;      /* such clusters that fit on the device at once (0: unknown) */
+  size_t smem_bytes;     /* dynamic shared memory per CTA of that kernel */
 } gn_plan_desc;
 
 /* Fills *out with the plan of gn_fwd/gn_bwd for this problem, assuming every
