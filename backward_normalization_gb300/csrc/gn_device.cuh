@@ -249,6 +249,16 @@ __device__ __forceinline__ void tma_load_1d(void* dst, const void* src, uint32_t
       "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(pol)
       : "memory");
 }
+// One 2-D tile [rows x cols] at (col c0, row r0) of the tensor map -> shared
+// memory (rows packed, no swizzle), completing on `bar`.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int32_t c0,
+                                            int32_t r0, uint64_t* bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(r0), "r"(smem_addr(bar)), "l"(pol)
+      : "memory");
+}
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(

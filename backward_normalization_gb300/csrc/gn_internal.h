@@ -2,6 +2,7 @@
 // by the C-ABI layer and the kernels.  Not part of the public interface.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -55,8 +56,11 @@ struct Geom {
   int64_t m;           // NCHW: pieces per channel plane (K = Cg*m)
   int64_t units;       // clusters: N*G (NCHW) or N (NHWC)
   int64_t slice;       // NCHW: elements per piece; NHWC: rows per CTA
-  int64_t chunk;       // NCHW: elements per chunk; NHWC: rows per chunk
-  int64_t chunk_bytes; // bytes of one tensor's chunk
+  int64_t chunk;       // NCHW: elements per chunk; NHWC: rows per chunk (TMA box rows)
+  int64_t Cb;          // NHWC: channels per unit (whole groups); a unit is (n, channel block)
+  int64_t ncbu;        // NHWC: channel blocks per sample (C / Cb)
+  int64_t chunk_bytes; // bytes of one tensor's chunk (the TMA transfer)
+  int64_t ten_stride;  // bytes between a slot's x and dy parts (chunk_bytes rounded up to 128)
   int nres, S;         // resident chunk slots, ring slots
   size_t smem;         // dynamic shared memory bytes
   size_t off_ring, off_red, off_xch, off_tot, off_grp, off_bar;
@@ -73,6 +77,8 @@ struct WsLayout {
 };
 
 struct KParams {
+  CUtensorMap tmx;   // resident NHWC: 2-D [N*HW, C] views of x and dy for TMA tiles
+  CUtensorMap tmdy;
   Geom g;
   const void* x;
   const void* dy;

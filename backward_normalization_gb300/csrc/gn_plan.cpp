@@ -59,10 +59,12 @@ cudaError_t prepare_resident_kernel(const void* kernel, const Geom& g) {
 
 namespace {
 constexpr size_t kSmemPerCta = 227 * 1024 - 1024;  // dynamic smem budget (static use ~1 KB)
-constexpr int64_t kMaxUnitBytes = 32ll << 20;       // per-unit input (x, or x + dy)
-constexpr int64_t kChunkBytes = 16 * 1024;
+constexpr size_t kSmallSlice = 88 * 1024;           // slice that lets two CTAs share an SM
+constexpr int64_t kMaxUnitBytes = 16ll << 20;       // per-unit input (x, or x + dy)
+constexpr int kRingDeep = 8;                        // ring slots when a slice streams
 
 size_t a128(size_t v) { return (v + 127) & ~size_t(127); }
+int64_t gcd64(int64_t a, int64_t b) { return b ? gcd64(b, a % b) : a; }
 
 // Clusters of the resident kernel that fit on the device at once (0 if none,
 // -1 when no device is visible).
@@ -105,64 +107,68 @@ bool plan_resident(Geom& g, int op) {
   if (g.vw != vec) return false;
   Geom r = g;
   size_t red_f, xch_f, tot_f, grp_f;
-  int64_t slice_elems, chunk_elems;
+  int64_t nch;  // chunks per slice
   if (g.layout == kNCHW) {
     if (g.Cg > 16) return false;
-    const int64_t unit_bytes = g.Cg * g.HW * esz * nten;
-    if (unit_bytes > kMaxUnitBytes) return false;
+    if (g.Cg * g.HW * esz * nten > kMaxUnitBytes) return false;
+    const int64_t cbytes = op == kBwd ? 8 * 1024 : 16 * 1024;
     int64_t m = 16 / g.Cg;
-    while (m > 1 && g.HW * esz / m < 2 * kChunkBytes) m /= 2;
+    while (m > 1 && g.HW * esz / m < 2 * cbytes) m /= 2;
     r.m = m;
     r.K = (int)(g.Cg * m);
     r.tpb = 512;
     r.slice = rup(cdiv(g.HW, m), vec);
-    r.chunk = kChunkBytes / esz;
-    r.chunk_bytes = kChunkBytes;
+    r.chunk = cbytes / esz;
+    r.chunk_bytes = cbytes;
     r.units = g.N * g.G;
-    slice_elems = r.slice;
-    chunk_elems = r.chunk;
+    nch = cdiv(r.slice, r.chunk);
     red_f = 2 * (size_t)r.tpb;
     xch_f = 2;
     tot_f = 0;
     grp_f = 2;
   } else {
-    const int64_t V = g.C / vec;
-    if (V > 512) return false;
-    const int64_t unit_bytes = g.HW * g.C * esz * nten;
-    if (unit_bytes > kMaxUnitBytes) return false;
+    // channel block: whole groups, whole 16-byte vectors, at most 128 channels
+    // when possible (TMA boxes hold at most 256 elements per dimension)
+    const int64_t step = g.Cg / gcd64(g.Cg, vec) * vec;
+    int64_t cb = 0;
+    for (int64_t c = step; c <= g.C && c <= 256; c += step)
+      if (g.C % c == 0 && (c <= 128 || cb == 0)) cb = c;
+    if (cb == 0) return false;
+    if (g.HW * cb * esz * nten > kMaxUnitBytes) return false;
+    if (g.N * g.HW > 0x7fffffffLL) return false;  // TMA row coordinates are 32-bit
+    r.Cb = cb;
+    r.ncbu = g.C / cb;
     r.ncb = 1;
-    r.Wv = (int)V;
-    r.rpi = (int)(512 / V);
+    r.Wv = (int)(cb / vec);
+    r.rpi = 256 / r.Wv > 0 ? 256 / r.Wv : 1;
     r.tpb = r.Wv * r.rpi;
-    const int64_t row_bytes = g.C * esz;
-    r.chunk = kChunkBytes / row_bytes > 0 ? kChunkBytes / row_bytes : 1;
-    r.chunk_bytes = r.chunk * row_bytes;
-    r.units = g.N;
-    red_f = 2 * (size_t)vec * r.tpb;
-    xch_f = 2 * (size_t)g.C;
-    tot_f = 2 * (size_t)g.C;
-    grp_f = 2 * (size_t)g.G;
-    chunk_elems = r.chunk * g.C;
-    // smallest power-of-two K whose slices fit the chunk budget (at most 16)
-    const size_t fixed = a128(red_f * 4) + a128(xch_f * 4) + a128(tot_f * 4) + a128(grp_f * 4) + 1024;
-    const size_t budget = kSmemPerCta > fixed ? kSmemPerCta - fixed : 0;
+    const int64_t row_bytes = cb * esz;
+    r.units = g.N * r.ncbu;
     r.K = 1;
-    while (r.K < 16 && (size_t)(cdiv(cdiv(g.HW, r.K), r.chunk) * r.chunk_bytes * nten) > budget) r.K *= 2;
+    while (r.K < 16 && (size_t)(cdiv(g.HW, r.K) * row_bytes * nten) > kSmallSlice) r.K *= 2;
     r.slice = cdiv(g.HW, r.K);
-    slice_elems = r.slice * g.C;
+    // chunks of at most 16 KB (and 256 rows, the TMA box limit) that tile the
+    // slice evenly
+    const int64_t max_rows = clamp64((16 * 1024) / row_bytes, 1, 256);
+    nch = cdiv(r.slice, max_rows);
+    r.chunk = cdiv(r.slice, nch);
+    r.chunk_bytes = r.chunk * row_bytes;
+    red_f = 2 * (size_t)vec * r.tpb;
+    xch_f = 2 * (size_t)cb;
+    tot_f = 2 * (size_t)cb;
+    grp_f = 2 * (size_t)(cb / g.Cg);
   }
   const size_t fixed = a128(red_f * 4) + a128(xch_f * 4) + a128(tot_f * 4) + a128(grp_f * 4);
-  const size_t slot = (size_t)r.chunk_bytes * nten;
-  const int64_t nch = cdiv(slice_elems, chunk_elems);
-  if (kSmemPerCta < fixed + 512) return false;
-  // slots left after the fixed areas and one mbarrier per slot
-  int64_t slots = (int64_t)((kSmemPerCta - fixed - 512) / (slot + 8));
+  r.ten_stride = (int64_t)a128((size_t)r.chunk_bytes);
+  const size_t slot = (size_t)r.ten_stride * nten;
+  if (kSmemPerCta < fixed + 1024) return false;
+  const int64_t slots = (int64_t)((kSmemPerCta - fixed - 512) / (slot + 8));
   if (nch <= slots) {
     r.nres = (int)nch;
     r.S = 0;
   } else {
     if (slots < 3) return false;
-    r.S = 2;
+    r.S = (int)(slots - 1 < kRingDeep ? slots - 1 : kRingDeep);
     r.nres = (int)(slots - r.S);
   }
   size_t off = 0;
@@ -179,7 +185,7 @@ bool plan_resident(Geom& g, int op) {
   off += a128(grp_f * 4);
   r.off_bar = off;
   off += a128(8 * (size_t)(r.nres + r.S));
-  r.smem = off;
+  r.smem = off + 128;  // slack for aligning the dynamic shared memory base
   if (r.smem > kSmemPerCta) return false;
   if (r.units * r.K > 0x7fffffffLL) return false;
   r.regime = kRegimeResident;

@@ -1,13 +1,14 @@
 // gn_resident.cu -- the cluster-resident regime: one kernel per op.
 //
-// A thread-block cluster of K CTAs owns one reduction unit -- one (n, g)
-// span for NCHW (Cg channel planes, contiguous), one sample n for NHWC (HW
-// rows of C channels, contiguous) -- and each CTA owns one contiguous slice of
-// it (NCHW: 1/m of one channel plane, K = Cg*m; NHWC: HW/K rows).
+// A thread-block cluster of K CTAs owns one reduction unit made of whole
+// groups: for NCHW one (n, g) span (Cg channel planes, contiguous), for NHWC
+// one (sample n, block of Cb channels) -- HW rows of Cb channels, read as 2-D
+// TMA tiles from a [N*HW, C] view.  Each CTA owns a contiguous slice of the
+// unit (NCHW: 1/m of one channel plane, K = Cg*m; NHWC: HW/K rows).
 //
-//   pass 1  TMA bulk copies bring the slice into shared memory in chunks: the
+//   pass 1  TMA copies bring the slice into shared memory in chunks: the
 //           first nres chunks into slots of their own (all issued at once),
-//           the rest through an S-slot ring.  Every chunk is folded into the
+//           the rest through an S-slot ring.  Each chunk is folded into the
 //           per-channel (NHWC) or per-slice (NCHW) sums as it lands.
 //   reduce  CTA tree, then every CTA adds the K partials of the cluster in
 //           rank order through DSMEM, so all CTAs hold identical statistics.
@@ -23,58 +24,75 @@
 // Every mbarrier wait is bounded.  A wait that runs out raises the workspace
 // error word; the CTA then stops computing, still takes part in every cluster
 // barrier, and before exiting waits (bounded) for the copies it issued.
+#include <cudaTypedefs.h>
+
 #include "gn_finalize.cuh"
 
 namespace gn {
 namespace {
 
-struct ResCtx {
-  const Geom& g;
-  char* res;
-  char* ring;
-  float* red;
-  float* xch;
-  float* tot;
-  float* grp;
-  uint64_t* bar;
-  int* abort_flag;
-};
-
-__device__ __forceinline__ bool res_wait(const ResCtx& c, uint64_t* bar, uint32_t parity,
+__device__ __forceinline__ bool res_wait(int* abort_flag, uint64_t* bar, uint32_t parity,
                                          unsigned* err) {
-  if (*reinterpret_cast<volatile int*>(c.abort_flag)) return false;
+  if (*reinterpret_cast<volatile int*>(abort_flag)) return false;
   if (mbar_wait(bar, parity, err)) return true;
-  *reinterpret_cast<volatile int*>(c.abort_flag) = 1;
+  *reinterpret_cast<volatile int*>(abort_flag) = 1;
   return false;
+}
+
+// Sum of a float2 held at `local + 2*idx` in every CTA of the cluster, in
+// rank order (at most 16 ranks; the remote loads are all issued first).
+__device__ __forceinline__ float2 cluster_sum_at(cg::cluster_group& cluster, float* local,
+                                                 int64_t idx, int K) {
+  float2 v[16];
+#pragma unroll
+  for (int r = 0; r < 16; ++r) {
+    if (r < K) {
+      const float* rem = cluster.map_shared_rank(local, r);
+      v[r] = *reinterpret_cast<const float2*>(rem + 2 * idx);
+    } else {
+      v[r] = make_float2(0.f, 0.f);
+    }
+  }
+  float2 s = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int r = 0; r < 16; ++r) {
+    s.x += v[r].x;
+    s.y += v[r].y;
+  }
+  return s;
 }
 
 template <typename T, int VW, int LAYOUT, bool BWD>
 __global__ void __launch_bounds__(512, 1) resident_kernel(const __grid_constant__ KParams p) {
-  extern __shared__ __align__(128) char smem[];
+  extern __shared__ __align__(128) char smem_raw[];
+  // TMA tile destinations need 128-byte alignment: align the base here (the
+  // plan reserves 128 bytes of slack)
+  char* smem = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
   const Geom& g = p.g;
   constexpr int ESZ = sizeof(T);
-  constexpr int NT_TENS = BWD ? 2 : 1;
+  constexpr int NTEN = BWD ? 2 : 1;
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
   const int64_t unit = blockIdx.x / g.K;
   const int tid = threadIdx.x, nt = blockDim.x;
   __shared__ int s_abort;
 
-  ResCtx cx{g,
-            smem,
-            smem + g.off_ring,
-            reinterpret_cast<float*>(smem + g.off_red),
-            reinterpret_cast<float*>(smem + g.off_xch),
-            reinterpret_cast<float*>(smem + g.off_tot),
-            reinterpret_cast<float*>(smem + g.off_grp),
-            reinterpret_cast<uint64_t*>(smem + g.off_bar),
-            &s_abort};
+  char* res = smem;
+  char* ring = smem + g.off_ring;
+  float* red = reinterpret_cast<float*>(smem + g.off_red);
+  float* xch = reinterpret_cast<float*>(smem + g.off_xch);
+  float* tot = reinterpret_cast<float*>(smem + g.off_tot);
+  float* grp = reinterpret_cast<float*>(smem + g.off_grp);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + g.off_bar);
   const T* x = static_cast<const T*>(p.x);
   const T* dy = static_cast<const T*>(p.dy);
   T* out = static_cast<T*>(p.out);
 
-  // ---- this CTA's slice [e0, e1) of the flat tensor
-  int64_t n, e0, e1, chan = 0;
+  // ---- this CTA's slice
+  // NCHW: elements [e0, e1) of one channel plane.  NHWC: rows [r0, r1) of
+  // sample n, channels [cbase, cbase + Cb).
+  int64_t n, e0 = 0, e1 = 0, chan = 0, r0 = 0, r1 = 0, cbase = 0, ngrp0;
+  int nch;
   if (LAYOUT == kNCHW) {
     n = unit / g.G;
     const int64_t gi = unit % g.G;
@@ -83,73 +101,84 @@ __global__ void __launch_bounds__(512, 1) resident_kernel(const __grid_constant_
     const int64_t h1 = (h0 + g.slice < g.HW) ? h0 + g.slice : g.HW;
     e0 = (n * g.C + chan) * g.HW + h0;
     e1 = (n * g.C + chan) * g.HW + (h1 > h0 ? h1 : h0);
+    nch = (int)((e1 - e0 + g.chunk - 1) / g.chunk);
+    ngrp0 = unit;  // index of the unit's (only) group in mean/rstd
   } else {
-    n = unit;
-    const int64_t r0 = (int64_t)rank * g.slice;
-    const int64_t r1 = (r0 + g.slice < g.HW) ? r0 + g.slice : g.HW;
-    e0 = (n * g.HW + r0) * g.C;
-    e1 = (n * g.HW + (r1 > r0 ? r1 : r0)) * g.C;
+    n = unit / g.ncbu;
+    cbase = (unit % g.ncbu) * g.Cb;
+    r0 = (int64_t)rank * g.slice;
+    r1 = (r0 + g.slice < g.HW) ? r0 + g.slice : g.HW;
+    if (r1 < r0) r1 = r0;
+    nch = (int)((r1 - r0 + g.chunk - 1) / g.chunk);
+    ngrp0 = n * g.G + cbase / g.Cg;
   }
-  const int64_t ce = LAYOUT == kNCHW ? g.chunk : g.chunk * g.C;  // elements per chunk
-  const int nch = (int)((e1 - e0 + ce - 1) / ce);
   const int nres = nch < g.nres ? nch : g.nres;
   const int nstr = nch - nres;
   const int S = g.S;
-  const size_t slot_bytes = (size_t)g.chunk_bytes * NT_TENS;
+  const size_t slot_bytes = (size_t)g.ten_stride * NTEN;  // slots stay 128-byte aligned
 
   if (tid == 0) {
     s_abort = 0;
-    for (int i = 0; i < g.nres + S; ++i) mbar_init(cx.bar + i, 1);
+    for (int i = 0; i < g.nres + S; ++i) mbar_init(bar + i, 1);
     fence_mbar_init();
   }
   __syncthreads();
 
   const uint64_t pol_once = policy_evict_first();  // resident chunks: read once from HBM
   const uint64_t pol_again = policy_evict_last();  // streamed chunks: read again in pass 2
-  // Producer (thread 0): chunk i of the slice into `dst`, completing on `bar`.
-  auto issue = [&](int i, char* dst, uint64_t* bar, uint64_t pol) {
-    const int64_t a = e0 + (int64_t)i * ce;
-    const int64_t b = (a + ce < e1) ? a + ce : e1;
-    const uint32_t bytes = (uint32_t)((b - a) * ESZ);
-    mbar_arrive_expect_tx(bar, bytes * NT_TENS);
-    tma_load_1d(dst, x + a, bytes, bar, pol);
-    if (BWD) tma_load_1d(dst + g.chunk_bytes, dy + a, bytes, bar, pol);
+  // Producer (thread 0): chunk i of the slice into `dst`, completing on `b`.
+  auto issue = [&](int i, char* dst, uint64_t* b, uint64_t pol) {
+    if (LAYOUT == kNCHW) {
+      const int64_t a = e0 + (int64_t)i * g.chunk;
+      const int64_t e = (a + g.chunk < e1) ? a + g.chunk : e1;
+      const uint32_t bytes = (uint32_t)((e - a) * ESZ);
+      mbar_arrive_expect_tx(b, bytes * NTEN);
+      tma_load_1d(dst, x + a, bytes, b, pol);
+      if (BWD) tma_load_1d(dst + g.ten_stride, dy + a, bytes, b, pol);
+    } else {
+      // a full box is always transferred; rows past the slice are ignored
+      const int32_t row = (int32_t)(n * g.HW + r0 + (int64_t)i * g.chunk);
+      mbar_arrive_expect_tx(b, (uint32_t)g.chunk_bytes * NTEN);
+      tma_load_2d(dst, &p.tmx, (int32_t)cbase, row, b, pol);
+      if (BWD) tma_load_2d(dst + g.ten_stride, &p.tmdy, (int32_t)cbase, row, b, pol);
+    }
   };
   // Ring loads are numbered seq = 0 .. 2*nstr-1: pass-1 streamed chunks in
   // order, then the pass-2 reloads newest first.
   auto seq_chunk = [&](int seq) { return seq < nstr ? nres + seq : nch - 1 - (seq - nstr); };
   auto seq_issue = [&](int seq) {
     const int slot = seq % S;
-    issue(seq_chunk(seq), cx.ring + slot * slot_bytes, cx.bar + g.nres + slot,
+    issue(seq_chunk(seq), ring + slot * slot_bytes, bar + g.nres + slot,
           seq < nstr ? pol_again : pol_once);
   };
-  int issued = 0;  // ring loads issued (thread 0's view)
+  int issued = 0;  // ring loads issued (meaningful in thread 0)
   if (tid == 0) {
-    for (int i = 0; i < nres; ++i) issue(i, cx.res + i * slot_bytes, cx.bar + i, pol_once);
+    for (int i = 0; i < nres; ++i) issue(i, res + i * slot_bytes, bar + i, pol_once);
     for (; issued < S && issued < 2 * nstr; ++issued) seq_issue(issued);
   }
 
   // ---- per-thread layout inside a chunk
-  // NHWC: thread (r, j) owns column j (VW channels) and rows r, r+rpi, ...
+  // NHWC: thread (rl, j) owns column j (VW channels of the block) and rows
+  // rl, rl + rpi, ...; NCHW: threads stride the chunk's 16-byte vectors.
   const int j = LAYOUT == kNHWC ? tid % g.Wv : 0;
   const int rl = LAYOUT == kNHWC ? tid / g.Wv : 0;
   const bool col_ok = LAYOUT == kNHWC ? rl < g.rpi : true;
-  float K[VW];  // forward shift: x(n, c, hw = 0) (NHWC per channel, NCHW per group)
-  if (!BWD) {
-    if (LAYOUT == kNHWC) {
-      if (col_ok) Access<T, VW>::load(x + n * g.HW * g.C + j * VW, K, pol_once);
-    } else {
-      const float k0 = Elem<T>::to_f(x[(n * g.C + (unit % g.G) * g.Cg) * g.HW]);
-#pragma unroll
-      for (int k = 0; k < VW; ++k) K[k] = k0;
-    }
-  }
-  float mu[VW];  // backward: the group mean of each owned channel
-  if (BWD) {
+  float K[VW];  // forward shift: x(n, c, hw = 0) per channel (NHWC) or per group (NCHW)
+  float mu[VW];  // backward: group mean of each owned channel
+  if (LAYOUT == kNHWC) {
 #pragma unroll
     for (int k = 0; k < VW; ++k) {
-      const int64_t c = LAYOUT == kNHWC ? (int64_t)j * VW + k : chan;
-      mu[k] = (LAYOUT == kNCHW || col_ok) ? __ldg(p.mean + n * g.G + c / g.Cg) : 0.f;
+      const int64_t c = cbase + (int64_t)j * VW + k;
+      K[k] = (!BWD && col_ok) ? Elem<T>::to_f(x[n * g.HW * g.C + c]) : 0.f;
+      mu[k] = (BWD && col_ok) ? __ldg(p.mean + n * g.G + c / g.Cg) : 0.f;
+    }
+  } else {
+    const float k0 = BWD ? 0.f : Elem<T>::to_f(x[(n * g.C + (unit % g.G) * g.Cg) * g.HW]);
+    const float m0 = BWD ? __ldg(p.mean + unit) : 0.f;
+#pragma unroll
+    for (int k = 0; k < VW; ++k) {
+      K[k] = k0;
+      mu[k] = m0;
     }
   }
   float acc[2 * VW];
@@ -157,18 +186,18 @@ __global__ void __launch_bounds__(512, 1) resident_kernel(const __grid_constant_
   for (int q = 0; q < 2 * VW; ++q) acc[q] = 0.f;
 
   using Raw = typename Access<T, VW>::Raw;
-  // Folds one chunk (at `slot`, chunk index i) into acc.
+  const int64_t rowp = g.Cb * ESZ;  // NHWC: bytes per row in shared memory
+  // Folds chunk i (at `slot`) into acc.
   auto consume = [&](const char* slot, int i) {
-    const int64_t a = e0 + (int64_t)i * ce;
-    const int64_t cnt = ((a + ce < e1) ? a + ce : e1) - a;  // elements
     if (LAYOUT == kNCHW) {
-      const int64_t nv = cnt / VW;
+      const int64_t a = e0 + (int64_t)i * g.chunk;
+      const int64_t nv = (((a + g.chunk < e1) ? a + g.chunk : e1) - a) / VW;
       for (int64_t v = tid; v < nv; v += nt) {
         float xv[VW];
         Access<T, VW>::unpack(*reinterpret_cast<const Raw*>(slot + v * 16), xv);
         if (BWD) {
           float dv[VW];
-          Access<T, VW>::unpack(*reinterpret_cast<const Raw*>(slot + g.chunk_bytes + v * 16), dv);
+          Access<T, VW>::unpack(*reinterpret_cast<const Raw*>(slot + g.ten_stride + v * 16), dv);
 #pragma unroll
           for (int k = 0; k < VW; ++k) {
             acc[0] += dv[k];
@@ -184,14 +213,15 @@ __global__ void __launch_bounds__(512, 1) resident_kernel(const __grid_constant_
         }
       }
     } else if (col_ok) {
-      const int64_t rows = cnt / g.C;
+      const int64_t rs = r0 + (int64_t)i * g.chunk;
+      const int64_t rows = ((rs + g.chunk < r1) ? rs + g.chunk : r1) - rs;
       for (int64_t r = rl; r < rows; r += g.rpi) {
-        const int64_t off = (r * g.C + (int64_t)j * VW) * ESZ;
+        const int64_t off = r * rowp + (int64_t)j * 16;
         float xv[VW];
         Access<T, VW>::unpack(*reinterpret_cast<const Raw*>(slot + off), xv);
         if (BWD) {
           float dv[VW];
-          Access<T, VW>::unpack(*reinterpret_cast<const Raw*>(slot + g.chunk_bytes + off), dv);
+          Access<T, VW>::unpack(*reinterpret_cast<const Raw*>(slot + g.ten_stride + off), dv);
 #pragma unroll
           for (int k = 0; k < VW; ++k) {
             acc[2 * k] += dv[k];
@@ -211,11 +241,11 @@ __global__ void __launch_bounds__(512, 1) resident_kernel(const __grid_constant_
 
   // ---- pass 1
   for (int i = 0; i < nres; ++i)
-    if (res_wait(cx, cx.bar + i, 0, p.err)) consume(cx.res + i * slot_bytes, i);
+    if (res_wait(&s_abort, bar + i, 0, p.err)) consume(res + i * slot_bytes, i);
   for (int seq = 0; seq < nstr; ++seq) {
     const int slot = seq % S;
-    if (res_wait(cx, cx.bar + g.nres + slot, (seq / S) & 1, p.err))
-      consume(cx.ring + slot * slot_bytes, seq_chunk(seq));
+    if (res_wait(&s_abort, bar + g.nres + slot, (seq / S) & 1, p.err))
+      consume(ring + slot * slot_bytes, seq_chunk(seq));
     __syncthreads();  // the slot is free again
     if (tid == 0 && issued < 2 * nstr && !s_abort) {
       fence_proxy_async_smem();
@@ -225,58 +255,52 @@ __global__ void __launch_bounds__(512, 1) resident_kernel(const __grid_constant_
 
   // ---- reduce: CTA, then cluster (every CTA sums the K partials in rank order)
   if (LAYOUT == kNCHW) {
-    const float2 t = block_sum2_t0(acc[0], acc[1], cx.red);
+    const float2 t = block_sum2_t0(acc[0], acc[1], red);
     if (tid == 0) {
-      cx.xch[0] = t.x;
-      cx.xch[1] = t.y;
+      xch[0] = t.x;
+      xch[1] = t.y;
     }
   } else {
-    const int tpb = nt;
 #pragma unroll
-    for (int q = 0; q < 2 * VW; ++q) cx.red[q * tpb + tid] = acc[q];
+    for (int q = 0; q < 2 * VW; ++q) red[q * nt + tid] = acc[q];
     __syncthreads();
     for (int s = 1; s < g.rpi; s <<= 1) {
       if (col_ok && (rl % (2 * s)) == 0 && rl + s < g.rpi) {
 #pragma unroll
-        for (int q = 0; q < 2 * VW; ++q) cx.red[q * tpb + tid] += cx.red[q * tpb + tid + s * g.Wv];
+        for (int q = 0; q < 2 * VW; ++q) red[q * nt + tid] += red[q * nt + tid + s * g.Wv];
       }
       __syncthreads();
     }
     if (rl == 0) {
 #pragma unroll
       for (int k = 0; k < VW; ++k) {
-        cx.xch[2 * (j * VW + k)] = cx.red[(2 * k) * tpb + tid];
-        cx.xch[2 * (j * VW + k) + 1] = cx.red[(2 * k + 1) * tpb + tid];
+        xch[2 * (j * VW + k)] = red[(2 * k) * nt + tid];
+        xch[2 * (j * VW + k) + 1] = red[(2 * k + 1) * nt + tid];
       }
     }
   }
   cluster.sync();
 
-  // Per-thread output constants: y = (x - mu)*a + b, or
-  // dx = A*dy + B*(x - mu) + D.
+  // Per-thread output constants: y = (x - cm)*ca + cb, or
+  // dx = ca*dy + cb*(x - cm) + cd.
   float ca[VW], cb[VW], cm[VW], cd[VW];
   const float hwf = (float)g.HW;
   const float mf = (float)(g.Cg * g.HW);
   if (LAYOUT == kNCHW) {
     if (tid == 0) {
       if (!BWD) {
-        float s = 0.f, q = 0.f;
-        for (int r = 0; r < g.K; ++r) {
-          const float* rem = cluster.map_shared_rank(cx.xch, r);
-          s += rem[0];
-          q += rem[1];
-        }
-        const float sm = s / mf;
-        const float var = fmaxf(fmaf(-s, sm, q), 0.f) / mf;
-        cx.grp[0] = K[0] + sm;                  // mean
-        cx.grp[1] = 1.0f / sqrtf(var + p.eps);  // rstd
+        const float2 t = cluster_sum_at(cluster, xch, 0, g.K);
+        const float sm = t.x / mf;
+        const float var = fmaxf(fmaf(-t.x, sm, t.y), 0.f) / mf;
+        grp[0] = K[0] + sm;                    // mean
+        grp[1] = 1.0f / sqrtf(var + p.eps);    // rstd
       } else {
-        // per channel of the group: sum of the m pieces, then the group sums
+        // per channel of the group: the m pieces in order, then the group sums
         float c1 = 0.f, c2 = 0.f;
         for (int64_t cl = 0; cl < g.Cg; ++cl) {
           float s1 = 0.f, s2 = 0.f;
-          for (int q = 0; q < g.m; ++q) {
-            const float* rem = cluster.map_shared_rank(cx.xch, (int)(cl * g.m + q));
+          for (int64_t q = 0; q < g.m; ++q) {
+            const float* rem = cluster.map_shared_rank(xch, (int)(cl * g.m + q));
             s1 += rem[0];
             s2 += rem[1];
           }
@@ -287,50 +311,42 @@ __global__ void __launch_bounds__(512, 1) resident_kernel(const __grid_constant_
           c2 = fmaf(gm, s2, c2);
         }
         const float r = __ldg(p.rstd + unit);
-        cx.grp[0] = -(r * r * r) * c2 / mf;  // B
-        cx.grp[1] = -r * c1 / mf;            // D
+        grp[0] = -(r * r * r) * c2 / mf;  // B
+        grp[1] = -r * c1 / mf;            // D
       }
     }
     __syncthreads();
-    if (!BWD) {
-      const float m_ = cx.grp[0], r = cx.grp[1];
-      if (rank == 0 && tid == 0) {
-        p.mean[unit] = m_;
-        p.rstd[unit] = r;
-      }
-      cm[0] = m_;
-      ca[0] = p.gamma ? r * __ldg(p.gamma + chan) : r;
-      cb[0] = p.beta ? __ldg(p.beta + chan) : 0.f;
-    } else {
-      const float r = __ldg(p.rstd + unit);
-      cm[0] = mu[0];
-      ca[0] = p.gamma ? r * __ldg(p.gamma + chan) : r;
-      cb[0] = cx.grp[0];
-      cd[0] = cx.grp[1];
+    const float r = BWD ? __ldg(p.rstd + unit) : grp[1];
+    if (!BWD && rank == 0 && tid == 0) {
+      p.mean[unit] = grp[0];
+      p.rstd[unit] = grp[1];
+    }
+#pragma unroll
+    for (int k = 0; k < VW; ++k) {
+      cm[k] = BWD ? mu[0] : grp[0];
+      ca[k] = p.gamma ? r * __ldg(p.gamma + chan) : r;
+      cb[k] = BWD ? grp[0] : (p.beta ? __ldg(p.beta + chan) : 0.f);
+      cd[k] = BWD ? grp[1] : 0.f;
     }
   } else {
-    // channel totals (rank order), then per group
-    for (int64_t c = tid; c < g.C; c += nt) {
-      float s = 0.f, q = 0.f;
-      for (int r = 0; r < g.K; ++r) {
-        const float* rem = cluster.map_shared_rank(cx.xch, r);
-        s += rem[2 * c];
-        q += rem[2 * c + 1];
-      }
+    // channel totals of the block (rank order), then per group of the block
+    for (int64_t c = tid; c < g.Cb; c += nt) {
+      const float2 t = cluster_sum_at(cluster, xch, c, g.K);
       if (!BWD) {
-        const float K0 = Elem<T>::to_f(x[n * g.HW * g.C + c]);
-        const float sm = s / hwf;
-        cx.tot[2 * c] = K0 + sm;                          // mean_c
-        cx.tot[2 * c + 1] = fmaxf(fmaf(-s, sm, q), 0.f);  // M2_c
+        const float K0 = Elem<T>::to_f(x[n * g.HW * g.C + cbase + c]);
+        const float sm = t.x / hwf;
+        tot[2 * c] = K0 + sm;                              // mean_c
+        tot[2 * c + 1] = fmaxf(fmaf(-t.x, sm, t.y), 0.f);  // M2_c
       } else {
-        cx.tot[2 * c] = s;
-        cx.tot[2 * c + 1] = q;
-        if (rank == 0) p.chst[n * g.C + c] = make_float2(s, q);
+        tot[2 * c] = t.x;
+        tot[2 * c + 1] = t.y;
+        if (rank == 0) p.chst[n * g.C + cbase + c] = t;
       }
     }
     __syncthreads();
-    for (int64_t gi = tid; gi < g.G; gi += nt) {
-      const float* ts = cx.tot + 2 * gi * g.Cg;
+    const int64_t gb = g.Cb / g.Cg;
+    for (int64_t gi = tid; gi < gb; gi += nt) {
+      const float* ts = tot + 2 * gi * g.Cg;
       if (!BWD) {
         float s = 0.f;
         for (int64_t k = 0; k < g.Cg; ++k) s += ts[2 * k];
@@ -341,44 +357,46 @@ __global__ void __launch_bounds__(512, 1) resident_kernel(const __grid_constant_
           m2 += fmaf(hwf * d, d, ts[2 * k + 1]);
         }
         const float r = 1.0f / sqrtf(m2 / mf + p.eps);
-        cx.grp[2 * gi] = mg;
-        cx.grp[2 * gi + 1] = r;
+        grp[2 * gi] = mg;
+        grp[2 * gi + 1] = r;
         if (rank == 0) {
-          p.mean[n * g.G + gi] = mg;
-          p.rstd[n * g.G + gi] = r;
+          p.mean[ngrp0 + gi] = mg;
+          p.rstd[ngrp0 + gi] = r;
         }
       } else {
         float c1 = 0.f, c2 = 0.f;
         for (int64_t k = 0; k < g.Cg; ++k) {
-          const float gm = p.gamma ? __ldg(p.gamma + gi * g.Cg + k) : 1.0f;
+          const float gm = p.gamma ? __ldg(p.gamma + cbase + gi * g.Cg + k) : 1.0f;
           c1 = fmaf(gm, ts[2 * k], c1);
           c2 = fmaf(gm, ts[2 * k + 1], c2);
         }
-        const float r = __ldg(p.rstd + n * g.G + gi);
-        cx.grp[2 * gi] = -(r * r * r) * c2 / mf;  // B
-        cx.grp[2 * gi + 1] = -r * c1 / mf;        // D
+        const float r = __ldg(p.rstd + ngrp0 + gi);
+        grp[2 * gi] = -(r * r * r) * c2 / mf;  // B
+        grp[2 * gi + 1] = -r * c1 / mf;        // D
       }
     }
     __syncthreads();
 #pragma unroll
     for (int k = 0; k < VW; ++k) {
-      const int64_t c = (int64_t)j * VW + k;
-      const int64_t gi = c / g.Cg;
+      const int64_t cl = (int64_t)j * VW + k;
+      const int64_t gi = cl / g.Cg;
+      const int64_t c = cbase + cl;
       if (!col_ok) {
         cm[k] = ca[k] = cb[k] = cd[k] = 0.f;
         continue;
       }
       if (!BWD) {
-        const float r = cx.grp[2 * gi + 1];
-        cm[k] = cx.grp[2 * gi];
+        const float r = grp[2 * gi + 1];
+        cm[k] = grp[2 * gi];
         ca[k] = p.gamma ? r * __ldg(p.gamma + c) : r;
         cb[k] = p.beta ? __ldg(p.beta + c) : 0.f;
+        cd[k] = 0.f;
       } else {
-        const float r = __ldg(p.rstd + n * g.G + gi);
+        const float r = __ldg(p.rstd + ngrp0 + gi);
         cm[k] = mu[k];
         ca[k] = p.gamma ? r * __ldg(p.gamma + c) : r;
-        cb[k] = cx.grp[2 * gi];
-        cd[k] = cx.grp[2 * gi + 1];
+        cb[k] = grp[2 * gi];
+        cd[k] = grp[2 * gi + 1];
       }
     }
   }
@@ -386,47 +404,47 @@ __global__ void __launch_bounds__(512, 1) resident_kernel(const __grid_constant_
   // ---- pass 2: outputs
   const uint64_t pol_out = policy_evict_first();
   auto produce = [&](const char* slot, int i) {
-    const int64_t a = e0 + (int64_t)i * ce;
-    const int64_t cnt = ((a + ce < e1) ? a + ce : e1) - a;
     if (LAYOUT == kNCHW) {
-      const int64_t nv = cnt / VW;
+      const int64_t a = e0 + (int64_t)i * g.chunk;
+      const int64_t nv = (((a + g.chunk < e1) ? a + g.chunk : e1) - a) / VW;
       for (int64_t v = tid; v < nv; v += nt) {
         float xv[VW];
         Access<T, VW>::unpack(*reinterpret_cast<const Raw*>(slot + v * 16), xv);
         if (BWD) {
           float dv[VW];
-          Access<T, VW>::unpack(*reinterpret_cast<const Raw*>(slot + g.chunk_bytes + v * 16), dv);
-#pragma unroll
-          for (int k = 0; k < VW; ++k) xv[k] = fmaf(ca[0], dv[k], fmaf(cb[0], xv[k] - cm[0], cd[0]));
-        } else {
-#pragma unroll
-          for (int k = 0; k < VW; ++k) xv[k] = fmaf(xv[k] - cm[0], ca[0], cb[0]);
-        }
-        Access<T, VW>::store(out + a + v * VW, xv, pol_out);
-      }
-    } else if (col_ok) {
-      const int64_t rows = cnt / g.C;
-      for (int64_t r = rl; r < rows; r += g.rpi) {
-        const int64_t eoff = r * g.C + (int64_t)j * VW;
-        float xv[VW];
-        Access<T, VW>::unpack(*reinterpret_cast<const Raw*>(slot + eoff * ESZ), xv);
-        if (BWD) {
-          float dv[VW];
-          Access<T, VW>::unpack(*reinterpret_cast<const Raw*>(slot + g.chunk_bytes + eoff * ESZ), dv);
+          Access<T, VW>::unpack(*reinterpret_cast<const Raw*>(slot + g.ten_stride + v * 16), dv);
 #pragma unroll
           for (int k = 0; k < VW; ++k) xv[k] = fmaf(ca[k], dv[k], fmaf(cb[k], xv[k] - cm[k], cd[k]));
         } else {
 #pragma unroll
           for (int k = 0; k < VW; ++k) xv[k] = fmaf(xv[k] - cm[k], ca[k], cb[k]);
         }
-        Access<T, VW>::store(out + a + eoff, xv, pol_out);
+        Access<T, VW>::store(out + a + v * VW, xv, pol_out);
+      }
+    } else if (col_ok) {
+      const int64_t rs = r0 + (int64_t)i * g.chunk;
+      const int64_t rows = ((rs + g.chunk < r1) ? rs + g.chunk : r1) - rs;
+      for (int64_t r = rl; r < rows; r += g.rpi) {
+        const int64_t off = r * rowp + (int64_t)j * 16;
+        float xv[VW];
+        Access<T, VW>::unpack(*reinterpret_cast<const Raw*>(slot + off), xv);
+        if (BWD) {
+          float dv[VW];
+          Access<T, VW>::unpack(*reinterpret_cast<const Raw*>(slot + g.ten_stride + off), dv);
+#pragma unroll
+          for (int k = 0; k < VW; ++k) xv[k] = fmaf(ca[k], dv[k], fmaf(cb[k], xv[k] - cm[k], cd[k]));
+        } else {
+#pragma unroll
+          for (int k = 0; k < VW; ++k) xv[k] = fmaf(xv[k] - cm[k], ca[k], cb[k]);
+        }
+        Access<T, VW>::store(out + (n * g.HW + rs + r) * g.C + cbase + (int64_t)j * VW, xv, pol_out);
       }
     }
   };
   for (int seq = nstr; seq < 2 * nstr; ++seq) {
     const int slot = seq % S;
-    if (res_wait(cx, cx.bar + g.nres + slot, (seq / S) & 1, p.err))
-      produce(cx.ring + slot * slot_bytes, seq_chunk(seq));
+    if (res_wait(&s_abort, bar + g.nres + slot, (seq / S) & 1, p.err))
+      produce(ring + slot * slot_bytes, seq_chunk(seq));
     __syncthreads();
     if (tid == 0 && issued < 2 * nstr && !s_abort) {
       fence_proxy_async_smem();
@@ -434,14 +452,13 @@ __global__ void __launch_bounds__(512, 1) resident_kernel(const __grid_constant_
     }
   }
   if (!s_abort)
-    for (int i = nres - 1; i >= 0; --i) produce(cx.res + i * slot_bytes, i);
+    for (int i = nres - 1; i >= 0; --i) produce(res + i * slot_bytes, i);
 
   // ---- after an abandoned wait: drain this CTA's own copies (bounded)
   __syncthreads();
   if (s_abort && tid == 0) {
-    for (int i = 0; i < nres; ++i) mbar_wait(cx.bar + i, 0, p.err);
-    for (int seq = 0; seq < issued; ++seq)
-      mbar_wait(cx.bar + g.nres + seq % S, (seq / S) & 1, p.err);
+    for (int i = 0; i < nres; ++i) mbar_wait(bar + i, 0, p.err);
+    for (int seq = 0; seq < issued; ++seq) mbar_wait(bar + g.nres + seq % S, (seq / S) & 1, p.err);
   }
   // no CTA leaves while a peer may still read its partials
   cluster.sync();
@@ -453,7 +470,7 @@ __global__ void __launch_bounds__(512, 1) resident_kernel(const __grid_constant_
     if (tid == 0) s_last = publish_and_arrive(p.tickets + g.N, (unsigned)g.units);
     __syncthreads();
     if (s_last) {
-      finalize_params(p, cx.red);
+      finalize_params(p, red);
       if (tid == 0) atomicExch(p.tickets + g.N, 0u);
     }
   }
@@ -472,6 +489,41 @@ const void* pick(int layout, bool bwd) {
   return bwd ? kernel_ptr<T, V, kNHWC, true>() : kernel_ptr<T, V, kNHWC, false>();
 }
 
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// against libcuda needed).
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess) {
+      cudaGetLastError();
+      f = nullptr;
+    }
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }();
+  return fn;
+}
+
+// [N*HW, C] view of an NHWC tensor, boxes of [chunk rows, Cb channels].
+cudaError_t encode_nhwc_map(CUtensorMap* map, const void* base, const Geom& g) {
+  auto fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  const CUtensorMapDataType dt = g.dtype == kF32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                 : g.dtype == kF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                   : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const int esz = g.dtype == kF32 ? 4 : 2;
+  const cuuint64_t dims[2] = {(cuuint64_t)g.C, (cuuint64_t)(g.N * g.HW)};
+  const cuuint64_t strides[1] = {(cuuint64_t)(g.C * esz)};
+  const cuuint32_t box[2] = {(cuuint32_t)g.Cb, (cuuint32_t)g.chunk};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 }  // namespace
 
 const void* resident_kernel_ptr(const Geom& g, bool bwd) {
@@ -482,10 +534,17 @@ const void* resident_kernel_ptr(const Geom& g, bool bwd) {
   }
 }
 
-cudaError_t launch_resident(const KParams& p, cudaStream_t s, bool bwd) {
+cudaError_t launch_resident(const KParams& p_in, cudaStream_t s, bool bwd) {
+  KParams p = p_in;
   const Geom& g = p.g;
+  cudaError_t e;
+  if (g.layout == kNHWC) {
+    e = encode_nhwc_map(&p.tmx, p.x, g);
+    if (e == cudaSuccess && bwd) e = encode_nhwc_map(&p.tmdy, p.dy, g);
+    if (e != cudaSuccess) return e;
+  }
   const void* fn = resident_kernel_ptr(g, bwd);
-  cudaError_t e = prepare_resident_kernel(fn, g);
+  e = prepare_resident_kernel(fn, g);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(g.units * g.K), 1, 1);
@@ -499,7 +558,7 @@ cudaError_t launch_resident(const KParams& p, cudaStream_t s, bool bwd) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  void* args[] = {const_cast<KParams*>(&p)};
+  void* args[] = {&p};
   const TimingEvents& ev = timing_events();
   if (ev.begin) cudaEventRecord(ev.begin, s);
   e = cudaLaunchKernelExC(&cfg, fn, args);
