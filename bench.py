@@ -241,9 +241,15 @@ def time_configs(gn, synth, torch, flush, names=None, reps=20):
     out = {}
     peak, _ = load_peaks()
     stream = torch.cuda.current_stream()
+    todo = []
     for w in synth.WORKLOADS[1:]:
-        if names and w.name not in names:
-            continue
+        if not names:
+            todo.append(w)
+        for nm in names or ():
+            base, _, nn = nm.partition(":")  # "workload" or "workload:N" (batch override)
+            if base == w.name:
+                todo.append(w.scaled(N=int(nn)) if nn else w)
+    for w in todo:
         inp = synth.make_inputs(w, "cuda", seed=0)
         x, dy, gm, bt = inp["x"], inp["dy"], inp["gamma"], inp["beta"]
         y = torch.empty_like(x)
@@ -278,7 +284,7 @@ def time_configs(gn, synth, torch, flush, names=None, reps=20):
         med = {k: statistics.median(v) for k, v in rec.items()}
         fwd_gbs = mb["fwd"] / (med["fwd"] * 1e-3) / 1e9
         bwd_gbs = mb["bwd"] / (med["bwd"] * 1e-3) / 1e9
-        out[w.name] = {
+        out[w.name if w.N == synth.BY_NAME[w.name].N else f"{w.name}:N={w.N}"] = {
             "regime": {"fwd": "resident" if pf.launches == 1 else "two-kernel",
                        "bwd": "resident" if pb.launches == 1 else "two-kernel"},
             "fwd_us": round(med["fwd"] * 1e3, 2), "bwd_us": round(med["bwd"] * 1e3, 2),
@@ -495,7 +501,8 @@ def main():
     ap.add_argument("--no-per-config", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--configs", default="", help="comma-separated workload names for the per-workload leg")
+    ap.add_argument("--configs", default="",
+                    help="comma-separated workload names for the per-workload leg; name:N overrides the batch")
     ap.add_argument("--reps", type=int, default=20, help="timed calls per workload in the per-workload leg")
     args = ap.parse_args()
     if args.warmup < 3:
