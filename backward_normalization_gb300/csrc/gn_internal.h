@@ -129,6 +129,8 @@ const void* nchw_first_kernel(const Geom& g, bool bwd, size_t* smem);
 // gn_resident.cu
 const void* resident_kernel_ptr(const Geom& g, bool bwd);
 cudaError_t launch_resident(const KParams& p, cudaStream_t s, bool bwd);
+// Threads of a resident CTA: the consumer warps plus one producer warp.
+inline int resident_threads(const Geom& g) { return (g.tpb + 31) / 32 * 32 + 32; }
 // Sets the kernel attributes a resident launch needs (large shared memory,
 // 16-CTA clusters); idempotent.
 cudaError_t prepare_resident_kernel(const void* kernel, const Geom& g);

@@ -81,7 +81,7 @@ int64_t resident_clusters(const Geom& g, int op) {
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)g.K, 1, 1);
-  cfg.blockDim = dim3((unsigned)g.tpb, 1, 1);
+  cfg.blockDim = dim3((unsigned)resident_threads(g), 1, 1);
   cfg.dynamicSmemBytes = g.smem;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -111,18 +111,19 @@ bool plan_resident(Geom& g, int op) {
   if (g.layout == kNCHW) {
     if (g.Cg > 16) return false;
     if (g.Cg * g.HW * esz * nten > kMaxUnitBytes) return false;
-    const int64_t cbytes = op == kBwd ? 8 * 1024 : 16 * 1024;
+    // large chunks: the per-chunk cost of the pipeline is then small
+    const int64_t cbytes = op == kBwd ? 32 * 1024 : 64 * 1024;
     int64_t m = 16 / g.Cg;
     while (m > 1 && g.HW * esz / m < 2 * cbytes) m /= 2;
     r.m = m;
     r.K = (int)(g.Cg * m);
     r.tpb = 512;
     r.slice = rup(cdiv(g.HW, m), vec);
-    r.chunk = cbytes / esz;
-    r.chunk_bytes = cbytes;
+    r.chunk = cbytes / esz < r.slice ? cbytes / esz : r.slice;
+    r.chunk_bytes = r.chunk * esz;
     r.units = g.N * g.G;
     nch = cdiv(r.slice, r.chunk);
-    red_f = 2 * (size_t)r.tpb;
+    red_f = 2 * (size_t)resident_threads(r);
     xch_f = 2;
     tot_f = 0;
     grp_f = 2;
@@ -153,7 +154,8 @@ bool plan_resident(Geom& g, int op) {
     nch = cdiv(r.slice, max_rows);
     r.chunk = cdiv(r.slice, nch);
     r.chunk_bytes = r.chunk * row_bytes;
-    red_f = 2 * (size_t)vec * r.tpb;
+    red_f = 2 * (size_t)vec * ((r.tpb + 31) / 32 * 32);
+    if (red_f < 2 * (size_t)resident_threads(r)) red_f = 2 * (size_t)resident_threads(r);
     xch_f = 2 * (size_t)cb;
     tot_f = 2 * (size_t)cb;
     grp_f = 2 * (size_t)(cb / g.Cg);
@@ -162,7 +164,7 @@ bool plan_resident(Geom& g, int op) {
   r.ten_stride = (int64_t)a128((size_t)r.chunk_bytes);
   const size_t slot = (size_t)r.ten_stride * nten;
   if (kSmemPerCta < fixed + 1024) return false;
-  const int64_t slots = (int64_t)((kSmemPerCta - fixed - 512) / (slot + 8));
+  const int64_t slots = (int64_t)((kSmemPerCta - fixed - 512) / (slot + 16));
   if (nch <= slots) {
     r.nres = (int)nch;
     r.S = 0;
@@ -184,7 +186,7 @@ bool plan_resident(Geom& g, int op) {
   r.off_grp = off;
   off += a128(grp_f * 4);
   r.off_bar = off;
-  off += a128(8 * (size_t)(r.nres + r.S));
+  off += a128(8 * (size_t)(r.nres + 2 * r.S));  // full barriers, and empty barriers for the ring
   r.smem = off + 128;  // slack for aligning the dynamic shared memory base
   if (r.smem > kSmemPerCta) return false;
   if (r.units * r.K > 0x7fffffffLL) return false;

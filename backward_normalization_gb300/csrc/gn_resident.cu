@@ -62,8 +62,33 @@ __device__ __forceinline__ float2 cluster_sum_at(cg::cluster_group& cluster, flo
   return s;
 }
 
+// Consumer-only barrier (hardware barrier 1): the producer warp does not take
+// part.
+__device__ __forceinline__ void csync(int ncpad) { named_sync(1, ncpad); }
+
+// Block sum of two values over the consumer threads (fixed order); the
+// totals are returned in thread 0.  `scratch` holds 64 floats.
+__device__ __forceinline__ float2 consumer_sum2_t0(float a, float b, float* scratch, int ncpad) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  a = warp_sum_lane0(a);
+  b = warp_sum_lane0(b);
+  if (lane == 0) {
+    scratch[2 * warp] = a;
+    scratch[2 * warp + 1] = b;
+  }
+  csync(ncpad);
+  float2 r = make_float2(0.f, 0.f);
+  if (threadIdx.x == 0)
+    for (int w = 0; w < ncpad / 32; ++w) {
+      r.x += scratch[2 * w];
+      r.y += scratch[2 * w + 1];
+    }
+  csync(ncpad);
+  return r;
+}
+
 template <typename T, int VW, int LAYOUT, bool BWD>
-__global__ void __launch_bounds__(512, 1) resident_kernel(const __grid_constant__ KParams p) {
+__global__ void __launch_bounds__(544, 1) resident_kernel(const __grid_constant__ KParams p) {
   extern __shared__ __align__(128) char smem_raw[];
   // TMA tile destinations need 128-byte alignment: align the base here (the
   // plan reserves 128 bytes of slack)
@@ -74,7 +99,11 @@ __global__ void __launch_bounds__(512, 1) resident_kernel(const __grid_constant_
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
   const int64_t unit = blockIdx.x / g.K;
-  const int tid = threadIdx.x, nt = blockDim.x;
+  const int tid = threadIdx.x;
+  const int nc = g.tpb;                   // consumer threads doing work
+  const int ncpad = (nc + 31) / 32 * 32;  // consumer threads (whole warps)
+  const int ncw = ncpad / 32;             // consumer warps
+  const bool producer = tid >= ncpad;     // the last warp issues the TMA copies
   __shared__ int s_abort;
 
   char* res = smem;
@@ -83,7 +112,8 @@ __global__ void __launch_bounds__(512, 1) resident_kernel(const __grid_constant_
   float* xch = reinterpret_cast<float*>(smem + g.off_xch);
   float* tot = reinterpret_cast<float*>(smem + g.off_tot);
   float* grp = reinterpret_cast<float*>(smem + g.off_grp);
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + g.off_bar);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + g.off_bar);
+  uint64_t* empty = full + g.nres + g.S;
   const T* x = static_cast<const T*>(p.x);
   const T* dy = static_cast<const T*>(p.dy);
   T* out = static_cast<T*>(p.out);
@@ -119,14 +149,15 @@ __global__ void __launch_bounds__(512, 1) resident_kernel(const __grid_constant_
 
   if (tid == 0) {
     s_abort = 0;
-    for (int i = 0; i < g.nres + S; ++i) mbar_init(bar + i, 1);
+    for (int i = 0; i < g.nres + S; ++i) mbar_init(full + i, 1);
+    for (int i = 0; i < S; ++i) mbar_init(empty + i, (uint32_t)ncw);
     fence_mbar_init();
   }
   __syncthreads();
 
   const uint64_t pol_once = policy_evict_first();  // resident chunks: read once from HBM
   const uint64_t pol_again = policy_evict_last();  // streamed chunks: read again in pass 2
-  // Producer (thread 0): chunk i of the slice into `dst`, completing on `b`.
+  // chunk i of the slice into `dst`, completing on `b`
   auto issue = [&](int i, char* dst, uint64_t* b, uint64_t pol) {
     if (LAYOUT == kNCHW) {
       const int64_t a = e0 + (int64_t)i * g.chunk;
@@ -144,41 +175,60 @@ __global__ void __launch_bounds__(512, 1) resident_kernel(const __grid_constant_
     }
   };
   // Ring loads are numbered seq = 0 .. 2*nstr-1: pass-1 streamed chunks in
-  // order, then the pass-2 reloads newest first.
+  // order, then the pass-2 reloads newest first.  Load seq uses slot seq % S;
+  // it is issued once every consumer warp has released the slot's previous
+  // load (phase seq/S - 1 of that slot's empty barrier).
   auto seq_chunk = [&](int seq) { return seq < nstr ? nres + seq : nch - 1 - (seq - nstr); };
-  auto seq_issue = [&](int seq) {
-    const int slot = seq % S;
-    issue(seq_chunk(seq), ring + slot * slot_bytes, bar + g.nres + slot,
-          seq < nstr ? pol_again : pol_once);
+  int issued = 0;  // producer lane 0: ring loads issued
+  auto produce_until = [&](int upto) {
+    for (; issued < upto; ++issued) {
+      const int slot = issued % S;
+      if (issued >= S) {
+        if (!res_wait(&s_abort, empty + slot, ((issued / S) - 1) & 1, p.err)) return;
+        fence_proxy_async_smem();  // the consumers' reads of the slot precede the new copy
+      }
+      issue(seq_chunk(issued), ring + slot * slot_bytes, full + g.nres + slot,
+            issued < nstr ? pol_again : pol_once);
+    }
   };
-  int issued = 0;  // ring loads issued (meaningful in thread 0)
-  if (tid == 0) {
-    for (int i = 0; i < nres; ++i) issue(i, res + i * slot_bytes, bar + i, pol_once);
-    for (; issued < S && issued < 2 * nstr; ++issued) seq_issue(issued);
+  const bool lead = producer && (tid & 31) == 0;
+  if (lead) {
+    for (int i = 0; i < nres; ++i) issue(i, res + i * slot_bytes, full + i, pol_once);
+    // every pass-1 load, plus the first pass-2 reloads (they land during the reduction)
+    produce_until(nstr + S < 2 * nstr ? nstr + S : 2 * nstr);
   }
 
-  // ---- per-thread layout inside a chunk
+  // ---- per-thread layout inside a chunk (consumers)
   // NHWC: thread (rl, j) owns column j (VW channels of the block) and rows
   // rl, rl + rpi, ...; NCHW: threads stride the chunk's 16-byte vectors.
+  const bool worker = tid < nc;
   const int j = LAYOUT == kNHWC ? tid % g.Wv : 0;
   const int rl = LAYOUT == kNHWC ? tid / g.Wv : 0;
-  const bool col_ok = LAYOUT == kNHWC ? rl < g.rpi : true;
-  float K[VW];  // forward shift: x(n, c, hw = 0) per channel (NHWC) or per group (NCHW)
-  float mu[VW];  // backward: group mean of each owned channel
-  if (LAYOUT == kNHWC) {
+  const bool col_ok = worker && (LAYOUT == kNHWC ? rl < g.rpi : true);
+  // Everything the constants need is loaded now; the latency hides under pass 1.
+  float K[VW], mu[VW], gmv[VW], btv[VW], rsv[VW];
 #pragma unroll
-    for (int k = 0; k < VW; ++k) {
-      const int64_t c = cbase + (int64_t)j * VW + k;
-      K[k] = (!BWD && col_ok) ? Elem<T>::to_f(x[n * g.HW * g.C + c]) : 0.f;
-      mu[k] = (BWD && col_ok) ? __ldg(p.mean + n * g.G + c / g.Cg) : 0.f;
-    }
-  } else {
-    const float k0 = BWD ? 0.f : Elem<T>::to_f(x[(n * g.C + (unit % g.G) * g.Cg) * g.HW]);
-    const float m0 = BWD ? __ldg(p.mean + unit) : 0.f;
+  for (int k = 0; k < VW; ++k) {
+    const int64_t c = LAYOUT == kNHWC ? cbase + (int64_t)j * VW + k : chan;
+    const int64_t gidx = LAYOUT == kNHWC ? n * g.G + c / g.Cg : unit;
+    const bool ok = col_ok && (LAYOUT == kNHWC || k == 0);
+    K[k] = 0.f;
+    if (!BWD && ok)
+      K[k] = LAYOUT == kNHWC ? Elem<T>::to_f(x[n * g.HW * g.C + c])
+                             : Elem<T>::to_f(x[(n * g.C + (unit % g.G) * g.Cg) * g.HW]);
+    mu[k] = (BWD && ok) ? __ldg(p.mean + gidx) : 0.f;
+    rsv[k] = (BWD && ok) ? __ldg(p.rstd + gidx) : 0.f;
+    gmv[k] = (ok && p.gamma) ? __ldg(p.gamma + c) : 1.f;
+    btv[k] = (!BWD && ok && p.beta) ? __ldg(p.beta + c) : 0.f;
+  }
+  if (LAYOUT == kNCHW) {
 #pragma unroll
-    for (int k = 0; k < VW; ++k) {
-      K[k] = k0;
-      mu[k] = m0;
+    for (int k = 1; k < VW; ++k) {
+      K[k] = K[0];
+      mu[k] = mu[0];
+      rsv[k] = rsv[0];
+      gmv[k] = gmv[0];
+      btv[k] = btv[0];
     }
   }
   float acc[2 * VW];
@@ -190,9 +240,10 @@ __global__ void __launch_bounds__(512, 1) resident_kernel(const __grid_constant_
   // Folds chunk i (at `slot`) into acc.
   auto consume = [&](const char* slot, int i) {
     if (LAYOUT == kNCHW) {
+      if (!worker) return;
       const int64_t a = e0 + (int64_t)i * g.chunk;
       const int64_t nv = (((a + g.chunk < e1) ? a + g.chunk : e1) - a) / VW;
-      for (int64_t v = tid; v < nv; v += nt) {
+      for (int64_t v = tid; v < nv; v += nc) {
         float xv[VW];
         Access<T, VW>::unpack(*reinterpret_cast<const Raw*>(slot + v * 16), xv);
         if (BWD) {
@@ -238,62 +289,70 @@ __global__ void __launch_bounds__(512, 1) resident_kernel(const __grid_constant_
       }
     }
   };
+  // A consumer warp is done with ring load seq: release its slot.
+  auto release = [&](int seq) {
+    __syncwarp();
+    if ((tid & 31) == 0) mbar_arrive(empty + seq % S);
+  };
 
-  // ---- pass 1
-  for (int i = 0; i < nres; ++i)
-    if (res_wait(&s_abort, bar + i, 0, p.err)) consume(res + i * slot_bytes, i);
-  for (int seq = 0; seq < nstr; ++seq) {
-    const int slot = seq % S;
-    if (res_wait(&s_abort, bar + g.nres + slot, (seq / S) & 1, p.err))
-      consume(ring + slot * slot_bytes, seq_chunk(seq));
-    __syncthreads();  // the slot is free again
-    if (tid == 0 && issued < 2 * nstr && !s_abort) {
-      fence_proxy_async_smem();
-      seq_issue(issued++);
+  float ca[VW], cb[VW], cm[VW], cd[VW];  // output constants (see below)
+  if (!producer) {
+    // ---- pass 1
+    for (int i = 0; i < nres; ++i)
+      if (res_wait(&s_abort, full + i, 0, p.err)) consume(res + i * slot_bytes, i);
+    for (int seq = 0; seq < nstr; ++seq) {
+      if (res_wait(&s_abort, full + g.nres + seq % S, (seq / S) & 1, p.err))
+        consume(ring + (seq % S) * slot_bytes, seq_chunk(seq));
+      release(seq);
+    }
+    // ---- reduce within the CTA
+    if (LAYOUT == kNCHW) {
+      const float2 t = consumer_sum2_t0(acc[0], acc[1], red, ncpad);
+      if (tid == 0) {
+        xch[0] = t.x;
+        xch[1] = t.y;
+      }
+    } else {
+#pragma unroll
+      for (int q = 0; q < 2 * VW; ++q) red[q * ncpad + tid] = acc[q];
+      csync(ncpad);
+      for (int s = 1; s < g.rpi; s <<= 1) {
+        if (col_ok && (rl % (2 * s)) == 0 && rl + s < g.rpi) {
+#pragma unroll
+          for (int q = 0; q < 2 * VW; ++q) red[q * ncpad + tid] += red[q * ncpad + tid + s * g.Wv];
+        }
+        csync(ncpad);
+      }
+      if (col_ok && rl == 0) {
+#pragma unroll
+        for (int k = 0; k < VW; ++k) {
+          xch[2 * (j * VW + k)] = red[(2 * k) * ncpad + tid];
+          xch[2 * (j * VW + k) + 1] = red[(2 * k + 1) * ncpad + tid];
+          if (!BWD) tot[2 * (j * VW + k)] = K[k];  // the channel's shift, for the totals
+        }
+      }
     }
   }
+  cluster.sync();  // every CTA of the cluster has published its partials
 
-  // ---- reduce: CTA, then cluster (every CTA sums the K partials in rank order)
-  if (LAYOUT == kNCHW) {
-    const float2 t = block_sum2_t0(acc[0], acc[1], red);
-    if (tid == 0) {
-      xch[0] = t.x;
-      xch[1] = t.y;
-    }
-  } else {
-#pragma unroll
-    for (int q = 0; q < 2 * VW; ++q) red[q * nt + tid] = acc[q];
-    __syncthreads();
-    for (int s = 1; s < g.rpi; s <<= 1) {
-      if (col_ok && (rl % (2 * s)) == 0 && rl + s < g.rpi) {
-#pragma unroll
-        for (int q = 0; q < 2 * VW; ++q) red[q * nt + tid] += red[q * nt + tid + s * g.Wv];
-      }
-      __syncthreads();
-    }
-    if (rl == 0) {
-#pragma unroll
-      for (int k = 0; k < VW; ++k) {
-        xch[2 * (j * VW + k)] = red[(2 * k) * nt + tid];
-        xch[2 * (j * VW + k) + 1] = red[(2 * k + 1) * nt + tid];
-      }
-    }
-  }
-  cluster.sync();
-
-  // Per-thread output constants: y = (x - cm)*ca + cb, or
-  // dx = ca*dy + cb*(x - cm) + cd.
-  float ca[VW], cb[VW], cm[VW], cd[VW];
+  // ---- statistics / coefficients (consumers); the producer keeps loading
+  // Output constants: y = (x - cm)*ca + cb, or dx = ca*dy + cb*(x - cm) + cd.
   const float hwf = (float)g.HW;
   const float mf = (float)(g.Cg * g.HW);
-  if (LAYOUT == kNCHW) {
+  if (producer) {
+    if (lead) produce_until(2 * nstr);
+  } else if (LAYOUT == kNCHW) {
     if (tid == 0) {
       if (!BWD) {
         const float2 t = cluster_sum_at(cluster, xch, 0, g.K);
         const float sm = t.x / mf;
         const float var = fmaxf(fmaf(-t.x, sm, t.y), 0.f) / mf;
-        grp[0] = K[0] + sm;                    // mean
-        grp[1] = 1.0f / sqrtf(var + p.eps);    // rstd
+        grp[0] = K[0] + sm;                  // mean
+        grp[1] = 1.0f / sqrtf(var + p.eps);  // rstd
+        if (rank == 0) {
+          p.mean[unit] = grp[0];
+          p.rstd[unit] = grp[1];
+        }
       } else {
         // per channel of the group: the m pieces in order, then the group sums
         float c1 = 0.f, c2 = 0.f;
@@ -310,32 +369,27 @@ __global__ void __launch_bounds__(512, 1) resident_kernel(const __grid_constant_
           c1 = fmaf(gm, s1, c1);
           c2 = fmaf(gm, s2, c2);
         }
-        const float r = __ldg(p.rstd + unit);
+        const float r = rsv[0];
         grp[0] = -(r * r * r) * c2 / mf;  // B
         grp[1] = -r * c1 / mf;            // D
       }
     }
-    __syncthreads();
-    const float r = BWD ? __ldg(p.rstd + unit) : grp[1];
-    if (!BWD && rank == 0 && tid == 0) {
-      p.mean[unit] = grp[0];
-      p.rstd[unit] = grp[1];
-    }
+    csync(ncpad);
+    const float r = BWD ? rsv[0] : grp[1];
 #pragma unroll
     for (int k = 0; k < VW; ++k) {
       cm[k] = BWD ? mu[0] : grp[0];
-      ca[k] = p.gamma ? r * __ldg(p.gamma + chan) : r;
-      cb[k] = BWD ? grp[0] : (p.beta ? __ldg(p.beta + chan) : 0.f);
+      ca[k] = r * gmv[0];
+      cb[k] = BWD ? grp[0] : btv[0];
       cd[k] = BWD ? grp[1] : 0.f;
     }
   } else {
     // channel totals of the block (rank order), then per group of the block
-    for (int64_t c = tid; c < g.Cb; c += nt) {
+    for (int64_t c = tid; c < g.Cb; c += ncpad) {
       const float2 t = cluster_sum_at(cluster, xch, c, g.K);
       if (!BWD) {
-        const float K0 = Elem<T>::to_f(x[n * g.HW * g.C + cbase + c]);
         const float sm = t.x / hwf;
-        tot[2 * c] = K0 + sm;                              // mean_c
+        tot[2 * c] += sm;                                  // mean_c = shift + S/HW
         tot[2 * c + 1] = fmaxf(fmaf(-t.x, sm, t.y), 0.f);  // M2_c
       } else {
         tot[2 * c] = t.x;
@@ -343,9 +397,9 @@ __global__ void __launch_bounds__(512, 1) resident_kernel(const __grid_constant_
         if (rank == 0) p.chst[n * g.C + cbase + c] = t;
       }
     }
-    __syncthreads();
+    csync(ncpad);
     const int64_t gb = g.Cb / g.Cg;
-    for (int64_t gi = tid; gi < gb; gi += nt) {
+    for (int64_t gi = tid; gi < gb; gi += ncpad) {
       const float* ts = tot + 2 * gi * g.Cg;
       if (!BWD) {
         float s = 0.f;
@@ -375,12 +429,10 @@ __global__ void __launch_bounds__(512, 1) resident_kernel(const __grid_constant_
         grp[2 * gi + 1] = -r * c1 / mf;        // D
       }
     }
-    __syncthreads();
+    csync(ncpad);
 #pragma unroll
     for (int k = 0; k < VW; ++k) {
-      const int64_t cl = (int64_t)j * VW + k;
-      const int64_t gi = cl / g.Cg;
-      const int64_t c = cbase + cl;
+      const int64_t gi = ((int64_t)j * VW + k) / g.Cg;
       if (!col_ok) {
         cm[k] = ca[k] = cb[k] = cd[k] = 0.f;
         continue;
@@ -388,77 +440,74 @@ __global__ void __launch_bounds__(512, 1) resident_kernel(const __grid_constant_
       if (!BWD) {
         const float r = grp[2 * gi + 1];
         cm[k] = grp[2 * gi];
-        ca[k] = p.gamma ? r * __ldg(p.gamma + c) : r;
-        cb[k] = p.beta ? __ldg(p.beta + c) : 0.f;
+        ca[k] = r * gmv[k];
+        cb[k] = btv[k];
         cd[k] = 0.f;
       } else {
-        const float r = __ldg(p.rstd + ngrp0 + gi);
         cm[k] = mu[k];
-        ca[k] = p.gamma ? r * __ldg(p.gamma + c) : r;
+        ca[k] = rsv[k] * gmv[k];
         cb[k] = grp[2 * gi];
         cd[k] = grp[2 * gi + 1];
       }
     }
   }
 
-  // ---- pass 2: outputs
-  const uint64_t pol_out = policy_evict_first();
-  auto produce = [&](const char* slot, int i) {
-    if (LAYOUT == kNCHW) {
-      const int64_t a = e0 + (int64_t)i * g.chunk;
-      const int64_t nv = (((a + g.chunk < e1) ? a + g.chunk : e1) - a) / VW;
-      for (int64_t v = tid; v < nv; v += nt) {
-        float xv[VW];
-        Access<T, VW>::unpack(*reinterpret_cast<const Raw*>(slot + v * 16), xv);
-        if (BWD) {
-          float dv[VW];
-          Access<T, VW>::unpack(*reinterpret_cast<const Raw*>(slot + g.ten_stride + v * 16), dv);
+  // ---- pass 2: outputs (consumers)
+  if (!producer) {
+    const uint64_t pol_out = policy_evict_first();
+    auto emit = [&](const char* slot, int i) {
+      if (LAYOUT == kNCHW) {
+        if (!worker) return;
+        const int64_t a = e0 + (int64_t)i * g.chunk;
+        const int64_t nv = (((a + g.chunk < e1) ? a + g.chunk : e1) - a) / VW;
+        for (int64_t v = tid; v < nv; v += nc) {
+          float xv[VW];
+          Access<T, VW>::unpack(*reinterpret_cast<const Raw*>(slot + v * 16), xv);
+          if (BWD) {
+            float dv[VW];
+            Access<T, VW>::unpack(*reinterpret_cast<const Raw*>(slot + g.ten_stride + v * 16), dv);
 #pragma unroll
-          for (int k = 0; k < VW; ++k) xv[k] = fmaf(ca[k], dv[k], fmaf(cb[k], xv[k] - cm[k], cd[k]));
-        } else {
+            for (int k = 0; k < VW; ++k) xv[k] = fmaf(ca[k], dv[k], fmaf(cb[k], xv[k] - cm[k], cd[k]));
+          } else {
 #pragma unroll
-          for (int k = 0; k < VW; ++k) xv[k] = fmaf(xv[k] - cm[k], ca[k], cb[k]);
+            for (int k = 0; k < VW; ++k) xv[k] = fmaf(xv[k] - cm[k], ca[k], cb[k]);
+          }
+          Access<T, VW>::store(out + a + v * VW, xv, pol_out);
         }
-        Access<T, VW>::store(out + a + v * VW, xv, pol_out);
-      }
-    } else if (col_ok) {
-      const int64_t rs = r0 + (int64_t)i * g.chunk;
-      const int64_t rows = ((rs + g.chunk < r1) ? rs + g.chunk : r1) - rs;
-      for (int64_t r = rl; r < rows; r += g.rpi) {
-        const int64_t off = r * rowp + (int64_t)j * 16;
-        float xv[VW];
-        Access<T, VW>::unpack(*reinterpret_cast<const Raw*>(slot + off), xv);
-        if (BWD) {
-          float dv[VW];
-          Access<T, VW>::unpack(*reinterpret_cast<const Raw*>(slot + g.ten_stride + off), dv);
+      } else if (col_ok) {
+        const int64_t rs = r0 + (int64_t)i * g.chunk;
+        const int64_t rows = ((rs + g.chunk < r1) ? rs + g.chunk : r1) - rs;
+        for (int64_t r = rl; r < rows; r += g.rpi) {
+          const int64_t off = r * rowp + (int64_t)j * 16;
+          float xv[VW];
+          Access<T, VW>::unpack(*reinterpret_cast<const Raw*>(slot + off), xv);
+          if (BWD) {
+            float dv[VW];
+            Access<T, VW>::unpack(*reinterpret_cast<const Raw*>(slot + g.ten_stride + off), dv);
 #pragma unroll
-          for (int k = 0; k < VW; ++k) xv[k] = fmaf(ca[k], dv[k], fmaf(cb[k], xv[k] - cm[k], cd[k]));
-        } else {
+            for (int k = 0; k < VW; ++k) xv[k] = fmaf(ca[k], dv[k], fmaf(cb[k], xv[k] - cm[k], cd[k]));
+          } else {
 #pragma unroll
-          for (int k = 0; k < VW; ++k) xv[k] = fmaf(xv[k] - cm[k], ca[k], cb[k]);
+            for (int k = 0; k < VW; ++k) xv[k] = fmaf(xv[k] - cm[k], ca[k], cb[k]);
+          }
+          Access<T, VW>::store(out + (n * g.HW + rs + r) * g.C + cbase + (int64_t)j * VW, xv, pol_out);
         }
-        Access<T, VW>::store(out + (n * g.HW + rs + r) * g.C + cbase + (int64_t)j * VW, xv, pol_out);
       }
+    };
+    for (int seq = nstr; seq < 2 * nstr; ++seq) {
+      if (res_wait(&s_abort, full + g.nres + seq % S, (seq / S) & 1, p.err))
+        emit(ring + (seq % S) * slot_bytes, seq_chunk(seq));
+      release(seq);
     }
-  };
-  for (int seq = nstr; seq < 2 * nstr; ++seq) {
-    const int slot = seq % S;
-    if (res_wait(&s_abort, bar + g.nres + slot, (seq / S) & 1, p.err))
-      produce(ring + slot * slot_bytes, seq_chunk(seq));
-    __syncthreads();
-    if (tid == 0 && issued < 2 * nstr && !s_abort) {
-      fence_proxy_async_smem();
-      seq_issue(issued++);
-    }
+    if (!*reinterpret_cast<volatile int*>(&s_abort))
+      for (int i = nres - 1; i >= 0; --i) emit(res + i * slot_bytes, i);
   }
-  if (!s_abort)
-    for (int i = nres - 1; i >= 0; --i) produce(res + i * slot_bytes, i);
 
   // ---- after an abandoned wait: drain this CTA's own copies (bounded)
   __syncthreads();
-  if (s_abort && tid == 0) {
-    for (int i = 0; i < nres; ++i) mbar_wait(bar + i, 0, p.err);
-    for (int seq = 0; seq < issued; ++seq) mbar_wait(bar + g.nres + seq % S, (seq / S) & 1, p.err);
+  if (s_abort && lead) {
+    for (int i = 0; i < nres; ++i) mbar_wait(full + i, 0, p.err);
+    for (int seq = 0; seq < issued; ++seq) mbar_wait(full + g.nres + seq % S, (seq / S) & 1, p.err);
   }
   // no CTA leaves while a peer may still read its partials
   cluster.sync();
@@ -548,7 +597,7 @@ cudaError_t launch_resident(const KParams& p_in, cudaStream_t s, bool bwd) {
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(g.units * g.K), 1, 1);
-  cfg.blockDim = dim3((unsigned)g.tpb, 1, 1);
+  cfg.blockDim = dim3((unsigned)resident_threads(g), 1, 1);
   cfg.dynamicSmemBytes = g.smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
