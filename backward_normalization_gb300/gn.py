@@ -68,6 +68,9 @@ def lib() -> ctypes.CDLL:
         L.gn_plan_info.argtypes = [ctypes.c_int, _I64, _I64, _I64, _I64, ctypes.c_int, ctypes.c_int,
                                    ctypes.c_int, ctypes.POINTER(PlanDesc)]
         L.gn_plan_info.restype = ctypes.c_int
+        L.gn_fwd_static_ws.argtypes = [_VP, _I64, _I64, _I64, _I64, ctypes.c_int, ctypes.c_int, _VP,
+                                       _VP, ctypes.c_float, _VP, _VP, _VP, _VP]
+        L.gn_fwd_static_ws.restype = ctypes.c_int
         L.gn_set_regime.argtypes = [ctypes.c_int]
         L.gn_set_regime.restype = ctypes.c_int
         L.gn_set_timing_events.argtypes = [_VP, _VP, _VP]
@@ -117,6 +120,15 @@ def fwd_raw(x, N, C, HW, G, layout, gamma, beta, eps, y, mean, rstd, workspace,
     return lib().gn_fwd(_ptr(x), N, C, HW, G, LAYOUT[layout], DTYPE[x.dtype], _ptr(gamma),
                         _ptr(beta), float(eps), _ptr(y), _ptr(mean), _ptr(rstd),
                         _ptr(workspace), ws_bytes, _stream(stream))
+
+
+def fwd_static_ws_raw(x, N, C, HW, G, layout, gamma, beta, eps, y, mean, rstd,
+                      stream=None) -> int:
+    """gn_fwd_static_ws on torch tensors (no workspace argument); returns the
+    gn_status."""
+    return lib().gn_fwd_static_ws(_ptr(x), N, C, HW, G, LAYOUT[layout], DTYPE[x.dtype],
+                                  _ptr(gamma), _ptr(beta), float(eps), _ptr(y), _ptr(mean),
+                                  _ptr(rstd), _stream(stream))
 
 
 def bwd_raw(dy, x, mean, rstd, gamma, N, C, HW, G, layout, dx, dgamma, dbeta, workspace,

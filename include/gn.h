@@ -106,6 +106,35 @@ GN_API int gn_bwd(const void* dy, const void* x, const float* mean, const float*
            int dtype, void* dx, float* dgamma, float* dbeta, void* workspace,
            size_t workspace_bytes, void* stream);
 
+/* Size of the device scratch area that gn_fwd_static_ws uses (per device). */
+#define GN_STATIC_WS_BYTES ((size_t)4 << 20)
+
+/* gn_fwd for callers that cannot allocate device memory.  (The pages have no
+ * counterpart: this entry point exists for the library's users.)  Some callers
+ * have no way to provide the workspace gn_fwd asks for: serving code that runs
+ * under a fixed memory budget and must not allocate once it has started,
+ * plugins whose host framework gives them no allocator, and code running where
+ * calling cudaMalloc is not permitted.  This call takes the same arguments as
+ * gn_fwd without the workspace, and computes the same results with the same
+ * kernels, using instead a scratch area that the library holds in a statically
+ * sized device array of GN_STATIC_WS_BYTES bytes.  It calls no cudaMalloc,
+ * cudaFree or other allocating routine.
+ *  - The array is reserved on every device that loads the library and stays
+ *    reserved until the process exits.
+ *  - A problem whose gn_workspace_size(GN_OP_FWD, ...) exceeds
+ *    GN_STATIC_WS_BYTES is rejected with GN_ERR_WORKSPACE before anything is
+ *    enqueued.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current); make that first call
+ *    before any stream capture.
+ *  - Each call clears the part of the array it uses (cudaMemsetAsync on
+ *    `stream`) before its kernels run.
+ *  - All calls share the one array: calls that overlap on the GPU (on two
+ *    streams, or from two host threads) race and must not be made. */
+GN_API int gn_fwd_static_ws(const void* x, int64_t N, int64_t C, int64_t HW, int64_t G,
+                            int layout, int dtype, const float* gamma, const float* beta,
+                            float eps, void* y, float* mean, float* rstd, void* stream);
+
 /* Static, human-readable name of a status code. */
 GN_API const char* gn_status_string(int status);
 
