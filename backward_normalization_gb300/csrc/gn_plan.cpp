@@ -98,6 +98,16 @@ int64_t resident_clusters(const Geom& g, int op) {
   return nc;
 }
 
+// The automatic choice, from measurements on GB300: the resident kernel wins
+// for channels_last forwards and for small NCHW units; for large NCHW units
+// and the channels_last backward the two-kernel path is faster today (the
+// resident kernel cannot keep every SM streaming there).
+bool resident_preferred(const Geom& g, int op) {
+  const int esz = g.dtype == kF32 ? 4 : 2;
+  if (g.layout == kNHWC) return op == kFwd;
+  return g.Cg * g.HW * esz <= (1 << 20);
+}
+
 // Fills the resident-regime fields of g; false when the problem does not fit
 // the regime (the two-kernel path then runs).
 bool plan_resident(Geom& g, int op) {
@@ -359,7 +369,11 @@ Geom make_geom(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout, 
     g.keep_from = item_len - (int64_t)((double)item_len * keep_frac);
   g.regime = kRegimeGeneric;
   const int ov = g_regime_override.load();
-  if (ov != kRegimeGeneric) plan_resident(g, op);
+  if (ov == kRegimeResident) {
+    plan_resident(g, op);  // wherever the problem fits the regime
+  } else if (ov == kRegimeAuto && resident_preferred(g, op)) {
+    plan_resident(g, op);
+  }
   return g;
 }
 

@@ -158,11 +158,11 @@ GN_API int gn_set_timing_events(void* ev_begin, void* ev_mid, void* ev_end);
 #define GN_REGIME_TWO_KERNEL 0
 #define GN_REGIME_RESIDENT 1
 
-/* Test hook, process-wide: GN_REGIME_AUTO (default) lets each call choose;
- * GN_REGIME_TWO_KERNEL forces the two-kernel path; GN_REGIME_RESIDENT is the
- * same as automatic (the resident regime wherever it applies).  Not
- * thread-safe with respect to calls in flight on other threads.  Returns a
- * gn_status. */
+/* Test hook, process-wide: GN_REGIME_AUTO (default) lets each call choose
+ * the faster family for its shape; GN_REGIME_TWO_KERNEL forces the two-kernel
+ * path; GN_REGIME_RESIDENT forces the resident regime wherever the problem
+ * fits it (else the two-kernel path runs).  Not thread-safe with respect to
+ * calls in flight on other threads.  Returns a gn_status. */
 GN_API int gn_set_regime(int regime);
 
 /* What a call would run, for tests and reports (host-only, no launch). */

@@ -145,6 +145,12 @@ def test_regime_choice(gn):
         assert d.regime == 0 and d.launches == 2
     finally:
         gn.set_regime(gn.REGIME_AUTO)
+    gn.set_regime(gn.REGIME_RESIDENT)
+    try:
+        d = gn.plan_info(1, 8, 320, 4096, 32, "nhwc", "bf16")
+        assert d.regime == 1 and d.launches == 1
+    finally:
+        gn.set_regime(gn.REGIME_AUTO)
     with pytest.raises(gn.GnError):
         gn.set_regime(7)
 

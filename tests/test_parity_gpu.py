@@ -54,11 +54,14 @@ STREAMING = [
 ]
 
 
-@pytest.fixture(params=["auto", "two_kernel"])
+REGIMES = {"auto": gn.REGIME_AUTO, "two_kernel": gn.REGIME_TWO_KERNEL, "resident": gn.REGIME_RESIDENT}
+
+
+@pytest.fixture(params=list(REGIMES))
 def regime(request):
-    """Runs a test with the automatic kernel choice and with the two-kernel
-    path forced, so both families see every case."""
-    gn.set_regime(gn.REGIME_AUTO if request.param == "auto" else gn.REGIME_TWO_KERNEL)
+    """Runs a test under the automatic kernel choice and with each family
+    forced, so both families see every case they can run."""
+    gn.set_regime(REGIMES[request.param])
     yield request.param
     gn.set_regime(gn.REGIME_AUTO)
 
@@ -276,7 +279,9 @@ def _sample_offsets(w, k=4096, seed=0):
     return np.unique(np.concatenate([idx, edge])).astype(np.int64)
 
 
-FULL = [(w, "auto") for w in synth.WORKLOADS[1:]] + [(synth.WORKLOADS[3], "two_kernel")]
+FULL = ([(w, "auto") for w in synth.WORKLOADS[1:]]
+        + [(synth.WORKLOADS[3], "resident"), (synth.WORKLOADS[2], "resident"),
+           (synth.WORKLOADS[4], "two_kernel")])
 
 
 @pytest.mark.parametrize("w,reg", FULL, ids=[f"{w.name}-{r}" for w, r in FULL])
@@ -286,7 +291,7 @@ def test_full_size_sampled(w, reg):
     rerun.  Large NCHW inputs are handed to the oracle one sample at a time
     (the statistics of sample n depend on sample n only)."""
     dev = "cuda"
-    gn.set_regime(gn.REGIME_AUTO if reg == "auto" else gn.REGIME_TWO_KERNEL)
+    gn.set_regime(REGIMES[reg])
     try:
         inp = synth.make_inputs(w, dev, seed=0)
         got = _gpu_run(inp, w)
