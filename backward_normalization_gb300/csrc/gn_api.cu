@@ -52,7 +52,9 @@ int prepare(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout, int
   char* ws = static_cast<char*>(workspace);
   p->tickets = reinterpret_cast<unsigned*>(ws + w.tickets);
   p->err = reinterpret_cast<unsigned*>(ws + w.err);
+  p->cnt1 = p->tickets + N + 1;
   p->part = reinterpret_cast<float2*>(ws + w.part);
+  p->part0 = p->g.l1 > 1 ? reinterpret_cast<float2*>(ws + w.part0) : p->part;
   p->chst = reinterpret_cast<float2*>(ws + w.chst);
   p->coef = reinterpret_cast<float2*>(ws + w.coef);
   return GN_OK;
@@ -209,9 +211,9 @@ int gn_plan_info(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout
   out->vector_width = g.vw;
   out->threads = g.tpb;
   out->ctas = g.regime == gn::kRegimeResident ? g.units * g.K : g.items;
-  out->partials = g.N * g.C * g.Tp;
+  out->partials = g.N * g.C * (g.T + (g.l1 > 1 ? g.Tp : 0));
   out->workspace_bytes = gn::ws_layout(op, g).total;
-  out->cluster_ctas = g.regime == gn::kRegimeResident ? g.K : g.cl;
+  out->cluster_ctas = g.regime == gn::kRegimeResident ? g.K : 1;
   const int64_t mc = gn::plan_max_clusters(g, op);
   out->max_clusters = mc > 0 ? (int)mc : 0;
   if (g.regime == gn::kRegimeResident) {
@@ -219,9 +221,9 @@ int gn_plan_info(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout
   } else {
     size_t sm = 0;
     if (g.layout == GN_LAYOUT_NHWC)
-      gn::nhwc_first_kernel(g, op == GN_OP_BWD, &sm);
+      gn::nhwc_kernel(g, op == GN_OP_BWD, 0, &sm);
     else
-      gn::nchw_first_kernel(g, op == GN_OP_BWD, &sm);
+      gn::nchw_kernel(g, op == GN_OP_BWD, 0, &sm);
     out->smem_bytes = sm;
   }
   return GN_OK;

@@ -204,14 +204,26 @@ __device__ __forceinline__ void finalize_params(const KParams& p, float* sm) {
   }
 }
 
-// Tail of every CTA that published a cluster-level partial: arrive on the
-// sample's counter and, if the sample is now complete, run its finalisation
-// (and, in the backward, the parameter-gradient step once every sample is
-// complete).  Must be reached by all threads of the CTA.
-template <typename T, bool kBwd>
-__device__ __forceinline__ void arrive_and_finalize(const KParams& p, int64_t n, float* sm,
+// Tail of every first-kernel CTA, after it has written its item record.
+// With level-1 groups (l1 > 1) the CTA arrives on its group's counter; the
+// group's last CTA runs merge() (the group record from its item records, in
+// item order) and arrives on the sample's counter.  The sample's last arrival
+// runs its finalisation and, in the backward, the last sample runs the
+// parameter-gradient step.  Every counter is reset by the CTA that completed
+// it.  Must be reached by all threads of the CTA.
+template <typename T, bool kBwd, typename Merge>
+__device__ __forceinline__ void arrive_and_finalize(const KParams& p, int64_t n, int64_t group1,
+                                                    unsigned gsize, Merge merge, float* sm,
                                                     int64_t sm_floats) {
   __shared__ int s_last;
+  if (p.g.l1 > 1) {
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = publish_and_arrive(p.cnt1 + group1, gsize);
+    __syncthreads();
+    if (!s_last) return;
+    merge();
+    if (threadIdx.x == 0) atomicExch(p.cnt1 + group1, 0u);
+  }
   __syncthreads();
   if (threadIdx.x == 0) s_last = publish_and_arrive(p.tickets + n, (unsigned)p.g.arrivals_per_n);
   __syncthreads();

@@ -20,9 +20,13 @@ enum Regime {
   kRegimeResident = 1,  // one kernel: a cluster holds a unit in shared memory
 };
 
-// How one call is cut into "items" (one CTA each).  Both kernels of an op use
-// the same items; the second kernel walks them in reverse so that the data the
-// first kernel read last is still in L2 when it is needed again.
+// How one call is cut into "items" for the two-kernel path.  Both kernels
+// run one CTA per item (one wave when the problem allows).  Each item's
+// partial sums go to a fixed slot, groups of l1 consecutive items are merged
+// by the group's last CTA, and the last group of a sample finalises it --
+// every sum in a fixed order, whichever CTA runs it.  The second kernel is
+// elementwise and walks the items in reverse order (the data the first kernel
+// read last is still in L2).
 struct Geom {
   int64_t N, C, HW, G, Cg;
   int layout, dtype;
@@ -41,11 +45,11 @@ struct Geom {
   int64_t RB;    // mode 1: rows per item
   // common
   int64_t T;     // items per (n, column block) (NHWC) or per row (NCHW)
-  int cl;        // CTAs per thread-block cluster of the first kernel (1 or 8);
-                 // a cluster = cl consecutive items that merge their partials through DSMEM
-  int64_t Tp;    // partial records per (n, c) = T / cl
-  int64_t cstride, tstride;  // partial index = n*C*Tp + c*cstride + t'*tstride
-  int64_t arrivals_per_n;    // cluster-level partials that complete sample n
+  int l1;        // items per level-1 group (1: no level-1 merge)
+  int64_t Tp;    // level-1 records per (n, c) = ceil(T / l1)
+  int64_t groups1;           // level-1 groups in the call
+  int64_t cstride, tstride;  // level-1 record index = n*C*Tp + c*cstride + t1*tstride
+  int64_t arrivals_per_n;    // level-1 records that complete sample n
   int64_t items_per_n;       // NCHW mode 1: items per sample
   int64_t items;
   int64_t keep_from;  // item-relative row/element index from which the first kernel
@@ -68,9 +72,10 @@ struct Geom {
 
 // Workspace layout (byte offsets, each 256-byte aligned).
 struct WsLayout {
-  size_t tickets;  // (N + 1) uint32 arrival counters: one per sample, one global
+  size_t tickets;  // uint32 counters: N per sample, 1 global, then one per level-1 group
   size_t err;      // uint32 error word (a bounded wait ran out)
-  size_t part;     // N*C*Tp float2 partial sums
+  size_t part0;    // N*C*T float2 item partial sums (when l1 > 1)
+  size_t part;     // N*C*Tp float2 level-1 partial sums
   size_t chst;     // N*C float2 per-channel results of the finalisation
   size_t coef;     // N*G float2 dx coefficients (backward only)
   size_t total;
@@ -90,8 +95,10 @@ struct KParams {
   float* dgamma;
   float* dbeta;
   float eps;
-  unsigned* tickets;
+  unsigned* tickets;  // [0, N) per sample, [N] global
+  unsigned* cnt1;     // per level-1 group
   unsigned* err;
+  float2* part0;      // item partials (== part when l1 == 1)
   float2* part;
   float2* chst;
   float2* coef;
@@ -103,9 +110,9 @@ int device_sm_count();
 int64_t plan_max_clusters(const Geom& g, int op);
 // Test hook: force a regime (kRegimeAuto = automatic choice).
 void set_regime_override(int regime);
-// CTAs of the op's first kernel that fit on the current device at once when
-// launched with g.tpb threads in clusters of `cl` CTAs (0: no device).
-int64_t resident_first_ctas(const Geom& g, int op, int cl);
+// CTAs of the op's first (second = 0) or second (second = 1) two-kernel-path
+// kernel that fit on the current device at once (0: no device visible).
+int64_t resident_ctas(const Geom& g, int op, int second);
 Geom make_geom(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout,
                int dtype, bool aligned);
 WsLayout ws_layout(int op, const Geom& g);
@@ -117,15 +124,14 @@ struct TimingEvents {
 };
 const TimingEvents& timing_events();
 
-// Launches the first kernel of an op (one CTA per item, clusters of g.cl CTAs).
-cudaError_t launch_first(const void* kernel, const KParams& p, size_t smem, cudaStream_t s);
 
 // kernels (gn_nhwc.cu / gn_nchw.cu): enqueue the two kernels of an op.
 cudaError_t launch_nhwc(const KParams& p, cudaStream_t s, bool bwd);
 cudaError_t launch_nchw(const KParams& p, cudaStream_t s, bool bwd);
-// The first kernel's function and dynamic shared memory for a plan.
-const void* nhwc_first_kernel(const Geom& g, bool bwd, size_t* smem);
-const void* nchw_first_kernel(const Geom& g, bool bwd, size_t* smem);
+// The first (second = 0) or second (second = 1) kernel's function and its
+// dynamic shared memory for a plan.
+const void* nhwc_kernel(const Geom& g, bool bwd, int second, size_t* smem);
+const void* nchw_kernel(const Geom& g, bool bwd, int second, size_t* smem);
 // gn_resident.cu
 const void* resident_kernel_ptr(const Geom& g, bool bwd);
 cudaError_t launch_resident(const KParams& p, cudaStream_t s, bool bwd);

@@ -1,17 +1,17 @@
-// gn_nchw.cu -- GroupNorm kernels for NCHW activations.
+// gn_nchw.cu -- two-kernel GroupNorm path for NCHW activations.
 //
 // Memory: element (n, c, hw) sits at (n*C + c)*HW + hw, so each (n, c)
 // channel plane ("row") is HW contiguous elements and a group is Cg
 // consecutive planes.  Two item shapes:
 //   mode 0 (large planes): item = (row, chunk of L elements), numbered
-//          row*T + chunk; the whole CTA strides the chunk with 16-byte loads.
-//          When a plane has T >= 8 chunks, 8 consecutive chunks form a
-//          thread-block cluster that merges its sums through DSMEM.
+//          row*T + chunk; the whole CTA strides the chunk with 16-byte loads
+//          and writes one record; groups of l1 chunks of a row are merged by
+//          their last CTA.
 //   mode 1 (small planes): item = RB consecutive rows of one sample; each warp
-//          takes whole rows; one partial per row.
-// The kernels mirror gn_nhwc.cu: stats/reduce kernels publish partial sums and
-// the last CTA of a sample finalises it; apply/dx kernels walk the items (and
-// the elements of a chunk) in reverse order.
+//          takes whole rows; one record per row.
+// As in gn_nhwc.cu, the last arrival of a sample finalises it, and the
+// elementwise second kernels walk the items (and the elements of a chunk) in
+// reverse order, starting on the data the first kernel left in L2.
 #include "gn_finalize.cuh"
 
 namespace gn {
@@ -44,26 +44,6 @@ __device__ __forceinline__ void acc_grad(const float (&xv)[VW], const float (&dv
   }
 }
 
-// Mode-0 tail of the first kernels: CTA sum (thread 0), cluster merge, publish.
-// Returns false in the CTAs that do not publish (cluster ranks other than 0).
-__device__ __forceinline__ bool publish_chunk(const KParams& p, int64_t row, int64_t ch, float a,
-                                              float b, float* sm) {
-  const Geom& g = p.g;
-  const float2 tot = block_sum2_t0(a, b, sm);
-  if (g.cl > 1) {
-    if (threadIdx.x == 0) {
-      sm[0] = tot.x;
-      sm[1] = tot.y;
-    }
-    cluster_sum_to_rank0<2>(sm, 1, 0, threadIdx.x == 0);
-    if (cluster_rank() != 0) return false;
-    if (threadIdx.x == 0) p.part[row * g.Tp + ch / g.cl] = make_float2(sm[0], sm[1]);
-  } else if (threadIdx.x == 0) {
-    p.part[row * g.Tp + ch] = tot;
-  }
-  return true;
-}
-
 struct Chunk {
   int64_t row, ch, h0, h1;
 };
@@ -77,6 +57,27 @@ __device__ __forceinline__ Chunk chunk_of(const Geom& g, int64_t item) {
   return c;
 }
 
+// Mode-0 tail of the first kernels: CTA sum, the chunk's record, the arrival
+// chain (group of l1 chunks of the row, then the sample).
+template <typename T, bool kBwd>
+__device__ __forceinline__ void publish_chunk(const KParams& p, const Chunk& k, float a, float b,
+                                              float* sm) {
+  const Geom& g = p.g;
+  const float2 tot = block_sum2_t0(a, b, sm);
+  if (threadIdx.x == 0) p.part0[k.row * g.T + k.ch] = tot;
+  const int64_t t1 = k.ch / g.l1;
+  const int64_t tlo = t1 * g.l1;
+  const unsigned gsize = (unsigned)((tlo + g.l1 < g.T) ? g.l1 : g.T - tlo);
+  auto merge = [&]() {
+    if (threadIdx.x != 0) return;
+    float ax = 0.f, ay = 0.f;
+    sum_records(p.part0 + k.row * g.T + tlo, 1, 0, 1, gsize, ax, ay);
+    p.part[k.row * g.Tp + t1] = make_float2(ax, ay);
+  };
+  arrive_and_finalize<T, kBwd>(p, k.row / g.C, k.row * g.Tp + t1, gsize, merge, sm,
+                               nchw_smem_floats(g));
+}
+
 // ------------------------------------------------------------------ forward
 template <typename T, int VW>
 __global__ void __launch_bounds__(512) nchw_fwd_stats(const __grid_constant__ KParams p) {
@@ -85,10 +86,8 @@ __global__ void __launch_bounds__(512) nchw_fwd_stats(const __grid_constant__ KP
   const int tid = threadIdx.x;
   const T* x = static_cast<const T*>(p.x);
   const uint64_t pfirst = policy_evict_first(), plast = policy_evict_last();
-  int64_t n;
   if (g.mode == 0) {
     const Chunk k = chunk_of(g, blockIdx.x);
-    n = k.row / g.C;
     const T* xr = x + k.row * g.HW;
     const float K = Elem<T>::to_f(xr[0]);
     const int64_t keep = k.h0 + g.keep_from;
@@ -108,10 +107,10 @@ __global__ void __launch_bounds__(512) nchw_fwd_stats(const __grid_constant__ KP
       Access<T, VW>::load(xr + h, v, h >= keep ? plast : pfirst);
       acc_shifted<VW>(v, K, s, q);
     }
-    if (!publish_chunk(p, k.row, k.ch, s, q, sm)) return;
+    publish_chunk<T, false>(p, k, s, q, sm);
   } else {
     const int64_t item = blockIdx.x;
-    n = item / g.items_per_n;
+    const int64_t n = item / g.items_per_n;
     const int64_t c0 = (item % g.items_per_n) * g.RB;
     const int64_t c1 = (c0 + g.RB < g.C) ? c0 + g.RB : g.C;
     const int lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
@@ -130,8 +129,8 @@ __global__ void __launch_bounds__(512) nchw_fwd_stats(const __grid_constant__ KP
       q = warp_sum_lane0(q);
       if (lane == 0) p.part[row] = make_float2(s, q);
     }
+    arrive_and_finalize<T, false>(p, n, 0, 1, [] {}, sm, nchw_smem_floats(g));
   }
-  arrive_and_finalize<T, false>(p, n, sm, nchw_smem_floats(g));
 }
 
 template <typename T, int VW>
@@ -204,10 +203,9 @@ __global__ void __launch_bounds__(512) nchw_bwd_reduce(const __grid_constant__ K
   const T* x = static_cast<const T*>(p.x);
   const T* dy = static_cast<const T*>(p.dy);
   const uint64_t pfirst = policy_evict_first(), plast = policy_evict_last();
-  int64_t n;
   if (g.mode == 0) {
     const Chunk k = chunk_of(g, blockIdx.x);
-    n = k.row / g.C;
+    const int64_t n = k.row / g.C;
     const float mu = __ldg(p.mean + n * g.G + (k.row % g.C) / g.Cg);
     const T* xr = x + k.row * g.HW;
     const T* dr = dy + k.row * g.HW;
@@ -233,10 +231,10 @@ __global__ void __launch_bounds__(512) nchw_bwd_reduce(const __grid_constant__ K
       Access<T, VW>::load(dr + h, dv, pol);
       acc_grad<VW>(xv, dv, mu, s1, s2);
     }
-    if (!publish_chunk(p, k.row, k.ch, s1, s2, sm)) return;
+    publish_chunk<T, true>(p, k, s1, s2, sm);
   } else {
     const int64_t item = blockIdx.x;
-    n = item / g.items_per_n;
+    const int64_t n = item / g.items_per_n;
     const int64_t c0 = (item % g.items_per_n) * g.RB;
     const int64_t c1 = (c0 + g.RB < g.C) ? c0 + g.RB : g.C;
     const int lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
@@ -257,8 +255,8 @@ __global__ void __launch_bounds__(512) nchw_bwd_reduce(const __grid_constant__ K
       s2 = warp_sum_lane0(s2);
       if (lane == 0) p.part[row] = make_float2(s1, s2);
     }
+    arrive_and_finalize<T, true>(p, n, 0, 1, [] {}, sm, nchw_smem_floats(g));
   }
-  arrive_and_finalize<T, true>(p, n, sm, nchw_smem_floats(g));
 }
 
 template <typename T, int VW>
@@ -336,8 +334,11 @@ cudaError_t run_op(const KParams& p, cudaStream_t s, bool bwd) {
   const size_t sm1 = sizeof(float) * nchw_smem_floats(g);
   const TimingEvents& ev = timing_events();
   if (ev.begin) cudaEventRecord(ev.begin, s);
-  cudaError_t e = launch_first(bwd ? (const void*)nchw_bwd_reduce<T, VW> : (const void*)nchw_fwd_stats<T, VW>,
-                               p, sm1, s);
+  if (bwd)
+    nchw_bwd_reduce<T, VW><<<(unsigned)g.items, g.tpb, sm1, s>>>(p);
+  else
+    nchw_fwd_stats<T, VW><<<(unsigned)g.items, g.tpb, sm1, s>>>(p);
+  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (ev.mid) cudaEventRecord(ev.mid, s);
   if (bwd)
@@ -354,25 +355,26 @@ cudaError_t dispatch_vw(const KParams& p, cudaStream_t s, bool bwd) {
   return p.g.vw == 1 ? run_op<T, 1>(p, s, bwd) : run_op<T, Elem<T>::VEC>(p, s, bwd);
 }
 
-
 template <typename T, int VW>
-const void* first_t(const Geom& g, bool bwd, size_t* smem) {
-  *smem = sizeof(float) * nchw_smem_floats(g);
+const void* kernel_t(const Geom& g, bool bwd, int second, size_t* smem) {
+  *smem = second ? 0 : sizeof(float) * nchw_smem_floats(g);
+  if (second) return bwd ? (const void*)nchw_bwd_dx<T, VW> : (const void*)nchw_fwd_apply<T, VW>;
   return bwd ? (const void*)nchw_bwd_reduce<T, VW> : (const void*)nchw_fwd_stats<T, VW>;
 }
 
 template <typename T>
-const void* first_vw(const Geom& g, bool bwd, size_t* smem) {
-  return g.vw == 1 ? first_t<T, 1>(g, bwd, smem) : first_t<T, Elem<T>::VEC>(g, bwd, smem);
+const void* kernel_vw(const Geom& g, bool bwd, int second, size_t* smem) {
+  return g.vw == 1 ? kernel_t<T, 1>(g, bwd, second, smem)
+                   : kernel_t<T, Elem<T>::VEC>(g, bwd, second, smem);
 }
 
 }  // namespace
 
-const void* nchw_first_kernel(const Geom& g, bool bwd, size_t* smem) {
+const void* nchw_kernel(const Geom& g, bool bwd, int second, size_t* smem) {
   switch (g.dtype) {
-    case kF32: return first_vw<float>(g, bwd, smem);
-    case kF16: return first_vw<__half>(g, bwd, smem);
-    default: return first_vw<__nv_bfloat16>(g, bwd, smem);
+    case kF32: return kernel_vw<float>(g, bwd, second, smem);
+    case kF16: return kernel_vw<__half>(g, bwd, second, smem);
+    default: return kernel_vw<__nv_bfloat16>(g, bwd, second, smem);
   }
 }
 

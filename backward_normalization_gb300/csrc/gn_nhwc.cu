@@ -1,21 +1,20 @@
-// gn_nhwc.cu -- GroupNorm kernels for channels_last activations.
+// gn_nhwc.cu -- two-kernel GroupNorm path for channels_last activations.
 //
 // Memory: element (n, c, hw) sits at (n*HW + hw)*C + c, so one spatial
 // position ("row") holds the C channels contiguously and a group is a run of
-// Cg channels inside every row.  A CTA owns an item = (sample n, column block
-// cb, block t of rb consecutive rows); each thread owns one column of vw
-// channels (one 16-byte vector) and walks the item's rows with stride rpi, so
-// every warp issues fully coalesced 16-byte loads and each thread's channels
-// (and their group constants) never change.  Items are numbered
-// ((n*ncb + cb)*T + t), so the cl CTAs of a thread-block cluster hold cl
-// consecutive row blocks of the same (n, cb).
+// Cg channels inside every row.  An item = (sample n, column block cb, block
+// t of rb consecutive rows), numbered ((n*ncb + cb)*T + t); each thread owns
+// one column of vw channels (one 16-byte vector) and walks the item's rows
+// with stride rpi, so every warp issues coalesced 16-byte loads and a
+// thread's channels (and their group constants) never change.
 //
-// Forward : nhwc_fwd_stats  -> per-(cluster, channel) shifted sums; the last
-//                              cluster of a sample merges them into mean/rstd
+// Forward : nhwc_fwd_stats  -> per-(item, channel) shifted sums; groups of l1
+//                              items, then the sample, are merged by their
+//                              last CTA into mean/rstd per group
 //           nhwc_fwd_apply  -> y = (x - mean) * rstd*gamma + beta
-// Backward: nhwc_bwd_reduce -> per-(cluster, channel) sum(dy), sum(dy*(x-mean));
-//                              the last cluster of a sample forms the dx
-//                              coefficients, the last sample dgamma/dbeta
+// Backward: nhwc_bwd_reduce -> per-(item, channel) sum(dy), sum(dy*(x-mean));
+//                              merged the same way into the dx coefficients,
+//                              the last sample forms dgamma/dbeta
 //           nhwc_bwd_dx     -> dx = rstd*gamma*dy + B*(x - mean) + D
 // The second kernel of each op walks items and rows in the reverse order of
 // the first, so it starts on the data the first kernel left in L2.
@@ -25,7 +24,7 @@ namespace gn {
 namespace {
 
 struct NhwcItem {
-  int64_t n, t, col, row0, row1;
+  int64_t n, t, cb, col, row0, row1;
   int j, r;
   bool active;
 };
@@ -37,52 +36,50 @@ __device__ __forceinline__ NhwcItem nhwc_item(const Geom& g, int64_t item) {
   it.r = tid / g.Wv;
   it.t = item % g.T;
   item /= g.T;
-  const int cb = (int)(item % g.ncb);
+  it.cb = item % g.ncb;
   it.n = item / g.ncb;
-  it.col = (int64_t)cb * g.Wv + it.j;
+  it.col = it.cb * g.Wv + it.j;
   it.active = (it.r < g.rpi) && (it.col < g.V);
   it.row0 = it.t * g.rb;
   it.row1 = (it.row0 + g.rb < g.HW) ? it.row0 + g.rb : g.HW;  // may be <= row0: empty item
   return it;
 }
 
-// Fixed-order tree over the rpi row lanes of each column, in shared memory.
-// On return thread (r = 0, j) holds the CTA totals in red[q*tpb + tid].
-template <int NQ>
-__device__ __forceinline__ void reduce_row_lanes(const Geom& g, float* red, const float (&v)[NQ],
-                                                 int r) {
-  const int tid = threadIdx.x, tpb = blockDim.x;
-#pragma unroll
-  for (int q = 0; q < NQ; ++q) red[q * tpb + tid] = v[q];
-  __syncthreads();
-  for (int s = 1; s < g.rpi; s <<= 1) {
-    if ((r % (2 * s)) == 0 && r + s < g.rpi) {
-#pragma unroll
-      for (int q = 0; q < NQ; ++q) red[q * tpb + tid] += red[q * tpb + tid + s * g.Wv];
-    }
-    __syncthreads();
-  }
-}
-
-// Shared tail of the two first kernels: CTA tree, cluster merge, publish the
-// cluster partial, arrive.
+// Tail of both first kernels.  CTA sums: each (column, value) pair adds its
+// rpi row lanes in lane order (one barrier, no tree).  Then the item record
+// part0[n][t][c], and the arrival chain (group of l1 items, sample).
 template <typename T, int VW, bool kBwd>
 __device__ __forceinline__ void publish_nhwc(const KParams& p, const NhwcItem& it, float* red,
                                              const float (&acc)[2 * VW]) {
   const Geom& g = p.g;
-  reduce_row_lanes<2 * VW>(g, red, acc, it.r);
-  if (g.cl > 1) {
-    cluster_sum_to_rank0<2 * VW>(red, blockDim.x, threadIdx.x, it.r == 0 && it.active);
-    if (cluster_rank() != 0) return;
-  }
-  if (it.r == 0 && it.active) {
-    float2* out = p.part + it.n * g.C * g.Tp + (it.t / g.cl) * g.C + it.col * VW;
+  const int tid = threadIdx.x, tpb = blockDim.x;
 #pragma unroll
-    for (int k = 0; k < VW; ++k)
-      out[k] = make_float2(red[(2 * k) * blockDim.x + threadIdx.x],
-                           red[(2 * k + 1) * blockDim.x + threadIdx.x]);
+  for (int q = 0; q < 2 * VW; ++q) red[q * tpb + tid] = acc[q];
+  __syncthreads();
+  float* rec = reinterpret_cast<float*>(p.part0 + it.n * g.C * g.T + it.t * g.C);
+  for (int pi = tid; pi < g.Wv * 2 * VW; pi += tpb) {
+    const int q = pi / g.Wv, j = pi % g.Wv;
+    const int64_t col = it.cb * g.Wv + j;
+    if (col >= g.V) continue;
+    float s = 0.f;
+    for (int r = 0; r < g.rpi; ++r) s += red[q * tpb + r * g.Wv + j];
+    rec[2 * (col * VW + q / 2) + (q & 1)] = s;
   }
-  arrive_and_finalize<T, kBwd>(p, it.n, red, (int64_t)2 * VW * blockDim.x);
+  const int64_t t1 = it.t / g.l1;
+  const int64_t tlo = t1 * g.l1;
+  const unsigned gsize = (unsigned)((tlo + g.l1 < g.T) ? g.l1 : g.T - tlo);
+  auto merge = [&]() {
+    // group record of the column block's channels: its items' records in item order
+    const int64_t c0 = it.cb * g.Wv * VW;
+    const int64_t c1 = (c0 + (int64_t)g.Wv * VW < g.C) ? c0 + (int64_t)g.Wv * VW : g.C;
+    for (int64_t c = c0 + tid; c < c1; c += tpb) {
+      float ax = 0.f, ay = 0.f;
+      sum_records(p.part0 + it.n * g.C * g.T + tlo * g.C + c, g.C, 0, 1, gsize, ax, ay);
+      p.part[it.n * g.C * g.Tp + t1 * g.C + c] = make_float2(ax, ay);
+    }
+  };
+  arrive_and_finalize<T, kBwd>(p, it.n, (it.n * g.ncb + it.cb) * g.Tp + t1, gsize, merge, red,
+                               (int64_t)2 * VW * tpb);
 }
 
 template <typename T, int VW>
@@ -132,49 +129,6 @@ __global__ void __launch_bounds__(512, 2) nhwc_fwd_stats(const __grid_constant__
     }
   }
   publish_nhwc<T, VW, false>(p, it, red, acc);
-}
-
-template <typename T, int VW>
-__global__ void __launch_bounds__(512) nhwc_fwd_apply(const __grid_constant__ KParams p) {
-  const Geom& g = p.g;
-  const NhwcItem it = nhwc_item(g, g.items - 1 - (int64_t)blockIdx.x);
-  if (!it.active) return;
-  const int64_t cnt = it.row1 - it.row0 - it.r;  // rows of this lane: r, r+step, ...
-  if (cnt <= 0) return;
-  float a[VW], mu[VW], b[VW];
-#pragma unroll
-  for (int k = 0; k < VW; ++k) {
-    const int64_t c = it.col * VW + k;
-    const int64_t ng = it.n * g.G + c / g.Cg;
-    const float r = __ldg(p.rstd + ng);
-    mu[k] = __ldg(p.mean + ng);
-    a[k] = p.gamma ? r * __ldg(p.gamma + c) : r;
-    b[k] = p.beta ? __ldg(p.beta + c) : 0.f;
-  }
-  const int64_t off = it.n * g.HW * g.C + it.col * VW;
-  const T* xn = static_cast<const T*>(p.x) + off;
-  T* yn = static_cast<T*>(p.out) + off;
-  const uint64_t pol = policy_evict_first();
-  const int64_t step = g.rpi;
-  int64_t row = it.row0 + it.r + ((cnt - 1) / step) * step;  // last row of the lane
-  for (; row - 3 * step >= it.row0; row -= 4 * step) {
-    float v[4][VW];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) Access<T, VW>::load(xn + (row - u * step) * g.C, v[u], pol);
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-#pragma unroll
-      for (int k = 0; k < VW; ++k) v[u][k] = fmaf(v[u][k] - mu[k], a[k], b[k]);
-      Access<T, VW>::store(yn + (row - u * step) * g.C, v[u], pol);
-    }
-  }
-  for (; row >= it.row0; row -= step) {
-    float v[VW];
-    Access<T, VW>::load(xn + row * g.C, v, pol);
-#pragma unroll
-    for (int k = 0; k < VW; ++k) v[k] = fmaf(v[k] - mu[k], a[k], b[k]);
-    Access<T, VW>::store(yn + row * g.C, v, pol);
-  }
 }
 
 template <typename T, int VW>
@@ -234,6 +188,49 @@ __global__ void __launch_bounds__(512, 2) nhwc_bwd_reduce(const __grid_constant_
 }
 
 template <typename T, int VW>
+__global__ void __launch_bounds__(512) nhwc_fwd_apply(const __grid_constant__ KParams p) {
+  const Geom& g = p.g;
+  const NhwcItem it = nhwc_item(g, g.items - 1 - (int64_t)blockIdx.x);
+  if (!it.active) return;
+  const int64_t cnt = it.row1 - it.row0 - it.r;  // rows of this lane: r, r+step, ...
+  if (cnt <= 0) return;
+  float a[VW], mu[VW], b[VW];
+#pragma unroll
+  for (int k = 0; k < VW; ++k) {
+    const int64_t c = it.col * VW + k;
+    const int64_t ng = it.n * g.G + c / g.Cg;
+    const float r = __ldg(p.rstd + ng);
+    mu[k] = __ldg(p.mean + ng);
+    a[k] = p.gamma ? r * __ldg(p.gamma + c) : r;
+    b[k] = p.beta ? __ldg(p.beta + c) : 0.f;
+  }
+  const int64_t off = it.n * g.HW * g.C + it.col * VW;
+  const T* xn = static_cast<const T*>(p.x) + off;
+  T* yn = static_cast<T*>(p.out) + off;
+  const uint64_t pol = policy_evict_first();
+  const int64_t step = g.rpi;
+  int64_t row = it.row0 + it.r + ((cnt - 1) / step) * step;  // last row of the lane
+  for (; row - 3 * step >= it.row0; row -= 4 * step) {
+    float v[4][VW];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) Access<T, VW>::load(xn + (row - u * step) * g.C, v[u], pol);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+#pragma unroll
+      for (int k = 0; k < VW; ++k) v[u][k] = fmaf(v[u][k] - mu[k], a[k], b[k]);
+      Access<T, VW>::store(yn + (row - u * step) * g.C, v[u], pol);
+    }
+  }
+  for (; row >= it.row0; row -= step) {
+    float v[VW];
+    Access<T, VW>::load(xn + row * g.C, v, pol);
+#pragma unroll
+    for (int k = 0; k < VW; ++k) v[k] = fmaf(v[k] - mu[k], a[k], b[k]);
+    Access<T, VW>::store(yn + row * g.C, v, pol);
+  }
+}
+
+template <typename T, int VW>
 __global__ void __launch_bounds__(512) nhwc_bwd_dx(const __grid_constant__ KParams p) {
   const Geom& g = p.g;
   const NhwcItem it = nhwc_item(g, g.items - 1 - (int64_t)blockIdx.x);
@@ -289,8 +286,11 @@ cudaError_t run_op(const KParams& p, cudaStream_t s, bool bwd) {
   const size_t sm1 = sizeof(float) * 2 * VW * g.tpb;
   const TimingEvents& ev = timing_events();
   if (ev.begin) cudaEventRecord(ev.begin, s);
-  cudaError_t e = launch_first(bwd ? (const void*)nhwc_bwd_reduce<T, VW> : (const void*)nhwc_fwd_stats<T, VW>,
-                               p, sm1, s);
+  if (bwd)
+    nhwc_bwd_reduce<T, VW><<<(unsigned)g.items, g.tpb, sm1, s>>>(p);
+  else
+    nhwc_fwd_stats<T, VW><<<(unsigned)g.items, g.tpb, sm1, s>>>(p);
+  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (ev.mid) cudaEventRecord(ev.mid, s);
   if (bwd)
@@ -307,25 +307,26 @@ cudaError_t dispatch_vw(const KParams& p, cudaStream_t s, bool bwd) {
   return p.g.vw == 1 ? run_op<T, 1>(p, s, bwd) : run_op<T, Elem<T>::VEC>(p, s, bwd);
 }
 
-
 template <typename T, int VW>
-const void* first_t(const Geom& g, bool bwd, size_t* smem) {
-  *smem = sizeof(float) * 2 * VW * g.tpb;
+const void* kernel_t(const Geom& g, bool bwd, int second, size_t* smem) {
+  *smem = second ? 0 : sizeof(float) * 2 * VW * g.tpb;
+  if (second) return bwd ? (const void*)nhwc_bwd_dx<T, VW> : (const void*)nhwc_fwd_apply<T, VW>;
   return bwd ? (const void*)nhwc_bwd_reduce<T, VW> : (const void*)nhwc_fwd_stats<T, VW>;
 }
 
 template <typename T>
-const void* first_vw(const Geom& g, bool bwd, size_t* smem) {
-  return g.vw == 1 ? first_t<T, 1>(g, bwd, smem) : first_t<T, Elem<T>::VEC>(g, bwd, smem);
+const void* kernel_vw(const Geom& g, bool bwd, int second, size_t* smem) {
+  return g.vw == 1 ? kernel_t<T, 1>(g, bwd, second, smem)
+                   : kernel_t<T, Elem<T>::VEC>(g, bwd, second, smem);
 }
 
 }  // namespace
 
-const void* nhwc_first_kernel(const Geom& g, bool bwd, size_t* smem) {
+const void* nhwc_kernel(const Geom& g, bool bwd, int second, size_t* smem) {
   switch (g.dtype) {
-    case kF32: return first_vw<float>(g, bwd, smem);
-    case kF16: return first_vw<__half>(g, bwd, smem);
-    default: return first_vw<__nv_bfloat16>(g, bwd, smem);
+    case kF32: return kernel_vw<float>(g, bwd, second, smem);
+    case kF16: return kernel_vw<__half>(g, bwd, second, smem);
+    default: return kernel_vw<__nv_bfloat16>(g, bwd, second, smem);
   }
 }
 

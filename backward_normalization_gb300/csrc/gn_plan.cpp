@@ -21,20 +21,21 @@ size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_regime_override{kRegimeAuto};
-constexpr int64_t kCluster = 8;           // CTAs per cluster in the first kernels
+constexpr int kGroup1 = 8;                // items per level-1 group (when an (n, c) has >= 16)
 constexpr double kKeepBytes = 64.0 * (1 << 20);  // input kept in L2 for the second kernel
 std::atomic<int> g_sm_cache[kMaxDevices];
 
 }  // namespace
 
 namespace {
-// Resident CTAs of the first kernel, or an estimate when no device is visible
-// (two 512-thread CTAs per SM, clusters fitting 4 per 19-SM GPC).
-int64_t resident_or(const Geom& g, int op, int cl, int sm_count) {
-  const int64_t r = resident_first_ctas(g, op, cl);
+// Co-resident CTAs of the op's first (second = 0) or second (second = 1)
+// kernel, or an estimate when no device is visible (two 512-thread or four
+// 256-thread CTAs per SM).
+int64_t resident_or(const Geom& g, int op, int second, int sm_count) {
+  const int64_t r = resident_ctas(g, op, second);
   if (r > 0) return r;
   const int64_t per_sm = g.tpb > 256 ? 2 : 4;
-  return cl > 1 ? (int64_t)sm_count * per_sm * 16 / 19 : (int64_t)sm_count * per_sm;
+  return (int64_t)sm_count * per_sm;
 }
 }  // namespace
 
@@ -201,7 +202,10 @@ bool plan_resident(Geom& g, int op) {
   if (r.smem > kSmemPerCta) return false;
   if (r.units * r.K > 0x7fffffffLL) return false;
   r.regime = kRegimeResident;
+  r.T = 0;  // no two-kernel partial records
+  r.l1 = 1;
   r.Tp = 0;
+  r.groups1 = 0;
   if (resident_clusters(r, op) == 0) return false;
   g = r;
   return true;
@@ -210,8 +214,8 @@ bool plan_resident(Geom& g, int op) {
 
 int64_t plan_max_clusters(const Geom& g, int op) {
   if (g.regime == kRegimeResident) return resident_clusters(g, op);
-  const int64_t r = resident_first_ctas(g, op, g.cl);
-  return r > 0 ? r / g.cl : -1;
+  const int64_t r = resident_ctas(g, op, 0);
+  return r > 0 ? r : -1;
 }
 
 int device_sm_count() {
@@ -233,44 +237,28 @@ int device_sm_count() {
   return sms;
 }
 
-int64_t resident_first_ctas(const Geom& g, int op, int cl) {
+int64_t resident_ctas(const Geom& g, int op, int second) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
   size_t smem = 0;
-  const void* fn = g.layout == kNHWC ? nhwc_first_kernel(g, op == kBwd, &smem)
-                                     : nchw_first_kernel(g, op == kBwd, &smem);
-  using Key = std::tuple<int, const void*, int, size_t, int>;
+  const void* fn = g.layout == kNHWC ? nhwc_kernel(g, op == kBwd, second, &smem)
+                                     : nchw_kernel(g, op == kBwd, second, &smem);
+  using Key = std::tuple<int, const void*, int, size_t>;
   static std::mutex mu;
   static std::map<Key, int64_t> cache;
-  const Key key{dev, fn, g.tpb, smem, cl};
+  const Key key{dev, fn, g.tpb, smem};
   {
     std::lock_guard<std::mutex> lock(mu);
     auto it = cache.find(key);
     if (it != cache.end()) return it->second;
   }
   int64_t r = 0;
-  if (cl > 1) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)cl, 1, 1);
-    cfg.blockDim = dim3((unsigned)g.tpb, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)cl;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int nc = 0;
-    if (cudaOccupancyMaxActiveClusters(&nc, fn, &cfg) == cudaSuccess) r = (int64_t)nc * cl;
-  } else {
-    int nb = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fn, g.tpb, smem) == cudaSuccess)
-      r = (int64_t)nb * device_sm_count();
-  }
+  int nb = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fn, g.tpb, smem) == cudaSuccess)
+    r = (int64_t)nb * device_sm_count();
   cudaGetLastError();
   std::lock_guard<std::mutex> lock(mu);
   cache[key] = r;
@@ -301,21 +289,14 @@ Geom make_geom(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout, 
     g.rpi = 512 / g.Wv;
     if (g.rpi < 1) g.rpi = 1;
     g.tpb = g.Wv * g.rpi;
-    // One wave: as many row blocks per (n, cb) as the resident clusters allow.
+    // One wave: as many row blocks per (n, cb) as CTAs fit on the device.
     const int64_t units = N * g.ncb;
-    const int64_t r8 = resident_or(g, op, kCluster, sm_count);
-    int64_t T = (r8 / units) / kCluster * kCluster;
-    if (T >= kCluster) {
-      T = (T < rup(cdiv(HW, g.rpi), kCluster)) ? T : rup(cdiv(HW, g.rpi), kCluster);
-    } else {
-      const int64_t r1 = resident_or(g, op, 1, sm_count);
-      T = clamp64(r1 / units, 1, cdiv(HW, g.rpi));
-      if (T >= kCluster) T = T / kCluster * kCluster;
-    }
+    const int64_t T = clamp64(resident_or(g, op, 0, sm_count) / units, 1, cdiv(HW, g.rpi));
     g.rb = rup(cdiv(HW, T), g.rpi);
     g.T = T;  // trailing items may be empty when rb*T > HW
-    g.cl = T % kCluster == 0 ? kCluster : 1;
-    g.Tp = T / g.cl;
+    g.l1 = T >= 2 * kGroup1 ? kGroup1 : 1;
+    g.Tp = cdiv(T, g.l1);
+    g.groups1 = g.l1 > 1 ? units * g.Tp : 0;
     g.cstride = 1;
     g.tstride = C;
     g.arrivals_per_n = g.Tp * g.ncb;
@@ -327,18 +308,12 @@ Geom make_geom(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout, 
       g.mode = 0;
       g.tpb = 512;
       const int64_t pmax = cdiv(HW, (int64_t)g.tpb * g.vw);
-      const int64_t r8 = resident_or(g, op, kCluster, sm_count);
-      int64_t P = (r8 / (N * C)) / kCluster * kCluster;
-      if (P >= kCluster) {
-        P = (P < rup(pmax, kCluster)) ? P : rup(pmax, kCluster);
-      } else {
-        P = clamp64(resident_or(g, op, 1, sm_count) / (N * C), 1, pmax);
-        if (P >= kCluster) P = P / kCluster * kCluster;
-      }
+      const int64_t P = clamp64(resident_or(g, op, 0, sm_count) / (N * C), 1, pmax);
       g.L = rup(cdiv(HW, P), g.vw);
       g.T = P;  // trailing chunks may be empty when L*P > HW
-      g.cl = P % kCluster == 0 ? kCluster : 1;
-      g.Tp = P / g.cl;
+      g.l1 = P >= 2 * kGroup1 ? kGroup1 : 1;
+      g.Tp = cdiv(P, g.l1);
+      g.groups1 = g.l1 > 1 ? N * C * g.Tp : 0;
       g.cstride = g.Tp;
       g.tstride = 1;
       g.arrivals_per_n = C * g.Tp;
@@ -347,10 +322,11 @@ Geom make_geom(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout, 
     } else {
       g.mode = 1;
       g.tpb = 256;
-      g.RB = clamp64(cdiv(N * C, resident_or(g, op, 1, sm_count)), 8, C);
+      g.RB = clamp64(cdiv(N * C, resident_or(g, op, 0, sm_count)), 8, C);
       g.T = 1;
-      g.cl = 1;
+      g.l1 = 1;
       g.Tp = 1;
+      g.groups1 = 0;
       g.cstride = 1;
       g.tstride = 1;
       g.items_per_n = cdiv(C, g.RB);
@@ -381,9 +357,11 @@ WsLayout ws_layout(int op, const Geom& g) {
   WsLayout w{};
   size_t off = 0;
   w.tickets = off;
-  off = align256(off + sizeof(unsigned) * (size_t)(g.N + 1));
+  off = align256(off + sizeof(unsigned) * (size_t)(g.N + 1 + g.groups1));
   w.err = off;
   off = align256(off + sizeof(unsigned));
+  w.part0 = off;
+  if (g.l1 > 1) off = align256(off + 2 * sizeof(float) * (size_t)(g.N * g.C * g.T));
   w.part = off;
   off = align256(off + 2 * sizeof(float) * (size_t)(g.N * g.C * g.Tp));
   w.chst = off;
@@ -392,25 +370,6 @@ WsLayout ws_layout(int op, const Geom& g) {
   if (op == kBwd) off = align256(off + 2 * sizeof(float) * (size_t)(g.N * g.G));
   w.total = off;
   return w;
-}
-
-cudaError_t launch_first(const void* kernel, const KParams& p, size_t smem, cudaStream_t s) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)p.g.items, 1, 1);
-  cfg.blockDim = dim3((unsigned)p.g.tpb, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  if (p.g.cl > 1) {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)p.g.cl;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-  }
-  void* args[] = {const_cast<KParams*>(&p)};
-  return cudaLaunchKernelExC(&cfg, kernel, args);
 }
 
 }  // namespace gn
