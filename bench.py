@@ -348,14 +348,14 @@ def run_ours(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
 
-    from backward_normalization_gb300 import gn, synth
+    from backward_normalization_gb300 import gn, replicas, synth
 
     gn.lib()
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream()
     w = synth.BY_NAME[WORKLOAD]
-    inp = synth.make_inputs(w, dev, seed=rank)
+    inp = synth.make_inputs(w, dev, seed=replicas.rank_seed(0, rank))
     x, dy, gm, bt = inp["x"], inp["dy"], inp["gamma"], inp["beta"]
     y = torch.empty_like(x)
     dx = torch.empty_like(x)
@@ -364,7 +364,8 @@ def run_ours(args, rank, world, local_rank):
     dg = torch.empty(w.C, device=dev)
     db = torch.empty(w.C, device=dev)
     ws = gn.alloc_workspace(gn.OP_BWD, w.N, w.C, w.HW, w.G, w.layout, x.dtype, dev)
-    gathered = torch.empty(world, 2 * w.C, device=dev) if world > 1 else None
+    replicas.broadcast_params(gm, bt)  # one model: rank 0's gamma and beta everywhere
+    grad_sum = replicas.ParamGradSum(w.C, dev)
     flush_buf = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     flush_out = torch.empty((), dtype=torch.float32, device=dev)
 
@@ -384,14 +385,7 @@ def run_ours(args, rank, world, local_rank):
             gn.set_timing_events()
         if rc:
             raise RuntimeError(f"gn call failed: {rc}")
-        if world > 1:
-            # dgamma/dbeta summed over ranks in rank order (deterministic)
-            dist.all_gather_into_tensor(gathered.view(-1), torch.cat([dg, db]))
-            tot = gathered[0].clone()
-            for r in range(1, world):
-                tot += gathered[r]
-            dg.copy_(tot[:w.C])
-            db.copy_(tot[w.C:])
+        grad_sum(dg, db)  # dgamma/dbeta over all ranks, rank order (no-op on one rank)
 
     for _ in range(args.warmup):
         step()
