@@ -346,4 +346,38 @@ __device__ __forceinline__ unsigned cluster_rank() {
   return cg::this_cluster().block_rank();
 }
 
+// ------------------------------------------- programmatic dependent launch
+// The two-kernel path launches every kernel with programmatic stream
+// serialisation: a kernel may be scheduled while the previous kernel on the
+// stream is still running, and waits (grid_dependency_wait) for that kernel to
+// complete and its writes to be visible before it touches global memory that
+// earlier work produced or will read.  Each kernel lets its successor launch
+// as soon as all of its own CTAs are running (grid_launch_dependents), so the
+// successor's CTAs take the SMs as this kernel's CTAs exit instead of after a
+// launch gap.  Without the launch attribute both instructions are no-ops.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Host: launches kernel(p) on `grid` CTAs with the programmatic-serialisation
+// attribute (see above).
+template <typename Kernel>
+inline cudaError_t launch_pdl(Kernel kernel, int64_t grid, int block, size_t smem,
+                              cudaStream_t s, const KParams& p) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  cfg.blockDim = dim3((unsigned)block, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
 }  // namespace gn

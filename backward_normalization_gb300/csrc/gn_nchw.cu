@@ -81,6 +81,8 @@ __device__ __forceinline__ void publish_chunk(const KParams& p, const Chunk& k, 
 // ------------------------------------------------------------------ forward
 template <typename T, int VW>
 __global__ void __launch_bounds__(512) nchw_fwd_stats(const __grid_constant__ KParams p) {
+  grid_dependency_wait();  // the previous kernel's results (and x, dy) are complete
+  grid_launch_dependents();
   extern __shared__ float sm[];
   const Geom& g = p.g;
   const int tid = threadIdx.x;
@@ -135,6 +137,8 @@ __global__ void __launch_bounds__(512) nchw_fwd_stats(const __grid_constant__ KP
 
 template <typename T, int VW>
 __global__ void __launch_bounds__(512) nchw_fwd_apply(const __grid_constant__ KParams p) {
+  grid_dependency_wait();  // the previous kernel's results (and x, dy) are complete
+  grid_launch_dependents();
   const Geom& g = p.g;
   const int tid = threadIdx.x;
   const T* x = static_cast<const T*>(p.x);
@@ -197,6 +201,8 @@ __global__ void __launch_bounds__(512) nchw_fwd_apply(const __grid_constant__ KP
 // ----------------------------------------------------------------- backward
 template <typename T, int VW>
 __global__ void __launch_bounds__(512) nchw_bwd_reduce(const __grid_constant__ KParams p) {
+  grid_dependency_wait();  // the previous kernel's results (and x, dy) are complete
+  grid_launch_dependents();
   extern __shared__ float sm[];
   const Geom& g = p.g;
   const int tid = threadIdx.x;
@@ -261,6 +267,8 @@ __global__ void __launch_bounds__(512) nchw_bwd_reduce(const __grid_constant__ K
 
 template <typename T, int VW>
 __global__ void __launch_bounds__(512) nchw_bwd_dx(const __grid_constant__ KParams p) {
+  grid_dependency_wait();  // the previous kernel's results (and x, dy) are complete
+  grid_launch_dependents();
   const Geom& g = p.g;
   const int tid = threadIdx.x;
   const T* x = static_cast<const T*>(p.x);
@@ -334,18 +342,12 @@ cudaError_t run_op(const KParams& p, cudaStream_t s, bool bwd) {
   const size_t sm1 = sizeof(float) * nchw_smem_floats(g);
   const TimingEvents& ev = timing_events();
   if (ev.begin) cudaEventRecord(ev.begin, s);
-  if (bwd)
-    nchw_bwd_reduce<T, VW><<<(unsigned)g.items, g.tpb, sm1, s>>>(p);
-  else
-    nchw_fwd_stats<T, VW><<<(unsigned)g.items, g.tpb, sm1, s>>>(p);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = bwd ? launch_pdl(nchw_bwd_reduce<T, VW>, g.items, g.tpb, sm1, s, p)
+                      : launch_pdl(nchw_fwd_stats<T, VW>, g.items, g.tpb, sm1, s, p);
   if (e != cudaSuccess) return e;
   if (ev.mid) cudaEventRecord(ev.mid, s);
-  if (bwd)
-    nchw_bwd_dx<T, VW><<<(unsigned)g.items, g.tpb, 0, s>>>(p);
-  else
-    nchw_fwd_apply<T, VW><<<(unsigned)g.items, g.tpb, 0, s>>>(p);
-  e = cudaGetLastError();
+  e = bwd ? launch_pdl(nchw_bwd_dx<T, VW>, g.items, g.tpb, 0, s, p)
+          : launch_pdl(nchw_fwd_apply<T, VW>, g.items, g.tpb, 0, s, p);
   if (ev.end) cudaEventRecord(ev.end, s);
   return e;
 }

@@ -84,6 +84,8 @@ __device__ __forceinline__ void publish_nhwc(const KParams& p, const NhwcItem& i
 
 template <typename T, int VW>
 __global__ void __launch_bounds__(512, 2) nhwc_fwd_stats(const __grid_constant__ KParams p) {
+  grid_dependency_wait();  // the previous kernel's results (and x, dy) are complete
+  grid_launch_dependents();
   extern __shared__ float red[];
   const Geom& g = p.g;
   const NhwcItem it = nhwc_item(g, blockIdx.x);
@@ -133,6 +135,8 @@ __global__ void __launch_bounds__(512, 2) nhwc_fwd_stats(const __grid_constant__
 
 template <typename T, int VW>
 __global__ void __launch_bounds__(512, 2) nhwc_bwd_reduce(const __grid_constant__ KParams p) {
+  grid_dependency_wait();  // the previous kernel's results (and x, dy) are complete
+  grid_launch_dependents();
   extern __shared__ float red[];
   const Geom& g = p.g;
   const NhwcItem it = nhwc_item(g, blockIdx.x);
@@ -189,6 +193,8 @@ __global__ void __launch_bounds__(512, 2) nhwc_bwd_reduce(const __grid_constant_
 
 template <typename T, int VW>
 __global__ void __launch_bounds__(512) nhwc_fwd_apply(const __grid_constant__ KParams p) {
+  grid_dependency_wait();  // the previous kernel's results (and x, dy) are complete
+  grid_launch_dependents();
   const Geom& g = p.g;
   const NhwcItem it = nhwc_item(g, g.items - 1 - (int64_t)blockIdx.x);
   if (!it.active) return;
@@ -232,6 +238,8 @@ __global__ void __launch_bounds__(512) nhwc_fwd_apply(const __grid_constant__ KP
 
 template <typename T, int VW>
 __global__ void __launch_bounds__(512) nhwc_bwd_dx(const __grid_constant__ KParams p) {
+  grid_dependency_wait();  // the previous kernel's results (and x, dy) are complete
+  grid_launch_dependents();
   const Geom& g = p.g;
   const NhwcItem it = nhwc_item(g, g.items - 1 - (int64_t)blockIdx.x);
   if (!it.active) return;
@@ -286,18 +294,12 @@ cudaError_t run_op(const KParams& p, cudaStream_t s, bool bwd) {
   const size_t sm1 = sizeof(float) * 2 * VW * g.tpb;
   const TimingEvents& ev = timing_events();
   if (ev.begin) cudaEventRecord(ev.begin, s);
-  if (bwd)
-    nhwc_bwd_reduce<T, VW><<<(unsigned)g.items, g.tpb, sm1, s>>>(p);
-  else
-    nhwc_fwd_stats<T, VW><<<(unsigned)g.items, g.tpb, sm1, s>>>(p);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = bwd ? launch_pdl(nhwc_bwd_reduce<T, VW>, g.items, g.tpb, sm1, s, p)
+                      : launch_pdl(nhwc_fwd_stats<T, VW>, g.items, g.tpb, sm1, s, p);
   if (e != cudaSuccess) return e;
   if (ev.mid) cudaEventRecord(ev.mid, s);
-  if (bwd)
-    nhwc_bwd_dx<T, VW><<<(unsigned)g.items, g.tpb, 0, s>>>(p);
-  else
-    nhwc_fwd_apply<T, VW><<<(unsigned)g.items, g.tpb, 0, s>>>(p);
-  e = cudaGetLastError();
+  e = bwd ? launch_pdl(nhwc_bwd_dx<T, VW>, g.items, g.tpb, 0, s, p)
+          : launch_pdl(nhwc_fwd_apply<T, VW>, g.items, g.tpb, 0, s, p);
   if (ev.end) cudaEventRecord(ev.end, s);
   return e;
 }
