@@ -45,6 +45,19 @@ __device__ __forceinline__ NhwcItem nhwc_item(const Geom& g, int64_t item) {
   return it;
 }
 
+// Values that depend only on the group, for the vw channels of a thread's
+// vector: NG = 1 when the vector lies inside one group (vw divides Cg, or
+// vw = 1), else NG = vw values, one per channel.  The single value keeps the
+// per-thread constants of the wide vectors in few registers.
+template <int VW, int NG>
+struct PerGroup {
+  float v[NG];
+  __device__ __forceinline__ float operator[](int e) const { return v[NG == 1 ? 0 : e]; }
+};
+
+// Whether a plan's vectors lie inside one group each.
+inline bool one_group_per_vector(const Geom& g) { return g.vw == 1 || g.Cg % g.vw == 0; }
+
 // Tail of both first kernels.  CTA sums: each (column, value) pair adds its
 // rpi row lanes in lane order (one barrier, no tree).  Then the item record
 // part0[n][t][c], and the arrival chain (group of l1 items, sample).
@@ -133,7 +146,7 @@ __global__ void __launch_bounds__(512, 2) nhwc_fwd_stats(const __grid_constant__
   publish_nhwc<T, VW, false>(p, it, red, acc);
 }
 
-template <typename T, int VW>
+template <typename T, int VW, int NG>
 __global__ void __launch_bounds__(512, 2) nhwc_bwd_reduce(const __grid_constant__ KParams p) {
   grid_dependency_wait();  // the previous kernel's results (and x, dy) are complete
   grid_launch_dependents();
@@ -144,9 +157,9 @@ __global__ void __launch_bounds__(512, 2) nhwc_bwd_reduce(const __grid_constant_
 #pragma unroll
   for (int q = 0; q < 2 * VW; ++q) acc[q] = 0.f;
   if (it.active && it.row0 < it.row1) {
-    float mu[VW];
+    PerGroup<VW, NG> mu;
 #pragma unroll
-    for (int k = 0; k < VW; ++k) mu[k] = __ldg(p.mean + it.n * g.G + (it.col * VW + k) / g.Cg);
+    for (int k = 0; k < NG; ++k) mu.v[k] = __ldg(p.mean + it.n * g.G + (it.col * VW + k) / g.Cg);
     const int64_t off = it.n * g.HW * g.C + it.col * VW;
     const T* xn = static_cast<const T*>(p.x) + off;
     const T* dyn = static_cast<const T*>(p.dy) + off;
@@ -191,8 +204,8 @@ __global__ void __launch_bounds__(512, 2) nhwc_bwd_reduce(const __grid_constant_
   publish_nhwc<T, VW, true>(p, it, red, acc);
 }
 
-template <typename T, int VW>
-__global__ void __launch_bounds__(512) nhwc_fwd_apply(const __grid_constant__ KParams p) {
+template <typename T, int VW, int NG>
+__global__ void __launch_bounds__(512, 2) nhwc_fwd_apply(const __grid_constant__ KParams p) {
   grid_dependency_wait();  // the previous kernel's results (and x, dy) are complete
   grid_launch_dependents();
   const Geom& g = p.g;
@@ -200,15 +213,16 @@ __global__ void __launch_bounds__(512) nhwc_fwd_apply(const __grid_constant__ KP
   if (!it.active) return;
   const int64_t cnt = it.row1 - it.row0 - it.r;  // rows of this lane: r, r+step, ...
   if (cnt <= 0) return;
-  float a[VW], mu[VW], b[VW];
+  PerGroup<VW, NG> mu;
+  float a[VW], b[VW];
 #pragma unroll
   for (int k = 0; k < VW; ++k) {
     const int64_t c = it.col * VW + k;
     const int64_t ng = it.n * g.G + c / g.Cg;
     const float r = __ldg(p.rstd + ng);
-    mu[k] = __ldg(p.mean + ng);
     a[k] = p.gamma ? r * __ldg(p.gamma + c) : r;
     b[k] = p.beta ? __ldg(p.beta + c) : 0.f;
+    if (NG > 1 || k == 0) mu.v[NG > 1 ? k : 0] = __ldg(p.mean + ng);
   }
   const int64_t off = it.n * g.HW * g.C + it.col * VW;
   const T* xn = static_cast<const T*>(p.x) + off;
@@ -236,8 +250,8 @@ __global__ void __launch_bounds__(512) nhwc_fwd_apply(const __grid_constant__ KP
   }
 }
 
-template <typename T, int VW>
-__global__ void __launch_bounds__(512) nhwc_bwd_dx(const __grid_constant__ KParams p) {
+template <typename T, int VW, int NG>
+__global__ void __launch_bounds__(512, 2) nhwc_bwd_dx(const __grid_constant__ KParams p) {
   grid_dependency_wait();  // the previous kernel's results (and x, dy) are complete
   grid_launch_dependents();
   const Geom& g = p.g;
@@ -245,17 +259,20 @@ __global__ void __launch_bounds__(512) nhwc_bwd_dx(const __grid_constant__ KPara
   if (!it.active) return;
   const int64_t cnt = it.row1 - it.row0 - it.r;
   if (cnt <= 0) return;
-  float A[VW], mu[VW], B[VW], D[VW];
+  PerGroup<VW, NG> mu, B, D;
+  float A[VW];
 #pragma unroll
   for (int k = 0; k < VW; ++k) {
     const int64_t c = it.col * VW + k;
     const int64_t ng = it.n * g.G + c / g.Cg;
     const float r = __ldg(p.rstd + ng);
-    const float2 cf = __ldcg(p.coef + ng);
-    mu[k] = __ldg(p.mean + ng);
     A[k] = p.gamma ? r * __ldg(p.gamma + c) : r;
-    B[k] = cf.x;
-    D[k] = cf.y;
+    if (NG > 1 || k == 0) {
+      const float2 cf = __ldcg(p.coef + ng);
+      mu.v[NG > 1 ? k : 0] = __ldg(p.mean + ng);
+      B.v[NG > 1 ? k : 0] = cf.x;
+      D.v[NG > 1 ? k : 0] = cf.y;
+    }
   }
   const int64_t off = it.n * g.HW * g.C + it.col * VW;
   const T* xn = static_cast<const T*>(p.x) + off;
@@ -264,18 +281,22 @@ __global__ void __launch_bounds__(512) nhwc_bwd_dx(const __grid_constant__ KPara
   const uint64_t pol = policy_evict_first();
   const int64_t step = g.rpi;
   int64_t row = it.row0 + it.r + ((cnt - 1) / step) * step;
+  using Raw = typename Access<T, VW>::Raw;
   for (; row - step >= it.row0; row -= 2 * step) {
-    float xv[2][VW], dv[2][VW];
+    Raw rx[2], rd[2];  // packed until used: fewer live registers
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
-      Access<T, VW>::load(xn + (row - u * step) * g.C, xv[u], pol);
-      Access<T, VW>::load(dyn + (row - u * step) * g.C, dv[u], pol);
+      rx[u] = Access<T, VW>::load_raw(xn + (row - u * step) * g.C, pol);
+      rd[u] = Access<T, VW>::load_raw(dyn + (row - u * step) * g.C, pol);
     }
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
+      float xv[VW], dv[VW];
+      Access<T, VW>::unpack(rx[u], xv);
+      Access<T, VW>::unpack(rd[u], dv);
 #pragma unroll
-      for (int k = 0; k < VW; ++k) xv[u][k] = fmaf(A[k], dv[u][k], fmaf(B[k], xv[u][k] - mu[k], D[k]));
-      Access<T, VW>::store(dxn + (row - u * step) * g.C, xv[u], pol);
+      for (int k = 0; k < VW; ++k) xv[k] = fmaf(A[k], dv[k], fmaf(B[k], xv[k] - mu[k], D[k]));
+      Access<T, VW>::store(dxn + (row - u * step) * g.C, xv, pol);
     }
   }
   for (; row >= it.row0; row -= step) {
@@ -288,38 +309,43 @@ __global__ void __launch_bounds__(512) nhwc_bwd_dx(const __grid_constant__ KPara
   }
 }
 
-template <typename T, int VW>
+template <typename T, int VW, int NG>
 cudaError_t run_op(const KParams& p, cudaStream_t s, bool bwd) {
   const Geom& g = p.g;
   const size_t sm1 = sizeof(float) * 2 * VW * g.tpb;
   const TimingEvents& ev = timing_events();
   if (ev.begin) cudaEventRecord(ev.begin, s);
-  cudaError_t e = bwd ? launch_pdl(nhwc_bwd_reduce<T, VW>, g.items, g.tpb, sm1, s, p)
+  cudaError_t e = bwd ? launch_pdl(nhwc_bwd_reduce<T, VW, NG>, g.items, g.tpb, sm1, s, p)
                       : launch_pdl(nhwc_fwd_stats<T, VW>, g.items, g.tpb, sm1, s, p);
   if (e != cudaSuccess) return e;
   if (ev.mid) cudaEventRecord(ev.mid, s);
-  e = bwd ? launch_pdl(nhwc_bwd_dx<T, VW>, g.items, g.tpb, 0, s, p)
-          : launch_pdl(nhwc_fwd_apply<T, VW>, g.items, g.tpb, 0, s, p);
+  e = bwd ? launch_pdl(nhwc_bwd_dx<T, VW, NG>, g.items, g.tpb, 0, s, p)
+          : launch_pdl(nhwc_fwd_apply<T, VW, NG>, g.items, g.tpb, 0, s, p);
   if (ev.end) cudaEventRecord(ev.end, s);
   return e;
 }
 
 template <typename T>
 cudaError_t dispatch_vw(const KParams& p, cudaStream_t s, bool bwd) {
-  return p.g.vw == 1 ? run_op<T, 1>(p, s, bwd) : run_op<T, Elem<T>::VEC>(p, s, bwd);
+  constexpr int V = Elem<T>::VEC;
+  if (p.g.vw == 1) return run_op<T, 1, 1>(p, s, bwd);
+  return one_group_per_vector(p.g) ? run_op<T, V, 1>(p, s, bwd) : run_op<T, V, V>(p, s, bwd);
 }
 
-template <typename T, int VW>
+template <typename T, int VW, int NG>
 const void* kernel_t(const Geom& g, bool bwd, int second, size_t* smem) {
   *smem = second ? 0 : sizeof(float) * 2 * VW * g.tpb;
-  if (second) return bwd ? (const void*)nhwc_bwd_dx<T, VW> : (const void*)nhwc_fwd_apply<T, VW>;
-  return bwd ? (const void*)nhwc_bwd_reduce<T, VW> : (const void*)nhwc_fwd_stats<T, VW>;
+  if (second)
+    return bwd ? (const void*)nhwc_bwd_dx<T, VW, NG> : (const void*)nhwc_fwd_apply<T, VW, NG>;
+  return bwd ? (const void*)nhwc_bwd_reduce<T, VW, NG> : (const void*)nhwc_fwd_stats<T, VW>;
 }
 
 template <typename T>
 const void* kernel_vw(const Geom& g, bool bwd, int second, size_t* smem) {
-  return g.vw == 1 ? kernel_t<T, 1>(g, bwd, second, smem)
-                   : kernel_t<T, Elem<T>::VEC>(g, bwd, second, smem);
+  constexpr int V = Elem<T>::VEC;
+  if (g.vw == 1) return kernel_t<T, 1, 1>(g, bwd, second, smem);
+  return one_group_per_vector(g) ? kernel_t<T, V, 1>(g, bwd, second, smem)
+                                 : kernel_t<T, V, V>(g, bwd, second, smem);
 }
 
 }  // namespace
