@@ -45,19 +45,38 @@ int prepare(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout, int
             bool aligned, void* workspace, size_t workspace_bytes, gn::KParams* p) {
   std::memset(p, 0, sizeof(*p));
   p->g = gn::make_geom(op, N, C, HW, G, layout, dtype, aligned);
-  if (p->g.regime != gn::kRegimeResident && (p->g.items <= 0 || p->g.items > 0x7fffffffLL))
+  if (p->g.regime == gn::kRegimeGeneric && (p->g.items <= 0 || p->g.items > 0x7fffffffLL))
     return GN_ERR_UNSUPPORTED;
   const gn::WsLayout w = gn::ws_layout(op, p->g);
   if (!workspace || workspace_bytes < w.total || !aligned16(workspace)) return GN_ERR_WORKSPACE;
   char* ws = static_cast<char*>(workspace);
   p->tickets = reinterpret_cast<unsigned*>(ws + w.tickets);
   p->err = reinterpret_cast<unsigned*>(ws + w.err);
-  p->cnt1 = p->tickets + N + 1;
+  // counters: one per unit, the global one, one per level-1 group, then (pipelined)
+  // a ready flag and a pass-2 counter per unit and the task queue
+  const int64_t U = p->g.units_fin;
+  p->cnt1 = p->tickets + U + 1;
+  if (p->g.regime == gn::kRegimePipelined) {
+    p->ready = p->cnt1 + p->g.groups1;
+    p->p2cnt = p->ready + U;
+    p->queue = p->p2cnt + U;
+  }
   p->part = reinterpret_cast<float2*>(ws + w.part);
   p->part0 = p->g.l1 > 1 ? reinterpret_cast<float2*>(ws + w.part0) : p->part;
   p->chst = reinterpret_cast<float2*>(ws + w.chst);
   p->coef = reinterpret_cast<float2*>(ws + w.coef);
   return GN_OK;
+}
+
+// Enqueues the plan's kernel(s).
+cudaError_t launch(const gn::KParams& p, cudaStream_t s, bool bwd) {
+  const bool nhwc = p.g.layout == GN_LAYOUT_NHWC;
+  switch (p.g.regime) {
+    case gn::kRegimeResident: return gn::launch_resident(p, s, bwd);
+    case gn::kRegimePipelined:
+      return nhwc ? gn::launch_nhwc_pipelined(p, s, bwd) : gn::launch_nchw_pipelined(p, s, bwd);
+    default: return nhwc ? gn::launch_nhwc(p, s, bwd) : gn::launch_nchw(p, s, bwd);
+  }
 }
 
 size_t ws_size_any_alignment(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout,
@@ -118,9 +137,7 @@ int gn_fwd(const void* x, int64_t N, int64_t C, int64_t HW, int64_t G, int layou
   p.rstd = rstd;
   p.eps = eps;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const cudaError_t e = p.g.regime == gn::kRegimeResident ? gn::launch_resident(p, s, false)
-                        : layout == GN_LAYOUT_NHWC       ? gn::launch_nhwc(p, s, false)
-                                                         : gn::launch_nchw(p, s, false);
+  const cudaError_t e = launch(p, s, false);
   return e == cudaSuccess ? GN_OK : cuda_fail(e);
 }
 
@@ -164,9 +181,7 @@ int gn_bwd(const void* dy, const void* x, const float* mean, const float* rstd,
   p.rstd = const_cast<float*>(rstd);
   p.dgamma = dgamma;
   p.dbeta = dbeta;
-  const cudaError_t e = p.g.regime == gn::kRegimeResident ? gn::launch_resident(p, s, true)
-                        : layout == GN_LAYOUT_NHWC       ? gn::launch_nhwc(p, s, true)
-                                                         : gn::launch_nchw(p, s, true);
+  const cudaError_t e = launch(p, s, true);
   return e == cudaSuccess ? GN_OK : cuda_fail(e);
 }
 
@@ -184,7 +199,8 @@ const char* gn_status_string(int status) {
 int gn_last_cuda_error(void) { return t_last_cuda_error; }
 
 int gn_set_regime(int regime) {
-  if (regime != GN_REGIME_AUTO && regime != GN_REGIME_TWO_KERNEL && regime != GN_REGIME_RESIDENT)
+  if (regime != GN_REGIME_AUTO && regime != GN_REGIME_TWO_KERNEL && regime != GN_REGIME_RESIDENT &&
+      regime != GN_REGIME_PIPELINED)
     return GN_ERR_INVALID;
   gn::set_regime_override(regime);
   return GN_OK;
@@ -207,17 +223,27 @@ int gn_plan_info(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout
   if (N == 0 || C == 0 || HW == 0) return GN_OK;
   const gn::Geom g = gn::make_geom(op, N, C, HW, G, layout, dtype, aligned != 0);
   out->regime = g.regime;
-  out->launches = g.regime == gn::kRegimeResident ? 1 : 2;
+  out->launches = g.regime == gn::kRegimeGeneric ? 2 : 1;
   out->vector_width = g.vw;
   out->threads = g.tpb;
-  out->ctas = g.regime == gn::kRegimeResident ? g.units * g.K : g.items;
+  out->ctas = g.regime == gn::kRegimeResident    ? g.units * g.K
+              : g.regime == gn::kRegimePipelined ? g.grid
+                                                 : g.items;
   out->partials = g.N * g.C * (g.T + (g.l1 > 1 ? g.Tp : 0));
   out->workspace_bytes = gn::ws_layout(op, g).total;
+  out->err_offset = gn::ws_layout(op, g).err;
   out->cluster_ctas = g.regime == gn::kRegimeResident ? g.K : 1;
   const int64_t mc = gn::plan_max_clusters(g, op);
   out->max_clusters = mc > 0 ? (int)mc : 0;
   if (g.regime == gn::kRegimeResident) {
     out->smem_bytes = g.smem;
+  } else if (g.regime == gn::kRegimePipelined) {
+    size_t sm = 0;
+    if (g.layout == GN_LAYOUT_NHWC)
+      gn::nhwc_pipelined_kernel(g, op == GN_OP_BWD, &sm);
+    else
+      gn::nchw_pipelined_kernel(g, op == GN_OP_BWD, &sm);
+    out->smem_bytes = sm;
   } else {
     size_t sm = 0;
     if (g.layout == GN_LAYOUT_NHWC)

@@ -1,7 +1,8 @@
 // gn_finalize.cuh -- the cross-CTA steps of both ops, run by the CTA whose
-// arrival completes a sample n (and, in the backward, by the CTA that
-// completes the last sample).  All sums run in a fixed order, so results are
-// bit-identical from run to run on the same device.
+// arrival completes a unit (a sample, or in the pipelined NCHW kernel one
+// (sample, group)) and, in the backward, by the CTA that completes the last
+// unit.  All sums run in a fixed order, so results are bit-identical from run
+// to run on the same device.
 #pragma once
 
 #include "gn_device.cuh"
@@ -45,27 +46,27 @@ __device__ __forceinline__ SliceLayout slice_layout(int64_t C, int64_t count) {
   return L;
 }
 
-// For every channel c of sample n, sums the g.Tp partial records of (n, c)
-// and calls fn(c, total) from one thread.  Slice s adds records s, s + nsl,
-// ... in order, then the slice sums are added in slice order.
+// For every channel c in [ca, cb) of sample n, sums the g.Tp partial records
+// of (n, c) and calls fn(c, total) from one thread.  Slice s adds records s,
+// s + nsl, ... in order, then the slice sums are added in slice order.
 // `sm` holds at least 2 * blockDim.x floats.  Ends with __syncthreads().
 template <typename Fn>
-__device__ __forceinline__ void sum_channel_partials(const KParams& p, int64_t n, float* sm,
-                                                     Fn fn) {
+__device__ __forceinline__ void sum_channel_partials(const KParams& p, int64_t n, int64_t ca,
+                                                     int64_t cb, float* sm, Fn fn) {
   const Geom& g = p.g;
-  const SliceLayout L = slice_layout(g.C, g.Tp);
+  const SliceLayout L = slice_layout(cb - ca, g.Tp);
   const float2* base = p.part + n * g.C * g.Tp;
-  for (int64_t c0 = 0; c0 < g.C; c0 += L.cpb) {
+  for (int64_t c0 = ca; c0 < cb; c0 += L.cpb) {
     const int64_t c = c0 + L.cl;
     float ax = 0.f, ay = 0.f;
-    if (L.sl < L.nsl && c < g.C)
+    if (L.sl < L.nsl && c < cb)
       sum_records(base + c * g.cstride, g.tstride, L.sl, L.nsl, g.Tp, ax, ay);
     if (L.sl < L.nsl) {
       sm[2 * (L.sl * L.cpb + L.cl)] = ax;
       sm[2 * (L.sl * L.cpb + L.cl) + 1] = ay;
     }
     __syncthreads();
-    if (L.sl == 0 && c < g.C) {
+    if (L.sl == 0 && c < cb) {
       for (int s = 1; s < L.nsl; ++s) {
         ax += sm[2 * (s * L.cpb + L.cl)];
         ay += sm[2 * (s * L.cpb + L.cl) + 1];
@@ -91,18 +92,20 @@ __device__ __forceinline__ int64_t first_elem_offset(const Geom& g, int64_t n, i
   return g.layout == kNCHW ? (n * g.C + c) * g.HW : n * g.HW * g.C + c;
 }
 
-// Forward, sample n.  The partial records hold, per channel, S = sum(x - K_c)
+// Forward, channels [ca, cb) (whole groups) of sample n.  The partial records
+// hold, per channel, S = sum(x - K_c)
 // and Q = sum((x - K_c)^2) with K_c = x(n, c, hw = 0).  Each channel gives
 // (mean_c, M2_c); the Cg channels of a group (HW elements each) merge into
 //   mean_g = avg_c(mean_c),  M2_g = sum_c M2_c + HW * sum_c (mean_c - mean_g)^2,
 // and var = M2_g / (Cg*HW) (biased), rstd = 1/sqrt(var + eps).
 template <typename T>
-__device__ void finalize_fwd(const KParams& p, int64_t n, float* sm, int64_t sm_floats) {
+__device__ void finalize_fwd(const KParams& p, int64_t n, int64_t ca, int64_t cb, float* sm,
+                             int64_t sm_floats) {
   const Geom& g = p.g;
   const T* x = static_cast<const T*>(p.x);
   const float hw = (float)g.HW;
   float2* stage = channel_stage(p, n, sm, sm_floats);
-  sum_channel_partials(p, n, sm, [&](int64_t c, float2 s) {
+  sum_channel_partials(p, n, ca, cb, sm, [&](int64_t c, float2 s) {
     const float K = Elem<T>::to_f(x[first_elem_offset(g, n, c)]);
     const float q = s.x / hw;
     const float m2 = fmaxf(fmaf(-s.x, q, s.y), 0.f);
@@ -110,7 +113,7 @@ __device__ void finalize_fwd(const KParams& p, int64_t n, float* sm, int64_t sm_
   });
   const float cgf = (float)g.Cg;
   const float mf = (float)(g.Cg * g.HW);
-  for (int64_t gi = threadIdx.x; gi < g.G; gi += blockDim.x) {
+  for (int64_t gi = ca / g.Cg + threadIdx.x; gi < cb / g.Cg; gi += blockDim.x) {
     const float2* cs = stage + gi * g.Cg;
     float s = 0.f;
     for (int64_t k = 0; k < g.Cg; ++k) s += cs[k].x;
@@ -127,24 +130,25 @@ __device__ void finalize_fwd(const KParams& p, int64_t n, float* sm, int64_t sm_
   }
 }
 
-// Backward, sample n.  The partial records hold, per channel,
+// Backward, channels [ca, cb) (whole groups) of sample n.  The partial
+// records hold, per channel,
 // S1 = sum(dy) and S2 = sum(dy * (x - mean_g)).  Per group:
 //   c1 = sum_c gamma_c * S1_c          (= sum over the group of gamma*dy)
 //   c2 = sum_c gamma_c * S2_c          (sum of gamma*dy*xhat = rstd * c2)
 // and dx = rstd*gamma_c*dy + B*(x - mean) + D with
 //   B = -rstd^3 * c2 / M,  D = -rstd * c1 / M,  M = Cg*HW.
 // The per-channel (S1, S2) stay in chst for the dgamma/dbeta step.
-__device__ __forceinline__ void finalize_bwd(const KParams& p, int64_t n, float* sm,
-                                             int64_t sm_floats) {
+__device__ __forceinline__ void finalize_bwd(const KParams& p, int64_t n, int64_t ca, int64_t cb,
+                                             float* sm, int64_t sm_floats) {
   const Geom& g = p.g;
   float2* stage = channel_stage(p, n, sm, sm_floats);
   float2* chst = p.chst + n * g.C;
-  sum_channel_partials(p, n, sm, [&](int64_t c, float2 s) {
+  sum_channel_partials(p, n, ca, cb, sm, [&](int64_t c, float2 s) {
     chst[c] = s;  // kept for the dgamma/dbeta step
     stage[c] = s;
   });
   const float mf = (float)(g.Cg * g.HW);
-  for (int64_t gi = threadIdx.x; gi < g.G; gi += blockDim.x) {
+  for (int64_t gi = ca / g.Cg + threadIdx.x; gi < cb / g.Cg; gi += blockDim.x) {
     const float2* cs = stage + gi * g.Cg;
     float c1 = 0.f, c2 = 0.f;
     for (int64_t k = 0; k < g.Cg; ++k) {
@@ -204,42 +208,80 @@ __device__ __forceinline__ void finalize_params(const KParams& p, float* sm) {
   }
 }
 
-// Tail of every first-kernel CTA, after it has written its item record.
-// With level-1 groups (l1 > 1) the CTA arrives on its group's counter; the
-// group's last CTA runs merge() (the group record from its item records, in
-// item order) and arrives on the sample's counter.  The sample's last arrival
-// runs its finalisation and, in the backward, the last sample runs the
-// parameter-gradient step.  Every counter is reset by the CTA that completed
-// it.  Must be reached by all threads of the CTA.
+// A finalisation unit: the channels [c0, c1) (whole groups) of sample n,
+// completed by `arrivals` arrivals on *ticket.  With a ready flag (pipelined
+// kernel) the finaliser sets it once the unit's statistics are written.
+struct Unit {
+  int64_t n, c0, c1;
+  unsigned* ticket;
+  unsigned arrivals;
+  unsigned* ready;
+};
+
+// The unit that channel c of sample n belongs to: the whole sample, or one
+// (sample, group) when g.unit_groups is set.  Its ticket (and ready flag) is
+// the unit's index n or n*G + c/Cg.
+__device__ __forceinline__ Unit unit_of(const KParams& p, int64_t n, int64_t c) {
+  const Geom& g = p.g;
+  Unit u;
+  u.n = n;
+  int64_t id = n;
+  if (g.unit_groups) {
+    u.c0 = c / g.Cg * g.Cg;
+    u.c1 = u.c0 + g.Cg;
+    id = n * g.G + c / g.Cg;
+  } else {
+    u.c0 = 0;
+    u.c1 = g.C;
+  }
+  u.ticket = p.tickets + id;
+  u.arrivals = (unsigned)g.arrivals_per_n;
+  u.ready = p.ready ? p.ready + id : nullptr;
+  return u;
+}
+
+// Tail of every CTA that has written a partial record.  With level-1 groups
+// (l1 > 1) the CTA arrives on its group's counter; the group's last CTA runs
+// merge() (the group record from its item records, in item order) and
+// arrives on the unit's counter.  The unit's last arrival runs its
+// finalisation (and raises the unit's ready flag); in the backward, the last
+// unit then runs the parameter-gradient step.  Every counter is reset by the
+// CTA that completed it.  Must be reached by all threads of the CTA.
 template <typename T, bool kBwd, typename Merge>
-__device__ __forceinline__ void arrive_and_finalize(const KParams& p, int64_t n, int64_t group1,
-                                                    unsigned gsize, Merge merge, float* sm,
-                                                    int64_t sm_floats) {
+__device__ __forceinline__ void arrive_and_finalize(const KParams& p, const Unit& un,
+                                                    int64_t group1, unsigned gsize, Merge merge,
+                                                    float* sm, int64_t sm_floats) {
   __shared__ int s_last;
+  __threadfence();  // this thread's record stores, before the CTA's arrival
   if (p.g.l1 > 1) {
     __syncthreads();
     if (threadIdx.x == 0) s_last = publish_and_arrive(p.cnt1 + group1, gsize);
     __syncthreads();
     if (!s_last) return;
     merge();
+    __threadfence();
     if (threadIdx.x == 0) atomicExch(p.cnt1 + group1, 0u);
   }
   __syncthreads();
-  if (threadIdx.x == 0) s_last = publish_and_arrive(p.tickets + n, (unsigned)p.g.arrivals_per_n);
+  if (threadIdx.x == 0) s_last = publish_and_arrive(un.ticket, un.arrivals);
   __syncthreads();
   if (!s_last) return;
   if (kBwd)
-    finalize_bwd(p, n, sm, sm_floats);
+    finalize_bwd(p, un.n, un.c0, un.c1, sm, sm_floats);
   else
-    finalize_fwd<T>(p, n, sm, sm_floats);
+    finalize_fwd<T>(p, un.n, un.c0, un.c1, sm, sm_floats);
+  __threadfence();  // the unit's statistics, before the ready flag and the next arrival
   __syncthreads();
-  if (threadIdx.x == 0) atomicExch(p.tickets + n, 0u);
+  if (threadIdx.x == 0) {
+    atomicExch(un.ticket, 0u);
+    if (un.ready) atomicExch(un.ready, 1u);
+  }
   if (!kBwd) return;
-  if (threadIdx.x == 0) s_last = publish_and_arrive(p.tickets + p.g.N, (unsigned)p.g.N);
+  if (threadIdx.x == 0) s_last = publish_and_arrive(p.tickets + p.g.units_fin, (unsigned)p.g.units_fin);
   __syncthreads();
   if (!s_last) return;
   finalize_params(p, sm);
-  if (threadIdx.x == 0) atomicExch(p.tickets + p.g.N, 0u);
+  if (threadIdx.x == 0) atomicExch(p.tickets + p.g.units_fin, 0u);
 }
 
 }  // namespace gn

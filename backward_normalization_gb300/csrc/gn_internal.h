@@ -18,6 +18,8 @@ enum Regime {
   kRegimeAuto = -1,
   kRegimeGeneric = 0,   // stats/reduce kernel + apply/dx kernel, any shape
   kRegimeResident = 1,  // one kernel: a cluster holds a unit in shared memory
+  kRegimePipelined = 2, // one persistent kernel: pass-1 and pass-2 tasks of
+                        // units in flight, the second pass reading from L2
 };
 
 // How one call is cut into "items" for the two-kernel path.  Both kernels
@@ -49,11 +51,19 @@ struct Geom {
   int64_t Tp;    // level-1 records per (n, c) = ceil(T / l1)
   int64_t groups1;           // level-1 groups in the call
   int64_t cstride, tstride;  // level-1 record index = n*C*Tp + c*cstride + t1*tstride
-  int64_t arrivals_per_n;    // level-1 records that complete sample n
+  int64_t arrivals_per_n;    // records that complete a finalisation unit
+  int64_t units_fin;         // finalisation units: N (a unit is a sample) or N*G
+  int unit_groups;           // 1: a unit is one (sample, group) (pipelined NCHW)
   int64_t items_per_n;       // NCHW mode 1: items per sample
   int64_t items;
   int64_t keep_from;  // item-relative row/element index from which the first kernel
                       // loads with the L2 evict_last policy (the part read again first)
+  // pipelined regime: units_fin units of `pieces` pass-1 and `pieces` pass-2
+  // tasks each (a piece is item u*T + q: NHWC, or plane q/T of the unit's
+  // group, segment q%T: NCHW); pass-2 tasks trail pass-1 tasks by `lag` units
+  int64_t pieces, lag;
+  int64_t grid;        // persistent CTAs (all co-resident)
+  int64_t counters;    // uint32 counter slots this plan uses at the start of the workspace
   // resident regime (gn_resident.cu)
   int regime;
   int K;               // CTAs per unit (cluster size)
@@ -72,7 +82,10 @@ struct Geom {
 
 // Workspace layout (byte offsets, each 256-byte aligned).
 struct WsLayout {
-  size_t tickets;  // uint32 counters: N per sample, 1 global, then one per level-1 group
+  size_t tickets;  // uint32 counters: one per finalisation unit, 1 global, one per level-1
+                   // group; pipelined: then a ready flag and a pass-2 counter per unit
+                   // and the task queue (next task, CTAs done).  Sized by
+                   // problem_counters(), whichever op and alignment the call has.
   size_t err;      // uint32 error word (a bounded wait ran out)
   size_t part0;    // N*C*T float2 item partial sums (when l1 > 1)
   size_t part;     // N*C*Tp float2 level-1 partial sums
@@ -95,8 +108,11 @@ struct KParams {
   float* dgamma;
   float* dbeta;
   float eps;
-  unsigned* tickets;  // [0, N) per sample, [N] global
+  unsigned* tickets;  // [0, units_fin) per unit, [units_fin] global
   unsigned* cnt1;     // per level-1 group
+  unsigned* ready;    // pipelined: per unit, 1 once its statistics are written
+  unsigned* p2cnt;    // pipelined: per unit, pass-2 tasks done
+  unsigned* queue;    // pipelined: [0] next task, [1] CTAs done
   unsigned* err;
   float2* part0;      // item partials (== part when l1 == 1)
   float2* part;
@@ -116,6 +132,9 @@ int64_t resident_ctas(const Geom& g, int op, int second);
 Geom make_geom(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout,
                int dtype, bool aligned);
 WsLayout ws_layout(int op, const Geom& g);
+// Counter slots of a problem: the most that any plan of it (either op, either
+// alignment) uses; the workspace layout reserves this many for every call.
+int64_t problem_counters(const Geom& g);
 
 // Events recorded around/between the kernels of a call (benchmark hook; the
 // launchers record the non-null ones on the call's stream).
@@ -128,6 +147,11 @@ const TimingEvents& timing_events();
 // kernels (gn_nhwc.cu / gn_nchw.cu): enqueue the two kernels of an op.
 cudaError_t launch_nhwc(const KParams& p, cudaStream_t s, bool bwd);
 cudaError_t launch_nchw(const KParams& p, cudaStream_t s, bool bwd);
+// The pipelined regime's kernel (one launch, cooperative).
+cudaError_t launch_nhwc_pipelined(const KParams& p, cudaStream_t s, bool bwd);
+cudaError_t launch_nchw_pipelined(const KParams& p, cudaStream_t s, bool bwd);
+const void* nhwc_pipelined_kernel(const Geom& g, bool bwd, size_t* smem);
+const void* nchw_pipelined_kernel(const Geom& g, bool bwd, size_t* smem);
 // The first (second = 0) or second (second = 1) kernel's function and its
 // dynamic shared memory for a plan.
 const void* nhwc_kernel(const Geom& g, bool bwd, int second, size_t* smem);

@@ -1,4 +1,5 @@
-// gn_nchw.cu -- two-kernel GroupNorm path for NCHW activations.
+// gn_nchw.cu -- GroupNorm for NCHW activations: the two-kernel path and the
+// pipelined kernel.
 //
 // Memory: element (n, c, hw) sits at (n*C + c)*HW + hw, so each (n, c)
 // channel plane ("row") is HW contiguous elements and a group is Cg
@@ -9,10 +10,12 @@
 //          their last CTA.
 //   mode 1 (small planes): item = RB consecutive rows of one sample; each warp
 //          takes whole rows; one record per row.
-// As in gn_nhwc.cu, the last arrival of a sample finalises it, and the
+// In the two-kernel path the last arrival of a sample finalises it and the
 // elementwise second kernels walk the items (and the elements of a chunk) in
-// reverse order, starting on the data the first kernel left in L2.
-#include "gn_finalize.cuh"
+// reverse order, starting on the data the first kernel left in L2.  The
+// pipelined kernel (mode 0 only) runs the same chunk functions as tasks of
+// gn_tasks.cuh, with one (sample, group) per unit.
+#include "gn_tasks.cuh"
 
 namespace gn {
 namespace {
@@ -57,8 +60,8 @@ __device__ __forceinline__ Chunk chunk_of(const Geom& g, int64_t item) {
   return c;
 }
 
-// Mode-0 tail of the first kernels: CTA sum, the chunk's record, the arrival
-// chain (group of l1 chunks of the row, then the sample).
+// Mode-0 tail of pass 1: CTA sum, the chunk's record, the arrival chain
+// (group of l1 chunks of the row, then the chunk's unit).
 template <typename T, bool kBwd>
 __device__ __forceinline__ void publish_chunk(const KParams& p, const Chunk& k, float a, float b,
                                               float* sm) {
@@ -74,266 +77,334 @@ __device__ __forceinline__ void publish_chunk(const KParams& p, const Chunk& k, 
     sum_records(p.part0 + k.row * g.T + tlo, 1, 0, 1, gsize, ax, ay);
     p.part[k.row * g.Tp + t1] = make_float2(ax, ay);
   };
-  arrive_and_finalize<T, kBwd>(p, k.row / g.C, k.row * g.Tp + t1, gsize, merge, sm,
-                               nchw_smem_floats(g));
+  arrive_and_finalize<T, kBwd>(p, unit_of(p, k.row / g.C, k.row % g.C), k.row * g.Tp + t1, gsize,
+                               merge, sm, nchw_smem_floats(g));
 }
 
-// ------------------------------------------------------------------ forward
+// ---------------------------------------------------------- mode 0 (chunks)
+// Forward pass 1 of one chunk: shifted sums with K = x(n, c, 0).
 template <typename T, int VW>
-__global__ void __launch_bounds__(512) nchw_fwd_stats(const __grid_constant__ KParams p) {
-  grid_dependency_wait();  // the previous kernel's results (and x, dy) are complete
-  grid_launch_dependents();
-  extern __shared__ float sm[];
+__device__ __forceinline__ void stats_chunk(const KParams& p, int64_t item, float* sm) {
   const Geom& g = p.g;
   const int tid = threadIdx.x;
-  const T* x = static_cast<const T*>(p.x);
   const uint64_t pfirst = policy_evict_first(), plast = policy_evict_last();
-  if (g.mode == 0) {
-    const Chunk k = chunk_of(g, blockIdx.x);
-    const T* xr = x + k.row * g.HW;
-    const float K = Elem<T>::to_f(xr[0]);
-    const int64_t keep = k.h0 + g.keep_from;
-    float s = 0.f, q = 0.f;
-    const int64_t st = (int64_t)blockDim.x * VW;
-    int64_t h = k.h0 + (int64_t)tid * VW;
-    for (; h + 3 * st < k.h1; h += 4 * st) {
-      const uint64_t pol = h >= keep ? plast : pfirst;
-      float v[4][VW];
+  const Chunk k = chunk_of(g, item);
+  const T* xr = static_cast<const T*>(p.x) + k.row * g.HW;
+  const float K = Elem<T>::to_f(xr[0]);
+  const int64_t keep = k.h0 + g.keep_from;
+  float s = 0.f, q = 0.f;
+  const int64_t st = (int64_t)blockDim.x * VW;
+  int64_t h = k.h0 + (int64_t)tid * VW;
+  for (; h + 3 * st < k.h1; h += 4 * st) {
+    const uint64_t pol = h >= keep ? plast : pfirst;
+    float v[4][VW];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) Access<T, VW>::load(xr + h + u * st, v[u], pol);
+    for (int u = 0; u < 4; ++u) Access<T, VW>::load(xr + h + u * st, v[u], pol);
 #pragma unroll
-      for (int u = 0; u < 4; ++u) acc_shifted<VW>(v[u], K, s, q);
+    for (int u = 0; u < 4; ++u) acc_shifted<VW>(v[u], K, s, q);
+  }
+  for (; h < k.h1; h += st) {
+    float v[VW];
+    Access<T, VW>::load(xr + h, v, h >= keep ? plast : pfirst);
+    acc_shifted<VW>(v, K, s, q);
+  }
+  publish_chunk<T, false>(p, k, s, q, sm);
+}
+
+// Backward pass 1 of one chunk: sum(dy), sum(dy*(x-mean)).
+template <typename T, int VW>
+__device__ __forceinline__ void reduce_chunk(const KParams& p, int64_t item, float* sm) {
+  const Geom& g = p.g;
+  const int tid = threadIdx.x;
+  const uint64_t pfirst = policy_evict_first(), plast = policy_evict_last();
+  const Chunk k = chunk_of(g, item);
+  const int64_t n = k.row / g.C;
+  const float mu = __ldg(p.mean + n * g.G + (k.row % g.C) / g.Cg);
+  const T* xr = static_cast<const T*>(p.x) + k.row * g.HW;
+  const T* dr = static_cast<const T*>(p.dy) + k.row * g.HW;
+  const int64_t keep = k.h0 + g.keep_from;
+  float s1 = 0.f, s2 = 0.f;
+  const int64_t st = (int64_t)blockDim.x * VW;
+  int64_t h = k.h0 + (int64_t)tid * VW;
+  for (; h + st < k.h1; h += 2 * st) {
+    const uint64_t pol = h >= keep ? plast : pfirst;
+    float xv[2][VW], dv[2][VW];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      Access<T, VW>::load(xr + h + u * st, xv[u], pol);
+      Access<T, VW>::load(dr + h + u * st, dv[u], pol);
     }
-    for (; h < k.h1; h += st) {
+#pragma unroll
+    for (int u = 0; u < 2; ++u) acc_grad<VW>(xv[u], dv[u], mu, s1, s2);
+  }
+  for (; h < k.h1; h += st) {
+    const uint64_t pol = h >= keep ? plast : pfirst;
+    float xv[VW], dv[VW];
+    Access<T, VW>::load(xr + h, xv, pol);
+    Access<T, VW>::load(dr + h, dv, pol);
+    acc_grad<VW>(xv, dv, mu, s1, s2);
+  }
+  publish_chunk<T, true>(p, k, s1, s2, sm);
+}
+
+// Forward pass 2 of one chunk, last vector to first.
+template <typename T, int VW>
+__device__ __forceinline__ void apply_chunk(const KParams& p, int64_t item) {
+  const Geom& g = p.g;
+  const int tid = threadIdx.x;
+  const uint64_t pol = policy_evict_first();
+  const Chunk k = chunk_of(g, item);
+  if (k.h0 >= k.h1) return;
+  const int64_t n = k.row / g.C, c = k.row % g.C, ng = n * g.G + c / g.Cg;
+  // mean/rstd may have been written earlier in this launch: coherent loads
+  const float r = __ldcg(p.rstd + ng), mu = __ldcg(p.mean + ng);
+  const float a = p.gamma ? r * __ldg(p.gamma + c) : r;
+  const float b = p.beta ? __ldg(p.beta + c) : 0.f;
+  const T* xr = static_cast<const T*>(p.x) + k.row * g.HW + k.h0;
+  T* yr = static_cast<T*>(p.out) + k.row * g.HW + k.h0;
+  const int64_t nv = (k.h1 - k.h0) / VW;
+  const int64_t st = blockDim.x;
+  int64_t i = nv - 1 - tid;
+  for (; i - 3 * st >= 0; i -= 4 * st) {
+    float v[4][VW];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) Access<T, VW>::load(xr + (i - u * st) * VW, v[u], pol);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+#pragma unroll
+      for (int e = 0; e < VW; ++e) v[u][e] = fmaf(v[u][e] - mu, a, b);
+      Access<T, VW>::store(yr + (i - u * st) * VW, v[u], pol);
+    }
+  }
+  for (; i >= 0; i -= st) {
+    float v[VW];
+    Access<T, VW>::load(xr + i * VW, v, pol);
+#pragma unroll
+    for (int e = 0; e < VW; ++e) v[e] = fmaf(v[e] - mu, a, b);
+    Access<T, VW>::store(yr + i * VW, v, pol);
+  }
+}
+
+// Backward pass 2 of one chunk, last vector to first.
+template <typename T, int VW>
+__device__ __forceinline__ void dx_chunk(const KParams& p, int64_t item) {
+  const Geom& g = p.g;
+  const int tid = threadIdx.x;
+  const uint64_t pol = policy_evict_first();
+  const Chunk k = chunk_of(g, item);
+  if (k.h0 >= k.h1) return;
+  const int64_t n = k.row / g.C, c = k.row % g.C, ng = n * g.G + c / g.Cg;
+  const float r = __ldg(p.rstd + ng), mu = __ldg(p.mean + ng);
+  const float A = p.gamma ? r * __ldg(p.gamma + c) : r;
+  const float2 cf = __ldcg(p.coef + ng);
+  const T* xr = static_cast<const T*>(p.x) + k.row * g.HW + k.h0;
+  const T* dr = static_cast<const T*>(p.dy) + k.row * g.HW + k.h0;
+  T* outr = static_cast<T*>(p.out) + k.row * g.HW + k.h0;
+  const int64_t nv = (k.h1 - k.h0) / VW;
+  const int64_t st = blockDim.x;
+  int64_t i = nv - 1 - tid;
+  for (; i - st >= 0; i -= 2 * st) {
+    float xv[2][VW], dv[2][VW];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      Access<T, VW>::load(xr + (i - u * st) * VW, xv[u], pol);
+      Access<T, VW>::load(dr + (i - u * st) * VW, dv[u], pol);
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+#pragma unroll
+      for (int e = 0; e < VW; ++e) xv[u][e] = fmaf(A, dv[u][e], fmaf(cf.x, xv[u][e] - mu, cf.y));
+      Access<T, VW>::store(outr + (i - u * st) * VW, xv[u], pol);
+    }
+  }
+  for (; i >= 0; i -= st) {
+    float xv[VW], dv[VW];
+    Access<T, VW>::load(xr + i * VW, xv, pol);
+    Access<T, VW>::load(dr + i * VW, dv, pol);
+#pragma unroll
+    for (int e = 0; e < VW; ++e) xv[e] = fmaf(A, dv[e], fmaf(cf.x, xv[e] - mu, cf.y));
+    Access<T, VW>::store(outr + i * VW, xv, pol);
+  }
+}
+
+// ------------------------------------------------------- mode 1 (row blocks)
+struct RowBlock {
+  int64_t n, c0, c1;
+};
+__device__ __forceinline__ RowBlock rows_of(const Geom& g, int64_t item) {
+  RowBlock b;
+  b.n = item / g.items_per_n;
+  b.c0 = (item % g.items_per_n) * g.RB;
+  b.c1 = (b.c0 + g.RB < g.C) ? b.c0 + g.RB : g.C;
+  return b;
+}
+
+template <typename T, int VW>
+__device__ __forceinline__ void stats_rows(const KParams& p, int64_t item, float* sm) {
+  const Geom& g = p.g;
+  const RowBlock rb = rows_of(g, item);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  const uint64_t pol = g.keep_from == 0 ? policy_evict_last() : policy_evict_first();
+  for (int64_t c = rb.c0 + warp; c < rb.c1; c += nwarps) {
+    const int64_t row = rb.n * g.C + c;
+    const T* xr = static_cast<const T*>(p.x) + row * g.HW;
+    const float K = Elem<T>::to_f(xr[0]);
+    float s = 0.f, q = 0.f;
+    for (int64_t h = (int64_t)lane * VW; h < g.HW; h += 32 * VW) {
       float v[VW];
-      Access<T, VW>::load(xr + h, v, h >= keep ? plast : pfirst);
+      Access<T, VW>::load(xr + h, v, pol);
       acc_shifted<VW>(v, K, s, q);
     }
-    publish_chunk<T, false>(p, k, s, q, sm);
-  } else {
-    const int64_t item = blockIdx.x;
-    const int64_t n = item / g.items_per_n;
-    const int64_t c0 = (item % g.items_per_n) * g.RB;
-    const int64_t c1 = (c0 + g.RB < g.C) ? c0 + g.RB : g.C;
-    const int lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
-    const uint64_t pol = g.keep_from == 0 ? plast : pfirst;
-    for (int64_t c = c0 + warp; c < c1; c += nwarps) {
-      const int64_t row = n * g.C + c;
-      const T* xr = x + row * g.HW;
-      const float K = Elem<T>::to_f(xr[0]);
-      float s = 0.f, q = 0.f;
-      for (int64_t h = (int64_t)lane * VW; h < g.HW; h += 32 * VW) {
-        float v[VW];
-        Access<T, VW>::load(xr + h, v, pol);
-        acc_shifted<VW>(v, K, s, q);
-      }
-      s = warp_sum_lane0(s);
-      q = warp_sum_lane0(q);
-      if (lane == 0) p.part[row] = make_float2(s, q);
-    }
-    arrive_and_finalize<T, false>(p, n, 0, 1, [] {}, sm, nchw_smem_floats(g));
+    s = warp_sum_lane0(s);
+    q = warp_sum_lane0(q);
+    if (lane == 0) p.part[row] = make_float2(s, q);
   }
+  arrive_and_finalize<T, false>(p, unit_of(p, rb.n, 0), 0, 1, [] {}, sm, nchw_smem_floats(g));
 }
 
 template <typename T, int VW>
-__global__ void __launch_bounds__(512) nchw_fwd_apply(const __grid_constant__ KParams p) {
-  grid_dependency_wait();  // the previous kernel's results (and x, dy) are complete
-  grid_launch_dependents();
+__device__ __forceinline__ void reduce_rows(const KParams& p, int64_t item, float* sm) {
   const Geom& g = p.g;
-  const int tid = threadIdx.x;
-  const T* x = static_cast<const T*>(p.x);
-  T* y = static_cast<T*>(p.out);
-  const uint64_t pol = policy_evict_first();
-  const int64_t item = g.items - 1 - (int64_t)blockIdx.x;
-  if (g.mode == 0) {
-    const Chunk k = chunk_of(g, item);
-    if (k.h0 >= k.h1) return;
-    const int64_t n = k.row / g.C, c = k.row % g.C, ng = n * g.G + c / g.Cg;
-    const float r = __ldg(p.rstd + ng), mu = __ldg(p.mean + ng);
-    const float a = p.gamma ? r * __ldg(p.gamma + c) : r;
-    const float b = p.beta ? __ldg(p.beta + c) : 0.f;
-    const T* xr = x + k.row * g.HW + k.h0;
-    T* yr = y + k.row * g.HW + k.h0;
-    const int64_t nv = (k.h1 - k.h0) / VW;
-    const int64_t st = blockDim.x;
-    int64_t i = nv - 1 - tid;
-    for (; i - 3 * st >= 0; i -= 4 * st) {
-      float v[4][VW];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) Access<T, VW>::load(xr + (i - u * st) * VW, v[u], pol);
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-#pragma unroll
-        for (int e = 0; e < VW; ++e) v[u][e] = fmaf(v[u][e] - mu, a, b);
-        Access<T, VW>::store(yr + (i - u * st) * VW, v[u], pol);
-      }
-    }
-    for (; i >= 0; i -= st) {
-      float v[VW];
-      Access<T, VW>::load(xr + i * VW, v, pol);
-#pragma unroll
-      for (int e = 0; e < VW; ++e) v[e] = fmaf(v[e] - mu, a, b);
-      Access<T, VW>::store(yr + i * VW, v, pol);
-    }
-  } else {
-    const int64_t n = item / g.items_per_n;
-    const int64_t c0 = (item % g.items_per_n) * g.RB;
-    const int64_t c1 = (c0 + g.RB < g.C) ? c0 + g.RB : g.C;
-    const int lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
-    for (int64_t c = c0 + warp; c < c1; c += nwarps) {
-      const int64_t row = n * g.C + c, ng = n * g.G + c / g.Cg;
-      const float r = __ldg(p.rstd + ng), mu = __ldg(p.mean + ng);
-      const float a = p.gamma ? r * __ldg(p.gamma + c) : r;
-      const float b = p.beta ? __ldg(p.beta + c) : 0.f;
-      const T* xr = x + row * g.HW;
-      T* yr = y + row * g.HW;
-      for (int64_t h = (int64_t)lane * VW; h < g.HW; h += 32 * VW) {
-        float v[VW];
-        Access<T, VW>::load(xr + h, v, pol);
-#pragma unroll
-        for (int e = 0; e < VW; ++e) v[e] = fmaf(v[e] - mu, a, b);
-        Access<T, VW>::store(yr + h, v, pol);
-      }
-    }
-  }
-}
-
-// ----------------------------------------------------------------- backward
-template <typename T, int VW>
-__global__ void __launch_bounds__(512) nchw_bwd_reduce(const __grid_constant__ KParams p) {
-  grid_dependency_wait();  // the previous kernel's results (and x, dy) are complete
-  grid_launch_dependents();
-  extern __shared__ float sm[];
-  const Geom& g = p.g;
-  const int tid = threadIdx.x;
-  const T* x = static_cast<const T*>(p.x);
-  const T* dy = static_cast<const T*>(p.dy);
-  const uint64_t pfirst = policy_evict_first(), plast = policy_evict_last();
-  if (g.mode == 0) {
-    const Chunk k = chunk_of(g, blockIdx.x);
-    const int64_t n = k.row / g.C;
-    const float mu = __ldg(p.mean + n * g.G + (k.row % g.C) / g.Cg);
-    const T* xr = x + k.row * g.HW;
-    const T* dr = dy + k.row * g.HW;
-    const int64_t keep = k.h0 + g.keep_from;
+  const RowBlock rb = rows_of(g, item);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  const uint64_t pol = g.keep_from == 0 ? policy_evict_last() : policy_evict_first();
+  for (int64_t c = rb.c0 + warp; c < rb.c1; c += nwarps) {
+    const int64_t row = rb.n * g.C + c;
+    const float mu = __ldg(p.mean + rb.n * g.G + c / g.Cg);
+    const T* xr = static_cast<const T*>(p.x) + row * g.HW;
+    const T* dr = static_cast<const T*>(p.dy) + row * g.HW;
     float s1 = 0.f, s2 = 0.f;
-    const int64_t st = (int64_t)blockDim.x * VW;
-    int64_t h = k.h0 + (int64_t)tid * VW;
-    for (; h + st < k.h1; h += 2 * st) {
-      const uint64_t pol = h >= keep ? plast : pfirst;
-      float xv[2][VW], dv[2][VW];
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        Access<T, VW>::load(xr + h + u * st, xv[u], pol);
-        Access<T, VW>::load(dr + h + u * st, dv[u], pol);
-      }
-#pragma unroll
-      for (int u = 0; u < 2; ++u) acc_grad<VW>(xv[u], dv[u], mu, s1, s2);
-    }
-    for (; h < k.h1; h += st) {
-      const uint64_t pol = h >= keep ? plast : pfirst;
+    for (int64_t h = (int64_t)lane * VW; h < g.HW; h += 32 * VW) {
       float xv[VW], dv[VW];
       Access<T, VW>::load(xr + h, xv, pol);
       Access<T, VW>::load(dr + h, dv, pol);
       acc_grad<VW>(xv, dv, mu, s1, s2);
     }
-    publish_chunk<T, true>(p, k, s1, s2, sm);
-  } else {
-    const int64_t item = blockIdx.x;
-    const int64_t n = item / g.items_per_n;
-    const int64_t c0 = (item % g.items_per_n) * g.RB;
-    const int64_t c1 = (c0 + g.RB < g.C) ? c0 + g.RB : g.C;
-    const int lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
-    const uint64_t pol = g.keep_from == 0 ? plast : pfirst;
-    for (int64_t c = c0 + warp; c < c1; c += nwarps) {
-      const int64_t row = n * g.C + c;
-      const float mu = __ldg(p.mean + n * g.G + c / g.Cg);
-      const T* xr = x + row * g.HW;
-      const T* dr = dy + row * g.HW;
-      float s1 = 0.f, s2 = 0.f;
-      for (int64_t h = (int64_t)lane * VW; h < g.HW; h += 32 * VW) {
-        float xv[VW], dv[VW];
-        Access<T, VW>::load(xr + h, xv, pol);
-        Access<T, VW>::load(dr + h, dv, pol);
-        acc_grad<VW>(xv, dv, mu, s1, s2);
-      }
-      s1 = warp_sum_lane0(s1);
-      s2 = warp_sum_lane0(s2);
-      if (lane == 0) p.part[row] = make_float2(s1, s2);
+    s1 = warp_sum_lane0(s1);
+    s2 = warp_sum_lane0(s2);
+    if (lane == 0) p.part[row] = make_float2(s1, s2);
+  }
+  arrive_and_finalize<T, true>(p, unit_of(p, rb.n, 0), 0, 1, [] {}, sm, nchw_smem_floats(g));
+}
+
+template <typename T, int VW>
+__device__ __forceinline__ void apply_rows(const KParams& p, int64_t item) {
+  const Geom& g = p.g;
+  const RowBlock rb = rows_of(g, item);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  const uint64_t pol = policy_evict_first();
+  for (int64_t c = rb.c0 + warp; c < rb.c1; c += nwarps) {
+    const int64_t row = rb.n * g.C + c, ng = rb.n * g.G + c / g.Cg;
+    const float r = __ldcg(p.rstd + ng), mu = __ldcg(p.mean + ng);
+    const float a = p.gamma ? r * __ldg(p.gamma + c) : r;
+    const float b = p.beta ? __ldg(p.beta + c) : 0.f;
+    const T* xr = static_cast<const T*>(p.x) + row * g.HW;
+    T* yr = static_cast<T*>(p.out) + row * g.HW;
+    for (int64_t h = (int64_t)lane * VW; h < g.HW; h += 32 * VW) {
+      float v[VW];
+      Access<T, VW>::load(xr + h, v, pol);
+#pragma unroll
+      for (int e = 0; e < VW; ++e) v[e] = fmaf(v[e] - mu, a, b);
+      Access<T, VW>::store(yr + h, v, pol);
     }
-    arrive_and_finalize<T, true>(p, n, 0, 1, [] {}, sm, nchw_smem_floats(g));
   }
 }
 
 template <typename T, int VW>
-__global__ void __launch_bounds__(512) nchw_bwd_dx(const __grid_constant__ KParams p) {
-  grid_dependency_wait();  // the previous kernel's results (and x, dy) are complete
-  grid_launch_dependents();
+__device__ __forceinline__ void dx_rows(const KParams& p, int64_t item) {
   const Geom& g = p.g;
-  const int tid = threadIdx.x;
-  const T* x = static_cast<const T*>(p.x);
-  const T* dy = static_cast<const T*>(p.dy);
-  T* dx = static_cast<T*>(p.out);
+  const RowBlock rb = rows_of(g, item);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   const uint64_t pol = policy_evict_first();
-  const int64_t item = g.items - 1 - (int64_t)blockIdx.x;
-  if (g.mode == 0) {
-    const Chunk k = chunk_of(g, item);
-    if (k.h0 >= k.h1) return;
-    const int64_t n = k.row / g.C, c = k.row % g.C, ng = n * g.G + c / g.Cg;
+  for (int64_t c = rb.c0 + warp; c < rb.c1; c += nwarps) {
+    const int64_t row = rb.n * g.C + c, ng = rb.n * g.G + c / g.Cg;
     const float r = __ldg(p.rstd + ng), mu = __ldg(p.mean + ng);
     const float A = p.gamma ? r * __ldg(p.gamma + c) : r;
     const float2 cf = __ldcg(p.coef + ng);
-    const T* xr = x + k.row * g.HW + k.h0;
-    const T* dr = dy + k.row * g.HW + k.h0;
-    T* outr = dx + k.row * g.HW + k.h0;
-    const int64_t nv = (k.h1 - k.h0) / VW;
-    const int64_t st = blockDim.x;
-    int64_t i = nv - 1 - tid;
-    for (; i - st >= 0; i -= 2 * st) {
-      float xv[2][VW], dv[2][VW];
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        Access<T, VW>::load(xr + (i - u * st) * VW, xv[u], pol);
-        Access<T, VW>::load(dr + (i - u * st) * VW, dv[u], pol);
-      }
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-#pragma unroll
-        for (int e = 0; e < VW; ++e) xv[u][e] = fmaf(A, dv[u][e], fmaf(cf.x, xv[u][e] - mu, cf.y));
-        Access<T, VW>::store(outr + (i - u * st) * VW, xv[u], pol);
-      }
-    }
-    for (; i >= 0; i -= st) {
+    const T* xr = static_cast<const T*>(p.x) + row * g.HW;
+    const T* dr = static_cast<const T*>(p.dy) + row * g.HW;
+    T* outr = static_cast<T*>(p.out) + row * g.HW;
+    for (int64_t h = (int64_t)lane * VW; h < g.HW; h += 32 * VW) {
       float xv[VW], dv[VW];
-      Access<T, VW>::load(xr + i * VW, xv, pol);
-      Access<T, VW>::load(dr + i * VW, dv, pol);
+      Access<T, VW>::load(xr + h, xv, pol);
+      Access<T, VW>::load(dr + h, dv, pol);
 #pragma unroll
       for (int e = 0; e < VW; ++e) xv[e] = fmaf(A, dv[e], fmaf(cf.x, xv[e] - mu, cf.y));
-      Access<T, VW>::store(outr + i * VW, xv, pol);
-    }
-  } else {
-    const int64_t n = item / g.items_per_n;
-    const int64_t c0 = (item % g.items_per_n) * g.RB;
-    const int64_t c1 = (c0 + g.RB < g.C) ? c0 + g.RB : g.C;
-    const int lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
-    for (int64_t c = c0 + warp; c < c1; c += nwarps) {
-      const int64_t row = n * g.C + c, ng = n * g.G + c / g.Cg;
-      const float r = __ldg(p.rstd + ng), mu = __ldg(p.mean + ng);
-      const float A = p.gamma ? r * __ldg(p.gamma + c) : r;
-      const float2 cf = __ldcg(p.coef + ng);
-      const T* xr = x + row * g.HW;
-      const T* dr = dy + row * g.HW;
-      T* outr = dx + row * g.HW;
-      for (int64_t h = (int64_t)lane * VW; h < g.HW; h += 32 * VW) {
-        float xv[VW], dv[VW];
-        Access<T, VW>::load(xr + h, xv, pol);
-        Access<T, VW>::load(dr + h, dv, pol);
-#pragma unroll
-        for (int e = 0; e < VW; ++e) xv[e] = fmaf(A, dv[e], fmaf(cf.x, xv[e] - mu, cf.y));
-        Access<T, VW>::store(outr + h, xv, pol);
-      }
+      Access<T, VW>::store(outr + h, xv, pol);
     }
   }
+}
+
+// ------------------------------------------------------- two-kernel kernels
+template <typename T, int VW>
+__global__ void __launch_bounds__(512) nchw_fwd_stats(const __grid_constant__ KParams p) {
+  grid_dependency_wait();  // the previous kernel's results (and x, dy) are complete
+  grid_launch_dependents();
+  extern __shared__ float sm[];
+  if (p.g.mode == 0)
+    stats_chunk<T, VW>(p, blockIdx.x, sm);
+  else
+    stats_rows<T, VW>(p, blockIdx.x, sm);
+}
+
+template <typename T, int VW>
+__global__ void __launch_bounds__(512) nchw_fwd_apply(const __grid_constant__ KParams p) {
+  grid_dependency_wait();
+  grid_launch_dependents();
+  const int64_t item = p.g.items - 1 - (int64_t)blockIdx.x;
+  if (p.g.mode == 0)
+    apply_chunk<T, VW>(p, item);
+  else
+    apply_rows<T, VW>(p, item);
+}
+
+template <typename T, int VW>
+__global__ void __launch_bounds__(512) nchw_bwd_reduce(const __grid_constant__ KParams p) {
+  grid_dependency_wait();
+  grid_launch_dependents();
+  extern __shared__ float sm[];
+  if (p.g.mode == 0)
+    reduce_chunk<T, VW>(p, blockIdx.x, sm);
+  else
+    reduce_rows<T, VW>(p, blockIdx.x, sm);
+}
+
+template <typename T, int VW>
+__global__ void __launch_bounds__(512) nchw_bwd_dx(const __grid_constant__ KParams p) {
+  grid_dependency_wait();
+  grid_launch_dependents();
+  const int64_t item = p.g.items - 1 - (int64_t)blockIdx.x;
+  if (p.g.mode == 0)
+    dx_chunk<T, VW>(p, item);
+  else
+    dx_rows<T, VW>(p, item);
+}
+
+// The pipelined regime: a unit is one (sample n, group), its pieces the
+// chunks of its Cg planes (piece q: plane group*Cg + q/T, chunk q%T).
+template <typename T, int VW, bool kBwd>
+__global__ void __launch_bounds__(512) nchw_pipelined(const __grid_constant__ KParams p) {
+  extern __shared__ float sm[];
+  grid_dependency_wait();
+  const Geom& g = p.g;
+  run_tasks(p, [&](const Task& t) {
+    const int64_t n = t.unit / g.G, grp = t.unit % g.G;
+    const int64_t item = (n * g.C + grp * g.Cg + t.piece / g.T) * g.T + t.piece % g.T;
+    if (t.pass == 1) {
+      if (kBwd)
+        reduce_chunk<T, VW>(p, item, sm);
+      else
+        stats_chunk<T, VW>(p, item, sm);
+      return;
+    }
+    if (wait_ready(p.ready + t.unit, p.err)) {
+      if (kBwd)
+        dx_chunk<T, VW>(p, item);
+      else
+        apply_chunk<T, VW>(p, item);
+    }
+    finish_pass2(p, t.unit);
+  });
 }
 
 template <typename T, int VW>
@@ -370,6 +441,13 @@ const void* kernel_vw(const Geom& g, bool bwd, int second, size_t* smem) {
                    : kernel_t<T, Elem<T>::VEC>(g, bwd, second, smem);
 }
 
+template <typename T>
+const void* pipelined_t(const Geom& g, bool bwd, size_t* smem) {
+  *smem = sizeof(float) * nchw_smem_floats(g);
+  constexpr int V = Elem<T>::VEC;
+  return bwd ? (const void*)nchw_pipelined<T, V, true> : (const void*)nchw_pipelined<T, V, false>;
+}
+
 }  // namespace
 
 const void* nchw_kernel(const Geom& g, bool bwd, int second, size_t* smem) {
@@ -386,6 +464,21 @@ cudaError_t launch_nchw(const KParams& p, cudaStream_t s, bool bwd) {
     case kF16: return dispatch_vw<__half>(p, s, bwd);
     default: return dispatch_vw<__nv_bfloat16>(p, s, bwd);
   }
+}
+
+// The pipelined kernel of a plan (16-byte vectors only).
+const void* nchw_pipelined_kernel(const Geom& g, bool bwd, size_t* smem) {
+  switch (g.dtype) {
+    case kF32: return pipelined_t<float>(g, bwd, smem);
+    case kF16: return pipelined_t<__half>(g, bwd, smem);
+    default: return pipelined_t<__nv_bfloat16>(g, bwd, smem);
+  }
+}
+
+cudaError_t launch_nchw_pipelined(const KParams& p, cudaStream_t s, bool bwd) {
+  size_t smem = 0;
+  const void* k = nchw_pipelined_kernel(p.g, bwd, &smem);
+  return launch_cooperative(k, p, smem, s);
 }
 
 }  // namespace gn

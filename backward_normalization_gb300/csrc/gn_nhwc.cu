@@ -18,7 +18,7 @@
 //           nhwc_bwd_dx     -> dx = rstd*gamma*dy + B*(x - mean) + D
 // The second kernel of each op walks items and rows in the reverse order of
 // the first, so it starts on the data the first kernel left in L2.
-#include "gn_finalize.cuh"
+#include "gn_tasks.cuh"
 
 namespace gn {
 namespace {
@@ -91,17 +91,15 @@ __device__ __forceinline__ void publish_nhwc(const KParams& p, const NhwcItem& i
       p.part[it.n * g.C * g.Tp + t1 * g.C + c] = make_float2(ax, ay);
     }
   };
-  arrive_and_finalize<T, kBwd>(p, it.n, (it.n * g.ncb + it.cb) * g.Tp + t1, gsize, merge, red,
-                               (int64_t)2 * VW * tpb);
+  arrive_and_finalize<T, kBwd>(p, unit_of(p, it.n, 0), (it.n * g.ncb + it.cb) * g.Tp + t1, gsize,
+                               merge, red, (int64_t)2 * VW * tpb);
 }
 
+// Forward pass 1 of one item: per-channel shifted sums, then publish.
 template <typename T, int VW>
-__global__ void __launch_bounds__(512, 2) nhwc_fwd_stats(const __grid_constant__ KParams p) {
-  grid_dependency_wait();  // the previous kernel's results (and x, dy) are complete
-  grid_launch_dependents();
-  extern __shared__ float red[];
+__device__ __forceinline__ void stats_item(const KParams& p, int64_t item, float* red) {
   const Geom& g = p.g;
-  const NhwcItem it = nhwc_item(g, blockIdx.x);
+  const NhwcItem it = nhwc_item(g, item);
   float acc[2 * VW];
 #pragma unroll
   for (int q = 0; q < 2 * VW; ++q) acc[q] = 0.f;
@@ -146,13 +144,19 @@ __global__ void __launch_bounds__(512, 2) nhwc_fwd_stats(const __grid_constant__
   publish_nhwc<T, VW, false>(p, it, red, acc);
 }
 
-template <typename T, int VW, int NG>
-__global__ void __launch_bounds__(512, 2) nhwc_bwd_reduce(const __grid_constant__ KParams p) {
+template <typename T, int VW>
+__global__ void __launch_bounds__(512, 2) nhwc_fwd_stats(const __grid_constant__ KParams p) {
   grid_dependency_wait();  // the previous kernel's results (and x, dy) are complete
   grid_launch_dependents();
   extern __shared__ float red[];
+  stats_item<T, VW>(p, blockIdx.x, red);
+}
+
+// Backward pass 1 of one item: per-channel sum(dy), sum(dy*(x-mean)), then publish.
+template <typename T, int VW, int NG>
+__device__ __forceinline__ void reduce_item(const KParams& p, int64_t item, float* red) {
   const Geom& g = p.g;
-  const NhwcItem it = nhwc_item(g, blockIdx.x);
+  const NhwcItem it = nhwc_item(g, item);
   float acc[2 * VW];
 #pragma unroll
   for (int q = 0; q < 2 * VW; ++q) acc[q] = 0.f;
@@ -205,11 +209,18 @@ __global__ void __launch_bounds__(512, 2) nhwc_bwd_reduce(const __grid_constant_
 }
 
 template <typename T, int VW, int NG>
-__global__ void __launch_bounds__(512, 2) nhwc_fwd_apply(const __grid_constant__ KParams p) {
+__global__ void __launch_bounds__(512, 2) nhwc_bwd_reduce(const __grid_constant__ KParams p) {
   grid_dependency_wait();  // the previous kernel's results (and x, dy) are complete
   grid_launch_dependents();
+  extern __shared__ float red[];
+  reduce_item<T, VW, NG>(p, blockIdx.x, red);
+}
+
+// Forward pass 2 of one item: y = (x - mean) * rstd*gamma + beta, rows last to first.
+template <typename T, int VW, int NG>
+__device__ __forceinline__ void apply_item(const KParams& p, int64_t item) {
   const Geom& g = p.g;
-  const NhwcItem it = nhwc_item(g, g.items - 1 - (int64_t)blockIdx.x);
+  const NhwcItem it = nhwc_item(g, item);
   if (!it.active) return;
   const int64_t cnt = it.row1 - it.row0 - it.r;  // rows of this lane: r, r+step, ...
   if (cnt <= 0) return;
@@ -219,10 +230,10 @@ __global__ void __launch_bounds__(512, 2) nhwc_fwd_apply(const __grid_constant__
   for (int k = 0; k < VW; ++k) {
     const int64_t c = it.col * VW + k;
     const int64_t ng = it.n * g.G + c / g.Cg;
-    const float r = __ldg(p.rstd + ng);
+    const float r = __ldcg(p.rstd + ng);  // written earlier in this call: not the read-only path
     a[k] = p.gamma ? r * __ldg(p.gamma + c) : r;
     b[k] = p.beta ? __ldg(p.beta + c) : 0.f;
-    if (NG > 1 || k == 0) mu.v[NG > 1 ? k : 0] = __ldg(p.mean + ng);
+    if (NG > 1 || k == 0) mu.v[NG > 1 ? k : 0] = __ldcg(p.mean + ng);
   }
   const int64_t off = it.n * g.HW * g.C + it.col * VW;
   const T* xn = static_cast<const T*>(p.x) + off;
@@ -250,12 +261,11 @@ __global__ void __launch_bounds__(512, 2) nhwc_fwd_apply(const __grid_constant__
   }
 }
 
+// Backward pass 2 of one item: dx = rstd*gamma*dy + B*(x - mean) + D, rows last to first.
 template <typename T, int VW, int NG>
-__global__ void __launch_bounds__(512, 2) nhwc_bwd_dx(const __grid_constant__ KParams p) {
-  grid_dependency_wait();  // the previous kernel's results (and x, dy) are complete
-  grid_launch_dependents();
+__device__ __forceinline__ void dx_item(const KParams& p, int64_t item) {
   const Geom& g = p.g;
-  const NhwcItem it = nhwc_item(g, g.items - 1 - (int64_t)blockIdx.x);
+  const NhwcItem it = nhwc_item(g, item);
   if (!it.active) return;
   const int64_t cnt = it.row1 - it.row0 - it.r;
   if (cnt <= 0) return;
@@ -310,6 +320,47 @@ __global__ void __launch_bounds__(512, 2) nhwc_bwd_dx(const __grid_constant__ KP
 }
 
 template <typename T, int VW, int NG>
+__global__ void __launch_bounds__(512, 2) nhwc_fwd_apply(const __grid_constant__ KParams p) {
+  grid_dependency_wait();  // the previous kernel's results (and x, dy) are complete
+  grid_launch_dependents();
+  apply_item<T, VW, NG>(p, p.g.items - 1 - (int64_t)blockIdx.x);
+}
+
+template <typename T, int VW, int NG>
+__global__ void __launch_bounds__(512, 2) nhwc_bwd_dx(const __grid_constant__ KParams p) {
+  grid_dependency_wait();
+  grid_launch_dependents();
+  dx_item<T, VW, NG>(p, p.g.items - 1 - (int64_t)blockIdx.x);
+}
+
+// The pipelined regime: one persistent kernel over the tasks of gn_tasks.cuh.
+// A unit is a sample, a piece is one row block (item u*T + q; one column
+// block per row).
+template <typename T, int VW, int NG, bool kBwd>
+__global__ void __launch_bounds__(512, 2) nhwc_pipelined(const __grid_constant__ KParams p) {
+  extern __shared__ float red[];
+  grid_dependency_wait();
+  const Geom& g = p.g;
+  run_tasks(p, [&](const Task& t) {
+    const int64_t item = t.unit * g.T + t.piece;
+    if (t.pass == 1) {
+      if (kBwd)
+        reduce_item<T, VW, NG>(p, item, red);
+      else
+        stats_item<T, VW>(p, item, red);
+      return;
+    }
+    if (wait_ready(p.ready + t.unit, p.err)) {
+      if (kBwd)
+        dx_item<T, VW, NG>(p, item);
+      else
+        apply_item<T, VW, NG>(p, item);
+    }
+    finish_pass2(p, t.unit);
+  });
+}
+
+template <typename T, int VW, int NG>
 cudaError_t run_op(const KParams& p, cudaStream_t s, bool bwd) {
   const Geom& g = p.g;
   const size_t sm1 = sizeof(float) * 2 * VW * g.tpb;
@@ -348,7 +399,35 @@ const void* kernel_vw(const Geom& g, bool bwd, int second, size_t* smem) {
                                  : kernel_t<T, V, V>(g, bwd, second, smem);
 }
 
+template <typename T, int NG>
+const void* pipelined_t(const Geom& g, bool bwd, size_t* smem) {
+  constexpr int V = Elem<T>::VEC;
+  *smem = sizeof(float) * 2 * V * g.tpb;
+  return bwd ? (const void*)nhwc_pipelined<T, V, NG, true> : (const void*)nhwc_pipelined<T, V, NG, false>;
+}
+
+template <typename T>
+const void* pipelined_vw(const Geom& g, bool bwd, size_t* smem) {
+  return one_group_per_vector(g) ? pipelined_t<T, 1>(g, bwd, smem)
+                                 : pipelined_t<T, Elem<T>::VEC>(g, bwd, smem);
+}
+
 }  // namespace
+
+// The pipelined kernel of a plan (16-byte vectors only).
+const void* nhwc_pipelined_kernel(const Geom& g, bool bwd, size_t* smem) {
+  switch (g.dtype) {
+    case kF32: return pipelined_vw<float>(g, bwd, smem);
+    case kF16: return pipelined_vw<__half>(g, bwd, smem);
+    default: return pipelined_vw<__nv_bfloat16>(g, bwd, smem);
+  }
+}
+
+cudaError_t launch_nhwc_pipelined(const KParams& p, cudaStream_t s, bool bwd) {
+  size_t smem = 0;
+  const void* k = nhwc_pipelined_kernel(p.g, bwd, &smem);
+  return launch_cooperative(k, p, smem, s);
+}
 
 const void* nhwc_kernel(const Geom& g, bool bwd, int second, size_t* smem) {
   switch (g.dtype) {

@@ -212,6 +212,118 @@ bool plan_resident(Geom& g, int op) {
 }
 }  // namespace
 
+namespace {
+// Pipelined regime.  A piece holds about kPipePieceBytes of input (x, or x
+// and dy), in whole unrolled load rounds; pass-2 tasks trail pass-1 tasks by
+// enough units that about kPipeLagCtas tasks lie between the two passes of a
+// unit, while the lagging units' input (what pass 2 finds in L2) stays within
+// kPipeL2Bytes.
+#ifndef GN_PIPE_PIECE_BYTES
+#define GN_PIPE_PIECE_BYTES (128 * 1024)
+#endif
+#ifndef GN_PIPE_TASKS_PER_CTA
+#define GN_PIPE_TASKS_PER_CTA 2
+#endif
+#ifndef GN_PIPE_LAG_CTAS
+#define GN_PIPE_LAG_CTAS 2
+#endif
+#ifndef GN_PIPE_L2_BYTES
+#define GN_PIPE_L2_BYTES (64ll << 20)
+#endif
+constexpr int64_t kPipePieceBytes = GN_PIPE_PIECE_BYTES;
+constexpr int64_t kPipeLagCtas = GN_PIPE_LAG_CTAS;
+constexpr int64_t kPipeTasksPerCta = GN_PIPE_TASKS_PER_CTA;
+constexpr int64_t kPipeL2Bytes = GN_PIPE_L2_BYTES;
+
+// CTAs of the pipelined kernel that fit on the device at once, or an estimate
+// (two 512-thread CTAs per SM) when no device is visible; 0 if none fit.
+int64_t pipelined_ctas(const Geom& g, int op, int sm_count) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return (int64_t)sm_count * (g.tpb > 256 ? 2 : 4);
+  }
+  size_t smem = 0;
+  const void* fn = g.layout == kNHWC ? nhwc_pipelined_kernel(g, op == kBwd, &smem)
+                                     : nchw_pipelined_kernel(g, op == kBwd, &smem);
+  int nb = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fn, g.tpb, smem) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return (int64_t)nb * sm_count;
+}
+
+// Fills the pipelined-regime fields of g (a two-kernel plan of the same
+// problem); false when the problem does not fit the regime.
+bool plan_pipelined(Geom& g, int op, int sm_count) {
+  const int esz = g.dtype == kF32 ? 4 : 2;
+  const int vec = 16 / esz;
+  const int nten = op == kBwd ? 2 : 1;
+  if (g.vw != vec) return false;
+  Geom r = g;
+  // The persistent grid: sized before the pieces (the kernel does not depend
+  // on them).
+  r.regime = kRegimePipelined;
+  r.grid = pipelined_ctas(r, op, sm_count);
+  if (r.grid <= 0) return false;
+  // Piece size: about kPipeTasksPerCta pass-1 tasks per CTA, at most
+  // kPipePieceBytes of input each.
+  const int64_t in_bytes = g.N * g.C * g.HW * esz * nten;
+  const int64_t piece_bytes =
+      clamp64(cdiv(in_bytes, kPipeTasksPerCta * r.grid), 1, kPipePieceBytes);
+  int64_t unit_bytes;
+  if (g.layout == kNHWC) {
+    if (g.ncb != 1) return false;
+    unit_bytes = g.HW * g.C * esz * nten;
+    // rows per piece: whole steps of the rpi row lanes
+    const int64_t row_bytes = g.C * esz * nten;
+    const int64_t rb = rup(clamp64(piece_bytes / row_bytes, 1, g.HW), g.rpi);
+    r.rb = rb;
+    r.T = cdiv(g.HW, rb);
+    r.units_fin = g.N;
+    r.unit_groups = 0;
+    r.pieces = r.T;
+    r.l1 = r.T >= 2 * kGroup1 ? kGroup1 : 1;
+    r.Tp = cdiv(r.T, r.l1);
+    r.groups1 = r.l1 > 1 ? g.N * r.Tp : 0;
+    r.cstride = 1;
+    r.tstride = g.C;
+    r.arrivals_per_n = r.Tp;
+    r.items_per_n = r.T;
+  } else {
+    if (g.mode != 0) return false;
+    unit_bytes = g.Cg * g.HW * esz * nten;
+    // chunk: whole steps of tpb threads x one vector
+    const int64_t step = (int64_t)g.tpb * vec;
+    int64_t L = rup(clamp64(piece_bytes / (esz * nten), 1, g.HW), step);
+    if (L > rup(g.HW, vec)) L = rup(g.HW, vec);
+    r.L = L;
+    r.T = cdiv(g.HW, L);
+    r.units_fin = g.N * g.G;
+    r.unit_groups = 1;
+    r.pieces = g.Cg * r.T;
+    r.l1 = r.T >= 2 * kGroup1 ? kGroup1 : 1;
+    r.Tp = cdiv(r.T, r.l1);
+    r.groups1 = r.l1 > 1 ? g.N * g.C * r.Tp : 0;
+    r.cstride = r.Tp;
+    r.tstride = 1;
+    r.arrivals_per_n = g.Cg * r.Tp;
+    r.items_per_n = g.C * r.T;
+  }
+  if (2 * unit_bytes > kPipeL2Bytes) return false;
+  r.items = g.N * r.items_per_n;
+  r.keep_from = 0;  // pass 1 keeps everything it reads in L2 for pass 2
+  const int64_t U = r.units_fin;
+  if (2 * U * r.pieces > 0x7fffffffLL) return false;  // task indices are 32-bit
+  int64_t lag = cdiv(kPipeLagCtas * r.grid, 2 * r.pieces);
+  lag = clamp64(lag, 1, kPipeL2Bytes / unit_bytes);
+  r.lag = clamp64(lag, 1, U);
+  g = r;
+  return true;
+}
+}  // namespace
+
 int64_t plan_max_clusters(const Geom& g, int op) {
   if (g.regime == kRegimeResident) return resident_clusters(g, op);
   const int64_t r = resident_ctas(g, op, 0);
@@ -265,7 +377,8 @@ int64_t resident_ctas(const Geom& g, int op, int second) {
   return r;
 }
 
-Geom make_geom(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout, int dtype,
+namespace {
+Geom plan_geom(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout, int dtype,
                bool aligned) {
   const int sm_count = device_sm_count();
   Geom g{};
@@ -343,21 +456,71 @@ Geom make_geom(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout, 
     g.keep_from = keep_frac >= 1.0 ? 0 : 1;  // whole rows: all or nothing
   else
     g.keep_from = item_len - (int64_t)((double)item_len * keep_frac);
+  g.units_fin = N;  // the two-kernel path finalises per sample
+  g.unit_groups = 0;
   g.regime = kRegimeGeneric;
   const int ov = g_regime_override.load();
   if (ov == kRegimeResident) {
     plan_resident(g, op);  // wherever the problem fits the regime
+  } else if (ov == kRegimePipelined) {
+    plan_pipelined(g, op, sm_count);
   } else if (ov == kRegimeAuto && resident_preferred(g, op)) {
+    // measured on GB300: the pipelined kernel is not yet faster than these
+    // families on any workload here, so it runs only when asked for
     plan_resident(g, op);
   }
+  const int64_t pipe = g.regime == kRegimePipelined ? 2 * g.units_fin + 2 : 0;
+  g.counters = g.regime == kRegimeResident ? 0 : g.units_fin + 1 + g.groups1 + pipe;
   return g;
+}
+
+// Plans are cached per (device, regime override, op, problem, alignment):
+// building one queries occupancy, and every call (and every workspace layout,
+// which looks at the plans of both ops) needs them.
+using PlanKey = std::tuple<int, int, int, int64_t, int64_t, int64_t, int64_t, int, int, int>;
+std::mutex g_plan_mu;
+std::map<PlanKey, Geom> g_plan_cache;
+constexpr size_t kPlanCacheMax = 4096;
+}  // namespace
+
+Geom make_geom(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout, int dtype,
+               bool aligned) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    dev = -1;
+  }
+  const PlanKey key{dev, g_regime_override.load(), op, N, C, HW, G, layout, dtype, aligned ? 1 : 0};
+  {
+    std::lock_guard<std::mutex> lock(g_plan_mu);
+    auto it = g_plan_cache.find(key);
+    if (it != g_plan_cache.end()) return it->second;
+  }
+  const Geom g = plan_geom(op, N, C, HW, G, layout, dtype, aligned);
+  std::lock_guard<std::mutex> lock(g_plan_mu);
+  if (g_plan_cache.size() >= kPlanCacheMax) g_plan_cache.clear();
+  g_plan_cache.emplace(key, g);
+  return g;
+}
+
+int64_t problem_counters(const Geom& g) {
+  int64_t c = 0;
+  for (int op = 0; op < 2; ++op)
+    for (int a = 0; a < 2; ++a) {
+      const Geom o = make_geom(op, g.N, g.C, g.HW, g.G, g.layout, g.dtype, a != 0);
+      if (o.counters > c) c = o.counters;
+    }
+  return c;
 }
 
 WsLayout ws_layout(int op, const Geom& g) {
   WsLayout w{};
   size_t off = 0;
   w.tickets = off;
-  off = align256(off + sizeof(unsigned) * (size_t)(g.N + 1 + g.groups1));
+  // the counter region is the same for both ops and both alignments of a
+  // problem, so that a workspace serves a forward and its backward
+  (void)op;
+  off = align256(off + sizeof(unsigned) * (size_t)problem_counters(g));
   w.err = off;
   off = align256(off + sizeof(unsigned));
   w.part0 = off;

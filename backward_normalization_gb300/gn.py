@@ -39,7 +39,8 @@ class PlanDesc(ctypes.Structure):
                 ("vector_width", ctypes.c_int), ("threads", ctypes.c_int),
                 ("ctas", ctypes.c_int64), ("partials", ctypes.c_int64),
                 ("workspace_bytes", ctypes.c_size_t), ("cluster_ctas", ctypes.c_int),
-                ("max_clusters", ctypes.c_int), ("smem_bytes", ctypes.c_size_t)]
+                ("max_clusters", ctypes.c_int), ("smem_bytes", ctypes.c_size_t),
+                ("err_offset", ctypes.c_size_t)]
 
 
 _lib = None
@@ -140,7 +141,7 @@ def bwd_raw(dy, x, mean, rstd, gamma, N, C, HW, G, layout, dx, dgamma, dbeta, wo
                         _ptr(workspace), ws_bytes, _stream(stream))
 
 
-REGIME_AUTO, REGIME_TWO_KERNEL, REGIME_RESIDENT = -1, 0, 1
+REGIME_AUTO, REGIME_TWO_KERNEL, REGIME_RESIDENT, REGIME_PIPELINED = -1, 0, 1, 2
 
 
 def set_regime(regime: int) -> None:

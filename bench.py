@@ -44,36 +44,43 @@ def min_bytes(w):
     return {"fwd": 2 * e, "bwd": 3 * e}
 
 
-def kernel_bytes(w, fwd_launches=2, bwd_launches=2):
+REGIME_NAMES = {0: "two-kernel", 1: "resident", 2: "pipelined"}
+
+
+def kernel_bytes(w, fwd_regime=0, bwd_regime=0):
     """Algorithmic bytes of each kernel (what it must move at least).  The
-    two-kernel path reads its input twice by construction; the resident path
-    runs one kernel per op that moves the op's minimal traffic."""
+    two-kernel path reads its input twice by construction; the resident and
+    pipelined regimes run one kernel per op that moves the op's minimal
+    traffic."""
     e = w.E * esize(w.dtype)
     kb = {}
-    if fwd_launches == 2:
+    if fwd_regime == 0:
         kb.update({"fwd_stats": e, "fwd_apply": 2 * e})
     else:
-        kb["fwd_resident"] = 2 * e
-    if bwd_launches == 2:
+        kb["fwd_" + REGIME_NAMES[fwd_regime]] = 2 * e
+    if bwd_regime == 0:
         kb.update({"bwd_reduce": 2 * e, "bwd_dx": 3 * e})
     else:
-        kb["bwd_resident"] = 3 * e
+        kb["bwd_" + REGIME_NAMES[bwd_regime]] = 3 * e
     return kb
 
 
 def kernel_times(kb, ev):
     """Per-kernel ms from the six events of one step (fwd: 0-2, bwd: 3-5)."""
     t = {}
-    if "fwd_stats" in kb:
-        t["fwd_stats"] = ev[0].elapsed_time(ev[1])
-        t["fwd_apply"] = ev[1].elapsed_time(ev[2])
-    else:
-        t["fwd_resident"] = ev[0].elapsed_time(ev[2])
-    if "bwd_reduce" in kb:
-        t["bwd_reduce"] = ev[3].elapsed_time(ev[4])
-        t["bwd_dx"] = ev[4].elapsed_time(ev[5])
-    else:
-        t["bwd_resident"] = ev[3].elapsed_time(ev[5])
+    for k in kb:
+        if k == "fwd_stats":
+            t[k] = ev[0].elapsed_time(ev[1])
+        elif k == "fwd_apply":
+            t[k] = ev[1].elapsed_time(ev[2])
+        elif k == "bwd_reduce":
+            t[k] = ev[3].elapsed_time(ev[4])
+        elif k == "bwd_dx":
+            t[k] = ev[4].elapsed_time(ev[5])
+        elif k.startswith("fwd_"):
+            t[k] = ev[0].elapsed_time(ev[2])
+        else:
+            t[k] = ev[3].elapsed_time(ev[5])
     return t
 
 
@@ -279,7 +286,7 @@ def time_configs(gn, synth, torch, flush, names=None, reps=20):
         torch.cuda.synchronize()
         pf = gn.plan_info(0, w.N, w.C, w.HW, w.G, w.layout, w.dtype)
         pb = gn.plan_info(1, w.N, w.C, w.HW, w.G, w.layout, w.dtype)
-        kb = kernel_bytes(w, pf.launches, pb.launches)
+        kb = kernel_bytes(w, pf.regime, pb.regime)
         rec = {"fwd": [], "bwd": []}
         for ev, ek in zip(evs[3:], evk[3:]):
             rec["fwd"].append(ev[0].elapsed_time(ev[2]))
@@ -291,8 +298,7 @@ def time_configs(gn, synth, torch, flush, names=None, reps=20):
         fwd_gbs = mb["fwd"] / (med["fwd"] * 1e-3) / 1e9
         bwd_gbs = mb["bwd"] / (med["bwd"] * 1e-3) / 1e9
         out[w.name if w.N == synth.BY_NAME[w.name].N else f"{w.name}:N={w.N}"] = {
-            "regime": {"fwd": "resident" if pf.launches == 1 else "two-kernel",
-                       "bwd": "resident" if pb.launches == 1 else "two-kernel"},
+            "regime": {"fwd": REGIME_NAMES[pf.regime], "bwd": REGIME_NAMES[pb.regime]},
             "fwd_us": round(med["fwd"] * 1e3, 2), "bwd_us": round(med["bwd"] * 1e3, 2),
             "fwd_gbs": round(fwd_gbs, 1), "bwd_gbs": round(bwd_gbs, 1),
             "fwd_frac": round(fwd_gbs / peak, 4), "bwd_frac": round(bwd_gbs / peak, 4),
@@ -432,7 +438,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     plan_f = gn.plan_info(0, w.N, w.C, w.HW, w.G, w.layout, w.dtype)
     plan_b = gn.plan_info(1, w.N, w.C, w.HW, w.G, w.layout, w.dtype)
-    kb = kernel_bytes(w, plan_f.launches, plan_b.launches)
+    kb = kernel_bytes(w, plan_f.regime, plan_b.regime)
     kern = {}
     for e in evs[:Ks]:
         for k, v in kernel_times(kb, e).items():

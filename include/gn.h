@@ -37,11 +37,15 @@
  *
  * Workspace: a caller-provided device buffer of at least gn_workspace_size()
  * bytes, 16-byte aligned, ZERO-FILLED before its first use (for example with
- * cudaMemsetAsync).  Its first bytes hold the arrival counters of the
- * cross-CTA reductions; every call that runs to completion leaves them at zero
- * again, so one workspace can serve any sequence of later calls, of any shape
- * and either op, without being cleared again.  The rest is scratch.  Two calls
- * that are in flight at the same time must not share one workspace.
+ * cudaMemsetAsync).  Its first bytes hold the arrival counters, ready flags
+ * and task queue of the cross-CTA reductions, laid out alike for both ops and
+ * both pointer alignments of one problem (N, C, HW, G, layout, dtype); every
+ * call that runs to completion leaves them at zero again, so one workspace
+ * serves any sequence of later calls of that problem, either op, without
+ * being cleared.  The rest is scratch.  Before a workspace serves a problem of
+ * another shape, zero-fill it again (the new problem's counters may lie where
+ * the old one kept scratch).  Two calls that are in flight at the same time
+ * must not share one workspace.
  */
 #ifndef GN_H_
 #define GN_H_
@@ -153,21 +157,29 @@ GN_API int gn_set_timing_events(void* ev_begin, void* ev_mid, void* ev_end);
  * elementwise kernel (y, or dx).  GN_REGIME_RESIDENT runs one kernel in which
  * a thread-block cluster holds a whole reduction unit -- one (n, group) span
  * for NCHW, one sample for NHWC -- in shared memory; it is taken for 16-byte
- * aligned inputs whose unit is at most 32 MiB. */
+ * aligned inputs whose unit is at most 32 MiB.  GN_REGIME_PIPELINED runs one
+ * persistent kernel (a cooperative launch) whose CTAs take tasks from a queue:
+ * the first pass over a piece of a unit (one sample for NHWC, one (n, group)
+ * for NCHW), and, a few units behind, the second pass over the same pieces,
+ * which finds the unit's input still in L2; it is taken for 16-byte aligned
+ * inputs whose unit (x, or x and dy) is at most 32 MiB, and NHWC rows of at
+ * most 256 16-byte vectors.  Every regime gives results within the same
+ * tolerances of the definition, each bit-identical from run to run. */
 #define GN_REGIME_AUTO (-1)
 #define GN_REGIME_TWO_KERNEL 0
 #define GN_REGIME_RESIDENT 1
+#define GN_REGIME_PIPELINED 2
 
 /* Test hook, process-wide: GN_REGIME_AUTO (default) lets each call choose
  * the faster family for its shape; GN_REGIME_TWO_KERNEL forces the two-kernel
- * path; GN_REGIME_RESIDENT forces the resident regime wherever the problem
- * fits it (else the two-kernel path runs).  Not thread-safe with respect to
+ * path; GN_REGIME_RESIDENT and GN_REGIME_PIPELINED force that regime wherever
+ * the problem fits it (else the two-kernel path runs).  Not thread-safe with respect to
  * calls in flight on other threads.  Returns a gn_status. */
 GN_API int gn_set_regime(int regime);
 
 /* What a call would run, for tests and reports (host-only, no launch). */
 typedef struct gn_plan_desc {
-  int regime;            /* GN_REGIME_TWO_KERNEL or GN_REGIME_RESIDENT */
+  int regime;            /* GN_REGIME_TWO_KERNEL, GN_REGIME_RESIDENT or GN_REGIME_PIPELINED */
   int launches;          /* kernels one call enqueues */
   int vector_width;      /* elements per access: 16-byte vectors, or 1 (scalar path) */
   int threads;           /* threads per CTA */
@@ -177,6 +189,8 @@ typedef struct gn_plan_desc {
   int cluster_ctas;      /* CTAs per thread-block cluster of the first (or only) kernel */
   int max_clusters;      /* such clusters that fit on the device at once (0: unknown) */
   size_t smem_bytes;     /* dynamic shared memory per CTA of that kernel */
+  size_t err_offset;     /* workspace byte offset of the uint32 error word; the
+                            counters, flags and task queue lie before it */
 } gn_plan_desc;
 
 /* Fills *out with the plan of gn_fwd/gn_bwd for this problem, assuming every

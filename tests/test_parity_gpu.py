@@ -40,6 +40,10 @@ def _small_cases():
         ("fp16_nchw_2x16x64x64_g4", c1.scaled(name="f16nchw", layout="nchw", N=2, C=16, G=4, H=64, W=64)),
         ("bf16_nchw_2x8x3x683_g2_scalar", c2.scaled(name="b16nchw", layout="nchw", N=2, C=8, G=2, H=3, W=683)),
         ("bf16_nhwc_1x32x300x300_g8_many_rows", c2.scaled(name="rows", N=1, C=32, G=8, H=300, W=300)),
+        # many reduction units: pass-2 tasks of the pipelined kernel trail pass 1 by fewer units
+        # than there are, so both passes of different units interleave in its task order
+        ("fp32_nchw_16x64x48x48_g8_many_units", c3.scaled(name="mu3", N=16, H=48, W=48)),
+        ("bf16_nhwc_40x64x48x48_g8_many_units", c4.scaled(name="mu4", N=40, C=64, G=8, H=48, W=48)),
     ]
 
 
@@ -54,7 +58,8 @@ STREAMING = [
 ]
 
 
-REGIMES = {"auto": gn.REGIME_AUTO, "two_kernel": gn.REGIME_TWO_KERNEL, "resident": gn.REGIME_RESIDENT}
+REGIMES = {"auto": gn.REGIME_AUTO, "two_kernel": gn.REGIME_TWO_KERNEL, "resident": gn.REGIME_RESIDENT,
+           "pipelined": gn.REGIME_PIPELINED}
 
 
 @pytest.fixture(params=list(REGIMES))
@@ -203,8 +208,9 @@ def test_workspace_reuse_and_canaries(regime):
     wsb = torch.randint(0, 256, (n_ws + 256,), dtype=torch.uint8, device=dev)
     canary_ws = wsb[n_ws:].clone()
     ws = wsb[:n_ws]
-    err_off = (4 * (w.N + 1) + 255) // 256 * 256
-    ws[:err_off + 4].zero_()  # arrival counters and error word (the rest is scratch)
+    err_off = gn.plan_info(gn.OP_BWD, w.N, w.C, w.HW, w.G, w.layout, dt).err_offset
+    assert err_off == gn.plan_info(gn.OP_FWD, w.N, w.C, w.HW, w.G, w.layout, dt).err_offset
+    ws[:err_off + 4].zero_()  # counters, flags, task queue and error word (the rest is scratch)
 
     def padded(n, dtype):
         b = torch.full((n + 2 * pad,), 7.0, dtype=dtype, device=dev)
@@ -223,21 +229,48 @@ def test_workspace_reuse_and_canaries(regime):
         assert gn.bwd_raw(dy, x, mean, rstd, gm, w.N, w.C, w.HW, w.G, w.layout, dx, dg, db, ws) == 0
     torch.cuda.synchronize()
     assert torch.equal(wsb[n_ws:], canary_ws)
-    assert torch.all(ws[:4 * (w.N + 1)] == 0), "arrival counters not returned to zero"
+    assert torch.all(ws[:err_off] == 0), "arrival counters, flags or the task queue not returned to zero"
     assert int(ws[err_off:err_off + 4].view(torch.int32).item()) == 0, "a bounded wait ran out"
     for b in (yb, dxb, mb, rb, gb, bb):
         assert torch.all(b[:pad] == 7.0) and torch.all(b[-pad:] == 7.0)
     _compare(dict(y=y, mean=mean, rstd=rstd, dx=dx, dgamma=dg, dbeta=db), ref, w)
 
 
+def test_workspace_shared_by_fwd_and_bwd(regime):
+    """A forward and its backward (twice over) on one workspace give the same
+    bits as calls on fresh workspaces.  At this shape the backward's plan uses
+    more counters than the forward's (level-1 merges of its shorter chunks), so
+    a layout that followed each op's own plan would put the backward's counters
+    on the forward's partial records."""
+    w = synth.WORKLOADS[3].scaled(name="fb3", N=2)
+    dev = "cuda"
+    inp = synth.make_inputs(w, dev, seed=7)
+    x, dy, gm, bt = inp["x"], inp["dy"], inp["gamma"], inp["beta"]
+    ref = _gpu_run(inp, w)
+    dt = x.dtype
+    ws = gn.alloc_workspace(gn.OP_BWD, w.N, w.C, w.HW, w.G, w.layout, dt)
+    err_off = gn.plan_info(gn.OP_FWD, w.N, w.C, w.HW, w.G, w.layout, dt).err_offset
+    for _ in range(2):
+        y, mean, rstd = gn.forward(x, w.N, w.C, w.HW, w.G, w.layout, gm, bt, w.eps, workspace=ws)
+        dx, dg, db = gn.backward(dy, x, mean, rstd, w.N, w.C, w.HW, w.G, w.layout, gm, workspace=ws)
+        torch.cuda.synchronize()
+        got = dict(y=y, mean=mean, rstd=rstd, dx=dx, dgamma=dg, dbeta=db)
+        for k in got:
+            assert torch.equal(got[k], ref[k]), k
+    assert torch.all(ws[:err_off] == 0)
+    assert int(ws[err_off:err_off + 4].view(torch.int32).item()) == 0
+
+
 def test_shared_workspace_across_shapes(regime):
-    """Calls of different shapes in a row on one workspace stay correct."""
+    """One buffer serves calls of different shapes in a row when it is
+    zero-filled again before each new shape (the contract of gn.h)."""
     dev = "cuda"
     cases = [SMALL[0][1], SMALL[2][1], SMALL[3][1], SMALL[2][1]]
     n_ws = max(gn.workspace_size(op, w.N, w.C, w.HW, w.G, w.layout, w.dtype)
                for w in cases for op in (0, 1))
     ws = torch.zeros((n_ws,), dtype=torch.uint8, device=dev)
     for i, w in enumerate(cases):
+        ws.zero_()
         inp = synth.make_inputs(w, "cpu", seed=10 + i)
         x, dy = inp["x"].to(dev), inp["dy"].to(dev)
         gm, bt = inp["gamma"].to(dev), inp["beta"].to(dev)
@@ -281,7 +314,7 @@ def _sample_offsets(w, k=4096, seed=0):
 
 FULL = ([(w, "auto") for w in synth.WORKLOADS[1:]]
         + [(synth.WORKLOADS[3], "resident"), (synth.WORKLOADS[2], "resident"),
-           (synth.WORKLOADS[4], "two_kernel")])
+           (synth.WORKLOADS[4], "two_kernel"), (synth.WORKLOADS[2], "two_kernel")])
 
 
 @pytest.mark.parametrize("w,reg", FULL, ids=[f"{w.name}-{r}" for w, r in FULL])
