@@ -53,13 +53,13 @@ int prepare(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout, int
   p->tickets = reinterpret_cast<unsigned*>(ws + w.tickets);
   p->err = reinterpret_cast<unsigned*>(ws + w.err);
   // counters: one per unit, the global one, one per level-1 group, then (pipelined)
-  // a ready flag and a pass-2 counter per unit and the task queue
+  // a 64-bit ready record per unit and the count of CTAs done
   const int64_t U = p->g.units_fin;
   p->cnt1 = p->tickets + U + 1;
   if (p->g.regime == gn::kRegimePipelined) {
-    p->ready = p->cnt1 + p->g.groups1;
-    p->p2cnt = p->ready + U;
-    p->queue = p->p2cnt + U;
+    const int64_t r = U + 1 + p->g.groups1;
+    p->ready = p->tickets + (r + 1) / 2 * 2;  // 8-byte aligned records
+    p->queue = p->ready + 2 * U;
   }
   p->part = reinterpret_cast<float2*>(ws + w.part);
   p->part0 = p->g.l1 > 1 ? reinterpret_cast<float2*>(ws + w.part0) : p->part;
@@ -73,8 +73,7 @@ cudaError_t launch(const gn::KParams& p, cudaStream_t s, bool bwd) {
   const bool nhwc = p.g.layout == GN_LAYOUT_NHWC;
   switch (p.g.regime) {
     case gn::kRegimeResident: return gn::launch_resident(p, s, bwd);
-    case gn::kRegimePipelined:
-      return nhwc ? gn::launch_nhwc_pipelined(p, s, bwd) : gn::launch_nchw_pipelined(p, s, bwd);
+    case gn::kRegimePipelined: return gn::launch_nchw_pipelined(p, s, bwd);
     default: return nhwc ? gn::launch_nhwc(p, s, bwd) : gn::launch_nchw(p, s, bwd);
   }
 }
@@ -238,12 +237,7 @@ int gn_plan_info(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout
   if (g.regime == gn::kRegimeResident) {
     out->smem_bytes = g.smem;
   } else if (g.regime == gn::kRegimePipelined) {
-    size_t sm = 0;
-    if (g.layout == GN_LAYOUT_NHWC)
-      gn::nhwc_pipelined_kernel(g, op == GN_OP_BWD, &sm);
-    else
-      gn::nchw_pipelined_kernel(g, op == GN_OP_BWD, &sm);
-    out->smem_bytes = sm;
+    out->smem_bytes = g.smem;
   } else {
     size_t sm = 0;
     if (g.layout == GN_LAYOUT_NHWC)

@@ -64,6 +64,10 @@ struct Geom {
   int64_t pieces, lag;
   int64_t grid;        // persistent CTAs (all co-resident)
   int64_t counters;    // uint32 counter slots this plan uses at the start of the workspace
+  int dy_in_ring;      // pipelined backward: each ring slot holds a dy chunk after the x chunk
+  // pipelined: S ring slots of ten_stride bytes per tensor; a chunk is `chunk`
+  // elements (NCHW) or rows (NHWC); slot headers at off_tot, mbarriers at
+  // off_bar, reduction scratch at off_red; smem bytes in all
   // resident regime (gn_resident.cu)
   int regime;
   int K;               // CTAs per unit (cluster size)
@@ -80,11 +84,15 @@ struct Geom {
   size_t off_ring, off_red, off_xch, off_tot, off_grp, off_bar;
 };
 
+// Bytes reserved per ring-slot header of the pipelined kernel (the header
+// struct of gn_tasks.cuh is checked against it at compile time).
+constexpr size_t kSlotHdrBytes = 112;
+
 // Workspace layout (byte offsets, each 256-byte aligned).
 struct WsLayout {
   size_t tickets;  // uint32 counters: one per finalisation unit, 1 global, one per level-1
-                   // group; pipelined: then a ready flag and a pass-2 counter per unit
-                   // and the task queue (next task, CTAs done).  Sized by
+                   // group; pipelined: then (8-byte aligned) a 64-bit ready
+                   // record per unit and the count of CTAs done.  Sized by
                    // problem_counters(), whichever op and alignment the call has.
   size_t err;      // uint32 error word (a bounded wait ran out)
   size_t part0;    // N*C*T float2 item partial sums (when l1 > 1)
@@ -110,9 +118,8 @@ struct KParams {
   float eps;
   unsigned* tickets;  // [0, units_fin) per unit, [units_fin] global
   unsigned* cnt1;     // per level-1 group
-  unsigned* ready;    // pipelined: per unit, 1 once its statistics are written
-  unsigned* p2cnt;    // pipelined: per unit, pass-2 tasks done
-  unsigned* queue;    // pipelined: [0] next task, [1] CTAs done
+  unsigned* ready;    // pipelined: per unit a 64-bit ready record (8-byte aligned)
+  unsigned* queue;    // pipelined: [0] CTAs done
   unsigned* err;
   float2* part0;      // item partials (== part when l1 == 1)
   float2* part;
@@ -147,11 +154,10 @@ const TimingEvents& timing_events();
 // kernels (gn_nhwc.cu / gn_nchw.cu): enqueue the two kernels of an op.
 cudaError_t launch_nhwc(const KParams& p, cudaStream_t s, bool bwd);
 cudaError_t launch_nchw(const KParams& p, cudaStream_t s, bool bwd);
-// The pipelined regime's kernel (one launch, cooperative).
-cudaError_t launch_nhwc_pipelined(const KParams& p, cudaStream_t s, bool bwd);
+// The pipelined regime's kernel (NCHW; one launch, cooperative).
 cudaError_t launch_nchw_pipelined(const KParams& p, cudaStream_t s, bool bwd);
-const void* nhwc_pipelined_kernel(const Geom& g, bool bwd, size_t* smem);
 const void* nchw_pipelined_kernel(const Geom& g, bool bwd, size_t* smem);
+int64_t nchw_pipelined_scratch_floats(const Geom& g);
 // The first (second = 0) or second (second = 1) kernel's function and its
 // dynamic shared memory for a plan.
 const void* nhwc_kernel(const Geom& g, bool bwd, int second, size_t* smem);

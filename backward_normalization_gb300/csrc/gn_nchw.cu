@@ -13,8 +13,8 @@
 // In the two-kernel path the last arrival of a sample finalises it and the
 // elementwise second kernels walk the items (and the elements of a chunk) in
 // reverse order, starting on the data the first kernel left in L2.  The
-// pipelined kernel (mode 0 only) runs the same chunk functions as tasks of
-// gn_tasks.cuh, with one (sample, group) per unit.
+// pipelined kernel (mode-0 shapes, 16-byte vectors) runs the lockstep
+// schedule of gn_tasks.cuh over (sample, group) units, fed by bulk copies.
 #include "gn_tasks.cuh"
 
 namespace gn {
@@ -380,31 +380,155 @@ __global__ void __launch_bounds__(512) nchw_bwd_dx(const __grid_constant__ KPara
     dx_rows<T, VW>(p, item);
 }
 
-// The pipelined regime: a unit is one (sample n, group), its pieces the
-// chunks of its Cg planes (piece q: plane group*Cg + q/T, chunk q%T).
+// The pipelined regime (schedule in gn_tasks.cuh): a unit is one (sample n,
+// group), its pieces the segments of its Cg planes (piece q: plane
+// group*Cg + q/T, segment q%T), piece q of every unit streamed by CTA q in
+// chunks of g.chunk elements; thread t takes the chunk's 16-byte vectors t,
+// t + blockDim.x, ...  A pass-1 piece leaves one record (its shifted sums, or
+// sum(dy) and sum(dy*(x - mean))); the unit's finaliser merges the Cg*T
+// records as the two-kernel path does and publishes (mean, rstd) or (B, D).
 template <typename T, int VW, bool kBwd>
-__global__ void __launch_bounds__(512) nchw_pipelined(const __grid_constant__ KParams p) {
-  extern __shared__ float sm[];
-  grid_dependency_wait();
+__global__ void __launch_bounds__(512, 1) nchw_pipelined(const __grid_constant__ KParams p) {
+  extern __shared__ __align__(128) char smem_raw[];
+  char* smem = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
   const Geom& g = p.g;
-  run_tasks(p, [&](const Task& t) {
+  const RingSmem R = ring_smem(g, smem);
+  float* sm = reinterpret_cast<float*>(smem + g.off_red);
+  const int64_t sm_floats = nchw_smem_floats(g);
+  unsigned long long* rec = reinterpret_cast<unsigned long long*>(p.ready);
+  const int tid = threadIdx.x, nt = blockDim.x;
+  const uint64_t pfirst = policy_evict_first();
+  float s1 = 0.f, s2 = 0.f, K = 0.f;               // pass-1 sums; shift (fwd) or mean (bwd)
+  float ca = 0.f, cb = 0.f, cc = 0.f, cmu = 0.f;   // pass-2 constants
+  bool ok = false;
+  Pending pd;
+  pd.unit[0] = pd.unit[1] = -1;
+  // piece of task t: plane a (channel e) of sample unit / G, segment b = [c, d)
+  auto describe = [&](const Task& t, SlotHdr& h) {
     const int64_t n = t.unit / g.G, grp = t.unit % g.G;
-    const int64_t item = (n * g.C + grp * g.Cg + t.piece / g.T) * g.T + t.piece % g.T;
+    const int64_t plane = grp * g.Cg + t.piece / g.T, seg = t.piece % g.T;
+    h.a = n * g.C + plane;
+    h.b = seg;
+    h.c = seg * g.L;
+    h.d = (h.c + g.L < g.HW) ? h.c + g.L : g.HW;
+    h.e = plane;
+    h.nchunks = (int32_t)((h.d - h.c + g.chunk - 1) / g.chunk);
+    // pass 1 brings along its shift: the plane's first element (forward) or
+    // the group's mean (backward, when mean is 16-byte aligned)
+    h.aux_off = 0;
     if (t.pass == 1) {
-      if (kBwd)
-        reduce_chunk<T, VW>(p, item, sm);
-      else
-        stats_chunk<T, VW>(p, item, sm);
+      if (!kBwd)
+        h.aux_off = reinterpret_cast<int64_t>(static_cast<const T*>(p.x) + h.a * g.HW);
+      else if ((reinterpret_cast<uintptr_t>(p.mean) & 15) == 0)
+        h.aux_off = reinterpret_cast<int64_t>(p.mean + (t.unit & ~int64_t(3)));
+    }
+  };
+  auto chunk_off = [&](const SlotHdr& h, int c, int32_t* bytes) {
+    const int64_t e0 = h.c + (int64_t)c * g.chunk;
+    *bytes = (int32_t)(((h.d - e0 < g.chunk) ? h.d - e0 : g.chunk) * (int64_t)sizeof(T));
+    return h.a * g.HW + e0;
+  };
+  // finalisation of unit u by the CTA whose arrival completed it
+  auto fin = [&](int64_t u) {
+    const int64_t n = u / g.G, c0 = (u % g.G) * g.Cg;
+    if (kBwd)
+      finalize_bwd(p, n, c0, c0 + g.Cg, sm, sm_floats);
+    else
+      finalize_fwd<T>(p, n, c0, c0 + g.Cg, sm, sm_floats);
+    __threadfence();
+    __syncthreads();
+    __shared__ int s_last;
+    if (tid == 0) {
+      atomicExch(p.tickets + u, 0u);
+      if (kBwd) {
+        const float2 cf = p.coef[u];
+        put_record(rec + u, cf.x, cf.y);
+        s_last = publish_and_arrive(p.tickets + g.units_fin, (unsigned)g.units_fin);
+      } else {
+        put_record(rec + u, p.mean[u], p.rstd[u]);
+      }
+    }
+    if (!kBwd) return;
+    __syncthreads();
+    if (!s_last) return;
+    finalize_params(p, sm);  // the last unit: dgamma, dbeta
+    if (tid == 0) atomicExch(p.tickets + g.units_fin, 0u);
+  };
+  auto consume = [&](const SlotHdr& h, const char* sx, const char* sd) {
+    const int c = h.chunk, nc = h.nchunks, bytes = h.bytes;
+    if (c == 0) settle(p, pd, h.step, fin);
+    const int64_t ch = h.e, ng = h.unit;
+    const int nv = bytes / 16;
+    const uint4* vx = reinterpret_cast<const uint4*>(sx);
+    const uint4* vd = reinterpret_cast<const uint4*>(sd);
+    if (h.pass == 1) {
+      if (c == 0) {
+        s1 = s2 = 0.f;
+        if (!kBwd)
+          K = Elem<T>::to_f(reinterpret_cast<const T*>(&h.aux)[0]);
+        else
+          K = h.aux_off ? reinterpret_cast<const float*>(&h.aux)[ng & 3] : __ldg(p.mean + ng);
+      }
+#pragma unroll 4
+      for (int v = tid; v < nv; v += nt) {
+        float xv[VW];
+        Access<T, VW>::unpack(vx[v], xv);
+        if (kBwd) {
+          float dv[VW];
+          Access<T, VW>::unpack(vd[v], dv);
+          acc_grad<VW>(xv, dv, K, s1, s2);
+        } else {
+          acc_shifted<VW>(xv, K, s1, s2);
+        }
+      }
+      if (c == nc - 1) {
+        const float2 tot = block_sum2_t0(s1, s2, sm);
+        if (tid == 0) {
+          p.part[h.a * g.T + h.b] = tot;
+          arrive_async(p, pd, ng, h.step);
+        }
+      }
       return;
     }
-    if (wait_ready(p.ready + t.unit, p.err)) {
-      if (kBwd)
-        dx_chunk<T, VW>(p, item);
-      else
-        apply_chunk<T, VW>(p, item);
+    if (c == 0) {
+      float lo, hi;
+      if (kBwd) {  // inputs: loaded before the wait, so the two latencies overlap
+        const float r = __ldg(p.rstd + ng);
+        ca = p.gamma ? r * __ldg(p.gamma + ch) : r;
+        cmu = __ldg(p.mean + ng);
+      } else {
+        ca = p.gamma ? __ldg(p.gamma + ch) : 1.f;
+        cb = p.beta ? __ldg(p.beta + ch) : 0.f;
+      }
+      ok = wait_record(rec + ng, p.err, &lo, &hi);
+      if (kBwd) {
+        cb = lo;
+        cc = hi;
+      } else {
+        cmu = lo;
+        ca *= hi;  // rstd * gamma
+      }
     }
-    finish_pass2(p, t.unit);
-  });
+    if (ok) {
+      T* out = static_cast<T*>(p.out) + h.a * g.HW + h.c + (int64_t)c * g.chunk;
+#pragma unroll 4
+      for (int v = tid; v < nv; v += nt) {
+        float xv[VW];
+        Access<T, VW>::unpack(vx[v], xv);
+        if (kBwd) {
+          float dv[VW];
+          Access<T, VW>::unpack(vd[v], dv);
+#pragma unroll
+          for (int e = 0; e < VW; ++e) xv[e] = fmaf(ca, dv[e], fmaf(cb, xv[e] - cmu, cc));
+        } else {
+#pragma unroll
+          for (int e = 0; e < VW; ++e) xv[e] = fmaf(xv[e] - cmu, ca, cb);
+        }
+        Access<T, VW>::store(out + (int64_t)v * VW, xv, pfirst);
+      }
+    }
+  };
+  run_ring<kBwd>(p, R, describe, chunk_off, consume);
 }
 
 template <typename T, int VW>
@@ -443,7 +567,7 @@ const void* kernel_vw(const Geom& g, bool bwd, int second, size_t* smem) {
 
 template <typename T>
 const void* pipelined_t(const Geom& g, bool bwd, size_t* smem) {
-  *smem = sizeof(float) * nchw_smem_floats(g);
+  *smem = g.smem;
   constexpr int V = Elem<T>::VEC;
   return bwd ? (const void*)nchw_pipelined<T, V, true> : (const void*)nchw_pipelined<T, V, false>;
 }
@@ -465,6 +589,10 @@ cudaError_t launch_nchw(const KParams& p, cudaStream_t s, bool bwd) {
     default: return dispatch_vw<__nv_bfloat16>(p, s, bwd);
   }
 }
+
+// Reduction scratch of the pipelined kernel (floats): the CTA sums and the
+// per-channel staging of the finalisation.
+int64_t nchw_pipelined_scratch_floats(const Geom& g) { return nchw_smem_floats(g); }
 
 // The pipelined kernel of a plan (16-byte vectors only).
 const void* nchw_pipelined_kernel(const Geom& g, bool bwd, size_t* smem) {

@@ -18,7 +18,7 @@
 //           nhwc_bwd_dx     -> dx = rstd*gamma*dy + B*(x - mean) + D
 // The second kernel of each op walks items and rows in the reverse order of
 // the first, so it starts on the data the first kernel left in L2.
-#include "gn_tasks.cuh"
+#include "gn_finalize.cuh"
 
 namespace gn {
 namespace {
@@ -333,33 +333,6 @@ __global__ void __launch_bounds__(512, 2) nhwc_bwd_dx(const __grid_constant__ KP
   dx_item<T, VW, NG>(p, p.g.items - 1 - (int64_t)blockIdx.x);
 }
 
-// The pipelined regime: one persistent kernel over the tasks of gn_tasks.cuh.
-// A unit is a sample, a piece is one row block (item u*T + q; one column
-// block per row).
-template <typename T, int VW, int NG, bool kBwd>
-__global__ void __launch_bounds__(512, 2) nhwc_pipelined(const __grid_constant__ KParams p) {
-  extern __shared__ float red[];
-  grid_dependency_wait();
-  const Geom& g = p.g;
-  run_tasks(p, [&](const Task& t) {
-    const int64_t item = t.unit * g.T + t.piece;
-    if (t.pass == 1) {
-      if (kBwd)
-        reduce_item<T, VW, NG>(p, item, red);
-      else
-        stats_item<T, VW>(p, item, red);
-      return;
-    }
-    if (wait_ready(p.ready + t.unit, p.err)) {
-      if (kBwd)
-        dx_item<T, VW, NG>(p, item);
-      else
-        apply_item<T, VW, NG>(p, item);
-    }
-    finish_pass2(p, t.unit);
-  });
-}
-
 template <typename T, int VW, int NG>
 cudaError_t run_op(const KParams& p, cudaStream_t s, bool bwd) {
   const Geom& g = p.g;
@@ -399,35 +372,7 @@ const void* kernel_vw(const Geom& g, bool bwd, int second, size_t* smem) {
                                  : kernel_t<T, V, V>(g, bwd, second, smem);
 }
 
-template <typename T, int NG>
-const void* pipelined_t(const Geom& g, bool bwd, size_t* smem) {
-  constexpr int V = Elem<T>::VEC;
-  *smem = sizeof(float) * 2 * V * g.tpb;
-  return bwd ? (const void*)nhwc_pipelined<T, V, NG, true> : (const void*)nhwc_pipelined<T, V, NG, false>;
-}
-
-template <typename T>
-const void* pipelined_vw(const Geom& g, bool bwd, size_t* smem) {
-  return one_group_per_vector(g) ? pipelined_t<T, 1>(g, bwd, smem)
-                                 : pipelined_t<T, Elem<T>::VEC>(g, bwd, smem);
-}
-
 }  // namespace
-
-// The pipelined kernel of a plan (16-byte vectors only).
-const void* nhwc_pipelined_kernel(const Geom& g, bool bwd, size_t* smem) {
-  switch (g.dtype) {
-    case kF32: return pipelined_vw<float>(g, bwd, smem);
-    case kF16: return pipelined_vw<__half>(g, bwd, smem);
-    default: return pipelined_vw<__nv_bfloat16>(g, bwd, smem);
-  }
-}
-
-cudaError_t launch_nhwc_pipelined(const KParams& p, cudaStream_t s, bool bwd) {
-  size_t smem = 0;
-  const void* k = nhwc_pipelined_kernel(p.g, bwd, &smem);
-  return launch_cooperative(k, p, smem, s);
-}
 
 const void* nhwc_kernel(const Geom& g, bool bwd, int second, size_t* smem) {
   switch (g.dtype) {

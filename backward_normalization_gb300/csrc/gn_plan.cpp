@@ -4,6 +4,7 @@
 // whether every data pointer is 16-byte aligned, and on the device's SM count,
 // so the same call on the same device always runs the same reduction tree and
 // gives bit-identical results.
+#include <algorithm>
 #include <atomic>
 #include <map>
 #include <mutex>
@@ -213,41 +214,47 @@ bool plan_resident(Geom& g, int op) {
 }  // namespace
 
 namespace {
-// Pipelined regime.  A piece holds about kPipePieceBytes of input (x, or x
-// and dy), in whole unrolled load rounds; pass-2 tasks trail pass-1 tasks by
-// enough units that about kPipeLagCtas tasks lie between the two passes of a
-// unit, while the lagging units' input (what pass 2 finds in L2) stays within
-// kPipeL2Bytes.
-#ifndef GN_PIPE_PIECE_BYTES
-#define GN_PIPE_PIECE_BYTES (128 * 1024)
+// Pipelined regime (NCHW): every CTA takes one piece of every unit, in
+// lockstep, so the input read between a unit's two passes is only the lag's
+// D units; its chunks of at most kPipeChunkBytes per tensor stream through a
+// ring of at least kPipeMinSlots slots in the CTA's share of shared memory.
+#ifndef GN_PIPE_CHUNK_BYTES
+#define GN_PIPE_CHUNK_BYTES (16 * 1024)
 #endif
-#ifndef GN_PIPE_TASKS_PER_CTA
-#define GN_PIPE_TASKS_PER_CTA 2
-#endif
-#ifndef GN_PIPE_LAG_CTAS
-#define GN_PIPE_LAG_CTAS 2
+#ifndef GN_PIPE_LAG
+#define GN_PIPE_LAG 2
 #endif
 #ifndef GN_PIPE_L2_BYTES
 #define GN_PIPE_L2_BYTES (64ll << 20)
 #endif
-constexpr int64_t kPipePieceBytes = GN_PIPE_PIECE_BYTES;
-constexpr int64_t kPipeLagCtas = GN_PIPE_LAG_CTAS;
-constexpr int64_t kPipeTasksPerCta = GN_PIPE_TASKS_PER_CTA;
-constexpr int64_t kPipeL2Bytes = GN_PIPE_L2_BYTES;
+#ifndef GN_PIPE_MAX_SLOTS
+#define GN_PIPE_MAX_SLOTS 16
+#endif
+#ifndef GN_PIPE_CTAS_PER_SM
+#define GN_PIPE_CTAS_PER_SM 2
+#endif
+constexpr int64_t kPipeChunkBytes = GN_PIPE_CHUNK_BYTES;
+constexpr int64_t kPipeLag = GN_PIPE_LAG;         // D: pass 2 of unit u runs in step u + D
+constexpr int64_t kPipeL2Bytes = GN_PIPE_L2_BYTES;  // the D + 1 units in flight must fit
+constexpr int kPipeMaxSlots = GN_PIPE_MAX_SLOTS;
+constexpr int kPipeCtasPerSm = GN_PIPE_CTAS_PER_SM;
+constexpr int kPipeMinSlots = 4;
+constexpr size_t kSmemPerSm = 228 * 1024;
 
 // CTAs of the pipelined kernel that fit on the device at once, or an estimate
-// (two 512-thread CTAs per SM) when no device is visible; 0 if none fit.
+// (kPipeCtasPerSm per SM) when no device is visible; 0 if none fit.
 int64_t pipelined_ctas(const Geom& g, int op, int sm_count) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) {
     cudaGetLastError();
-    return (int64_t)sm_count * (g.tpb > 256 ? 2 : 4);
+    return (int64_t)sm_count * kPipeCtasPerSm;
   }
   size_t smem = 0;
-  const void* fn = g.layout == kNHWC ? nhwc_pipelined_kernel(g, op == kBwd, &smem)
-                                     : nchw_pipelined_kernel(g, op == kBwd, &smem);
+  const void* fn = nchw_pipelined_kernel(g, op == kBwd, &smem);
   int nb = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fn, g.tpb, smem) != cudaSuccess) {
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+          cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fn, g.tpb, smem) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
@@ -260,65 +267,53 @@ bool plan_pipelined(Geom& g, int op, int sm_count) {
   const int esz = g.dtype == kF32 ? 4 : 2;
   const int vec = 16 / esz;
   const int nten = op == kBwd ? 2 : 1;
-  if (g.vw != vec) return false;
+  if (g.layout != kNCHW || g.mode != 0 || g.vw != vec) return false;
+  const int64_t unit_bytes = g.Cg * g.HW * esz * nten;
+  if ((kPipeLag + 1) * unit_bytes > kPipeL2Bytes) return false;
   Geom r = g;
-  // The persistent grid: sized before the pieces (the kernel does not depend
-  // on them).
   r.regime = kRegimePipelined;
+  r.tpb = 512 / kPipeCtasPerSm / 32 * 32;
+  const size_t smem_cap = std::min(kSmemPerCta, kSmemPerSm / kPipeCtasPerSm - 2048);
+  // ---- the ring
+  const int64_t scratch = nchw_pipelined_scratch_floats(r);
+  r.off_red = 0;
+  const size_t fixed = a128((size_t)scratch * 4);
+  const size_t overhead = kSlotHdrBytes + sizeof(uint64_t) + 128;  // header, mbarrier, padding
+  if (smem_cap < fixed + 512 + kPipeMinSlots * overhead) return false;
+  const int64_t fit = (int64_t)((smem_cap - fixed - 512) / kPipeMinSlots - overhead) / nten;
+  const int64_t cbytes = std::min<int64_t>(kPipeChunkBytes, fit);
+  r.chunk = cbytes / 128 * 128 / esz;  // elements (a multiple of the vector width)
+  if (r.chunk < (int64_t)r.tpb * vec) return false;
+  r.chunk_bytes = r.chunk * esz;
+  r.ten_stride = (int64_t)a128((size_t)r.chunk_bytes);
+  r.dy_in_ring = nten == 2 ? 1 : 0;
+  const size_t slot = (size_t)r.ten_stride * nten;
+  const size_t per_slot = slot + kSlotHdrBytes + sizeof(uint64_t);  // data, header, mbarrier
+  r.S = (int)std::min<int64_t>(kPipeMaxSlots, (int64_t)((smem_cap - fixed - 512) / per_slot));
+  r.off_tot = fixed;                                          // slot headers
+  r.off_bar = r.off_tot + a128(kSlotHdrBytes * (size_t)r.S);  // mbarriers
+  r.off_ring = r.off_bar + a128(8 * (size_t)r.S);
+  r.smem = r.off_ring + (size_t)r.S * slot + 128;  // slack for aligning the dynamic smem base
+  if (r.smem > smem_cap) return false;
   r.grid = pipelined_ctas(r, op, sm_count);
-  if (r.grid <= 0) return false;
-  // Piece size: about kPipeTasksPerCta pass-1 tasks per CTA, at most
-  // kPipePieceBytes of input each.
-  const int64_t in_bytes = g.N * g.C * g.HW * esz * nten;
-  const int64_t piece_bytes =
-      clamp64(cdiv(in_bytes, kPipeTasksPerCta * r.grid), 1, kPipePieceBytes);
-  int64_t unit_bytes;
-  if (g.layout == kNHWC) {
-    if (g.ncb != 1) return false;
-    unit_bytes = g.HW * g.C * esz * nten;
-    // rows per piece: whole steps of the rpi row lanes
-    const int64_t row_bytes = g.C * esz * nten;
-    const int64_t rb = rup(clamp64(piece_bytes / row_bytes, 1, g.HW), g.rpi);
-    r.rb = rb;
-    r.T = cdiv(g.HW, rb);
-    r.units_fin = g.N;
-    r.unit_groups = 0;
-    r.pieces = r.T;
-    r.l1 = r.T >= 2 * kGroup1 ? kGroup1 : 1;
-    r.Tp = cdiv(r.T, r.l1);
-    r.groups1 = r.l1 > 1 ? g.N * r.Tp : 0;
-    r.cstride = 1;
-    r.tstride = g.C;
-    r.arrivals_per_n = r.Tp;
-    r.items_per_n = r.T;
-  } else {
-    if (g.mode != 0) return false;
-    unit_bytes = g.Cg * g.HW * esz * nten;
-    // chunk: whole steps of tpb threads x one vector
-    const int64_t step = (int64_t)g.tpb * vec;
-    int64_t L = rup(clamp64(piece_bytes / (esz * nten), 1, g.HW), step);
-    if (L > rup(g.HW, vec)) L = rup(g.HW, vec);
-    r.L = L;
-    r.T = cdiv(g.HW, L);
-    r.units_fin = g.N * g.G;
-    r.unit_groups = 1;
-    r.pieces = g.Cg * r.T;
-    r.l1 = r.T >= 2 * kGroup1 ? kGroup1 : 1;
-    r.Tp = cdiv(r.T, r.l1);
-    r.groups1 = r.l1 > 1 ? g.N * g.C * r.Tp : 0;
-    r.cstride = r.Tp;
-    r.tstride = 1;
-    r.arrivals_per_n = g.Cg * r.Tp;
-    r.items_per_n = g.C * r.T;
-  }
-  if (2 * unit_bytes > kPipeL2Bytes) return false;
+  if (r.grid < g.Cg) return false;
+  // ---- the pieces: segments of each plane, one per CTA
+  const int64_t m = r.grid / g.Cg;
+  r.L = rup(cdiv(g.HW, m), vec);
+  r.T = cdiv(g.HW, r.L);
+  r.units_fin = g.N * g.G;
+  r.unit_groups = 1;
+  r.pieces = g.Cg * r.T;
+  r.l1 = 1;  // the finaliser merges the Cg*T records of its unit directly
+  r.Tp = r.T;
+  r.groups1 = 0;
+  r.cstride = r.T;
+  r.tstride = 1;
+  r.arrivals_per_n = g.Cg * r.T;
+  r.items_per_n = g.C * r.T;
   r.items = g.N * r.items_per_n;
-  r.keep_from = 0;  // pass 1 keeps everything it reads in L2 for pass 2
-  const int64_t U = r.units_fin;
-  if (2 * U * r.pieces > 0x7fffffffLL) return false;  // task indices are 32-bit
-  int64_t lag = cdiv(kPipeLagCtas * r.grid, 2 * r.pieces);
-  lag = clamp64(lag, 1, kPipeL2Bytes / unit_bytes);
-  r.lag = clamp64(lag, 1, U);
+  r.keep_from = 0;
+  r.lag = std::min<int64_t>(kPipeLag, r.units_fin);
   g = r;
   return true;
 }
@@ -465,11 +460,12 @@ Geom plan_geom(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout, 
   } else if (ov == kRegimePipelined) {
     plan_pipelined(g, op, sm_count);
   } else if (ov == kRegimeAuto && resident_preferred(g, op)) {
-    // measured on GB300: the pipelined kernel is not yet faster than these
-    // families on any workload here, so it runs only when asked for
+    // measured on GB300: the pipelined kernel moves the minimal traffic but is
+    // slower than these families on every workload here (its steps are
+    // latency-bound), so it runs only when asked for
     plan_resident(g, op);
   }
-  const int64_t pipe = g.regime == kRegimePipelined ? 2 * g.units_fin + 2 : 0;
+  const int64_t pipe = g.regime == kRegimePipelined ? 2 * g.units_fin + 3 : 0;
   g.counters = g.regime == kRegimeResident ? 0 : g.units_fin + 1 + g.groups1 + pipe;
   return g;
 }

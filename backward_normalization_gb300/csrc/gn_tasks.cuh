@@ -1,22 +1,27 @@
-// gn_tasks.cuh -- the task queue of the pipelined regime.
+// gn_tasks.cuh -- the pipelined regime: a lockstep schedule of the reduction
+// units, fed by a ring of bulk copies.
 //
-// One persistent, cooperatively launched kernel (all CTAs co-resident) runs
-// two kinds of task per unit (a sample, or one (sample, group)):
-//   pass 1, piece q: stream the piece, write its partial record to a fixed
-//           slot, arrive on the unit's counter; the last arrival finalises
-//           the unit and raises its ready flag;
-//   pass 2, piece q: wait for the unit's ready flag, then the elementwise
-//           output of the piece, reading its input again (from L2).
-// Tasks are handed out in one global order in which every pass-1 task of a
-// unit precedes all pass-2 tasks of that unit, and the pass-2 tasks of unit u
-// follow the pass-1 tasks of unit u + lag.  A CTA waiting on a flag holds at
-// most one later task (its prefetched next index); following the waits from
-// any waiting CTA leads to strictly earlier pass-2 tasks, so the earliest
-// waiting task's unit only needs tasks that are running or done, and every
-// wait ends.  Each wait is also bounded: after kReadyWaitLimit polls the CTA
-// raises bit 1 of the workspace error word and skips that piece's output.
-// Results do not depend on which CTA runs which task: records have fixed
-// slots and every sum has a fixed order.
+// One persistent kernel, cooperatively launched so that all its CTAs are
+// co-resident.  A unit (one (sample, group)) is cut into P pieces; piece i of
+// every unit belongs to CTA i.  Every CTA runs the same steps s = 0, 1, ...,
+// U + D - 1:
+//   pass 1 of unit s (s < U):     stream the piece, add it up, write its record
+//                                 and arrive on the unit's counter -- without
+//                                 waiting for the counter's old value;
+//   pass 2 of unit s - D (s >= D): wait for that unit's ready record, stream
+//                                 the piece again (it is still in L2: only D
+//                                 units were read since) and write the output.
+// The first task of each step settles the arrivals of earlier steps: the CTA
+// whose arrival completed a unit finalises it (statistics, then the unit's
+// ready record).  So an arrival is settled one step after it was made, its
+// latency hidden behind a step of streaming, and always before the CTA waits
+// on any unit.  Deadlock-free: take the smallest unit w that some CTA waits
+// for; w's last arriver has either settled w (its step w + 1 came before any
+// wait on a unit >= w + 1 - D, and by minimality it waits on nothing smaller)
+// or is still running; either way w gets finalised.  Every wait is also
+// bounded: after kReadyWaitLimit polls the CTA raises bit 1 of the workspace
+// error word and skips that piece's output.  Results do not depend on timing:
+// records have fixed slots and every sum has a fixed order.
 #pragma once
 
 #include "gn_finalize.cuh"
@@ -27,45 +32,38 @@ constexpr uint32_t kReadyWaitLimit = 1u << 22;  // polls, about 100 ns apart
 
 struct Task {
   int pass;
-  int64_t unit, piece;
+  int64_t unit, piece, step;
 };
 
-// Queue index k -> task, for U units of P pieces and a lag of D units:
-//   P1(0) .. P1(D-1) | P1(D) P2(0) | P1(D+1) P2(1) | ... | P2(U-D) .. P2(U-1)
-// where P1(u) / P2(u) stand for the P pass-1 / pass-2 tasks of unit u.
-__device__ __forceinline__ Task decode_task(int64_t k, int64_t U, int64_t P, int64_t D) {
-  Task t;
-  const int64_t a = D * P, b = (U - D) * 2 * P;
-  if (k < a) {
-    t.pass = 1;
-    t.unit = k / P;
-    t.piece = k % P;
-  } else if (k < a + b) {
-    const int64_t j = k - a, s = D + j / (2 * P), r = j % (2 * P);
-    t.pass = r < P ? 1 : 2;
-    t.unit = r < P ? s : s - D;
-    t.piece = r < P ? r : r - P;
-  } else {
-    const int64_t j = k - a - b;
-    t.pass = 2;
-    t.unit = U - D + j / P;
-    t.piece = j % P;
-  }
-  return t;
+// A unit's ready record: two floats (the forward's mean and rstd, or the
+// backward's coefficients B and D) in one 64-bit word, each XORed with
+// kRecKey, so that the zero-filled workspace reads "not ready" and a written
+// record never does (kRecKey is a NaN bit pattern that no arithmetic
+// produces).  Written once with release semantics, read with acquire.
+constexpr uint32_t kRecKey = 0x7fbadbadu;
+
+__device__ __forceinline__ void put_record(unsigned long long* rec, float lo, float hi) {
+  const unsigned long long v =
+      ((unsigned long long)(__float_as_uint(hi) ^ kRecKey) << 32) | (__float_as_uint(lo) ^ kRecKey);
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(rec), "l"(v) : "memory");
 }
 
-// Thread 0 polls the flag with acquire semantics, at most kReadyWaitLimit
-// times; every thread then learns whether it was seen.  On timeout bit 1 of
-// the error word is raised.
-__device__ __forceinline__ bool wait_ready(const unsigned* flag, unsigned* err) {
+// Thread 0 polls the record with acquire loads, at most kReadyWaitLimit
+// times; the whole CTA then learns whether it was seen and its two floats.
+// On timeout bit 1 of the error word is raised.
+__device__ __forceinline__ bool wait_record(const unsigned long long* rec, unsigned* err,
+                                            float* lo, float* hi) {
   __shared__ int s_ok;
+  __shared__ float s_v[2];
   if (threadIdx.x == 0) {
     int ok = 0;
     for (uint32_t i = 0; i < kReadyWaitLimit; ++i) {
-      unsigned v;
-      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+      unsigned long long v;
+      asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(rec) : "memory");
       if (v) {
         ok = 1;
+        s_v[0] = __uint_as_float((unsigned)v ^ kRecKey);
+        s_v[1] = __uint_as_float((unsigned)(v >> 32) ^ kRecKey);
         break;
       }
       __nanosleep(64);
@@ -74,46 +72,245 @@ __device__ __forceinline__ bool wait_ready(const unsigned* flag, unsigned* err) 
     s_ok = ok;
   }
   __syncthreads();
-  __threadfence();
+  *lo = s_v[0];
+  *hi = s_v[1];
   return s_ok != 0;
 }
 
-// Runs f(task) on the tasks this CTA takes from the queue; the next index is
-// fetched while the current task runs.  The last CTA to leave resets the
-// queue, so every call starts from task 0.
-template <typename F>
-__device__ __forceinline__ void run_tasks(const KParams& p, F f) {
-  const Geom& g = p.g;
-  const int64_t total = 2 * g.units_fin * g.pieces;
-  __shared__ unsigned s_k[2];
-  unsigned* q = p.queue;
-  if (threadIdx.x == 0) s_k[0] = atomicAdd(q, 1u);
-  __syncthreads();
-  int b = 0;
-  unsigned k = s_k[0];
-  while ((int64_t)k < total) {
-    if (threadIdx.x == 0) s_k[b ^ 1] = atomicAdd(q, 1u);
-    f(decode_task((int64_t)k, g.units_fin, g.pieces, g.lag));
-    __syncthreads();
-    b ^= 1;
-    k = s_k[b];
-  }
-  if (threadIdx.x == 0) {
-    __threadfence();
-    if (atomicAdd(q + 1, 1u) == gridDim.x - 1) {
-      atomicExch(q, 0u);
-      atomicExch(q + 1, 0u);
-    }
-  }
+// Arrivals not yet settled (thread 0's registers): at most two, from the
+// current step and the one before.
+struct Pending {
+  int64_t unit[2], step[2];
+  unsigned old[2];
+};
+
+// Thread 0 arrives on unit u's counter in step `step` and keeps the old value
+// for later (the atomic's latency is not waited for here).  The record
+// stores before it are ordered by the fence.
+__device__ __forceinline__ void arrive_async(const KParams& p, Pending& pd, int64_t u,
+                                             int64_t step) {
+  __threadfence();
+  const int sl = (int)(step & 1);
+  pd.unit[sl] = u;
+  pd.step[sl] = step;
+  pd.old[sl] = atomicAdd(p.tickets + u, 1u);
 }
 
-// After a pass-2 task of unit u: the unit's last pass-2 task clears the
-// unit's ready flag and counter, so the workspace leaves the call as it came.
-__device__ __forceinline__ void finish_pass2(const KParams& p, int64_t u) {
+// Settles the arrivals made before step `step`: the units they completed are
+// finalised by the whole CTA with fin(u).  Called by every thread at the
+// first chunk of a task.
+template <typename Fin>
+__device__ __forceinline__ void settle(const KParams& p, Pending& pd, int64_t step, Fin fin) {
+  __shared__ long long s_fin[2];
+  if (threadIdx.x == 0) {
+    for (int sl = 0; sl < 2; ++sl) {
+      s_fin[sl] = -1;
+      if (pd.unit[sl] >= 0 && pd.step[sl] < step) {
+        if (pd.old[sl] == (unsigned)p.g.arrivals_per_n - 1) s_fin[sl] = pd.unit[sl];
+        pd.unit[sl] = -1;
+      }
+    }
+  }
   __syncthreads();
-  if (threadIdx.x == 0 && atomicAdd(p.p2cnt + u, 1u) == (unsigned)p.g.pieces - 1) {
-    atomicExch(p.ready + u, 0u);
-    atomicExch(p.p2cnt + u, 0u);
+  const long long f0 = s_fin[0], f1 = s_fin[1];
+  __syncthreads();
+  if (f0 >= 0) fin(f0);
+  if (f1 >= 0) fin(f1);
+}
+
+// ------------------------------------------------------------ the ring
+// Thread 0 streams the chunks of the CTA's tasks, in step order, into a ring
+// of S shared-memory slots with 1-D bulk copies (TMA), each slot completing on
+// its own mbarrier; S - 1 chunks stay in flight while the whole CTA consumes
+// the current one.  A slot holds one chunk of x (and, in the backward, the
+// matching chunk of dy at offset ten_stride) and a header naming its task and
+// chunk; a header with k = kStopTask ends the loop.
+
+constexpr int64_t kStopTask = -1;
+
+// A slot's header: the task and chunk it holds, decoded once by thread 0 so
+// that consumers do no index arithmetic of their own.  a..e describe the
+// piece in the layout's terms (set by the kernel's describe function).
+struct SlotHdr {
+  int64_t k;     // task sequence number in this CTA, or kStopTask
+  int64_t unit;  // reduction unit
+  int64_t step;  // the step the task belongs to
+  int64_t a, b, c, d, e;
+  int32_t pass, chunk, nchunks, bytes;  // bytes: of each tensor's chunk
+  int64_t aux_off;                      // byte address of the 16-byte aux copy, or 0
+  int64_t pad_;
+  uint4 aux;  // 16 bytes copied with the first chunk of a task (see run_ring)
+};
+
+static_assert(sizeof(SlotHdr) <= kSlotHdrBytes, "slot header larger than the plan reserves");
+
+struct RingSmem {
+  char* ring;       // S slots, slot s at ring + s * slot_stride
+  SlotHdr* hdr;     // S headers
+  uint64_t* full;   // S mbarriers
+  int S;
+  int64_t slot_stride, ten_stride;
+};
+
+__device__ __forceinline__ RingSmem ring_smem(const Geom& g, char* smem) {
+  RingSmem r;
+  r.ring = smem + g.off_ring;
+  r.hdr = reinterpret_cast<SlotHdr*>(smem + g.off_tot);  // kSlotHdrBytes apart
+  r.full = reinterpret_cast<uint64_t*>(smem + g.off_bar);
+  r.S = g.S;
+  r.ten_stride = g.ten_stride;
+  r.slot_stride = g.ten_stride * (g.dy_in_ring ? 2 : 1);
+  return r;
+}
+
+__device__ __forceinline__ SlotHdr* hdr_at(const RingSmem& R, int s) {
+  return reinterpret_cast<SlotHdr*>(reinterpret_cast<char*>(R.hdr) + s * kSlotHdrBytes);
+}
+
+// Runs the CTA's tasks through the ring.  Thread 0 only:
+// `describe(task, hdr)` fills hdr.a..e, hdr.nchunks and hdr.aux_off (the
+// 16-byte aligned global address of 16 bytes the task's first chunk brings
+// along into hdr.aux, or 0 for none) for a task, and
+// `chunk_off(hdr, c, &bytes)` gives the element offset in x (and dy) of chunk
+// c and its bytes.  `consume(hdr, slot_x, slot_dy)` is called by every thread
+// of the CTA for each chunk in order and may use __syncthreads.  Every wait is
+// bounded: a copy that does not land in time raises bit 0 of the error word,
+// the CTA stops consuming, waits (bounded) for the copies it issued and
+// leaves.  The last CTA to leave clears the ready records and its counter.
+template <bool kDy, typename Describe, typename ChunkOff, typename Consume>
+__device__ __forceinline__ void run_ring(const KParams& p, const RingSmem& R, Describe describe,
+                                         ChunkOff chunk_off, Consume consume) {
+  const Geom& g = p.g;
+  const int64_t U = g.units_fin, D = g.lag, piece = blockIdx.x;
+  const char* xb = static_cast<const char*>(p.x);
+  const char* db = static_cast<const char*>(p.dy);
+  const int esz = g.dtype == kF32 ? 4 : 2;
+  __shared__ int s_ok;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < R.S; ++i) mbar_init(R.full + i, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  // thread 0's issue state: the step and half-step (pass) of the next task
+  int64_t st = 0, seq = 0;
+  int half = 0;
+  SlotHdr cur{};
+  bool idone = piece >= g.pieces;  // CTAs beyond the pieces have no tasks
+  int issued = 0;                  // slots issued and not yet consumed
+  cur.nchunks = 0;
+  cur.chunk = 0;
+  const uint64_t pol1 = policy_evict_last(), pol2 = policy_evict_first();
+  auto next_task = [&](Task& t) {
+    while (st < U + D) {
+      if (half == 0) {
+        half = 1;
+        if (st < U) {
+          t.pass = 1;
+          t.unit = st;
+          t.piece = piece;
+          t.step = st;
+          return true;
+        }
+      } else {
+        half = 0;
+        const int64_t u = st - D, s0 = st++;
+        if (u >= 0) {
+          t.pass = 2;
+          t.unit = u;
+          t.piece = piece;
+          t.step = s0;
+          return true;
+        }
+      }
+    }
+    return false;
+  };
+  auto stop = [&](int s) {  // the stop marker: completes the phase, no bytes expected
+    hdr_at(R, s)->k = kStopTask;
+    mbar_arrive(R.full + s);
+    idone = true;
+    ++issued;
+  };
+  auto issue = [&](int s) {
+    if (idone) return;
+    if (cur.chunk == cur.nchunks) {
+      Task t;
+      if (!next_task(t)) {
+        stop(s);
+        return;
+      }
+      cur.k = seq++;
+      cur.pass = t.pass;
+      cur.unit = t.unit;
+      cur.step = t.step;
+      describe(t, cur);
+      cur.chunk = 0;
+    }
+    int32_t bytes = 0;
+    const int64_t off = chunk_off(cur, cur.chunk, &bytes);
+    cur.bytes = bytes;
+    SlotHdr* hd = hdr_at(R, s);
+    *hd = cur;
+    const bool aux = cur.chunk == 0 && cur.aux_off != 0;
+    if (aux) fence_proxy_async_smem();  // the header store before the copy into hd->aux
+    const uint64_t pol = cur.pass == 1 ? pol1 : pol2;  // pass 1 keeps its input in L2 for pass 2
+    char* slot = R.ring + s * R.slot_stride;
+    mbar_arrive_expect_tx(R.full + s, (uint32_t)bytes * (kDy ? 2u : 1u) + (aux ? 16u : 0u));
+    if (aux)
+      tma_load_1d(&hd->aux, reinterpret_cast<const void*>(cur.aux_off), 16u, R.full + s, pol1);
+    tma_load_1d(slot, xb + off * esz, (uint32_t)bytes, R.full + s, pol);
+    if (kDy) tma_load_1d(slot + R.ten_stride, db + off * esz, (uint32_t)bytes, R.full + s, pol);
+    ++cur.chunk;
+    ++issued;
+  };
+  if (threadIdx.x == 0) {
+    if (idone)
+      stop(0);
+    else
+      for (int i = 0; i < R.S && !idone; ++i) issue(i);
+  }
+  int s = 0;
+  uint32_t ph = 0;
+  while (true) {
+    if (threadIdx.x == 0) s_ok = mbar_wait(R.full + s, ph, p.err) ? 1 : 0;
+    __syncthreads();
+    if (!s_ok) break;  // the same decision in every thread
+    mbar_wait(R.full + s, ph, p.err);  // completed: returns at once (acquire for this thread)
+    const SlotHdr& h = *hdr_at(R, s);
+    if (h.k == kStopTask) {
+      if (threadIdx.x == 0) --issued;
+      break;
+    }
+    const char* slot = R.ring + s * R.slot_stride;
+    consume(h, slot, slot + R.ten_stride);
+    __syncthreads();  // every thread is done with slot s
+    if (threadIdx.x == 0) {
+      --issued;
+      fence_proxy_async_smem();  // the slot's reads before the next copy into it
+      issue(s);
+    }
+    if (++s == R.S) {
+      s = 0;
+      ph ^= 1u;
+    }
+  }
+  unsigned* q = p.queue;
+  if (threadIdx.x == 0) {
+    // after an abort: wait (bounded) for the copies still in flight
+    for (int i = 0; i < issued; ++i) {
+      const int si = (s + i) % R.S;
+      const uint32_t pi = ph ^ (uint32_t)(((s + i) / R.S) & 1);
+      mbar_wait(R.full + si, pi, p.err);
+    }
+    __threadfence();
+    s_ok = atomicAdd(q, 1u) == gridDim.x - 1 ? 1 : 0;
+  }
+  __syncthreads();
+  if (s_ok) {
+    // every CTA has left its steps: no record is read any more in this call
+    unsigned long long* rec = reinterpret_cast<unsigned long long*>(p.ready);
+    for (int64_t u = threadIdx.x; u < U; u += blockDim.x) rec[u] = 0ull;
+    if (threadIdx.x == 0) atomicExch(q, 0u);
   }
 }
 
@@ -121,6 +318,11 @@ __device__ __forceinline__ void finish_pass2(const KParams& p, int64_t u) {
 // CTAs of g.tpb threads, between the timing events when they are set.
 inline cudaError_t launch_cooperative(const void* kernel, const KParams& p, size_t smem,
                                       cudaStream_t s) {
+  if (smem > 48 * 1024) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
   const TimingEvents& ev = timing_events();
   if (ev.begin) cudaEventRecord(ev.begin, s);
   cudaLaunchConfig_t cfg = {};

@@ -158,12 +158,11 @@ GN_API int gn_set_timing_events(void* ev_begin, void* ev_mid, void* ev_end);
  * a thread-block cluster holds a whole reduction unit -- one (n, group) span
  * for NCHW, one sample for NHWC -- in shared memory; it is taken for 16-byte
  * aligned inputs whose unit is at most 32 MiB.  GN_REGIME_PIPELINED runs one
- * persistent kernel (a cooperative launch) whose CTAs take tasks from a queue:
- * the first pass over a piece of a unit (one sample for NHWC, one (n, group)
- * for NCHW), and, a few units behind, the second pass over the same pieces,
- * which finds the unit's input still in L2; it is taken for 16-byte aligned
- * inputs whose unit (x, or x and dy) is at most 32 MiB, and NHWC rows of at
- * most 256 16-byte vectors.  Every regime gives results within the same
+ * persistent kernel (a cooperative launch, NCHW with HW >= 2048 and 16-byte
+ * aligned data): every CTA takes one piece of every (n, group) unit, unit
+ * after unit, the second pass of a unit trailing its first by a few units so
+ * that it finds the input still in L2; data arrives through bulk copies into
+ * shared memory.  Every regime gives results within the same
  * tolerances of the definition, each bit-identical from run to run. */
 #define GN_REGIME_AUTO (-1)
 #define GN_REGIME_TWO_KERNEL 0
