@@ -12,7 +12,7 @@ count and value distributions:
 
 Each call is one forward followed by one backward on the same stream, so the
 kernels launch in the order fwd-first, fwd-second, bwd-first, bwd-second
-(one kernel per op in the resident regime).
+(one kernel per op in the resident and pipelined regimes).
 """
 from __future__ import annotations
 
@@ -31,14 +31,15 @@ def main(argv=None) -> int:
     ap.add_argument("--H", type=int)
     ap.add_argument("--W", type=int)
     ap.add_argument("--calls", type=int, default=2)
-    ap.add_argument("--regime", choices=["auto", "two_kernel", "resident"], default="auto")
+    ap.add_argument("--regime", choices=["auto", "two_kernel", "resident", "pipelined"],
+                    default="auto")
     a = ap.parse_args(argv)
     w = synth.BY_NAME[a.workload]
     over = {k: v for k, v in (("N", a.N), ("H", a.H), ("W", a.W)) if v is not None}
     if over:
         w = w.scaled(**over)
     gn.set_regime({"auto": gn.REGIME_AUTO, "two_kernel": gn.REGIME_TWO_KERNEL,
-                   "resident": gn.REGIME_RESIDENT}[a.regime])
+                   "resident": gn.REGIME_RESIDENT, "pipelined": gn.REGIME_PIPELINED}[a.regime])
     inp = synth.make_inputs(w, "cuda", seed=0)
     x, dy, gm, bt = inp["x"], inp["dy"], inp["gamma"], inp["beta"]
     y, dx = torch.empty_like(x), torch.empty_like(x)
