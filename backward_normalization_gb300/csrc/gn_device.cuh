@@ -126,14 +126,15 @@ struct Access<float, 4> {
     f[2] = __uint_as_float(u.z);
     f[3] = __uint_as_float(u.w);
   }
-  __device__ static void store(float* p, const float (&f)[4], uint64_t pol) {
+  __device__ static Raw pack(const float (&f)[4]) {
     uint4 u;
     u.x = __float_as_uint(f[0]);
     u.y = __float_as_uint(f[1]);
     u.z = __float_as_uint(f[2]);
     u.w = __float_as_uint(f[3]);
-    st16(p, u, pol);
+    return u;
   }
+  __device__ static void store(float* p, const float (&f)[4], uint64_t pol) { st16(p, pack(f), pol); }
 };
 template <>
 struct Access<__half, 8> {
@@ -150,14 +151,15 @@ struct Access<__half, 8> {
     f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
     f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
   }
-  __device__ static void store(__half* p, const float (&f)[8], uint64_t pol) {
+  __device__ static Raw pack(const float (&f)[8]) {
     uint4 u;
     u.x = f2h(f[0], f[1]);
     u.y = f2h(f[2], f[3]);
     u.z = f2h(f[4], f[5]);
     u.w = f2h(f[6], f[7]);
-    st16(p, u, pol);
+    return u;
   }
+  __device__ static void store(__half* p, const float (&f)[8], uint64_t pol) { st16(p, pack(f), pol); }
 };
 template <>
 struct Access<__nv_bfloat16, 8> {
@@ -174,13 +176,16 @@ struct Access<__nv_bfloat16, 8> {
     f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
     f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
   }
-  __device__ static void store(__nv_bfloat16* p, const float (&f)[8], uint64_t pol) {
+  __device__ static Raw pack(const float (&f)[8]) {
     uint4 u;
     u.x = f2b(f[0], f[1]);
     u.y = f2b(f[2], f[3]);
     u.z = f2b(f[4], f[5]);
     u.w = f2b(f[6], f[7]);
-    st16(p, u, pol);
+    return u;
+  }
+  __device__ static void store(__nv_bfloat16* p, const float (&f)[8], uint64_t pol) {
+    st16(p, pack(f), pol);
   }
 };
 
@@ -248,6 +253,29 @@ __device__ __forceinline__ void tma_load_1d(void* dst, const void* src, uint32_t
       "[%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
       "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(pol)
       : "memory");
+}
+// One contiguous shared -> global copy of `bytes` (16-byte aligned, multiple
+// of 16) in the current bulk async-group, with an L2 eviction policy for the
+// destination.
+__device__ __forceinline__ void tma_store_1d(void* dst, const void* src, uint32_t bytes,
+                                             uint64_t pol) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::
+                   "l"(dst), "r"(smem_addr(src)), "r"(bytes), "l"(pol)
+               : "memory");
+}
+// Closes the current bulk async-group (an empty one if it holds no copy).
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Waits until at most N bulk async-groups are still reading their shared
+// memory sources (.read), or are still in flight at all.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+template <int N>
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
 }
 // One 2-D tile [rows x cols] at (col c0, row r0) of the tensor map -> shared
 // memory (rows packed, no swizzle), completing on `bar`.

@@ -397,12 +397,9 @@ __global__ void __launch_bounds__(512, 1) nchw_pipelined(const __grid_constant__
   const int64_t sm_floats = nchw_smem_floats(g);
   unsigned long long* rec = reinterpret_cast<unsigned long long*>(p.ready);
   const int tid = threadIdx.x, nt = blockDim.x;
-  const uint64_t pfirst = policy_evict_first();
   float s1 = 0.f, s2 = 0.f, K = 0.f;               // pass-1 sums; shift (fwd) or mean (bwd)
   float ca = 0.f, cb = 0.f, cc = 0.f, cmu = 0.f;   // pass-2 constants
   bool ok = false;
-  Pending pd;
-  pd.unit[0] = pd.unit[1] = -1;
   // piece of task t: plane a (channel e) of sample unit / G, segment b = [c, d)
   auto describe = [&](const Task& t, SlotHdr& h) {
     const int64_t n = t.unit / g.G, grp = t.unit % g.G;
@@ -428,7 +425,7 @@ __global__ void __launch_bounds__(512, 1) nchw_pipelined(const __grid_constant__
     *bytes = (int32_t)(((h.d - e0 < g.chunk) ? h.d - e0 : g.chunk) * (int64_t)sizeof(T));
     return h.a * g.HW + e0;
   };
-  // finalisation of unit u by the CTA whose arrival completed it
+  // finalisation of unit u by its designated CTA
   auto fin = [&](int64_t u) {
     const int64_t n = u / g.G, c0 = (u % g.G) * g.Cg;
     if (kBwd)
@@ -454,12 +451,15 @@ __global__ void __launch_bounds__(512, 1) nchw_pipelined(const __grid_constant__
     finalize_params(p, sm);  // the last unit: dgamma, dbeta
     if (tid == 0) atomicExch(p.tickets + g.units_fin, 0u);
   };
-  auto consume = [&](const SlotHdr& h, const char* sx, const char* sd) {
+  auto out_at = [&](const SlotHdr& h) {
+    return static_cast<T*>(p.out) + h.a * g.HW + h.c + (int64_t)h.chunk * g.chunk;
+  };
+  auto consume = [&](const SlotHdr& h, char* sx, const char* sd) {
     const int c = h.chunk, nc = h.nchunks, bytes = h.bytes;
-    if (c == 0) settle(p, pd, h.step, fin);
+    if (c == 0 && (h.pass == 1 || h.step >= g.units_fin)) finalize_due(p, h.step, fin);
     const int64_t ch = h.e, ng = h.unit;
     const int nv = bytes / 16;
-    const uint4* vx = reinterpret_cast<const uint4*>(sx);
+    uint4* vx = reinterpret_cast<uint4*>(sx);
     const uint4* vd = reinterpret_cast<const uint4*>(sd);
     if (h.pass == 1) {
       if (c == 0) {
@@ -485,10 +485,10 @@ __global__ void __launch_bounds__(512, 1) nchw_pipelined(const __grid_constant__
         const float2 tot = block_sum2_t0(s1, s2, sm);
         if (tid == 0) {
           p.part[h.a * g.T + h.b] = tot;
-          arrive_async(p, pd, ng, h.step);
+          arrive_release(p, ng);
         }
       }
-      return;
+      return false;
     }
     if (c == 0) {
       float lo, hi;
@@ -509,8 +509,7 @@ __global__ void __launch_bounds__(512, 1) nchw_pipelined(const __grid_constant__
         ca *= hi;  // rstd * gamma
       }
     }
-    if (ok) {
-      T* out = static_cast<T*>(p.out) + h.a * g.HW + h.c + (int64_t)c * g.chunk;
+    if (ok) {  // the output replaces x in the slot; thread 0 stores it
 #pragma unroll 4
       for (int v = tid; v < nv; v += nt) {
         float xv[VW];
@@ -524,11 +523,12 @@ __global__ void __launch_bounds__(512, 1) nchw_pipelined(const __grid_constant__
 #pragma unroll
           for (int e = 0; e < VW; ++e) xv[e] = fmaf(xv[e] - cmu, ca, cb);
         }
-        Access<T, VW>::store(out + (int64_t)v * VW, xv, pfirst);
+        vx[v] = Access<T, VW>::pack(xv);
       }
     }
+    return ok;
   };
-  run_ring<kBwd>(p, R, describe, chunk_off, consume);
+  run_ring<kBwd>(p, R, describe, chunk_off, consume, out_at);
 }
 
 template <typename T, int VW>

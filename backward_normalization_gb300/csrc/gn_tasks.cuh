@@ -11,14 +11,13 @@
 //   pass 2 of unit s - D (s >= D): wait for that unit's ready record, stream
 //                                 the piece again (it is still in L2: only D
 //                                 units were read since) and write the output.
-// The first task of each step settles the arrivals of earlier steps: the CTA
-// whose arrival completed a unit finalises it (statistics, then the unit's
-// ready record).  So an arrival is settled one step after it was made, its
-// latency hidden behind a step of streaming, and always before the CTA waits
-// on any unit.  Deadlock-free: take the smallest unit w that some CTA waits
-// for; w's last arriver has either settled w (its step w + 1 came before any
-// wait on a unit >= w + 1 - D, and by minimality it waits on nothing smaller)
-// or is still running; either way w gets finalised.  Every wait is also
+// Unit u is finalised (statistics, then its ready record) by CTA u mod P at
+// the start of its step u + 1, once all pieces of u have arrived; arrivals are
+// fire-and-forget.  Deadlock-free: take the smallest unit w that some CTA
+// waits for, either for w's record or, as w's finaliser, for w's arrivals.
+// Every CTA's waits before its pass 1 of w (steps <= w) are on units < w, so
+// by minimality each CTA gets past its pass 1 of w; then w's finaliser, whose
+// waits before step w + 1 are also on smaller units, finalises w.  Every wait is also
 // bounded: after kReadyWaitLimit polls the CTA raises bit 1 of the workspace
 // error word and skips that piece's output.  Results do not depend on timing:
 // records have fixed slots and every sum has a fixed order.
@@ -77,45 +76,39 @@ __device__ __forceinline__ bool wait_record(const unsigned long long* rec, unsig
   return s_ok != 0;
 }
 
-// Arrivals not yet settled (thread 0's registers): at most two, from the
-// current step and the one before.
-struct Pending {
-  int64_t unit[2], step[2];
-  unsigned old[2];
-};
-
-// Thread 0 arrives on unit u's counter in step `step` and keeps the old value
-// for later (the atomic's latency is not waited for here).  The record
-// stores before it are ordered by the fence.
-__device__ __forceinline__ void arrive_async(const KParams& p, Pending& pd, int64_t u,
-                                             int64_t step) {
-  __threadfence();
-  const int sl = (int)(step & 1);
-  pd.unit[sl] = u;
-  pd.step[sl] = step;
-  pd.old[sl] = atomicAdd(p.tickets + u, 1u);
+// Thread 0 arrives on unit u's counter; the record stores before it are
+// ordered by the release.  Nothing waits for the counter's value here.
+__device__ __forceinline__ void arrive_release(const KParams& p, int64_t u) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(p.tickets + u) : "memory");
 }
 
-// Settles the arrivals made before step `step`: the units they completed are
-// finalised by the whole CTA with fin(u).  Called by every thread at the
-// first chunk of a task.
+// At the first task of step `step`: if this CTA is the finaliser of unit
+// step - 1 (CTA u mod P for unit u), thread 0 waits (bounded) until all P
+// pieces of that unit have arrived, then the whole CTA runs fin(u).  The
+// finalisation work rotates over the CTAs, so no CTA falls behind by doing
+// all of it.  Called by every thread.
 template <typename Fin>
-__device__ __forceinline__ void settle(const KParams& p, Pending& pd, int64_t step, Fin fin) {
-  __shared__ long long s_fin[2];
+__device__ __forceinline__ void finalize_due(const KParams& p, int64_t step, Fin fin) {
+  const int64_t u = step - 1;
+  if (u < 0 || u >= p.g.units_fin || u % p.g.pieces != (int64_t)blockIdx.x) return;
+  __shared__ int s_go;
   if (threadIdx.x == 0) {
-    for (int sl = 0; sl < 2; ++sl) {
-      s_fin[sl] = -1;
-      if (pd.unit[sl] >= 0 && pd.step[sl] < step) {
-        if (pd.old[sl] == (unsigned)p.g.arrivals_per_n - 1) s_fin[sl] = pd.unit[sl];
-        pd.unit[sl] = -1;
+    int ok = 0;
+    const unsigned want = (unsigned)p.g.arrivals_per_n;
+    for (uint32_t i = 0; i < kReadyWaitLimit; ++i) {
+      unsigned v;
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p.tickets + u) : "memory");
+      if (v == want) {
+        ok = 1;
+        break;
       }
+      __nanosleep(32);
     }
+    if (!ok) atomicOr(p.err, 2u);
+    s_go = ok;
   }
   __syncthreads();
-  const long long f0 = s_fin[0], f1 = s_fin[1];
-  __syncthreads();
-  if (f0 >= 0) fin(f0);
-  if (f1 >= 0) fin(f1);
+  if (s_go) fin(u);
 }
 
 // ------------------------------------------------------------ the ring
@@ -173,13 +166,18 @@ __device__ __forceinline__ SlotHdr* hdr_at(const RingSmem& R, int s) {
 // along into hdr.aux, or 0 for none) for a task, and
 // `chunk_off(hdr, c, &bytes)` gives the element offset in x (and dy) of chunk
 // c and its bytes.  `consume(hdr, slot_x, slot_dy)` is called by every thread
-// of the CTA for each chunk in order and may use __syncthreads.  Every wait is
+// of the CTA for each chunk in order and may use __syncthreads; it returns
+// (the same in every thread) whether it left an output chunk in place of x in
+// the slot, which thread 0 then sends to `out_at(hdr)` with a bulk store (one
+// bulk group per chunk, empty if there is none).  A slot is refilled one chunk
+// later, once its store has read it, so the CTA's threads make no global
+// stores of their own for the output and a fence waits for none.  Every wait is
 // bounded: a copy that does not land in time raises bit 0 of the error word,
 // the CTA stops consuming, waits (bounded) for the copies it issued and
 // leaves.  The last CTA to leave clears the ready records and its counter.
-template <bool kDy, typename Describe, typename ChunkOff, typename Consume>
+template <bool kDy, typename Describe, typename ChunkOff, typename Consume, typename OutAt>
 __device__ __forceinline__ void run_ring(const KParams& p, const RingSmem& R, Describe describe,
-                                         ChunkOff chunk_off, Consume consume) {
+                                         ChunkOff chunk_off, Consume consume, OutAt out_at) {
   const Geom& g = p.g;
   const int64_t U = g.units_fin, D = g.lag, piece = blockIdx.x;
   const char* xb = static_cast<const char*>(p.x);
@@ -269,8 +267,9 @@ __device__ __forceinline__ void run_ring(const KParams& p, const RingSmem& R, De
     else
       for (int i = 0; i < R.S && !idone; ++i) issue(i);
   }
-  int s = 0;
+  int s = 0, refill = -1;  // refill: the slot consumed one chunk ago
   uint32_t ph = 0;
+  const uint64_t pfirst = pol2;
   while (true) {
     if (threadIdx.x == 0) s_ok = mbar_wait(R.full + s, ph, p.err) ? 1 : 0;
     __syncthreads();
@@ -281,13 +280,19 @@ __device__ __forceinline__ void run_ring(const KParams& p, const RingSmem& R, De
       if (threadIdx.x == 0) --issued;
       break;
     }
-    const char* slot = R.ring + s * R.slot_stride;
-    consume(h, slot, slot + R.ten_stride);
+    char* slot = R.ring + s * R.slot_stride;
+    const bool out = consume(h, slot, slot + R.ten_stride);
     __syncthreads();  // every thread is done with slot s
     if (threadIdx.x == 0) {
       --issued;
-      fence_proxy_async_smem();  // the slot's reads before the next copy into it
-      issue(s);
+      fence_proxy_async_smem();  // the slot's generic accesses before async-proxy ones
+      if (out) tma_store_1d(out_at(h), slot, (uint32_t)h.bytes, pfirst);
+      bulk_commit();
+      if (refill >= 0) {
+        bulk_wait_read<1>();  // the refilled slot's store (if any) has read it
+        issue(refill);
+      }
+      refill = s;
     }
     if (++s == R.S) {
       s = 0;
@@ -296,6 +301,7 @@ __device__ __forceinline__ void run_ring(const KParams& p, const RingSmem& R, De
   }
   unsigned* q = p.queue;
   if (threadIdx.x == 0) {
+    bulk_wait_all<0>();  // the output stores are complete
     // after an abort: wait (bounded) for the copies still in flight
     for (int i = 0; i < issued; ++i) {
       const int si = (s + i) % R.S;
