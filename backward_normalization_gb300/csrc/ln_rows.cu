@@ -1,0 +1,556 @@
+// ln_rows.cu -- LayerNorm and RMSNorm over the last dimension of a row-major
+// [M, N] array, forward and backward (include/ln.h), after "Optimize AMD
+// normalization backward kernel by using tiled and two pass" (ROCm/pytorch PR
+// #3564: layer_norm / rms_norm backward with their gamma/beta gradients).
+//
+// A row is held in registers by a team of TW threads (a power of two, at most
+// the CTA's 256): thread `lane` of the team owns the row's 16-byte vectors
+// lane, lane + TW, ..., VPT of them, so its columns are the same for every row
+// it visits.  Team sums are xor butterflies (every lane ends with the same
+// bits: each pairwise add is commutative) or, for teams wider than a warp,
+// per-warp butterflies added in warp order through shared memory.
+//
+//   forward:  load the row, mean (LayerNorm), sum of squared deviations (a
+//             second pass over the registers), rstd, then y; one read of x,
+//             one write of y.
+//   backward: load x and dy rows, xhat and g = gamma*dy, the two row sums,
+//             dx; dgamma/dbeta partials stay in registers across the CTA's
+//             rows.  The CTA then adds its teams' partials in team order into
+//             one record per feature, and a second kernel adds the CTAs'
+//             records in CTA order: the two-level deterministic reduction of
+//             the GroupNorm path, applied to rows.
+// Rows are assigned to CTAs in a fixed grid-stride order (the grid depends
+// only on the problem and the device), so results are bit-identical from run
+// to run.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include "../../include/ln.h"
+#include "gn_device.cuh"
+
+namespace gn {
+namespace {
+
+constexpr int kRowThreads = 256;
+
+struct RowParams {
+  const void* x;
+  const void* dy;
+  void* out;  // y or dx
+  const float* gamma;
+  const float* beta;
+  float* mean;   // forward: written (LayerNorm); backward: read
+  float* rstd;   // forward: written; backward: read
+  float* dgamma;
+  float* dbeta;
+  float2* part;  // backward: [grid][N] (dgamma, dbeta) partials
+  int64_t M, N, V;  // V: vectors per row
+  int tw;           // team width
+  float eps;
+  int want_part;    // backward: 1 if any parameter gradient is wanted
+};
+
+// Sum over the team of `v` (TW a power of two).  Every thread of the CTA must
+// call it the same number of times; `red` holds blockDim/32 floats.
+__device__ __forceinline__ float team_sum(float v, int tw, float* red) {
+  const int w = tw < 32 ? tw : 32;
+  for (int o = w >> 1; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  if (tw <= 32) return v;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  const int first = (threadIdx.x / tw) * (tw >> 5);
+  float s = 0.f;
+  for (int k = 0; k < (tw >> 5); ++k) s += red[first + k];
+  __syncthreads();
+  return s;
+}
+
+// gamma / beta for one vector of features (fp32, VW wide).
+template <int VW>
+__device__ __forceinline__ void load_param(const float* p, int64_t c0, float dflt,
+                                           float (&out)[VW]) {
+  if (!p) {
+#pragma unroll
+    for (int e = 0; e < VW; ++e) out[e] = dflt;
+    return;
+  }
+  if (VW == 8 || VW == 4) {
+#pragma unroll
+    for (int e = 0; e < VW; e += 4) {
+      const float4 f = __ldg(reinterpret_cast<const float4*>(p + c0 + e));
+      out[e] = f.x;
+      out[e + 1] = f.y;
+      out[e + 2] = f.z;
+      out[e + 3] = f.w;
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < VW; ++e) out[e] = __ldg(p + c0 + e);
+  }
+}
+
+// ------------------------------------------------------------------ forward
+template <typename T, int VW, int VPT, bool kRms>
+__global__ void __launch_bounds__(kRowThreads) row_fwd(const __grid_constant__ RowParams p) {
+  __shared__ float red[kRowThreads / 32];
+  const int tw = p.tw, team = threadIdx.x / tw, lane = threadIdx.x % tw;
+  const int nteams = blockDim.x / tw;
+  const float inv_n = 1.0f / (float)p.N;
+  const T* x = static_cast<const T*>(p.x);
+  T* y = static_cast<T*>(p.out);
+  const uint64_t pol = policy_evict_first();
+  for (int64_t r0 = (int64_t)blockIdx.x * nteams; r0 < p.M; r0 += (int64_t)gridDim.x * nteams) {
+    const int64_t row = r0 + team;
+    const bool act = row < p.M;
+    float v[VPT][VW];
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int64_t vi = lane + (int64_t)k * tw;
+      if (act && vi < p.V) {
+        Access<T, VW>::load(x + row * p.N + vi * VW, v[k], pol);
+      } else {
+#pragma unroll
+        for (int e = 0; e < VW; ++e) v[k][e] = 0.f;
+      }
+    }
+    float mean = 0.f;
+    if (!kRms) {
+      float s = 0.f;
+#pragma unroll
+      for (int k = 0; k < VPT; ++k)
+#pragma unroll
+        for (int e = 0; e < VW; ++e) s += v[k][e];
+      mean = team_sum(s, tw, red) * inv_n;
+    }
+    float q = 0.f;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const bool in = act && lane + (int64_t)k * tw < p.V;
+#pragma unroll
+      for (int e = 0; e < VW; ++e) {
+        const float d = in ? v[k][e] - mean : 0.f;
+        q = fmaf(d, d, q);
+      }
+    }
+    const float rstd = 1.0f / sqrtf(team_sum(q, tw, red) * inv_n + p.eps);
+    if (!act) continue;  // no barrier follows in this iteration
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int64_t vi = lane + (int64_t)k * tw;
+      if (vi >= p.V) continue;
+      float gm[VW], bt[VW];
+      load_param<VW>(p.gamma, vi * VW, 1.f, gm);
+      load_param<VW>(kRms ? nullptr : p.beta, vi * VW, 0.f, bt);
+#pragma unroll
+      for (int e = 0; e < VW; ++e) v[k][e] = fmaf(v[k][e] - mean, rstd * gm[e], bt[e]);
+      Access<T, VW>::store(y + row * p.N + vi * VW, v[k], pol);
+    }
+    if (lane == 0) {
+      if (!kRms) p.mean[row] = mean;
+      p.rstd[row] = rstd;
+    }
+  }
+}
+
+// ----------------------------------------------------------------- backward
+// Dynamic shared memory: nteams * N floats for dgamma partials, the same for
+// dbeta (teams' per-feature partials before the CTA adds them in team order).
+template <typename T, int VW, int VPT, bool kRms>
+__global__ void __launch_bounds__(kRowThreads) row_bwd(const __grid_constant__ RowParams p) {
+  extern __shared__ float colsum[];
+  __shared__ float red[kRowThreads / 32];
+  const int tw = p.tw, team = threadIdx.x / tw, lane = threadIdx.x % tw;
+  const int nteams = blockDim.x / tw;
+  const float inv_n = 1.0f / (float)p.N;
+  const T* x = static_cast<const T*>(p.x);
+  const T* dy = static_cast<const T*>(p.dy);
+  T* dx = static_cast<T*>(p.out);
+  const uint64_t pol = policy_evict_first();
+  float pg[VPT][VW], pb[VPT][VW];  // this thread's dgamma / dbeta partials
+#pragma unroll
+  for (int k = 0; k < VPT; ++k)
+#pragma unroll
+    for (int e = 0; e < VW; ++e) pg[k][e] = pb[k][e] = 0.f;
+  for (int64_t r0 = (int64_t)blockIdx.x * nteams; r0 < p.M; r0 += (int64_t)gridDim.x * nteams) {
+    const int64_t row = r0 + team;
+    const bool act = row < p.M;
+    const float mean = (!kRms && act) ? __ldg(p.mean + row) : 0.f;
+    const float rstd = act ? __ldg(p.rstd + row) : 0.f;
+    float xv[VPT][VW], dv[VPT][VW];
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int64_t vi = lane + (int64_t)k * tw;
+      if (act && vi < p.V) {
+        Access<T, VW>::load(x + row * p.N + vi * VW, xv[k], pol);
+        Access<T, VW>::load(dy + row * p.N + vi * VW, dv[k], pol);
+      } else {
+#pragma unroll
+        for (int e = 0; e < VW; ++e) xv[k][e] = dv[k][e] = 0.f;
+      }
+    }
+    // xhat in xv, g = gamma*dy kept apart from dy (both are needed)
+    float s1 = 0.f, s2 = 0.f;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int64_t vi = lane + (int64_t)k * tw;
+      float gm[VW];
+      load_param<VW>(p.gamma, (vi < p.V ? vi : 0) * VW, 1.f, gm);
+#pragma unroll
+      for (int e = 0; e < VW; ++e) {
+        xv[k][e] = (xv[k][e] - mean) * rstd;
+        const float g = gm[e] * dv[k][e];
+        s1 += g;
+        s2 = fmaf(g, xv[k][e], s2);
+      }
+    }
+    const float c1 = kRms ? 0.f : team_sum(s1, tw, red) * inv_n;
+    const float c2 = team_sum(s2, tw, red) * inv_n;
+    if (!act) continue;  // no barrier follows in this iteration
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int64_t vi = lane + (int64_t)k * tw;
+      if (vi >= p.V) continue;
+      float gm[VW], o[VW];
+      load_param<VW>(p.gamma, vi * VW, 1.f, gm);
+#pragma unroll
+      for (int e = 0; e < VW; ++e) {
+        const float g = gm[e] * dv[k][e];
+        o[e] = rstd * (g - c1 - xv[k][e] * c2);
+        pg[k][e] = fmaf(dv[k][e], xv[k][e], pg[k][e]);
+        pb[k][e] += dv[k][e];
+      }
+      Access<T, VW>::store(dx + row * p.N + vi * VW, o, pol);
+    }
+  }
+  if (!p.want_part) return;
+  // the teams' partials -> shared memory -> one record per feature, in team order
+  float* sg = colsum;
+  float* sb = colsum + (int64_t)nteams * p.N;
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    const int64_t vi = lane + (int64_t)k * tw;
+    if (vi >= p.V) continue;
+#pragma unroll
+    for (int e = 0; e < VW; ++e) {
+      sg[team * p.N + vi * VW + e] = pg[k][e];
+      sb[team * p.N + vi * VW + e] = pb[k][e];
+    }
+  }
+  __syncthreads();
+  for (int64_t c = threadIdx.x; c < p.N; c += blockDim.x) {
+    float a = 0.f, b = 0.f;
+    for (int t = 0; t < nteams; ++t) {
+      a += sg[t * p.N + c];
+      b += sb[t * p.N + c];
+    }
+    p.part[(int64_t)blockIdx.x * p.N + c] = make_float2(a, b);
+  }
+  grid_launch_dependents();  // the column kernel may start launching
+}
+
+// dgamma[c] = sum over the P CTA records of feature c, dbeta likewise: eight
+// slices per feature (records s, s + 8, ... in order), then the slices in
+// order.  256 threads: 32 features x 8 slices.
+__global__ void __launch_bounds__(256) row_col_reduce(const __grid_constant__ RowParams p,
+                                                      int64_t P) {
+  __shared__ float2 acc[8][32];
+  grid_dependency_wait();  // the records of the row kernel are complete
+  const int j = threadIdx.x & 31, sl = threadIdx.x >> 5;
+  const int64_t c = (int64_t)blockIdx.x * 32 + j;
+  float a = 0.f, b = 0.f;
+  if (c < p.N) {
+    for (int64_t r = sl; r < P; r += 8 * 8) {
+      float2 v[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int64_t rr = r + 8 * k;
+        v[k] = rr < P ? __ldcg(p.part + rr * p.N + c) : make_float2(0.f, 0.f);
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        a += v[k].x;
+        b += v[k].y;
+      }
+    }
+  }
+  acc[sl][j] = make_float2(a, b);
+  __syncthreads();
+  if (sl == 0 && c < p.N) {
+    for (int s = 1; s < 8; ++s) {
+      a += acc[s][j].x;
+      b += acc[s][j].y;
+    }
+    if (p.dgamma) p.dgamma[c] = a;
+    if (p.dbeta) p.dbeta[c] = b;
+  }
+}
+
+// -------------------------------------------------------------------- host
+int64_t cdiv64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+int pow2ceil(int64_t v) {
+  int p = 1;
+  while (p < v) p <<= 1;
+  return p;
+}
+
+// The shape of one call: vector width, vectors per thread, team width, grid.
+struct RowPlan {
+  int vw = 0, vpt = 0, tw = 0, nteams = 0;
+  int64_t V = 0, grid = 0;
+  size_t smem = 0;  // backward: dynamic shared memory
+  bool ok = false;
+};
+
+// Only the combinations the plan can choose are instantiated (backward at
+// most 16 values per thread, forward at most 32).
+template <typename T, int VW, int VPT, bool kRms>
+const void* row_kernel(bool bwd) {
+  if (bwd) {
+    if constexpr (VPT * VW <= 16) return (const void*)row_bwd<T, VW, VPT, kRms>;
+    return nullptr;
+  }
+  if constexpr (VPT * VW <= 32) return (const void*)row_fwd<T, VW, VPT, kRms>;
+  return nullptr;
+}
+
+template <typename T, int VW, bool kRms>
+const void* row_kernel_vpt(int vpt, bool bwd) {
+  switch (vpt) {
+    case 1: return row_kernel<T, VW, 1, kRms>(bwd);
+    case 2: return row_kernel<T, VW, 2, kRms>(bwd);
+    case 4: return row_kernel<T, VW, 4, kRms>(bwd);
+    default: return row_kernel<T, VW, 8, kRms>(bwd);
+  }
+}
+
+template <typename T, bool kRms>
+const void* row_kernel_for(const RowPlan& pl, bool bwd) {
+  constexpr int V = Elem<T>::VEC;
+  return pl.vw == 1 ? row_kernel_vpt<T, 1, kRms>(pl.vpt, bwd)
+                    : row_kernel_vpt<T, V, kRms>(pl.vpt, bwd);
+}
+
+const void* kernel_of(const RowPlan& pl, int dtype, bool rms, bool bwd) {
+  switch (dtype) {
+    case kF32: return rms ? row_kernel_for<float, true>(pl, bwd) : row_kernel_for<float, false>(pl, bwd);
+    case kF16: return rms ? row_kernel_for<__half, true>(pl, bwd) : row_kernel_for<__half, false>(pl, bwd);
+    default:
+      return rms ? row_kernel_for<__nv_bfloat16, true>(pl, bwd)
+                 : row_kernel_for<__nv_bfloat16, false>(pl, bwd);
+  }
+}
+
+// Co-resident CTAs of a kernel on the current device (cached), or an estimate
+// of 4 per SM with no device.
+int64_t resident(const void* fn, size_t smem) {
+  static std::mutex mu;
+  static std::map<std::tuple<int, const void*, size_t>, int64_t> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 152 * 4;
+  }
+  const auto key = std::make_tuple(dev, fn, smem);
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+  }
+  int sms = 0, nb = 0;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (smem > 48 * 1024)
+    cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fn, kRowThreads, smem) != cudaSuccess)
+    nb = 0;
+  cudaGetLastError();
+  const int64_t r = (int64_t)nb * (sms > 0 ? sms : 152);
+  std::lock_guard<std::mutex> lock(mu);
+  cache[key] = r;
+  return r;
+}
+
+// vw: 16-byte vectors when rows and parameters allow, else 1.  vpt: as many
+// vectors per thread as registers allow (forward 32 values, backward 16, as
+// the backward also holds dy and two partials per value); team width the
+// power of two that covers the row.
+RowPlan row_plan(int64_t M, int64_t N, int dtype, bool rms, bool bwd, bool aligned) {
+  RowPlan pl;
+  const int esz = dtype == kF32 ? 4 : 2;
+  pl.vw = (aligned && (N * esz) % 16 == 0) ? 16 / esz : 1;
+  pl.V = N / pl.vw;
+  const int cap = bwd ? 16 : 32;
+  int vmax = cap / pl.vw;
+  if (vmax > 8) vmax = 8;
+  if (vmax < 1) vmax = 1;
+  int vpt = 1;
+  while (vpt < vmax && vpt < pl.V) vpt <<= 1;
+  pl.vpt = vpt;
+  pl.tw = pow2ceil(cdiv64(pl.V, vpt));
+  if (pl.tw > kRowThreads) return pl;  // rows too long to hold in one CTA's registers
+  pl.nteams = kRowThreads / pl.tw;
+  pl.smem = bwd ? sizeof(float) * 2 * (size_t)pl.nteams * (size_t)N : 0;
+  if (pl.smem > 200 * 1024) return pl;
+  const int64_t res = resident(kernel_of(pl, dtype, rms, bwd), pl.smem);
+  pl.grid = std::min<int64_t>(cdiv64(M, pl.nteams), res > 0 ? res : 1);
+  if (pl.grid < 1) pl.grid = 1;
+  pl.ok = true;
+  return pl;
+}
+
+bool a16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  if (!a || !b) return false;
+  const char* pa = static_cast<const char*>(a);
+  const char* pb = static_cast<const char*>(b);
+  return pa < pb + nb && pb < pa + na;
+}
+
+int fail(cudaError_t e) {
+  return e == cudaSuccess ? GN_OK : GN_ERR_CUDA;
+}
+
+int run_fwd(const void* x, int64_t M, int64_t N, int dtype, const float* gamma, const float* beta,
+            float eps, void* y, float* mean, float* rstd, void* stream, bool rms) {
+  if (dtype != kF32 && dtype != kF16 && dtype != kBF16) return GN_ERR_UNSUPPORTED;
+  if (M < 0 || N <= 0 || !(eps >= 0.f)) return GN_ERR_INVALID;
+  if (M == 0) return GN_OK;
+  if (!x || !y || !rstd || (!rms && !mean)) return GN_ERR_INVALID;
+  const size_t bytes = (size_t)M * (size_t)N * (dtype == kF32 ? 4 : 2);
+  if (y != x && overlaps(y, bytes, x, bytes)) return GN_ERR_INVALID;
+  if (overlaps(rstd, sizeof(float) * M, y, bytes) || overlaps(mean, sizeof(float) * M, y, bytes) ||
+      overlaps(mean, sizeof(float) * M, rstd, sizeof(float) * M))
+    return GN_ERR_INVALID;
+  const bool aligned = a16(x) && a16(y) && (!gamma || a16(gamma)) && (!beta || a16(beta));
+  const RowPlan pl = row_plan(M, N, dtype, rms, false, aligned);
+  if (!pl.ok) return GN_ERR_UNSUPPORTED;
+  RowParams p{};
+  p.x = x;
+  p.out = y;
+  p.gamma = gamma;
+  p.beta = rms ? nullptr : beta;
+  p.mean = mean;
+  p.rstd = rstd;
+  p.M = M;
+  p.N = N;
+  p.V = pl.V;
+  p.tw = pl.tw;
+  p.eps = eps;
+  const void* fn = kernel_of(pl, dtype, rms, false);
+  void* args[] = {&p};
+  return fail(cudaLaunchKernel(fn, dim3((unsigned)pl.grid), dim3(kRowThreads), args, 0,
+                               static_cast<cudaStream_t>(stream)));
+}
+
+int run_bwd(const void* dy, const void* x, const float* mean, const float* rstd,
+            const float* gamma, int64_t M, int64_t N, int dtype, void* dx, float* dgamma,
+            float* dbeta, void* workspace, size_t workspace_bytes, void* stream, bool rms) {
+  if (dtype != kF32 && dtype != kF16 && dtype != kBF16) return GN_ERR_UNSUPPORTED;
+  if (M < 0 || N <= 0) return GN_ERR_INVALID;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (rms) dbeta = nullptr;
+  if (M == 0) {  // empty sums
+    if (dgamma && cudaMemsetAsync(dgamma, 0, sizeof(float) * N, s) != cudaSuccess) return GN_ERR_CUDA;
+    if (dbeta && cudaMemsetAsync(dbeta, 0, sizeof(float) * N, s) != cudaSuccess) return GN_ERR_CUDA;
+    return GN_OK;
+  }
+  if (!dy || !x || !rstd || !dx || (!rms && !mean)) return GN_ERR_INVALID;
+  const size_t bytes = (size_t)M * (size_t)N * (dtype == kF32 ? 4 : 2);
+  if (dx != dy && overlaps(dx, bytes, dy, bytes)) return GN_ERR_INVALID;
+  if (overlaps(dx, bytes, x, bytes)) return GN_ERR_INVALID;
+  const size_t nb = sizeof(float) * (size_t)N;
+  if (overlaps(dgamma, nb, dx, bytes) || overlaps(dbeta, nb, dx, bytes) ||
+      overlaps(dgamma, nb, dbeta, nb))
+    return GN_ERR_INVALID;
+  const bool aligned = a16(x) && a16(dy) && a16(dx) && (!gamma || a16(gamma));
+  const RowPlan pl = row_plan(M, N, dtype, rms, true, aligned);
+  if (!pl.ok) return GN_ERR_UNSUPPORTED;
+  const bool want = dgamma || dbeta;
+  const size_t need = want ? sizeof(float2) * (size_t)pl.grid * (size_t)N : 0;
+  if (want && (!workspace || workspace_bytes < need || !a16(workspace))) return GN_ERR_WORKSPACE;
+  RowParams p{};
+  p.x = x;
+  p.dy = dy;
+  p.out = dx;
+  p.gamma = gamma;
+  p.mean = const_cast<float*>(mean);
+  p.rstd = const_cast<float*>(rstd);
+  p.dgamma = dgamma;
+  p.dbeta = dbeta;
+  p.part = static_cast<float2*>(workspace);
+  p.M = M;
+  p.N = N;
+  p.V = pl.V;
+  p.tw = pl.tw;
+  p.want_part = want ? 1 : 0;
+  const void* fn = kernel_of(pl, dtype, rms, true);
+  if (pl.smem > 48 * 1024) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
+    if (e != cudaSuccess) return GN_ERR_CUDA;
+  }
+  void* args[] = {&p};
+  cudaError_t e = cudaLaunchKernel(fn, dim3((unsigned)pl.grid), dim3(kRowThreads), args,
+                                   want ? pl.smem : 0, s);
+  if (e != cudaSuccess || !want) return fail(e);
+  // the column kernel, launched early (programmatic dependent launch): it
+  // waits for the row kernel's records before reading them
+  int64_t P = pl.grid;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)cdiv64(N, 32), 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return fail(cudaLaunchKernelEx(&cfg, row_col_reduce, p, P));
+}
+
+}  // namespace
+}  // namespace gn
+
+extern "C" {
+
+size_t ln_workspace_size(int64_t M, int64_t N, int dtype) {
+  if (M <= 0 || N <= 0 || (dtype != gn::kF32 && dtype != gn::kF16 && dtype != gn::kBF16)) return 0;
+  size_t best = 0;
+  for (int rms = 0; rms < 2; ++rms)
+    for (int a = 0; a < 2; ++a) {
+      const gn::RowPlan pl = gn::row_plan(M, N, dtype, rms != 0, true, a != 0);
+      if (pl.ok) best = std::max(best, sizeof(float2) * (size_t)pl.grid * (size_t)N);
+    }
+  return best;
+}
+
+int ln_fwd(const void* x, int64_t M, int64_t N, int dtype, const float* gamma, const float* beta,
+           float eps, void* y, float* mean, float* rstd, void* stream) {
+  return gn::run_fwd(x, M, N, dtype, gamma, beta, eps, y, mean, rstd, stream, false);
+}
+
+int ln_bwd(const void* dy, const void* x, const float* mean, const float* rstd,
+           const float* gamma, int64_t M, int64_t N, int dtype, void* dx, float* dgamma,
+           float* dbeta, void* workspace, size_t workspace_bytes, void* stream) {
+  return gn::run_bwd(dy, x, mean, rstd, gamma, M, N, dtype, dx, dgamma, dbeta, workspace,
+                     workspace_bytes, stream, false);
+}
+
+int rms_fwd(const void* x, int64_t M, int64_t N, int dtype, const float* gamma, float eps,
+            void* y, float* rstd, void* stream) {
+  return gn::run_fwd(x, M, N, dtype, gamma, nullptr, eps, y, nullptr, rstd, stream, true);
+}
+
+int rms_bwd(const void* dy, const void* x, const float* rstd, const float* gamma, int64_t M,
+            int64_t N, int dtype, void* dx, float* dgamma, void* workspace,
+            size_t workspace_bytes, void* stream) {
+  return gn::run_bwd(dy, x, nullptr, rstd, gamma, M, N, dtype, dx, dgamma, nullptr, workspace,
+                     workspace_bytes, stream, true);
+}
+
+}  // extern "C"

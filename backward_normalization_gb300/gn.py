@@ -76,6 +76,18 @@ def lib() -> ctypes.CDLL:
         L.gn_set_regime.restype = ctypes.c_int
         L.gn_set_timing_events.argtypes = [_VP, _VP, _VP]
         L.gn_set_timing_events.restype = ctypes.c_int
+        # LayerNorm / RMSNorm over rows (include/ln.h)
+        L.ln_workspace_size.argtypes = [_I64, _I64, ctypes.c_int]
+        L.ln_workspace_size.restype = ctypes.c_size_t
+        L.ln_fwd.argtypes = [_VP, _I64, _I64, ctypes.c_int, _VP, _VP, ctypes.c_float, _VP, _VP,
+                             _VP, _VP]
+        L.ln_bwd.argtypes = [_VP, _VP, _VP, _VP, _VP, _I64, _I64, ctypes.c_int, _VP, _VP, _VP,
+                             _VP, ctypes.c_size_t, _VP]
+        L.rms_fwd.argtypes = [_VP, _I64, _I64, ctypes.c_int, _VP, ctypes.c_float, _VP, _VP, _VP]
+        L.rms_bwd.argtypes = [_VP, _VP, _VP, _VP, _I64, _I64, ctypes.c_int, _VP, _VP, _VP,
+                              ctypes.c_size_t, _VP]
+        for f in (L.ln_fwd, L.ln_bwd, L.rms_fwd, L.rms_bwd):
+            f.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -200,3 +212,85 @@ def backward(dy, x, mean, rstd, N, C, HW, G, layout, gamma=None, workspace=None,
     if rc != GN_OK:
         raise GnError(rc, "gn_bwd")
     return dx, dgamma, dbeta
+
+
+# ------------------------------------------------ LayerNorm / RMSNorm over rows
+def ln_workspace_size(M, N, dtype) -> int:
+    dt = DTYPE[dtype] if isinstance(dtype, torch.dtype) else (
+        DTYPE_NAME[dtype] if isinstance(dtype, str) else int(dtype))
+    return int(lib().ln_workspace_size(M, N, dt))
+
+
+def ln_fwd_raw(x, M, N, gamma, beta, eps, y, mean, rstd, stream=None) -> int:
+    return lib().ln_fwd(_ptr(x), M, N, DTYPE[x.dtype], _ptr(gamma), _ptr(beta), float(eps),
+                        _ptr(y), _ptr(mean), _ptr(rstd), _stream(stream))
+
+
+def ln_bwd_raw(dy, x, mean, rstd, gamma, M, N, dx, dgamma, dbeta, workspace, stream=None) -> int:
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    return lib().ln_bwd(_ptr(dy), _ptr(x), _ptr(mean), _ptr(rstd), _ptr(gamma), M, N,
+                        DTYPE[x.dtype], _ptr(dx), _ptr(dgamma), _ptr(dbeta), _ptr(workspace),
+                        ws_bytes, _stream(stream))
+
+
+def rms_fwd_raw(x, M, N, gamma, eps, y, rstd, stream=None) -> int:
+    return lib().rms_fwd(_ptr(x), M, N, DTYPE[x.dtype], _ptr(gamma), float(eps), _ptr(y),
+                         _ptr(rstd), _stream(stream))
+
+
+def rms_bwd_raw(dy, x, rstd, gamma, M, N, dx, dgamma, workspace, stream=None) -> int:
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    return lib().rms_bwd(_ptr(dy), _ptr(x), _ptr(rstd), _ptr(gamma), M, N, DTYPE[x.dtype],
+                         _ptr(dx), _ptr(dgamma), _ptr(workspace), ws_bytes, _stream(stream))
+
+
+def _row_ws(M, N, dtype, device):
+    n = ln_workspace_size(M, N, dtype)
+    return torch.empty(max(n, 16), dtype=torch.uint8, device=device)
+
+
+def ln_forward(x, M, N, gamma=None, beta=None, eps=1e-5, stream=None):
+    """LayerNorm over rows of x [M, N] (flat); returns (y, mean, rstd)."""
+    y = torch.empty_like(x)
+    mean = torch.empty(M, dtype=torch.float32, device=x.device)
+    rstd = torch.empty(M, dtype=torch.float32, device=x.device)
+    rc = ln_fwd_raw(x, M, N, gamma, beta, eps, y, mean, rstd, stream)
+    if rc != GN_OK:
+        raise GnError(rc, "ln_fwd")
+    return y, mean, rstd
+
+
+def ln_backward(dy, x, mean, rstd, M, N, gamma=None, want=(True, True), workspace=None,
+                stream=None):
+    """LayerNorm backward; returns (dx, dgamma or None, dbeta or None)."""
+    dx = torch.empty_like(x)
+    dg = torch.empty(N, dtype=torch.float32, device=x.device) if want[0] else None
+    db = torch.empty(N, dtype=torch.float32, device=x.device) if want[1] else None
+    if workspace is None:
+        workspace = _row_ws(M, N, x.dtype, x.device)
+    rc = ln_bwd_raw(dy, x, mean, rstd, gamma, M, N, dx, dg, db, workspace, stream)
+    if rc != GN_OK:
+        raise GnError(rc, "ln_bwd")
+    return dx, dg, db
+
+
+def rms_forward(x, M, N, gamma=None, eps=1e-5, stream=None):
+    """RMSNorm over rows of x [M, N] (flat); returns (y, rstd)."""
+    y = torch.empty_like(x)
+    rstd = torch.empty(M, dtype=torch.float32, device=x.device)
+    rc = rms_fwd_raw(x, M, N, gamma, eps, y, rstd, stream)
+    if rc != GN_OK:
+        raise GnError(rc, "rms_fwd")
+    return y, rstd
+
+
+def rms_backward(dy, x, rstd, M, N, gamma=None, want_dgamma=True, workspace=None, stream=None):
+    """RMSNorm backward; returns (dx, dgamma or None)."""
+    dx = torch.empty_like(x)
+    dg = torch.empty(N, dtype=torch.float32, device=x.device) if want_dgamma else None
+    if workspace is None:
+        workspace = _row_ws(M, N, x.dtype, x.device)
+    rc = rms_bwd_raw(dy, x, rstd, gamma, M, N, dx, dg, workspace, stream)
+    if rc != GN_OK:
+        raise GnError(rc, "rms_bwd")
+    return dx, dg

@@ -116,3 +116,49 @@ def to_nchw_view(flat: torch.Tensor, w: Workload) -> torch.Tensor:
     if w.layout == "nchw":
         return flat.view(w.N, w.C, w.HW)
     return flat.view(w.N, w.HW, w.C).permute(0, 2, 1)
+
+
+# ------------------------------------------------ rows: LayerNorm / RMSNorm
+@dataclasses.dataclass(frozen=True)
+class RowWorkload:
+    """A row-normalization problem over the last dimension of [M, N].  The
+    shapes are those of the ROCm normalization-backward benchmark table
+    (M = product of the leading dimensions); the page gives no value
+    distributions, so x, dy ~ N(0, 1), gamma ~ N(1, 0.1), beta ~ N(0, 0.1)."""
+    name: str
+    op: str       # "ln" | "rms"
+    dtype: str    # "f32" | "f16" | "bf16"
+    M: int
+    N: int
+    eps: float = 1e-5
+
+    @property
+    def E(self) -> int:
+        return self.M * self.N
+
+
+ROW_WORKLOADS = [
+    RowWorkload("ln_f16_4096x1024", "ln", "f16", 4096, 1024),
+    RowWorkload("ln_bf16_4096x1024", "ln", "bf16", 4096, 1024),
+    RowWorkload("ln_f32_4096x1024", "ln", "f32", 4096, 1024),
+    RowWorkload("ln_f16_1024x768", "ln", "f16", 1024, 768),
+    RowWorkload("ln_f16_131072x64", "ln", "f16", 131072, 64),
+    RowWorkload("ln_bf16_131072x4096", "ln", "bf16", 32 * 4096, 4096),
+    RowWorkload("ln_f16_8192x768", "ln", "f16", 8 * 1024, 768),
+    RowWorkload("rms_f16_4096x1024", "rms", "f16", 4096, 1024),
+    RowWorkload("rms_bf16_131072x4096", "rms", "bf16", 32 * 4096, 4096),
+    RowWorkload("rms_f16_131072x64", "rms", "f16", 131072, 64),
+]
+ROW_BY_NAME = {w.name: w for w in ROW_WORKLOADS}
+
+
+def make_row_inputs(w: RowWorkload, device="cpu", seed: int = 0):
+    """dict(x, dy, gamma, beta): x/dy flat [M*N] in w.dtype; gamma/beta fp32 [N].
+    Draw order: x, dy, gamma, beta."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    x = _draw(("normal", 0.0, 1.0), w.E, gen, device).to(DTYPES[w.dtype])
+    dy = _draw(("normal", 0.0, 1.0), w.E, gen, device).to(DTYPES[w.dtype])
+    gamma = _draw(("normal", 1.0, 0.1), w.N, gen, device)
+    beta = _draw(("normal", 0.0, 0.1), w.N, gen, device)
+    return {"x": x, "dy": dy, "gamma": gamma, "beta": beta}
