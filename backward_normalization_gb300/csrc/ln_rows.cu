@@ -10,9 +10,9 @@
 // bits: each pairwise add is commutative) or, for teams wider than a warp,
 // per-warp butterflies added in warp order through shared memory.
 //
-//   forward:  load the row, mean (LayerNorm), sum of squared deviations (a
-//             second pass over the registers), rstd, then y; one read of x,
-//             one write of y.
+//   forward:  load the row, shifted sums of x and x^2 (one team reduction),
+//             mean and biased variance, rstd, then y; one read of x, one
+//             write of y.
 //   backward: load x and dy rows, xhat and g = gamma*dy, the two row sums,
 //             dx; dgamma/dbeta partials stay in registers across the CTA's
 //             rows.  The CTA then adds its teams' partials in team order into
@@ -54,20 +54,29 @@ struct RowParams {
   int want_part;    // backward: 1 if any parameter gradient is wanted
 };
 
-// Sum over the team of `v` (TW a power of two).  Every thread of the CTA must
-// call it the same number of times; `red` holds blockDim/32 floats.
-__device__ __forceinline__ float team_sum(float v, int tw, float* red) {
+// Sum over the team of the pair (a, b) (TW a power of two), one exchange for
+// both; `red` holds blockDim/16 floats.  Same calling rule as team_sum.
+__device__ __forceinline__ float2 team_sum2(float a, float b, int tw, float* red) {
   const int w = tw < 32 ? tw : 32;
-  for (int o = w >> 1; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  if (tw <= 32) return v;
+  for (int o = w >> 1; o > 0; o >>= 1) {
+    a += __shfl_xor_sync(0xffffffffu, a, o);
+    b += __shfl_xor_sync(0xffffffffu, b, o);
+  }
+  if (tw <= 32) return make_float2(a, b);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (lane == 0) red[warp] = v;
+  if (lane == 0) {
+    red[2 * warp] = a;
+    red[2 * warp + 1] = b;
+  }
   __syncthreads();
   const int first = (threadIdx.x / tw) * (tw >> 5);
-  float s = 0.f;
-  for (int k = 0; k < (tw >> 5); ++k) s += red[first + k];
+  float sa = 0.f, sb = 0.f;
+  for (int k = 0; k < (tw >> 5); ++k) {
+    sa += red[2 * (first + k)];
+    sb += red[2 * (first + k) + 1];
+  }
   __syncthreads();
-  return s;
+  return make_float2(sa, sb);
 }
 
 // gamma / beta for one vector of features (fp32, VW wide).
@@ -97,63 +106,84 @@ __device__ __forceinline__ void load_param(const float* p, int64_t c0, float dfl
 // ------------------------------------------------------------------ forward
 template <typename T, int VW, int VPT, bool kRms>
 __global__ void __launch_bounds__(kRowThreads) row_fwd(const __grid_constant__ RowParams p) {
-  __shared__ float red[kRowThreads / 32];
+  __shared__ float red[kRowThreads / 16];
   const int tw = p.tw, team = threadIdx.x / tw, lane = threadIdx.x % tw;
   const int nteams = blockDim.x / tw;
   const float inv_n = 1.0f / (float)p.N;
   const T* x = static_cast<const T*>(p.x);
   T* y = static_cast<T*>(p.out);
   const uint64_t pol = policy_evict_first();
-  for (int64_t r0 = (int64_t)blockIdx.x * nteams; r0 < p.M; r0 += (int64_t)gridDim.x * nteams) {
+  // rows are software-pipelined: the next row's vectors are requested before
+  // the current row's reductions, so two rows per team are in flight
+  using Raw = typename Access<T, VW>::Raw;
+  Raw cur[VPT], nxt[VPT];
+  T kcur{}, knxt{};  // LayerNorm: the row's first element (the shift), fetched with the row
+  const int64_t step = (int64_t)gridDim.x * nteams;
+  auto fetch = [&](int64_t r0, Raw (&buf)[VPT], T& kb) {
+    const int64_t row = r0 + team;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int64_t vi = lane + (int64_t)k * tw;
+      buf[k] = (row < p.M && vi < p.V) ? Access<T, VW>::load_raw(x + row * p.N + vi * VW, pol) : Raw{};
+    }
+    if (!kRms && row < p.M) kb = __ldg(x + row * p.N);
+  };
+  int64_t r0 = (int64_t)blockIdx.x * nteams;
+  if (r0 < p.M) fetch(r0, cur, kcur);
+  for (; r0 < p.M; r0 += step) {
+    if (r0 + step < p.M) fetch(r0 + step, nxt, knxt);
     const int64_t row = r0 + team;
     const bool act = row < p.M;
     float v[VPT][VW];
 #pragma unroll
-    for (int k = 0; k < VPT; ++k) {
-      const int64_t vi = lane + (int64_t)k * tw;
-      if (act && vi < p.V) {
-        Access<T, VW>::load(x + row * p.N + vi * VW, v[k], pol);
-      } else {
-#pragma unroll
-        for (int e = 0; e < VW; ++e) v[k][e] = 0.f;
-      }
-    }
-    float mean = 0.f;
-    if (!kRms) {
-      float s = 0.f;
-#pragma unroll
-      for (int k = 0; k < VPT; ++k)
-#pragma unroll
-        for (int e = 0; e < VW; ++e) s += v[k][e];
-      mean = team_sum(s, tw, red) * inv_n;
-    }
-    float q = 0.f;
+    for (int k = 0; k < VPT; ++k) Access<T, VW>::unpack(cur[k], v[k]);
+    // LayerNorm: shifted sums S = sum(x - K), Q = sum((x - K)^2) with K the
+    // row's first element, one team reduction for both; mean = K + S/N and
+    // var = Q/N - (S/N)^2 (exact in real arithmetic; the shift keeps the
+    // subtraction well conditioned, as for the GroupNorm statistics).
+    // RMSNorm: Q = sum(x^2).
+    const float K = kRms ? 0.f : Elem<T>::to_f(kcur);
+    float sx = 0.f, q = 0.f;
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
       const bool in = act && lane + (int64_t)k * tw < p.V;
 #pragma unroll
       for (int e = 0; e < VW; ++e) {
-        const float d = in ? v[k][e] - mean : 0.f;
+        const float d = in ? v[k][e] - K : 0.f;
+        sx += d;
         q = fmaf(d, d, q);
       }
     }
-    const float rstd = 1.0f / sqrtf(team_sum(q, tw, red) * inv_n + p.eps);
-    if (!act) continue;  // no barrier follows in this iteration
-#pragma unroll
-    for (int k = 0; k < VPT; ++k) {
-      const int64_t vi = lane + (int64_t)k * tw;
-      if (vi >= p.V) continue;
-      float gm[VW], bt[VW];
-      load_param<VW>(p.gamma, vi * VW, 1.f, gm);
-      load_param<VW>(kRms ? nullptr : p.beta, vi * VW, 0.f, bt);
-#pragma unroll
-      for (int e = 0; e < VW; ++e) v[k][e] = fmaf(v[k][e] - mean, rstd * gm[e], bt[e]);
-      Access<T, VW>::store(y + row * p.N + vi * VW, v[k], pol);
+    const float2 t = team_sum2(sx, q, tw, red);
+    float mean = 0.f, var;
+    if (kRms) {
+      var = t.y * inv_n;
+    } else {
+      const float sm = t.x * inv_n;
+      mean = K + sm;
+      var = fmaxf(fmaf(-sm, sm, t.y * inv_n), 0.f);
     }
-    if (lane == 0) {
-      if (!kRms) p.mean[row] = mean;
-      p.rstd[row] = rstd;
+    const float rstd = 1.0f / sqrtf(var + p.eps);
+    if (act) {
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) {
+        const int64_t vi = lane + (int64_t)k * tw;
+        if (vi >= p.V) continue;
+        float gm[VW], bt[VW];
+        load_param<VW>(p.gamma, vi * VW, 1.f, gm);
+        load_param<VW>(kRms ? nullptr : p.beta, vi * VW, 0.f, bt);
+#pragma unroll
+        for (int e = 0; e < VW; ++e) v[k][e] = fmaf(v[k][e] - mean, rstd * gm[e], bt[e]);
+        Access<T, VW>::store(y + row * p.N + vi * VW, v[k], pol);
+      }
+      if (lane == 0) {
+        if (!kRms) p.mean[row] = mean;
+        p.rstd[row] = rstd;
+      }
     }
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) cur[k] = nxt[k];
+    kcur = knxt;
   }
 }
 
@@ -163,7 +193,7 @@ __global__ void __launch_bounds__(kRowThreads) row_fwd(const __grid_constant__ R
 template <typename T, int VW, int VPT, bool kRms>
 __global__ void __launch_bounds__(kRowThreads) row_bwd(const __grid_constant__ RowParams p) {
   extern __shared__ float colsum[];
-  __shared__ float red[kRowThreads / 32];
+  __shared__ float red[kRowThreads / 16];
   const int tw = p.tw, team = threadIdx.x / tw, lane = threadIdx.x % tw;
   const int nteams = blockDim.x / tw;
   const float inv_n = 1.0f / (float)p.N;
@@ -176,22 +206,36 @@ __global__ void __launch_bounds__(kRowThreads) row_bwd(const __grid_constant__ R
   for (int k = 0; k < VPT; ++k)
 #pragma unroll
     for (int e = 0; e < VW; ++e) pg[k][e] = pb[k][e] = 0.f;
-  for (int64_t r0 = (int64_t)blockIdx.x * nteams; r0 < p.M; r0 += (int64_t)gridDim.x * nteams) {
+  // rows are software-pipelined: x, dy, mean and rstd of the next row are
+  // requested before the current row's reductions
+  using Raw = typename Access<T, VW>::Raw;
+  Raw cx[VPT], cd[VPT], nx[VPT], nd[VPT];
+  float cm = 0.f, cr = 0.f, nm = 0.f, nr = 0.f;  // mean, rstd of the current / next row
+  const int64_t step = (int64_t)gridDim.x * nteams;
+  auto fetch = [&](int64_t r0, Raw (&bx)[VPT], Raw (&bd)[VPT], float& m, float& r) {
     const int64_t row = r0 + team;
-    const bool act = row < p.M;
-    const float mean = (!kRms && act) ? __ldg(p.mean + row) : 0.f;
-    const float rstd = act ? __ldg(p.rstd + row) : 0.f;
-    float xv[VPT][VW], dv[VPT][VW];
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
       const int64_t vi = lane + (int64_t)k * tw;
-      if (act && vi < p.V) {
-        Access<T, VW>::load(x + row * p.N + vi * VW, xv[k], pol);
-        Access<T, VW>::load(dy + row * p.N + vi * VW, dv[k], pol);
-      } else {
+      const bool in = row < p.M && vi < p.V;
+      bx[k] = in ? Access<T, VW>::load_raw(x + row * p.N + vi * VW, pol) : Raw{};
+      bd[k] = in ? Access<T, VW>::load_raw(dy + row * p.N + vi * VW, pol) : Raw{};
+    }
+    m = (!kRms && row < p.M) ? __ldg(p.mean + row) : 0.f;
+    r = row < p.M ? __ldg(p.rstd + row) : 0.f;
+  };
+  int64_t r0 = (int64_t)blockIdx.x * nteams;
+  if (r0 < p.M) fetch(r0, cx, cd, cm, cr);
+  for (; r0 < p.M; r0 += step) {
+    if (r0 + step < p.M) fetch(r0 + step, nx, nd, nm, nr);
+    const int64_t row = r0 + team;
+    const bool act = row < p.M;
+    const float mean = cm, rstd = cr;
+    float xv[VPT][VW], dv[VPT][VW];
 #pragma unroll
-        for (int e = 0; e < VW; ++e) xv[k][e] = dv[k][e] = 0.f;
-      }
+    for (int k = 0; k < VPT; ++k) {
+      Access<T, VW>::unpack(cx[k], xv[k]);
+      Access<T, VW>::unpack(cd[k], dv[k]);
     }
     // xhat in xv, g = gamma*dy kept apart from dy (both are needed)
     float s1 = 0.f, s2 = 0.f;
@@ -208,24 +252,33 @@ __global__ void __launch_bounds__(kRowThreads) row_bwd(const __grid_constant__ R
         s2 = fmaf(g, xv[k][e], s2);
       }
     }
-    const float c1 = kRms ? 0.f : team_sum(s1, tw, red) * inv_n;
-    const float c2 = team_sum(s2, tw, red) * inv_n;
-    if (!act) continue;  // no barrier follows in this iteration
+    const float2 cs = team_sum2(s1, s2, tw, red);
+    const float c1 = kRms ? 0.f : cs.x * inv_n;
+    const float c2 = cs.y * inv_n;
+    if (act) {
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) {
+        const int64_t vi = lane + (int64_t)k * tw;
+        if (vi >= p.V) continue;
+        float gm[VW], o[VW];
+        load_param<VW>(p.gamma, vi * VW, 1.f, gm);
+#pragma unroll
+        for (int e = 0; e < VW; ++e) {
+          const float g = gm[e] * dv[k][e];
+          o[e] = rstd * (g - c1 - xv[k][e] * c2);
+          pg[k][e] = fmaf(dv[k][e], xv[k][e], pg[k][e]);
+          pb[k][e] += dv[k][e];
+        }
+        Access<T, VW>::store(dx + row * p.N + vi * VW, o, pol);
+      }
+    }
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
-      const int64_t vi = lane + (int64_t)k * tw;
-      if (vi >= p.V) continue;
-      float gm[VW], o[VW];
-      load_param<VW>(p.gamma, vi * VW, 1.f, gm);
-#pragma unroll
-      for (int e = 0; e < VW; ++e) {
-        const float g = gm[e] * dv[k][e];
-        o[e] = rstd * (g - c1 - xv[k][e] * c2);
-        pg[k][e] = fmaf(dv[k][e], xv[k][e], pg[k][e]);
-        pb[k][e] += dv[k][e];
-      }
-      Access<T, VW>::store(dx + row * p.N + vi * VW, o, pol);
+      cx[k] = nx[k];
+      cd[k] = nd[k];
     }
+    cm = nm;
+    cr = nr;
   }
   if (!p.want_part) return;
   // the teams' partials -> shared memory -> one record per feature, in team order
