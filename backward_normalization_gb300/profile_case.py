@@ -26,7 +26,10 @@ from . import gn, synth
 
 def main(argv=None) -> int:
     ap = argparse.ArgumentParser()
-    ap.add_argument("--workload", required=True, choices=[w.name for w in synth.WORKLOADS])
+    ap.add_argument("--workload", choices=[w.name for w in synth.WORKLOADS])
+    ap.add_argument("--row-workload", choices=[w.name for w in synth.ROW_WORKLOADS],
+                    help="a LayerNorm / RMSNorm row workload instead (--M overrides its rows)")
+    ap.add_argument("--M", type=int)
     ap.add_argument("--N", type=int)
     ap.add_argument("--H", type=int)
     ap.add_argument("--W", type=int)
@@ -34,6 +37,10 @@ def main(argv=None) -> int:
     ap.add_argument("--regime", choices=["auto", "two_kernel", "resident", "pipelined"],
                     default="auto")
     a = ap.parse_args(argv)
+    if a.row_workload:
+        return run_rows(a)
+    if not a.workload:
+        ap.error("--workload or --row-workload is required")
     w = synth.BY_NAME[a.workload]
     over = {k: v for k, v in (("N", a.N), ("H", a.H), ("W", a.W)) if v is not None}
     if over:
@@ -62,6 +69,25 @@ def main(argv=None) -> int:
     pb = gn.plan_info(gn.OP_BWD, w.N, w.C, w.HW, w.G, w.layout, w.dtype)
     print(f"{w.name} N={w.N} H={w.H} W={w.W}: {a.calls} calls, fwd launches {pf.launches} "
           f"(ctas {pf.ctas}), bwd launches {pb.launches} (ctas {pb.ctas})")
+    return 0
+
+
+def run_rows(a) -> int:
+    """One row workload's forward then backward, --calls times."""
+    w = synth.ROW_BY_NAME[a.row_workload]
+    if a.M:
+        w = synth.RowWorkload(w.name, w.op, w.dtype, a.M, w.N, w.eps)
+    inp = synth.make_row_inputs(w, "cuda", seed=0)
+    x, dy, gm, bt = inp["x"], inp["dy"], inp["gamma"], inp["beta"]
+    for _ in range(a.calls):
+        if w.op == "ln":
+            y, mean, rstd = gn.ln_forward(x, w.M, w.N, gm, bt, w.eps)
+            gn.ln_backward(dy, x, mean, rstd, w.M, w.N, gm)
+        else:
+            y, rstd = gn.rms_forward(x, w.M, w.N, gm, w.eps)
+            gn.rms_backward(dy, x, rstd, w.M, w.N, gm)
+    torch.cuda.synchronize()
+    print(f"{w.name} M={w.M} N={w.N}: {a.calls} calls")
     return 0
 
 
