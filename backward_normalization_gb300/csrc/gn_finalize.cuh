@@ -244,9 +244,8 @@ __device__ __forceinline__ Unit unit_of(const KParams& p, int64_t n, int64_t c) 
 // (l1 > 1) the CTA arrives on its group's counter; the group's last CTA runs
 // merge() (the group record from its item records, in item order) and
 // arrives on the unit's counter.  The unit's last arrival runs its
-// finalisation (and raises the unit's ready flag); in the backward, the last
-// unit then runs the parameter-gradient step.  Every counter is reset by the
-// CTA that completed it.  Must be reached by all threads of the CTA.
+// finalisation (and raises the unit's ready flag).  Every counter is reset by
+// the CTA that completed it.  Must be reached by all threads of the CTA.
 template <typename T, bool kBwd, typename Merge>
 __device__ __forceinline__ void arrive_and_finalize(const KParams& p, const Unit& un,
                                                     int64_t group1, unsigned gsize, Merge merge,
@@ -276,12 +275,8 @@ __device__ __forceinline__ void arrive_and_finalize(const KParams& p, const Unit
     atomicExch(un.ticket, 0u);
     if (un.ready) atomicExch(un.ready, 1u);
   }
-  if (!kBwd) return;
-  if (threadIdx.x == 0) s_last = publish_and_arrive(p.tickets + p.g.units_fin, (unsigned)p.g.units_fin);
-  __syncthreads();
-  if (!s_last) return;
-  finalize_params(p, sm);
-  if (threadIdx.x == 0) atomicExch(p.tickets + p.g.units_fin, 0u);
+  // the backward's dgamma / dbeta are added up by the dx kernel, whose first
+  // CTA finds every channel's sums complete when it starts
 }
 
 }  // namespace gn

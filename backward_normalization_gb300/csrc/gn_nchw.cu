@@ -371,8 +371,12 @@ __global__ void __launch_bounds__(512) nchw_bwd_reduce(const __grid_constant__ K
 
 template <typename T, int VW>
 __global__ void __launch_bounds__(512) nchw_bwd_dx(const __grid_constant__ KParams p) {
+  extern __shared__ float sm[];
   grid_dependency_wait();
   grid_launch_dependents();
+  // the first CTA also adds up dgamma / dbeta: every channel's sums are
+  // complete once the first kernel is
+  if (blockIdx.x == 0) finalize_params(p, sm);
   const int64_t item = p.g.items - 1 - (int64_t)blockIdx.x;
   if (p.g.mode == 0)
     dx_chunk<T, VW>(p, item);
@@ -541,7 +545,7 @@ cudaError_t run_op(const KParams& p, cudaStream_t s, bool bwd) {
                       : launch_pdl(nchw_fwd_stats<T, VW>, g.items, g.tpb, sm1, s, p);
   if (e != cudaSuccess) return e;
   if (ev.mid) cudaEventRecord(ev.mid, s);
-  e = bwd ? launch_pdl(nchw_bwd_dx<T, VW>, g.items, g.tpb, 0, s, p)
+  e = bwd ? launch_pdl(nchw_bwd_dx<T, VW>, g.items, g.tpb, sizeof(float) * 2 * g.tpb, s, p)
           : launch_pdl(nchw_fwd_apply<T, VW>, g.items, g.tpb, 0, s, p);
   if (ev.end) cudaEventRecord(ev.end, s);
   return e;
@@ -554,7 +558,7 @@ cudaError_t dispatch_vw(const KParams& p, cudaStream_t s, bool bwd) {
 
 template <typename T, int VW>
 const void* kernel_t(const Geom& g, bool bwd, int second, size_t* smem) {
-  *smem = second ? 0 : sizeof(float) * nchw_smem_floats(g);
+  *smem = second ? (bwd ? sizeof(float) * 2 * g.tpb : 0) : sizeof(float) * nchw_smem_floats(g);
   if (second) return bwd ? (const void*)nchw_bwd_dx<T, VW> : (const void*)nchw_fwd_apply<T, VW>;
   return bwd ? (const void*)nchw_bwd_reduce<T, VW> : (const void*)nchw_fwd_stats<T, VW>;
 }

@@ -328,8 +328,12 @@ __global__ void __launch_bounds__(512, 2) nhwc_fwd_apply(const __grid_constant__
 
 template <typename T, int VW, int NG>
 __global__ void __launch_bounds__(512, 2) nhwc_bwd_dx(const __grid_constant__ KParams p) {
+  extern __shared__ float sm[];
   grid_dependency_wait();
   grid_launch_dependents();
+  // the first CTA also adds up dgamma / dbeta: every channel's sums are
+  // complete once the first kernel is
+  if (blockIdx.x == 0) finalize_params(p, sm);
   dx_item<T, VW, NG>(p, p.g.items - 1 - (int64_t)blockIdx.x);
 }
 
@@ -343,7 +347,7 @@ cudaError_t run_op(const KParams& p, cudaStream_t s, bool bwd) {
                       : launch_pdl(nhwc_fwd_stats<T, VW>, g.items, g.tpb, sm1, s, p);
   if (e != cudaSuccess) return e;
   if (ev.mid) cudaEventRecord(ev.mid, s);
-  e = bwd ? launch_pdl(nhwc_bwd_dx<T, VW, NG>, g.items, g.tpb, 0, s, p)
+  e = bwd ? launch_pdl(nhwc_bwd_dx<T, VW, NG>, g.items, g.tpb, sizeof(float) * 2 * g.tpb, s, p)
           : launch_pdl(nhwc_fwd_apply<T, VW, NG>, g.items, g.tpb, 0, s, p);
   if (ev.end) cudaEventRecord(ev.end, s);
   return e;
@@ -358,7 +362,7 @@ cudaError_t dispatch_vw(const KParams& p, cudaStream_t s, bool bwd) {
 
 template <typename T, int VW, int NG>
 const void* kernel_t(const Geom& g, bool bwd, int second, size_t* smem) {
-  *smem = second ? 0 : sizeof(float) * 2 * VW * g.tpb;
+  *smem = second ? (bwd ? sizeof(float) * 2 * g.tpb : 0) : sizeof(float) * 2 * VW * g.tpb;
   if (second)
     return bwd ? (const void*)nhwc_bwd_dx<T, VW, NG> : (const void*)nhwc_fwd_apply<T, VW, NG>;
   return bwd ? (const void*)nhwc_bwd_reduce<T, VW, NG> : (const void*)nhwc_fwd_stats<T, VW>;

@@ -466,7 +466,7 @@ Geom plan_geom(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout, 
     plan_resident(g, op);
   }
   const int64_t pipe = g.regime == kRegimePipelined ? 2 * g.units_fin + 3 : 0;
-  g.counters = g.regime == kRegimeResident ? 0 : g.units_fin + 1 + g.groups1 + pipe;
+  g.counters = g.units_fin + 1 + g.groups1 + pipe;  // resident: units_fin = N, groups1 = 0
   return g;
 }
 
