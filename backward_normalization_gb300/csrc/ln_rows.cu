@@ -49,6 +49,7 @@ struct RowParams {
   float* dbeta;
   float2* part;  // backward: [grid][N] (dgamma, dbeta) partials
   int64_t M, N, V;  // V: vectors per row
+  int64_t ldx, ldd, ldo;  // row strides (elements) of x, dy and the output
   int tw;           // team width
   float eps;
   int want_part;    // backward: 1 if any parameter gradient is wanted
@@ -124,9 +125,9 @@ __global__ void __launch_bounds__(kRowThreads) row_fwd(const __grid_constant__ R
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
       const int64_t vi = lane + (int64_t)k * tw;
-      buf[k] = (row < p.M && vi < p.V) ? Access<T, VW>::load_raw(x + row * p.N + vi * VW, pol) : Raw{};
+      buf[k] = (row < p.M && vi < p.V) ? Access<T, VW>::load_raw(x + row * p.ldx + vi * VW, pol) : Raw{};
     }
-    if (!kRms && row < p.M) kb = __ldg(x + row * p.N);
+    if (!kRms && row < p.M) kb = __ldg(x + row * p.ldx);
   };
   int64_t r0 = (int64_t)blockIdx.x * nteams;
   if (r0 < p.M) fetch(r0, cur, kcur);
@@ -174,7 +175,7 @@ __global__ void __launch_bounds__(kRowThreads) row_fwd(const __grid_constant__ R
         load_param<VW>(kRms ? nullptr : p.beta, vi * VW, 0.f, bt);
 #pragma unroll
         for (int e = 0; e < VW; ++e) v[k][e] = fmaf(v[k][e] - mean, rstd * gm[e], bt[e]);
-        Access<T, VW>::store(y + row * p.N + vi * VW, v[k], pol);
+        Access<T, VW>::store(y + row * p.ldo + vi * VW, v[k], pol);
       }
       if (lane == 0) {
         if (!kRms) p.mean[row] = mean;
@@ -218,8 +219,8 @@ __global__ void __launch_bounds__(kRowThreads) row_bwd(const __grid_constant__ R
     for (int k = 0; k < VPT; ++k) {
       const int64_t vi = lane + (int64_t)k * tw;
       const bool in = row < p.M && vi < p.V;
-      bx[k] = in ? Access<T, VW>::load_raw(x + row * p.N + vi * VW, pol) : Raw{};
-      bd[k] = in ? Access<T, VW>::load_raw(dy + row * p.N + vi * VW, pol) : Raw{};
+      bx[k] = in ? Access<T, VW>::load_raw(x + row * p.ldx + vi * VW, pol) : Raw{};
+      bd[k] = in ? Access<T, VW>::load_raw(dy + row * p.ldd + vi * VW, pol) : Raw{};
     }
     m = (!kRms && row < p.M) ? __ldg(p.mean + row) : 0.f;
     r = row < p.M ? __ldg(p.rstd + row) : 0.f;
@@ -269,7 +270,7 @@ __global__ void __launch_bounds__(kRowThreads) row_bwd(const __grid_constant__ R
           pg[k][e] = fmaf(dv[k][e], xv[k][e], pg[k][e]);
           pb[k][e] += dv[k][e];
         }
-        Access<T, VW>::store(dx + row * p.N + vi * VW, o, pol);
+        Access<T, VW>::store(dx + row * p.ldo + vi * VW, o, pol);
       }
     }
 #pragma unroll
@@ -434,7 +435,7 @@ int64_t resident(const void* fn, size_t smem) {
 RowPlan row_plan(int64_t M, int64_t N, int dtype, bool rms, bool bwd, bool aligned) {
   RowPlan pl;
   const int esz = dtype == kF32 ? 4 : 2;
-  pl.vw = (aligned && (N * esz) % 16 == 0) ? 16 / esz : 1;
+  pl.vw = (aligned && (N * esz) % 16 == 0) ? 16 / esz : 1;  // aligned: bases and strides
   pl.V = N / pl.vw;
   const int cap = bwd ? 16 : 32;
   int vmax = cap / pl.vw;
@@ -468,18 +469,28 @@ int fail(cudaError_t e) {
   return e == cudaSuccess ? GN_OK : GN_ERR_CUDA;
 }
 
-int run_fwd(const void* x, int64_t M, int64_t N, int dtype, const float* gamma, const float* beta,
-            float eps, void* y, float* mean, float* rstd, void* stream, bool rms) {
+// Bytes spanned by M rows of N elements, `ld` elements apart.
+size_t span(int64_t M, int64_t N, int64_t ld, int esz) {
+  return ((size_t)(M - 1) * (size_t)ld + (size_t)N) * (size_t)esz;
+}
+
+bool stride_ok(int64_t ld, int esz) { return (ld * esz) % 16 == 0; }
+
+int run_fwd(const void* x, int64_t ldx, int64_t M, int64_t N, int dtype, const float* gamma,
+            const float* beta, float eps, void* y, int64_t ldy, float* mean, float* rstd,
+            void* stream, bool rms) {
   if (dtype != kF32 && dtype != kF16 && dtype != kBF16) return GN_ERR_UNSUPPORTED;
-  if (M < 0 || N <= 0 || !(eps >= 0.f)) return GN_ERR_INVALID;
+  if (M < 0 || N <= 0 || !(eps >= 0.f) || ldx < N || ldy < N) return GN_ERR_INVALID;
   if (M == 0) return GN_OK;
   if (!x || !y || !rstd || (!rms && !mean)) return GN_ERR_INVALID;
-  const size_t bytes = (size_t)M * (size_t)N * (dtype == kF32 ? 4 : 2);
-  if (y != x && overlaps(y, bytes, x, bytes)) return GN_ERR_INVALID;
-  if (overlaps(rstd, sizeof(float) * M, y, bytes) || overlaps(mean, sizeof(float) * M, y, bytes) ||
+  const int esz = dtype == kF32 ? 4 : 2;
+  const size_t bx = span(M, N, ldx, esz), by = span(M, N, ldy, esz);
+  if (y == x ? ldy != ldx : overlaps(y, by, x, bx)) return GN_ERR_INVALID;
+  if (overlaps(rstd, sizeof(float) * M, y, by) || overlaps(mean, sizeof(float) * M, y, by) ||
       overlaps(mean, sizeof(float) * M, rstd, sizeof(float) * M))
     return GN_ERR_INVALID;
-  const bool aligned = a16(x) && a16(y) && (!gamma || a16(gamma)) && (!beta || a16(beta));
+  const bool aligned = a16(x) && a16(y) && (!gamma || a16(gamma)) && (!beta || a16(beta)) &&
+                       stride_ok(ldx, esz) && stride_ok(ldy, esz);
   const RowPlan pl = row_plan(M, N, dtype, rms, false, aligned);
   if (!pl.ok) return GN_ERR_UNSUPPORTED;
   RowParams p{};
@@ -492,6 +503,8 @@ int run_fwd(const void* x, int64_t M, int64_t N, int dtype, const float* gamma, 
   p.M = M;
   p.N = N;
   p.V = pl.V;
+  p.ldx = ldx;
+  p.ldo = ldy;
   p.tw = pl.tw;
   p.eps = eps;
   const void* fn = kernel_of(pl, dtype, rms, false);
@@ -500,11 +513,12 @@ int run_fwd(const void* x, int64_t M, int64_t N, int dtype, const float* gamma, 
                                static_cast<cudaStream_t>(stream)));
 }
 
-int run_bwd(const void* dy, const void* x, const float* mean, const float* rstd,
-            const float* gamma, int64_t M, int64_t N, int dtype, void* dx, float* dgamma,
-            float* dbeta, void* workspace, size_t workspace_bytes, void* stream, bool rms) {
+int run_bwd(const void* dy, int64_t ldd, const void* x, int64_t ldx, const float* mean,
+            const float* rstd, const float* gamma, int64_t M, int64_t N, int dtype, void* dx,
+            int64_t ldo, float* dgamma, float* dbeta, void* workspace, size_t workspace_bytes,
+            void* stream, bool rms) {
   if (dtype != kF32 && dtype != kF16 && dtype != kBF16) return GN_ERR_UNSUPPORTED;
-  if (M < 0 || N <= 0) return GN_ERR_INVALID;
+  if (M < 0 || N <= 0 || ldd < N || ldx < N || ldo < N) return GN_ERR_INVALID;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (rms) dbeta = nullptr;
   if (M == 0) {  // empty sums
@@ -513,14 +527,16 @@ int run_bwd(const void* dy, const void* x, const float* mean, const float* rstd,
     return GN_OK;
   }
   if (!dy || !x || !rstd || !dx || (!rms && !mean)) return GN_ERR_INVALID;
-  const size_t bytes = (size_t)M * (size_t)N * (dtype == kF32 ? 4 : 2);
-  if (dx != dy && overlaps(dx, bytes, dy, bytes)) return GN_ERR_INVALID;
-  if (overlaps(dx, bytes, x, bytes)) return GN_ERR_INVALID;
+  const int esz = dtype == kF32 ? 4 : 2;
+  const size_t bd = span(M, N, ldd, esz), bx = span(M, N, ldx, esz), bo = span(M, N, ldo, esz);
+  if (dx == dy ? ldo != ldd : overlaps(dx, bo, dy, bd)) return GN_ERR_INVALID;
+  if (overlaps(dx, bo, x, bx)) return GN_ERR_INVALID;
   const size_t nb = sizeof(float) * (size_t)N;
-  if (overlaps(dgamma, nb, dx, bytes) || overlaps(dbeta, nb, dx, bytes) ||
+  if (overlaps(dgamma, nb, dx, bo) || overlaps(dbeta, nb, dx, bo) ||
       overlaps(dgamma, nb, dbeta, nb))
     return GN_ERR_INVALID;
-  const bool aligned = a16(x) && a16(dy) && a16(dx) && (!gamma || a16(gamma));
+  const bool aligned = a16(x) && a16(dy) && a16(dx) && (!gamma || a16(gamma)) &&
+                       stride_ok(ldd, esz) && stride_ok(ldx, esz) && stride_ok(ldo, esz);
   const RowPlan pl = row_plan(M, N, dtype, rms, true, aligned);
   if (!pl.ok) return GN_ERR_UNSUPPORTED;
   const bool want = dgamma || dbeta;
@@ -539,6 +555,9 @@ int run_bwd(const void* dy, const void* x, const float* mean, const float* rstd,
   p.M = M;
   p.N = N;
   p.V = pl.V;
+  p.ldx = ldx;
+  p.ldd = ldd;
+  p.ldo = ldo;
   p.tw = pl.tw;
   p.want_part = want ? 1 : 0;
   const void* fn = kernel_of(pl, dtype, rms, true);
@@ -582,28 +601,55 @@ size_t ln_workspace_size(int64_t M, int64_t N, int dtype) {
   return best;
 }
 
+int ln_fwd_ex(const void* x, int64_t ldx, int64_t M, int64_t N, int dtype, const float* gamma,
+              const float* beta, float eps, void* y, int64_t ldy, float* mean, float* rstd,
+              void* stream) {
+  return gn::run_fwd(x, ldx, M, N, dtype, gamma, beta, eps, y, ldy, mean, rstd, stream, false);
+}
+
+int ln_bwd_ex(const void* dy, int64_t lddy, const void* x, int64_t ldx, const float* mean,
+              const float* rstd, const float* gamma, int64_t M, int64_t N, int dtype, void* dx,
+              int64_t lddx, float* dgamma, float* dbeta, void* workspace,
+              size_t workspace_bytes, void* stream) {
+  return gn::run_bwd(dy, lddy, x, ldx, mean, rstd, gamma, M, N, dtype, dx, lddx, dgamma, dbeta,
+                     workspace, workspace_bytes, stream, false);
+}
+
+int rms_fwd_ex(const void* x, int64_t ldx, int64_t M, int64_t N, int dtype, const float* gamma,
+               float eps, void* y, int64_t ldy, float* rstd, void* stream) {
+  return gn::run_fwd(x, ldx, M, N, dtype, gamma, nullptr, eps, y, ldy, nullptr, rstd, stream,
+                     true);
+}
+
+int rms_bwd_ex(const void* dy, int64_t lddy, const void* x, int64_t ldx, const float* rstd,
+               const float* gamma, int64_t M, int64_t N, int dtype, void* dx, int64_t lddx,
+               float* dgamma, void* workspace, size_t workspace_bytes, void* stream) {
+  return gn::run_bwd(dy, lddy, x, ldx, nullptr, rstd, gamma, M, N, dtype, dx, lddx, dgamma,
+                     nullptr, workspace, workspace_bytes, stream, true);
+}
+
 int ln_fwd(const void* x, int64_t M, int64_t N, int dtype, const float* gamma, const float* beta,
            float eps, void* y, float* mean, float* rstd, void* stream) {
-  return gn::run_fwd(x, M, N, dtype, gamma, beta, eps, y, mean, rstd, stream, false);
+  return ln_fwd_ex(x, N, M, N, dtype, gamma, beta, eps, y, N, mean, rstd, stream);
 }
 
 int ln_bwd(const void* dy, const void* x, const float* mean, const float* rstd,
            const float* gamma, int64_t M, int64_t N, int dtype, void* dx, float* dgamma,
            float* dbeta, void* workspace, size_t workspace_bytes, void* stream) {
-  return gn::run_bwd(dy, x, mean, rstd, gamma, M, N, dtype, dx, dgamma, dbeta, workspace,
-                     workspace_bytes, stream, false);
+  return ln_bwd_ex(dy, N, x, N, mean, rstd, gamma, M, N, dtype, dx, N, dgamma, dbeta, workspace,
+                   workspace_bytes, stream);
 }
 
 int rms_fwd(const void* x, int64_t M, int64_t N, int dtype, const float* gamma, float eps,
             void* y, float* rstd, void* stream) {
-  return gn::run_fwd(x, M, N, dtype, gamma, nullptr, eps, y, nullptr, rstd, stream, true);
+  return rms_fwd_ex(x, N, M, N, dtype, gamma, eps, y, N, rstd, stream);
 }
 
 int rms_bwd(const void* dy, const void* x, const float* rstd, const float* gamma, int64_t M,
             int64_t N, int dtype, void* dx, float* dgamma, void* workspace,
             size_t workspace_bytes, void* stream) {
-  return gn::run_bwd(dy, x, nullptr, rstd, gamma, M, N, dtype, dx, dgamma, nullptr, workspace,
-                     workspace_bytes, stream, true);
+  return rms_bwd_ex(dy, N, x, N, rstd, gamma, M, N, dtype, dx, N, dgamma, workspace,
+                    workspace_bytes, stream);
 }
 
 }  // extern "C"

@@ -86,7 +86,16 @@ def lib() -> ctypes.CDLL:
         L.rms_fwd.argtypes = [_VP, _I64, _I64, ctypes.c_int, _VP, ctypes.c_float, _VP, _VP, _VP]
         L.rms_bwd.argtypes = [_VP, _VP, _VP, _VP, _I64, _I64, ctypes.c_int, _VP, _VP, _VP,
                               ctypes.c_size_t, _VP]
-        for f in (L.ln_fwd, L.ln_bwd, L.rms_fwd, L.rms_bwd):
+        L.ln_fwd_ex.argtypes = [_VP, _I64, _I64, _I64, ctypes.c_int, _VP, _VP, ctypes.c_float,
+                                _VP, _I64, _VP, _VP, _VP]
+        L.ln_bwd_ex.argtypes = [_VP, _I64, _VP, _I64, _VP, _VP, _VP, _I64, _I64, ctypes.c_int,
+                                _VP, _I64, _VP, _VP, _VP, ctypes.c_size_t, _VP]
+        L.rms_fwd_ex.argtypes = [_VP, _I64, _I64, _I64, ctypes.c_int, _VP, ctypes.c_float, _VP,
+                                 _I64, _VP, _VP]
+        L.rms_bwd_ex.argtypes = [_VP, _I64, _VP, _I64, _VP, _VP, _I64, _I64, ctypes.c_int, _VP,
+                                 _I64, _VP, _VP, ctypes.c_size_t, _VP]
+        for f in (L.ln_fwd, L.ln_bwd, L.rms_fwd, L.rms_bwd, L.ln_fwd_ex, L.ln_bwd_ex,
+                  L.rms_fwd_ex, L.rms_bwd_ex):
             f.restype = ctypes.c_int
         _lib = L
     return _lib
@@ -294,3 +303,30 @@ def rms_backward(dy, x, rstd, M, N, gamma=None, want_dgamma=True, workspace=None
     if rc != GN_OK:
         raise GnError(rc, "rms_bwd")
     return dx, dg
+
+
+def ln_fwd_ex_raw(x, ldx, M, N, gamma, beta, eps, y, ldy, mean, rstd, stream=None) -> int:
+    """ln_fwd_ex: rows ldx / ldy elements apart (x and y may be views into wider buffers)."""
+    return lib().ln_fwd_ex(_ptr(x), ldx, M, N, DTYPE[x.dtype], _ptr(gamma), _ptr(beta),
+                           float(eps), _ptr(y), ldy, _ptr(mean), _ptr(rstd), _stream(stream))
+
+
+def ln_bwd_ex_raw(dy, lddy, x, ldx, mean, rstd, gamma, M, N, dx, lddx, dgamma, dbeta,
+                  workspace, stream=None) -> int:
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    return lib().ln_bwd_ex(_ptr(dy), lddy, _ptr(x), ldx, _ptr(mean), _ptr(rstd), _ptr(gamma),
+                           M, N, DTYPE[x.dtype], _ptr(dx), lddx, _ptr(dgamma), _ptr(dbeta),
+                           _ptr(workspace), ws_bytes, _stream(stream))
+
+
+def rms_fwd_ex_raw(x, ldx, M, N, gamma, eps, y, ldy, rstd, stream=None) -> int:
+    return lib().rms_fwd_ex(_ptr(x), ldx, M, N, DTYPE[x.dtype], _ptr(gamma), float(eps),
+                            _ptr(y), ldy, _ptr(rstd), _stream(stream))
+
+
+def rms_bwd_ex_raw(dy, lddy, x, ldx, rstd, gamma, M, N, dx, lddx, dgamma, workspace,
+                   stream=None) -> int:
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    return lib().rms_bwd_ex(_ptr(dy), lddy, _ptr(x), ldx, _ptr(rstd), _ptr(gamma), M, N,
+                            DTYPE[x.dtype], _ptr(dx), lddx, _ptr(dgamma), _ptr(workspace),
+                            ws_bytes, _stream(stream))

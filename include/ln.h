@@ -7,8 +7,8 @@
  * using tiled and two pass" (ROCm/pytorch PR #3564): layer_norm and rms_norm
  * backward with their gamma/beta gradients, on the shapes of its "Layer Norm
  * Backward Benchmark" table, with output masks (dgamma only, dbeta only) and
- * the M = 1 / N = 1 edge cases of its test list.  Per row m, over its N
- * features (biased variance, eps inside the square root):
+ * the M = 1 / N = 1 and non-contiguous-input cases of its test list.  Per
+ * row m, over its N features (biased variance, eps inside the square root):
  *
  *   LayerNorm:  mean = sum x / N,  rstd = 1 / sqrt(sum (x - mean)^2 / N + eps),
  *               xhat = (x - mean) * rstd,  y = xhat * gamma[n] + beta[n]
@@ -72,6 +72,26 @@ GN_API int rms_fwd(const void* x, int64_t M, int64_t N, int dtype, const float* 
 GN_API int rms_bwd(const void* dy, const void* x, const float* rstd, const float* gamma,
                    int64_t M, int64_t N, int dtype, void* dx, float* dgamma, void* workspace,
                    size_t workspace_bytes, void* stream);
+
+/* Strided rows (the non-contiguous inputs of the page's test list): the same
+ * operations on rows `ld*` elements apart (ld >= N) for x, dy and the output
+ * y or dx; the functions above are these with every ld = N.  In place needs
+ * equal strides.  The vector path needs every ld * element size to be a
+ * multiple of 16 bytes as well. */
+GN_API int ln_fwd_ex(const void* x, int64_t ldx, int64_t M, int64_t N, int dtype,
+                     const float* gamma, const float* beta, float eps, void* y, int64_t ldy,
+                     float* mean, float* rstd, void* stream);
+GN_API int ln_bwd_ex(const void* dy, int64_t lddy, const void* x, int64_t ldx, const float* mean,
+                     const float* rstd, const float* gamma, int64_t M, int64_t N, int dtype,
+                     void* dx, int64_t lddx, float* dgamma, float* dbeta, void* workspace,
+                     size_t workspace_bytes, void* stream);
+GN_API int rms_fwd_ex(const void* x, int64_t ldx, int64_t M, int64_t N, int dtype,
+                      const float* gamma, float eps, void* y, int64_t ldy, float* rstd,
+                      void* stream);
+GN_API int rms_bwd_ex(const void* dy, int64_t lddy, const void* x, int64_t ldx,
+                      const float* rstd, const float* gamma, int64_t M, int64_t N, int dtype,
+                      void* dx, int64_t lddx, float* dgamma, void* workspace,
+                      size_t workspace_bytes, void* stream);
 
 #ifdef __cplusplus
 }

@@ -152,6 +152,53 @@ def test_row_misaligned_pointers_and_in_place():
     checks.assert_param("dbeta", db, ref["dbeta"])
 
 
+@pytest.mark.parametrize("op", ["ln", "rms"])
+@pytest.mark.parametrize("dtype,N,pads", [("bf16", 1024, (8, 16, 24)), ("f32", 768, (4, 0, 12)),
+                                         ("f16", 256, (3, 5, 1))],
+                         ids=["bf16_vector", "f32_vector", "f16_scalar_strides"])
+def test_row_strided(op, dtype, N, pads):
+    """Rows of x, dy and the output lie in wider buffers (ld = N + pad each);
+    the results equal the dense computation, and the padding is not touched."""
+    M = 37
+    w = RW(f"{op}_{dtype}_{M}x{N}", op, dtype, M, N)
+    inp = synth.make_row_inputs(w, "cpu", seed=5)
+    ref = _oracle(inp, w)
+    dt = synth.DTYPES[dtype]
+    ldx, ldd, ldo = N + pads[0], N + pads[1], N + pads[2]
+
+    def wide(src, ld):
+        b = torch.full((M, ld), 7.0, dtype=dt, device="cuda")
+        if src is not None:
+            b[:, :N].copy_(src.view(M, N))
+        return b
+
+    xb, dyb = wide(inp["x"], ldx), wide(inp["dy"], ldd)
+    yb, dxb = wide(None, ldo), wide(None, ldo)
+    g, b = inp["gamma"].cuda(), inp["beta"].cuda()
+    mean = torch.empty(M, device="cuda")
+    rstd = torch.empty(M, device="cuda")
+    dg = torch.empty(N, device="cuda")
+    db = torch.empty(N, device="cuda")
+    ws = torch.empty(max(gn.ln_workspace_size(M, N, dtype), 16), dtype=torch.uint8, device="cuda")
+    if op == "ln":
+        assert gn.ln_fwd_ex_raw(xb, ldx, M, N, g, b, w.eps, yb, ldo, mean, rstd) == 0
+        assert gn.ln_bwd_ex_raw(dyb, ldd, xb, ldx, mean, rstd, g, M, N, dxb, ldo, dg, db, ws) == 0
+    else:
+        assert gn.rms_fwd_ex_raw(xb, ldx, M, N, g, w.eps, yb, ldo, rstd) == 0
+        assert gn.rms_bwd_ex_raw(dyb, ldd, xb, ldx, rstd, g, M, N, dxb, ldo, dg, ws) == 0
+    torch.cuda.synchronize()
+    checks.assert_out("y", yb[:, :N].reshape(-1), ref["y"], dtype)
+    checks.assert_out("dx", dxb[:, :N].reshape(-1), ref["dx"], dtype)
+    checks.assert_stat("rstd", rstd, ref["rstd"])
+    checks.assert_param("dgamma", dg, ref["dgamma"])
+    if op == "ln":
+        checks.assert_stat("mean", mean, ref["mean"])
+        checks.assert_param("dbeta", db, ref["dbeta"])
+    for buf in (yb, dxb):
+        assert torch.all(buf[:, N:] == 7.0), "padding written"
+    assert gn.ln_fwd_ex_raw(xb, N - 1, M, N, g, b, w.eps, yb, ldo, mean, rstd) == gn.GN_ERR_INVALID
+
+
 def test_row_empty_and_errors():
     dev = "cuda"
     x = torch.empty(0, device=dev, dtype=torch.float16)
