@@ -64,6 +64,7 @@ int prepare(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout, int
   p->part = reinterpret_cast<float2*>(ws + w.part);
   p->part0 = p->g.l1 > 1 ? reinterpret_cast<float2*>(ws + w.part0) : p->part;
   p->chst = reinterpret_cast<float2*>(ws + w.chst);
+  p->kst = reinterpret_cast<float*>(ws + w.chst);
   p->coef = reinterpret_cast<float2*>(ws + w.coef);
   return GN_OK;
 }
@@ -232,6 +233,8 @@ int gn_plan_info(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout
   out->workspace_bytes = gn::ws_layout(op, g).total;
   out->err_offset = gn::ws_layout(op, g).err;
   out->cluster_ctas = g.regime == gn::kRegimeResident ? g.K : 1;
+  out->finalise_second = g.fin2;
+  out->level1_items = g.l1 > 1 ? g.l1 : 1;
   const int64_t mc = gn::plan_max_clusters(g, op);
   out->max_clusters = mc > 0 ? (int)mc : 0;
   if (g.regime == gn::kRegimeResident) {

@@ -345,6 +345,19 @@ __device__ __forceinline__ bool publish_and_arrive(unsigned* t, unsigned total) 
   return last;
 }
 
+// 16-byte asynchronous copy from global to shared memory that bypasses L1
+// (the data may have been written by the previous kernel).  Both addresses
+// must be 16-byte aligned; the copy is complete after cp_async_wait_all() in
+// the issuing thread (then a barrier publishes it to the CTA).
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)),
+               "l"(__cvta_generic_to_global(src))
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 // ------------------------------------------------------ cluster reduction
 // Adds, for every q < NQ, red[q*stride + slot] of all CTAs of the cluster into
 // the copy of cluster rank 0, in rank order.  Every thread of every CTA of the

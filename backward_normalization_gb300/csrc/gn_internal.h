@@ -58,6 +58,15 @@ struct Geom {
   int64_t items;
   int64_t keep_from;  // item-relative row/element index from which the first kernel
                       // loads with the L2 evict_last policy (the part read again first)
+  // Finalisation in the second kernel (NCHW two-kernel path, when the
+  // records are few): the first kernel ends with its item records (and at
+  // most the level-1 merge); every CTA of the second kernel sums the Tp
+  // records of the channels of its groups itself, in one fixed order, and
+  // the parameter gradients are spread over its CTAs by channel.  Otherwise
+  // the last arrival of a sample finalises it in the first kernel.
+  int fin2;
+  int nsl2;        // fixed slices per channel in those sums
+  int64_t maxch2;  // most channels (whole groups) that one second-kernel CTA covers
   // pipelined regime: units_fin units of `pieces` pass-1 and `pieces` pass-2
   // tasks each (a piece is item u*T + q: NHWC, or plane q/T of the unit's
   // group, segment q%T: NCHW); pass-2 tasks trail pass-1 tasks by `lag` units
@@ -87,6 +96,29 @@ struct Geom {
 // Bytes reserved per ring-slot header of the pipelined kernel (the header
 // struct of gn_tasks.cuh is checked against it at compile time).
 constexpr size_t kSlotHdrBytes = 112;
+
+// Shared memory of a fin2 second kernel's finalisation (NCHW), in floats
+// from the 16-byte aligned base: the staged records (one run, channel-major,
+// copied from an even record index, so with up to one extra record at each
+// end), the slice sums, the per-channel stage, the per-group values and
+// per-warp sums of the parameter step.
+struct Fin2Smem {
+  int64_t recs, part, stage, grp, wpart, total;
+};
+__host__ __device__ inline Fin2Smem fin2_smem(const Geom& g) {
+  Fin2Smem s{};
+  if (!g.fin2) return s;
+  const int64_t run = (g.maxch2 * g.Tp + 3) & ~int64_t(1);
+  const int64_t pairs = (int64_t)g.nsl2 * g.maxch2;
+  s.recs = 0;
+  s.part = s.recs + 2 * run;
+  s.stage = s.part + 2 * (pairs > 64 ? pairs : 64);
+  s.grp = s.stage + 2 * g.maxch2;
+  s.wpart = s.grp + 2 * (g.maxch2 / g.Cg + 1);
+  s.total = s.wpart + 64;
+  return s;
+}
+__host__ __device__ inline int64_t fin2_smem_floats(const Geom& g) { return fin2_smem(g).total; }
 
 // Workspace layout (byte offsets, each 256-byte aligned).
 struct WsLayout {
@@ -125,6 +157,8 @@ struct KParams {
   float2* part;
   float2* chst;
   float2* coef;
+  float* kst;         // forward with fin2: the per-(n, c) shifts x(n, c, hw = 0), saved by
+                      // the first kernel (the second may overwrite x in place); aliases chst
 };
 
 // plan.cpp

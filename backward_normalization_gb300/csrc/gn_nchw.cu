@@ -10,9 +10,12 @@
 //          their last CTA.
 //   mode 1 (small planes): item = RB consecutive rows of one sample; each warp
 //          takes whole rows; one record per row.
-// In the two-kernel path the last arrival of a sample finalises it and the
-// elementwise second kernels walk the items (and the elements of a chunk) in
-// reverse order, starting on the data the first kernel left in L2.  The
+// In the two-kernel path the elementwise second kernels walk the items (and
+// the elements of a chunk) in reverse order, starting on the data the first
+// kernel left in L2.  When a second-kernel CTA's groups have few records
+// (g.fin2), that CTA derives their statistics (or dx coefficients) from the
+// records itself and the first kernel ends with its records; otherwise the
+// first kernel's last arrival of a sample finalises it.  The
 // pipelined kernel (mode-0 shapes, 16-byte vectors) runs the lockstep
 // schedule of gn_tasks.cuh over (sample, group) units, fed by bulk copies.
 #include "gn_tasks.cuh"
@@ -77,6 +80,10 @@ __device__ __forceinline__ void publish_chunk(const KParams& p, const Chunk& k, 
     sum_records(p.part0 + k.row * g.T + tlo, 1, 0, 1, gsize, ax, ay);
     p.part[k.row * g.Tp + t1] = make_float2(ax, ay);
   };
+  if (g.fin2) {  // the second kernel finalises: at most the level-1 merge here
+    if (g.l1 > 1) arrive_level1(p, k.row * g.Tp + t1, gsize, merge);
+    return;
+  }
   arrive_and_finalize<T, kBwd>(p, unit_of(p, k.row / g.C, k.row % g.C), k.row * g.Tp + t1, gsize,
                                merge, sm, nchw_smem_floats(g));
 }
@@ -91,6 +98,7 @@ __device__ __forceinline__ void stats_chunk(const KParams& p, int64_t item, floa
   const Chunk k = chunk_of(g, item);
   const T* xr = static_cast<const T*>(p.x) + k.row * g.HW;
   const float K = Elem<T>::to_f(xr[0]);
+  if (g.fin2 && k.ch == 0 && tid == 0) p.kst[k.row] = K;  // for the second kernel
   const int64_t keep = k.h0 + g.keep_from;
   float s = 0.f, q = 0.f;
   const int64_t st = (int64_t)blockDim.x * VW;
@@ -147,9 +155,10 @@ __device__ __forceinline__ void reduce_chunk(const KParams& p, int64_t item, flo
   publish_chunk<T, true>(p, k, s1, s2, sm);
 }
 
-// Forward pass 2 of one chunk, last vector to first.
+// Forward pass 2 of one chunk, last vector to first.  grp (fin2 plans): the
+// chunk's group (mean, rstd) in shared memory.
 template <typename T, int VW>
-__device__ __forceinline__ void apply_chunk(const KParams& p, int64_t item) {
+__device__ __forceinline__ void apply_chunk(const KParams& p, int64_t item, const float2* grp) {
   const Geom& g = p.g;
   const int tid = threadIdx.x;
   const uint64_t pol = policy_evict_first();
@@ -157,7 +166,8 @@ __device__ __forceinline__ void apply_chunk(const KParams& p, int64_t item) {
   if (k.h0 >= k.h1) return;
   const int64_t n = k.row / g.C, c = k.row % g.C, ng = n * g.G + c / g.Cg;
   // mean/rstd may have been written earlier in this launch: coherent loads
-  const float r = __ldcg(p.rstd + ng), mu = __ldcg(p.mean + ng);
+  const float2 mr = grp ? grp[0] : make_float2(__ldcg(p.mean + ng), __ldcg(p.rstd + ng));
+  const float r = mr.y, mu = mr.x;
   const float a = p.gamma ? r * __ldg(p.gamma + c) : r;
   const float b = p.beta ? __ldg(p.beta + c) : 0.f;
   const T* xr = static_cast<const T*>(p.x) + k.row * g.HW + k.h0;
@@ -185,9 +195,10 @@ __device__ __forceinline__ void apply_chunk(const KParams& p, int64_t item) {
   }
 }
 
-// Backward pass 2 of one chunk, last vector to first.
+// Backward pass 2 of one chunk, last vector to first.  grp (fin2 plans): the
+// chunk's group (B, D) in shared memory.
 template <typename T, int VW>
-__device__ __forceinline__ void dx_chunk(const KParams& p, int64_t item) {
+__device__ __forceinline__ void dx_chunk(const KParams& p, int64_t item, const float2* grp) {
   const Geom& g = p.g;
   const int tid = threadIdx.x;
   const uint64_t pol = policy_evict_first();
@@ -196,7 +207,7 @@ __device__ __forceinline__ void dx_chunk(const KParams& p, int64_t item) {
   const int64_t n = k.row / g.C, c = k.row % g.C, ng = n * g.G + c / g.Cg;
   const float r = __ldg(p.rstd + ng), mu = __ldg(p.mean + ng);
   const float A = p.gamma ? r * __ldg(p.gamma + c) : r;
-  const float2 cf = __ldcg(p.coef + ng);
+  const float2 cf = grp ? grp[0] : __ldcg(p.coef + ng);
   const T* xr = static_cast<const T*>(p.x) + k.row * g.HW + k.h0;
   const T* dr = static_cast<const T*>(p.dy) + k.row * g.HW + k.h0;
   T* outr = static_cast<T*>(p.out) + k.row * g.HW + k.h0;
@@ -249,6 +260,7 @@ __device__ __forceinline__ void stats_rows(const KParams& p, int64_t item, float
     const int64_t row = rb.n * g.C + c;
     const T* xr = static_cast<const T*>(p.x) + row * g.HW;
     const float K = Elem<T>::to_f(xr[0]);
+    if (g.fin2 && lane == 0) p.kst[row] = K;  // for the second kernel
     float s = 0.f, q = 0.f;
     for (int64_t h = (int64_t)lane * VW; h < g.HW; h += 32 * VW) {
       float v[VW];
@@ -259,7 +271,8 @@ __device__ __forceinline__ void stats_rows(const KParams& p, int64_t item, float
     q = warp_sum_lane0(q);
     if (lane == 0) p.part[row] = make_float2(s, q);
   }
-  arrive_and_finalize<T, false>(p, unit_of(p, rb.n, 0), 0, 1, [] {}, sm, nchw_smem_floats(g));
+  if (!g.fin2)
+    arrive_and_finalize<T, false>(p, unit_of(p, rb.n, 0), 0, 1, [] {}, sm, nchw_smem_floats(g));
 }
 
 template <typename T, int VW>
@@ -284,18 +297,22 @@ __device__ __forceinline__ void reduce_rows(const KParams& p, int64_t item, floa
     s2 = warp_sum_lane0(s2);
     if (lane == 0) p.part[row] = make_float2(s1, s2);
   }
-  arrive_and_finalize<T, true>(p, unit_of(p, rb.n, 0), 0, 1, [] {}, sm, nchw_smem_floats(g));
+  if (!g.fin2)
+    arrive_and_finalize<T, true>(p, unit_of(p, rb.n, 0), 0, 1, [] {}, sm, nchw_smem_floats(g));
 }
 
+// grp (fin2 plans): (mean, rstd) of groups g0, g0 + 1, ... in shared memory.
 template <typename T, int VW>
-__device__ __forceinline__ void apply_rows(const KParams& p, int64_t item) {
+__device__ __forceinline__ void apply_rows(const KParams& p, int64_t item, const float2* grp,
+                                           int64_t g0) {
   const Geom& g = p.g;
   const RowBlock rb = rows_of(g, item);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   const uint64_t pol = policy_evict_first();
   for (int64_t c = rb.c0 + warp; c < rb.c1; c += nwarps) {
     const int64_t row = rb.n * g.C + c, ng = rb.n * g.G + c / g.Cg;
-    const float r = __ldcg(p.rstd + ng), mu = __ldcg(p.mean + ng);
+    const float2 mr = grp ? grp[c / g.Cg - g0] : make_float2(__ldcg(p.mean + ng), __ldcg(p.rstd + ng));
+    const float r = mr.y, mu = mr.x;
     const float a = p.gamma ? r * __ldg(p.gamma + c) : r;
     const float b = p.beta ? __ldg(p.beta + c) : 0.f;
     const T* xr = static_cast<const T*>(p.x) + row * g.HW;
@@ -310,8 +327,10 @@ __device__ __forceinline__ void apply_rows(const KParams& p, int64_t item) {
   }
 }
 
+// grp (fin2 plans): (B, D) of groups g0, g0 + 1, ... in shared memory.
 template <typename T, int VW>
-__device__ __forceinline__ void dx_rows(const KParams& p, int64_t item) {
+__device__ __forceinline__ void dx_rows(const KParams& p, int64_t item, const float2* grp,
+                                        int64_t g0) {
   const Geom& g = p.g;
   const RowBlock rb = rows_of(g, item);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
@@ -320,7 +339,7 @@ __device__ __forceinline__ void dx_rows(const KParams& p, int64_t item) {
     const int64_t row = rb.n * g.C + c, ng = rb.n * g.G + c / g.Cg;
     const float r = __ldg(p.rstd + ng), mu = __ldg(p.mean + ng);
     const float A = p.gamma ? r * __ldg(p.gamma + c) : r;
-    const float2 cf = __ldcg(p.coef + ng);
+    const float2 cf = grp ? grp[c / g.Cg - g0] : __ldcg(p.coef + ng);
     const T* xr = static_cast<const T*>(p.x) + row * g.HW;
     const T* dr = static_cast<const T*>(p.dy) + row * g.HW;
     T* outr = static_cast<T*>(p.out) + row * g.HW;
@@ -340,29 +359,73 @@ template <typename T, int VW>
 __global__ void __launch_bounds__(512) nchw_fwd_stats(const __grid_constant__ KParams p) {
   grid_dependency_wait();  // the previous kernel's results (and x, dy) are complete
   grid_launch_dependents();
-  extern __shared__ float sm[];
+  extern __shared__ __align__(16) float sm[];
   if (p.g.mode == 0)
     stats_chunk<T, VW>(p, blockIdx.x, sm);
   else
     stats_rows<T, VW>(p, blockIdx.x, sm);
 }
 
+// fin2 plans: the channels a second-kernel item finalises (its plane's group,
+// or its block of planes extended to whole groups) and the groups whose
+// mean/rstd it writes (each group by the item holding its first plane's
+// first chunk).
+struct Fin2Range {
+  int64_t n, ca, cb, wa, wb;
+};
+__device__ __forceinline__ Fin2Range nchw_fin2_range(const Geom& g, int64_t item) {
+  Fin2Range r;
+  if (g.mode == 0) {
+    const Chunk k = chunk_of(g, item);
+    const int64_t c = k.row % g.C, gi = c / g.Cg;
+    r.n = k.row / g.C;
+    r.ca = gi * g.Cg;
+    r.cb = r.ca + g.Cg;
+    const bool writer = k.ch == 0 && c == r.ca;
+    r.wa = writer ? gi : 0;
+    r.wb = writer ? gi + 1 : 0;
+  } else {
+    const RowBlock b = rows_of(g, item);
+    r.n = b.n;
+    r.ca = b.c0 / g.Cg * g.Cg;
+    r.cb = (b.c1 + g.Cg - 1) / g.Cg * g.Cg;
+    r.wa = (b.c0 + g.Cg - 1) / g.Cg;
+    r.wb = (b.c1 + g.Cg - 1) / g.Cg;
+  }
+  return r;
+}
+
+// Dynamic shared memory of the second kernels, in bytes.
+inline size_t second_smem(const Geom& g, bool bwd) {
+  const int64_t f = fin2_smem_floats(g);
+  const int64_t params = bwd ? 2 * (int64_t)g.tpb : 0;  // finalize_params scratch
+  return sizeof(float) * (size_t)(f > params ? f : params);
+}
+
 template <typename T, int VW>
 __global__ void __launch_bounds__(512) nchw_fwd_apply(const __grid_constant__ KParams p) {
+  extern __shared__ __align__(16) float sm[];
   grid_dependency_wait();
   grid_launch_dependents();
   const int64_t item = p.g.items - 1 - (int64_t)blockIdx.x;
+  const float2* grp = nullptr;
+  int64_t g0 = 0;
+  if (p.g.fin2) {
+    const Fin2Range r = nchw_fin2_range(p.g, item);
+    grp = fin2_groups<false>(p, r.n, r.ca, r.cb, r.wa, r.wb, sm);
+    g0 = r.ca / p.g.Cg;
+  }
   if (p.g.mode == 0)
-    apply_chunk<T, VW>(p, item);
+    apply_chunk<T, VW>(p, item, grp);
   else
-    apply_rows<T, VW>(p, item);
+    apply_rows<T, VW>(p, item, grp, g0);
 }
 
 template <typename T, int VW>
 __global__ void __launch_bounds__(512) nchw_bwd_reduce(const __grid_constant__ KParams p) {
   grid_dependency_wait();
   grid_launch_dependents();
-  extern __shared__ float sm[];
+  extern __shared__ __align__(16) float sm[];
   if (p.g.mode == 0)
     reduce_chunk<T, VW>(p, blockIdx.x, sm);
   else
@@ -371,17 +434,25 @@ __global__ void __launch_bounds__(512) nchw_bwd_reduce(const __grid_constant__ K
 
 template <typename T, int VW>
 __global__ void __launch_bounds__(512) nchw_bwd_dx(const __grid_constant__ KParams p) {
-  extern __shared__ float sm[];
+  extern __shared__ __align__(16) float sm[];
   grid_dependency_wait();
   grid_launch_dependents();
-  // the first CTA also adds up dgamma / dbeta: every channel's sums are
-  // complete once the first kernel is
-  if (blockIdx.x == 0) finalize_params(p, sm);
   const int64_t item = p.g.items - 1 - (int64_t)blockIdx.x;
+  const float2* grp = nullptr;
+  int64_t g0 = 0;
+  if (p.g.fin2) {
+    const Fin2Range r = nchw_fin2_range(p.g, item);
+    grp = fin2_groups<true>(p, r.n, r.ca, r.cb, 0, 0, sm);
+    g0 = r.ca / p.g.Cg;
+  } else if (blockIdx.x == 0) {
+    // the first CTA adds up dgamma / dbeta: every channel's sums are
+    // complete once the first kernel is
+    finalize_params(p, sm);
+  }
   if (p.g.mode == 0)
-    dx_chunk<T, VW>(p, item);
+    dx_chunk<T, VW>(p, item, grp);
   else
-    dx_rows<T, VW>(p, item);
+    dx_rows<T, VW>(p, item, grp, g0);
 }
 
 // The pipelined regime (schedule in gn_tasks.cuh): a unit is one (sample n,
@@ -545,8 +616,8 @@ cudaError_t run_op(const KParams& p, cudaStream_t s, bool bwd) {
                       : launch_pdl(nchw_fwd_stats<T, VW>, g.items, g.tpb, sm1, s, p);
   if (e != cudaSuccess) return e;
   if (ev.mid) cudaEventRecord(ev.mid, s);
-  e = bwd ? launch_pdl(nchw_bwd_dx<T, VW>, g.items, g.tpb, sizeof(float) * 2 * g.tpb, s, p)
-          : launch_pdl(nchw_fwd_apply<T, VW>, g.items, g.tpb, 0, s, p);
+  e = bwd ? launch_pdl(nchw_bwd_dx<T, VW>, g.items, g.tpb, second_smem(g, true), s, p)
+          : launch_pdl(nchw_fwd_apply<T, VW>, g.items, g.tpb, second_smem(g, false), s, p);
   if (ev.end) cudaEventRecord(ev.end, s);
   return e;
 }
@@ -558,7 +629,7 @@ cudaError_t dispatch_vw(const KParams& p, cudaStream_t s, bool bwd) {
 
 template <typename T, int VW>
 const void* kernel_t(const Geom& g, bool bwd, int second, size_t* smem) {
-  *smem = second ? (bwd ? sizeof(float) * 2 * g.tpb : 0) : sizeof(float) * nchw_smem_floats(g);
+  *smem = second ? second_smem(g, bwd) : sizeof(float) * nchw_smem_floats(g);
   if (second) return bwd ? (const void*)nchw_bwd_dx<T, VW> : (const void*)nchw_fwd_apply<T, VW>;
   return bwd ? (const void*)nchw_bwd_reduce<T, VW> : (const void*)nchw_fwd_stats<T, VW>;
 }

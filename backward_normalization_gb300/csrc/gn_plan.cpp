@@ -373,6 +373,68 @@ int64_t resident_ctas(const Geom& g, int op, int second) {
 }
 
 namespace {
+#ifndef GN_FIN2_BYTES
+#define GN_FIN2_BYTES (4 * 1024)
+#endif
+// Records one second-kernel CTA may read to finalise its groups itself, and
+// the most shared memory that finalisation may take (the default dynamic
+// limit, so the second kernels need no opt-in and keep two CTAs per SM).
+// Every CTA of a sample repeats that work, so it pays only while the records
+// are few: measured on GB300, NCHW planes (Cg records per CTA) gain, while
+// channels-last rows (4608 records per CTA at 512 channels) lost more in the
+// second kernel than the chain costs the first.
+constexpr int64_t kFin2Bytes = GN_FIN2_BYTES;
+constexpr int64_t kFin2SmemBytes = 48 * 1024;
+
+// Most channels, extended to whole groups, that one second-kernel CTA covers:
+// an NCHW plane (mode 0) or block of RB planes (mode 1).
+int64_t fin2_channels(const Geom& g) {
+  if (g.mode == 0) return g.Cg;
+  const int64_t blk = g.RB, nblk = g.items_per_n;
+  int64_t best = 0;
+  for (int64_t b = 0; b < nblk; ++b) {
+    const int64_t lo = b * blk, hi = std::min(g.C, lo + blk);
+    if (lo >= hi) continue;
+    best = std::max(best, cdiv(hi, g.Cg) * g.Cg - lo / g.Cg * g.Cg);
+  }
+  return best;
+}
+
+// Moves the finalisation of an NCHW plan into the second kernel when each of
+// its CTAs reads at most kFin2Bytes of records: with every item record (no
+// chain at all in the first kernel) if they are few enough, else with
+// level-1 records (the first kernel keeps only the level-1 merge).
+// Otherwise the plan is left as it is.  Channels-last CTAs cover whole rows
+// of C channels, far more records than the budget at the shapes here, so
+// that layout keeps the chain (its kernels carry no second-kernel
+// finalisation at all).
+void plan_fin2(Geom& g) {
+  if (g.layout != kNCHW) return;
+  const int64_t mc = fin2_channels(g);
+  for (int l1 : {1, kGroup1}) {
+    if (l1 > 1 && g.T < 2 * kGroup1) break;
+    const int64_t Tp = cdiv(g.T, l1);
+    if (mc * Tp * (int64_t)sizeof(float) * 2 > kFin2Bytes) continue;
+    Geom f = g;
+    f.fin2 = 1;
+    f.maxch2 = mc;
+    f.nsl2 = (int)clamp64(g.tpb / mc, 1, Tp);
+    f.Tp = Tp;
+    if (fin2_smem_floats(f) * (int64_t)sizeof(float) > kFin2SmemBytes) continue;
+    g.fin2 = 1;
+    g.maxch2 = mc;
+    g.nsl2 = f.nsl2;
+    g.l1 = l1;
+    g.Tp = Tp;
+    g.groups1 = l1 > 1 ? g.N * g.C * Tp : 0;
+    if (g.mode == 0) {
+      g.cstride = Tp;
+      g.arrivals_per_n = g.C * Tp;
+    }
+    return;
+  }
+}
+
 Geom plan_geom(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout, int dtype,
                bool aligned) {
   const int sm_count = device_sm_count();
@@ -465,6 +527,7 @@ Geom plan_geom(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout, 
     // latency-bound), so it runs only when asked for
     plan_resident(g, op);
   }
+  if (g.regime == kRegimeGeneric) plan_fin2(g);
   const int64_t pipe = g.regime == kRegimePipelined ? 2 * g.units_fin + 3 : 0;
   g.counters = g.units_fin + 1 + g.groups1 + pipe;  // resident: units_fin = N, groups1 = 0
   return g;

@@ -40,7 +40,8 @@ class PlanDesc(ctypes.Structure):
                 ("ctas", ctypes.c_int64), ("partials", ctypes.c_int64),
                 ("workspace_bytes", ctypes.c_size_t), ("cluster_ctas", ctypes.c_int),
                 ("max_clusters", ctypes.c_int), ("smem_bytes", ctypes.c_size_t),
-                ("err_offset", ctypes.c_size_t)]
+                ("err_offset", ctypes.c_size_t), ("finalise_second", ctypes.c_int),
+                ("level1_items", ctypes.c_int)]
 
 
 _lib = None

@@ -190,6 +190,11 @@ typedef struct gn_plan_desc {
   size_t smem_bytes;     /* dynamic shared memory per CTA of that kernel */
   size_t err_offset;     /* workspace byte offset of the uint32 error word; the
                             counters, flags and task queue lie before it */
+  int finalise_second;   /* two-kernel path: 1 when every CTA of the second kernel
+                            derives its groups' statistics (or dx coefficients)
+                            from the partial records itself, 0 when the last
+                            arrival of a sample does it in the first kernel */
+  int level1_items;      /* items merged per level-1 record (1: none) */
 } gn_plan_desc;
 
 /* Fills *out with the plan of gn_fwd/gn_bwd for this problem, assuming every

@@ -155,6 +155,35 @@ def test_regime_choice(gn):
         gn.set_regime(7)
 
 
+def test_finalisation_placement(gn):
+    """NCHW two-kernel plans finalise in the second kernel when each of its
+    CTAs reads at most 4 KB of partial records; otherwise (and always for
+    channels-last) the first kernel's last arrival of a sample does it, after
+    level-1 merges of 8 items when a sample has 16 items or more."""
+    gn.set_regime(gn.REGIME_TWO_KERNEL)
+    try:
+        # NCHW planes: one group's Cg records per CTA
+        d = gn.plan_info(1, 112, 64, 512 * 512, 8, "nchw", "f32")
+        assert (d.finalise_second, d.level1_items) == (1, 1)
+        # NCHW small planes (blocks of rows)
+        d = gn.plan_info(0, 2, 36, 100, 3, "nchw", "f32")
+        assert (d.finalise_second, d.level1_items) == (1, 1)
+        # channels-last keeps the chain even with few records
+        d = gn.plan_info(1, 16, 32, 64, 8, "nhwc", "bf16")
+        assert (d.finalise_second, d.level1_items) == (0, 1)
+        # one sample, 128 channels, hundreds of items: the chain, with level-1 merges
+        d = gn.plan_info(0, 1, 128, 2048 * 1024, 16, "nhwc", "f16")
+        assert (d.finalise_second, d.level1_items) == (0, 8)
+        # 512 channels, a few items per sample: the chain
+        d = gn.plan_info(1, 32, 512, 32 * 32, 32, "nhwc", "bf16")
+        assert (d.finalise_second, d.level1_items) == (0, 1)
+    finally:
+        gn.set_regime(gn.REGIME_AUTO)
+    # the resident regime finalises in its one kernel
+    d = gn.plan_info(0, 8, 320, 4096, 32, "nhwc", "bf16")
+    assert d.regime == 1 and d.finalise_second == 0
+
+
 def test_configs_cover_both_layouts_and_vector_paths(gn):
     seen = set()
     for w in synth.WORKLOADS:

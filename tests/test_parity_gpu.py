@@ -44,6 +44,11 @@ def _small_cases():
         # than there are, so both passes of different units interleave in its task order
         ("fp32_nchw_16x64x48x48_g8_many_units", c3.scaled(name="mu3", N=16, H=48, W=48)),
         ("bf16_nhwc_40x64x48x48_g8_many_units", c4.scaled(name="mu4", N=40, C=64, G=8, H=48, W=48)),
+        # groups of 80 channels across the two 600-channel column blocks: both blocks'
+        # second-kernel CTAs derive the shared group's statistics
+        ("fp32_nhwc_2x1200x2x3_g15_straddle", c0.scaled(name="strad", layout="nhwc", N=2, C=1200, G=15, H=2, W=3)),
+        # blocks of 8 planes cut groups of 12 planes
+        ("fp32_nchw_2x36x10x10_g3_row_blocks", c0.scaled(name="blk", N=2, C=36, G=3, H=10, W=10)),
     ]
 
 
@@ -278,6 +283,37 @@ def test_shared_workspace_across_shapes(regime):
         dx, dg, db = gn.backward(dy, x, mean, rstd, w.N, w.C, w.HW, w.G, w.layout, gm, workspace=ws)
         torch.cuda.synchronize()
         _compare(dict(y=y, mean=mean, rstd=rstd, dx=dx, dgamma=dg, dbeta=db), _oracle_full(inp, w), w)
+
+
+FINALISATION = [
+    # (case, finalised in the second kernel, items per level-1 record)
+    ("fp16_nhwc_1x128x64x64_g16_chain_level1", synth.WORKLOADS[1].scaled(name="f2l1", H=64, W=64), 0, 8),
+    ("fp16_nhwc_1x2048x32x32_g32_chain", synth.WORKLOADS[1].scaled(name="f2ch", C=2048, G=32, H=32, W=32), 0, 8),
+    ("bf16_nhwc_16x512x8x8_g32_chain", synth.WORKLOADS[4].scaled(name="f2c4", N=16, H=8, W=8), 0, 1),
+    ("fp32_nchw_2x16x64x64_g4_records", synth.WORKLOADS[3].scaled(name="f2r", N=2, C=16, G=4, H=64, W=64), 1, 1),
+    ("fp32_nchw_2x36x10x10_g3_row_blocks", synth.WORKLOADS[0].scaled(name="f2b", N=2, C=36, G=3, H=10, W=10), 1, 1),
+]
+
+
+@pytest.mark.parametrize("name,w,fin2,l1", FINALISATION, ids=[c[0] for c in FINALISATION])
+def test_finalisation_paths(name, w, fin2, l1):
+    """Both places of the finalisation (the second kernel's CTAs from the
+    records, or the first kernel's last arrival) and both record levels, on
+    the two-kernel path, element by element against the oracle; repeated
+    calls are bit-identical."""
+    gn.set_regime(gn.REGIME_TWO_KERNEL)
+    try:
+        for op in (gn.OP_FWD, gn.OP_BWD):
+            d = gn.plan_info(op, w.N, w.C, w.HW, w.G, w.layout, w.dtype)
+            assert (d.regime, d.finalise_second, d.level1_items) == (0, fin2, l1)
+        inp = synth.make_inputs(w, "cpu", seed=5)
+        a = _gpu_run(inp, w)
+        b = _gpu_run(inp, w)
+    finally:
+        gn.set_regime(gn.REGIME_AUTO)
+    _compare(a, _oracle_full(inp, w), w)
+    for k in a:
+        assert torch.equal(a[k], b[k]), k
 
 
 def test_zero_extents():
