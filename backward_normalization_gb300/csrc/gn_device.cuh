@@ -333,16 +333,16 @@ __device__ __forceinline__ uint4 lds16(const void* p) {
 // has to be zero-filled once, before its first use.)  atomicAdd never retries,
 // so arrivals cost one atomic each however many CTAs arrive together.
 //
-// Called by one thread after the CTA's partial stores and a __syncthreads():
-// the first fence makes this CTA's stores visible device-wide before its
-// arrival; the last CTA's fence orders its reads of the other CTAs' partials
-// after the arrival.
+// Called by one thread after the CTA's partial stores and a __syncthreads().
+// One acquire-release atomic at GPU scope: its release half publishes every
+// store the barrier ordered before it (the whole CTA's partials) ahead of the
+// arrival, and its acquire half orders the last CTA's reads of the other
+// CTAs' partials after it (that CTA's other threads read after a following
+// barrier).  Returns whether this arrival completed the count.
 __device__ __forceinline__ bool publish_and_arrive(unsigned* t, unsigned total) {
-  __threadfence();
-  const unsigned old = atomicAdd(t, 1u);
-  const bool last = (old == total - 1u);
-  if (last) __threadfence();
-  return last;
+  unsigned old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(t) : "memory");
+  return old == total - 1u;
 }
 
 // 16-byte asynchronous copy from global to shared memory that bypasses L1

@@ -167,8 +167,12 @@ __device__ void finalize_fwd(const KParams& p, int64_t n, int64_t ca, int64_t cb
   const T* x = static_cast<const T*>(p.x);
   const float hw = (float)g.HW;
   float2* stage = channel_stage(p, n, sm, sm_floats);
+  // the shift of this thread's first channel (ca + tid), requested with the records
+  auto shift = [&](int64_t c) { return Elem<T>::to_f(x[first_elem_offset(g, n, c)]); };
+  const int64_t c_pre = ca + threadIdx.x;
+  const float k_pre = c_pre < cb ? shift(c_pre) : 0.f;
   sum_channel_partials(p, n, ca, cb, sm, [&](int64_t c, float2 s) {
-    stage[c] = channel_moments(Elem<T>::to_f(x[first_elem_offset(g, n, c)]), s, hw);
+    stage[c] = channel_moments(c == c_pre ? k_pre : shift(c), s, hw);
   });
   for (int64_t gi = ca / g.Cg + threadIdx.x; gi < cb / g.Cg; gi += blockDim.x) {
     const float2 mr = group_moments(stage + gi * g.Cg, g, p.eps);
@@ -186,12 +190,18 @@ __device__ __forceinline__ void finalize_bwd(const KParams& p, int64_t n, int64_
   float2* stage = channel_stage(p, n, sm, sm_floats);
   float2* chst = p.chst + n * g.C;
   const bool terms = stage != chst;  // a stage of its own: the channel terms go there
+  // gamma of this thread's first channel and rstd of its first group,
+  // requested with the records
+  auto gam = [&](int64_t c) { return p.gamma ? __ldg(p.gamma + c) : 1.0f; };
+  const int64_t c_pre = ca + threadIdx.x, g_pre = ca / g.Cg + threadIdx.x;
+  const float gam_pre = c_pre < cb ? gam(c_pre) : 0.f;
+  const float r_pre = g_pre < cb / g.Cg ? __ldg(p.rstd + n * g.G + g_pre) : 0.f;
   sum_channel_partials(p, n, ca, cb, sm, [&](int64_t c, float2 s) {
     chst[c] = s;  // kept for the dgamma/dbeta step
-    stage[c] = terms ? channel_terms(p.gamma ? __ldg(p.gamma + c) : 1.0f, s) : s;
+    stage[c] = terms ? channel_terms(c == c_pre ? gam_pre : gam(c), s) : s;
   });
   for (int64_t gi = ca / g.Cg + threadIdx.x; gi < cb / g.Cg; gi += blockDim.x) {
-    const float r = __ldg(p.rstd + n * g.G + gi);
+    const float r = gi == g_pre ? r_pre : __ldg(p.rstd + n * g.G + gi);
     p.coef[n * g.G + gi] = terms ? group_coef(stage + gi * g.Cg, g, r)
                                  : group_coef_sums(stage + gi * g.Cg, p, gi, r);
   }
@@ -286,14 +296,12 @@ __device__ __forceinline__ void arrive_and_finalize(const KParams& p, const Unit
                                                     int64_t group1, unsigned gsize, Merge merge,
                                                     float* sm, int64_t sm_floats) {
   __shared__ int s_last;
-  __threadfence();  // this thread's record stores, before the CTA's arrival
   if (p.g.l1 > 1) {
-    __syncthreads();
+    __syncthreads();  // the CTA's record stores, before thread 0's arrival
     if (threadIdx.x == 0) s_last = publish_and_arrive(p.cnt1 + group1, gsize);
     __syncthreads();
     if (!s_last) return;
     merge();
-    __threadfence();
     if (threadIdx.x == 0) atomicExch(p.cnt1 + group1, 0u);
   }
   __syncthreads();
@@ -304,11 +312,13 @@ __device__ __forceinline__ void arrive_and_finalize(const KParams& p, const Unit
     finalize_bwd(p, un.n, un.c0, un.c1, sm, sm_floats);
   else
     finalize_fwd<T>(p, un.n, un.c0, un.c1, sm, sm_floats);
-  __threadfence();  // the unit's statistics, before the ready flag and the next arrival
-  __syncthreads();
+  __syncthreads();  // the unit's statistics, before the ready flag
   if (threadIdx.x == 0) {
     atomicExch(un.ticket, 0u);
-    if (un.ready) atomicExch(un.ready, 1u);
+    if (un.ready) {
+      __threadfence();
+      atomicExch(un.ready, 1u);
+    }
   }
   // the backward's dgamma / dbeta are added up by the dx kernel, whose first
   // CTA finds every channel's sums complete when it starts
@@ -323,8 +333,7 @@ template <typename Merge>
 __device__ __forceinline__ void arrive_level1(const KParams& p, int64_t group1, unsigned gsize,
                                               Merge merge) {
   __shared__ int s_last1;
-  __threadfence();  // this thread's record stores, before the CTA's arrival
-  __syncthreads();
+  __syncthreads();  // the CTA's record stores, before thread 0's arrival
   if (threadIdx.x == 0) s_last1 = publish_and_arrive(p.cnt1 + group1, gsize);
   __syncthreads();
   if (!s_last1) return;
