@@ -307,22 +307,25 @@ __global__ void __launch_bounds__(kRowThreads) row_bwd(const __grid_constant__ R
   grid_launch_dependents();  // the column kernel may start launching
 }
 
-// dgamma[c] = sum over the P CTA records of feature c, dbeta likewise: eight
-// slices per feature (records s, s + 8, ... in order), then the slices in
-// order.  256 threads: 32 features x 8 slices.
-__global__ void __launch_bounds__(256) row_col_reduce(const __grid_constant__ RowParams p,
-                                                      int64_t P) {
-  __shared__ float2 acc[8][32];
+// dgamma[c] = sum over the P CTA records of feature c, dbeta likewise.  A CTA
+// takes kColF features with kColS slices each: slice s adds records s,
+// s + kColS, ... in order (eight loads in flight at a time, so up to
+// 8*kColS records cost one round trip to L2), then the slices are added by a
+// fixed pairwise tree.  kColF * kColS threads.
+constexpr int kColF = 16, kColS = 64;
+__global__ void __launch_bounds__(kColF * kColS) row_col_reduce(const __grid_constant__ RowParams p,
+                                                               int64_t P) {
+  __shared__ float2 acc[kColS][kColF];
   grid_dependency_wait();  // the records of the row kernel are complete
-  const int j = threadIdx.x & 31, sl = threadIdx.x >> 5;
-  const int64_t c = (int64_t)blockIdx.x * 32 + j;
+  const int j = threadIdx.x % kColF, sl = threadIdx.x / kColF;
+  const int64_t c = (int64_t)blockIdx.x * kColF + j;
   float a = 0.f, b = 0.f;
   if (c < p.N) {
-    for (int64_t r = sl; r < P; r += 8 * 8) {
+    for (int64_t r = sl; r < P; r += 8 * kColS) {
       float2 v[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
-        const int64_t rr = r + 8 * k;
+        const int64_t rr = r + (int64_t)kColS * k;
         v[k] = rr < P ? __ldcg(p.part + rr * p.N + c) : make_float2(0.f, 0.f);
       }
 #pragma unroll
@@ -334,13 +337,18 @@ __global__ void __launch_bounds__(256) row_col_reduce(const __grid_constant__ Ro
   }
   acc[sl][j] = make_float2(a, b);
   __syncthreads();
-  if (sl == 0 && c < p.N) {
-    for (int s = 1; s < 8; ++s) {
-      a += acc[s][j].x;
-      b += acc[s][j].y;
+#pragma unroll
+  for (int h = kColS / 2; h > 0; h >>= 1) {
+    if (sl < h) {
+      const float2 o = acc[sl + h][j];
+      acc[sl][j].x += o.x;
+      acc[sl][j].y += o.y;
     }
-    if (p.dgamma) p.dgamma[c] = a;
-    if (p.dbeta) p.dbeta[c] = b;
+    __syncthreads();
+  }
+  if (sl == 0 && c < p.N) {
+    if (p.dgamma) p.dgamma[c] = acc[0][j].x;
+    if (p.dbeta) p.dbeta[c] = acc[0][j].y;
   }
 }
 
@@ -574,8 +582,8 @@ int run_bwd(const void* dy, int64_t ldd, const void* x, int64_t ldx, const float
   // waits for the row kernel's records before reading them
   int64_t P = pl.grid;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)cdiv64(N, 32), 1, 1);
-  cfg.blockDim = dim3(256, 1, 1);
+  cfg.gridDim = dim3((unsigned)cdiv64(N, kColF), 1, 1);
+  cfg.blockDim = dim3(kColF * kColS, 1, 1);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
