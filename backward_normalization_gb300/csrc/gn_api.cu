@@ -10,7 +10,7 @@ namespace {
 thread_local int t_last_cuda_error = 0;
 thread_local gn::TimingEvents t_events = {nullptr, nullptr, nullptr};
 
-int elem_size(int dtype) { return dtype == gn::kF32 ? 4 : 2; }
+int elem_size(int dtype) { return gn::dtype_size(dtype); }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -23,7 +23,8 @@ bool overlap(const void* a, size_t na, const void* b, size_t nb) {
 
 int check_problem(int64_t N, int64_t C, int64_t HW, int64_t G, int layout, int dtype) {
   if (layout != GN_LAYOUT_NCHW && layout != GN_LAYOUT_NHWC) return GN_ERR_UNSUPPORTED;
-  if (dtype != GN_DTYPE_F32 && dtype != GN_DTYPE_F16 && dtype != GN_DTYPE_BF16)
+  if (dtype != GN_DTYPE_F32 && dtype != GN_DTYPE_F16 && dtype != GN_DTYPE_BF16 &&
+      dtype != GN_DTYPE_F64)
     return GN_ERR_UNSUPPORTED;
   if (N < 0 || C < 0 || HW < 0 || G <= 0) return GN_ERR_INVALID;
   if (C % G != 0) return GN_ERR_INVALID;

@@ -70,6 +70,13 @@ struct Elem<__nv_bfloat16> {
   __device__ static __nv_bfloat16 from_f(float v) { return __float2bfloat16_rn(v); }
 };
 
+template <>
+struct Elem<double> {  // storage only: computed in fp32
+  static constexpr int VEC = 2;
+  __device__ static float to_f(double v) { return __double2float_rn(v); }
+  __device__ static double from_f(float v) { return (double)v; }
+};
+
 __device__ __forceinline__ float2 h2f(uint32_t w) {
   __half2 h;
   *reinterpret_cast<uint32_t*>(&h) = w;
@@ -135,6 +142,28 @@ struct Access<float, 4> {
     return u;
   }
   __device__ static void store(float* p, const float (&f)[4], uint64_t pol) { st16(p, pack(f), pol); }
+};
+template <>
+struct Access<double, 2> {  // two doubles per 16 bytes, rounded to fp32 on load
+  using Raw = uint4;
+  __device__ static Raw load_raw(const double* p, uint64_t pol) { return ld16(p, pol); }
+  __device__ static void unpack(const Raw& u, float (&f)[2]) {
+    f[0] = __double2float_rn(__hiloint2double((int)u.y, (int)u.x));
+    f[1] = __double2float_rn(__hiloint2double((int)u.w, (int)u.z));
+  }
+  __device__ static void load(const double* p, float (&f)[2], uint64_t pol) {
+    unpack(ld16(p, pol), f);
+  }
+  __device__ static Raw pack(const float (&f)[2]) {
+    const double a = f[0], b = f[1];
+    uint4 u;
+    u.x = (uint32_t)__double2loint(a);
+    u.y = (uint32_t)__double2hiint(a);
+    u.z = (uint32_t)__double2loint(b);
+    u.w = (uint32_t)__double2hiint(b);
+    return u;
+  }
+  __device__ static void store(double* p, const float (&f)[2], uint64_t pol) { st16(p, pack(f), pol); }
 };
 template <>
 struct Access<__half, 8> {

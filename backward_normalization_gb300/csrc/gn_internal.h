@@ -10,7 +10,13 @@
 namespace gn {
 
 enum Layout { kNCHW = 0, kNHWC = 1 };
-enum DType { kF32 = 0, kF16 = 1, kBF16 = 2 };
+enum DType { kF32 = 0, kF16 = 1, kBF16 = 2, kF64 = 3 };
+
+// Bytes per stored element.  Every dtype is computed in fp32; f64 is a
+// storage type (16-byte vectors of two doubles, converted on load and store).
+__host__ __device__ inline int dtype_size(int dtype) {
+  return dtype == kF64 ? 8 : dtype == kF32 ? 4 : 2;
+}
 enum Op { kFwd = 0, kBwd = 1 };
 
 // Regimes (which kernel family runs a call).

@@ -653,6 +653,7 @@ const void* nchw_kernel(const Geom& g, bool bwd, int second, size_t* smem) {
   switch (g.dtype) {
     case kF32: return kernel_vw<float>(g, bwd, second, smem);
     case kF16: return kernel_vw<__half>(g, bwd, second, smem);
+    case kF64: return kernel_vw<double>(g, bwd, second, smem);
     default: return kernel_vw<__nv_bfloat16>(g, bwd, second, smem);
   }
 }
@@ -661,6 +662,7 @@ cudaError_t launch_nchw(const KParams& p, cudaStream_t s, bool bwd) {
   switch (p.g.dtype) {
     case kF32: return dispatch_vw<float>(p, s, bwd);
     case kF16: return dispatch_vw<__half>(p, s, bwd);
+    case kF64: return dispatch_vw<double>(p, s, bwd);
     default: return dispatch_vw<__nv_bfloat16>(p, s, bwd);
   }
 }
@@ -674,6 +676,7 @@ const void* nchw_pipelined_kernel(const Geom& g, bool bwd, size_t* smem) {
   switch (g.dtype) {
     case kF32: return pipelined_t<float>(g, bwd, smem);
     case kF16: return pipelined_t<__half>(g, bwd, smem);
+    case kF64: return nullptr;  // f64 runs on the two-kernel path only
     default: return pipelined_t<__nv_bfloat16>(g, bwd, smem);
   }
 }

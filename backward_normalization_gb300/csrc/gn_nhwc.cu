@@ -382,6 +382,7 @@ const void* nhwc_kernel(const Geom& g, bool bwd, int second, size_t* smem) {
   switch (g.dtype) {
     case kF32: return kernel_vw<float>(g, bwd, second, smem);
     case kF16: return kernel_vw<__half>(g, bwd, second, smem);
+    case kF64: return kernel_vw<double>(g, bwd, second, smem);
     default: return kernel_vw<__nv_bfloat16>(g, bwd, second, smem);
   }
 }
@@ -390,6 +391,7 @@ cudaError_t launch_nhwc(const KParams& p, cudaStream_t s, bool bwd) {
   switch (p.g.dtype) {
     case kF32: return dispatch_vw<float>(p, s, bwd);
     case kF16: return dispatch_vw<__half>(p, s, bwd);
+    case kF64: return dispatch_vw<double>(p, s, bwd);
     default: return dispatch_vw<__nv_bfloat16>(p, s, bwd);
   }
 }

@@ -105,7 +105,7 @@ int64_t resident_clusters(const Geom& g, int op) {
 // and the channels_last backward the two-kernel path is faster today (the
 // resident kernel cannot keep every SM streaming there).
 bool resident_preferred(const Geom& g, int op) {
-  const int esz = g.dtype == kF32 ? 4 : 2;
+  const int esz = dtype_size(g.dtype);
   if (g.layout == kNHWC) return op == kFwd;
   return g.Cg * g.HW * esz <= (1 << 20);
 }
@@ -113,10 +113,10 @@ bool resident_preferred(const Geom& g, int op) {
 // Fills the resident-regime fields of g; false when the problem does not fit
 // the regime (the two-kernel path then runs).
 bool plan_resident(Geom& g, int op) {
-  const int esz = g.dtype == kF32 ? 4 : 2;
+  const int esz = dtype_size(g.dtype);
   const int vec = 16 / esz;
   const int nten = op == kBwd ? 2 : 1;
-  if (g.vw != vec) return false;
+  if (g.vw != vec || g.dtype == kF64) return false;  // f64: two-kernel path only
   Geom r = g;
   size_t red_f, xch_f, tot_f, grp_f;
   int64_t nch;  // chunks per slice
@@ -264,10 +264,10 @@ int64_t pipelined_ctas(const Geom& g, int op, int sm_count) {
 // Fills the pipelined-regime fields of g (a two-kernel plan of the same
 // problem); false when the problem does not fit the regime.
 bool plan_pipelined(Geom& g, int op, int sm_count) {
-  const int esz = g.dtype == kF32 ? 4 : 2;
+  const int esz = dtype_size(g.dtype);
   const int vec = 16 / esz;
   const int nten = op == kBwd ? 2 : 1;
-  if (g.layout != kNCHW || g.mode != 0 || g.vw != vec) return false;
+  if (g.layout != kNCHW || g.mode != 0 || g.vw != vec || g.dtype == kF64) return false;
   const int64_t unit_bytes = g.Cg * g.HW * esz * nten;
   if ((kPipeLag + 1) * unit_bytes > kPipeL2Bytes) return false;
   Geom r = g;
@@ -446,7 +446,7 @@ Geom plan_geom(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout, 
   g.Cg = C / G;
   g.layout = layout;
   g.dtype = dtype;
-  const int esz = dtype == kF32 ? 4 : 2;
+  const int esz = dtype_size(dtype);
   const int vec = 16 / esz;
   // One item per CTA of the first kernel, and as many items as fit on the
   // device at once (one wave) unless the problem needs more.

@@ -182,7 +182,7 @@ __device__ __forceinline__ void run_ring(const KParams& p, const RingSmem& R, De
   const int64_t U = g.units_fin, D = g.lag, piece = blockIdx.x;
   const char* xb = static_cast<const char*>(p.x);
   const char* db = static_cast<const char*>(p.dy);
-  const int esz = g.dtype == kF32 ? 4 : 2;
+  const int esz = dtype_size(g.dtype);
   __shared__ int s_ok;
   if (threadIdx.x == 0) {
     for (int i = 0; i < R.S; ++i) mbar_init(R.full + i, 1);

@@ -21,8 +21,8 @@ LIB_PATH = os.path.join(HERE, "libgn.so")
 GN_OK, GN_ERR_INVALID, GN_ERR_UNSUPPORTED, GN_ERR_WORKSPACE, GN_ERR_CUDA = range(5)
 OP_FWD, OP_BWD = 0, 1
 LAYOUT = {"nchw": 0, "nhwc": 1}
-DTYPE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
-DTYPE_NAME = {"f32": 0, "f16": 1, "bf16": 2}
+DTYPE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2, torch.float64: 3}
+DTYPE_NAME = {"f32": 0, "f16": 1, "bf16": 2, "f64": 3}
 
 _I64 = ctypes.c_int64
 _VP = ctypes.c_void_p

@@ -16,14 +16,14 @@ import dataclasses
 
 import torch
 
-DTYPES = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
+DTYPES = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16, "f64": torch.float64}
 LAYOUTS = {"nchw": 0, "nhwc": 1}
 
 
 @dataclasses.dataclass(frozen=True)
 class Workload:
     name: str
-    dtype: str          # "f32" | "f16" | "bf16"  (x, y, dy, dx)
+    dtype: str          # "f32" | "f16" | "bf16" | "f64"  (x, y, dy, dx)
     layout: str         # "nchw" | "nhwc"
     N: int
     C: int
@@ -71,21 +71,22 @@ WORKLOADS = [
 BY_NAME = {w.name: w for w in WORKLOADS}
 
 
-def _draw(spec, n, gen, device):
+def _draw(spec, n, gen, device, dtype=torch.float32):
     kind = spec[0]
     if kind == "normal":
-        t = torch.randn(n, generator=gen, device=device, dtype=torch.float32)
+        t = torch.randn(n, generator=gen, device=device, dtype=dtype)
         return t.mul_(spec[2]).add_(spec[1])
     if kind == "uniform":
-        t = torch.rand(n, generator=gen, device=device, dtype=torch.float32)
+        t = torch.rand(n, generator=gen, device=device, dtype=dtype)
         return t.mul_(spec[2] - spec[1]).add_(spec[1])
     if kind == "const":
-        return torch.full((n,), float(spec[1]), device=device, dtype=torch.float32)
+        return torch.full((n,), float(spec[1]), device=device, dtype=dtype)
     raise ValueError(spec)
 
 
 def _activation(w: Workload, spec, gen, device, offset):
-    t = _draw(spec, w.E, gen, device)
+    # f64 activations are drawn in f64 (most values then lie between fp32 values)
+    t = _draw(spec, w.E, gen, device, torch.float64 if w.dtype == "f64" else torch.float32)
     if offset is not None:
         # one value per channel, shared by every n and every spatial position
         if w.layout == "nchw":

@@ -23,10 +23,14 @@
  * Tensors are densely packed in one of these layouts; strided views are not
  * accepted.
  *
- * Types: x, y, dy, dx are all of `dtype` (fp32, fp16 or bf16); every
+ * Types: x, y, dy, dx are all of `dtype` (fp32, fp16, bf16 or fp64); every
  * reduction and every intermediate is fp32.  gamma, beta, dgamma, dbeta are
  * fp32 [C]; mean and rstd are fp32 [N*G] indexed n*G + g.  y and dx are
- * rounded once, to nearest even, from fp32.
+ * rounded once, to nearest even, from fp32.  fp64 is a storage type
+ * ("baracuda-kernels src/norm/group_norm_backward.rs", GroupNormBackwardPlan::
+ * select: f64 among the wired element types, under a precision guarantee of
+ * fp32 math with an fp32 accumulator): its values are converted to fp32 on
+ * load and written back exactly; it runs on the two-kernel path only.
  *
  * Ownership and execution: every pointer except `workspace_bytes`-sized
  * scalars is a DEVICE pointer owned by the caller.  The library allocates
@@ -64,7 +68,12 @@ extern "C" {
 #endif
 
 typedef enum gn_layout { GN_LAYOUT_NCHW = 0, GN_LAYOUT_NHWC = 1 } gn_layout;
-typedef enum gn_dtype { GN_DTYPE_F32 = 0, GN_DTYPE_F16 = 1, GN_DTYPE_BF16 = 2 } gn_dtype;
+typedef enum gn_dtype {
+  GN_DTYPE_F32 = 0,
+  GN_DTYPE_F16 = 1,
+  GN_DTYPE_BF16 = 2,
+  GN_DTYPE_F64 = 3 /* storage only: fp32 arithmetic (see above) */
+} gn_dtype;
 typedef enum gn_op { GN_OP_FWD = 0, GN_OP_BWD = 1 } gn_op;
 
 /* Status codes ("baracuda-kernels src/norm/group_norm_backward.rs",

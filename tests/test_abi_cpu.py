@@ -184,6 +184,27 @@ def test_finalisation_placement(gn):
     assert d.regime == 1 and d.finalise_second == 0
 
 
+def test_f64_storage_plans(gn):
+    """fp64 is accepted as a storage type: 16-byte vectors of two doubles, or
+    the scalar path, always on the two-kernel path (whatever regime is
+    asked for); the row family does not take it."""
+    d = gn.plan_info(0, 2, 16, 4096, 4, "nchw", "f64")
+    assert (d.regime, d.vector_width, d.launches) == (0, 2, 2)
+    assert gn.plan_info(1, 3, 40, 99, 8, "nhwc", "f64").vector_width == 2
+    assert gn.plan_info(1, 2, 3, 25, 3, "nhwc", "f64").vector_width == 1   # 3 doubles: not 16 B
+    assert gn.plan_info(0, 2, 6, 63, 3, "nchw", "f64").vector_width == 1   # 63 doubles per plane
+    for reg in (gn.REGIME_RESIDENT, gn.REGIME_PIPELINED):
+        gn.set_regime(reg)
+        try:
+            assert gn.plan_info(1, 2, 16, 4096, 4, "nchw", "f64").regime == 0
+            assert gn.plan_info(0, 8, 64, 1024, 8, "nhwc", "f64").regime == 0
+        finally:
+            gn.set_regime(gn.REGIME_AUTO)
+    # workspace of an f64 problem: the same records as the fp32 one
+    assert gn.lib().gn_workspace_size(1, 2, 16, 4096, 4, 0, 3) > 0
+    assert gn.lib().ln_workspace_size(16, 64, 3) == 0
+
+
 def test_configs_cover_both_layouts_and_vector_paths(gn):
     seen = set()
     for w in synth.WORKLOADS:

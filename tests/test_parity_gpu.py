@@ -49,6 +49,13 @@ def _small_cases():
         ("fp32_nhwc_2x1200x2x3_g15_straddle", c0.scaled(name="strad", layout="nhwc", N=2, C=1200, G=15, H=2, W=3)),
         # blocks of 8 planes cut groups of 12 planes
         ("fp32_nchw_2x36x10x10_g3_row_blocks", c0.scaled(name="blk", N=2, C=36, G=3, H=10, W=10)),
+        # fp64 storage (computed in fp32): row blocks, plane chunks, channels-last vectors
+        # of two doubles that span groups (Cg = 5), and both scalar paths
+        ("fp64_nchw_2x32x16x16_g8", c0.scaled(name="d0", dtype="f64")),
+        ("fp64_nchw_2x16x64x64_g4", c0.scaled(name="d1", dtype="f64", C=16, G=4, H=64, W=64)),
+        ("fp64_nhwc_3x40x9x11_g8", c0.scaled(name="d2", dtype="f64", layout="nhwc", N=3, C=40, G=8, H=9, W=11)),
+        ("fp64_nchw_2x6x7x9_g3_scalar", c0.scaled(name="d3", dtype="f64", C=6, G=3, H=7, W=9)),
+        ("fp64_nhwc_2x3x5x5_g3_scalar", c0.scaled(name="d4", dtype="f64", layout="nhwc", C=3, G=3, H=5, W=5)),
     ]
 
 
