@@ -369,21 +369,29 @@ def time_rows(gn, synth, torch, flush, reps=20):
     return out
 
 
-def run_e2e(args, torch, dist, world, stream, x, dy, gm, bt, y, dx, mean, rstd, dg, db, step,
-            flush, bytes_step):
+def run_e2e(args, torch, dist, world, stream, x, dy, gm, bt, y, dx, mean, rstd, dg, db, fwd,
+            bwd, flush, bytes_step):
     """The same metric through the C ABI with pinned host buffers: every step
-    copies x, dy, gamma, beta in and y, dx, mean, rstd, dgamma, dbeta out."""
+    copies x, dy, gamma, beta in and y, dx, mean, rstd, dgamma, dbeta out.
+    The host link moves about 210 GB/s each way here (copy engines and SM
+    loads alike) and more with both directions busy, so the copies follow the
+    op's data flow: an input stream brings gamma, beta and x, then dy; the
+    forward starts once x has landed (dy arrives meanwhile); an output stream
+    sends y, mean and rstd back while the backward runs; dx and the parameter
+    gradients follow the backward.  All of it lies between the step's events."""
     w_numel = x.numel()
     hx = x.cpu().pin_memory()
     hdy = dy.cpu().pin_memory()
     hg, hb = gm.cpu().pin_memory(), bt.cpu().pin_memory()
     hy = torch.empty_like(hx).pin_memory()
     hdx = torch.empty_like(hx).pin_memory()
-    hst = torch.empty(mean.numel() + rstd.numel() + dg.numel() + db.numel(),
-                      dtype=torch.float32).pin_memory()
+    hmean, hrstd = mean.cpu().pin_memory(), rstd.cpu().pin_memory()
+    hdg, hdb = dg.cpu().pin_memory(), db.cpu().pin_memory()
     h2d = (hx.numel() + hdy.numel()) * hx.element_size() + (hg.numel() + hb.numel()) * 4
-    d2h = (hy.numel() + hdx.numel()) * hy.element_size() + hst.numel() * 4
+    d2h = ((hy.numel() + hdx.numel()) * hy.element_size()
+           + (hmean.numel() + hrstd.numel() + hdg.numel() + hdb.numel()) * 4)
     assert hx.numel() == w_numel
+    s_in, s_out = torch.cuda.Stream(device=x.device), torch.cuda.Stream(device=x.device)
     Ke = max(3, min(10, args.steps))
     times = []
     for k in range(Ke + 2):
@@ -392,15 +400,30 @@ def run_e2e(args, torch, dist, world, stream, x, dy, gm, bt, y, dx, mean, rstd, 
             dist.barrier()
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
+        x_in, dy_in, f_done = torch.cuda.Event(), torch.cuda.Event(), torch.cuda.Event()
         a.record(stream)
-        x.copy_(hx, non_blocking=True)
-        dy.copy_(hdy, non_blocking=True)
-        gm.copy_(hg, non_blocking=True)
-        bt.copy_(hb, non_blocking=True)
-        step()
-        hy.copy_(y, non_blocking=True)
+        s_in.wait_stream(stream)
+        with torch.cuda.stream(s_in):
+            gm.copy_(hg, non_blocking=True)
+            bt.copy_(hb, non_blocking=True)
+            x.copy_(hx, non_blocking=True)
+            x_in.record(s_in)
+            dy.copy_(hdy, non_blocking=True)
+            dy_in.record(s_in)
+        stream.wait_event(x_in)
+        fwd()
+        f_done.record(stream)
+        s_out.wait_event(f_done)
+        with torch.cuda.stream(s_out):
+            hy.copy_(y, non_blocking=True)
+            hmean.copy_(mean, non_blocking=True)
+            hrstd.copy_(rstd, non_blocking=True)
+        stream.wait_event(dy_in)
+        bwd()
         hdx.copy_(dx, non_blocking=True)
-        hst.copy_(torch.cat([mean, rstd, dg, db]), non_blocking=True)
+        hdg.copy_(dg, non_blocking=True)
+        hdb.copy_(db, non_blocking=True)
+        stream.wait_stream(s_out)
         b.record(stream)
         torch.cuda.synchronize()
         if k >= 2:
@@ -444,18 +467,26 @@ def run_ours(args, rank, world, local_rank):
         # leaves clean ones, so no write-back lands in the next timed kernel
         torch.sum(flush_buf, dim=0, out=flush_out)
 
+    def fwd():
+        rc = gn.fwd_raw(x, w.N, w.C, w.HW, w.G, w.layout, gm, bt, w.eps, y, mean, rstd, ws, stream)
+        if rc:
+            raise RuntimeError(f"gn_fwd failed: {rc}")
+
+    def bwd():
+        rc = gn.bwd_raw(dy, x, mean, rstd, gm, w.N, w.C, w.HW, w.G, w.layout, dx, dg, db, ws, stream)
+        if rc:
+            raise RuntimeError(f"gn_bwd failed: {rc}")
+        grad_sum(dg, db)  # dgamma/dbeta over all ranks, rank order (no-op on one rank)
+
     def step(evs=None):
         if evs:
             gn.set_timing_events(evs[0], evs[1], evs[2])
-        rc = gn.fwd_raw(x, w.N, w.C, w.HW, w.G, w.layout, gm, bt, w.eps, y, mean, rstd, ws, stream)
+        fwd()
         if evs:
             gn.set_timing_events(evs[3], evs[4], evs[5])
-        rc |= gn.bwd_raw(dy, x, mean, rstd, gm, w.N, w.C, w.HW, w.G, w.layout, dx, dg, db, ws, stream)
+        bwd()
         if evs:
             gn.set_timing_events()
-        if rc:
-            raise RuntimeError(f"gn call failed: {rc}")
-        grad_sum(dg, db)  # dgamma/dbeta over all ranks, rank order (no-op on one rank)
 
     for _ in range(args.warmup):
         step()
@@ -513,7 +544,7 @@ def run_ours(args, rank, world, local_rank):
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(args, torch, dist, world, stream, x, dy, gm, bt, y, dx, mean, rstd, dg, db,
-                      step, flush, bytes_step)
+                      fwd, bwd, flush, bytes_step)
 
     if rank != 0:
         return 0
@@ -573,7 +604,7 @@ def run_ours(args, rank, world, local_rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--steps", type=int, default=1500)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-per-config", action="store_true")
