@@ -235,7 +235,6 @@ __global__ void __launch_bounds__(544, 1) resident_kernel(const __grid_constant_
 #pragma unroll
   for (int q = 0; q < 2 * VW; ++q) acc[q] = 0.f;
 
-  using Raw = typename Access<T, VW>::Raw;
   const int64_t rowp = g.Cb * ESZ;  // NHWC: bytes per row in shared memory
   // Folds chunk i (at `slot`) into acc.
   auto consume = [&](const char* slot, int i) {
@@ -245,10 +244,10 @@ __global__ void __launch_bounds__(544, 1) resident_kernel(const __grid_constant_
       const int64_t nv = (((a + g.chunk < e1) ? a + g.chunk : e1) - a) / VW;
       for (int64_t v = tid; v < nv; v += nc) {
         float xv[VW];
-        Access<T, VW>::unpack(*reinterpret_cast<const Raw*>(slot + v * 16), xv);
+        Access<T, VW>::unpack(lds16(slot + v * 16), xv);
         if (BWD) {
           float dv[VW];
-          Access<T, VW>::unpack(*reinterpret_cast<const Raw*>(slot + g.ten_stride + v * 16), dv);
+          Access<T, VW>::unpack(lds16(slot + g.ten_stride + v * 16), dv);
 #pragma unroll
           for (int k = 0; k < VW; ++k) {
             acc[0] += dv[k];
@@ -269,10 +268,10 @@ __global__ void __launch_bounds__(544, 1) resident_kernel(const __grid_constant_
       for (int64_t r = rl; r < rows; r += g.rpi) {
         const int64_t off = r * rowp + (int64_t)j * 16;
         float xv[VW];
-        Access<T, VW>::unpack(*reinterpret_cast<const Raw*>(slot + off), xv);
+        Access<T, VW>::unpack(lds16(slot + off), xv);
         if (BWD) {
           float dv[VW];
-          Access<T, VW>::unpack(*reinterpret_cast<const Raw*>(slot + g.ten_stride + off), dv);
+          Access<T, VW>::unpack(lds16(slot + g.ten_stride + off), dv);
 #pragma unroll
           for (int k = 0; k < VW; ++k) {
             acc[2 * k] += dv[k];
@@ -462,10 +461,10 @@ __global__ void __launch_bounds__(544, 1) resident_kernel(const __grid_constant_
         const int64_t nv = (((a + g.chunk < e1) ? a + g.chunk : e1) - a) / VW;
         for (int64_t v = tid; v < nv; v += nc) {
           float xv[VW];
-          Access<T, VW>::unpack(*reinterpret_cast<const Raw*>(slot + v * 16), xv);
+          Access<T, VW>::unpack(lds16(slot + v * 16), xv);
           if (BWD) {
             float dv[VW];
-            Access<T, VW>::unpack(*reinterpret_cast<const Raw*>(slot + g.ten_stride + v * 16), dv);
+            Access<T, VW>::unpack(lds16(slot + g.ten_stride + v * 16), dv);
 #pragma unroll
             for (int k = 0; k < VW; ++k) xv[k] = fmaf(ca[k], dv[k], fmaf(cb[k], xv[k] - cm[k], cd[k]));
           } else {
@@ -480,10 +479,10 @@ __global__ void __launch_bounds__(544, 1) resident_kernel(const __grid_constant_
         for (int64_t r = rl; r < rows; r += g.rpi) {
           const int64_t off = r * rowp + (int64_t)j * 16;
           float xv[VW];
-          Access<T, VW>::unpack(*reinterpret_cast<const Raw*>(slot + off), xv);
+          Access<T, VW>::unpack(lds16(slot + off), xv);
           if (BWD) {
             float dv[VW];
-            Access<T, VW>::unpack(*reinterpret_cast<const Raw*>(slot + g.ten_stride + off), dv);
+            Access<T, VW>::unpack(lds16(slot + g.ten_stride + off), dv);
 #pragma unroll
             for (int k = 0; k < VW; ++k) xv[k] = fmaf(ca[k], dv[k], fmaf(cb[k], xv[k] - cm[k], cd[k]));
           } else {
