@@ -61,6 +61,7 @@ cudaError_t prepare_resident_kernel(const void* kernel, const Geom& g) {
 
 namespace {
 constexpr size_t kSmemPerCta = 227 * 1024 - 1024;  // dynamic smem budget (static use ~1 KB)
+constexpr size_t kSmemPerSm = 228 * 1024;           // shared memory of one SM
 constexpr size_t kSmallSlice = 88 * 1024;           // slice that lets two CTAs share an SM
 constexpr int64_t kMaxUnitBytes = 16ll << 20;       // per-unit input (x, or x + dy)
 constexpr int kRingDeep = 8;                        // ring slots when a slice streams
@@ -110,9 +111,19 @@ bool resident_preferred(const Geom& g, int op) {
   return g.Cg * g.HW * esz <= (1 << 20);
 }
 
+// Input that counts as tiny for the automatic choice (see plan_resident).
+constexpr double kResidentTinyBytes = 1 << 20;
+
 // Fills the resident-regime fields of g; false when the problem does not fit
-// the regime (the two-kernel path then runs).
-bool plan_resident(Geom& g, int op) {
+// the regime (the two-kernel path then runs).  For the automatic choice
+// (`auto_choice`) the regime is also declined unless one wave of clusters
+// covers every unit, or the input is tiny: measured on GB300, a cluster's
+// load / reduce / write phases barely overlap, so later waves cost nearly a
+// whole cluster latency each (bf16 channels-last 8x320x64x64 G32: 22.3 us
+// resident against 28.8 us two-kernel in one wave of 32 clusters, but 38.7
+// against 34.9 us at N = 16 and 127.8 against 89.0 us at N = 64; fp32 NCHW
+// 512x32x16x16 G8: 248 against 28 us).
+bool plan_resident(Geom& g, int op, bool auto_choice) {
   const int esz = dtype_size(g.dtype);
   const int vec = 16 / esz;
   const int nten = op == kBwd ? 2 : 1;
@@ -207,7 +218,16 @@ bool plan_resident(Geom& g, int op) {
   r.l1 = 1;
   r.Tp = 0;
   r.groups1 = 0;
-  if (resident_clusters(r, op) == 0) return false;
+  const int64_t nc = resident_clusters(r, op);
+  if (nc == 0) return false;
+  if (auto_choice) {
+    // co-resident clusters (an estimate when no device is visible: one or two
+    // CTAs per SM by shared memory)
+    const int64_t waves_of =
+        nc > 0 ? nc : (int64_t)device_sm_count() * (r.smem <= kSmemPerSm / 2 ? 2 : 1) / r.K;
+    const double in_bytes = (double)g.N * g.C * g.HW * esz * nten;
+    if (r.units > waves_of && in_bytes > kResidentTinyBytes) return false;
+  }
   g = r;
   return true;
 }
@@ -239,7 +259,6 @@ constexpr int64_t kPipeL2Bytes = GN_PIPE_L2_BYTES;  // the D + 1 units in flight
 constexpr int kPipeMaxSlots = GN_PIPE_MAX_SLOTS;
 constexpr int kPipeCtasPerSm = GN_PIPE_CTAS_PER_SM;
 constexpr int kPipeMinSlots = 4;
-constexpr size_t kSmemPerSm = 228 * 1024;
 
 // CTAs of the pipelined kernel that fit on the device at once, or an estimate
 // (kPipeCtasPerSm per SM) when no device is visible; 0 if none fit.
@@ -518,14 +537,14 @@ Geom plan_geom(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout, 
   g.regime = kRegimeGeneric;
   const int ov = g_regime_override.load();
   if (ov == kRegimeResident) {
-    plan_resident(g, op);  // wherever the problem fits the regime
+    plan_resident(g, op, false);  // wherever the problem fits the regime
   } else if (ov == kRegimePipelined) {
     plan_pipelined(g, op, sm_count);
   } else if (ov == kRegimeAuto && resident_preferred(g, op)) {
     // measured on GB300: the pipelined kernel moves the minimal traffic but is
     // slower than these families on every workload here (its steps are
     // latency-bound), so it runs only when asked for
-    plan_resident(g, op);
+    plan_resident(g, op, true);
   }
   if (g.regime == kRegimeGeneric) plan_fin2(g);
   const int64_t pipe = g.regime == kRegimePipelined ? 2 * g.units_fin + 3 : 0;

@@ -205,6 +205,21 @@ def test_f64_storage_plans(gn):
     assert gn.lib().ln_workspace_size(16, 64, 3) == 0
 
 
+def test_automatic_resident_choice_needs_one_wave(gn):
+    """The automatic choice takes the resident regime only when one wave of
+    clusters covers every unit, or the input is tiny (at most 1 MB): later
+    waves of clusters cost more than the two-kernel path saves."""
+    assert gn.plan_info(0, 2, 32, 256, 8, "nchw", "f32").regime == 1       # 64 KB
+    assert gn.plan_info(0, 512, 32, 256, 8, "nchw", "f32").regime == 0     # 4096 units
+    assert gn.plan_info(0, 8, 320, 4096, 32, "nhwc", "bf16").regime == 1   # 32 clusters
+    assert gn.plan_info(0, 64, 320, 4096, 32, "nhwc", "bf16").regime == 0  # 256 clusters
+    gn.set_regime(gn.REGIME_RESIDENT)  # asked for: wherever the problem fits
+    try:
+        assert gn.plan_info(0, 512, 32, 256, 8, "nchw", "f32").regime == 1
+    finally:
+        gn.set_regime(gn.REGIME_AUTO)
+
+
 def test_configs_cover_both_layouts_and_vector_paths(gn):
     seen = set()
     for w in synth.WORKLOADS:
