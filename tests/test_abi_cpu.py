@@ -29,8 +29,8 @@ def _declared_symbols():
     for h in os.listdir(os.path.join(ROOT, "include")):
         if h.endswith(".h"):
             txt = open(os.path.join(ROOT, "include", h)).read()
-            names += re.findall(r"GN_API[^;{(]*?\b(gn_\w+)\s*\(", txt)
-    return sorted(set(names))
+            names += re.findall(r"GN_API[^;{(]*?\b(\w+)\s*\(", txt)
+    return sorted(n for n in set(names) if not n.startswith("__"))  # not the macro itself
 
 
 def test_every_declared_symbol_is_exported(gn):
