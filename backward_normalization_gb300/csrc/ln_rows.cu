@@ -119,12 +119,13 @@ __device__ __forceinline__ void load_param(const float* p, int64_t c0, float dfl
 }
 
 // ------------------------------------------------------------------ forward
-// Three CTAs per SM (at most 85 registers) while a thread holds at most 16
-// values: measured on GB300 the large forwards gain (LayerNorm bf16
-// 131072x4096 454 -> 443 us, RMSNorm 361 -> 350 us); wider threads (and the
-// backward, with its dgamma/dbeta registers) would spill under that bound.
+// Three CTAs per SM (at most 85 registers) while a thread holds at most 64
+// bytes of its row: measured on GB300 the large forwards gain (LayerNorm
+// bf16 131072x4096 454 -> 443 us, RMSNorm 361 -> 350 us); fp32 threads
+// holding 32 values (and the backward, with its dgamma/dbeta registers)
+// would spill under that bound.
 template <typename T, int VW, int VPT, bool kRms>
-__global__ void __launch_bounds__(kRowThreads, (VPT * VW > 16 ? 2 : 3))
+__global__ void __launch_bounds__(kRowThreads, (VPT * VW * (int)sizeof(T) > 64 ? 2 : 3))
     row_fwd(const __grid_constant__ RowParams p) {
   __shared__ float red[kRowThreads / 16];
   const int tw = p.tw, team = threadIdx.x / tw, lane = threadIdx.x % tw;
