@@ -130,14 +130,24 @@ __device__ __forceinline__ void stats_item(const KParams& p, int64_t item, float
         }
       }
     }
-    for (; row < it.row1; row += step) {
-      float v[VW];
-      Access<T, VW>::load(xn + row * g.C, v, row >= keep ? plast : pfirst);
+    if (row < it.row1) {  // the last (< U) rows: one predicated batch, not a row at a time
+      const uint64_t pol = row >= keep ? plast : pfirst;
+      Raw raw[U];
 #pragma unroll
-      for (int k = 0; k < VW; ++k) {
-        const float d = v[k] - K[k];
-        acc[2 * k] += d;
-        acc[2 * k + 1] = fmaf(d, d, acc[2 * k + 1]);
+      for (int u = 0; u < U; ++u)
+        raw[u] = row + u * step < it.row1 ? Access<T, VW>::load_raw(xn + (row + u * step) * g.C, pol)
+                                          : Raw{};
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        if (row + u * step >= it.row1) break;
+        float v[VW];
+        Access<T, VW>::unpack(raw[u], v);
+#pragma unroll
+        for (int k = 0; k < VW; ++k) {
+          const float d = v[k] - K[k];
+          acc[2 * k] += d;
+          acc[2 * k + 1] = fmaf(d, d, acc[2 * k + 1]);
+        }
       }
     }
   }
@@ -193,15 +203,38 @@ __device__ __forceinline__ void reduce_item(const KParams& p, int64_t item, floa
         }
       }
     }
-    for (; row < it.row1; row += step) {
-      const uint64_t pol = row >= keep ? plast : pfirst;
-      float xv[VW], dv[VW];
-      Access<T, VW>::load(xn + row * g.C, xv, pol);
-      Access<T, VW>::load(dyn + row * g.C, dv, pol);
+    if (NG > 1) {  // per-channel group constants: a predicated batch would spill here
+      for (; row < it.row1; row += step) {
+        const uint64_t pol = row >= keep ? plast : pfirst;
+        float xv[VW], dv[VW];
+        Access<T, VW>::load(xn + row * g.C, xv, pol);
+        Access<T, VW>::load(dyn + row * g.C, dv, pol);
 #pragma unroll
-      for (int k = 0; k < VW; ++k) {
-        acc[2 * k] += dv[k];
-        acc[2 * k + 1] = fmaf(dv[k], xv[k] - mu[k], acc[2 * k + 1]);
+        for (int k = 0; k < VW; ++k) {
+          acc[2 * k] += dv[k];
+          acc[2 * k + 1] = fmaf(dv[k], xv[k] - mu[k], acc[2 * k + 1]);
+        }
+      }
+    } else if (row < it.row1) {  // the last (< U) rows: one predicated batch (masked rows add 0)
+      const uint64_t pol = row >= keep ? plast : pfirst;
+      Raw rx[U], rd[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const bool in = row + u * step < it.row1;
+        rx[u] = in ? Access<T, VW>::load_raw(xn + (row + u * step) * g.C, pol) : Raw{};
+        rd[u] = in ? Access<T, VW>::load_raw(dyn + (row + u * step) * g.C, pol) : Raw{};
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        if (row + u * step >= it.row1) break;
+        float xv[VW], dv[VW];
+        Access<T, VW>::unpack(rx[u], xv);
+        Access<T, VW>::unpack(rd[u], dv);
+#pragma unroll
+        for (int k = 0; k < VW; ++k) {
+          acc[2 * k] += dv[k];
+          acc[2 * k + 1] = fmaf(dv[k], xv[k] - mu[k], acc[2 * k + 1]);
+        }
       }
     }
   }
