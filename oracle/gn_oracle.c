@@ -360,5 +360,5 @@ int gno_backward_at(const double* dy, const double* x, int64_t N, int64_t C,
   return rc;
 }
 
-/* Which mistake (if any) this build plants; 0 for the real oracle. */
+/* Which mistake (if any) this compiled copy plants; 0 for the real oracle. */
 int gno_mutant_id(void) { return GNO_MUTANT; }
