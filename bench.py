@@ -34,7 +34,7 @@ L2_FLUSH_BYTES = 512 << 20
 
 
 def esize(dtype: str) -> int:
-    return 4 if dtype == "f32" else 2
+    return {"f32": 4, "f64": 8}.get(dtype, 2)
 
 
 def min_bytes(w):
