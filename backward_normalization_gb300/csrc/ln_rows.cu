@@ -36,6 +36,9 @@ namespace gn {
 namespace {
 
 constexpr int kRowThreads = 256;
+// Dynamic shared memory above which a launch must opt in (the 48 KB default,
+// less room for the kernels' static shared memory).
+constexpr size_t kSmemNoOptIn = 44 * 1024;
 
 struct RowParams {
   const void* x;
@@ -92,6 +95,24 @@ __device__ __forceinline__ float2 team_sum2(float a, float b, int tw, float* red
   else
     __syncthreads();
   return make_float2(sa, sb);
+}
+
+// VW consecutive fp32 values from shared memory (16-byte aligned when VW >= 4).
+template <int VW>
+__device__ __forceinline__ void load_smem(const float* s, int64_t c0, float (&out)[VW]) {
+  if (VW == 8 || VW == 4) {
+#pragma unroll
+    for (int e = 0; e < VW; e += 4) {
+      const float4 f = *reinterpret_cast<const float4*>(s + c0 + e);
+      out[e] = f.x;
+      out[e + 1] = f.y;
+      out[e + 2] = f.z;
+      out[e + 3] = f.w;
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < VW; ++e) out[e] = s[c0 + e];
+  }
 }
 
 // gamma / beta for one vector of features (fp32, VW wide).
@@ -213,10 +234,11 @@ __global__ void __launch_bounds__(kRowThreads, (VPT * VW * (int)sizeof(T) > 64 ?
 // dbeta (teams' per-feature partials before the CTA adds them in team order).
 template <typename T, int VW, int VPT, bool kRms>
 __global__ void __launch_bounds__(kRowThreads) row_bwd(const __grid_constant__ RowParams p) {
-  extern __shared__ float colsum[];
+  extern __shared__ __align__(16) float colsum[];
   __shared__ float red[kRowThreads / 16];
   const int tw = p.tw, team = threadIdx.x / tw, lane = threadIdx.x % tw;
   const int nteams = blockDim.x / tw;
+  float* gs = colsum + (int64_t)2 * nteams * p.N;  // gamma, staged below
   const float inv_n = 1.0f / (float)p.N;
   const T* x = static_cast<const T*>(p.x);
   const T* dy = static_cast<const T*>(p.dy);
@@ -247,6 +269,11 @@ __global__ void __launch_bounds__(kRowThreads) row_bwd(const __grid_constant__ R
   };
   int64_t r0 = (int64_t)blockIdx.x * nteams;
   if (r0 < p.M) fetch(r0, cx, cd, cm, cr);
+  // gamma (1 without one) staged once per CTA after the partials' area, while
+  // the first row is in flight: the rows read it from shared memory instead of
+  // reloading it through L1
+  for (int64_t c = threadIdx.x; c < p.N; c += blockDim.x) gs[c] = p.gamma ? __ldg(p.gamma + c) : 1.f;
+  __syncthreads();
   for (; r0 < p.M; r0 += step) {
     if (r0 + step < p.M) fetch(r0 + step, nx, nd, nm, nr);
     const int64_t row = r0 + team;
@@ -264,7 +291,7 @@ __global__ void __launch_bounds__(kRowThreads) row_bwd(const __grid_constant__ R
     for (int k = 0; k < VPT; ++k) {
       const int64_t vi = lane + (int64_t)k * tw;
       float gm[VW];
-      load_param<VW>(p.gamma, (vi < p.V ? vi : 0) * VW, 1.f, gm);
+      load_smem<VW>(gs, (vi < p.V ? vi : 0) * VW, gm);
 #pragma unroll
       for (int e = 0; e < VW; ++e) {
         xv[k][e] = (xv[k][e] - mean) * rstd;
@@ -282,7 +309,7 @@ __global__ void __launch_bounds__(kRowThreads) row_bwd(const __grid_constant__ R
         const int64_t vi = lane + (int64_t)k * tw;
         if (vi >= p.V) continue;
         float gm[VW], o[VW];
-        load_param<VW>(p.gamma, vi * VW, 1.f, gm);
+        load_smem<VW>(gs, vi * VW, gm);
 #pragma unroll
         for (int e = 0; e < VW; ++e) {
           const float g = gm[e] * dv[k][e];
@@ -445,7 +472,7 @@ int64_t resident(const void* fn, size_t smem) {
   }
   int sms = 0, nb = 0;
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (smem > 48 * 1024)
+  if (smem > kSmemNoOptIn)
     cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fn, kRowThreads, smem) != cudaSuccess)
     nb = 0;
@@ -475,7 +502,8 @@ RowPlan row_plan(int64_t M, int64_t N, int dtype, bool rms, bool bwd, bool align
   pl.tw = pow2ceil(cdiv64(pl.V, vpt));
   if (pl.tw > kRowThreads) return pl;  // rows too long to hold in one CTA's registers
   pl.nteams = kRowThreads / pl.tw;
-  pl.smem = bwd ? sizeof(float) * 2 * (size_t)pl.nteams * (size_t)N : 0;
+  // backward: the teams' partials, then gamma
+  pl.smem = bwd ? sizeof(float) * (2 * (size_t)pl.nteams + 1) * (size_t)N : 0;
   if (pl.smem > 200 * 1024) return pl;
   const int64_t res = resident(kernel_of(pl, dtype, rms, bwd), pl.smem);
   pl.grid = std::min<int64_t>(cdiv64(M, pl.nteams), res > 0 ? res : 1);
@@ -589,14 +617,14 @@ int run_bwd(const void* dy, int64_t ldd, const void* x, int64_t ldx, const float
   p.tw = pl.tw;
   p.want_part = want ? 1 : 0;
   const void* fn = kernel_of(pl, dtype, rms, true);
-  if (pl.smem > 48 * 1024) {
+  if (pl.smem > kSmemNoOptIn) {
     const cudaError_t e =
         cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
     if (e != cudaSuccess) return GN_ERR_CUDA;
   }
   void* args[] = {&p};
   cudaError_t e = cudaLaunchKernel(fn, dim3((unsigned)pl.grid), dim3(kRowThreads), args,
-                                   want ? pl.smem : 0, s);
+                                   pl.smem, s);
   if (e != cudaSuccess || !want) return fail(e);
   // the column kernel, launched early (programmatic dependent launch): it
   // waits for the row kernel's records before reading them
