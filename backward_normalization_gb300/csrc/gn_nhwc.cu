@@ -13,9 +13,9 @@
 //                              last CTA into mean/rstd per group
 //           nhwc_fwd_apply  -> y = (x - mean) * rstd*gamma + beta
 // Backward: nhwc_bwd_reduce -> per-(item, channel) sum(dy), sum(dy*(x-mean));
-//                              merged the same way into the dx coefficients,
-//                              the last sample forms dgamma/dbeta
-//           nhwc_bwd_dx     -> dx = rstd*gamma*dy + B*(x - mean) + D
+//                              merged the same way into the dx coefficients
+//           nhwc_bwd_dx     -> dx = rstd*gamma*dy + B*(x - mean) + D; its first
+//                              CTA forms dgamma/dbeta
 // The second kernel of each op walks items and rows in the reverse order of
 // the first, so it starts on the data the first kernel left in L2.
 #include "gn_finalize.cuh"
