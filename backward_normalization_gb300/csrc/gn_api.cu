@@ -1,14 +1,40 @@
 // gn_api.cu -- the C ABI declared in include/gn.h: argument validation
 // (before anything is enqueued), planning and kernel dispatch.
+#include <atomic>
+#include <cstdlib>
 #include <cstring>
 
 #include "../../include/gn.h"
-#include "gn_internal.h"
+#include "gn_device.cuh"
 
 namespace {
 
 thread_local int t_last_cuda_error = 0;
 thread_local gn::TimingEvents t_events = {nullptr, nullptr, nullptr};
+
+// Fault injection (test hook).  GN_FAULT_LAUNCH makes every call fail with
+// GN_ERR_CUDA after validation and before anything is enqueued, as a failed
+// launch would; GN_FAULT_STALL makes the next wave-regime call withhold one
+// arrival, so that the bounded waits on that unit run out.  The environment
+// variable GN_FAULT_INJECT=launch sets GN_FAULT_LAUNCH at the first call.
+std::atomic<int> g_fault{-1};  // -1: not read from the environment yet
+
+int fault_mode() {
+  int f = g_fault.load(std::memory_order_relaxed);
+  if (f >= 0) return f;
+  const char* e = std::getenv("GN_FAULT_INJECT");
+  f = (e && std::strcmp(e, "launch") == 0) ? GN_FAULT_LAUNCH : GN_FAULT_NONE;
+  int expect = -1;
+  g_fault.compare_exchange_strong(expect, f);
+  return g_fault.load(std::memory_order_relaxed);
+}
+
+// GN_FAULT_STALL applies to one call: the unit whose arrival that call
+// withholds (unit 0), then the mode returns to GN_FAULT_NONE.
+int take_stall() {
+  int f = GN_FAULT_STALL;
+  return g_fault.compare_exchange_strong(f, GN_FAULT_NONE) ? 0 : -1;
+}
 
 int elem_size(int dtype) { return gn::dtype_size(dtype); }
 
@@ -38,6 +64,7 @@ int check_problem(int64_t N, int64_t C, int64_t HW, int64_t G, int layout, int d
 
 int cuda_fail(cudaError_t e) {
   t_last_cuda_error = (int)e;
+  cudaGetLastError();  // a failed launch must not poison the caller's next CUDA call
   return GN_ERR_CUDA;
 }
 
@@ -45,6 +72,7 @@ int cuda_fail(cudaError_t e) {
 int prepare(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout, int dtype,
             bool aligned, void* workspace, size_t workspace_bytes, gn::KParams* p) {
   std::memset(p, 0, sizeof(*p));
+  p->stall_unit = -1;
   p->g = gn::make_geom(op, N, C, HW, G, layout, dtype, aligned);
   if (p->g.regime == gn::kRegimeGeneric && (p->g.items <= 0 || p->g.items > 0x7fffffffLL))
     return GN_ERR_UNSUPPORTED;
@@ -53,6 +81,7 @@ int prepare(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout, int
   char* ws = static_cast<char*>(workspace);
   p->tickets = reinterpret_cast<unsigned*>(ws + w.tickets);
   p->err = reinterpret_cast<unsigned*>(ws + w.err);
+  p->clear_words = (int)(w.clear / sizeof(unsigned));
   // counters: one per unit, the global one, one per level-1 group, then (pipelined)
   // a 64-bit ready record per unit and the count of CTAs done
   const int64_t U = p->g.units_fin;
@@ -70,9 +99,35 @@ int prepare(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout, int
   return GN_OK;
 }
 
-// Enqueues the plan's kernel(s).
+// Zero-fills the workspace's error word and counters ([0, clear_words)) on
+// the call's stream.  Launched with programmatic stream serialisation: it may
+// be scheduled while the previous work on the stream runs, waits for that
+// work to complete before it writes (the previous call may still use the same
+// workspace), and the call's first kernel waits for it in turn.
+__global__ void __launch_bounds__(256) ws_clear(unsigned* ws, int words) {
+  gn::grid_launch_dependents();
+  gn::grid_dependency_wait();
+  for (int i = threadIdx.x; i < words; i += blockDim.x) ws[i] = 0u;
+}
+
+// Enqueues the workspace clear, then the plan's kernel(s).
 cudaError_t launch(const gn::KParams& p, cudaStream_t s, bool bwd) {
   const bool nhwc = p.g.layout == GN_LAYOUT_NHWC;
+  {
+    const gn::TimingEvents& ev = gn::timing_events();
+    if (ev.begin) cudaEventRecord(ev.begin, s);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1, 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, ws_clear, p.err, p.clear_words);
+    if (e != cudaSuccess) return e;
+  }
   switch (p.g.regime) {
     case gn::kRegimeResident: return gn::launch_resident(p, s, bwd);
     case gn::kRegimePipelined: return gn::launch_nchw_pipelined(p, s, bwd);
@@ -99,6 +154,7 @@ size_t ws_size_any_alignment(int op, int64_t N, int64_t C, int64_t HW, int64_t G
 
 namespace gn {
 const TimingEvents& timing_events() { return t_events; }
+int record_cuda_error(cudaError_t e) { return cuda_fail(e); }
 }  // namespace gn
 
 extern "C" {
@@ -137,6 +193,8 @@ int gn_fwd(const void* x, int64_t N, int64_t C, int64_t HW, int64_t G, int layou
   p.mean = mean;
   p.rstd = rstd;
   p.eps = eps;
+  if (fault_mode() == GN_FAULT_LAUNCH) return cuda_fail(cudaErrorLaunchFailure);
+  p.stall_unit = take_stall();
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const cudaError_t e = launch(p, s, false);
   return e == cudaSuccess ? GN_OK : cuda_fail(e);
@@ -152,6 +210,8 @@ int gn_bwd(const void* dy, const void* x, const float* mean, const float* rstd,
   if (C == 0) return GN_OK;
   if (N == 0 || HW == 0) {
     // empty sums: the parameter gradients are zero
+    if ((dgamma || dbeta) && fault_mode() == GN_FAULT_LAUNCH)
+      return cuda_fail(cudaErrorLaunchFailure);
     if (dgamma) {
       const cudaError_t e = cudaMemsetAsync(dgamma, 0, sizeof(float) * (size_t)C, s);
       if (e != cudaSuccess) return cuda_fail(e);
@@ -182,6 +242,8 @@ int gn_bwd(const void* dy, const void* x, const float* mean, const float* rstd,
   p.rstd = const_cast<float*>(rstd);
   p.dgamma = dgamma;
   p.dbeta = dbeta;
+  if (fault_mode() == GN_FAULT_LAUNCH) return cuda_fail(cudaErrorLaunchFailure);
+  p.stall_unit = take_stall();
   const cudaError_t e = launch(p, s, true);
   return e == cudaSuccess ? GN_OK : cuda_fail(e);
 }
@@ -193,11 +255,30 @@ const char* gn_status_string(int status) {
     case GN_ERR_UNSUPPORTED: return "GN_ERR_UNSUPPORTED: unsupported layout, dtype or size";
     case GN_ERR_WORKSPACE: return "GN_ERR_WORKSPACE: workspace missing, misaligned or too small";
     case GN_ERR_CUDA: return "GN_ERR_CUDA: a CUDA call failed";
+    case GN_ERR_TIMEOUT:
+      return "GN_ERR_TIMEOUT: a bounded wait in a kernel ran out; that call's outputs are not valid";
     default: return "unknown gn_status";
   }
 }
 
 int gn_last_cuda_error(void) { return t_last_cuda_error; }
+
+int gn_set_fault_injection(int mode) {
+  if (mode != GN_FAULT_NONE && mode != GN_FAULT_LAUNCH && mode != GN_FAULT_STALL)
+    return GN_ERR_INVALID;
+  g_fault.store(mode);
+  return GN_OK;
+}
+
+int gn_workspace_status(const void* workspace, void* stream) {
+  if (!workspace || !aligned16(workspace)) return GN_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned word = 0;
+  cudaError_t e = cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return word ? GN_ERR_TIMEOUT : GN_OK;
+}
 
 int gn_set_regime(int regime) {
   if (regime != GN_REGIME_AUTO && regime != GN_REGIME_TWO_KERNEL && regime != GN_REGIME_RESIDENT &&
@@ -233,11 +314,26 @@ int gn_plan_info(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout
   out->partials = g.N * g.C * (g.T + (g.l1 > 1 ? g.Tp : 0));
   out->workspace_bytes = gn::ws_layout(op, g).total;
   out->err_offset = gn::ws_layout(op, g).err;
+  out->clear_bytes = gn::ws_layout(op, g).clear;
   out->cluster_ctas = g.regime == gn::kRegimeResident ? g.K : 1;
   out->finalise_second = g.fin2;
   out->level1_items = g.l1 > 1 ? g.l1 : 1;
   const int64_t mc = gn::plan_max_clusters(g, op);
   out->max_clusters = mc > 0 ? (int)mc : 0;
+  // item / piece shape (the boundaries the parity tests sample)
+  if (g.regime == gn::kRegimeResident) {
+    out->piece_elems = g.slice;
+    out->pieces_per_unit = g.K;
+  } else if (g.layout == GN_LAYOUT_NHWC) {
+    out->piece_elems = g.rb;
+    out->pieces_per_unit = g.T;
+  } else if (g.mode == 0) {
+    out->piece_elems = g.L;
+    out->pieces_per_unit = g.T;
+  } else {
+    out->piece_elems = g.RB * g.HW;
+    out->pieces_per_unit = g.items_per_n;
+  }
   if (g.regime == gn::kRegimeResident) {
     out->smem_bytes = g.smem;
   } else if (g.regime == gn::kRegimePipelined) {

@@ -126,13 +126,14 @@ __host__ __device__ inline Fin2Smem fin2_smem(const Geom& g) {
 }
 __host__ __device__ inline int64_t fin2_smem_floats(const Geom& g) { return fin2_smem(g).total; }
 
-// Workspace layout (byte offsets, each 256-byte aligned).
+// Workspace layout (byte offsets; the scratch regions are 256-byte aligned).
 struct WsLayout {
-  size_t tickets;  // uint32 counters: one per finalisation unit, 1 global, one per level-1
-                   // group; pipelined: then (8-byte aligned) a 64-bit ready
+  size_t err;      // uint32 error word at offset 0 (a bounded wait ran out)
+  size_t tickets;  // uint32 counters at offset 16: one per finalisation unit, 1 global, one
+                   // per level-1 group; pipelined: then (8-byte aligned) a 64-bit ready
                    // record per unit and the count of CTAs done.  Sized by
                    // problem_counters(), whichever op and alignment the call has.
-  size_t err;      // uint32 error word (a bounded wait ran out)
+  size_t clear;    // bytes [0, clear) that every call zero-fills before its kernels
   size_t part0;    // N*C*T float2 item partial sums (when l1 > 1)
   size_t part;     // N*C*Tp float2 level-1 partial sums
   size_t chst;     // N*C float2 per-channel results of the finalisation
@@ -159,6 +160,8 @@ struct KParams {
   unsigned* ready;    // pipelined: per unit a 64-bit ready record (8-byte aligned)
   unsigned* queue;    // pipelined: [0] CTAs done
   unsigned* err;
+  int clear_words;    // uint32 words at the start of the workspace cleared before the kernels
+  int stall_unit;     // fault injection: a unit whose arrival is withheld (-1: none)
   float2* part0;      // item partials (== part when l1 == 1)
   float2* part;
   float2* chst;
@@ -166,6 +169,10 @@ struct KParams {
   float* kst;         // forward with fin2: the per-(n, c) shifts x(n, c, hw = 0), saved by
                       // the first kernel (the second may overwrite x in place); aliases chst
 };
+
+// gn_api.cu: records e as this thread's last CUDA error (gn_last_cuda_error),
+// clears the runtime's sticky launch error and returns GN_ERR_CUDA.
+int record_cuda_error(cudaError_t e);
 
 // plan.cpp
 int device_sm_count();

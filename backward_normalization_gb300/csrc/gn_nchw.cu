@@ -611,7 +611,6 @@ cudaError_t run_op(const KParams& p, cudaStream_t s, bool bwd) {
   const Geom& g = p.g;
   const size_t sm1 = sizeof(float) * nchw_smem_floats(g);
   const TimingEvents& ev = timing_events();
-  if (ev.begin) cudaEventRecord(ev.begin, s);
   cudaError_t e = bwd ? launch_pdl(nchw_bwd_reduce<T, VW>, g.items, g.tpb, sm1, s, p)
                       : launch_pdl(nchw_fwd_stats<T, VW>, g.items, g.tpb, sm1, s, p);
   if (e != cudaSuccess) return e;

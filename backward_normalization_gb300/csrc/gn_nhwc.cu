@@ -375,7 +375,6 @@ cudaError_t run_op(const KParams& p, cudaStream_t s, bool bwd) {
   const Geom& g = p.g;
   const size_t sm1 = sizeof(float) * 2 * VW * g.tpb;
   const TimingEvents& ev = timing_events();
-  if (ev.begin) cudaEventRecord(ev.begin, s);
   cudaError_t e = bwd ? launch_pdl(nhwc_bwd_reduce<T, VW, NG>, g.items, g.tpb, sm1, s, p)
                       : launch_pdl(nhwc_fwd_stats<T, VW>, g.items, g.tpb, sm1, s, p);
   if (e != cudaSuccess) return e;

@@ -593,14 +593,15 @@ int64_t problem_counters(const Geom& g) {
 
 WsLayout ws_layout(int op, const Geom& g) {
   WsLayout w{};
-  size_t off = 0;
-  w.tickets = off;
-  // the counter region is the same for both ops and both alignments of a
-  // problem, so that a workspace serves a forward and its backward
+  // the error word first, then the counters; every call clears [0, clear) on
+  // its stream before its kernels run.  The counter region is the same for
+  // both ops and both alignments of a problem, so that a forward and its
+  // backward lay it out alike.
   (void)op;
-  off = align256(off + sizeof(unsigned) * (size_t)problem_counters(g));
-  w.err = off;
-  off = align256(off + sizeof(unsigned));
+  w.err = 0;
+  w.tickets = 16;
+  w.clear = w.tickets + sizeof(unsigned) * (size_t)problem_counters(g);
+  size_t off = align256(w.clear);
   w.part0 = off;
   if (g.l1 > 1) off = align256(off + 2 * sizeof(float) * (size_t)(g.N * g.C * g.T));
   w.part = off;

@@ -608,7 +608,6 @@ cudaError_t launch_resident(const KParams& p_in, cudaStream_t s, bool bwd) {
   cfg.numAttrs = 1;
   void* args[] = {&p};
   const TimingEvents& ev = timing_events();
-  if (ev.begin) cudaEventRecord(ev.begin, s);
   e = cudaLaunchKernelExC(&cfg, fn, args);
   if (ev.mid) cudaEventRecord(ev.mid, s);
   if (ev.end) cudaEventRecord(ev.end, s);

@@ -12,7 +12,8 @@
 // The array exists once per device that loads the library and stays reserved
 // until the process exits.  Every call shares it, so calls that overlap on
 // the GPU (two streams at once, or two host threads) race and must not be
-// made.
+// made.  Like any workspace it needs no clearing: each call zero-fills the
+// counters it uses, on its own stream, before its kernels run.
 #include <mutex>
 
 #include "../../include/gn.h"
@@ -61,15 +62,11 @@ int gn_fwd_static_ws(const void* x, int64_t N, int64_t C, int64_t HW, int64_t G,
     return gn_fwd(x, N, C, HW, G, layout, dtype, gamma, beta, eps, y, mean, rstd, nullptr, 0,
                   stream);
   void* ws = nullptr;
-  cudaError_t e = static_ws_address(&ws);
-  if (e != cudaSuccess) {
-    cudaGetLastError();
-    return GN_ERR_CUDA;
-  }
-  // The area keeps whatever the previous call left; the workspace contract
-  // wants it zero-filled, so clear the part this call uses.
-  e = cudaMemsetAsync(ws, 0, need, static_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return GN_ERR_CUDA;
+  const cudaError_t e = static_ws_address(&ws);
+  if (e != cudaSuccess) return gn::record_cuda_error(e);
+  // gn_fwd validates every argument before it enqueues anything, and clears
+  // the counters of the area at the start of its work on `stream`, so the
+  // contents the previous call left do not matter.
   return gn_fwd(x, N, C, HW, G, layout, dtype, gamma, beta, eps, y, mean, rstd, ws,
                 kStaticWsBytes, stream);
 }

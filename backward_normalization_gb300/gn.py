@@ -18,7 +18,8 @@ import torch
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libgn.so")
 
-GN_OK, GN_ERR_INVALID, GN_ERR_UNSUPPORTED, GN_ERR_WORKSPACE, GN_ERR_CUDA = range(5)
+GN_OK, GN_ERR_INVALID, GN_ERR_UNSUPPORTED, GN_ERR_WORKSPACE, GN_ERR_CUDA, GN_ERR_TIMEOUT = range(6)
+FAULT_NONE, FAULT_LAUNCH, FAULT_STALL = 0, 1, 2
 OP_FWD, OP_BWD = 0, 1
 LAYOUT = {"nchw": 0, "nhwc": 1}
 DTYPE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2, torch.float64: 3}
@@ -41,7 +42,8 @@ class PlanDesc(ctypes.Structure):
                 ("workspace_bytes", ctypes.c_size_t), ("cluster_ctas", ctypes.c_int),
                 ("max_clusters", ctypes.c_int), ("smem_bytes", ctypes.c_size_t),
                 ("err_offset", ctypes.c_size_t), ("finalise_second", ctypes.c_int),
-                ("level1_items", ctypes.c_int)]
+                ("level1_items", ctypes.c_int), ("clear_bytes", ctypes.c_size_t),
+                ("piece_elems", ctypes.c_int64), ("pieces_per_unit", ctypes.c_int64)]
 
 
 _lib = None
@@ -73,6 +75,10 @@ def lib() -> ctypes.CDLL:
         L.gn_fwd_static_ws.argtypes = [_VP, _I64, _I64, _I64, _I64, ctypes.c_int, ctypes.c_int, _VP,
                                        _VP, ctypes.c_float, _VP, _VP, _VP, _VP]
         L.gn_fwd_static_ws.restype = ctypes.c_int
+        L.gn_workspace_status.argtypes = [_VP, _VP]
+        L.gn_workspace_status.restype = ctypes.c_int
+        L.gn_set_fault_injection.argtypes = [ctypes.c_int]
+        L.gn_set_fault_injection.restype = ctypes.c_int
         L.gn_set_regime.argtypes = [ctypes.c_int]
         L.gn_set_regime.restype = ctypes.c_int
         L.gn_set_timing_events.argtypes = [_VP, _VP, _VP]
@@ -186,9 +192,24 @@ def set_timing_events(ev_begin=None, ev_mid=None, ev_end=None) -> None:
 
 
 def alloc_workspace(op, N, C, HW, G, layout, dtype, device="cuda"):
-    """A zero-filled workspace (the library requires zeros before first use)."""
+    """A workspace for gn_fwd / gn_bwd of this problem.  Its contents do not
+    matter: every call clears the counters it uses before its kernels run."""
     n = workspace_size(op, N, C, HW, G, layout, dtype)
-    return torch.zeros(max(n, 16), dtype=torch.uint8, device=device)
+    return torch.empty(max(n, 16), dtype=torch.uint8, device=device)
+
+
+def workspace_status(workspace, stream=None) -> int:
+    """gn_workspace_status: waits for `stream` and returns GN_OK, or
+    GN_ERR_TIMEOUT when a bounded wait of the last call on `workspace` ran out."""
+    return lib().gn_workspace_status(_ptr(workspace), _stream(stream))
+
+
+def set_fault_injection(mode: int) -> None:
+    """Test hook: FAULT_NONE, FAULT_LAUNCH (calls fail before enqueuing
+    anything) or FAULT_STALL (the next wave-regime call withholds one arrival)."""
+    rc = lib().gn_set_fault_injection(int(mode))
+    if rc != GN_OK:
+        raise GnError(rc, "gn_set_fault_injection")
 
 
 def forward(x, N, C, HW, G, layout, gamma=None, beta=None, eps=1e-5, workspace=None,

@@ -40,16 +40,16 @@
  * for the same arguments on the same device.
  *
  * Workspace: a caller-provided device buffer of at least gn_workspace_size()
- * bytes, 16-byte aligned, ZERO-FILLED before its first use (for example with
- * cudaMemsetAsync).  Its first bytes hold the arrival counters, ready flags
- * and task queue of the cross-CTA reductions, laid out alike for both ops and
- * both pointer alignments of one problem (N, C, HW, G, layout, dtype); every
- * call that runs to completion leaves them at zero again, so one workspace
- * serves any sequence of later calls of that problem, either op, without
- * being cleared.  The rest is scratch.  Before a workspace serves a problem of
- * another shape, zero-fill it again (the new problem's counters may lie where
- * the old one kept scratch).  Two calls that are in flight at the same time
- * must not share one workspace.
+ * bytes, 16-byte aligned, borrowed for the duration of the call ("baracuda-
+ * kernels src/norm/group_norm_backward.rs", workspace_size / run: the caller
+ * lends scratch memory sized by the plan).  Its contents are dead between
+ * calls: it may hold anything when a call starts (fresh from a caching
+ * allocator, or left by a call of another shape), because every call first
+ * zero-fills, on `stream`, the few bytes at its start that hold the error
+ * word (offset 0) and the arrival counters of its cross-CTA reductions, and
+ * only then runs its kernels.  The rest is scratch that each call writes
+ * before it reads.  Two calls that are in flight at the same time must not
+ * share one workspace.
  */
 #ifndef GN_H_
 #define GN_H_
@@ -84,7 +84,10 @@ typedef enum gn_status {
   GN_ERR_INVALID = 1,     /* bad sizes, G not dividing C, missing or overlapping buffers */
   GN_ERR_UNSUPPORTED = 2, /* unknown layout or dtype, or a problem too large to launch */
   GN_ERR_WORKSPACE = 3,   /* workspace NULL, not 16-byte aligned or smaller than gn_workspace_size() */
-  GN_ERR_CUDA = 4         /* a CUDA call or kernel launch failed (see gn_last_cuda_error) */
+  GN_ERR_CUDA = 4,        /* a CUDA call or kernel launch failed (see gn_last_cuda_error) */
+  GN_ERR_TIMEOUT = 5      /* gn_workspace_status only: a bounded wait inside a kernel of the
+                             last call on that workspace ran out, so that call's outputs are
+                             not valid */
 } gn_status;
 
 /* Bytes of workspace that gn_fwd (op = GN_OP_FWD) or gn_bwd (op = GN_OP_BWD)
@@ -148,6 +151,37 @@ GN_API int gn_fwd_static_ws(const void* x, int64_t N, int64_t C, int64_t HW, int
                             int layout, int dtype, const float* gamma, const float* beta,
                             float eps, void* y, float* mean, float* rstd, void* stream);
 
+/* Outcome of the kernels of the last gn_fwd / gn_bwd / gn_fwd_static_ws call
+ * that ran on `workspace` (enqueued on `stream`): waits for `stream`, reads
+ * the workspace's error word (offset 0) and returns GN_OK when every bounded
+ * wait of those kernels completed, GN_ERR_TIMEOUT when one ran out (the
+ * call's outputs are then not valid; the next call on the workspace clears
+ * the word again), GN_ERR_WORKSPACE for a NULL or misaligned workspace, or
+ * GN_ERR_CUDA.  Kernels that wait on other CTAs bound every wait (in time,
+ * about 0.2 s, or in polls); a wait that runs out sets the word instead of
+ * hanging, and the kernel then returns. */
+GN_API int gn_workspace_status(const void* workspace, void* stream);
+
+/* Fault injection, a test hook (process-wide).
+ *   GN_FAULT_NONE   normal operation (the default).
+ *   GN_FAULT_LAUNCH every gn_fwd / gn_bwd returns GN_ERR_CUDA after validating
+ *                   its arguments and before enqueuing anything, as a failed
+ *                   launch would (gn_last_cuda_error() reports
+ *                   cudaErrorLaunchFailure); setting the environment variable
+ *                   GN_FAULT_INJECT=launch before the first call does the same.
+ *   GN_FAULT_STALL  the next gn_fwd / gn_bwd that runs on the wave regime
+ *                   withholds the arrival of one piece of unit 0, so the waits
+ *                   on that unit run out: that call's outputs for unit 0 are
+ *                   not valid and gn_workspace_status reports GN_ERR_TIMEOUT.
+ *                   The mode then returns to GN_FAULT_NONE by itself.
+ * Nothing here faults the GPU: every injected failure is made on the host, or
+ * is a wait that nothing satisfies and that gives up within its bound.
+ * Returns a gn_status. */
+#define GN_FAULT_NONE 0
+#define GN_FAULT_LAUNCH 1
+#define GN_FAULT_STALL 2
+GN_API int gn_set_fault_injection(int mode);
+
 /* Static, human-readable name of a status code. */
 GN_API const char* gn_status_string(int status);
 
@@ -164,9 +198,12 @@ GN_API int gn_set_timing_events(void* ev_begin, void* ev_mid, void* ev_end);
 /* Kernel families ("regimes").  GN_REGIME_TWO_KERNEL runs any shape: a
  * reduction kernel (statistics, or the backward group sums) and an
  * elementwise kernel (y, or dx).  GN_REGIME_RESIDENT runs one kernel in which
- * a thread-block cluster holds a whole reduction unit -- one (n, group) span
- * for NCHW, one sample for NHWC -- in shared memory; it is taken for 16-byte
- * aligned inputs whose unit is at most 32 MiB.  GN_REGIME_PIPELINED runs one
+ * a thread-block cluster of up to 16 CTAs owns a whole reduction unit -- one
+ * (n, group) span for NCHW (at most 16 channels per group), one (sample,
+ * block of whole groups of at most 128 channels where possible) for NHWC --
+ * streaming it through shared memory; it is taken for 16-byte aligned fp32 /
+ * fp16 / bf16 inputs whose unit holds at most 16 MiB of input (x, or x and dy).
+ * GN_REGIME_PIPELINED runs one
  * persistent kernel (a cooperative launch, NCHW with HW >= 2048 and 16-byte
  * aligned data): every CTA takes one piece of every (n, group) unit, unit
  * after unit, the second pass of a unit trailing its first by a few units so
@@ -197,13 +234,16 @@ typedef struct gn_plan_desc {
   int cluster_ctas;      /* CTAs per thread-block cluster of the first (or only) kernel */
   int max_clusters;      /* such clusters that fit on the device at once (0: unknown) */
   size_t smem_bytes;     /* dynamic shared memory per CTA of that kernel */
-  size_t err_offset;     /* workspace byte offset of the uint32 error word; the
-                            counters, flags and task queue lie before it */
+  size_t err_offset;     /* workspace byte offset of the uint32 error word (0) */
   int finalise_second;   /* two-kernel path: 1 when every CTA of the second kernel
                             derives its groups' statistics (or dx coefficients)
                             from the partial records itself, 0 when the last
                             arrival of a sample does it in the first kernel */
   int level1_items;      /* items merged per level-1 record (1: none) */
+  size_t clear_bytes;    /* bytes at the start of the workspace (error word and
+                            counters) that the call zero-fills before its kernels */
+  int64_t piece_elems;   /* wave regime: elements (NCHW) or rows (NHWC) per piece */
+  int64_t pieces_per_unit; /* wave regime: pieces of one reduction unit */
 } gn_plan_desc;
 
 /* Fills *out with the plan of gn_fwd/gn_bwd for this problem, assuming every

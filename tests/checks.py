@@ -6,6 +6,13 @@ Tolerances (stated once, used everywhere):
         max |got - ref| / (1 + |ref|)  <= 1e-4
   * fp16 / bf16 outputs (y, dx):  |got - ref| <= 1e-2 + 1e-2 * |ref|
   * dgamma, dbeta:  ||got - ref||_2 / ||ref||_2 <= 1e-3
+  * y, dx over a whole tensor, in addition (assert_out_l2):
+        ||got - ref||_2 / ||ref||_2 <= u + 1e-4
+    with u the unit roundoff of the storage type (2^-8 bf16, 2^-11 fp16,
+    2^-24 fp32): rounding each value to nearest moves it by at most u times
+    its magnitude, so the rounding alone is within u in relative L2, and
+    1e-4 covers the fp32 arithmetic before it.  This catches errors that stay
+    under the elementwise absolute floor of 1e-2 when the outputs are small.
 The reference is always the fp64 oracle, unrounded.
 """
 from __future__ import annotations
@@ -56,6 +63,17 @@ def rel_l2(got, ref) -> float:
     g, r = as_np(got), as_np(ref)
     den = np.linalg.norm(r)
     return float(np.linalg.norm(g - r) / (den if den > 0 else 1.0))
+
+
+UNIT_ROUNDOFF = {"bf16": 2.0 ** -8, "f16": 2.0 ** -11, "f32": 2.0 ** -24, "f64": 2.0 ** -24}
+
+
+def assert_out_l2(name, got, ref, dtype: str):
+    """Relative L2 error of a whole output against the rounding bound."""
+    e = rel_l2(got, ref)
+    bound = UNIT_ROUNDOFF[dtype] + 1e-4
+    assert e <= bound, f"{name}: rel L2 {e:.3e} > {bound:.3e}"
+    return e
 
 
 def assert_param(name, got, ref):

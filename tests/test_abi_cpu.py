@@ -42,7 +42,7 @@ def test_every_declared_symbol_is_exported(gn):
 
 
 def test_status_strings(gn):
-    for s in range(5):
+    for s in range(6):
         assert gn.status_string(s).startswith("GN_")
     assert "unknown" in gn.status_string(99)
 
@@ -226,3 +226,57 @@ def test_configs_cover_both_layouts_and_vector_paths(gn):
         d = gn.plan_info(0, w.N, w.C, w.HW, w.G, w.layout, w.dtype)
         seen.add((w.layout, d.vector_width > 1, d.threads))
     assert {s[0] for s in seen} == {"nchw", "nhwc"}
+
+
+def test_workspace_layout_error_word_first(gn):
+    """The error word sits at offset 0 and the counters after it; each call
+    clears that prefix itself, the same for both ops of a problem."""
+    for w in synth.WORKLOADS:
+        f = gn.plan_info(0, w.N, w.C, w.HW, w.G, w.layout, w.dtype)
+        b = gn.plan_info(1, w.N, w.C, w.HW, w.G, w.layout, w.dtype)
+        assert f.err_offset == 0 and b.err_offset == 0
+        assert f.clear_bytes == b.clear_bytes
+        assert 20 <= f.clear_bytes <= gn.workspace_size(0, w.N, w.C, w.HW, w.G, w.layout, w.dtype)
+
+
+def test_workspace_status_rejects_bad_workspace(gn):
+    assert gn.lib().gn_workspace_status(None, None) == gn.GN_ERR_WORKSPACE
+    assert gn.lib().gn_workspace_status(FAKE + 4, None) == gn.GN_ERR_WORKSPACE
+
+
+def test_fault_injection_launch(gn):
+    """GN_FAULT_LAUNCH: a valid call fails with GN_ERR_CUDA before anything
+    is enqueued (nothing touches the fake pointers), invalid calls are still
+    reported as invalid, and clearing the mode restores normal validation."""
+    gn.set_fault_injection(gn.FAULT_LAUNCH)
+    try:
+        assert _fwd(gn) == gn.GN_ERR_CUDA
+        assert gn.lib().gn_last_cuda_error() == 719  # cudaErrorLaunchFailure
+        assert _bwd(gn) == gn.GN_ERR_CUDA
+        assert _bwd(gn, HW=0, dgamma=FAKE * 7, dbeta=FAKE * 8) == gn.GN_ERR_CUDA
+        assert _fwd(gn, G=3) == gn.GN_ERR_INVALID
+        assert _fwd(gn, ws_bytes=8) == gn.GN_ERR_WORKSPACE
+        assert _fwd(gn, N=0) == 0
+    finally:
+        gn.set_fault_injection(gn.FAULT_NONE)
+    with pytest.raises(gn.GnError):
+        gn.set_fault_injection(9)
+
+
+def test_fault_injection_from_environment(gn):
+    """GN_FAULT_INJECT=launch in the environment of a fresh process."""
+    import subprocess
+    import sys
+
+    code = ("import sys; sys.path.insert(0, %r)\n"
+            "from backward_normalization_gb300 import gn\n"
+            "F = 1 << 20\n"
+            "rc = gn.lib().gn_fwd(F, 2, 8, 16, 2, 0, 0, None, None, 1e-5, F * 2, F * 3, F * 4,"
+            " F * 5, 1 << 30, None)\n"
+            "print(rc, gn.lib().gn_last_cuda_error())\n") % ROOT
+    env = dict(os.environ, GN_FAULT_INJECT="launch")
+    out = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                         timeout=300)
+    assert out.returncode == 0, out.stderr
+    rc, err = map(int, out.stdout.split())
+    assert rc == gn.GN_ERR_CUDA and err == 719

@@ -14,6 +14,7 @@ import torch
 import oracle
 from backward_normalization_gb300 import gn, synth
 from tests import checks
+from tests.cases import SPANNING, SPANNING_NAMES, strong_dy
 
 pytestmark = pytest.mark.gpu
 
@@ -56,10 +57,11 @@ def _small_cases():
         ("fp64_nhwc_3x40x9x11_g8", c0.scaled(name="d2", dtype="f64", layout="nhwc", N=3, C=40, G=8, H=9, W=11)),
         ("fp64_nchw_2x6x7x9_g3_scalar", c0.scaled(name="d3", dtype="f64", C=6, G=3, H=7, W=9)),
         ("fp64_nhwc_2x3x5x5_g3_scalar", c0.scaled(name="d4", dtype="f64", layout="nhwc", C=3, G=3, H=5, W=5)),
-    ]
+    ] + SPANNING
 
 
 SMALL = _small_cases()
+SMALL_BASE = [c for c in SMALL if c[1].name not in SPANNING_NAMES]
 
 # Slices larger than shared memory: the resident regime streams part of each
 # slice through its ring and reads it again in the second pass.
@@ -120,6 +122,8 @@ def _compare(got, ref, w):
 @pytest.mark.parametrize("name,w", SMALL + STREAMING, ids=[c[0] for c in SMALL + STREAMING])
 def test_small_parity(name, w, regime):
     inp = synth.make_inputs(w, "cpu", seed=0)
+    if w.name in SPANNING_NAMES:
+        inp = strong_dy(inp, w)
     got = _gpu_run(inp, w)
     _compare(got, _oracle_full(inp, w), w)
 
@@ -151,6 +155,30 @@ def test_no_affine_and_output_mask(name, w, regime):
     got2 = _gpu_run(inp2, w, gamma=True, beta=False)
     y2, _, _ = o.forward(x, w.N, w.C, w.HW, w.G, L, inp["gamma"].double().numpy(), None, w.eps)
     checks.assert_out("y(no beta)", got2["y"], y2, w.dtype)
+
+
+@pytest.mark.parametrize("name,w", [SMALL[1], SMALL[2], SMALL[3], SMALL[0]],
+                         ids=["nhwc", "nhwc_spanning", "nchw_m0", "nchw_m1"])
+def test_single_parameter_gradient_masks(name, w, regime):
+    """dgamma alone (dbeta NULL) and dbeta alone (dgamma NULL): the requested
+    gradient and dx match the oracle."""
+    inp = synth.make_inputs(w, "cpu", seed=8)
+    ref = _oracle_full(inp, w)
+    dev = "cuda"
+    x, dy = inp["x"].to(dev), inp["dy"].to(dev)
+    gm, bt = inp["gamma"].to(dev), inp["beta"].to(dev)
+    y, mean, rstd = gn.forward(x, w.N, w.C, w.HW, w.G, w.layout, gm, bt, w.eps)
+    ws = gn.alloc_workspace(gn.OP_BWD, w.N, w.C, w.HW, w.G, w.layout, x.dtype)
+    for want_g in (True, False):
+        dx = torch.empty_like(x)
+        out = torch.full((w.C,), 5.0, device=dev)
+        dg, db = (out, None) if want_g else (None, out)
+        rc = gn.bwd_raw(dy, x, mean, rstd, gm, w.N, w.C, w.HW, w.G, w.layout, dx, dg, db, ws)
+        assert rc == gn.GN_OK
+        torch.cuda.synchronize()
+        checks.assert_out("dx", dx, ref["dx"], w.dtype)
+        checks.assert_param("dgamma" if want_g else "dbeta", out,
+                            ref["dgamma"] if want_g else ref["dbeta"])
 
 
 @pytest.mark.parametrize("name,w", [SMALL[1], SMALL[3]], ids=["nhwc", "nchw"])
@@ -206,9 +234,10 @@ def test_in_place(name, w, regime):
 
 
 def test_workspace_reuse_and_canaries(regime):
-    """A workspace zero-filled once serves repeated calls of both ops, its
-    scratch part may hold anything, and nothing is written past the end of the
-    workspace or of any output."""
+    """The workspace's contents are dead between calls: refilled with random
+    bytes before every call, it gives the same bits as the first call; the
+    error word reads clear; nothing is written past the end of the workspace
+    or of any output."""
     w = SMALL[5][1]
     inp = synth.make_inputs(w, "cpu", seed=5)
     ref = _oracle_full(inp, w)
@@ -220,9 +249,7 @@ def test_workspace_reuse_and_canaries(regime):
     wsb = torch.randint(0, 256, (n_ws + 256,), dtype=torch.uint8, device=dev)
     canary_ws = wsb[n_ws:].clone()
     ws = wsb[:n_ws]
-    err_off = gn.plan_info(gn.OP_BWD, w.N, w.C, w.HW, w.G, w.layout, dt).err_offset
-    assert err_off == gn.plan_info(gn.OP_FWD, w.N, w.C, w.HW, w.G, w.layout, dt).err_offset
-    ws[:err_off + 4].zero_()  # counters, flags, task queue and error word (the rest is scratch)
+    gen = torch.Generator(device=dev).manual_seed(55)
 
     def padded(n, dtype):
         b = torch.full((n + 2 * pad,), 7.0, dtype=dtype, device=dev)
@@ -236,13 +263,20 @@ def test_workspace_reuse_and_canaries(regime):
     bb, db = padded(w.C, torch.float32)
     x, dy = inp["x"].to(dev), inp["dy"].to(dev)
     gm, bt = inp["gamma"].to(dev), inp["beta"].to(dev)
+    first = None
     for _ in range(3):
+        ws.copy_(torch.randint(0, 256, (n_ws,), dtype=torch.uint8, device=dev, generator=gen))
         assert gn.fwd_raw(x, w.N, w.C, w.HW, w.G, w.layout, gm, bt, w.eps, y, mean, rstd, ws) == 0
+        ws.copy_(torch.randint(0, 256, (n_ws,), dtype=torch.uint8, device=dev, generator=gen))
         assert gn.bwd_raw(dy, x, mean, rstd, gm, w.N, w.C, w.HW, w.G, w.layout, dx, dg, db, ws) == 0
+        assert gn.workspace_status(ws) == gn.GN_OK
+        got = [t.clone() for t in (y, mean, rstd, dx, dg, db)]
+        if first is None:
+            first = got
+        for a, b in zip(first, got):
+            assert torch.equal(a, b)
     torch.cuda.synchronize()
     assert torch.equal(wsb[n_ws:], canary_ws)
-    assert torch.all(ws[:err_off] == 0), "arrival counters, flags or the task queue not returned to zero"
-    assert int(ws[err_off:err_off + 4].view(torch.int32).item()) == 0, "a bounded wait ran out"
     for b in (yb, dxb, mb, rb, gb, bb):
         assert torch.all(b[:pad] == 7.0) and torch.all(b[-pad:] == 7.0)
     _compare(dict(y=y, mean=mean, rstd=rstd, dx=dx, dgamma=dg, dbeta=db), ref, w)
@@ -261,7 +295,6 @@ def test_workspace_shared_by_fwd_and_bwd(regime):
     ref = _gpu_run(inp, w)
     dt = x.dtype
     ws = gn.alloc_workspace(gn.OP_BWD, w.N, w.C, w.HW, w.G, w.layout, dt)
-    err_off = gn.plan_info(gn.OP_FWD, w.N, w.C, w.HW, w.G, w.layout, dt).err_offset
     for _ in range(2):
         y, mean, rstd = gn.forward(x, w.N, w.C, w.HW, w.G, w.layout, gm, bt, w.eps, workspace=ws)
         dx, dg, db = gn.backward(dy, x, mean, rstd, w.N, w.C, w.HW, w.G, w.layout, gm, workspace=ws)
@@ -269,20 +302,18 @@ def test_workspace_shared_by_fwd_and_bwd(regime):
         got = dict(y=y, mean=mean, rstd=rstd, dx=dx, dgamma=dg, dbeta=db)
         for k in got:
             assert torch.equal(got[k], ref[k]), k
-    assert torch.all(ws[:err_off] == 0)
-    assert int(ws[err_off:err_off + 4].view(torch.int32).item()) == 0
+    assert gn.workspace_status(ws) == gn.GN_OK
 
 
 def test_shared_workspace_across_shapes(regime):
-    """One buffer serves calls of different shapes in a row when it is
-    zero-filled again before each new shape (the contract of gn.h)."""
+    """One buffer, filled with random bytes once and never cleared, serves
+    calls of different shapes in a row (each call clears its own counters)."""
     dev = "cuda"
-    cases = [SMALL[0][1], SMALL[2][1], SMALL[3][1], SMALL[2][1]]
+    cases = [SMALL[0][1], SMALL[2][1], SMALL[3][1], SMALL[2][1], SMALL[5][1], SMALL[0][1]]
     n_ws = max(gn.workspace_size(op, w.N, w.C, w.HW, w.G, w.layout, w.dtype)
                for w in cases for op in (0, 1))
-    ws = torch.zeros((n_ws,), dtype=torch.uint8, device=dev)
+    ws = torch.randint(0, 256, (n_ws,), dtype=torch.uint8, device=dev)
     for i, w in enumerate(cases):
-        ws.zero_()
         inp = synth.make_inputs(w, "cpu", seed=10 + i)
         x, dy = inp["x"].to(dev), inp["dy"].to(dev)
         gm, bt = inp["gamma"].to(dev), inp["beta"].to(dev)
@@ -348,11 +379,98 @@ def test_constant_group_gives_beta(regime):
 
 
 # ------------------------------------------------------------- full sizes
-def _sample_offsets(w, k=4096, seed=0):
+# The two small channels-last workloads are compared element by element in
+# full; the two large ones at sampled offsets chosen per (n, g) group and at
+# the boundaries of the plan's items or pieces (see _boundary_offsets).
+FULL_COMPARE = {"bf16_nhwc_8x320x64x64_g32", "bf16_nhwc_32x512x32x32_g32"}
+
+
+def _boundary_offsets(w, plans, per_group=8, seed=0, max_planes=64):
+    """Flat offsets to check at full size:
+      * per (n, g) group: its first and last element and per_group random ones;
+      * NCHW: the first and last element of every channel plane, and, in
+        max_planes planes (the first, the last and random ones), both sides
+        of every item / piece boundary of each plan;
+      * NHWC: at both rows around every item / piece boundary of each plan,
+        in every sample, the first and last channel of every group."""
     rng = np.random.default_rng(seed)
-    idx = rng.integers(0, w.E, k)
-    edge = [0, w.E - 1, w.E // 2]
-    return np.unique(np.concatenate([idx, edge])).astype(np.int64)
+    N, C, HW, G = w.N, w.C, w.HW, w.G
+    Cg = C // G
+    out = []
+    n = np.repeat(np.arange(N), G)
+    g = np.tile(np.arange(G), N)
+    if w.layout == "nchw":
+        lo = (n * C + g * Cg) * HW
+        span = Cg * HW
+        out += [lo, lo + span - 1]
+        out += [lo + rng.integers(0, span, lo.size) for _ in range(per_group)]
+        planes = np.arange(N * C) * HW
+        out += [planes, planes + HW - 1]
+        pick = np.unique(np.concatenate([[0, N * C - 1], rng.integers(0, N * C, max_planes)]))
+        for d in plans:
+            L = int(d.piece_elems)
+            if 0 < L < HW:
+                cuts = np.arange(L, HW, L)
+                for pl in pick:
+                    out += [pl * HW + cuts - 1, pl * HW + cuts]
+    else:
+        first = n * HW * C + g * Cg
+        last = (n * HW + HW - 1) * C + (g + 1) * Cg - 1
+        out += [first, last]
+        for _ in range(per_group):
+            hw = rng.integers(0, HW, n.size)
+            c = g * Cg + rng.integers(0, Cg, n.size)
+            out.append((n * HW + hw) * C + c)
+        chans = np.concatenate([np.arange(G) * Cg, np.arange(G) * Cg + Cg - 1])
+        for d in plans:
+            rb = int(d.piece_elems)
+            if 0 < rb < HW:
+                rows = np.concatenate([np.arange(rb, HW, rb) - 1, np.arange(rb, HW, rb)])
+                for nn in range(N):
+                    out.append(((nn * HW + rows[:, None]) * C + chans[None, :]).reshape(-1))
+    idx = np.unique(np.concatenate([np.asarray(a, dtype=np.int64).reshape(-1) for a in out]))
+    assert idx.min() >= 0 and idx.max() < w.E
+    return idx
+
+
+def _oracle_by_samples(w, inp, idx=None):
+    """Oracle results for the whole batch, computed a block of samples at a
+    time (sample n's statistics depend on sample n only): full y and dx when
+    idx is None, else y and dx at the flat offsets idx; mean/rstd/dgamma/
+    dbeta in full."""
+    o = oracle.get()
+    L = synth.LAYOUTS[w.layout]
+    gm = inp["gamma"].double().cpu().numpy()
+    bt = inp["beta"].double().cpu().numpy()
+    per_n = w.C * w.HW
+    chunk_n = max(1, min(w.N, (1 << 27) // per_n))  # at most ~128M elements per oracle call
+    r = dict(mean=np.zeros(w.N * w.G), rstd=np.zeros(w.N * w.G), dgamma=np.zeros(w.C),
+             dbeta=np.zeros(w.C))
+    n_out = w.E if idx is None else idx.size
+    r["y"] = np.zeros(n_out)
+    r["dx"] = np.zeros(n_out)
+    for n0 in range(0, w.N, chunk_n):
+        n1 = min(w.N, n0 + chunk_n)
+        lo, hi = n0 * per_n, n1 * per_n
+        xs = inp["x"][lo:hi].double().cpu().numpy()
+        dys = inp["dy"][lo:hi].double().cpu().numpy()
+        if idx is None:
+            ya, m, rs = o.forward(xs, n1 - n0, w.C, w.HW, w.G, L, gm, bt, w.eps)
+            dxa, dg, db = o.backward(dys, xs, n1 - n0, w.C, w.HW, w.G, L, gm, w.eps)
+            r["y"][lo:hi] = ya
+            r["dx"][lo:hi] = dxa
+        else:
+            sel = (idx >= lo) & (idx < hi)
+            ya, m, rs = o.forward_at(xs, n1 - n0, w.C, w.HW, w.G, L, gm, bt, w.eps, idx[sel] - lo)
+            dxa, dg, db = o.backward_at(dys, xs, n1 - n0, w.C, w.HW, w.G, L, gm, w.eps,
+                                        idx[sel] - lo)
+            r["y"][sel] = ya
+            r["dx"][sel] = dxa
+        r["mean"][n0 * w.G:n1 * w.G] = m
+        r["rstd"][n0 * w.G:n1 * w.G] = rs
+        r["dgamma"] += dg
+        r["dbeta"] += db
+    return r
 
 
 FULL = ([(w, "auto") for w in synth.WORKLOADS[1:]]
@@ -361,14 +479,16 @@ FULL = ([(w, "auto") for w in synth.WORKLOADS[1:]]
 
 
 @pytest.mark.parametrize("w,reg", FULL, ids=[f"{w.name}-{r}" for w, r in FULL])
-def test_full_size_sampled(w, reg):
-    """The benchmarked workloads at full size: y and dx at sampled offsets and
-    mean/rstd/dgamma/dbeta in full, against the oracle; plus a bit-identical
-    rerun.  Large NCHW inputs are handed to the oracle one sample at a time
-    (the statistics of sample n depend on sample n only)."""
+def test_full_size(w, reg):
+    """The benchmarked workloads at full size, in the launch configuration
+    the benchmark times: y and dx in full (small workloads) or at per-group
+    and plan-boundary offsets (large ones), with the relative L2 error of the
+    whole of dx against the rounding bound on the small ones; mean, rstd,
+    dgamma and dbeta in full; plus a bit-identical rerun."""
     dev = "cuda"
     gn.set_regime(REGIMES[reg])
     try:
+        plans = [gn.plan_info(op, w.N, w.C, w.HW, w.G, w.layout, w.dtype) for op in (0, 1)]
         inp = synth.make_inputs(w, dev, seed=0)
         got = _gpu_run(inp, w)
         again = _gpu_run(inp, w)
@@ -380,37 +500,19 @@ def test_full_size_sampled(w, reg):
     for k in ("mean", "rstd", "dgamma", "dbeta"):
         assert torch.equal(got[k], again[k]), k
     del again
-    o = oracle.get()
-    L = synth.LAYOUTS[w.layout]
-    gm = inp["gamma"].double().cpu().numpy()
-    bt = inp["beta"].double().cpu().numpy()
-    idx = _sample_offsets(w)
-    per_n = w.C * w.HW
-    chunk_n = max(1, min(w.N, (1 << 27) // per_n))  # at most ~128M elements per oracle call
-    mean_ref = np.zeros(w.N * w.G)
-    rstd_ref = np.zeros(w.N * w.G)
-    dg_ref = np.zeros(w.C)
-    db_ref = np.zeros(w.C)
-    y_ref = np.zeros(idx.size)
-    dx_ref = np.zeros(idx.size)
-    for n0 in range(0, w.N, chunk_n):
-        n1 = min(w.N, n0 + chunk_n)
-        lo, hi = n0 * per_n, n1 * per_n
-        sel = (idx >= lo) & (idx < hi)
-        xs = inp["x"][lo:hi].double().cpu().numpy()
-        dys = inp["dy"][lo:hi].double().cpu().numpy()
-        ya, m, r = o.forward_at(xs, n1 - n0, w.C, w.HW, w.G, L, gm, bt, w.eps, idx[sel] - lo)
-        dxa, dg, db = o.backward_at(dys, xs, n1 - n0, w.C, w.HW, w.G, L, gm, w.eps, idx[sel] - lo)
-        y_ref[sel] = ya
-        dx_ref[sel] = dxa
-        mean_ref[n0 * w.G:n1 * w.G] = m
-        rstd_ref[n0 * w.G:n1 * w.G] = r
-        dg_ref += dg
-        db_ref += db
-    it = torch.from_numpy(idx).to(dev)
-    checks.assert_out("y", got["y"][it], y_ref, w.dtype)
-    checks.assert_out("dx", got["dx"][it], dx_ref, w.dtype)
-    checks.assert_stat("mean", got["mean"], mean_ref)
-    checks.assert_stat("rstd", got["rstd"], rstd_ref)
-    checks.assert_param("dgamma", got["dgamma"], dg_ref)
-    checks.assert_param("dbeta", got["dbeta"], db_ref)
+    if w.name in FULL_COMPARE:
+        ref = _oracle_by_samples(w, inp)
+        checks.assert_out("y", got["y"], ref["y"], w.dtype)
+        checks.assert_out("dx", got["dx"], ref["dx"], w.dtype)
+        checks.assert_out_l2("y", got["y"], ref["y"], w.dtype)
+        checks.assert_out_l2("dx", got["dx"], ref["dx"], w.dtype)
+    else:
+        idx = _boundary_offsets(w, plans)
+        ref = _oracle_by_samples(w, inp, idx)
+        it = torch.from_numpy(idx).to(dev)
+        checks.assert_out("y", got["y"][it], ref["y"], w.dtype)
+        checks.assert_out("dx", got["dx"][it], ref["dx"], w.dtype)
+    checks.assert_stat("mean", got["mean"], ref["mean"])
+    checks.assert_stat("rstd", got["rstd"], ref["rstd"])
+    checks.assert_param("dgamma", got["dgamma"], ref["dgamma"])
+    checks.assert_param("dbeta", got["dbeta"], ref["dbeta"])
