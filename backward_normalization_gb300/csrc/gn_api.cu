@@ -110,12 +110,14 @@ __global__ void __launch_bounds__(256) ws_clear(unsigned* ws, int words) {
   for (int i = threadIdx.x; i < words; i += blockDim.x) ws[i] = 0u;
 }
 
-// Enqueues the workspace clear, then the plan's kernel(s).
+// Enqueues the workspace clear, then the plan's kernel(s).  The wave
+// regime's kernel clears its counters itself (behind a grid barrier of its
+// cooperative launch) and needs no separate clear.
 cudaError_t launch(const gn::KParams& p, cudaStream_t s, bool bwd) {
   const bool nhwc = p.g.layout == GN_LAYOUT_NHWC;
-  {
-    const gn::TimingEvents& ev = gn::timing_events();
-    if (ev.begin) cudaEventRecord(ev.begin, s);
+  const gn::TimingEvents& ev = gn::timing_events();
+  if (ev.begin) cudaEventRecord(ev.begin, s);
+  if (p.g.regime != gn::kRegimeWave) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(1, 1, 1);
     cfg.blockDim = dim3(256, 1, 1);
@@ -131,6 +133,7 @@ cudaError_t launch(const gn::KParams& p, cudaStream_t s, bool bwd) {
   switch (p.g.regime) {
     case gn::kRegimeResident: return gn::launch_resident(p, s, bwd);
     case gn::kRegimePipelined: return gn::launch_nchw_pipelined(p, s, bwd);
+    case gn::kRegimeWave: return gn::launch_wave(p, s, bwd);
     default: return nhwc ? gn::launch_nhwc(p, s, bwd) : gn::launch_nchw(p, s, bwd);
   }
 }
@@ -282,7 +285,7 @@ int gn_workspace_status(const void* workspace, void* stream) {
 
 int gn_set_regime(int regime) {
   if (regime != GN_REGIME_AUTO && regime != GN_REGIME_TWO_KERNEL && regime != GN_REGIME_RESIDENT &&
-      regime != GN_REGIME_PIPELINED)
+      regime != GN_REGIME_PIPELINED && regime != GN_REGIME_WAVE)
     return GN_ERR_INVALID;
   gn::set_regime_override(regime);
   return GN_OK;
@@ -305,12 +308,14 @@ int gn_plan_info(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout
   if (N == 0 || C == 0 || HW == 0) return GN_OK;
   const gn::Geom g = gn::make_geom(op, N, C, HW, G, layout, dtype, aligned != 0);
   out->regime = g.regime;
-  out->launches = g.regime == gn::kRegimeGeneric ? 2 : 1;
+  // the plan's kernels, plus the workspace clear that precedes every regime
+  // but the wave regime (whose kernel clears its counters itself)
+  out->launches = (g.regime == gn::kRegimeGeneric ? 2 : 1) + (g.regime == gn::kRegimeWave ? 0 : 1);
   out->vector_width = g.vw;
   out->threads = g.tpb;
-  out->ctas = g.regime == gn::kRegimeResident    ? g.units * g.K
-              : g.regime == gn::kRegimePipelined ? g.grid
-                                                 : g.items;
+  out->ctas = g.regime == gn::kRegimeResident                                     ? g.units * g.K
+              : (g.regime == gn::kRegimePipelined || g.regime == gn::kRegimeWave) ? g.grid
+                                                                                  : g.items;
   out->partials = g.N * g.C * (g.T + (g.l1 > 1 ? g.Tp : 0));
   out->workspace_bytes = gn::ws_layout(op, g).total;
   out->err_offset = gn::ws_layout(op, g).err;
@@ -321,7 +326,10 @@ int gn_plan_info(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout
   const int64_t mc = gn::plan_max_clusters(g, op);
   out->max_clusters = mc > 0 ? (int)mc : 0;
   // item / piece shape (the boundaries the parity tests sample)
-  if (g.regime == gn::kRegimeResident) {
+  if (g.regime == gn::kRegimeWave) {
+    out->piece_elems = g.wR;
+    out->pieces_per_unit = g.wP;
+  } else if (g.regime == gn::kRegimeResident) {
     out->piece_elems = g.slice;
     out->pieces_per_unit = g.K;
   } else if (g.layout == GN_LAYOUT_NHWC) {
@@ -336,7 +344,7 @@ int gn_plan_info(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout
   }
   if (g.regime == gn::kRegimeResident) {
     out->smem_bytes = g.smem;
-  } else if (g.regime == gn::kRegimePipelined) {
+  } else if (g.regime == gn::kRegimePipelined || g.regime == gn::kRegimeWave) {
     out->smem_bytes = g.smem;
   } else {
     size_t sm = 0;

@@ -26,6 +26,8 @@ enum Regime {
   kRegimeResident = 1,  // one kernel: a cluster holds a unit in shared memory
   kRegimePipelined = 2, // one persistent kernel: pass-1 and pass-2 tasks of
                         // units in flight, the second pass reading from L2
+  kRegimeWave = 3,      // one persistent kernel: every piece of a unit stays in
+                        // shared memory until the unit's statistics are known
 };
 
 // How one call is cut into "items" for the two-kernel path.  Both kernels
@@ -97,6 +99,12 @@ struct Geom {
   int nres, S;         // resident chunk slots, ring slots
   size_t smem;         // dynamic shared memory bytes
   size_t off_ring, off_red, off_xch, off_tot, off_grp, off_bar;
+  // wave regime (gn_wave.cu): units (`units`) of wP pieces; a piece is wR
+  // elements of one channel plane (NCHW; wm pieces per plane) or wR rows of
+  // Cb channels (NHWC, read as wnb TMA boxes of `chunk` rows); `grid` CTAs
+  // hold S slots of ten_stride bytes per tensor; wcols parameter columns
+  // (channel blocks of a sample) finish dgamma/dbeta
+  int64_t wP, wR, wm, wnb, wcols;
 };
 
 // Bytes reserved per ring-slot header of the pipelined kernel (the header
@@ -209,7 +217,14 @@ int64_t nchw_pipelined_scratch_floats(const Geom& g);
 // dynamic shared memory for a plan.
 const void* nhwc_kernel(const Geom& g, bool bwd, int second, size_t* smem);
 const void* nchw_kernel(const Geom& g, bool bwd, int second, size_t* smem);
+// gn_wave.cu
+const void* wave_kernel_ptr(const Geom& g, bool bwd);
+cudaError_t launch_wave(const KParams& p, cudaStream_t s, bool bwd);
+// Threads of a wave-regime CTA.
+constexpr int kWaveThreads = 256;
 // gn_resident.cu
+// [N*HW, C] view of an NHWC tensor for TMA, boxes of [g.chunk rows, g.Cb channels].
+cudaError_t encode_nhwc_map(CUtensorMap* map, const void* base, const Geom& g);
 const void* resident_kernel_ptr(const Geom& g, bool bwd);
 cudaError_t launch_resident(const KParams& p, cudaStream_t s, bool bwd);
 // Threads of a resident CTA: the consumer warps plus one producer warp.

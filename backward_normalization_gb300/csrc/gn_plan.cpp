@@ -111,6 +111,13 @@ bool resident_preferred(const Geom& g, int op) {
   return g.Cg * g.HW * esz <= (1 << 20);
 }
 
+// The automatic choice of the wave regime (where its plan fits): measured on
+// GB300 it reads each input once and keeps every SM streaming.
+bool wave_preferred(const Geom& g) {
+  (void)g;
+  return true;
+}
+
 // Input that counts as tiny for the automatic choice (see plan_resident).
 constexpr double kResidentTinyBytes = 1 << 20;
 
@@ -338,6 +345,191 @@ bool plan_pipelined(Geom& g, int op, int sm_count) {
 }
 }  // namespace
 
+namespace {
+// Wave regime (gn_wave.cu): a unit's pieces are held by several CTAs at
+// once, S slots each; S >= 2 (one piece in use, one landing).
+#ifndef GN_WAVE_MIN_SLOTS
+#define GN_WAVE_MIN_SLOTS 3
+#endif
+#ifndef GN_WAVE_MAX_SLOTS
+#define GN_WAVE_MAX_SLOTS 8
+#endif
+#ifndef GN_WAVE_CTAS_PER_SM
+#define GN_WAVE_CTAS_PER_SM 1
+#endif
+#ifndef GN_WAVE_MAX_CB
+#define GN_WAVE_MAX_CB 128
+#endif
+constexpr int kWaveMinSlots = GN_WAVE_MIN_SLOTS;
+constexpr int kWaveMaxSlots = GN_WAVE_MAX_SLOTS;
+constexpr int kWaveCtasPerSm = GN_WAVE_CTAS_PER_SM;
+constexpr int64_t kWaveMaxCb = GN_WAVE_MAX_CB;  // channels per NHWC unit (TMA box <= 256)
+
+// CTAs of the wave kernel that fit on the device at once with `smem` bytes of
+// dynamic shared memory (an estimate when no device is visible).
+int64_t wave_ctas(const Geom& g, int op, size_t smem, int sm_count, int want_per_sm) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return (int64_t)sm_count * want_per_sm;
+  }
+  const void* fn = wave_kernel_ptr(g, op == kBwd);
+  int nb = 0;
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+          cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fn, kWaveThreads, smem) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return (int64_t)std::min(nb, want_per_sm) * sm_count;
+}
+
+// One candidate cut of a wave plan: pieces per unit P, values per piece R
+// (elements of a plane, or rows), slots S, CTAs NC; `cost` estimates its
+// time in microseconds.
+struct WaveCut {
+  int64_t P = 0, R = 0, m = 1, nb = 1, box = 0, Cb = 0, S = 0, steps = 0;
+  double cost = 0.0;
+  size_t slot = 0, out = 0;
+};
+
+// Cost model of a wave cut, from measurements on GB300: an SM moves about
+// 45 GB/s (in + out); every step adds about 0.4 us of work that copies do not
+// hide, a unit split over CTAs about 0.3 us more for its arrivals, and with
+// only two slots the wait for a unit is exposed (about 1 us).  A unit whose
+// pieces straddle two steps (P not dividing the CTA count) stalls its CTAs
+// for about one piece time.
+#ifndef GN_WAVE_FORCE_CB
+#define GN_WAVE_FORCE_CB 0
+#endif
+double wave_cost(const WaveCut& c, int64_t NC) {
+  const double t_io = (double)(c.slot + c.out) / 45.0e3;  // us at 45 GB/s
+  double per_step = t_io + 0.4 + (c.P > 1 ? 0.3 : 0.0) + (c.S < 3 ? 1.0 : 0.0);
+  if (c.P > 1 && NC % c.P != 0) per_step += t_io;
+  return (double)c.steps * per_step + t_io;
+}
+
+// Shared memory of a wave plan besides its slots: the records and CTA sums,
+// the per-channel and per-group values, the mbarriers.
+size_t wave_fixed_bytes(const Geom& g, int64_t P, int64_t Cb, int vec) {
+  const int64_t nch = g.layout == kNHWC ? Cb : 1;
+  int64_t red = 2 * P * nch + (g.layout == kNHWC ? 2 * vec * kWaveThreads + Cb : 64);
+  red = std::max<int64_t>(red, 2 * kWaveThreads);
+  const int64_t chs = g.layout == kNHWC ? Cb : g.Cg;
+  const int64_t grp = g.layout == kNHWC ? Cb / g.Cg : 1;
+  return a128((size_t)red * 4) + a128((size_t)chs * 8) + a128((size_t)grp * 8) + a128(8 * kWaveMaxSlots);
+}
+
+// Fills the wave-regime fields of g; false when the problem does not fit.
+bool plan_wave(Geom& g, int op, int sm_count) {
+  const int esz = dtype_size(g.dtype);
+  const int vec = 16 / esz;
+  const int nten = op == kBwd ? 2 : 1;
+  if (g.vw != vec || g.dtype == kF64) return false;
+  const size_t budget = kWaveCtasPerSm == 1 ? kSmemPerCta : kSmemPerSm / kWaveCtasPerSm - 2048;
+  const int64_t NC = (int64_t)sm_count * kWaveCtasPerSm;
+  WaveCut best;
+  auto consider = [&](WaveCut c, int64_t units) {
+    if (c.P < 1 || c.P > NC) return;
+    if (GN_WAVE_FORCE_CB > 0 && g.layout == kNHWC && c.Cb != GN_WAVE_FORCE_CB) return;
+    const size_t fixed = wave_fixed_bytes(g, c.P, c.Cb, vec);
+    if (fixed + 128 + 2 * c.slot > budget) return;
+    c.S = std::min<int64_t>(kWaveMaxSlots, (int64_t)((budget - fixed - 128) / c.slot));
+    if (c.S < 2) return;
+    c.steps = cdiv(units * c.P, NC);
+    c.cost = wave_cost(c, NC);
+    // the cheapest cut; at equal cost the one with more slots, then wider rows
+    auto key = [&](const WaveCut& w) { return std::make_tuple(-w.cost, w.S >= kWaveMinSlots, w.Cb); };
+    if (best.P == 0 || key(c) > key(best)) best = c;
+  };
+  if (g.layout == kNCHW) {
+    if ((g.HW * esz) % 16 != 0) return false;
+    for (int64_t m = 1; m * g.Cg <= NC; ++m) {
+      WaveCut c;
+      c.R = rup(cdiv(g.HW, m), vec);
+      c.m = cdiv(g.HW, c.R);
+      if (c.m != m) continue;
+      c.P = g.Cg * m;
+      c.slot = a128((size_t)(c.R * esz)) * nten;
+      c.out = (size_t)(c.R * esz);
+      consider(c, g.N * g.G);
+    }
+  } else {
+    if (g.N * g.HW > 0x7fffffffLL) return false;  // TMA row coordinates are 32-bit
+    const int64_t step = g.Cg / gcd64(g.Cg, vec) * vec;
+    for (int64_t cb = step; cb <= g.C && cb <= kWaveMaxCb; cb += step) {
+      if (g.C % cb != 0) continue;
+      const int64_t rowb = cb * esz;
+      for (int64_t P = 1; P <= NC && P <= g.HW; ++P) {
+        WaveCut c;
+        c.Cb = cb;
+        int64_t R = cdiv(g.HW, P);
+        if (R > 256) R = rup(R, 256);
+        if (cdiv(g.HW, R) != P) continue;  // another P gives this cut
+        c.P = P;
+        c.R = R;
+        c.box = R > 256 ? 256 : R;
+        c.nb = R / c.box;
+        c.slot = a128((size_t)(R * rowb)) * nten;
+        c.out = (size_t)(R * rowb);
+        consider(c, g.N * (g.C / cb));
+      }
+    }
+  }
+  if (best.P == 0) return false;
+  Geom r = g;
+  r.regime = kRegimeWave;
+  r.tpb = kWaveThreads;
+  r.wP = best.P;
+  r.wR = best.R;
+  r.wm = best.m;
+  r.S = (int)best.S;
+  if (g.layout == kNHWC) {
+    r.Cb = best.Cb;
+    r.ncbu = g.C / best.Cb;
+    r.units = g.N * r.ncbu;
+    r.chunk = best.box;
+    r.wnb = best.nb;
+    r.wcols = r.ncbu;
+    r.Tp = best.P;  // records per (n, c): one per piece
+  } else {
+    r.Cb = 0;
+    r.units = g.N * g.G;
+    r.chunk = 0;
+    r.wnb = 1;
+    r.wcols = g.G;
+    r.Tp = best.m;  // records per (n, c): one per segment of the plane
+  }
+  r.ten_stride = (int64_t)(best.slot / nten);
+  r.T = 0;
+  r.l1 = 1;
+  r.units_fin = r.units;  // a counter per unit, then one per parameter column
+  r.groups1 = r.wcols;
+  r.unit_groups = 0;
+  size_t off = 0;
+  r.off_ring = off;
+  off += (size_t)r.S * best.slot;
+  const int64_t nch = g.layout == kNHWC ? r.Cb : 1;
+  int64_t red = 2 * r.wP * nch + (g.layout == kNHWC ? 2 * vec * kWaveThreads + r.Cb : 64);
+  red = std::max<int64_t>(red, 2 * kWaveThreads);
+  r.off_red = off;
+  off += a128((size_t)red * 4);
+  r.off_tot = off;
+  off += a128((size_t)(g.layout == kNHWC ? r.Cb : g.Cg) * 8);
+  r.off_grp = off;
+  off += a128((size_t)(g.layout == kNHWC ? r.Cb / g.Cg : 1) * 8);
+  r.off_bar = off;
+  off += a128(8 * (size_t)r.S);
+  r.smem = off + 128;  // slack for aligning the dynamic shared memory base
+  if (r.smem > budget) return false;
+  const int64_t nc = wave_ctas(r, op, r.smem, sm_count, kWaveCtasPerSm);
+  if (nc < r.wP) return false;  // a unit's pieces must be co-resident
+  r.grid = std::min<int64_t>(nc, r.units * r.wP);
+  g = r;
+  return true;
+}
+}  // namespace
+
 int64_t plan_max_clusters(const Geom& g, int op) {
   if (g.regime == kRegimeResident) return resident_clusters(g, op);
   const int64_t r = resident_ctas(g, op, 0);
@@ -540,6 +732,10 @@ Geom plan_geom(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout, 
     plan_resident(g, op, false);  // wherever the problem fits the regime
   } else if (ov == kRegimePipelined) {
     plan_pipelined(g, op, sm_count);
+  } else if (ov == kRegimeWave) {
+    plan_wave(g, op, sm_count);
+  } else if (ov == kRegimeAuto && wave_preferred(g) && plan_wave(g, op, sm_count)) {
+    // taken
   } else if (ov == kRegimeAuto && resident_preferred(g, op)) {
     // measured on GB300: the pipelined kernel moves the minimal traffic but is
     // slower than these families on every workload here (its steps are

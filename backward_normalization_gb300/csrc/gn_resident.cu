@@ -554,6 +554,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+}  // namespace
+
 // [N*HW, C] view of an NHWC tensor, boxes of [chunk rows, Cb channels].
 cudaError_t encode_nhwc_map(CUtensorMap* map, const void* base, const Geom& g) {
   auto fn = encode_fn();
@@ -571,8 +573,6 @@ cudaError_t encode_nhwc_map(CUtensorMap* map, const void* base, const Geom& g) {
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
-
-}  // namespace
 
 const void* resident_kernel_ptr(const Geom& g, bool bwd) {
   switch (g.dtype) {

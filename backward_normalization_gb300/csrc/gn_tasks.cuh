@@ -330,7 +330,6 @@ inline cudaError_t launch_cooperative(const void* kernel, const KParams& p, size
     if (e != cudaSuccess) return e;
   }
   const TimingEvents& ev = timing_events();
-  if (ev.begin) cudaEventRecord(ev.begin, s);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)p.g.grid, 1, 1);
   cfg.blockDim = dim3((unsigned)p.g.tpb, 1, 1);

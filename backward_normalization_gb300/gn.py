@@ -169,7 +169,7 @@ def bwd_raw(dy, x, mean, rstd, gamma, N, C, HW, G, layout, dx, dgamma, dbeta, wo
                         _ptr(workspace), ws_bytes, _stream(stream))
 
 
-REGIME_AUTO, REGIME_TWO_KERNEL, REGIME_RESIDENT, REGIME_PIPELINED = -1, 0, 1, 2
+REGIME_AUTO, REGIME_TWO_KERNEL, REGIME_RESIDENT, REGIME_PIPELINED, REGIME_WAVE = -1, 0, 1, 2, 3
 
 
 def set_regime(regime: int) -> None:

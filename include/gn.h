@@ -208,24 +208,33 @@ GN_API int gn_set_timing_events(void* ev_begin, void* ev_mid, void* ev_end);
  * aligned data): every CTA takes one piece of every (n, group) unit, unit
  * after unit, the second pass of a unit trailing its first by a few units so
  * that it finds the input still in L2; data arrives through bulk copies into
- * shared memory.  Every regime gives results within the same
- * tolerances of the definition, each bit-identical from run to run. */
+ * shared memory.  GN_REGIME_WAVE runs one persistent kernel (a cooperative
+ * launch; 16-byte aligned fp32 / fp16 / bf16 data) that cuts every reduction
+ * unit -- one (n, group) span for NCHW, one (sample, block of whole groups)
+ * for NHWC -- into pieces held in the shared memory of several CTAs at once:
+ * each CTA reduces its piece, publishes per-channel partial sums, waits
+ * (bounded) for the unit's other pieces and writes its output from shared
+ * memory, so the input is read from HBM once; it is taken where every unit
+ * fits in the shared memory of the co-resident CTAs.  Every regime gives
+ * results within the same tolerances of the definition, each bit-identical
+ * from run to run. */
 #define GN_REGIME_AUTO (-1)
 #define GN_REGIME_TWO_KERNEL 0
 #define GN_REGIME_RESIDENT 1
 #define GN_REGIME_PIPELINED 2
+#define GN_REGIME_WAVE 3
 
 /* Test hook, process-wide: GN_REGIME_AUTO (default) lets each call choose
  * the faster family for its shape; GN_REGIME_TWO_KERNEL forces the two-kernel
- * path; GN_REGIME_RESIDENT and GN_REGIME_PIPELINED force that regime wherever
+ * path; GN_REGIME_RESIDENT, GN_REGIME_PIPELINED and GN_REGIME_WAVE force that regime wherever
  * the problem fits it (else the two-kernel path runs).  Not thread-safe with respect to
  * calls in flight on other threads.  Returns a gn_status. */
 GN_API int gn_set_regime(int regime);
 
 /* What a call would run, for tests and reports (host-only, no launch). */
 typedef struct gn_plan_desc {
-  int regime;            /* GN_REGIME_TWO_KERNEL, GN_REGIME_RESIDENT or GN_REGIME_PIPELINED */
-  int launches;          /* kernels one call enqueues */
+  int regime;            /* GN_REGIME_TWO_KERNEL, _RESIDENT, _PIPELINED or _WAVE */
+  int launches;          /* kernels one call enqueues, the workspace clear included */
   int vector_width;      /* elements per access: 16-byte vectors, or 1 (scalar path) */
   int threads;           /* threads per CTA */
   int64_t ctas;          /* CTAs per kernel */

@@ -117,7 +117,7 @@ def test_validation_before_any_launch(gn):
 
 def test_plan_vector_width_and_modes(gn):
     d = gn.plan_info(0, 1, 128, 2048 * 1024, 16, "nhwc", "f16")
-    assert d.vector_width == 8 and d.launches == 2
+    assert d.vector_width == 8 and d.launches == 3  # workspace clear + two kernels
     assert gn.plan_info(0, 2, 6, 77, 3, "nhwc", "f16").vector_width == 1       # C*2 % 16 != 0
     assert gn.plan_info(0, 2, 64, 2303, 8, "nchw", "f32").vector_width == 1    # HW*4 % 16 != 0
     assert gn.plan_info(0, 2, 64, 2304, 8, "nchw", "f32").vector_width == 4
@@ -142,15 +142,18 @@ def test_regime_choice(gn):
     gn.set_regime(gn.REGIME_TWO_KERNEL)
     try:
         d = gn.plan_info(1, 8, 320, 4096, 32, "nhwc", "bf16")
-        assert d.regime == 0 and d.launches == 2
+        assert d.regime == 0 and d.launches == 3
     finally:
         gn.set_regime(gn.REGIME_AUTO)
     gn.set_regime(gn.REGIME_RESIDENT)
     try:
         d = gn.plan_info(1, 8, 320, 4096, 32, "nhwc", "bf16")
-        assert d.regime == 1 and d.launches == 1
+        assert d.regime == 1 and d.launches == 2
     finally:
         gn.set_regime(gn.REGIME_AUTO)
+    # the wave kernel clears its own counters: one launch per op
+    d = gn.plan_info(1, 8, 320, 4096, 32, "nhwc", "bf16")
+    assert d.regime == 3 and d.launches == 1
     with pytest.raises(gn.GnError):
         gn.set_regime(7)
 
@@ -180,8 +183,12 @@ def test_finalisation_placement(gn):
     finally:
         gn.set_regime(gn.REGIME_AUTO)
     # the resident regime finalises in its one kernel
-    d = gn.plan_info(0, 8, 320, 4096, 32, "nhwc", "bf16")
-    assert d.regime == 1 and d.finalise_second == 0
+    gn.set_regime(gn.REGIME_RESIDENT)
+    try:
+        d = gn.plan_info(0, 8, 320, 4096, 32, "nhwc", "bf16")
+        assert d.regime == 1 and d.finalise_second == 0
+    finally:
+        gn.set_regime(gn.REGIME_AUTO)
 
 
 def test_f64_storage_plans(gn):
@@ -189,11 +196,11 @@ def test_f64_storage_plans(gn):
     the scalar path, always on the two-kernel path (whatever regime is
     asked for); the row family does not take it."""
     d = gn.plan_info(0, 2, 16, 4096, 4, "nchw", "f64")
-    assert (d.regime, d.vector_width, d.launches) == (0, 2, 2)
+    assert (d.regime, d.vector_width, d.launches) == (0, 2, 3)
     assert gn.plan_info(1, 3, 40, 99, 8, "nhwc", "f64").vector_width == 2
     assert gn.plan_info(1, 2, 3, 25, 3, "nhwc", "f64").vector_width == 1   # 3 doubles: not 16 B
     assert gn.plan_info(0, 2, 6, 63, 3, "nchw", "f64").vector_width == 1   # 63 doubles per plane
-    for reg in (gn.REGIME_RESIDENT, gn.REGIME_PIPELINED):
+    for reg in (gn.REGIME_RESIDENT, gn.REGIME_PIPELINED, gn.REGIME_WAVE):
         gn.set_regime(reg)
         try:
             assert gn.plan_info(1, 2, 16, 4096, 4, "nchw", "f64").regime == 0
@@ -205,17 +212,42 @@ def test_f64_storage_plans(gn):
     assert gn.lib().ln_workspace_size(16, 64, 3) == 0
 
 
-def test_automatic_resident_choice_needs_one_wave(gn):
-    """The automatic choice takes the resident regime only when one wave of
-    clusters covers every unit, or the input is tiny (at most 1 MB): later
-    waves of clusters cost more than the two-kernel path saves."""
-    assert gn.plan_info(0, 2, 32, 256, 8, "nchw", "f32").regime == 1       # 64 KB
-    assert gn.plan_info(0, 512, 32, 256, 8, "nchw", "f32").regime == 0     # 4096 units
-    assert gn.plan_info(0, 8, 320, 4096, 32, "nhwc", "bf16").regime == 1   # 32 clusters
-    assert gn.plan_info(0, 64, 320, 4096, 32, "nhwc", "bf16").regime == 0  # 256 clusters
+def test_automatic_choice(gn):
+    """The automatic choice takes the wave regime wherever its plan fits (16-byte
+    aligned fp32/fp16/bf16 data whose units fit in the co-resident CTAs'
+    shared memory), else the two-kernel path; the resident regime runs when
+    asked for."""
+    assert gn.plan_info(0, 2, 32, 256, 8, "nchw", "f32").regime == 3
+    assert gn.plan_info(1, 112, 64, 512 * 512, 8, "nchw", "f32").regime == 3   # 16 MiB units
+    assert gn.plan_info(0, 8, 320, 4096, 32, "nhwc", "bf16").regime == 3
+    assert gn.plan_info(1, 32, 512, 1024, 32, "nhwc", "bf16").regime == 3
+    # 32 MiB units (one group of the one-sample image) do not fit: two kernels
+    assert gn.plan_info(0, 1, 128, 2048 * 1024, 16, "nhwc", "f16").regime == 0
+    assert gn.plan_info(0, 2, 64, 2303, 8, "nchw", "f32").regime == 0       # scalar path
+    assert gn.plan_info(0, 2, 16, 4096, 4, "nchw", "f64").regime == 0       # f64 storage
     gn.set_regime(gn.REGIME_RESIDENT)  # asked for: wherever the problem fits
     try:
         assert gn.plan_info(0, 512, 32, 256, 8, "nchw", "f32").regime == 1
+    finally:
+        gn.set_regime(gn.REGIME_AUTO)
+
+
+def test_wave_plans(gn):
+    """Wave plans: a unit's pieces all fit on co-resident CTAs (P <= CTAs),
+    the pieces of the benchmarked units divide the CTA count (no unit
+    straddles two steps), and pieces hold whole 16-byte vectors."""
+    for w in synth.WORKLOADS[2:]:
+        for op in (0, 1):
+            d = gn.plan_info(op, w.N, w.C, w.HW, w.G, w.layout, w.dtype)
+            assert d.regime == 3 and d.launches == 1
+            assert 1 <= d.pieces_per_unit <= d.ctas
+            assert d.ctas % d.pieces_per_unit == 0
+            assert d.smem_bytes <= 227 * 1024
+            if w.layout == "nchw":
+                assert d.piece_elems * (4 if w.dtype == "f32" else 2) % 16 == 0
+    gn.set_regime(gn.REGIME_WAVE)
+    try:
+        assert gn.plan_info(0, 1, 128, 2048 * 1024, 16, "nhwc", "f16").regime == 0  # too large
     finally:
         gn.set_regime(gn.REGIME_AUTO)
 

@@ -1,7 +1,7 @@
 """GPU: the library's calls capture into a CUDA graph (the launch-bound small
 problems replay without per-call launch cost) and replay bit-identically to
 the eager calls, for every kernel family (two-kernel with programmatic
-dependent launch, resident clusters, rows)."""
+dependent launch, resident clusters, the cooperative wave kernel, rows)."""
 from __future__ import annotations
 
 import pytest
@@ -12,14 +12,31 @@ from backward_normalization_gb300 import gn, synth
 pytestmark = pytest.mark.gpu
 
 CASES = [
-    ("bf16_nhwc_8x320x16x16_g32_resident_fwd", synth.WORKLOADS[2].scaled(name="g2", H=16, W=16)),
-    ("bf16_nhwc_8x512x8x8_g32_two_kernel", synth.WORKLOADS[4].scaled(name="g4", N=8, H=8, W=8)),
-    ("fp32_nchw_4x64x48x48_g8_records", synth.WORKLOADS[3].scaled(name="g3", N=4, H=48, W=48)),
+    ("bf16_nhwc_8x320x16x16_g32_resident", synth.WORKLOADS[2].scaled(name="g2", H=16, W=16),
+     gn.REGIME_RESIDENT),
+    ("bf16_nhwc_8x512x8x8_g32_two_kernel", synth.WORKLOADS[4].scaled(name="g4", N=8, H=8, W=8),
+     gn.REGIME_TWO_KERNEL),
+    ("fp32_nchw_4x64x48x48_g8_records", synth.WORKLOADS[3].scaled(name="g3", N=4, H=48, W=48),
+     gn.REGIME_TWO_KERNEL),
+    # one cooperative launch per op, units split over CTAs
+    ("bf16_nhwc_8x320x16x16_g32_wave", synth.WORKLOADS[2].scaled(name="g2w", H=16, W=16),
+     gn.REGIME_WAVE),
+    ("fp32_nchw_4x64x48x48_g8_wave", synth.WORKLOADS[3].scaled(name="g3w", N=4, H=48, W=48),
+     gn.REGIME_WAVE),
 ]
 
 
-@pytest.mark.parametrize("name,w", CASES, ids=[c[0] for c in CASES])
-def test_groupnorm_graph_replay(name, w):
+@pytest.fixture
+def forced():
+    yield gn.set_regime
+    gn.set_regime(gn.REGIME_AUTO)
+
+
+@pytest.mark.parametrize("name,w,regime", CASES, ids=[c[0] for c in CASES])
+def test_groupnorm_graph_replay(name, w, regime, forced):
+    forced(regime)
+    for op in (gn.OP_FWD, gn.OP_BWD):
+        assert gn.plan_info(op, w.N, w.C, w.HW, w.G, w.layout, w.dtype).regime == regime
     inp = synth.make_inputs(w, "cuda", seed=7)
     x, dy, gm, bt = inp["x"], inp["dy"], inp["gamma"], inp["beta"]
     ws = gn.alloc_workspace(gn.OP_BWD, w.N, w.C, w.HW, w.G, w.layout, x.dtype)

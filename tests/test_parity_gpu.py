@@ -73,7 +73,7 @@ STREAMING = [
 
 
 REGIMES = {"auto": gn.REGIME_AUTO, "two_kernel": gn.REGIME_TWO_KERNEL, "resident": gn.REGIME_RESIDENT,
-           "pipelined": gn.REGIME_PIPELINED}
+           "pipelined": gn.REGIME_PIPELINED, "wave": gn.REGIME_WAVE}
 
 
 @pytest.fixture(params=list(REGIMES))
@@ -474,7 +474,7 @@ def _oracle_by_samples(w, inp, idx=None):
 
 
 FULL = ([(w, "auto") for w in synth.WORKLOADS[1:]]
-        + [(synth.WORKLOADS[3], "resident"), (synth.WORKLOADS[2], "resident"),
+        + [(synth.WORKLOADS[3], "two_kernel"), (synth.WORKLOADS[2], "resident"),
            (synth.WORKLOADS[4], "two_kernel"), (synth.WORKLOADS[2], "two_kernel")])
 
 
