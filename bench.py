@@ -44,7 +44,7 @@ def min_bytes(w):
     return {"fwd": 2 * e, "bwd": 3 * e}
 
 
-REGIME_NAMES = {0: "two-kernel", 1: "resident", 2: "pipelined"}
+REGIME_NAMES = {0: "two-kernel", 1: "resident", 2: "pipelined", 3: "wave"}
 
 
 def kernel_bytes(w, fwd_regime=0, bwd_regime=0):
@@ -155,36 +155,106 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------- oracle leg
-def oracle_sample(H):
-    """Times the fp64 CPU oracle (fwd + bwd) on a bounded slice of the
-    workload: the first H rows of the image (all channels and groups).
-    Returns (GB/s over the slice's minimal traffic, seconds, description)."""
-    import oracle
-    from backward_normalization_gb300 import synth
-
-    o = oracle.get()
-    w = synth.BY_NAME[WORKLOAD]
-    ws = w.scaled(H=H)
-    inp = synth.make_inputs(ws, "cpu", seed=0)
-    x = inp["x"].double().numpy()
-    dy = inp["dy"].double().numpy()
-    g = inp["gamma"].double().numpy()
-    b = inp["beta"].double().numpy()
-    t0 = time.perf_counter()
-    o.forward(x, ws.N, ws.C, ws.HW, ws.G, 1, g, b, ws.eps)
-    o.backward(dy, x, ws.N, ws.C, ws.HW, ws.G, 1, g, ws.eps)
-    dt = time.perf_counter() - t0
-    mb = min_bytes(ws)
-    gbs = (mb["fwd"] + mb["bwd"]) / dt / 1e9
-    desc = (f"fp64 oracle fwd+bwd on rows 0..{H - 1} of the image (N=1, C=128, G=16, "
-            f"H={H}, W=2048: {ws.E} elements, {H / w.H:.4f} of the workload), 1 thread")
-    return gbs, dt, desc
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
 
 
-def rows_for_seconds(target_s):
-    """Image rows whose oracle fwd+bwd takes about target_s seconds here."""
-    _, dt, _ = oracle_sample(2)
-    return int(max(1, min(1024, round(2 * target_s / max(dt, 1e-6)))))
+class OracleSample:
+    """A bounded sample of a workload for timing the fp64 CPU oracle: the first
+    `ns` samples of the batch (or, for a one-sample workload, its first `h`
+    image rows), cut into its (sample, group) units.  Each unit is handed to
+    the oracle as a one-group problem of its own -- the oracle's arithmetic
+    for a group depends on that group's values only, so this is the same
+    computation it does on the whole tensor, and units can run on separate
+    host threads (ctypes releases the GIL during each oracle call).  The
+    channels_last units are gathered into contiguous [HW, Cg] arrays before
+    the clock starts (a layout copy, not part of the method)."""
+
+    def __init__(self, w, ns=None, h=None, seed=0):
+        from backward_normalization_gb300 import synth
+
+        self.w = w.scaled(N=ns) if ns else w.scaled(H=h)
+        ws = self.w
+        inp = synth.make_inputs(ws, "cpu", seed=seed)
+        x = inp["x"].double().numpy()
+        dy = inp["dy"].double().numpy()
+        gm = inp["gamma"].double().numpy()
+        bt = inp["beta"].double().numpy()
+        Cg = ws.C // ws.G
+        self.units = []
+        for n in range(ws.N):
+            for g in range(ws.G):
+                c0 = g * Cg
+                if ws.layout == "nchw":
+                    lo = (n * ws.C + c0) * ws.HW
+                    xu, du = x[lo:lo + Cg * ws.HW], dy[lo:lo + Cg * ws.HW]
+                else:
+                    xs = x.reshape(ws.N, ws.HW, ws.C)[n, :, c0:c0 + Cg]
+                    ds = dy.reshape(ws.N, ws.HW, ws.C)[n, :, c0:c0 + Cg]
+                    xu, du = xs.copy().reshape(-1), ds.copy().reshape(-1)
+                self.units.append((xu, du, gm[c0:c0 + Cg].copy(), bt[c0:c0 + Cg].copy(), Cg))
+        self.layout = synth.LAYOUTS[ws.layout]
+        mb = min_bytes(ws)
+        self.bytes = mb["fwd"] + mb["bwd"]
+        part = f"samples 0..{ws.N - 1}" if ns else f"image rows 0..{ws.H - 1}"
+        self.desc = (f"fp64 oracle fwd+bwd on {part} of {w.name} ({ws.E} elements, "
+                     f"{ws.E / w.E:.4f} of the workload), {len(self.units)} (sample, group) units")
+
+    def run(self, threads: int) -> float:
+        """Seconds for fwd + bwd of every unit on `threads` host threads."""
+        import concurrent.futures as cf
+
+        import oracle
+
+        o = oracle.get()
+        ws, L = self.w, self.layout
+
+        def one(u):
+            xu, du, g, b, Cg = u
+            o.forward(xu, 1, Cg, ws.HW, 1, L, g, b, ws.eps)
+            o.backward(du, xu, 1, Cg, ws.HW, 1, L, g, ws.eps)
+
+        t0 = time.perf_counter()
+        if threads <= 1:
+            for u in self.units:
+                one(u)
+        else:
+            with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+                list(ex.map(one, self.units))
+        return time.perf_counter() - t0
+
+
+def oracle_sample_for(w, target_s: float, threads: int = 1):
+    """An OracleSample of w whose run on `threads` threads takes about
+    target_s seconds here (sized from a small calibration run)."""
+    if w.N > 1:
+        probe = OracleSample(w, ns=1)
+        per = probe.run(1) / max(1, min(threads, len(probe.units)))
+        ns = int(max(1, min(w.N, round(target_s / max(per, 1e-6)))))
+        return OracleSample(w, ns=ns)
+    probe = OracleSample(w, h=2)
+    per = probe.run(1) / 2 / max(1, min(threads, len(probe.units)))
+    h = int(max(1, min(w.H, round(target_s / max(per, 1e-6)))))
+    return OracleSample(w, h=h)
+
+
+def cpu_baselines(workloads, target_s=2.0):
+    """Per workload: the oracle on one thread and on all host cores, over the
+    same bounded sample (GB/s over the sample's minimal traffic)."""
+    nt = host_cores()
+    out = {}
+    for w in workloads:
+        smp = oracle_sample_for(w, target_s, 1)
+        t1 = smp.run(1)
+        tn = smp.run(nt)
+        out[w.name] = {"single_thread_gbs": round(smp.bytes / t1 / 1e9, 4),
+                       "all_cores_gbs": round(smp.bytes / tn / 1e9, 4), "cores": nt,
+                       "seconds_single": round(t1, 3), "seconds_all_cores": round(tn, 3),
+                       "sample": smp.desc}
+    return out
 
 
 def run_reference(args, rank, world):
@@ -193,25 +263,22 @@ def run_reference(args, rank, world):
     from backward_normalization_gb300 import synth
 
     w = synth.BY_NAME[WORKLOAD]
-    # the whole run stays within about two minutes of CPU time
-    H = rows_for_seconds(min(2.0, 120.0 / (args.steps + args.warmup)))
+    nt = host_cores()
+    # the whole run stays within about two minutes: each step a bounded
+    # sample of the workload, on all host cores
+    smp = oracle_sample_for(w, min(2.0, 120.0 / (args.steps + args.warmup)), nt)
     for _ in range(args.warmup):
-        oracle_sample(H)
-    times = []
-    desc = ""
-    for _ in range(args.steps):
-        _, dt, desc = oracle_sample(H)
-        times.append(dt)
-    mb = min_bytes(w.scaled(H=H))
+        smp.run(nt)
+    times = [smp.run(nt) for _ in range(args.steps)]
     ms = 1e3 * sum(times) / len(times)
-    value = (mb["fwd"] + mb["bwd"]) / (ms * 1e-3) / 1e9
+    value = smp.bytes / (ms * 1e-3) / 1e9
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": config_of(w, {"sample": desc}),
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": desc},
+            "config": config_of(w, {"sample": smp.desc}),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": nt, "kind": "oracle",
+                             "sample": smp.desc},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -576,9 +643,15 @@ def run_ours(args, rank, world, local_rank):
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        gbs, dt, desc = oracle_sample(rows_for_seconds(10.0))
-        cpu = {"value": round(gbs, 4), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc,
-               "seconds": round(dt, 2)}
+        todo = synth.WORKLOADS[1:] if per_config is not None else [w]
+        base = cpu_baselines(todo)
+        b = base[w.name]
+        cpu = {"value": b["all_cores_gbs"], "unit": UNIT, "cores": b["cores"], "kind": "oracle",
+               "sample": b["sample"], "single_thread_value": b["single_thread_gbs"],
+               "seconds": b["seconds_all_cores"]}
+        for name, v in base.items():
+            if per_config and name in per_config:
+                per_config[name]["cpu_oracle"] = v
 
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K,
