@@ -386,6 +386,17 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
 __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_all;" ::: "memory");
 }
+// 4-byte asynchronous copy from global to shared memory (both 4-byte
+// aligned), in the issuing thread's current cp.async group.
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)),
+               "l"(__cvta_generic_to_global(src))
+               : "memory");
+}
+// Closes this thread's current cp.async group (an empty one if it holds no copy).
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
 
 // ------------------------------------------------------ cluster reduction
 // Adds, for every q < NQ, red[q*stride + slot] of all CTAs of the cluster into

@@ -150,7 +150,7 @@ struct WsLayout {
 };
 
 struct KParams {
-  CUtensorMap tmx;   // resident NHWC: 2-D [N*HW, C] views of x and dy for TMA tiles
+  CUtensorMap tmx;   // resident / wave NHWC: 2-D [N*HW, C] views of x and dy for TMA tiles
   CUtensorMap tmdy;
   Geom g;
   const void* x;
@@ -220,8 +220,26 @@ const void* nchw_kernel(const Geom& g, bool bwd, int second, size_t* smem);
 // gn_wave.cu
 const void* wave_kernel_ptr(const Geom& g, bool bwd);
 cudaError_t launch_wave(const KParams& p, cudaStream_t s, bool bwd);
-// Threads of a wave-regime CTA.
-constexpr int kWaveThreads = 256;
+// Floats of one wave-regime slot's constants (prefetched with the piece):
+// NHWC, gamma and beta (forward) or gamma, then mean and rstd of its groups
+// (backward) of the unit's Cb channels; NCHW, gamma of the group's Cg
+// channels, then beta of the piece's channel (forward) or the unit's mean and
+// rstd (backward).  Rounded up to 4 floats.
+__host__ __device__ inline int wave_cst_floats(const Geom& g) {
+  const int64_t n = g.layout == kNHWC ? 2 * g.Cb + 2 * (g.Cb / g.Cg) : g.Cg + 2;
+  return (int)((n + 3) & ~int64_t(3));
+}
+
+// Threads of a wave-regime CTA, and such CTAs that share an SM (several
+// independent CTAs per SM overlap one another's barrier-bound phases).
+#ifndef GN_WAVE_THREADS
+#define GN_WAVE_THREADS 256
+#endif
+#ifndef GN_WAVE_CTAS_PER_SM
+#define GN_WAVE_CTAS_PER_SM 1
+#endif
+constexpr int kWaveThreads = GN_WAVE_THREADS;
+constexpr int kWaveCtasPerSm = GN_WAVE_CTAS_PER_SM;
 // gn_resident.cu
 // [N*HW, C] view of an NHWC tensor for TMA, boxes of [g.chunk rows, g.Cb channels].
 cudaError_t encode_nhwc_map(CUtensorMap* map, const void* base, const Geom& g);

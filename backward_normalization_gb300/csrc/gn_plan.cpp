@@ -111,11 +111,19 @@ bool resident_preferred(const Geom& g, int op) {
   return g.Cg * g.HW * esz <= (1 << 20);
 }
 
-// The automatic choice of the wave regime (where its plan fits): measured on
-// GB300 it reads each input once and keeps every SM streaming.
-bool wave_preferred(const Geom& g) {
-  (void)g;
-  return true;
+// The automatic choice of the wave regime (where its plan fits), from
+// measurements on GB300: it reads each input once, but every step of its
+// CTAs runs a chain of short barrier-separated phases (wait, reduce, publish,
+// gather, merge, write) that a 55 KB piece does not hide.  It wins where the
+// op's second read costs most and the units are large: the NCHW backward with
+// units of at least 4 MiB (fp32 112x64x512x512 G8: 4.82 ms against 5.26 ms
+// two-kernel); the NCHW forward (3.55-3.85 against 3.21 ms) and the small
+// channels-last workloads (bf16 8x320x64x64 G32: 41-44 / 92 us against 23 /
+// 40 us; bf16 32x512x32x32 G32: 43-48 / 56-62 against 35 / 38 us) stay with
+// the other families.
+bool wave_preferred(const Geom& g, int op) {
+  const int esz = dtype_size(g.dtype);
+  return g.layout == kNCHW && op == kBwd && g.Cg * g.HW * esz >= (4ll << 20);
 }
 
 // Input that counts as tiny for the automatic choice (see plan_resident).
@@ -354,15 +362,11 @@ namespace {
 #ifndef GN_WAVE_MAX_SLOTS
 #define GN_WAVE_MAX_SLOTS 8
 #endif
-#ifndef GN_WAVE_CTAS_PER_SM
-#define GN_WAVE_CTAS_PER_SM 1
-#endif
 #ifndef GN_WAVE_MAX_CB
 #define GN_WAVE_MAX_CB 128
 #endif
 constexpr int kWaveMinSlots = GN_WAVE_MIN_SLOTS;
 constexpr int kWaveMaxSlots = GN_WAVE_MAX_SLOTS;
-constexpr int kWaveCtasPerSm = GN_WAVE_CTAS_PER_SM;
 constexpr int64_t kWaveMaxCb = GN_WAVE_MAX_CB;  // channels per NHWC unit (TMA box <= 256)
 
 // CTAs of the wave kernel that fit on the device at once with `smem` bytes of
@@ -394,7 +398,7 @@ struct WaveCut {
 };
 
 // Cost model of a wave cut, from measurements on GB300: an SM moves about
-// 45 GB/s (in + out); every step adds about 0.4 us of work that copies do not
+// 45 GB/s (in + out), shared by its CTAs; every step adds about 0.4 us of work that copies do not
 // hide, a unit split over CTAs about 0.3 us more for its arrivals, and with
 // only two slots the wait for a unit is exposed (about 1 us).  A unit whose
 // pieces straddle two steps (P not dividing the CTA count) stalls its CTAs
@@ -403,7 +407,8 @@ struct WaveCut {
 #define GN_WAVE_FORCE_CB 0
 #endif
 double wave_cost(const WaveCut& c, int64_t NC) {
-  const double t_io = (double)(c.slot + c.out) / 45.0e3;  // us at 45 GB/s
+  // us at 45 GB/s per SM, shared by the CTAs on it
+  const double t_io = (double)(c.slot + c.out) * kWaveCtasPerSm / 45.0e3;
   double per_step = t_io + 0.4 + (c.P > 1 ? 0.3 : 0.0) + (c.S < 3 ? 1.0 : 0.0);
   if (c.P > 1 && NC % c.P != 0) per_step += t_io;
   return (double)c.steps * per_step + t_io;
@@ -411,13 +416,24 @@ double wave_cost(const WaveCut& c, int64_t NC) {
 
 // Shared memory of a wave plan besides its slots: the records and CTA sums,
 // the per-channel and per-group values, the mbarriers.
-size_t wave_fixed_bytes(const Geom& g, int64_t P, int64_t Cb, int vec) {
+int64_t wave_red_floats(const Geom& g, int64_t P, int64_t Cb, int vec) {
+  // the unit's records, then the CTA sums: per-thread partials, the shifts
+  // and the per-(column, value) totals of NHWC pieces, or a block-sum scratch
   const int64_t nch = g.layout == kNHWC ? Cb : 1;
-  int64_t red = 2 * P * nch + (g.layout == kNHWC ? 2 * vec * kWaveThreads + Cb : 64);
-  red = std::max<int64_t>(red, 2 * kWaveThreads);
-  const int64_t chs = g.layout == kNHWC ? Cb : g.Cg;
+  const int64_t recs = P > 1 ? P * nch : 2 * nch;  // gathered, or two pieces' own
+  const int64_t red = 2 * recs + (g.layout == kNHWC ? 2 * vec * kWaveThreads + 3 * Cb : 64);
+  return std::max<int64_t>(red, 2 * kWaveThreads);
+}
+
+size_t wave_fixed_bytes(const Geom& g, int64_t P, int64_t Cb, int vec) {
+  const int64_t red = wave_red_floats(g, P, Cb, vec);
   const int64_t grp = g.layout == kNHWC ? Cb / g.Cg : 1;
-  return a128((size_t)red * 4) + a128((size_t)chs * 8) + a128((size_t)grp * 8) + a128(8 * kWaveMaxSlots);
+  Geom t = g;
+  t.Cb = Cb;
+  const size_t cst = (size_t)wave_cst_floats(t) * 4 * kWaveMaxSlots;  // per-slot constants
+  const size_t tab = (size_t)2 * P * 4;                                 // piece counts, planes
+  return a128((size_t)red * 4) + a128(tab) + a128(cst) + a128((size_t)grp * 8) +
+         a128(8 * kWaveMaxSlots);
 }
 
 // Fills the wave-regime fields of g; false when the problem does not fit.
@@ -426,11 +442,13 @@ bool plan_wave(Geom& g, int op, int sm_count) {
   const int vec = 16 / esz;
   const int nten = op == kBwd ? 2 : 1;
   if (g.vw != vec || g.dtype == kF64) return false;
-  const size_t budget = kWaveCtasPerSm == 1 ? kSmemPerCta : kSmemPerSm / kWaveCtasPerSm - 2048;
+  const size_t budget = kWaveCtasPerSm == 1 ? kSmemPerCta : kSmemPerSm / kWaveCtasPerSm - 1024;
   const int64_t NC = (int64_t)sm_count * kWaveCtasPerSm;
   WaveCut best;
   auto consider = [&](WaveCut c, int64_t units) {
     if (c.P < 1 || c.P > NC) return;
+    // every thread polls at most 32 of a unit's records
+    if (c.P * (g.layout == kNHWC ? c.Cb : 1) > 32 * (int64_t)kWaveThreads) return;
     if (GN_WAVE_FORCE_CB > 0 && g.layout == kNHWC && c.Cb != GN_WAVE_FORCE_CB) return;
     const size_t fixed = wave_fixed_bytes(g, c.P, c.Cb, vec);
     if (fixed + 128 + 2 * c.slot > budget) return;
@@ -503,19 +521,19 @@ bool plan_wave(Geom& g, int op, int sm_count) {
   r.ten_stride = (int64_t)(best.slot / nten);
   r.T = 0;
   r.l1 = 1;
-  r.units_fin = r.units;  // a counter per unit, then one per parameter column
-  r.groups1 = r.wcols;
+  r.units_fin = 0;  // no counters: records are polled, the parameter step follows a grid barrier
+  r.groups1 = 0;
   r.unit_groups = 0;
   size_t off = 0;
   r.off_ring = off;
   off += (size_t)r.S * best.slot;
-  const int64_t nch = g.layout == kNHWC ? r.Cb : 1;
-  int64_t red = 2 * r.wP * nch + (g.layout == kNHWC ? 2 * vec * kWaveThreads + r.Cb : 64);
-  red = std::max<int64_t>(red, 2 * kWaveThreads);
+  const int64_t red = wave_red_floats(g, r.wP, r.Cb, vec);
   r.off_red = off;
   off += a128((size_t)red * 4);
-  r.off_tot = off;
-  off += a128((size_t)(g.layout == kNHWC ? r.Cb : g.Cg) * 8);
+  r.off_tot = off;  // piece counts (and NCHW planes) of a unit
+  off += a128((size_t)2 * r.wP * 4);
+  r.off_xch = off;  // per-slot constants
+  off += a128((size_t)wave_cst_floats(r) * 4 * r.S);
   r.off_grp = off;
   off += a128((size_t)(g.layout == kNHWC ? r.Cb / g.Cg : 1) * 8);
   r.off_bar = off;
@@ -524,6 +542,7 @@ bool plan_wave(Geom& g, int op, int sm_count) {
   if (r.smem > budget) return false;
   const int64_t nc = wave_ctas(r, op, r.smem, sm_count, kWaveCtasPerSm);
   if (nc < r.wP) return false;  // a unit's pieces must be co-resident
+  if (r.units * r.wP > 0x7fffffffLL || g.N * g.C * r.Tp > 0x7fffffffLL) return false;  // 32-bit indices
   r.grid = std::min<int64_t>(nc, r.units * r.wP);
   g = r;
   return true;
@@ -734,7 +753,7 @@ Geom plan_geom(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout, 
     plan_pipelined(g, op, sm_count);
   } else if (ov == kRegimeWave) {
     plan_wave(g, op, sm_count);
-  } else if (ov == kRegimeAuto && wave_preferred(g) && plan_wave(g, op, sm_count)) {
+  } else if (ov == kRegimeAuto && wave_preferred(g, op) && plan_wave(g, op, sm_count)) {
     // taken
   } else if (ov == kRegimeAuto && resident_preferred(g, op)) {
     // measured on GB300: the pipelined kernel moves the minimal traffic but is

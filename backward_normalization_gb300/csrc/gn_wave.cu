@@ -12,13 +12,20 @@
 // The plan makes P divide NC where it can, so that the pieces of a unit all
 // belong to one step and arrive together.
 //
-// Per piece: bulk (TMA) copies bring it into one of S shared-memory slots,
-// S-1 pieces ahead of the one in use; the CTA reduces it, writes one record
-// per channel to the workspace and arrives on the unit's counter; it waits
-// (bounded) until all P pieces of the unit have arrived, merges the unit's
-// records in a fixed order into the group statistics (forward) or the dx
-// coefficients (backward), and writes the piece's output from shared memory.
-// x (and dy) are read from HBM once.
+// Per piece: bulk (TMA) copies bring it into one of S shared-memory slots
+// (all slots are kept loading); stage A reduces the piece and writes one
+// record per channel to the workspace; stage B reads every record of the
+// piece's unit (polling until all are written, bounded), merges them in a
+// fixed order into the group statistics (forward) or the dx coefficients
+// (backward), and writes the piece's output from shared memory.  With three
+// or more slots stage A runs one piece ahead of stage B, so a unit's records
+// are normally all written when a CTA reaches it.  x (and dy) are read from
+// HBM once.
+//
+// Records are self-validating 64-bit words (a cleared word is zero, a written
+// one never is), written and polled with single relaxed accesses: no
+// release/acquire pair orders them, so publishing a record never waits for
+// the CTA's earlier output stores to drain.
 //
 // A CTA waits for other CTAs' pieces, so all CTAs must be co-resident: the
 // kernel is launched cooperatively.  Deadlock-freedom: a CTA publishes its
@@ -29,24 +36,26 @@
 // unit, since P <= NC); by the minimality of u those steps complete, so every
 // piece of u is published.
 //
-// The counters start from whatever the workspace holds: CTA 0 zero-fills the
-// error word and the counters, and a grid-wide barrier, entered after each
-// CTA has issued its first copies (whose latency hides it), orders that
-// before any arrival.  Every wait is bounded in time; one that runs out sets
-// a bit of the error word (gn_workspace_status reports it), after which every
-// CTA skips its remaining work, waiting only for its own copies in flight.
+// The workspace holds anything when the call starts: CTA 0 zero-fills the
+// error word, every CTA the record slots of its own pieces, and a grid-wide
+// barrier (entered after each CTA has issued its first copies, whose latency
+// hides it) orders that before any record is written.  Every wait is bounded
+// in time; one that runs out sets a bit of the error word (gn_workspace_status
+// reports it), after which every CTA skips its remaining work, waiting only
+// for its own copies in flight.  The backward's dgamma / dbeta follow a second
+// grid barrier, spread over the CTAs by channel.
 //
 // Statistics.  A forward record is, per (piece, channel), the mean and the
-// sum of squared deviations M2 of the piece's values, accumulated about the
-// piece's first value (a shift that keeps the sums small).  The records of a
-// channel are merged in piece order with the pairwise update of Chan, Golub
-// and LeVeque (counts na, nb: delta = mean_b - mean_a, mean = mean_a +
-// delta*nb/(na+nb), M2 = M2_a + M2_b + delta^2*na*nb/(na+nb)), and the
-// channels of a group by M2_g = sum M2_c + HW * sum (mean_c - mean_g)^2, the
-// same identity for equal counts.  A backward record is, per (piece,
-// channel), sum(dy) and sum(dy*(x - mean)), added per channel in piece order.
-// Every CTA of a unit merges the same records in the same order, so all of
-// them use identical statistics; results are bit-identical from run to run.
+// sum of squared deviations M2 of the piece's n_i values, accumulated about
+// the piece's first value (a shift that keeps the sums small).  A group's
+// records merge by the parallel-axis identity (Chan, Golub and LeVeque),
+// taken over all of them at once: mean = sum(n_i * mean_i) / M and M2 =
+// sum(M2_i + n_i * (mean_i - mean)^2), M = Cg*HW.  A backward record is, per
+// (piece, channel), sum(dy) and sum(dy*(x - mean)); a group's coefficients
+// come from sum gamma_c * S1 and sum gamma_c * S2 over its records.  Every
+// CTA of a unit merges the same records in the same order (lane i of a warp
+// takes records i, i + 32, ..., then a fixed xor tree), so all of them use
+// identical statistics; results are bit-identical from run to run.
 #include <cooperative_groups.h>
 
 #include "gn_finalize.cuh"
@@ -85,110 +94,178 @@ __device__ bool wait_bar_t0(uint64_t* bar, uint32_t parity, unsigned* err) {
   }
 }
 
-// Thread 0: waits until the counter reaches `want` (acquire), bounded in time;
-// gives up when the error word is raised.
-__device__ bool wait_count_t0(const unsigned* ctr, unsigned want, unsigned* err) {
+// A piece's record in the workspace: two floats in one 64-bit word, each
+// XORed with kWaveKey (a NaN bit pattern that arithmetic never produces), so
+// that a written record is never zero while a cleared slot is.  Written and
+// read as single 64-bit accesses: a reader that sees a non-zero word has the
+// record itself, and no release / acquire ordering is needed -- in
+// particular a CTA's records never wait for its earlier output stores.
+constexpr uint32_t kWaveKey = 0x7fbadbadu;
+
+__device__ __forceinline__ void put_rec(float2* slot, float2 v) {
+  const unsigned long long w =
+      ((unsigned long long)(__float_as_uint(v.y) ^ kWaveKey) << 32) | (__float_as_uint(v.x) ^ kWaveKey);
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(slot), "l"(w) : "memory");
+}
+
+__device__ __forceinline__ bool get_rec(const float2* slot, float2* v) {
+  unsigned long long w;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(w) : "l"(slot) : "memory");
+  if (w == 0ull) return false;
+  v->x = __uint_as_float((unsigned)w ^ kWaveKey);
+  v->y = __uint_as_float((unsigned)(w >> 32) ^ kWaveKey);
+  return true;
+}
+
+// A record's raw word, loaded without waiting for it (the caller decodes it
+// later, so the load's latency overlaps other work).
+__device__ __forceinline__ unsigned long long ld_rec_raw(const float2* slot) {
+  unsigned long long w;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(w) : "l"(slot) : "memory");
+  return w;
+}
+__device__ __forceinline__ float2 rec_decode(unsigned long long w) {
+  return make_float2(__uint_as_float((unsigned)w ^ kWaveKey),
+                     __uint_as_float((unsigned)(w >> 32) ^ kWaveKey));
+}
+
+// This thread's share of a unit's n records: records tid + i*blockDim.x,
+// bit i of the mask for each (a thread holds at most 32: n <= 32*blockDim.x).
+__device__ __forceinline__ unsigned record_mask(int n) {
+  const int tid = threadIdx.x, nt = blockDim.x;
+  unsigned todo = 0;
+  for (int i = 0; i < 32 && tid + i * nt < n; ++i) todo |= 1u << i;
+  return todo;
+}
+
+// Every thread: reads the records at src still marked in `todo` into dst
+// (shared memory), polling until all of them are written.  Bounded in time
+// (thread 0 keeps the clock); returns false, uniformly, when the bound runs
+// out or the error word is raised.
+__device__ bool gather_records(const float2* src, float2* dst, unsigned todo, unsigned* err,
+                               int* s_flag) {
+  const int tid = threadIdx.x, nt = blockDim.x;
   uint64_t t0 = 0;
-  for (uint32_t i = 0;; ++i) {
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
-    if (v == want) return true;
-    if ((i & 15) == 15) {
-      if (aborted(err)) return false;
-      const uint64_t t = now_ns();
-      if (t0 == 0) {
-        t0 = t;
-      } else if (t - t0 > kWaveWaitNs) {
-        atomicOr(err, kErrUnit);
-        return false;
+  for (unsigned round = 0;; ++round) {
+    for (int i = 0; i < 32 && (todo >> i) != 0u; ++i) {
+      if (!((todo >> i) & 1u)) continue;
+      float2 v;
+      if (get_rec(src + tid + i * nt, &v)) {
+        dst[tid + i * nt] = v;
+        todo &= ~(1u << i);
       }
     }
-    __nanosleep(20);
+    if (!__syncthreads_or(todo != 0u)) return true;
+    if (tid == 0) {
+      int go = 1;
+      if ((round & 7u) == 7u && aborted(err)) {
+        go = 0;
+      } else {
+        const uint64_t t = now_ns();
+        if (t0 == 0) {
+          t0 = t;
+        } else if (t - t0 > kWaveWaitNs) {
+          atomicOr(err, kErrUnit);
+          go = 0;
+        }
+      }
+      *s_flag = go;
+    }
+    __syncthreads();
+    if (!*s_flag) return false;
+    __nanosleep(64);
   }
 }
 
-// Pairwise merge of (count, mean, M2) accumulators (Chan, Golub, LeVeque).
-struct Moments {
-  float n, mean, m2;
-};
-__device__ __forceinline__ void merge_into(Moments& a, float nb, float mb, float m2b) {
-  const float n = a.n + nb;
-  const float delta = mb - a.mean;
-  const float f = nb / n;
-  a.mean = fmaf(delta, f, a.mean);
-  a.m2 = a.m2 + m2b + delta * delta * a.n * f;
-  a.n = n;
+// Sum over the 32 lanes of a warp with a fixed xor tree; every lane gets it.
+__device__ __forceinline__ float warp_allsum(float v) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  return v;
 }
 
-// The piece that CTA `b` processes at step k, decoded.
+// The piece that CTA b processes at step k, decoded (32-bit index arithmetic:
+// the plan keeps units * pieces below 2^31).
 struct Piece {
-  int64_t q, u, t;
-  int64_t n;       // sample
-  int64_t gi;      // NCHW: the unit's group
-  int64_t c;       // NCHW: the piece's channel
-  int64_t e0;      // NCHW: first element (flat offset)
-  int64_t len;     // NCHW: elements; NHWC: rows
-  int64_t cb;      // NHWC: channel block of the unit
-  int64_t cbase;   // NHWC: first channel of the unit
-  int64_t r0;      // NHWC: first row (within the sample)
+  int u, t;       // unit, piece within the unit
+  int n;          // sample
+  int gi;         // NCHW: the unit's group
+  int c;          // NCHW: the piece's channel
+  int cb;         // NHWC: channel block of the unit
+  int len;        // NCHW: elements; NHWC: rows
+  int64_t e0;     // NCHW: first element (flat offset)
+  int64_t row0;   // NHWC: first row in the [N*HW, C] view
+  int cbase;      // NHWC: first channel of the unit
 };
 
 template <int LAYOUT>
-__device__ __forceinline__ Piece piece_of(const Geom& g, int64_t q) {
+__device__ __forceinline__ Piece piece_of(const Geom& g, int q) {
   Piece pc;
-  pc.q = q;
-  pc.u = q / g.wP;
-  pc.t = q - pc.u * g.wP;
+  const int P = (int)g.wP;
+  pc.u = q / P;
+  pc.t = q - pc.u * P;
+  const int HW32 = (int)(g.HW < 0x7fffffff ? g.HW : 0x7fffffff);
+  const int R = (int)g.wR;
   if (LAYOUT == kNCHW) {
-    pc.n = pc.u / g.G;
-    pc.gi = pc.u - pc.n * g.G;
-    const int64_t plane = pc.t / g.wm, seg = pc.t - plane * g.wm;
-    pc.c = pc.gi * g.Cg + plane;
-    const int64_t h0 = seg * g.wR;
-    pc.len = (h0 + g.wR < g.HW) ? g.wR : g.HW - h0;
-    pc.e0 = (pc.n * g.C + pc.c) * g.HW + h0;
-    pc.cb = pc.cbase = pc.r0 = 0;
+    const int G = (int)g.G, wm = (int)g.wm;
+    pc.n = pc.u / G;
+    pc.gi = pc.u - pc.n * G;
+    const int plane = pc.t / wm, seg = pc.t - plane * wm;
+    pc.c = pc.gi * (int)g.Cg + plane;
+    const int64_t h0 = (int64_t)seg * R;
+    pc.len = (int)((h0 + R < g.HW) ? R : g.HW - h0);
+    pc.e0 = ((int64_t)pc.n * g.C + pc.c) * g.HW + h0;
+    pc.cb = pc.cbase = 0;
+    pc.row0 = 0;
   } else {
-    pc.n = pc.u / g.ncbu;
-    pc.cb = pc.u - pc.n * g.ncbu;
-    pc.cbase = pc.cb * g.Cb;
-    pc.r0 = pc.t * g.wR;
-    pc.len = (pc.r0 + g.wR < g.HW) ? g.wR : g.HW - pc.r0;
-    pc.gi = pc.c = pc.e0 = 0;
+    const int ncbu = (int)g.ncbu;
+    pc.n = pc.u / ncbu;
+    pc.cb = pc.u - pc.n * ncbu;
+    pc.cbase = pc.cb * (int)g.Cb;
+    const int r0 = pc.t * R;
+    pc.len = (r0 + R < HW32) ? R : HW32 - r0;
+    pc.row0 = (int64_t)pc.n * g.HW + r0;
+    pc.gi = pc.c = 0;
+    pc.e0 = 0;
   }
   return pc;
 }
 
-// Number of values of piece t of a unit (rows for NHWC, elements for NCHW).
-__device__ __forceinline__ float piece_count(const Geom& g, int64_t t) {
-  const int64_t seg = g.layout == kNCHW ? t % g.wm : t;
-  const int64_t a = seg * g.wR;
+// Values in piece t of a unit (rows for NHWC, elements of a plane for NCHW).
+__device__ __forceinline__ float piece_count(const Geom& g, int t) {
+  const int seg = g.layout == kNCHW ? t % (int)g.wm : t;
+  const int64_t a = (int64_t)seg * g.wR;
   return (float)((a + g.wR < g.HW) ? g.wR : g.HW - a);
 }
 
 template <typename T, int VW, int LAYOUT, bool BWD>
-__global__ void __launch_bounds__(kWaveThreads, 1) wave_kernel(const __grid_constant__ KParams p) {
+__global__ void __launch_bounds__(kWaveThreads, kWaveCtasPerSm) wave_kernel(const __grid_constant__ KParams p) {
   extern __shared__ __align__(128) char smem_raw[];
   char* smem =
       reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
   const Geom& g = p.g;
   constexpr int NTEN = BWD ? 2 : 1;
-  const int tid = threadIdx.x;
-  const int nt = blockDim.x;
+  const int tid = threadIdx.x, nt = blockDim.x;
+  const int lane = tid & 31, warp = tid >> 5, nwarps = nt >> 5;
   char* ring = smem + g.off_ring;
-  float* red = reinterpret_cast<float*>(smem + g.off_red);    // CTA sums, then the unit's records
-  float2* chs = reinterpret_cast<float2*>(smem + g.off_tot);  // per-channel results of the unit
+  float* red = reinterpret_cast<float*>(smem + g.off_red);
   float2* grp = reinterpret_cast<float2*>(smem + g.off_grp);  // per-group results of the unit
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + g.off_bar);
   __shared__ int s_ok;
-  __shared__ int s_last;
 
-  const int64_t NC = gridDim.x;
-  const int64_t total = g.units * g.wP;
-  const int64_t K = blockIdx.x < total ? (total - 1 - blockIdx.x) / NC + 1 : 0;
+  const int NC = gridDim.x, b = blockIdx.x;
+  const int P = (int)g.wP;
+  const int total = (int)(g.units * g.wP);
+  const int K = b < total ? (total - 1 - b) / NC + 1 : 0;  // this CTA's pieces
   const int S = g.S;
+  const int nch = LAYOUT == kNHWC ? (int)g.Cb : 1;  // channels of a piece
+  const int Cg = (int)g.Cg;
+  const int rec_unit = P * nch;  // records of a unit
+  // shared scratch: the unit's records (P > 1: gathered; P == 1: the CTA's
+  // own, two pieces' worth), then the CTA sums
+  float2* recs = reinterpret_cast<float2*>(red);
+  float* cred = red + 2 * (P > 1 ? rec_unit : 2 * nch);
   const size_t slot_bytes = (size_t)g.ten_stride * NTEN;
-  const int64_t P = g.wP;
   const T* x = static_cast<const T*>(p.x);
   const T* dy = static_cast<const T*>(p.dy);
   T* out = static_cast<T*>(p.out);
@@ -203,421 +280,512 @@ __global__ void __launch_bounds__(kWaveThreads, 1) wave_kernel(const __grid_cons
 
   // ---- copies: piece k of this CTA into slot k % S (thread 0)
   const uint64_t pol_in = policy_evict_first();
-  auto issue = [&](int64_t k) {
-    const Piece pc = piece_of<LAYOUT>(g, k * NC + blockIdx.x);
-    char* dst = ring + (k % S) * slot_bytes;
+  auto issue = [&](int k) {
+    const Piece pc = piece_of<LAYOUT>(g, k * NC + b);
+    char* dst = ring + (size_t)(k % S) * slot_bytes;
     uint64_t* bar = full + (k % S);
     if (LAYOUT == kNCHW) {
-      const uint32_t bytes = (uint32_t)(pc.len * (int64_t)sizeof(T));
+      const uint32_t bytes = (uint32_t)pc.len * (uint32_t)sizeof(T);
       mbar_arrive_expect_tx(bar, bytes * NTEN);
       tma_load_1d(dst, x + pc.e0, bytes, bar, pol_in);
       if (BWD) tma_load_1d(dst + g.ten_stride, dy + pc.e0, bytes, bar, pol_in);
     } else {
       const uint32_t box = (uint32_t)(g.chunk * g.Cb * (int64_t)sizeof(T));
       mbar_arrive_expect_tx(bar, box * (uint32_t)g.wnb * NTEN);
-      for (int64_t b = 0; b < g.wnb; ++b) {
-        const int32_t row = (int32_t)(pc.n * g.HW + pc.r0 + b * g.chunk);
-        tma_load_2d(dst + b * box, &p.tmx, (int32_t)pc.cbase, row, bar, pol_in);
-        if (BWD) tma_load_2d(dst + g.ten_stride + b * box, &p.tmdy, (int32_t)pc.cbase, row, bar, pol_in);
+      for (int bx = 0; bx < (int)g.wnb; ++bx) {
+        const int32_t row = (int32_t)(pc.row0 + (int64_t)bx * g.chunk);
+        tma_load_2d(dst + (size_t)bx * box, &p.tmx, pc.cbase, row, bar, pol_in);
+        if (BWD) tma_load_2d(dst + g.ten_stride + (size_t)bx * box, &p.tmdy, pc.cbase, row, bar, pol_in);
       }
     }
   };
-  int64_t issued = 0;  // thread 0: pieces whose copies were issued
+  int issued = 0;  // thread 0: pieces whose copies were issued
   if (tid == 0)
-    for (; issued < K && issued < S - 1; ++issued) issue(issued);
+    for (; issued < K && issued < S; ++issued) issue(issued);
 
-  // ---- the counters start from whatever the workspace held: clear them
-  // once, then a grid barrier before any arrival
-  if (blockIdx.x == 0)
+  // ---- the workspace holds anything when the call starts: CTA 0 clears the
+  // error word, every CTA the record slots of its own pieces, and a grid
+  // barrier orders those stores before any record is written or polled
+  if (b == 0)
     for (int i = tid; i < p.clear_words; i += nt) p.err[i] = 0u;
+  // a unit's piece counts (and, NCHW, each piece's plane), for the merges
+  float* cnt = reinterpret_cast<float*>(smem + g.off_tot);
+  int* plane_of = reinterpret_cast<int*>(cnt + P);
+  for (int t = tid; t < P; t += nt) {
+    cnt[t] = piece_count(g, t);
+    plane_of[t] = LAYOUT == kNCHW ? t / (int)g.wm : 0;
+  }
+  if (P > 1) {
+    unsigned long long* slots = reinterpret_cast<unsigned long long*>(p.part);
+    for (int i = tid; i < K * nch; i += nt) {
+      const int kk = i / nch, c = i - kk * nch;
+      const int q = kk * NC + b;
+      slots[(int64_t)(q / P) * rec_unit + (q % P) * nch + c] = 0ull;
+    }
+  }
   cooperative_groups::this_grid().sync();
 
-  // NHWC thread layout: column j (VW channels of the block) of rows rl,
-  // rl + rpi, ...; NCHW: the piece's 16-byte vectors tid, tid + nt, ...
-  const int Wv = LAYOUT == kNHWC ? (int)(g.Cb / VW) : 1;
+  // ---- per-thread layout.  NHWC: column j (VW channels of the block) of rows
+  // rl, rl + rpi, ...; qe[e] is the group (within the block) of its channel
+  // e.  NCHW: the piece's 16-byte vectors tid, tid + nt, ...
+  const int Wv = LAYOUT == kNHWC ? nch / VW : 1;
   const int rpi = LAYOUT == kNHWC ? nt / Wv : nt;
   const int j = LAYOUT == kNHWC ? tid % Wv : 0;
   const int rl = LAYOUT == kNHWC ? tid / Wv : tid;
   const bool lane_ok = LAYOUT == kNHWC ? rl < rpi : true;
-  const int64_t rowb = g.Cb * (int64_t)sizeof(T);  // NHWC: bytes per row in a slot
+  int qe[VW];
+#pragma unroll
+  for (int e = 0; e < VW; ++e) qe[e] = LAYOUT == kNHWC ? (j * VW + e) / Cg : 0;
+  const int rowb = nch * (int)sizeof(T);  // NHWC: bytes per row in a slot
   const uint64_t pol_out = policy_evict_first();
-  const int64_t nch = LAYOUT == kNHWC ? g.Cb : 1;  // channels of a piece
-  const int64_t rec_per_unit = P * nch;
+  const float Mg = (float)(g.Cg * g.HW);  // values per group
+  const int ngrp = LAYOUT == kNHWC ? nch / Cg : 1;  // groups of a unit
 
-  int64_t k = 0;
-  bool ok = true;
-  for (; k < K; ++k) {
-    if (tid == 0 && issued < K && issued == k + S - 1) {
-      fence_proxy_async_smem();  // the slot's previous reads precede the new copy
-      issue(issued);
-      ++issued;
+  // ---- per-slot constants of a piece, fetched one step ahead with 4-byte
+  // asynchronous copies (every thread commits one cp.async group per call)
+  const int CST = wave_cst_floats(g);
+  float* cstb = reinterpret_cast<float*>(smem + g.off_xch);
+  auto fetch_constants = [&](int k) {
+    if (k < K) {
+      const Piece pc = piece_of<LAYOUT>(g, k * NC + b);
+      float* cs = cstb + (k % S) * CST;
+      if (LAYOUT == kNHWC) {
+        for (int c = tid; c < nch; c += nt) {
+          if (p.gamma) cp_async4(cs + c, p.gamma + pc.cbase + c);
+          else cs[c] = 1.0f;
+          if (!BWD) {
+            if (p.beta) cp_async4(cs + nch + c, p.beta + pc.cbase + c);
+            else cs[nch + c] = 0.f;
+          }
+        }
+        if (BWD) {
+          const int64_t gb = (int64_t)pc.n * g.G + pc.cbase / Cg;
+          for (int q = tid; q < ngrp; q += nt) {
+            cp_async4(cs + nch + q, p.mean + gb + q);
+            cp_async4(cs + nch + ngrp + q, p.rstd + gb + q);
+          }
+        }
+      } else {
+        for (int cl = tid; cl < Cg; cl += nt) {
+          if (p.gamma) cp_async4(cs + cl, p.gamma + (int64_t)pc.gi * Cg + cl);
+          else cs[cl] = 1.0f;
+        }
+        if (tid == nt - 1) {
+          if (BWD) {
+            cp_async4(cs + Cg, p.mean + pc.u);
+            cp_async4(cs + Cg + 1, p.rstd + pc.u);
+          } else if (p.beta) {
+            cp_async4(cs + Cg, p.beta + pc.c);
+          } else {
+            cs[Cg] = 0.f;
+          }
+        }
+      }
     }
-    const Piece pc = piece_of<LAYOUT>(g, k * NC + blockIdx.x);
-    const char* slot = ring + (k % S) * slot_bytes;
+    cp_async_commit();
+  };
+  fetch_constants(0);
+
+  // ---- a unit's records are read ahead, during the stage A before their
+  // stage B (when stage A runs ahead): raw words land in registers while the
+  // stage works, and are decoded into shared memory at its end
+  constexpr int kPre = 8;  // records per thread read ahead (at most)
+  const bool read_ahead = P > 1 && S >= 3 && rec_unit <= kPre * nt;
+  unsigned long long pre[kPre];
+  int pre_unit = -1;       // the unit whose records sit in `recs`, or -1
+  unsigned pre_todo = 0;   // of those, the ones not yet written
+
+  // ---- stage A of piece k: wait for its copy, reduce it, publish its records
+  auto stage_a = [&](int k) -> bool {
+    const Piece pc = piece_of<LAYOUT>(g, k * NC + b);
+    const int si = k % S;
+    const char* slot = ring + (size_t)si * slot_bytes;
+    const float* cs = cstb + si * CST;
     const uint32_t parity = (uint32_t)((k / S) & 1);
-    if (tid == 0) s_ok = aborted(p.err) ? 0 : (wait_bar_t0(full + (k % S), parity, p.err) ? 1 : 0);
-    __syncthreads();
-    if (!s_ok) {
-      ok = false;
-      break;
+    cp_async_wait_all();    // this piece's constants (fetched one step ago)
+    fetch_constants(k + 1);  // and the next piece's, for the next step
+    // the records of the unit of the stage B that follows (piece k - 1)
+    const int pre_k = k - 1;
+    const int pre_u = read_ahead && pre_k >= 0 ? piece_of<LAYOUT>(g, pre_k * NC + b).u : -1;
+    if (pre_u >= 0) {
+      const float2* src = p.part + (int64_t)pre_u * rec_unit;
+#pragma unroll
+      for (int i = 0; i < kPre; ++i)
+        pre[i] = tid + i * nt < rec_unit ? ld_rec_raw(src + tid + i * nt) : 0ull;
     }
-    mbar_try_wait(full + (k % S), parity);  // completed: orders this thread's reads after the copy
-
-    // ---- reduce the piece: one record per channel
-    const int64_t rbase = pc.u * rec_per_unit + pc.t * nch;  // first record of the piece
-    float2* rec_g = p.part + rbase;
-    float2* rec_s = reinterpret_cast<float2*>(red) + pc.t * nch;  // P == 1: kept in smem
+    if (tid == 0)
+      s_ok = mbar_try_wait(full + si, parity)
+                 ? 1
+                 : (aborted(p.err) ? 0 : (wait_bar_t0(full + si, parity, p.err) ? 1 : 0));
+    __syncthreads();  // also publishes the constants to every thread
+    if (!s_ok) return false;
+    mbar_try_wait(full + si, parity);  // completed: orders this thread's reads after the copy
+    float2* rec_g = p.part + (int64_t)pc.u * rec_unit + pc.t * nch;
+    float2* rec_s = recs + (k & 1) * nch;  // P == 1: kept in shared memory
+    const bool publish = !(p.stall_unit == pc.u && pc.t == 0);  // fault injection
     if (LAYOUT == kNCHW) {
-      const float mu = BWD ? __ldg(p.mean + pc.u) : 0.f;
+      const float mu = BWD ? cs[Cg] : 0.f;
       const float K0 = BWD ? 0.f : Elem<T>::to_f(reinterpret_cast<const T*>(slot)[0]);
-      float a = 0.f, b = 0.f;
-      const int64_t nv = pc.len / VW;
-      for (int64_t v = tid; v < nv; v += nt) {
+      float a = 0.f, c = 0.f;
+      const int nv = pc.len / VW;
+#pragma unroll 4
+      for (int v = tid; v < nv; v += nt) {
         float xv[VW];
-        Access<T, VW>::unpack(lds16(slot + v * 16), xv);
+        Access<T, VW>::unpack(lds16(slot + (size_t)v * 16), xv);
         if (BWD) {
           float dv[VW];
-          Access<T, VW>::unpack(lds16(slot + g.ten_stride + v * 16), dv);
+          Access<T, VW>::unpack(lds16(slot + g.ten_stride + (size_t)v * 16), dv);
 #pragma unroll
           for (int e = 0; e < VW; ++e) {
             a += dv[e];
-            b = fmaf(dv[e], xv[e] - mu, b);
+            c = fmaf(dv[e], xv[e] - mu, c);
           }
         } else {
 #pragma unroll
           for (int e = 0; e < VW; ++e) {
             const float d = xv[e] - K0;
             a += d;
-            b = fmaf(d, d, b);
+            c = fmaf(d, d, c);
           }
         }
       }
-      const float2 s2 = block_sum2_t0(a, b, red + 2 * rec_per_unit);
+      const float2 s2 = block_sum2_t0(a, c, cred);
       if (tid == 0) {
         float2 r;
         if (BWD) {
           r = s2;
         } else {
-          const float n = (float)pc.len;
-          const float q = s2.x / n;
+          const float q = s2.x / (float)pc.len;
           r = make_float2(K0 + q, fmaxf(fmaf(-s2.x, q, s2.y), 0.f));
         }
-        if (P > 1) rec_g[0] = r;
-        else rec_s[0] = r;
+        if (P == 1) rec_s[0] = r;
+        else if (publish) put_rec(rec_g, r);
       }
     } else {
       float acc[2 * VW], Ks[VW];
 #pragma unroll
       for (int q = 0; q < 2 * VW; ++q) acc[q] = 0.f;
-      {
+      if (lane_ok) {
         float mu[VW];
+        if (BWD) {
 #pragma unroll
-        for (int e = 0; e < VW; ++e) mu[e] = 0.f;
-        if (lane_ok) {
+          for (int e = 0; e < VW; ++e) mu[e] = cs[nch + qe[e]];
+        } else {
+          Access<T, VW>::unpack(lds16(slot + j * 16), Ks);  // the piece's first row: the shift
+        }
+        const char* col = slot + j * 16;
+#pragma unroll 2
+        for (int r = rl; r < pc.len; r += rpi) {
+          float xv[VW];
+          Access<T, VW>::unpack(lds16(col + (size_t)r * rowb), xv);
           if (BWD) {
+            float dv[VW];
+            Access<T, VW>::unpack(lds16(col + g.ten_stride + (size_t)r * rowb), dv);
 #pragma unroll
-            for (int e = 0; e < VW; ++e)
-              mu[e] = __ldg(p.mean + pc.n * g.G + (pc.cbase + j * VW + e) / g.Cg);
+            for (int e = 0; e < VW; ++e) {
+              acc[2 * e] += dv[e];
+              acc[2 * e + 1] = fmaf(dv[e], xv[e] - mu[e], acc[2 * e + 1]);
+            }
           } else {
-            Access<T, VW>::unpack(lds16(slot + j * 16), Ks);  // the piece's first row
-          }
-          for (int64_t r = rl; r < pc.len; r += rpi) {
-            float xv[VW];
-            Access<T, VW>::unpack(lds16(slot + r * rowb + j * 16), xv);
-            if (BWD) {
-              float dv[VW];
-              Access<T, VW>::unpack(lds16(slot + g.ten_stride + r * rowb + j * 16), dv);
 #pragma unroll
-              for (int e = 0; e < VW; ++e) {
-                acc[2 * e] += dv[e];
-                acc[2 * e + 1] = fmaf(dv[e], xv[e] - mu[e], acc[2 * e + 1]);
-              }
-            } else {
-#pragma unroll
-              for (int e = 0; e < VW; ++e) {
-                const float d = xv[e] - Ks[e];
-                acc[2 * e] += d;
-                acc[2 * e + 1] = fmaf(d, d, acc[2 * e + 1]);
-              }
+            for (int e = 0; e < VW; ++e) {
+              const float d = xv[e] - Ks[e];
+              acc[2 * e] += d;
+              acc[2 * e + 1] = fmaf(d, d, acc[2 * e + 1]);
             }
           }
         }
       }
-      // CTA sums: every (column, value) adds its rpi row lanes in lane order
-      float* cred = red + 2 * rec_per_unit;  // after the records kept in smem
+      // CTA sums: each of the 2*nch sums (value q of column jj) is taken by
+      // tps lanes of one warp; lane l adds row lanes l, l + tps, ... into four
+      // accumulators in a fixed rotation, then the lanes meet in a fixed xor
+      // tree
 #pragma unroll
       for (int q = 0; q < 2 * VW; ++q) cred[q * nt + tid] = acc[q];
+      float* ksh = cred + 2 * VW * nt;
+      float* sums = ksh + nch;
       if (!BWD && rl == 0 && lane_ok) {
-        float* ksh = cred + 2 * VW * nt;
 #pragma unroll
         for (int e = 0; e < VW; ++e) ksh[j * VW + e] = Ks[e];
       }
       __syncthreads();
-      const float n = (float)pc.len;
-      for (int64_t c = tid; c < g.Cb; c += nt) {
-        const int jj = (int)(c / VW), e = (int)(c % VW);
-        float sa = 0.f, sb = 0.f;
-        for (int r = 0; r < rpi; ++r) {
-          sa += cred[(2 * e) * nt + r * Wv + jj];
-          sb += cred[(2 * e + 1) * nt + r * Wv + jj];
+      {
+        const int nsum = 2 * VW * Wv;
+        int tps = 1;
+        while (tps < 32 && 2 * tps * nsum <= nt) tps *= 2;
+        const int sidx = tid / tps, l = tid % tps;
+        const bool mine = sidx < nsum;
+        const int q = mine ? sidx / Wv : 0, jj = mine ? sidx % Wv : 0;
+        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+        if (mine) {
+          const float* src = cred + q * nt + jj;
+          int r = l;
+          for (; r + 3 * tps < rpi; r += 4 * tps) {
+            a0 += src[r * Wv];
+            a1 += src[(r + tps) * Wv];
+            a2 += src[(r + 2 * tps) * Wv];
+            a3 += src[(r + 3 * tps) * Wv];
+          }
+          for (; r < rpi; r += tps) a0 += src[r * Wv];
         }
+        float a = (a0 + a1) + (a2 + a3);
+        for (int off = tps / 2; off > 0; off >>= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
+        if (mine && l == 0) sums[sidx] = a;
+      }
+      __syncthreads();
+      const float n = (float)pc.len;
+      for (int c = tid; c < nch; c += nt) {
+        const int jj = c / VW, e = c - jj * VW;
+        const float sa = sums[(2 * e) * Wv + jj];
+        const float sb = sums[(2 * e + 1) * Wv + jj];
         float2 rr;
         if (BWD) {
           rr = make_float2(sa, sb);
         } else {
-          const float Kc = cred[2 * VW * nt + c];
           const float q = sa / n;
-          rr = make_float2(Kc + q, fmaxf(fmaf(-sa, q, sb), 0.f));
+          rr = make_float2(ksh[c] + q, fmaxf(fmaf(-sa, q, sb), 0.f));
         }
-        if (P > 1) rec_g[c] = rr;
-        else rec_s[c] = rr;
+        if (P == 1) rec_s[c] = rr;
+        else if (publish) put_rec(rec_g + c, rr);
       }
     }
+    __syncthreads();  // the records are out; the scratch is free
+    if (pre_u >= 0) {
+      unsigned todo = 0;
+#pragma unroll
+      for (int i = 0; i < kPre; ++i) {
+        if (tid + i * nt >= rec_unit) continue;
+        if (pre[i]) recs[tid + i * nt] = rec_decode(pre[i]);
+        else todo |= 1u << i;
+      }
+      pre_todo = todo;
+      pre_unit = pre_u;
+    }
+    return true;
+  };
 
-    // ---- publish the piece's records, wait for the unit
-    __syncthreads();
+  // ---- stage B of piece k: the unit's records (all published by now, or
+  // polled until they are), the group statistics, the piece's output
+  auto stage_b = [&](int k) -> bool {
+    const Piece pc = piece_of<LAYOUT>(g, k * NC + b);
+    const char* slot = ring + (size_t)(k % S) * slot_bytes;
+    const float* cs = cstb + (k % S) * CST;
+    const float2* R = recs + (k & 1) * nch;
     if (P > 1) {
-      if (tid == 0) {
-        if (!(p.stall_unit == pc.u && pc.t == 0))
-          asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(p.tickets + pc.u) : "memory");
-        s_ok = wait_count_t0(p.tickets + pc.u, (unsigned)P, p.err) ? 1 : 0;
-      }
-      __syncthreads();
-      if (!s_ok) {
-        ok = false;
-        ++k;  // this piece's data was consumed
-        break;
-      }
-      // the unit's records into shared memory (one round trip)
-      const float2* src = p.part + pc.u * rec_per_unit;
-      float2* dst = reinterpret_cast<float2*>(red);
-      for (int64_t i = tid; i < rec_per_unit; i += nt) dst[i] = __ldcg(src + i);
-      __syncthreads();
+      const unsigned todo = pre_unit == pc.u ? pre_todo : record_mask(rec_unit);
+      pre_unit = -1;
+      if (!gather_records(p.part + (int64_t)pc.u * rec_unit, recs, todo, p.err, &s_ok))
+        return false;
+      R = recs;
     }
-
-    // ---- merge: per channel over the pieces (piece order), then per group
-    const float2* recs = reinterpret_cast<const float2*>(red);
-    if (LAYOUT == kNCHW) {
-      // channel cl of the group: pieces cl*wm .. cl*wm + wm - 1
-      for (int64_t cl = tid; cl < g.Cg; cl += nt) {
-        if (BWD) {
-          float sa = 0.f, sb = 0.f;
-          for (int64_t s = 0; s < g.wm; ++s) {
-            const float2 v = recs[cl * g.wm + s];
-            sa += v.x;
-            sb += v.y;
-          }
-          chs[cl] = make_float2(sa, sb);
-        } else {
-          Moments m = {0.f, 0.f, 0.f};
-          for (int64_t s = 0; s < g.wm; ++s) {
-            const float2 v = recs[cl * g.wm + s];
-            merge_into(m, piece_count(g, s), v.x, v.y);
-          }
-          chs[cl] = make_float2(m.mean, m.m2);
+    // one warp per group of the unit, over the group's records (lane l takes
+    // records l, l + 32, ... in piece-major order), then a fixed xor tree.  Forward: mean =
+    // sum(n_i*mean_i) / M and M2 = sum(M2_i + n_i*(mean_i - mean)^2), the
+    // parallel-axis identity over all of a group's records at once; backward:
+    // c1 = sum gamma_c*S1 and c2 = sum gamma_c*S2.
+    const int64_t gbase = LAYOUT == kNHWC ? (int64_t)pc.n * g.G + pc.cbase / Cg : pc.u;
+    for (int q = warp; q < ngrp; q += nwarps) {
+      const int nrow = LAYOUT == kNHWC ? Cg : 1;  // records of a piece in the group
+      const float2* Rq = R + (LAYOUT == kNHWC ? q * Cg : 0);
+      const int rstride = LAYOUT == kNHWC ? nch : 1;
+      // record f of the group (f < P * nrow): piece f / nrow, channel f % nrow
+      const int nrec = P * nrow;
+      if (!BWD) {
+        float s = 0.f;
+        for (int f = lane; f < nrec; f += 32) {
+          const int t = f / nrow, i = f - t * nrow;
+          s = fmaf(cnt[t], Rq[t * rstride + i].x, s);
         }
-      }
-      __syncthreads();
-      if (tid == 0) {
-        const int64_t c0 = pc.gi * g.Cg;
-        if (BWD) {
-          float c1 = 0.f, c2 = 0.f;
-          for (int64_t cl = 0; cl < g.Cg; ++cl) {
-            const float2 t2 = channel_terms(p.gamma ? __ldg(p.gamma + c0 + cl) : 1.0f, chs[cl]);
-            c1 += t2.x;
-            c2 += t2.y;
-          }
-          grp[0] = coef_from(c1, c2, g, __ldg(p.rstd + pc.u));
-        } else {
-          grp[0] = group_moments(chs, g, p.eps);
+        const float mean = warp_allsum(s) / Mg;
+        float m2 = 0.f;
+        for (int f = lane; f < nrec; f += 32) {
+          const int t = f / nrow, i = f - t * nrow;
+          const float2 v = Rq[t * rstride + i];
+          const float d = v.x - mean;
+          m2 += fmaf(cnt[t] * d, d, v.y);
         }
-      }
-    } else {
-      for (int64_t c = tid; c < g.Cb; c += nt) {
-        if (BWD) {
-          float sa = 0.f, sb = 0.f;
-          for (int64_t t = 0; t < P; ++t) {
-            const float2 v = recs[t * g.Cb + c];
-            sa += v.x;
-            sb += v.y;
-          }
-          chs[c] = make_float2(sa, sb);
-        } else {
-          Moments m = {0.f, 0.f, 0.f};
-          for (int64_t t = 0; t < P; ++t) {
-            const float2 v = recs[t * g.Cb + c];
-            merge_into(m, piece_count(g, t), v.x, v.y);
-          }
-          chs[c] = make_float2(m.mean, m.m2);
-        }
-      }
-      __syncthreads();
-      const int64_t gb = g.Cb / g.Cg, g0 = pc.n * g.G + pc.cbase / g.Cg;
-      for (int64_t q = tid; q < gb; q += nt) {
-        if (BWD) {
-          float c1 = 0.f, c2 = 0.f;
-          for (int64_t cl = 0; cl < g.Cg; ++cl) {
-            const int64_t c = pc.cbase + q * g.Cg + cl;
-            const float2 t2 = channel_terms(p.gamma ? __ldg(p.gamma + c) : 1.0f, chs[q * g.Cg + cl]);
-            c1 += t2.x;
-            c2 += t2.y;
-          }
-          grp[q] = coef_from(c1, c2, g, __ldg(p.rstd + g0 + q));
-        } else {
-          grp[q] = group_moments(chs + q * g.Cg, g, p.eps);
-        }
-      }
-    }
-    __syncthreads();
-
-    // ---- the unit's outputs that the first piece writes: mean / rstd, or
-    // the per-channel sums for dgamma / dbeta
-    if (pc.t == 0) {
-      if (LAYOUT == kNCHW) {
-        if (BWD) {
-          for (int64_t cl = tid; cl < g.Cg; cl += nt) p.chst[pc.n * g.C + pc.gi * g.Cg + cl] = chs[cl];
-        } else if (tid == 0) {
-          p.mean[pc.u] = grp[0].x;
-          p.rstd[pc.u] = grp[0].y;
-        }
+        m2 = warp_allsum(m2);
+        if (lane == 0) grp[q] = make_float2(mean, 1.0f / sqrtf(m2 / Mg + p.eps));
       } else {
-        if (BWD) {
-          for (int64_t c = tid; c < g.Cb; c += nt) p.chst[pc.n * g.C + pc.cbase + c] = chs[c];
-        } else {
-          const int64_t g0 = pc.n * g.G + pc.cbase / g.Cg;
-          for (int64_t q = tid; q < g.Cb / g.Cg; q += nt) {
-            p.mean[g0 + q] = grp[q].x;
-            p.rstd[g0 + q] = grp[q].y;
-          }
+        float c1 = 0.f, c2 = 0.f;
+        for (int f = lane; f < nrec; f += 32) {
+          const int t = f / nrow, i = f - t * nrow;
+          const float gm = LAYOUT == kNHWC ? cs[q * Cg + i] : cs[plane_of[t]];
+          const float2 tm = channel_terms(gm, Rq[t * rstride + i]);
+          c1 += tm.x;
+          c2 += tm.y;
         }
+        c1 = warp_allsum(c1);
+        c2 = warp_allsum(c2);
+        const float r = LAYOUT == kNHWC ? cs[nch + ngrp + q] : cs[Cg + 1];
+        if (lane == 0) grp[q] = coef_from(c1, c2, g, r);
       }
     }
+    // the unit's first piece also writes its per-channel sums (backward, for
+    // dgamma / dbeta) -- channel c's pieces in piece order
+    if (BWD && pc.t == 0 && (p.dgamma || p.dbeta)) {
+      const int nchan = LAYOUT == kNHWC ? nch : Cg;
+      const int64_t c0 = LAYOUT == kNHWC ? pc.cbase : (int64_t)pc.gi * Cg;
+      for (int c = tid; c < nchan; c += nt) {
+        float sa = 0.f, sb = 0.f;
+        const int cnt_c = LAYOUT == kNHWC ? P : (int)g.wm;
+        for (int t = 0; t < cnt_c; ++t) {
+          const float2 v = LAYOUT == kNHWC ? R[t * nch + c] : R[c * (int)g.wm + t];
+          sa += v.x;
+          sb += v.y;
+        }
+        p.chst[(int64_t)pc.n * g.C + c0 + c] = make_float2(sa, sb);
+      }
+    }
+    __syncthreads();  // the groups' values
+    if (!BWD && pc.t == 0)
+      for (int q = tid; q < ngrp; q += nt) {
+        p.mean[gbase + q] = grp[q].x;
+        p.rstd[gbase + q] = grp[q].y;
+      }
 
-    // ---- output of the piece, from shared memory
+    // ---- the piece's output, from shared memory
     if (LAYOUT == kNCHW) {
       float ca, cb, cm, cd;
+      const float gm = cs[pc.c - pc.gi * Cg];
       if (BWD) {
-        const float r = __ldg(p.rstd + pc.u);
-        ca = r * (p.gamma ? __ldg(p.gamma + pc.c) : 1.0f);
-        cm = __ldg(p.mean + pc.u);
+        ca = cs[Cg + 1] * gm;
+        cm = cs[Cg];
         cb = grp[0].x;
         cd = grp[0].y;
       } else {
         cm = grp[0].x;
-        ca = grp[0].y * (p.gamma ? __ldg(p.gamma + pc.c) : 1.0f);
-        cb = p.beta ? __ldg(p.beta + pc.c) : 0.f;
+        ca = grp[0].y * gm;
+        cb = cs[Cg];
         cd = 0.f;
       }
-      const int64_t nv = pc.len / VW;
+      const int nv = pc.len / VW;
       T* o = out + pc.e0;
-      for (int64_t v = tid; v < nv; v += nt) {
+#pragma unroll 4
+      for (int v = tid; v < nv; v += nt) {
         float xv[VW];
-        Access<T, VW>::unpack(lds16(slot + v * 16), xv);
+        Access<T, VW>::unpack(lds16(slot + (size_t)v * 16), xv);
         if (BWD) {
           float dv[VW];
-          Access<T, VW>::unpack(lds16(slot + g.ten_stride + v * 16), dv);
+          Access<T, VW>::unpack(lds16(slot + g.ten_stride + (size_t)v * 16), dv);
 #pragma unroll
           for (int e = 0; e < VW; ++e) xv[e] = fmaf(ca, dv[e], fmaf(cb, xv[e] - cm, cd));
         } else {
 #pragma unroll
           for (int e = 0; e < VW; ++e) xv[e] = fmaf(xv[e] - cm, ca, cb);
         }
-        Access<T, VW>::store(o + v * VW, xv, pol_out);
+        Access<T, VW>::store(o + (int64_t)v * VW, xv, pol_out);
       }
     } else if (lane_ok) {
       float ca[VW], cb[VW], cm[VW], cd[VW];
 #pragma unroll
       for (int e = 0; e < VW; ++e) {
-        const int64_t cl = (int64_t)j * VW + e;
-        const int64_t c = pc.cbase + cl;
-        const int64_t q = cl / g.Cg;
-        const float gm = p.gamma ? __ldg(p.gamma + c) : 1.0f;
+        const int cl = j * VW + e;
+        const float gm = cs[cl];
+        const float2 gv = grp[qe[e]];
         if (BWD) {
-          const int64_t gidx = pc.n * g.G + c / g.Cg;
-          ca[e] = __ldg(p.rstd + gidx) * gm;
-          cm[e] = __ldg(p.mean + gidx);
-          cb[e] = grp[q].x;
-          cd[e] = grp[q].y;
+          ca[e] = cs[nch + ngrp + qe[e]] * gm;
+          cm[e] = cs[nch + qe[e]];
+          cb[e] = gv.x;
+          cd[e] = gv.y;
         } else {
-          cm[e] = grp[q].x;
-          ca[e] = grp[q].y * gm;
-          cb[e] = p.beta ? __ldg(p.beta + c) : 0.f;
+          cm[e] = gv.x;
+          ca[e] = gv.y * gm;
+          cb[e] = cs[nch + cl];
           cd[e] = 0.f;
         }
       }
-      T* o = out + (pc.n * g.HW + pc.r0) * g.C + pc.cbase + (int64_t)j * VW;
-      for (int64_t r = rl; r < pc.len; r += rpi) {
+      T* o = out + pc.row0 * g.C + pc.cbase + j * VW;
+      const char* col = slot + j * 16;
+#pragma unroll 2
+      for (int r = rl; r < pc.len; r += rpi) {
         float xv[VW];
-        Access<T, VW>::unpack(lds16(slot + r * rowb + j * 16), xv);
+        Access<T, VW>::unpack(lds16(col + (size_t)r * rowb), xv);
         if (BWD) {
           float dv[VW];
-          Access<T, VW>::unpack(lds16(slot + g.ten_stride + r * rowb + j * 16), dv);
+          Access<T, VW>::unpack(lds16(col + g.ten_stride + (size_t)r * rowb), dv);
 #pragma unroll
           for (int e = 0; e < VW; ++e) xv[e] = fmaf(ca[e], dv[e], fmaf(cb[e], xv[e] - cm[e], cd[e]));
         } else {
 #pragma unroll
           for (int e = 0; e < VW; ++e) xv[e] = fmaf(xv[e] - cm[e], ca[e], cb[e]);
         }
-        Access<T, VW>::store(o + r * g.C, xv, pol_out);
+        Access<T, VW>::store(o + (int64_t)r * g.C, xv, pol_out);
       }
     }
+    __syncthreads();  // the slot's reads are done; the scratch is free
+    return true;
+  };
 
-    // ---- backward: the column's dgamma / dbeta once its N units are done
-    if (BWD && pc.t == 0 && (p.dgamma || p.dbeta)) {
-      __syncthreads();  // this unit's chst stores, before thread 0's arrival
-      const int64_t col = LAYOUT == kNCHW ? pc.gi : pc.cb;
-      if (tid == 0) s_last = publish_and_arrive(p.cnt1 + col, (unsigned)g.N);
-      __syncthreads();
-      if (s_last) {
-        // channels [ca, cb) of the column, samples in fixed slices
-        const int64_t ca = LAYOUT == kNCHW ? pc.gi * g.Cg : pc.cbase;
-        const int64_t cw = LAYOUT == kNCHW ? g.Cg : g.Cb;
-        float* sm = red;
-        const SliceLayout L = slice_layout(cw, g.N);
-        for (int64_t c0 = 0; c0 < cw; c0 += L.cpb) {
-          const int64_t c = ca + c0 + L.cl;
-          float db = 0.f, dg = 0.f;
-          if (L.sl < L.nsl && c0 + L.cl < cw) {
-            const int64_t gi = c / g.Cg;
-            for (int64_t n = L.sl; n < g.N; n += 8 * L.nsl) {
-              float2 v[8];
-              float r[8];
-#pragma unroll
-              for (int u = 0; u < 8; ++u) {
-                const int64_t jn = n + u * L.nsl;
-                v[u] = jn < g.N ? __ldcg(p.chst + jn * g.C + c) : make_float2(0.f, 0.f);
-                r[u] = jn < g.N ? __ldg(p.rstd + jn * g.G + gi) : 0.f;
-              }
-#pragma unroll
-              for (int u = 0; u < 8; ++u) {
-                db += v[u].x;
-                dg = fmaf(r[u], v[u].y, dg);
-              }
-            }
-          }
-          if (L.sl < L.nsl) {
-            sm[2 * (L.sl * L.cpb + L.cl)] = db;
-            sm[2 * (L.sl * L.cpb + L.cl) + 1] = dg;
-          }
-          __syncthreads();
-          if (L.sl == 0 && c0 + L.cl < cw) {
-            for (int s = 1; s < L.nsl; ++s) {
-              db += sm[2 * (s * L.cpb + L.cl)];
-              dg += sm[2 * (s * L.cpb + L.cl) + 1];
-            }
-            if (p.dbeta) p.dbeta[c] = db;
-            if (p.dgamma) p.dgamma[c] = dg;
-          }
-          __syncthreads();
-        }
-      }
+  // ---- the pipeline.  With three or more slots, stage A runs one piece
+  // ahead of stage B: by the time a CTA needs a unit's records, every CTA
+  // has had a whole step to publish them.  After stage B of piece k its slot
+  // takes the copy of piece k + S.
+  const int ahead = S >= 3 ? 1 : 0;
+  int ka = 0;  // pieces through stage A
+  bool ok = true;
+  for (; ok && ka <= ahead && ka < K; ++ka) ok = stage_a(ka);
+  if (!ok) --ka;  // that piece's copy may still be in flight
+  for (int k = 0; ok && k < K; ++k) {
+    if (!stage_b(k)) {
+      ok = false;
+      break;
     }
-    __syncthreads();  // the slot and the shared scratch are free again
+    if (tid == 0 && issued < K) {
+      fence_proxy_async_smem();  // the slot's generic reads precede the new copy
+      issue(issued);
+      ++issued;
+    }
+    if (ka < K) {
+      if (!stage_a(ka)) {
+        ok = false;
+        break;
+      }
+      ++ka;
+    }
   }
 
-  // ---- after a wait ran out: this CTA's copies still in flight land before it exits
-  if (!ok && tid == 0) {
-    for (int64_t i = k; i < issued; ++i) wait_bar_t0(full + (i % S), (uint32_t)((i / S) & 1), p.err);
+  // ---- after a wait ran out: this CTA's copies still in flight land first
+  if (!ok && tid == 0)
+    for (int i = ka; i < issued; ++i) wait_bar_t0(full + (i % S), (uint32_t)((i / S) & 1), p.err);
+  cp_async_wait_all();  // no asynchronous copy into shared memory outlives the CTA
+
+  // ---- backward: dgamma / dbeta once every unit's per-channel sums are in
+  // the workspace (a grid barrier, which every CTA reaches), spread over the
+  // CTAs by channel:  dbeta_c = sum_n S1[n, c],  dgamma_c = sum_n rstd[n, g(c)] *
+  // S2[n, c]; thread t adds samples t, t + nt, ... in order, then the warps
+  // meet in a fixed tree and in warp order.
+  if (BWD && (p.dgamma || p.dbeta)) {
+    cooperative_groups::this_grid().sync();
+    if (!aborted(p.err)) {
+      float* wsum = red;
+      for (int64_t c = b; c < g.C; c += NC) {
+        const int64_t gi = c / g.Cg;
+        float db = 0.f, dg = 0.f;
+        for (int64_t n = tid; n < g.N; n += nt) {
+          const float2 v = __ldcg(p.chst + n * g.C + c);
+          db += v.x;
+          dg = fmaf(__ldg(p.rstd + n * g.G + gi), v.y, dg);
+        }
+        db = warp_sum_lane0(db);
+        dg = warp_sum_lane0(dg);
+        if (lane == 0) {
+          wsum[2 * warp] = db;
+          wsum[2 * warp + 1] = dg;
+        }
+        __syncthreads();
+        if (tid == 0) {
+          float tb = 0.f, tg = 0.f;
+          for (int w = 0; w < nwarps; ++w) {
+            tb += wsum[2 * w];
+            tg += wsum[2 * w + 1];
+          }
+          if (p.dbeta) p.dbeta[c] = tb;
+          if (p.dgamma) p.dgamma[c] = tg;
+        }
+        __syncthreads();
+      }
+    }
   }
 }
 

@@ -12,7 +12,8 @@ count and value distributions:
 
 Each call is one forward followed by one backward on the same stream, so the
 kernels launch in the order fwd-first, fwd-second, bwd-first, bwd-second
-(one kernel per op in the resident and pipelined regimes).
+(one kernel per op in the resident, pipelined and wave regimes); every
+regime but the wave regime first launches the small workspace-clear kernel.
 """
 from __future__ import annotations
 
@@ -34,7 +35,7 @@ def main(argv=None) -> int:
     ap.add_argument("--H", type=int)
     ap.add_argument("--W", type=int)
     ap.add_argument("--calls", type=int, default=2)
-    ap.add_argument("--regime", choices=["auto", "two_kernel", "resident", "pipelined"],
+    ap.add_argument("--regime", choices=["auto", "two_kernel", "resident", "pipelined", "wave"],
                     default="auto")
     a = ap.parse_args(argv)
     if a.row_workload:
@@ -46,7 +47,8 @@ def main(argv=None) -> int:
     if over:
         w = w.scaled(**over)
     gn.set_regime({"auto": gn.REGIME_AUTO, "two_kernel": gn.REGIME_TWO_KERNEL,
-                   "resident": gn.REGIME_RESIDENT, "pipelined": gn.REGIME_PIPELINED}[a.regime])
+                   "resident": gn.REGIME_RESIDENT, "pipelined": gn.REGIME_PIPELINED,
+                   "wave": gn.REGIME_WAVE}[a.regime])
     inp = synth.make_inputs(w, "cuda", seed=0)
     x, dy, gm, bt = inp["x"], inp["dy"], inp["gamma"], inp["beta"]
     y, dx = torch.empty_like(x), torch.empty_like(x)

@@ -29,6 +29,15 @@ def broadcast_params(*tensors, src: int = 0, group=None) -> None:
         dist.broadcast(t, src, group=group)
 
 
+def rank_order_sum(parts):
+    """parts[0] + parts[1] + ... in that order (fp32): the fixed order that
+    makes every rank's totals bit-identical."""
+    tot = parts[0].clone()
+    for t in parts[1:]:
+        tot += t
+    return tot
+
+
 class ParamGradSum:
     """Sums dgamma and dbeta over the ranks of a process group, in rank order.
 
@@ -49,8 +58,6 @@ class ParamGradSum:
             return
         mine = torch.cat([dgamma.reshape(-1), dbeta.reshape(-1)])
         dist.all_gather(self.parts, mine, group=self.group)
-        tot = self.parts[0].clone()
-        for r in range(1, self.world):
-            tot += self.parts[r]
+        tot = rank_order_sum(self.parts)
         dgamma.copy_(tot[:self.C].view_as(dgamma))
         dbeta.copy_(tot[self.C:].view_as(dbeta))

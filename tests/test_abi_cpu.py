@@ -152,8 +152,12 @@ def test_regime_choice(gn):
     finally:
         gn.set_regime(gn.REGIME_AUTO)
     # the wave kernel clears its own counters: one launch per op
-    d = gn.plan_info(1, 8, 320, 4096, 32, "nhwc", "bf16")
-    assert d.regime == 3 and d.launches == 1
+    gn.set_regime(gn.REGIME_WAVE)
+    try:
+        d = gn.plan_info(1, 8, 320, 4096, 32, "nhwc", "bf16")
+        assert d.regime == 3 and d.launches == 1
+    finally:
+        gn.set_regime(gn.REGIME_AUTO)
     with pytest.raises(gn.GnError):
         gn.set_regime(7)
 
@@ -213,18 +217,20 @@ def test_f64_storage_plans(gn):
 
 
 def test_automatic_choice(gn):
-    """The automatic choice takes the wave regime wherever its plan fits (16-byte
-    aligned fp32/fp16/bf16 data whose units fit in the co-resident CTAs'
-    shared memory), else the two-kernel path; the resident regime runs when
-    asked for."""
-    assert gn.plan_info(0, 2, 32, 256, 8, "nchw", "f32").regime == 3
-    assert gn.plan_info(1, 112, 64, 512 * 512, 8, "nchw", "f32").regime == 3   # 16 MiB units
-    assert gn.plan_info(0, 8, 320, 4096, 32, "nhwc", "bf16").regime == 3
-    assert gn.plan_info(1, 32, 512, 1024, 32, "nhwc", "bf16").regime == 3
-    # 32 MiB units (one group of the one-sample image) do not fit: two kernels
+    """The automatic choice: the wave regime for the NCHW backward with units
+    of at least 4 MiB; the resident regime for channels-last forwards and
+    small NCHW units when one wave of clusters covers every unit (or the
+    input is tiny); the two-kernel path otherwise."""
+    assert gn.plan_info(1, 112, 64, 512 * 512, 8, "nchw", "f32").regime == 3   # 8 MiB units
+    assert gn.plan_info(0, 112, 64, 512 * 512, 8, "nchw", "f32").regime == 0
+    assert gn.plan_info(0, 2, 32, 256, 8, "nchw", "f32").regime == 1        # 64 KB
+    assert gn.plan_info(0, 512, 32, 256, 8, "nchw", "f32").regime == 0      # 4096 units
+    assert gn.plan_info(0, 8, 320, 4096, 32, "nhwc", "bf16").regime == 1    # 32 clusters
+    assert gn.plan_info(0, 64, 320, 4096, 32, "nhwc", "bf16").regime == 0   # 256 clusters
+    assert gn.plan_info(1, 8, 320, 4096, 32, "nhwc", "bf16").regime == 0
     assert gn.plan_info(0, 1, 128, 2048 * 1024, 16, "nhwc", "f16").regime == 0
     assert gn.plan_info(0, 2, 64, 2303, 8, "nchw", "f32").regime == 0       # scalar path
-    assert gn.plan_info(0, 2, 16, 4096, 4, "nchw", "f64").regime == 0       # f64 storage
+    assert gn.plan_info(1, 2, 16, 4096 * 256, 4, "nchw", "f64").regime == 0  # f64 storage
     gn.set_regime(gn.REGIME_RESIDENT)  # asked for: wherever the problem fits
     try:
         assert gn.plan_info(0, 512, 32, 256, 8, "nchw", "f32").regime == 1
@@ -236,15 +242,19 @@ def test_wave_plans(gn):
     """Wave plans: a unit's pieces all fit on co-resident CTAs (P <= CTAs),
     the pieces of the benchmarked units divide the CTA count (no unit
     straddles two steps), and pieces hold whole 16-byte vectors."""
-    for w in synth.WORKLOADS[2:]:
-        for op in (0, 1):
-            d = gn.plan_info(op, w.N, w.C, w.HW, w.G, w.layout, w.dtype)
-            assert d.regime == 3 and d.launches == 1
-            assert 1 <= d.pieces_per_unit <= d.ctas
-            assert d.ctas % d.pieces_per_unit == 0
-            assert d.smem_bytes <= 227 * 1024
-            if w.layout == "nchw":
-                assert d.piece_elems * (4 if w.dtype == "f32" else 2) % 16 == 0
+    gn.set_regime(gn.REGIME_WAVE)
+    try:
+        plans = [(w, gn.plan_info(op, w.N, w.C, w.HW, w.G, w.layout, w.dtype))
+                 for w in synth.WORKLOADS[2:] for op in (0, 1)]
+    finally:
+        gn.set_regime(gn.REGIME_AUTO)
+    for w, d in plans:
+        assert d.regime == 3 and d.launches == 1
+        assert 1 <= d.pieces_per_unit <= d.ctas
+        assert d.ctas % d.pieces_per_unit == 0
+        assert d.smem_bytes <= 227 * 1024
+        if w.layout == "nchw":
+            assert d.piece_elems * (4 if w.dtype == "f32" else 2) % 16 == 0
     gn.set_regime(gn.REGIME_WAVE)
     try:
         assert gn.plan_info(0, 1, 128, 2048 * 1024, 16, "nhwc", "f16").regime == 0  # too large
