@@ -229,14 +229,16 @@ class OracleSample:
 
 def oracle_sample_for(w, target_s: float, threads: int = 1):
     """An OracleSample of w whose run on `threads` threads takes about
-    target_s seconds here (sized from a small calibration run)."""
+    target_s seconds here (sized from a small calibration run on as many
+    threads)."""
     if w.N > 1:
-        probe = OracleSample(w, ns=1)
-        per = probe.run(1) / max(1, min(threads, len(probe.units)))
+        ns = min(w.N, max(1, threads // max(1, w.G)))
+        probe = OracleSample(w, ns=ns)
+        per = probe.run(threads) / ns
         ns = int(max(1, min(w.N, round(target_s / max(per, 1e-6)))))
         return OracleSample(w, ns=ns)
-    probe = OracleSample(w, h=2)
-    per = probe.run(1) / 2 / max(1, min(threads, len(probe.units)))
+    probe = OracleSample(w, h=4)
+    per = probe.run(threads) / 4
     h = int(max(1, min(w.H, round(target_s / max(per, 1e-6)))))
     return OracleSample(w, h=h)
 
@@ -266,7 +268,7 @@ def run_reference(args, rank, world):
     nt = host_cores()
     # the whole run stays within about two minutes: each step a bounded
     # sample of the workload, on all host cores
-    smp = oracle_sample_for(w, min(2.0, 120.0 / (args.steps + args.warmup)), nt)
+    smp = oracle_sample_for(w, min(0.5, 60.0 / (args.steps + args.warmup)), nt)
     for _ in range(args.warmup):
         smp.run(nt)
     times = [smp.run(nt) for _ in range(args.steps)]
