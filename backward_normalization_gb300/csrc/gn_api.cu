@@ -70,10 +70,10 @@ int cuda_fail(cudaError_t e) {
 
 // Plan + workspace check shared by both ops.
 int prepare(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout, int dtype,
-            bool aligned, void* workspace, size_t workspace_bytes, gn::KParams* p) {
+            bool aligned, bool dense, void* workspace, size_t workspace_bytes, gn::KParams* p) {
   std::memset(p, 0, sizeof(*p));
   p->stall_unit = -1;
-  p->g = gn::make_geom(op, N, C, HW, G, layout, dtype, aligned);
+  p->g = gn::make_geom(op, N, C, HW, G, layout, dtype, aligned, dense);
   if (p->g.regime == gn::kRegimeGeneric && (p->g.items <= 0 || p->g.items > 0x7fffffffLL))
     return GN_ERR_UNSUPPORTED;
   const gn::WsLayout w = gn::ws_layout(op, p->g);
@@ -140,17 +140,175 @@ cudaError_t launch(const gn::KParams& p, cudaStream_t s, bool bwd) {
 
 size_t ws_size_any_alignment(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout,
                              int dtype) {
-  // Large enough for either op and either alignment, so that one workspace can
-  // serve a forward and the following backward.
+  // Large enough for either op, either alignment and dense or strided views,
+  // so that one workspace serves a forward and the following backward.
   (void)op;
   size_t best = 0;
   for (int o = 0; o < 2; ++o)
-    for (int a = 0; a < 2; ++a) {
-      const gn::Geom g = gn::make_geom(o, N, C, HW, G, layout, dtype, a != 0);
-      const size_t t = gn::ws_layout(o, g).total;
-      if (t > best) best = t;
-    }
+    for (int a = 0; a < 2; ++a)
+      for (int d = 0; d < 2; ++d) {
+        const gn::Geom g = gn::make_geom(o, N, C, HW, G, layout, dtype, a != 0, d != 0);
+        const size_t t = gn::ws_layout(o, g).total;
+        if (t > best) best = t;
+      }
   return best;
+}
+
+// A view's element strides: per sample (sn) and per channel plane (NCHW) or
+// spatial row (NHWC) (sr); within a plane (NCHW) or a row (NHWC) elements
+// are contiguous.
+struct View {
+  int64_t sn, sr;
+};
+
+View dense_view(int64_t N, int64_t C, int64_t HW, int layout) {
+  (void)N;
+  return layout == GN_LAYOUT_NCHW ? View{C * HW, HW} : View{HW * C, C};
+}
+
+bool is_dense(const View& v, int64_t N, int64_t C, int64_t HW, int layout) {
+  const View d = dense_view(N, C, HW, layout);
+  return (v.sn == d.sn || N == 1) && (v.sr == d.sr || (layout == GN_LAYOUT_NCHW ? C : HW) == 1);
+}
+
+// The strides keep distinct elements apart: planes (rows) are contiguous runs
+// of HW (C) elements, laid out sample-major or plane(row)-major without
+// overlap.  An extent of 1 leaves its stride free.
+bool view_ok(const View& v, int64_t N, int64_t C, int64_t HW, int layout) {
+  const int64_t run = layout == GN_LAYOUT_NCHW ? HW : C;    // contiguous elements
+  const int64_t cnt = layout == GN_LAYOUT_NCHW ? C : HW;    // runs per sample
+  if (v.sn < 0 || v.sr < 0) return false;
+  const int64_t sr = cnt > 1 ? v.sr : run, sn = N > 1 ? v.sn : run * cnt;
+  if (sr < run || sn < run) return false;
+  return sn >= cnt * sr || sr >= N * sn;
+}
+
+// Bytes from a view's first element to one past its last.
+size_t view_span(const View& v, int64_t N, int64_t C, int64_t HW, int layout, int esz) {
+  const int64_t run = layout == GN_LAYOUT_NCHW ? HW : C;
+  const int64_t cnt = layout == GN_LAYOUT_NCHW ? C : HW;
+  return (size_t)((N - 1) * v.sn + (cnt - 1) * v.sr + run) * (size_t)esz;
+}
+
+// The vector path needs the view's planes (rows) to start on 16-byte boundaries.
+bool view_aligned(const void* base, const View& v, int64_t N, int64_t C, int64_t HW, int layout,
+                  int esz) {
+  if (!aligned16(base)) return false;
+  const int64_t cnt = layout == GN_LAYOUT_NCHW ? C : HW;
+  if (N > 1 && (v.sn * esz) % 16 != 0) return false;
+  if (cnt > 1 && (v.sr * esz) % 16 != 0) return false;
+  return true;
+}
+
+void set_views(gn::KParams* p, const View& xv, const View& dv, const View& ov) {
+  p->xs_n = xv.sn;
+  p->xs_r = xv.sr;
+  p->ds_n = dv.sn;
+  p->ds_r = dv.sr;
+  p->os_n = ov.sn;
+  p->os_r = ov.sr;
+}
+
+int fwd_impl(const void* x, View xv, int64_t N, int64_t C, int64_t HW, int64_t G, int layout,
+             int dtype, const float* gamma, const float* beta, float eps, void* y, View yv,
+             float* mean, float* rstd, void* workspace, size_t workspace_bytes, void* stream) {
+  int rc = check_problem(N, C, HW, G, layout, dtype);
+  if (rc != GN_OK) return rc;
+  if (N == 0 || C == 0 || HW == 0) return GN_OK;
+  if (!x || !y || !mean || !rstd) return GN_ERR_INVALID;
+  if (!(eps >= 0.0f)) return GN_ERR_INVALID;  // rejects NaN and negative eps
+  if (!view_ok(xv, N, C, HW, layout) || !view_ok(yv, N, C, HW, layout)) return GN_ERR_INVALID;
+  const int esz = elem_size(dtype);
+  const size_t xb = view_span(xv, N, C, HW, layout, esz), yb = view_span(yv, N, C, HW, layout, esz);
+  const size_t sbytes = sizeof(float) * (size_t)(N * G);
+  const bool same = y == x && xv.sn == yv.sn && xv.sr == yv.sr;  // in place
+  if (!same && overlap(y, yb, x, xb)) return GN_ERR_INVALID;
+  if (overlap(mean, sbytes, x, xb) || overlap(mean, sbytes, y, yb) ||
+      overlap(rstd, sbytes, x, xb) || overlap(rstd, sbytes, y, yb) ||
+      overlap(mean, sbytes, rstd, sbytes))
+    return GN_ERR_INVALID;
+  const bool dense = is_dense(xv, N, C, HW, layout) && is_dense(yv, N, C, HW, layout);
+  const bool aligned = view_aligned(x, xv, N, C, HW, layout, esz) &&
+                       view_aligned(y, yv, N, C, HW, layout, esz);
+  gn::KParams p;
+  rc = prepare(GN_OP_FWD, N, C, HW, G, layout, dtype, aligned, dense, workspace, workspace_bytes,
+               &p);
+  if (rc != GN_OK) return rc;
+  set_views(&p, xv, xv, yv);
+  p.x = x;
+  p.out = y;
+  p.gamma = gamma;
+  p.beta = beta;
+  p.mean = mean;
+  p.rstd = rstd;
+  p.eps = eps;
+  if (fault_mode() == GN_FAULT_LAUNCH) return cuda_fail(cudaErrorLaunchFailure);
+  p.stall_unit = take_stall();
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = launch(p, s, false);
+  return e == cudaSuccess ? GN_OK : cuda_fail(e);
+}
+
+int bwd_impl(const void* dy, View dyv, const void* x, View xv, const float* mean,
+             const float* rstd, const float* gamma, int64_t N, int64_t C, int64_t HW, int64_t G,
+             int layout, int dtype, void* dx, View dxv, float* dgamma, float* dbeta,
+             void* workspace, size_t workspace_bytes, void* stream) {
+  int rc = check_problem(N, C, HW, G, layout, dtype);
+  if (rc != GN_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (C == 0) return GN_OK;
+  if (N == 0 || HW == 0) {
+    // empty sums: the parameter gradients are zero
+    if ((dgamma || dbeta) && fault_mode() == GN_FAULT_LAUNCH)
+      return cuda_fail(cudaErrorLaunchFailure);
+    if (dgamma) {
+      const cudaError_t e = cudaMemsetAsync(dgamma, 0, sizeof(float) * (size_t)C, s);
+      if (e != cudaSuccess) return cuda_fail(e);
+    }
+    if (dbeta) {
+      const cudaError_t e = cudaMemsetAsync(dbeta, 0, sizeof(float) * (size_t)C, s);
+      if (e != cudaSuccess) return cuda_fail(e);
+    }
+    return GN_OK;
+  }
+  if (!dy || !x || !mean || !rstd || !dx) return GN_ERR_INVALID;
+  if (!view_ok(dyv, N, C, HW, layout) || !view_ok(xv, N, C, HW, layout) ||
+      !view_ok(dxv, N, C, HW, layout))
+    return GN_ERR_INVALID;
+  const int esz = elem_size(dtype);
+  const size_t xb = view_span(xv, N, C, HW, layout, esz);
+  const size_t db = view_span(dyv, N, C, HW, layout, esz);
+  const size_t ob = view_span(dxv, N, C, HW, layout, esz);
+  const size_t cbytes = sizeof(float) * (size_t)C;
+  const bool on_dy = dx == dy && dxv.sn == dyv.sn && dxv.sr == dyv.sr;
+  const bool on_x = dx == x && dxv.sn == xv.sn && dxv.sr == xv.sr;
+  if (!on_dy && !on_x && (overlap(dx, ob, dy, db) || overlap(dx, ob, x, xb)))
+    return GN_ERR_INVALID;
+  if (overlap(dgamma, cbytes, dx, ob) || overlap(dbeta, cbytes, dx, ob) ||
+      overlap(dgamma, cbytes, dbeta, cbytes))
+    return GN_ERR_INVALID;
+  const bool dense = is_dense(dyv, N, C, HW, layout) && is_dense(xv, N, C, HW, layout) &&
+                     is_dense(dxv, N, C, HW, layout);
+  const bool aligned = view_aligned(x, xv, N, C, HW, layout, esz) &&
+                       view_aligned(dy, dyv, N, C, HW, layout, esz) &&
+                       view_aligned(dx, dxv, N, C, HW, layout, esz);
+  gn::KParams p;
+  rc = prepare(GN_OP_BWD, N, C, HW, G, layout, dtype, aligned, dense, workspace, workspace_bytes,
+               &p);
+  if (rc != GN_OK) return rc;
+  set_views(&p, xv, dyv, dxv);
+  p.x = x;
+  p.dy = dy;
+  p.out = dx;
+  p.gamma = gamma;
+  p.mean = const_cast<float*>(mean);
+  p.rstd = const_cast<float*>(rstd);
+  p.dgamma = dgamma;
+  p.dbeta = dbeta;
+  if (fault_mode() == GN_FAULT_LAUNCH) return cuda_fail(cudaErrorLaunchFailure);
+  p.stall_unit = take_stall();
+  const cudaError_t e = launch(p, s, true);
+  return e == cudaSuccess ? GN_OK : cuda_fail(e);
 }
 
 }  // namespace
@@ -173,82 +331,36 @@ size_t gn_workspace_size(int op, int64_t N, int64_t C, int64_t HW, int64_t G, in
 int gn_fwd(const void* x, int64_t N, int64_t C, int64_t HW, int64_t G, int layout, int dtype,
            const float* gamma, const float* beta, float eps, void* y, float* mean, float* rstd,
            void* workspace, size_t workspace_bytes, void* stream) {
-  int rc = check_problem(N, C, HW, G, layout, dtype);
-  if (rc != GN_OK) return rc;
-  if (N == 0 || C == 0 || HW == 0) return GN_OK;
-  if (!x || !y || !mean || !rstd) return GN_ERR_INVALID;
-  if (!(eps >= 0.0f)) return GN_ERR_INVALID;  // rejects NaN and negative eps
-  const size_t bytes = (size_t)(N * C * HW) * (size_t)elem_size(dtype);
-  const size_t sbytes = sizeof(float) * (size_t)(N * G);
-  if (y != x && overlap(y, bytes, x, bytes)) return GN_ERR_INVALID;
-  if (overlap(mean, sbytes, x, bytes) || overlap(mean, sbytes, y, bytes) ||
-      overlap(rstd, sbytes, x, bytes) || overlap(rstd, sbytes, y, bytes) ||
-      overlap(mean, sbytes, rstd, sbytes))
-    return GN_ERR_INVALID;
-  gn::KParams p;
-  rc = prepare(GN_OP_FWD, N, C, HW, G, layout, dtype, aligned16(x) && aligned16(y), workspace,
-               workspace_bytes, &p);
-  if (rc != GN_OK) return rc;
-  p.x = x;
-  p.out = y;
-  p.gamma = gamma;
-  p.beta = beta;
-  p.mean = mean;
-  p.rstd = rstd;
-  p.eps = eps;
-  if (fault_mode() == GN_FAULT_LAUNCH) return cuda_fail(cudaErrorLaunchFailure);
-  p.stall_unit = take_stall();
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const cudaError_t e = launch(p, s, false);
-  return e == cudaSuccess ? GN_OK : cuda_fail(e);
+  const View d = dense_view(N, C, HW, layout);
+  return fwd_impl(x, d, N, C, HW, G, layout, dtype, gamma, beta, eps, y, d, mean, rstd, workspace,
+                  workspace_bytes, stream);
+}
+
+int gn_fwd_ex(const void* x, int64_t x_sn, int64_t x_sr, int64_t N, int64_t C, int64_t HW,
+              int64_t G, int layout, int dtype, const float* gamma, const float* beta, float eps,
+              void* y, int64_t y_sn, int64_t y_sr, float* mean, float* rstd, void* workspace,
+              size_t workspace_bytes, void* stream) {
+  return fwd_impl(x, View{x_sn, x_sr}, N, C, HW, G, layout, dtype, gamma, beta, eps, y,
+                  View{y_sn, y_sr}, mean, rstd, workspace, workspace_bytes, stream);
 }
 
 int gn_bwd(const void* dy, const void* x, const float* mean, const float* rstd,
            const float* gamma, int64_t N, int64_t C, int64_t HW, int64_t G, int layout,
            int dtype, void* dx, float* dgamma, float* dbeta, void* workspace,
            size_t workspace_bytes, void* stream) {
-  int rc = check_problem(N, C, HW, G, layout, dtype);
-  if (rc != GN_OK) return rc;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (C == 0) return GN_OK;
-  if (N == 0 || HW == 0) {
-    // empty sums: the parameter gradients are zero
-    if ((dgamma || dbeta) && fault_mode() == GN_FAULT_LAUNCH)
-      return cuda_fail(cudaErrorLaunchFailure);
-    if (dgamma) {
-      const cudaError_t e = cudaMemsetAsync(dgamma, 0, sizeof(float) * (size_t)C, s);
-      if (e != cudaSuccess) return cuda_fail(e);
-    }
-    if (dbeta) {
-      const cudaError_t e = cudaMemsetAsync(dbeta, 0, sizeof(float) * (size_t)C, s);
-      if (e != cudaSuccess) return cuda_fail(e);
-    }
-    return GN_OK;
-  }
-  if (!dy || !x || !mean || !rstd || !dx) return GN_ERR_INVALID;
-  const size_t bytes = (size_t)(N * C * HW) * (size_t)elem_size(dtype);
-  const size_t cbytes = sizeof(float) * (size_t)C;
-  if (dx != dy && dx != x && (overlap(dx, bytes, dy, bytes) || overlap(dx, bytes, x, bytes)))
-    return GN_ERR_INVALID;
-  if (overlap(dgamma, cbytes, dx, bytes) || overlap(dbeta, cbytes, dx, bytes) ||
-      overlap(dgamma, cbytes, dbeta, cbytes))
-    return GN_ERR_INVALID;
-  gn::KParams p;
-  rc = prepare(GN_OP_BWD, N, C, HW, G, layout, dtype,
-               aligned16(x) && aligned16(dy) && aligned16(dx), workspace, workspace_bytes, &p);
-  if (rc != GN_OK) return rc;
-  p.x = x;
-  p.dy = dy;
-  p.out = dx;
-  p.gamma = gamma;
-  p.mean = const_cast<float*>(mean);
-  p.rstd = const_cast<float*>(rstd);
-  p.dgamma = dgamma;
-  p.dbeta = dbeta;
-  if (fault_mode() == GN_FAULT_LAUNCH) return cuda_fail(cudaErrorLaunchFailure);
-  p.stall_unit = take_stall();
-  const cudaError_t e = launch(p, s, true);
-  return e == cudaSuccess ? GN_OK : cuda_fail(e);
+  const View d = dense_view(N, C, HW, layout);
+  return bwd_impl(dy, d, x, d, mean, rstd, gamma, N, C, HW, G, layout, dtype, dx, d, dgamma,
+                  dbeta, workspace, workspace_bytes, stream);
+}
+
+int gn_bwd_ex(const void* dy, int64_t dy_sn, int64_t dy_sr, const void* x, int64_t x_sn,
+              int64_t x_sr, const float* mean, const float* rstd, const float* gamma, int64_t N,
+              int64_t C, int64_t HW, int64_t G, int layout, int dtype, void* dx, int64_t dx_sn,
+              int64_t dx_sr, float* dgamma, float* dbeta, void* workspace,
+              size_t workspace_bytes, void* stream) {
+  return bwd_impl(dy, View{dy_sn, dy_sr}, x, View{x_sn, x_sr}, mean, rstd, gamma, N, C, HW, G,
+                  layout, dtype, dx, View{dx_sn, dx_sr}, dgamma, dbeta, workspace,
+                  workspace_bytes, stream);
 }
 
 const char* gn_status_string(int status) {

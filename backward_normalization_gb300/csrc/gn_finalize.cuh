@@ -90,9 +90,17 @@ __device__ __forceinline__ float2* channel_stage(const KParams& p, int64_t n, fl
   return need <= sm_floats ? reinterpret_cast<float2*>(sm + 2 * blockDim.x) : p.chst + n * p.g.C;
 }
 
-// Offset of element (n, c, hw = 0): the per-channel shift of the forward sums.
-__device__ __forceinline__ int64_t first_elem_offset(const Geom& g, int64_t n, int64_t c) {
-  return g.layout == kNCHW ? (n * g.C + c) * g.HW : n * g.HW * g.C + c;
+// Offset of element (n, c, hw = 0) of x: the per-channel shift of the forward sums.
+__device__ __forceinline__ int64_t first_elem_offset(const KParams& p, int64_t n, int64_t c) {
+  return p.g.layout == kNCHW ? n * p.xs_n + c * p.xs_r : n * p.xs_n + c;
+}
+
+// Offset of channel plane `row` = n*C + c (NCHW) in a view with sample stride
+// s_n and plane stride s_r.
+__device__ __forceinline__ int64_t plane_offset(const Geom& g, int64_t row, int64_t s_n,
+                                                int64_t s_r) {
+  const int64_t n = row / g.C;
+  return n * s_n + (row - n * g.C) * s_r;
 }
 
 // Forward statistics.  The partial records hold, per channel, S = sum(x - K_c)
@@ -168,7 +176,7 @@ __device__ void finalize_fwd(const KParams& p, int64_t n, int64_t ca, int64_t cb
   const float hw = (float)g.HW;
   float2* stage = channel_stage(p, n, sm, sm_floats);
   // the shift of this thread's first channel (ca + tid), requested with the records
-  auto shift = [&](int64_t c) { return Elem<T>::to_f(x[first_elem_offset(g, n, c)]); };
+  auto shift = [&](int64_t c) { return Elem<T>::to_f(x[first_elem_offset(p, n, c)]); };
   const int64_t c_pre = ca + threadIdx.x;
   const float k_pre = c_pre < cb ? shift(c_pre) : 0.f;
   sum_channel_partials(p, n, ca, cb, sm, [&](int64_t c, float2 s) {

@@ -167,6 +167,12 @@ struct KParams {
   unsigned* cnt1;     // per level-1 group
   unsigned* ready;    // pipelined: per unit a 64-bit ready record (8-byte aligned)
   unsigned* queue;    // pipelined: [0] CTAs done
+  // Element strides of the views (two-kernel path; the other regimes take
+  // dense tensors only): per sample (s_n) and per channel plane (NCHW) or
+  // spatial row (NHWC) (s_r).  Dense NCHW: C*HW, HW; dense NHWC: HW*C, C.
+  int64_t xs_n, xs_r;   // x
+  int64_t ds_n, ds_r;   // dy
+  int64_t os_n, os_r;   // y or dx
   unsigned* err;
   int clear_words;    // uint32 words at the start of the workspace cleared before the kernels
   int stall_unit;     // fault injection: a unit whose arrival is withheld (-1: none)
@@ -191,11 +197,14 @@ void set_regime_override(int regime);
 // CTAs of the op's first (second = 0) or second (second = 1) two-kernel-path
 // kernel that fit on the current device at once (0: no device visible).
 int64_t resident_ctas(const Geom& g, int op, int second);
+// `dense`: every view is densely packed in its layout; strided views run on
+// the two-kernel path only.
 Geom make_geom(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout,
-               int dtype, bool aligned);
+               int dtype, bool aligned, bool dense = true);
 WsLayout ws_layout(int op, const Geom& g);
 // Counter slots of a problem: the most that any plan of it (either op, either
-// alignment) uses; the workspace layout reserves this many for every call.
+// alignment, dense or strided views) uses; the workspace layout reserves this
+// many for every call.
 int64_t problem_counters(const Geom& g);
 
 // Events recorded around/between the kernels of a call (benchmark hook; the

@@ -96,7 +96,7 @@ __device__ __forceinline__ void stats_chunk(const KParams& p, int64_t item, floa
   const int tid = threadIdx.x;
   const uint64_t pfirst = policy_evict_first(), plast = policy_evict_last();
   const Chunk k = chunk_of(g, item);
-  const T* xr = static_cast<const T*>(p.x) + k.row * g.HW;
+  const T* xr = static_cast<const T*>(p.x) + plane_offset(g, k.row, p.xs_n, p.xs_r);
   const float K = Elem<T>::to_f(xr[0]);
   if (g.fin2 && k.ch == 0 && tid == 0) p.kst[k.row] = K;  // for the second kernel
   const int64_t keep = k.h0 + g.keep_from;
@@ -128,8 +128,8 @@ __device__ __forceinline__ void reduce_chunk(const KParams& p, int64_t item, flo
   const Chunk k = chunk_of(g, item);
   const int64_t n = k.row / g.C;
   const float mu = __ldg(p.mean + n * g.G + (k.row % g.C) / g.Cg);
-  const T* xr = static_cast<const T*>(p.x) + k.row * g.HW;
-  const T* dr = static_cast<const T*>(p.dy) + k.row * g.HW;
+  const T* xr = static_cast<const T*>(p.x) + plane_offset(g, k.row, p.xs_n, p.xs_r);
+  const T* dr = static_cast<const T*>(p.dy) + plane_offset(g, k.row, p.ds_n, p.ds_r);
   const int64_t keep = k.h0 + g.keep_from;
   float s1 = 0.f, s2 = 0.f;
   const int64_t st = (int64_t)blockDim.x * VW;
@@ -170,8 +170,8 @@ __device__ __forceinline__ void apply_chunk(const KParams& p, int64_t item, cons
   const float r = mr.y, mu = mr.x;
   const float a = p.gamma ? r * __ldg(p.gamma + c) : r;
   const float b = p.beta ? __ldg(p.beta + c) : 0.f;
-  const T* xr = static_cast<const T*>(p.x) + k.row * g.HW + k.h0;
-  T* yr = static_cast<T*>(p.out) + k.row * g.HW + k.h0;
+  const T* xr = static_cast<const T*>(p.x) + plane_offset(g, k.row, p.xs_n, p.xs_r) + k.h0;
+  T* yr = static_cast<T*>(p.out) + plane_offset(g, k.row, p.os_n, p.os_r) + k.h0;
   const int64_t nv = (k.h1 - k.h0) / VW;
   const int64_t st = blockDim.x;
   int64_t i = nv - 1 - tid;
@@ -208,9 +208,9 @@ __device__ __forceinline__ void dx_chunk(const KParams& p, int64_t item, const f
   const float r = __ldg(p.rstd + ng), mu = __ldg(p.mean + ng);
   const float A = p.gamma ? r * __ldg(p.gamma + c) : r;
   const float2 cf = grp ? grp[0] : __ldcg(p.coef + ng);
-  const T* xr = static_cast<const T*>(p.x) + k.row * g.HW + k.h0;
-  const T* dr = static_cast<const T*>(p.dy) + k.row * g.HW + k.h0;
-  T* outr = static_cast<T*>(p.out) + k.row * g.HW + k.h0;
+  const T* xr = static_cast<const T*>(p.x) + plane_offset(g, k.row, p.xs_n, p.xs_r) + k.h0;
+  const T* dr = static_cast<const T*>(p.dy) + plane_offset(g, k.row, p.ds_n, p.ds_r) + k.h0;
+  T* outr = static_cast<T*>(p.out) + plane_offset(g, k.row, p.os_n, p.os_r) + k.h0;
   const int64_t nv = (k.h1 - k.h0) / VW;
   const int64_t st = blockDim.x;
   int64_t i = nv - 1 - tid;
@@ -258,7 +258,7 @@ __device__ __forceinline__ void stats_rows(const KParams& p, int64_t item, float
   const uint64_t pol = g.keep_from == 0 ? policy_evict_last() : policy_evict_first();
   for (int64_t c = rb.c0 + warp; c < rb.c1; c += nwarps) {
     const int64_t row = rb.n * g.C + c;
-    const T* xr = static_cast<const T*>(p.x) + row * g.HW;
+    const T* xr = static_cast<const T*>(p.x) + rb.n * p.xs_n + c * p.xs_r;
     const float K = Elem<T>::to_f(xr[0]);
     if (g.fin2 && lane == 0) p.kst[row] = K;  // for the second kernel
     float s = 0.f, q = 0.f;
@@ -284,8 +284,8 @@ __device__ __forceinline__ void reduce_rows(const KParams& p, int64_t item, floa
   for (int64_t c = rb.c0 + warp; c < rb.c1; c += nwarps) {
     const int64_t row = rb.n * g.C + c;
     const float mu = __ldg(p.mean + rb.n * g.G + c / g.Cg);
-    const T* xr = static_cast<const T*>(p.x) + row * g.HW;
-    const T* dr = static_cast<const T*>(p.dy) + row * g.HW;
+    const T* xr = static_cast<const T*>(p.x) + rb.n * p.xs_n + c * p.xs_r;
+    const T* dr = static_cast<const T*>(p.dy) + rb.n * p.ds_n + c * p.ds_r;
     float s1 = 0.f, s2 = 0.f;
     for (int64_t h = (int64_t)lane * VW; h < g.HW; h += 32 * VW) {
       float xv[VW], dv[VW];
@@ -310,13 +310,13 @@ __device__ __forceinline__ void apply_rows(const KParams& p, int64_t item, const
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   const uint64_t pol = policy_evict_first();
   for (int64_t c = rb.c0 + warp; c < rb.c1; c += nwarps) {
-    const int64_t row = rb.n * g.C + c, ng = rb.n * g.G + c / g.Cg;
+    const int64_t ng = rb.n * g.G + c / g.Cg;
     const float2 mr = grp ? grp[c / g.Cg - g0] : make_float2(__ldcg(p.mean + ng), __ldcg(p.rstd + ng));
     const float r = mr.y, mu = mr.x;
     const float a = p.gamma ? r * __ldg(p.gamma + c) : r;
     const float b = p.beta ? __ldg(p.beta + c) : 0.f;
-    const T* xr = static_cast<const T*>(p.x) + row * g.HW;
-    T* yr = static_cast<T*>(p.out) + row * g.HW;
+    const T* xr = static_cast<const T*>(p.x) + rb.n * p.xs_n + c * p.xs_r;
+    T* yr = static_cast<T*>(p.out) + rb.n * p.os_n + c * p.os_r;
     for (int64_t h = (int64_t)lane * VW; h < g.HW; h += 32 * VW) {
       float v[VW];
       Access<T, VW>::load(xr + h, v, pol);
@@ -336,13 +336,13 @@ __device__ __forceinline__ void dx_rows(const KParams& p, int64_t item, const fl
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   const uint64_t pol = policy_evict_first();
   for (int64_t c = rb.c0 + warp; c < rb.c1; c += nwarps) {
-    const int64_t row = rb.n * g.C + c, ng = rb.n * g.G + c / g.Cg;
+    const int64_t ng = rb.n * g.G + c / g.Cg;
     const float r = __ldg(p.rstd + ng), mu = __ldg(p.mean + ng);
     const float A = p.gamma ? r * __ldg(p.gamma + c) : r;
     const float2 cf = grp ? grp[c / g.Cg - g0] : __ldcg(p.coef + ng);
-    const T* xr = static_cast<const T*>(p.x) + row * g.HW;
-    const T* dr = static_cast<const T*>(p.dy) + row * g.HW;
-    T* outr = static_cast<T*>(p.out) + row * g.HW;
+    const T* xr = static_cast<const T*>(p.x) + rb.n * p.xs_n + c * p.xs_r;
+    const T* dr = static_cast<const T*>(p.dy) + rb.n * p.ds_n + c * p.ds_r;
+    T* outr = static_cast<T*>(p.out) + rb.n * p.os_n + c * p.os_r;
     for (int64_t h = (int64_t)lane * VW; h < g.HW; h += 32 * VW) {
       float xv[VW], dv[VW];
       Access<T, VW>::load(xr + h, xv, pol);

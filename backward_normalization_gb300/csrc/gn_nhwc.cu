@@ -104,7 +104,8 @@ __device__ __forceinline__ void stats_item(const KParams& p, int64_t item, float
 #pragma unroll
   for (int q = 0; q < 2 * VW; ++q) acc[q] = 0.f;
   if (it.active && it.row0 < it.row1) {
-    const T* xn = static_cast<const T*>(p.x) + it.n * g.HW * g.C + it.col * VW;
+    const T* xn = static_cast<const T*>(p.x) + it.n * p.xs_n + it.col * VW;
+    const int64_t xr = p.xs_r;
     const uint64_t pfirst = policy_evict_first(), plast = policy_evict_last();
     const int64_t keep = it.row0 + g.keep_from;  // rows from here on are read again first
     float K[VW];
@@ -117,7 +118,7 @@ __device__ __forceinline__ void stats_item(const KParams& p, int64_t item, float
       const uint64_t pol = row >= keep ? plast : pfirst;
       Raw raw[U];
 #pragma unroll
-      for (int u = 0; u < U; ++u) raw[u] = Access<T, VW>::load_raw(xn + (row + u * step) * g.C, pol);
+      for (int u = 0; u < U; ++u) raw[u] = Access<T, VW>::load_raw(xn + (row + u * step) * xr, pol);
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         float v[VW];
@@ -135,7 +136,7 @@ __device__ __forceinline__ void stats_item(const KParams& p, int64_t item, float
       Raw raw[U];
 #pragma unroll
       for (int u = 0; u < U; ++u)
-        raw[u] = row + u * step < it.row1 ? Access<T, VW>::load_raw(xn + (row + u * step) * g.C, pol)
+        raw[u] = row + u * step < it.row1 ? Access<T, VW>::load_raw(xn + (row + u * step) * xr, pol)
                                           : Raw{};
 #pragma unroll
       for (int u = 0; u < U; ++u) {
@@ -174,9 +175,9 @@ __device__ __forceinline__ void reduce_item(const KParams& p, int64_t item, floa
     PerGroup<VW, NG> mu;
 #pragma unroll
     for (int k = 0; k < NG; ++k) mu.v[k] = __ldg(p.mean + it.n * g.G + (it.col * VW + k) / g.Cg);
-    const int64_t off = it.n * g.HW * g.C + it.col * VW;
-    const T* xn = static_cast<const T*>(p.x) + off;
-    const T* dyn = static_cast<const T*>(p.dy) + off;
+    const T* xn = static_cast<const T*>(p.x) + it.n * p.xs_n + it.col * VW;
+    const T* dyn = static_cast<const T*>(p.dy) + it.n * p.ds_n + it.col * VW;
+    const int64_t xr = p.xs_r, dr = p.ds_r;
     const uint64_t pfirst = policy_evict_first(), plast = policy_evict_last();
     const int64_t keep = it.row0 + g.keep_from;
     const int64_t step = g.rpi;
@@ -188,8 +189,8 @@ __device__ __forceinline__ void reduce_item(const KParams& p, int64_t item, floa
       Raw rx[U], rd[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        rx[u] = Access<T, VW>::load_raw(xn + (row + u * step) * g.C, pol);
-        rd[u] = Access<T, VW>::load_raw(dyn + (row + u * step) * g.C, pol);
+        rx[u] = Access<T, VW>::load_raw(xn + (row + u * step) * xr, pol);
+        rd[u] = Access<T, VW>::load_raw(dyn + (row + u * step) * dr, pol);
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
@@ -207,8 +208,8 @@ __device__ __forceinline__ void reduce_item(const KParams& p, int64_t item, floa
       for (; row < it.row1; row += step) {
         const uint64_t pol = row >= keep ? plast : pfirst;
         float xv[VW], dv[VW];
-        Access<T, VW>::load(xn + row * g.C, xv, pol);
-        Access<T, VW>::load(dyn + row * g.C, dv, pol);
+        Access<T, VW>::load(xn + row * xr, xv, pol);
+        Access<T, VW>::load(dyn + row * dr, dv, pol);
 #pragma unroll
         for (int k = 0; k < VW; ++k) {
           acc[2 * k] += dv[k];
@@ -221,8 +222,8 @@ __device__ __forceinline__ void reduce_item(const KParams& p, int64_t item, floa
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const bool in = row + u * step < it.row1;
-        rx[u] = in ? Access<T, VW>::load_raw(xn + (row + u * step) * g.C, pol) : Raw{};
-        rd[u] = in ? Access<T, VW>::load_raw(dyn + (row + u * step) * g.C, pol) : Raw{};
+        rx[u] = in ? Access<T, VW>::load_raw(xn + (row + u * step) * xr, pol) : Raw{};
+        rd[u] = in ? Access<T, VW>::load_raw(dyn + (row + u * step) * dr, pol) : Raw{};
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
@@ -268,29 +269,29 @@ __device__ __forceinline__ void apply_item(const KParams& p, int64_t item) {
     b[k] = p.beta ? __ldg(p.beta + c) : 0.f;
     if (NG > 1 || k == 0) mu.v[NG > 1 ? k : 0] = __ldcg(p.mean + ng);
   }
-  const int64_t off = it.n * g.HW * g.C + it.col * VW;
-  const T* xn = static_cast<const T*>(p.x) + off;
-  T* yn = static_cast<T*>(p.out) + off;
+  const T* xn = static_cast<const T*>(p.x) + it.n * p.xs_n + it.col * VW;
+  T* yn = static_cast<T*>(p.out) + it.n * p.os_n + it.col * VW;
+  const int64_t xr = p.xs_r, yr = p.os_r;
   const uint64_t pol = policy_evict_first();
   const int64_t step = g.rpi;
   int64_t row = it.row0 + it.r + ((cnt - 1) / step) * step;  // last row of the lane
   for (; row - 3 * step >= it.row0; row -= 4 * step) {
     float v[4][VW];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) Access<T, VW>::load(xn + (row - u * step) * g.C, v[u], pol);
+    for (int u = 0; u < 4; ++u) Access<T, VW>::load(xn + (row - u * step) * xr, v[u], pol);
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
 #pragma unroll
       for (int k = 0; k < VW; ++k) v[u][k] = fmaf(v[u][k] - mu[k], a[k], b[k]);
-      Access<T, VW>::store(yn + (row - u * step) * g.C, v[u], pol);
+      Access<T, VW>::store(yn + (row - u * step) * yr, v[u], pol);
     }
   }
   for (; row >= it.row0; row -= step) {
     float v[VW];
-    Access<T, VW>::load(xn + row * g.C, v, pol);
+    Access<T, VW>::load(xn + row * xr, v, pol);
 #pragma unroll
     for (int k = 0; k < VW; ++k) v[k] = fmaf(v[k] - mu[k], a[k], b[k]);
-    Access<T, VW>::store(yn + row * g.C, v, pol);
+    Access<T, VW>::store(yn + row * yr, v, pol);
   }
 }
 
@@ -317,10 +318,10 @@ __device__ __forceinline__ void dx_item(const KParams& p, int64_t item) {
       D.v[NG > 1 ? k : 0] = cf.y;
     }
   }
-  const int64_t off = it.n * g.HW * g.C + it.col * VW;
-  const T* xn = static_cast<const T*>(p.x) + off;
-  const T* dyn = static_cast<const T*>(p.dy) + off;
-  T* dxn = static_cast<T*>(p.out) + off;
+  const T* xn = static_cast<const T*>(p.x) + it.n * p.xs_n + it.col * VW;
+  const T* dyn = static_cast<const T*>(p.dy) + it.n * p.ds_n + it.col * VW;
+  T* dxn = static_cast<T*>(p.out) + it.n * p.os_n + it.col * VW;
+  const int64_t xr = p.xs_r, dr = p.ds_r, orr = p.os_r;
   const uint64_t pol = policy_evict_first();
   const int64_t step = g.rpi;
   int64_t row = it.row0 + it.r + ((cnt - 1) / step) * step;
@@ -329,8 +330,8 @@ __device__ __forceinline__ void dx_item(const KParams& p, int64_t item) {
     Raw rx[2], rd[2];  // packed until used: fewer live registers
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
-      rx[u] = Access<T, VW>::load_raw(xn + (row - u * step) * g.C, pol);
-      rd[u] = Access<T, VW>::load_raw(dyn + (row - u * step) * g.C, pol);
+      rx[u] = Access<T, VW>::load_raw(xn + (row - u * step) * xr, pol);
+      rd[u] = Access<T, VW>::load_raw(dyn + (row - u * step) * dr, pol);
     }
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
@@ -339,16 +340,16 @@ __device__ __forceinline__ void dx_item(const KParams& p, int64_t item) {
       Access<T, VW>::unpack(rd[u], dv);
 #pragma unroll
       for (int k = 0; k < VW; ++k) xv[k] = fmaf(A[k], dv[k], fmaf(B[k], xv[k] - mu[k], D[k]));
-      Access<T, VW>::store(dxn + (row - u * step) * g.C, xv, pol);
+      Access<T, VW>::store(dxn + (row - u * step) * orr, xv, pol);
     }
   }
   for (; row >= it.row0; row -= step) {
     float xv[VW], dv[VW];
-    Access<T, VW>::load(xn + row * g.C, xv, pol);
-    Access<T, VW>::load(dyn + row * g.C, dv, pol);
+    Access<T, VW>::load(xn + row * xr, xv, pol);
+    Access<T, VW>::load(dyn + row * dr, dv, pol);
 #pragma unroll
     for (int k = 0; k < VW; ++k) xv[k] = fmaf(A[k], dv[k], fmaf(B[k], xv[k] - mu[k], D[k]));
-    Access<T, VW>::store(dxn + row * g.C, xv, pol);
+    Access<T, VW>::store(dxn + row * orr, xv, pol);
   }
 }
 

@@ -666,7 +666,7 @@ void plan_fin2(Geom& g) {
 }
 
 Geom plan_geom(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout, int dtype,
-               bool aligned) {
+               bool aligned, bool dense) {
   const int sm_count = device_sm_count();
   Geom g{};
   g.N = N;
@@ -746,7 +746,8 @@ Geom plan_geom(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout, 
   g.units_fin = N;  // the two-kernel path finalises per sample
   g.unit_groups = 0;
   g.regime = kRegimeGeneric;
-  const int ov = g_regime_override.load();
+  // strided views run on the two-kernel path only
+  const int ov = dense ? g_regime_override.load() : kRegimeGeneric;
   if (ov == kRegimeResident) {
     plan_resident(g, op, false);  // wherever the problem fits the regime
   } else if (ov == kRegimePipelined) {
@@ -770,26 +771,27 @@ Geom plan_geom(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout, 
 // Plans are cached per (device, regime override, op, problem, alignment):
 // building one queries occupancy, and every call (and every workspace layout,
 // which looks at the plans of both ops) needs them.
-using PlanKey = std::tuple<int, int, int, int64_t, int64_t, int64_t, int64_t, int, int, int>;
+using PlanKey = std::tuple<int, int, int, int64_t, int64_t, int64_t, int64_t, int, int, int, int>;
 std::mutex g_plan_mu;
 std::map<PlanKey, Geom> g_plan_cache;
 constexpr size_t kPlanCacheMax = 4096;
 }  // namespace
 
 Geom make_geom(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout, int dtype,
-               bool aligned) {
+               bool aligned, bool dense) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) {
     cudaGetLastError();
     dev = -1;
   }
-  const PlanKey key{dev, g_regime_override.load(), op, N, C, HW, G, layout, dtype, aligned ? 1 : 0};
+  const PlanKey key{dev, g_regime_override.load(), op, N, C, HW, G, layout, dtype, aligned ? 1 : 0,
+                    dense ? 1 : 0};
   {
     std::lock_guard<std::mutex> lock(g_plan_mu);
     auto it = g_plan_cache.find(key);
     if (it != g_plan_cache.end()) return it->second;
   }
-  const Geom g = plan_geom(op, N, C, HW, G, layout, dtype, aligned);
+  const Geom g = plan_geom(op, N, C, HW, G, layout, dtype, aligned, dense);
   std::lock_guard<std::mutex> lock(g_plan_mu);
   if (g_plan_cache.size() >= kPlanCacheMax) g_plan_cache.clear();
   g_plan_cache.emplace(key, g);
@@ -799,10 +801,11 @@ Geom make_geom(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout, 
 int64_t problem_counters(const Geom& g) {
   int64_t c = 0;
   for (int op = 0; op < 2; ++op)
-    for (int a = 0; a < 2; ++a) {
-      const Geom o = make_geom(op, g.N, g.C, g.HW, g.G, g.layout, g.dtype, a != 0);
-      if (o.counters > c) c = o.counters;
-    }
+    for (int a = 0; a < 2; ++a)
+      for (int d = 0; d < 2; ++d) {
+        const Geom o = make_geom(op, g.N, g.C, g.HW, g.G, g.layout, g.dtype, a != 0, d != 0);
+        if (o.counters > c) c = o.counters;
+      }
   return c;
 }
 

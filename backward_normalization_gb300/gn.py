@@ -75,6 +75,14 @@ def lib() -> ctypes.CDLL:
         L.gn_fwd_static_ws.argtypes = [_VP, _I64, _I64, _I64, _I64, ctypes.c_int, ctypes.c_int, _VP,
                                        _VP, ctypes.c_float, _VP, _VP, _VP, _VP]
         L.gn_fwd_static_ws.restype = ctypes.c_int
+        L.gn_fwd_ex.argtypes = [_VP, _I64, _I64, _I64, _I64, _I64, _I64, ctypes.c_int,
+                                ctypes.c_int, _VP, _VP, ctypes.c_float, _VP, _I64, _I64, _VP, _VP,
+                                _VP, ctypes.c_size_t, _VP]
+        L.gn_fwd_ex.restype = ctypes.c_int
+        L.gn_bwd_ex.argtypes = [_VP, _I64, _I64, _VP, _I64, _I64, _VP, _VP, _VP, _I64, _I64, _I64,
+                                _I64, ctypes.c_int, ctypes.c_int, _VP, _I64, _I64, _VP, _VP, _VP,
+                                ctypes.c_size_t, _VP]
+        L.gn_bwd_ex.restype = ctypes.c_int
         L.gn_workspace_status.argtypes = [_VP, _VP]
         L.gn_workspace_status.restype = ctypes.c_int
         L.gn_set_fault_injection.argtypes = [ctypes.c_int]
@@ -167,6 +175,27 @@ def bwd_raw(dy, x, mean, rstd, gamma, N, C, HW, G, layout, dx, dgamma, dbeta, wo
     return lib().gn_bwd(_ptr(dy), _ptr(x), _ptr(mean), _ptr(rstd), _ptr(gamma), N, C, HW, G,
                         LAYOUT[layout], DTYPE[x.dtype], _ptr(dx), _ptr(dgamma), _ptr(dbeta),
                         _ptr(workspace), ws_bytes, _stream(stream))
+
+
+def fwd_ex_raw(x, x_s, N, C, HW, G, layout, gamma, beta, eps, y, y_s, mean, rstd, workspace,
+               stream=None) -> int:
+    """gn_fwd_ex: x and y are tensors whose data_ptr() is element (0, 0, 0) of
+    the view; x_s and y_s are (sample stride, plane or row stride) in
+    elements.  Returns the gn_status."""
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    return lib().gn_fwd_ex(_ptr(x), x_s[0], x_s[1], N, C, HW, G, LAYOUT[layout], DTYPE[x.dtype],
+                           _ptr(gamma), _ptr(beta), float(eps), _ptr(y), y_s[0], y_s[1],
+                           _ptr(mean), _ptr(rstd), _ptr(workspace), ws_bytes, _stream(stream))
+
+
+def bwd_ex_raw(dy, dy_s, x, x_s, mean, rstd, gamma, N, C, HW, G, layout, dx, dx_s, dgamma,
+               dbeta, workspace, stream=None) -> int:
+    """gn_bwd_ex on strided views (see fwd_ex_raw); returns the gn_status."""
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    return lib().gn_bwd_ex(_ptr(dy), dy_s[0], dy_s[1], _ptr(x), x_s[0], x_s[1], _ptr(mean),
+                           _ptr(rstd), _ptr(gamma), N, C, HW, G, LAYOUT[layout], DTYPE[x.dtype],
+                           _ptr(dx), dx_s[0], dx_s[1], _ptr(dgamma), _ptr(dbeta),
+                           _ptr(workspace), ws_bytes, _stream(stream))
 
 
 REGIME_AUTO, REGIME_TWO_KERNEL, REGIME_RESIDENT, REGIME_PIPELINED, REGIME_WAVE = -1, 0, 1, 2, 3

@@ -20,8 +20,8 @@
  * NVIDIA/apex PR #2018, reproducer: channels_last activations):
  *     GN_LAYOUT_NCHW: element (n, c, hw) at offset (n*C + c)*HW + hw
  *     GN_LAYOUT_NHWC: element (n, c, hw) at offset (n*HW + hw)*C + c
- * Tensors are densely packed in one of these layouts; strided views are not
- * accepted.
+ * gn_fwd / gn_bwd take tensors densely packed in one of these layouts;
+ * gn_fwd_ex / gn_bwd_ex (below) take strided views.
  *
  * Types: x, y, dy, dx are all of `dtype` (fp32, fp16, bf16 or fp64); every
  * reduction and every intermediate is fp32.  gamma, beta, dgamma, dbeta are
@@ -121,6 +121,38 @@ GN_API int gn_bwd(const void* dy, const void* x, const float* mean, const float*
            const float* gamma, int64_t N, int64_t C, int64_t HW, int64_t G, int layout,
            int dtype, void* dx, float* dgamma, float* dbeta, void* workspace,
            size_t workspace_bytes, void* stream);
+
+/* Strided views ("baracuda-kernels src/norm/group_norm_backward.rs",
+ * GroupNormBackwardPlan::select: the plan takes views of rank 2 to 8; "Kimi-
+ * K2.6 l1_p35" POPCORNBENCH transcript, on inputs that are not contiguous).
+ * gn_fwd_ex and gn_bwd_ex are gn_fwd and gn_bwd on views whose elements lie
+ * at
+ *     GN_LAYOUT_NCHW: base + n*sn + c*sr + hw       (each channel plane contiguous)
+ *     GN_LAYOUT_NHWC: base + n*sn + hw*sr + c       (each spatial row contiguous)
+ * with strides in elements, one (sn, sr) pair per tensor -- for example a
+ * slice of the channels of a wider tensor, or planes padded to a row pitch.
+ * The dense strides are (C*HW, HW) for NCHW and (HW*C, C) for NHWC; with those
+ * the calls are gn_fwd / gn_bwd exactly.  A stride may be anything when its
+ * extent is 1 (sn when N == 1; sr when C == 1 for NCHW, HW == 1 for NHWC);
+ * otherwise the strides must keep elements apart -- planes (rows) laid out
+ * sample-major (sn >= count*sr, sr >= run) or plane(row)-major (sr >= N*sn,
+ * sn >= run), with run = HW (NCHW) or C (NHWC) -- else GN_ERR_INVALID.
+ * Outputs may be their input in place only with identical strides; an output
+ * whose address span meets an input's span is otherwise rejected, even when
+ * the views interleave without sharing an element.  Views that are not dense
+ * run on the two-kernel path; they take 16-byte vectors when every base and
+ * every stride (times the element size) is a multiple of 16 bytes, the scalar
+ * path otherwise.  Workspace, statistics, parameters, errors and execution
+ * are as for gn_fwd / gn_bwd; gn_workspace_size covers these calls too. */
+GN_API int gn_fwd_ex(const void* x, int64_t x_sn, int64_t x_sr, int64_t N, int64_t C, int64_t HW,
+                     int64_t G, int layout, int dtype, const float* gamma, const float* beta,
+                     float eps, void* y, int64_t y_sn, int64_t y_sr, float* mean, float* rstd,
+                     void* workspace, size_t workspace_bytes, void* stream);
+GN_API int gn_bwd_ex(const void* dy, int64_t dy_sn, int64_t dy_sr, const void* x, int64_t x_sn,
+                     int64_t x_sr, const float* mean, const float* rstd, const float* gamma,
+                     int64_t N, int64_t C, int64_t HW, int64_t G, int layout, int dtype, void* dx,
+                     int64_t dx_sn, int64_t dx_sr, float* dgamma, float* dbeta, void* workspace,
+                     size_t workspace_bytes, void* stream);
 
 /* Size of the device scratch area that gn_fwd_static_ws uses (per device). */
 #define GN_STATIC_WS_BYTES ((size_t)4 << 20)

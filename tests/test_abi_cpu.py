@@ -322,3 +322,38 @@ def test_fault_injection_from_environment(gn):
     assert out.returncode == 0, out.stderr
     rc, err = map(int, out.stdout.split())
     assert rc == gn.GN_ERR_CUDA and err == 719
+
+
+def _fwd_ex(gn, **kw):
+    a = dict(x=FAKE, xs=(8 * 16, 16), N=2, C=8, HW=16, G=2, layout=0, dtype=0, y=FAKE * 4,
+             ys=(8 * 16, 16), mean=FAKE * 8, rstd=FAKE * 9, ws=FAKE * 10, ws_bytes=1 << 30)
+    a.update(kw)
+    return gn.lib().gn_fwd_ex(a["x"], a["xs"][0], a["xs"][1], a["N"], a["C"], a["HW"], a["G"],
+                              a["layout"], a["dtype"], None, None, 1e-5, a["y"], a["ys"][0],
+                              a["ys"][1], a["mean"], a["rstd"], a["ws"], a["ws_bytes"], None)
+
+
+def test_strided_view_validation(gn):
+    """gn_fwd_ex checks its strides before anything else happens; calls that
+    pass validation run into GN_FAULT_LAUNCH here, so nothing is launched."""
+    INV, CUDA = gn.GN_ERR_INVALID, gn.GN_ERR_CUDA
+    gn.set_fault_injection(gn.FAULT_LAUNCH)
+    try:
+        assert _fwd_ex(gn) == CUDA                                   # dense NCHW
+        assert _fwd_ex(gn, xs=(12 * 16, 16)) == CUDA                 # a channel slice of 12
+        assert _fwd_ex(gn, xs=(16, 2 * 16)) == CUDA                  # channel-major batch
+        assert _fwd_ex(gn, xs=(8 * 20, 20)) == CUDA                  # padded planes
+        assert _fwd_ex(gn, xs=(8 * 16, 15)) == INV                   # planes overlap
+        assert _fwd_ex(gn, xs=(7 * 16, 16)) == INV                   # samples overlap
+        assert _fwd_ex(gn, xs=(-128, 16)) == INV
+        assert _fwd_ex(gn, N=1, xs=(5, 16)) == CUDA                  # N = 1: sample stride free
+        nhwc = dict(layout=1, ys=(16 * 8, 8))
+        assert _fwd_ex(gn, xs=(16 * 8, 8), **nhwc) == CUDA           # dense NHWC
+        assert _fwd_ex(gn, xs=(16 * 10, 10), **nhwc) == CUDA         # channel slice, NHWC
+        assert _fwd_ex(gn, xs=(16 * 8, 7), **nhwc) == INV            # rows overlap
+        # an output whose span meets the input's is rejected unless it is the input in place
+        assert _fwd_ex(gn, y=FAKE + 64) == INV
+        assert _fwd_ex(gn, y=FAKE) == CUDA
+        assert _fwd_ex(gn, y=FAKE, ys=(8 * 20, 20)) == INV
+    finally:
+        gn.set_fault_injection(gn.FAULT_NONE)
