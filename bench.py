@@ -310,9 +310,21 @@ def source_sha():
     return h.hexdigest()[:16]
 
 
-def time_configs(gn, synth, torch, flush, names=None, reps=20):
+def variant_workloads(synth):
+    """The special cases of the op on the large workloads' shapes, timed beside
+    them: InstanceNorm (G = C) and GroupNorm without affine parameters (gamma
+    and beta absent, so no dgamma / dbeta either)."""
+    c3, c4 = synth.BY_NAME["fp32_nchw_112x64x512x512_g8"], synth.BY_NAME["bf16_nhwc_32x512x32x32_g32"]
+    return [(c4.scaled(name="bf16_nhwc_32x512x32x32_g512_instancenorm", G=512), True),
+            (c3.scaled(name="fp32_nchw_16x64x512x512_g64_instancenorm", N=16, G=64), True),
+            (c4.scaled(name="bf16_nhwc_32x512x32x32_g32_no_affine"), False),
+            (c3.scaled(name="fp32_nchw_16x64x512x512_g8_no_affine", N=16), False)]
+
+
+def time_configs(gn, synth, torch, flush, names=None, reps=20, variants=False):
     """Per-workload fwd and bwd times (median of reps, L2 flushed before each
-    call) for the large workloads.  All reps are queued before the first
+    call) for the large workloads (and, with `variants`, the special cases of
+    variant_workloads).  All reps are queued before the first
     synchronisation, so the GPU never waits for the host between calls."""
     out = {}
     peak, _ = load_peaks()
@@ -320,20 +332,24 @@ def time_configs(gn, synth, torch, flush, names=None, reps=20):
     todo = []
     for w in synth.WORKLOADS[1:]:
         if not names:
-            todo.append(w)
+            todo.append((w, True))
         for nm in names or ():
             base, _, nn = nm.partition(":")  # "workload" or "workload:N" (batch override)
             if base == w.name:
-                todo.append(w.scaled(N=int(nn)) if nn else w)
-    for w in todo:
+                todo.append((w.scaled(N=int(nn)) if nn else w, True))
+    if variants:
+        todo += variant_workloads(synth)
+    for w, affine in todo:
         inp = synth.make_inputs(w, "cuda", seed=0)
         x, dy, gm, bt = inp["x"], inp["dy"], inp["gamma"], inp["beta"]
+        if not affine:
+            gm = bt = None
         y = torch.empty_like(x)
         dx = torch.empty_like(x)
         mean = torch.empty(w.N * w.G, device="cuda")
         rstd = torch.empty(w.N * w.G, device="cuda")
-        dg = torch.empty(w.C, device="cuda")
-        db = torch.empty(w.C, device="cuda")
+        dg = torch.empty(w.C, device="cuda") if affine else None
+        db = torch.empty(w.C, device="cuda") if affine else None
         ws = gn.alloc_workspace(gn.OP_BWD, w.N, w.C, w.HW, w.G, w.layout, x.dtype)
         n_it = reps + 3
         evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(n_it)]
@@ -366,7 +382,9 @@ def time_configs(gn, synth, torch, flush, names=None, reps=20):
         med = {k: statistics.median(v) for k, v in rec.items()}
         fwd_gbs = mb["fwd"] / (med["fwd"] * 1e-3) / 1e9
         bwd_gbs = mb["bwd"] / (med["bwd"] * 1e-3) / 1e9
-        out[w.name if w.N == synth.BY_NAME[w.name].N else f"{w.name}:N={w.N}"] = {
+        key = w.name if w.name not in synth.BY_NAME or w.N == synth.BY_NAME[w.name].N \
+            else f"{w.name}:N={w.N}"
+        out[key] = {
             "regime": {"fwd": REGIME_NAMES[pf.regime], "bwd": REGIME_NAMES[pb.regime]},
             "fwd_us": round(med["fwd"] * 1e3, 2), "bwd_us": round(med["bwd"] * 1e3, 2),
             "fwd_gbs": round(fwd_gbs, 1), "bwd_gbs": round(bwd_gbs, 1),
@@ -637,7 +655,7 @@ def run_ours(args, rank, world, local_rank):
         torch.cuda.empty_cache()
         per_config = time_configs(gn, synth, torch, flush,
                                   names=args.configs.split(",") if args.configs else None,
-                                  reps=args.reps)
+                                  reps=args.reps, variants=not args.configs)
 
     rows = None
     if not args.no_per_config and not args.no_rows and world == 1:
