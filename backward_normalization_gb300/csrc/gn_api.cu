@@ -438,6 +438,8 @@ int gn_plan_info(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout
   const int64_t mc = gn::plan_max_clusters(g, op);
   out->max_clusters = mc > 0 ? (int)mc : 0;
   // item / piece shape (the boundaries the parity tests sample)
+  out->slots = g.regime == gn::kRegimeGeneric ? 0 : g.S;
+  out->hold_buffers = g.regime == gn::kRegimeWave ? (int)g.wH : 0;
   if (g.regime == gn::kRegimeWave) {
     out->piece_elems = g.wR;
     out->pieces_per_unit = g.wP;

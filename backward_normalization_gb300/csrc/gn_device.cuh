@@ -398,6 +398,57 @@ __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;" ::: "memory");
 }
 
+// ------------------------------------------------------------ tensor memory
+// Tensor memory (TMEM): 128 lanes x 512 columns of 32-bit cells per SM.  An
+// address is (lane << 16) | column.  Warp w of a CTA reaches lanes
+// 32*(w % 4) .. 32*(w % 4) + 31; in the 32x32b shapes thread i of the warp
+// owns lane 32*(w % 4) + i and register r holds column (address column + r).
+// Allocation, release and every load / store below are warp-wide
+// (.sync.aligned): all 32 threads execute them with the same address.
+
+// Warp-wide: allocates `ncols` columns (a power of two, 32..512) and writes
+// the base address to *dst (shared memory).  Blocks until the columns are free.
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(dst)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+// Warp-wide: frees the columns of tmem_alloc.
+__device__ __forceinline__ void tmem_dealloc(uint32_t base, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(base), "r"(ncols) : "memory");
+}
+// Order tensor-memory operations across a thread barrier: `before` ahead of
+// the barrier, `after` behind it.
+__device__ __forceinline__ void tmem_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// Warp-wide: 16 consecutive columns of this thread's lane from / to registers.
+// A load's registers are valid only after tmem_wait_ld; a store has finished
+// (its cells readable, its columns reusable) after tmem_wait_st.
+__device__ __forceinline__ void tmem_st16(uint32_t a, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+      "%14, %15, %16};" ::"r"(a),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld16(uint32_t a, uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15}, [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
+        "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+      : "r"(a)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 // ------------------------------------------------------ cluster reduction
 // Adds, for every q < NQ, red[q*stride + slot] of all CTAs of the cluster into
 // the copy of cluster rank 0, in rank order.  Every thread of every CTA of the

@@ -26,8 +26,9 @@ enum Regime {
   kRegimeResident = 1,  // one kernel: a cluster holds a unit in shared memory
   kRegimePipelined = 2, // one persistent kernel: pass-1 and pass-2 tasks of
                         // units in flight, the second pass reading from L2
-  kRegimeWave = 3,      // one persistent kernel: every piece of a unit stays in
-                        // shared memory until the unit's statistics are known
+  kRegimeWave = 3,      // one persistent kernel: every piece of a unit stays on
+                        // chip (shared or tensor memory) until the unit's
+                        // statistics are known
 };
 
 // How one call is cut into "items" for the two-kernel path.  Both kernels
@@ -103,8 +104,12 @@ struct Geom {
   // elements of one channel plane (NCHW; wm pieces per plane) or wR rows of
   // Cb channels (NHWC, read as wnb TMA boxes of `chunk` rows); `grid` CTAs
   // hold S slots of ten_stride bytes per tensor; wcols parameter columns
-  // (channel blocks of a sample) finish dgamma/dbeta
-  int64_t wP, wR, wm, wnb, wcols;
+  // (channel blocks of a sample) finish dgamma/dbeta.  wH > 0: a reduced
+  // piece waits for its unit's statistics in one of wH tensor-memory
+  // buffers (wT 16-byte vectors per thread and tensor), which frees its slot
+  // for the next copy at once; wH = 0: it waits in its slot.  wB buffers of
+  // per-piece constants.
+  int64_t wP, wR, wm, wnb, wcols, wH, wT, wB;
 };
 
 // Bytes reserved per ring-slot header of the pipelined kernel (the header
@@ -249,6 +254,11 @@ __host__ __device__ inline int wave_cst_floats(const Geom& g) {
 #endif
 constexpr int kWaveThreads = GN_WAVE_THREADS;
 constexpr int kWaveCtasPerSm = GN_WAVE_CTAS_PER_SM;
+// Tensor-memory columns one wave CTA allocates (its share of the SM's 512).
+constexpr int kWaveTmemCols = 512 / GN_WAVE_CTAS_PER_SM;
+static_assert(kWaveTmemCols >= 32 && (kWaveTmemCols & (kWaveTmemCols - 1)) == 0,
+              "a tensor-memory allocation is a power of two of at least 32 columns");
+static_assert(kWaveThreads % 128 == 0, "whole warp quarters share the tensor-memory lanes");
 // gn_resident.cu
 // [N*HW, C] view of an NHWC tensor for TMA, boxes of [g.chunk rows, g.Cb channels].
 cudaError_t encode_nhwc_map(CUtensorMap* map, const void* base, const Geom& g);

@@ -116,11 +116,11 @@ bool resident_preferred(const Geom& g, int op) {
 // CTAs runs a chain of short barrier-separated phases (wait, reduce, publish,
 // gather, merge, write) that a 55 KB piece does not hide.  It wins where the
 // op's second read costs most and the units are large: the NCHW backward with
-// units of at least 4 MiB (fp32 112x64x512x512 G8: 4.82 ms against 5.26 ms
-// two-kernel); the NCHW forward (3.55-3.85 against 3.21 ms) and the small
-// channels-last workloads (bf16 8x320x64x64 G32: 41-44 / 92 us against 23 /
-// 40 us; bf16 32x512x32x32 G32: 43-48 / 56-62 against 35 / 38 us) stay with
-// the other families.
+// units of at least 4 MiB (fp32 112x64x512x512 G8: 4.52 ms with pieces held in
+// tensor memory, against 5.22-5.27 ms two-kernel); the NCHW forward (3.9-4.2
+// against 3.2 ms) and the small channels-last workloads (bf16 8x320x64x64
+// G32: 41-44 / 52-55 us against 29 / 38-40 us; bf16 32x512x32x32 G32: 47-53 /
+// 61-68 against 32 / 38 us) stay with the other families.
 bool wave_preferred(const Geom& g, int op) {
   const int esz = dtype_size(g.dtype);
   return g.layout == kNCHW && op == kBwd && g.Cg * g.HW * esz >= (4ll << 20);
@@ -365,9 +365,14 @@ namespace {
 #ifndef GN_WAVE_MAX_CB
 #define GN_WAVE_MAX_CB 128
 #endif
+// Tensor-memory buffers a wave CTA may hold reduced pieces in (0: none).
+#ifndef GN_WAVE_MAX_HOLD
+#define GN_WAVE_MAX_HOLD 4
+#endif
 constexpr int kWaveMinSlots = GN_WAVE_MIN_SLOTS;
 constexpr int kWaveMaxSlots = GN_WAVE_MAX_SLOTS;
 constexpr int64_t kWaveMaxCb = GN_WAVE_MAX_CB;  // channels per NHWC unit (TMA box <= 256)
+constexpr int64_t kWaveMaxHold = GN_WAVE_MAX_HOLD < kWaveMaxSlots - 1 ? GN_WAVE_MAX_HOLD : kWaveMaxSlots - 1;
 
 // CTAs of the wave kernel that fit on the device at once with `smem` bytes of
 // dynamic shared memory (an estimate when no device is visible).
@@ -392,48 +397,83 @@ int64_t wave_ctas(const Geom& g, int op, size_t smem, int sm_count, int want_per
 // (elements of a plane, or rows), slots S, CTAs NC; `cost` estimates its
 // time in microseconds.
 struct WaveCut {
-  int64_t P = 0, R = 0, m = 1, nb = 1, box = 0, Cb = 0, S = 0, steps = 0;
+  int64_t P = 0, R = 0, m = 1, nb = 1, box = 0, Cb = 0, S = 0, steps = 0, H = 0, T4 = 0;
   double cost = 0.0;
   size_t slot = 0, out = 0;
 };
 
+// Stage A of a wave step runs this many pieces ahead of stage B: with
+// tensor-memory buffers, one less than their number; else one when a third
+// slot lets a piece land while two are in use.
+int64_t wave_ahead(int64_t H, int64_t S) { return H > 0 ? H - 1 : (S >= 3 ? 1 : 0); }
+
 // Cost model of a wave cut, from measurements on GB300: an SM moves about
 // 45 GB/s (in + out), shared by its CTAs; every step adds about 0.4 us of work that copies do not
-// hide, a unit split over CTAs about 0.3 us more for its arrivals, and with
-// only two slots the wait for a unit is exposed (about 1 us).  A unit whose
+// hide, a unit split over CTAs about 0.3 us more for its arrivals, and
+// unless stage A runs ahead the wait for a unit is exposed (about 1 us).  A unit whose
 // pieces straddle two steps (P not dividing the CTA count) stalls its CTAs
 // for about one piece time.
 #ifndef GN_WAVE_FORCE_CB
 #define GN_WAVE_FORCE_CB 0
 #endif
+#ifndef GN_WAVE_FORCE_P
+#define GN_WAVE_FORCE_P 0
+#endif
 double wave_cost(const WaveCut& c, int64_t NC) {
   // us at 45 GB/s per SM, shared by the CTAs on it
   const double t_io = (double)(c.slot + c.out) * kWaveCtasPerSm / 45.0e3;
-  double per_step = t_io + 0.4 + (c.P > 1 ? 0.3 : 0.0) + (c.S < 3 ? 1.0 : 0.0);
+  double per_step = t_io + 0.4 + (c.P > 1 ? 0.3 : 0.0) + (wave_ahead(c.H, c.S) < 1 ? 1.0 : 0.0);
   if (c.P > 1 && NC % c.P != 0) per_step += t_io;
   return (double)c.steps * per_step + t_io;
 }
 
 // Shared memory of a wave plan besides its slots: the records and CTA sums,
 // the per-channel and per-group values, the mbarriers.
-int64_t wave_red_floats(const Geom& g, int64_t P, int64_t Cb, int vec) {
+int64_t wave_red_floats(const Geom& g, int64_t P, int64_t Cb, int vec, int64_t H) {
   // the unit's records, then the CTA sums: per-thread partials, the shifts
   // and the per-(column, value) totals of NHWC pieces, or a block-sum scratch
   const int64_t nch = g.layout == kNHWC ? Cb : 1;
-  const int64_t recs = P > 1 ? P * nch : 2 * nch;  // gathered, or two pieces' own
+  // gathered, or the CTA's own for the pieces between stages A and B
+  const int64_t recs = P > 1 ? P * nch : std::max<int64_t>(2, H) * nch;
   const int64_t red = 2 * recs + (g.layout == kNHWC ? 2 * vec * kWaveThreads + 3 * Cb : 64);
   return std::max<int64_t>(red, 2 * kWaveThreads);
 }
 
-size_t wave_fixed_bytes(const Geom& g, int64_t P, int64_t Cb, int vec) {
-  const int64_t red = wave_red_floats(g, P, Cb, vec);
+size_t wave_fixed_bytes(const Geom& g, int64_t P, int64_t Cb, int vec, int64_t H) {
+  const int64_t red = wave_red_floats(g, P, Cb, vec, H);
   const int64_t grp = g.layout == kNHWC ? Cb / g.Cg : 1;
   Geom t = g;
   t.Cb = Cb;
-  const size_t cst = (size_t)wave_cst_floats(t) * 4 * kWaveMaxSlots;  // per-slot constants
+  const size_t cst = (size_t)wave_cst_floats(t) * 4 * kWaveMaxSlots;  // per-piece constants (H + 1 <= max slots)
   const size_t tab = (size_t)2 * P * 4;                                 // piece counts, planes
   return a128((size_t)red * 4) + a128(tab) + a128(cst) + a128((size_t)grp * 8) +
          a128(8 * kWaveMaxSlots);
+}
+
+// Tensor-memory buffers for the reduced pieces of a cut (c.H, 0 when fewer
+// than two fit) and the 16-byte vectors a thread keeps per tensor (c.T4, a
+// multiple of 4).  Thread t of the CTA keeps its vectors -- the ones it reduces
+// in stage A and writes in stage B -- in lane 32*(warp % 4) + t % 32 of
+// every buffer, at column offset (warp / 4) * 4*nten*T4.
+void wave_hold(const Geom& g, WaveCut& c, int nten, int vec) {
+  c.H = c.T4 = 0;
+#if defined(GN_WAVE_TMEM) && GN_WAVE_TMEM == 0
+  return;
+#endif
+  int64_t per;  // vectors per thread and tensor
+  if (g.layout == kNCHW) {
+    per = cdiv(c.R / vec, kWaveThreads);
+  } else {
+    const int64_t wv = c.Cb / vec;
+    if (wv < 1 || wv > kWaveThreads) return;
+    per = cdiv(c.R, kWaveThreads / wv);
+  }
+  const int64_t T4 = rup(std::max<int64_t>(per, 1), 4);
+  const int64_t cols = 4 * nten * T4 * (kWaveThreads / 128);  // columns of one buffer
+  const int64_t H = std::min<int64_t>(kWaveMaxHold, kWaveTmemCols / cols);
+  if (H < 2) return;
+  c.H = H;
+  c.T4 = T4;
 }
 
 // Fills the wave-regime fields of g; false when the problem does not fit.
@@ -450,14 +490,19 @@ bool plan_wave(Geom& g, int op, int sm_count) {
     // every thread polls at most 32 of a unit's records
     if (c.P * (g.layout == kNHWC ? c.Cb : 1) > 32 * (int64_t)kWaveThreads) return;
     if (GN_WAVE_FORCE_CB > 0 && g.layout == kNHWC && c.Cb != GN_WAVE_FORCE_CB) return;
-    const size_t fixed = wave_fixed_bytes(g, c.P, c.Cb, vec);
+    if (GN_WAVE_FORCE_P > 0 && c.P != GN_WAVE_FORCE_P) return;
+    wave_hold(g, c, nten, vec);
+    const size_t fixed = wave_fixed_bytes(g, c.P, c.Cb, vec, c.H);
     if (fixed + 128 + 2 * c.slot > budget) return;
     c.S = std::min<int64_t>(kWaveMaxSlots, (int64_t)((budget - fixed - 128) / c.slot));
     if (c.S < 2) return;
     c.steps = cdiv(units * c.P, NC);
     c.cost = wave_cost(c, NC);
-    // the cheapest cut; at equal cost the one with more slots, then wider rows
-    auto key = [&](const WaveCut& w) { return std::make_tuple(-w.cost, w.S >= kWaveMinSlots, w.Cb); };
+    // the cheapest cut; at equal cost one whose stage A runs ahead, then
+    // the one with more slots, then wider rows
+    auto key = [&](const WaveCut& w) {
+      return std::make_tuple(-w.cost, wave_ahead(w.H, w.S) >= 1, w.S >= kWaveMinSlots, w.Cb);
+    };
     if (best.P == 0 || key(c) > key(best)) best = c;
   };
   if (g.layout == kNCHW) {
@@ -502,6 +547,9 @@ bool plan_wave(Geom& g, int op, int sm_count) {
   r.wR = best.R;
   r.wm = best.m;
   r.S = (int)best.S;
+  r.wH = best.H;
+  r.wT = best.T4;
+  r.wB = best.H > 0 ? best.H + 1 : best.S;  // constants live from stage A to stage B
   if (g.layout == kNHWC) {
     r.Cb = best.Cb;
     r.ncbu = g.C / best.Cb;
@@ -527,13 +575,13 @@ bool plan_wave(Geom& g, int op, int sm_count) {
   size_t off = 0;
   r.off_ring = off;
   off += (size_t)r.S * best.slot;
-  const int64_t red = wave_red_floats(g, r.wP, r.Cb, vec);
+  const int64_t red = wave_red_floats(g, r.wP, r.Cb, vec, r.wH);
   r.off_red = off;
   off += a128((size_t)red * 4);
   r.off_tot = off;  // piece counts (and NCHW planes) of a unit
   off += a128((size_t)2 * r.wP * 4);
-  r.off_xch = off;  // per-slot constants
-  off += a128((size_t)wave_cst_floats(r) * 4 * r.S);
+  r.off_xch = off;  // per-piece constants
+  off += a128((size_t)wave_cst_floats(r) * 4 * r.wB);
   r.off_grp = off;
   off += a128((size_t)(g.layout == kNHWC ? r.Cb / g.Cg : 1) * 8);
   r.off_bar = off;

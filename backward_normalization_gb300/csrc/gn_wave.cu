@@ -177,6 +177,17 @@ __device__ bool gather_records(const float2* src, float2* dst, unsigned todo, un
   }
 }
 
+// Vector u (4 words) of a 16-register tensor-memory transfer.
+__device__ __forceinline__ void put4(uint32_t (&w)[16], int u, const uint4& r) {
+  w[4 * u] = r.x;
+  w[4 * u + 1] = r.y;
+  w[4 * u + 2] = r.z;
+  w[4 * u + 3] = r.w;
+}
+__device__ __forceinline__ uint4 get4(const uint32_t (&w)[16], int u) {
+  return make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+}
+
 // Sum over the 32 lanes of a warp with a fixed xor tree; every lane gets it.
 __device__ __forceinline__ float warp_allsum(float v) {
 #pragma unroll
@@ -238,7 +249,7 @@ __device__ __forceinline__ float piece_count(const Geom& g, int t) {
   return (float)((a + g.wR < g.HW) ? g.wR : g.HW - a);
 }
 
-template <typename T, int VW, int LAYOUT, bool BWD>
+template <typename T, int VW, int LAYOUT, bool BWD, bool HOLD>
 __global__ void __launch_bounds__(kWaveThreads, kWaveCtasPerSm) wave_kernel(const __grid_constant__ KParams p) {
   extern __shared__ __align__(128) char smem_raw[];
   char* smem =
@@ -252,6 +263,7 @@ __global__ void __launch_bounds__(kWaveThreads, kWaveCtasPerSm) wave_kernel(cons
   float2* grp = reinterpret_cast<float2*>(smem + g.off_grp);  // per-group results of the unit
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + g.off_bar);
   __shared__ int s_ok;
+  __shared__ uint32_t s_tmem;  // HOLD: base address of the CTA's tensor memory
 
   const int NC = gridDim.x, b = blockIdx.x;
   const int P = (int)g.wP;
@@ -261,10 +273,16 @@ __global__ void __launch_bounds__(kWaveThreads, kWaveCtasPerSm) wave_kernel(cons
   const int nch = LAYOUT == kNHWC ? (int)g.Cb : 1;  // channels of a piece
   const int Cg = (int)g.Cg;
   const int rec_unit = P * nch;  // records of a unit
+  const int H = HOLD ? (int)g.wH : 0;  // tensor-memory buffers
+  // stage A runs `ahead` pieces before stage B: with tensor-memory buffers
+  // one less than their number, else one when a third slot is free to land
+  const int ahead = HOLD ? H - 1 : (S >= 3 ? 1 : 0);
+  const int NCB = (int)g.wB;            // buffers of per-piece constants
+  const int NRB = HOLD && H > 2 ? H : 2;  // P == 1: buffers of the CTA's own records
   // shared scratch: the unit's records (P > 1: gathered; P == 1: the CTA's
-  // own, two pieces' worth), then the CTA sums
+  // own, NRB pieces' worth), then the CTA sums
   float2* recs = reinterpret_cast<float2*>(red);
-  float* cred = red + 2 * (P > 1 ? rec_unit : 2 * nch);
+  float* cred = red + 2 * (P > 1 ? rec_unit : NRB * nch);
   const size_t slot_bytes = (size_t)g.ten_stride * NTEN;
   const T* x = static_cast<const T*>(p.x);
   const T* dy = static_cast<const T*>(p.dy);
@@ -274,7 +292,12 @@ __global__ void __launch_bounds__(kWaveThreads, kWaveCtasPerSm) wave_kernel(cons
     for (int i = 0; i < S; ++i) mbar_init(full + i, 1);
     fence_mbar_init();
   }
+  if (HOLD) {
+    if (warp == 0) tmem_alloc(&s_tmem, kWaveTmemCols);
+    tmem_fence_before();
+  }
   __syncthreads();
+  if (HOLD) tmem_fence_after();
   grid_dependency_wait();  // earlier work on the stream (the inputs, the workspace) is done
   grid_launch_dependents();
 
@@ -348,7 +371,7 @@ __global__ void __launch_bounds__(kWaveThreads, kWaveCtasPerSm) wave_kernel(cons
   auto fetch_constants = [&](int k) {
     if (k < K) {
       const Piece pc = piece_of<LAYOUT>(g, k * NC + b);
-      float* cs = cstb + (k % S) * CST;
+      float* cs = cstb + (k % NCB) * CST;
       if (LAYOUT == kNHWC) {
         for (int c = tid; c < nch; c += nt) {
           if (p.gamma) cp_async4(cs + c, p.gamma + pc.cbase + c);
@@ -390,22 +413,30 @@ __global__ void __launch_bounds__(kWaveThreads, kWaveCtasPerSm) wave_kernel(cons
   // stage B (when stage A runs ahead): raw words land in registers while the
   // stage works, and are decoded into shared memory at its end
   constexpr int kPre = 8;  // records per thread read ahead (at most)
-  const bool read_ahead = P > 1 && S >= 3 && rec_unit <= kPre * nt;
+  const bool read_ahead = P > 1 && ahead >= 1 && rec_unit <= kPre * nt;
   unsigned long long pre[kPre];
   int pre_unit = -1;       // the unit whose records sit in `recs`, or -1
   unsigned pre_todo = 0;   // of those, the ones not yet written
+
+  // ---- HOLD: thread t keeps the vectors it reduces in stage A (and writes
+  // in stage B) in tensor-memory lane 32*(warp % 4) + t % 32, T4 vectors of
+  // x then T4 of dy from column (warp / 4) * tcols of the piece's buffer
+  const int T4 = HOLD ? (int)g.wT : 0;
+  const uint32_t tcols = 4u * NTEN * (uint32_t)T4;
+  const uint32_t bcols = tcols * (uint32_t)(nt / 128);
+  const uint32_t tthr = HOLD ? s_tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(warp >> 2) * tcols : 0u;
 
   // ---- stage A of piece k: wait for its copy, reduce it, publish its records
   auto stage_a = [&](int k) -> bool {
     const Piece pc = piece_of<LAYOUT>(g, k * NC + b);
     const int si = k % S;
     const char* slot = ring + (size_t)si * slot_bytes;
-    const float* cs = cstb + si * CST;
+    const float* cs = cstb + (k % NCB) * CST;
     const uint32_t parity = (uint32_t)((k / S) & 1);
     cp_async_wait_all();    // this piece's constants (fetched one step ago)
     fetch_constants(k + 1);  // and the next piece's, for the next step
-    // the records of the unit of the stage B that follows (piece k - 1)
-    const int pre_k = k - 1;
+    // the records of the unit of the stage B that follows (piece k - ahead)
+    const int pre_k = k - ahead;
     const int pre_u = read_ahead && pre_k >= 0 ? piece_of<LAYOUT>(g, pre_k * NC + b).u : -1;
     if (pre_u >= 0) {
       const float2* src = p.part + (int64_t)pre_u * rec_unit;
@@ -421,20 +452,19 @@ __global__ void __launch_bounds__(kWaveThreads, kWaveCtasPerSm) wave_kernel(cons
     if (!s_ok) return false;
     mbar_try_wait(full + si, parity);  // completed: orders this thread's reads after the copy
     float2* rec_g = p.part + (int64_t)pc.u * rec_unit + pc.t * nch;
-    float2* rec_s = recs + (k & 1) * nch;  // P == 1: kept in shared memory
+    float2* rec_s = recs + (k % NRB) * nch;  // P == 1: kept in shared memory
     const bool publish = !(p.stall_unit == pc.u && pc.t == 0);  // fault injection
     if (LAYOUT == kNCHW) {
       const float mu = BWD ? cs[Cg] : 0.f;
       const float K0 = BWD ? 0.f : Elem<T>::to_f(reinterpret_cast<const T*>(slot)[0]);
       float a = 0.f, c = 0.f;
       const int nv = pc.len / VW;
-#pragma unroll 4
-      for (int v = tid; v < nv; v += nt) {
+      auto add = [&](const uint4& rx, const uint4& rd) {
         float xv[VW];
-        Access<T, VW>::unpack(lds16(slot + (size_t)v * 16), xv);
+        Access<T, VW>::unpack(rx, xv);
         if (BWD) {
           float dv[VW];
-          Access<T, VW>::unpack(lds16(slot + g.ten_stride + (size_t)v * 16), dv);
+          Access<T, VW>::unpack(rd, dv);
 #pragma unroll
           for (int e = 0; e < VW; ++e) {
             a += dv[e];
@@ -448,6 +478,33 @@ __global__ void __launch_bounds__(kWaveThreads, kWaveCtasPerSm) wave_kernel(cons
             c = fmaf(d, d, c);
           }
         }
+      };
+      if constexpr (HOLD) {
+        // vectors tid + i*nt, i < T4, also go to tensor memory (zeros past the piece)
+        const uint32_t tb = tthr + (uint32_t)(k % H) * bcols;
+        for (int i0 = 0; i0 < T4; i0 += 4) {
+          uint32_t wx[16], wd[16];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int v = tid + (i0 + u) * nt;
+            uint4 rx = make_uint4(0u, 0u, 0u, 0u), rd = rx;
+            if (v < nv) {
+              rx = lds16(slot + (size_t)v * 16);
+              if (BWD) rd = lds16(slot + g.ten_stride + (size_t)v * 16);
+              add(rx, rd);
+            }
+            put4(wx, u, rx);
+            if (BWD) put4(wd, u, rd);
+          }
+          tmem_st16(tb + 4u * (uint32_t)i0, wx);
+          if (BWD) tmem_st16(tb + 4u * (uint32_t)(T4 + i0), wd);
+        }
+        tmem_wait_st();
+      } else {
+#pragma unroll 4
+        for (int v = tid; v < nv; v += nt)
+          add(lds16(slot + (size_t)v * 16),
+              BWD ? lds16(slot + g.ten_stride + (size_t)v * 16) : make_uint4(0u, 0u, 0u, 0u));
       }
       const float2 s2 = block_sum2_t0(a, c, cred);
       if (tid == 0) {
@@ -462,39 +519,67 @@ __global__ void __launch_bounds__(kWaveThreads, kWaveCtasPerSm) wave_kernel(cons
         else if (publish) put_rec(rec_g, r);
       }
     } else {
-      float acc[2 * VW], Ks[VW];
+      float acc[2 * VW], Ks[VW], mu[VW];
 #pragma unroll
       for (int q = 0; q < 2 * VW; ++q) acc[q] = 0.f;
+#pragma unroll
+      for (int e = 0; e < VW; ++e) Ks[e] = mu[e] = 0.f;
       if (lane_ok) {
-        float mu[VW];
         if (BWD) {
 #pragma unroll
           for (int e = 0; e < VW; ++e) mu[e] = cs[nch + qe[e]];
         } else {
           Access<T, VW>::unpack(lds16(slot + j * 16), Ks);  // the piece's first row: the shift
         }
-        const char* col = slot + j * 16;
-#pragma unroll 2
-        for (int r = rl; r < pc.len; r += rpi) {
-          float xv[VW];
-          Access<T, VW>::unpack(lds16(col + (size_t)r * rowb), xv);
-          if (BWD) {
-            float dv[VW];
-            Access<T, VW>::unpack(lds16(col + g.ten_stride + (size_t)r * rowb), dv);
+      }
+      const char* col = slot + j * 16;
+      auto add = [&](const uint4& rx, const uint4& rd) {
+        float xv[VW];
+        Access<T, VW>::unpack(rx, xv);
+        if (BWD) {
+          float dv[VW];
+          Access<T, VW>::unpack(rd, dv);
 #pragma unroll
-            for (int e = 0; e < VW; ++e) {
-              acc[2 * e] += dv[e];
-              acc[2 * e + 1] = fmaf(dv[e], xv[e] - mu[e], acc[2 * e + 1]);
-            }
-          } else {
+          for (int e = 0; e < VW; ++e) {
+            acc[2 * e] += dv[e];
+            acc[2 * e + 1] = fmaf(dv[e], xv[e] - mu[e], acc[2 * e + 1]);
+          }
+        } else {
 #pragma unroll
-            for (int e = 0; e < VW; ++e) {
-              const float d = xv[e] - Ks[e];
-              acc[2 * e] += d;
-              acc[2 * e + 1] = fmaf(d, d, acc[2 * e + 1]);
-            }
+          for (int e = 0; e < VW; ++e) {
+            const float d = xv[e] - Ks[e];
+            acc[2 * e] += d;
+            acc[2 * e + 1] = fmaf(d, d, acc[2 * e + 1]);
           }
         }
+      };
+      if constexpr (HOLD) {
+        // rows rl + i*rpi, i < T4, of column j also go to tensor memory
+        // (zeros past the piece, and for threads without a column)
+        const uint32_t tb = tthr + (uint32_t)(k % H) * bcols;
+        for (int i0 = 0; i0 < T4; i0 += 4) {
+          uint32_t wx[16], wd[16];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int r = rl + (i0 + u) * rpi;
+            uint4 rx = make_uint4(0u, 0u, 0u, 0u), rd = rx;
+            if (lane_ok && r < pc.len) {
+              rx = lds16(col + (size_t)r * rowb);
+              if (BWD) rd = lds16(col + g.ten_stride + (size_t)r * rowb);
+              add(rx, rd);
+            }
+            put4(wx, u, rx);
+            if (BWD) put4(wd, u, rd);
+          }
+          tmem_st16(tb + 4u * (uint32_t)i0, wx);
+          if (BWD) tmem_st16(tb + 4u * (uint32_t)(T4 + i0), wd);
+        }
+        tmem_wait_st();
+      } else if (lane_ok) {
+#pragma unroll 2
+        for (int r = rl; r < pc.len; r += rpi)
+          add(lds16(col + (size_t)r * rowb),
+              BWD ? lds16(col + g.ten_stride + (size_t)r * rowb) : make_uint4(0u, 0u, 0u, 0u));
       }
       // CTA sums: each of the 2*nch sums (value q of column jj) is taken by
       // tps lanes of one warp; lane l adds row lanes l, l + tps, ... into four
@@ -568,9 +653,9 @@ __global__ void __launch_bounds__(kWaveThreads, kWaveCtasPerSm) wave_kernel(cons
   // polled until they are), the group statistics, the piece's output
   auto stage_b = [&](int k) -> bool {
     const Piece pc = piece_of<LAYOUT>(g, k * NC + b);
-    const char* slot = ring + (size_t)(k % S) * slot_bytes;
-    const float* cs = cstb + (k % S) * CST;
-    const float2* R = recs + (k & 1) * nch;
+    const char* slot = ring + (size_t)(k % S) * slot_bytes;  // without HOLD the piece is still there
+    const float* cs = cstb + (k % NCB) * CST;
+    const float2* R = recs + (k % NRB) * nch;
     if (P > 1) {
       const unsigned todo = pre_unit == pc.u ? pre_todo : record_mask(rec_unit);
       pre_unit = -1;
@@ -644,7 +729,7 @@ __global__ void __launch_bounds__(kWaveThreads, kWaveCtasPerSm) wave_kernel(cons
         p.rstd[gbase + q] = grp[q].y;
       }
 
-    // ---- the piece's output, from shared memory
+    // ---- the piece's output, from tensor memory (HOLD) or its slot
     if (LAYOUT == kNCHW) {
       float ca, cb, cm, cd;
       const float gm = cs[pc.c - pc.gi * Cg];
@@ -661,13 +746,12 @@ __global__ void __launch_bounds__(kWaveThreads, kWaveCtasPerSm) wave_kernel(cons
       }
       const int nv = pc.len / VW;
       T* o = out + pc.e0;
-#pragma unroll 4
-      for (int v = tid; v < nv; v += nt) {
+      auto put = [&](int v, const uint4& rx, const uint4& rd) {
         float xv[VW];
-        Access<T, VW>::unpack(lds16(slot + (size_t)v * 16), xv);
+        Access<T, VW>::unpack(rx, xv);
         if (BWD) {
           float dv[VW];
-          Access<T, VW>::unpack(lds16(slot + g.ten_stride + (size_t)v * 16), dv);
+          Access<T, VW>::unpack(rd, dv);
 #pragma unroll
           for (int e = 0; e < VW; ++e) xv[e] = fmaf(ca, dv[e], fmaf(cb, xv[e] - cm, cd));
         } else {
@@ -675,8 +759,30 @@ __global__ void __launch_bounds__(kWaveThreads, kWaveCtasPerSm) wave_kernel(cons
           for (int e = 0; e < VW; ++e) xv[e] = fmaf(xv[e] - cm, ca, cb);
         }
         Access<T, VW>::store(o + (int64_t)v * VW, xv, pol_out);
+      };
+      if constexpr (HOLD) {
+        const uint32_t tb = tthr + (uint32_t)(k % H) * bcols;
+        for (int i0 = 0; i0 < T4; i0 += 4) {
+          uint32_t wx[16], wd[16];
+          tmem_ld16(tb + 4u * (uint32_t)i0, wx);
+          if constexpr (BWD) tmem_ld16(tb + 4u * (uint32_t)(T4 + i0), wd);
+          tmem_wait_ld();
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int v = tid + (i0 + u) * nt;
+            if (v < nv) {
+              if constexpr (BWD) put(v, get4(wx, u), get4(wd, u));
+              else put(v, get4(wx, u), get4(wx, u));
+            }
+          }
+        }
+      } else {
+#pragma unroll 4
+        for (int v = tid; v < nv; v += nt)
+          put(v, lds16(slot + (size_t)v * 16),
+              BWD ? lds16(slot + g.ten_stride + (size_t)v * 16) : make_uint4(0u, 0u, 0u, 0u));
       }
-    } else if (lane_ok) {
+    } else {
       float ca[VW], cb[VW], cm[VW], cd[VW];
 #pragma unroll
       for (int e = 0; e < VW; ++e) {
@@ -697,13 +803,12 @@ __global__ void __launch_bounds__(kWaveThreads, kWaveCtasPerSm) wave_kernel(cons
       }
       T* o = out + pc.row0 * g.C + pc.cbase + j * VW;
       const char* col = slot + j * 16;
-#pragma unroll 2
-      for (int r = rl; r < pc.len; r += rpi) {
+      auto put = [&](int r, const uint4& rx, const uint4& rd) {
         float xv[VW];
-        Access<T, VW>::unpack(lds16(col + (size_t)r * rowb), xv);
+        Access<T, VW>::unpack(rx, xv);
         if (BWD) {
           float dv[VW];
-          Access<T, VW>::unpack(lds16(col + g.ten_stride + (size_t)r * rowb), dv);
+          Access<T, VW>::unpack(rd, dv);
 #pragma unroll
           for (int e = 0; e < VW; ++e) xv[e] = fmaf(ca[e], dv[e], fmaf(cb[e], xv[e] - cm[e], cd[e]));
         } else {
@@ -711,36 +816,65 @@ __global__ void __launch_bounds__(kWaveThreads, kWaveCtasPerSm) wave_kernel(cons
           for (int e = 0; e < VW; ++e) xv[e] = fmaf(xv[e] - cm[e], ca[e], cb[e]);
         }
         Access<T, VW>::store(o + (int64_t)r * g.C, xv, pol_out);
+      };
+      if constexpr (HOLD) {
+        const uint32_t tb = tthr + (uint32_t)(k % H) * bcols;
+        for (int i0 = 0; i0 < T4; i0 += 4) {
+          uint32_t wx[16], wd[16];
+          tmem_ld16(tb + 4u * (uint32_t)i0, wx);
+          if constexpr (BWD) tmem_ld16(tb + 4u * (uint32_t)(T4 + i0), wd);
+          tmem_wait_ld();
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int r = rl + (i0 + u) * rpi;
+            if (lane_ok && r < pc.len) {
+              if constexpr (BWD) put(r, get4(wx, u), get4(wd, u));
+              else put(r, get4(wx, u), get4(wx, u));
+            }
+          }
+        }
+      } else if (lane_ok) {
+#pragma unroll 2
+        for (int r = rl; r < pc.len; r += rpi)
+          put(r, lds16(col + (size_t)r * rowb),
+              BWD ? lds16(col + g.ten_stride + (size_t)r * rowb) : make_uint4(0u, 0u, 0u, 0u));
       }
     }
     __syncthreads();  // the slot's reads are done; the scratch is free
     return true;
   };
 
-  // ---- the pipeline.  With three or more slots, stage A runs one piece
-  // ahead of stage B: by the time a CTA needs a unit's records, every CTA
-  // has had a whole step to publish them.  After stage B of piece k its slot
-  // takes the copy of piece k + S.
-  const int ahead = S >= 3 ? 1 : 0;
+  // ---- the pipeline.  Stage A runs `ahead` pieces before stage B: by the
+  // time a CTA needs a unit's records, every CTA has had `ahead` steps to
+  // publish them.  A slot takes its next copy (piece k + S) once piece k is
+  // done with it: after stage A with HOLD (the piece waits in tensor
+  // memory), after stage B without.
+  auto issue_next = [&]() {
+    if (tid == 0 && issued < K) {
+      fence_proxy_async_smem();  // the slot's generic reads precede the new copy
+      issue(issued);
+      ++issued;
+    }
+  };
   int ka = 0;  // pieces through stage A
   bool ok = true;
-  for (; ok && ka <= ahead && ka < K; ++ka) ok = stage_a(ka);
+  for (; ok && ka <= ahead && ka < K; ++ka) {
+    ok = stage_a(ka);
+    if (ok && HOLD) issue_next();
+  }
   if (!ok) --ka;  // that piece's copy may still be in flight
   for (int k = 0; ok && k < K; ++k) {
     if (!stage_b(k)) {
       ok = false;
       break;
     }
-    if (tid == 0 && issued < K) {
-      fence_proxy_async_smem();  // the slot's generic reads precede the new copy
-      issue(issued);
-      ++issued;
-    }
+    if (!HOLD) issue_next();
     if (ka < K) {
       if (!stage_a(ka)) {
         ok = false;
         break;
       }
+      if (HOLD) issue_next();
       ++ka;
     }
   }
@@ -749,6 +883,14 @@ __global__ void __launch_bounds__(kWaveThreads, kWaveCtasPerSm) wave_kernel(cons
   if (!ok && tid == 0)
     for (int i = ka; i < issued; ++i) wait_bar_t0(full + (i % S), (uint32_t)((i / S) & 1), p.err);
   cp_async_wait_all();  // no asynchronous copy into shared memory outlives the CTA
+  if (HOLD) {  // every thread's tensor-memory accesses have completed (waited for)
+    tmem_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+      tmem_fence_after();
+      tmem_dealloc(s_tmem, kWaveTmemCols);
+    }
+  }
 
   // ---- backward: dgamma / dbeta once every unit's per-channel sums are in
   // the workspace (a grid barrier, which every CTA reaches), spread over the
@@ -790,25 +932,26 @@ __global__ void __launch_bounds__(kWaveThreads, kWaveCtasPerSm) wave_kernel(cons
 }
 
 template <typename T, int VW, int LAYOUT, bool BWD>
-const void* kernel_ptr() {
-  return (const void*)wave_kernel<T, VW, LAYOUT, BWD>;
+const void* kernel_ptr(bool hold) {
+  return hold ? (const void*)wave_kernel<T, VW, LAYOUT, BWD, true>
+              : (const void*)wave_kernel<T, VW, LAYOUT, BWD, false>;
 }
 
 template <typename T>
-const void* pick(int layout, bool bwd) {
+const void* pick(int layout, bool bwd, bool hold) {
   constexpr int V = Elem<T>::VEC;
   if (layout == kNCHW)
-    return bwd ? kernel_ptr<T, V, kNCHW, true>() : kernel_ptr<T, V, kNCHW, false>();
-  return bwd ? kernel_ptr<T, V, kNHWC, true>() : kernel_ptr<T, V, kNHWC, false>();
+    return bwd ? kernel_ptr<T, V, kNCHW, true>(hold) : kernel_ptr<T, V, kNCHW, false>(hold);
+  return bwd ? kernel_ptr<T, V, kNHWC, true>(hold) : kernel_ptr<T, V, kNHWC, false>(hold);
 }
 
 }  // namespace
 
 const void* wave_kernel_ptr(const Geom& g, bool bwd) {
   switch (g.dtype) {
-    case kF32: return pick<float>(g.layout, bwd);
-    case kF16: return pick<__half>(g.layout, bwd);
-    default: return pick<__nv_bfloat16>(g.layout, bwd);
+    case kF32: return pick<float>(g.layout, bwd, g.wH > 0);
+    case kF16: return pick<__half>(g.layout, bwd, g.wH > 0);
+    default: return pick<__nv_bfloat16>(g.layout, bwd, g.wH > 0);
   }
 }
 

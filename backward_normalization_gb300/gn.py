@@ -43,7 +43,8 @@ class PlanDesc(ctypes.Structure):
                 ("max_clusters", ctypes.c_int), ("smem_bytes", ctypes.c_size_t),
                 ("err_offset", ctypes.c_size_t), ("finalise_second", ctypes.c_int),
                 ("level1_items", ctypes.c_int), ("clear_bytes", ctypes.c_size_t),
-                ("piece_elems", ctypes.c_int64), ("pieces_per_unit", ctypes.c_int64)]
+                ("piece_elems", ctypes.c_int64), ("pieces_per_unit", ctypes.c_int64),
+                ("slots", ctypes.c_int), ("hold_buffers", ctypes.c_int)]
 
 
 _lib = None

@@ -285,6 +285,9 @@ typedef struct gn_plan_desc {
                             counters) that the call zero-fills before its kernels */
   int64_t piece_elems;   /* wave regime: elements (NCHW) or rows (NHWC) per piece */
   int64_t pieces_per_unit; /* wave regime: pieces of one reduction unit */
+  int slots;             /* resident / pipelined / wave regimes: shared-memory slots per CTA */
+  int hold_buffers;      /* wave regime: tensor-memory buffers holding reduced pieces
+                            (0: a piece waits for its unit's statistics in its slot) */
 } gn_plan_desc;
 
 /* Fills *out with the plan of gn_fwd/gn_bwd for this problem, assuming every
