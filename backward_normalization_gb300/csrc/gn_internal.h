@@ -108,8 +108,9 @@ struct Geom {
   // piece waits for its unit's statistics in one of wH tensor-memory
   // buffers (wT 16-byte vectors per thread and tensor), which frees its slot
   // for the next copy at once; wH = 0: it waits in its slot.  wB buffers of
-  // per-piece constants.
-  int64_t wP, wR, wm, wnb, wcols, wH, wT, wB;
+  // per-piece constants.  wWs = 1: stage A and stage B run on separate halves
+  // of the CTA (warp specialisation), handing pieces over through mbarriers.
+  int64_t wP, wR, wm, wnb, wcols, wH, wT, wB, wWs;
 };
 
 // Bytes reserved per ring-slot header of the pipelined kernel (the header
@@ -254,6 +255,12 @@ __host__ __device__ inline int wave_cst_floats(const Geom& g) {
 #endif
 constexpr int kWaveThreads = GN_WAVE_THREADS;
 constexpr int kWaveCtasPerSm = GN_WAVE_CTAS_PER_SM;
+// Wave plans that hold pieces in tensor memory run stage A and stage B on
+// separate halves of the CTA (1) or both on the whole CTA in turn (0).
+#ifndef GN_WAVE_WS
+#define GN_WAVE_WS 1
+#endif
+constexpr bool kWaveWs = GN_WAVE_WS != 0;
 // Tensor-memory columns one wave CTA allocates (its share of the SM's 512).
 constexpr int kWaveTmemCols = 512 / GN_WAVE_CTAS_PER_SM;
 static_assert(kWaveTmemCols >= 32 && (kWaveTmemCols & (kWaveTmemCols - 1)) == 0,

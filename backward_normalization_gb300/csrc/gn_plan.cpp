@@ -112,18 +112,19 @@ bool resident_preferred(const Geom& g, int op) {
 }
 
 // The automatic choice of the wave regime (where its plan fits), from
-// measurements on GB300: it reads each input once, but every step of its
-// CTAs runs a chain of short barrier-separated phases (wait, reduce, publish,
-// gather, merge, write) that a 55 KB piece does not hide.  It wins where the
-// op's second read costs most and the units are large: the NCHW backward with
-// units of at least 4 MiB (fp32 112x64x512x512 G8: 4.52 ms with pieces held in
-// tensor memory, against 5.22-5.27 ms two-kernel); the NCHW forward (3.9-4.2
-// against 3.2 ms) and the small channels-last workloads (bf16 8x320x64x64
-// G32: 41-44 / 52-55 us against 29 / 38-40 us; bf16 32x512x32x32 G32: 47-53 /
-// 61-68 against 32 / 38 us) stay with the other families.
+// measurements on GB300.  It reads each input once; with its pieces held in
+// tensor memory and stage A and stage B on separate warps, it wins for NCHW
+// problems whose units are large: fp32 112x64x512x512 G8, 8 MiB units, runs
+// the forward in 2.67 ms and the backward in 4.36 ms against 3.21 / 5.28 ms
+// two-kernel.  The small channels-last workloads stay with the other
+// families (bf16 8x320x64x64 G32: 50 / 55 us against 29 / 38 us; bf16
+// 32x512x32x32 G32: 38 / 53 us against 32 / 38 us): with a handful of steps
+// per CTA the cooperative launch and the pipeline's fill cost more than the
+// second read they save.
 bool wave_preferred(const Geom& g, int op) {
+  (void)op;
   const int esz = dtype_size(g.dtype);
-  return g.layout == kNCHW && op == kBwd && g.Cg * g.HW * esz >= (4ll << 20);
+  return g.layout == kNCHW && g.Cg * g.HW * esz >= (4ll << 20);
 }
 
 // Input that counts as tiny for the automatic choice (see plan_resident).
@@ -447,29 +448,34 @@ size_t wave_fixed_bytes(const Geom& g, int64_t P, int64_t Cb, int vec, int64_t H
   const size_t cst = (size_t)wave_cst_floats(t) * 4 * kWaveMaxSlots;  // per-piece constants (H + 1 <= max slots)
   const size_t tab = (size_t)2 * P * 4;                                 // piece counts, planes
   return a128((size_t)red * 4) + a128(tab) + a128(cst) + a128((size_t)grp * 8) +
-         a128(8 * kWaveMaxSlots);
+         a128(8 * (kWaveMaxSlots + 2 * kWaveMaxHold));
 }
+
+// Threads of one stage of a wave CTA: half of it with warp specialisation.
+int64_t wave_stage_threads(bool ws) { return ws ? kWaveThreads / 2 : kWaveThreads; }
 
 // Tensor-memory buffers for the reduced pieces of a cut (c.H, 0 when fewer
 // than two fit) and the 16-byte vectors a thread keeps per tensor (c.T4, a
-// multiple of 4).  Thread t of the CTA keeps its vectors -- the ones it reduces
-// in stage A and writes in stage B -- in lane 32*(warp % 4) + t % 32 of
-// every buffer, at column offset (warp / 4) * 4*nten*T4.
+// multiple of 4).  Thread t of a stage keeps its vectors -- the ones it
+// reduces in stage A and writes in stage B -- in lane 32*(warp % 4) + t % 32
+// of every buffer; without warp specialisation warps w and w + 4 share a lane,
+// at column offsets 0 and 4*nten*T4.
 void wave_hold(const Geom& g, WaveCut& c, int nten, int vec) {
   c.H = c.T4 = 0;
 #if defined(GN_WAVE_TMEM) && GN_WAVE_TMEM == 0
   return;
 #endif
+  const int64_t nthr = wave_stage_threads(kWaveWs);
   int64_t per;  // vectors per thread and tensor
   if (g.layout == kNCHW) {
-    per = cdiv(c.R / vec, kWaveThreads);
+    per = cdiv(c.R / vec, nthr);
   } else {
     const int64_t wv = c.Cb / vec;
-    if (wv < 1 || wv > kWaveThreads) return;
-    per = cdiv(c.R, kWaveThreads / wv);
+    if (wv < 1 || wv > nthr) return;
+    per = cdiv(c.R, nthr / wv);
   }
   const int64_t T4 = rup(std::max<int64_t>(per, 1), 4);
-  const int64_t cols = 4 * nten * T4 * (kWaveThreads / 128);  // columns of one buffer
+  const int64_t cols = 4 * nten * T4 * (nthr / 128);  // columns of one buffer
   const int64_t H = std::min<int64_t>(kWaveMaxHold, kWaveTmemCols / cols);
   if (H < 2) return;
   c.H = H;
@@ -487,8 +493,8 @@ bool plan_wave(Geom& g, int op, int sm_count) {
   WaveCut best;
   auto consider = [&](WaveCut c, int64_t units) {
     if (c.P < 1 || c.P > NC) return;
-    // every thread polls at most 32 of a unit's records
-    if (c.P * (g.layout == kNHWC ? c.Cb : 1) > 32 * (int64_t)kWaveThreads) return;
+    // every thread of stage B polls at most 32 of a unit's records
+    if (c.P * (g.layout == kNHWC ? c.Cb : 1) > 32 * wave_stage_threads(kWaveWs)) return;
     if (GN_WAVE_FORCE_CB > 0 && g.layout == kNHWC && c.Cb != GN_WAVE_FORCE_CB) return;
     if (GN_WAVE_FORCE_P > 0 && c.P != GN_WAVE_FORCE_P) return;
     wave_hold(g, c, nten, vec);
@@ -550,6 +556,7 @@ bool plan_wave(Geom& g, int op, int sm_count) {
   r.wH = best.H;
   r.wT = best.T4;
   r.wB = best.H > 0 ? best.H + 1 : best.S;  // constants live from stage A to stage B
+  r.wWs = best.H > 0 && kWaveWs ? 1 : 0;
   if (g.layout == kNHWC) {
     r.Cb = best.Cb;
     r.ncbu = g.C / best.Cb;
@@ -584,9 +591,13 @@ bool plan_wave(Geom& g, int op, int sm_count) {
   off += a128((size_t)wave_cst_floats(r) * 4 * r.wB);
   r.off_grp = off;
   off += a128((size_t)(g.layout == kNHWC ? r.Cb / g.Cg : 1) * 8);
-  r.off_bar = off;
-  off += a128(8 * (size_t)r.S);
+  r.off_bar = off;  // slots' mbarriers, then (warp specialisation) the hold buffers' full and empty ones
+  off += a128(8 * (size_t)(r.S + 2 * r.wH));
   r.smem = off + 128;  // slack for aligning the dynamic shared memory base
+  // a CTA that allocates tensor memory takes more than half of an SM's shared
+  // memory, so that no other CTA of the kernel can share its SM (and wait
+  // there for the columns it holds)
+  if (r.wH > 0) r.smem = std::max<size_t>(r.smem, kSmemPerSm / (kWaveCtasPerSm + 1) + 1024);
   if (r.smem > budget) return false;
   const int64_t nc = wave_ctas(r, op, r.smem, sm_count, kWaveCtasPerSm);
   if (nc < r.wP) return false;  // a unit's pieces must be co-resident

@@ -17,10 +17,22 @@
 // record per channel to the workspace; stage B reads every record of the
 // piece's unit (polling until all are written, bounded), merges them in a
 // fixed order into the group statistics (forward) or the dx coefficients
-// (backward), and writes the piece's output from shared memory.  With three
-// or more slots stage A runs one piece ahead of stage B, so a unit's records
-// are normally all written when a CTA reaches it.  x (and dy) are read from
-// HBM once.
+// (backward), and writes the piece's output.  x (and dy) are read from HBM
+// once.
+//
+// Where the plan allows (wH > 0), a reduced piece waits for its unit's
+// statistics in tensor memory rather than in its slot: in stage A every
+// thread also stores the 16-byte vectors it reduces into its own lane of one
+// of wH hold buffers (tcgen05.st), and stage B reads them back (tcgen05.ld),
+// so the slot takes its next copy as soon as stage A is done with it.  Stage
+// A then runs on warps 0-3 and stage B on warps 4-7 at the same time (warp
+// specialisation; thread t of either stage owns lane 32*(warp % 4) + t % 32):
+// the reduce of one piece (shared-memory reads, tensor-memory writes)
+// overlaps the output of an earlier one (tensor-memory reads, global
+// stores).  Per hold buffer an mbarrier `tm_full` tells stage B that a piece
+// is in, and `tm_empty` tells stage A that it has been written out.  Without
+// hold buffers the CTA runs the stages in turn, stage A one piece ahead of
+// stage B when a third slot is free, and the piece waits in its slot.
 //
 // Records are self-validating 64-bit words (a cleared word is zero, a written
 // one never is), written and polled with single relaxed accesses: no
@@ -29,12 +41,13 @@
 //
 // A CTA waits for other CTAs' pieces, so all CTAs must be co-resident: the
 // kernel is launched cooperatively.  Deadlock-freedom: a CTA publishes its
-// piece of step k before it waits for that piece's unit.  Take the smallest
-// unit u that some CTA waits for.  Every owner of a piece of u has published
-// it, or is still in an earlier step, whose piece has a smaller index and so
-// belongs to a unit smaller than u (an owner holds at most one piece of a
-// unit, since P <= NC); by the minimality of u those steps complete, so every
-// piece of u is published.
+// piece of step k before it waits for that piece's unit, and stage A of step
+// k waits only for copies and for the stage B of an earlier step of its own
+// CTA.  Take the smallest unit u that some CTA waits for.  Every owner of a
+// piece of u has published it, or is still in an earlier step, whose piece
+// has a smaller index and so belongs to a unit smaller than u (an owner holds
+// at most one piece of a unit, since P <= NC); by the minimality of u those
+// steps complete, so every piece of u is published.
 //
 // The workspace holds anything when the call starts: CTA 0 zero-fills the
 // error word, every CTA the record slots of its own pieces, and a grid-wide
@@ -129,22 +142,90 @@ __device__ __forceinline__ float2 rec_decode(unsigned long long w) {
                      __uint_as_float((unsigned)(w >> 32) ^ kWaveKey));
 }
 
-// This thread's share of a unit's n records: records tid + i*blockDim.x,
-// bit i of the mask for each (a thread holds at most 32: n <= 32*blockDim.x).
-__device__ __forceinline__ unsigned record_mask(int n) {
-  const int tid = threadIdx.x, nt = blockDim.x;
+// The threads that run one stage of the kernel: the whole CTA (barrier 0,
+// __syncthreads), or with warp specialisation one half of it on its own
+// named barrier.  t is this thread's index in the group, n the group's size.
+struct Group {
+  int id, n, t;
+  __device__ __forceinline__ void sync() const {
+    if (id == 0) __syncthreads();
+    else named_sync(id, n);
+  }
+  __device__ __forceinline__ bool sync_or(bool c) const {
+    if (id == 0) return __syncthreads_or(c) != 0;
+    return named_sync_or(id, n, c);
+  }
+};
+
+// This thread's share of a unit's n records: records t + i*gr.n, bit i of
+// the mask for each (a thread holds at most 32: n <= 32*gr.n).
+__device__ __forceinline__ unsigned record_mask(int n, const Group& gr) {
   unsigned todo = 0;
-  for (int i = 0; i < 32 && tid + i * nt < n; ++i) todo |= 1u << i;
+  for (int i = 0; i < 32 && gr.t + i * gr.n < n; ++i) todo |= 1u << i;
   return todo;
 }
 
-// Every thread: reads the records at src still marked in `todo` into dst
-// (shared memory), polling until all of them are written.  Bounded in time
-// (thread 0 keeps the clock); returns false, uniformly, when the bound runs
-// out or the error word is raised.
+// Sums of two values over a group with a fixed tree (shuffles within warps,
+// then the warp results in warp order); the totals land in the group's
+// thread 0.  `scratch` holds 2 floats per warp of the group.
+__device__ __forceinline__ float2 group_sum2_t0(float a, float b, float* scratch, const Group& gr) {
+  const int lane = gr.t & 31, w = gr.t >> 5;
+  a = warp_sum_lane0(a);
+  b = warp_sum_lane0(b);
+  if (lane == 0) {
+    scratch[2 * w] = a;
+    scratch[2 * w + 1] = b;
+  }
+  gr.sync();
+  float2 r = make_float2(0.f, 0.f);
+  if (gr.t == 0)
+    for (int i = 0; i < (gr.n >> 5); ++i) {
+      r.x += scratch[2 * i];
+      r.y += scratch[2 * i + 1];
+    }
+  gr.sync();
+  return r;
+}
+
+// Every thread of a group: waits until phase `parity` of `bar` has completed.
+// The group's thread 0 polls, bounded in time and giving up once the error
+// word is raised; the outcome reaches the group through *flag.  Returns true
+// (after an acquiring test of the barrier by every thread) or false, uniformly.
+__device__ bool group_wait(uint64_t* bar, uint32_t parity, unsigned* err, int* flag, const Group& gr) {
+  if (gr.t == 0) {
+    int go = 1;
+    if (!mbar_try_wait(bar, parity)) {
+      const uint64_t t0 = now_ns();
+      for (unsigned i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) break;
+        if ((i & 15u) == 0u) {
+          if (aborted(err)) {
+            go = 0;
+            break;
+          }
+          if (now_ns() - t0 > kWaveWaitNs) {
+            atomicOr(err, kErrData);
+            go = 0;
+            break;
+          }
+        }
+      }
+    }
+    *flag = go;
+  }
+  gr.sync();
+  if (!*flag) return false;
+  mbar_try_wait(bar, parity);  // completed: orders this thread's later reads after it
+  return true;
+}
+
+// Every thread of a group: reads the records at src still marked in `todo`
+// into dst (shared memory), polling until all of them are written.  Bounded
+// in time (the group's thread 0 keeps the clock); returns false, uniformly,
+// when the bound runs out or the error word is raised.
 __device__ bool gather_records(const float2* src, float2* dst, unsigned todo, unsigned* err,
-                               int* s_flag) {
-  const int tid = threadIdx.x, nt = blockDim.x;
+                               int* s_flag, const Group& gr) {
+  const int tid = gr.t, nt = gr.n;
   uint64_t t0 = 0;
   for (unsigned round = 0;; ++round) {
     for (int i = 0; i < 32 && (todo >> i) != 0u; ++i) {
@@ -155,7 +236,7 @@ __device__ bool gather_records(const float2* src, float2* dst, unsigned todo, un
         todo &= ~(1u << i);
       }
     }
-    if (!__syncthreads_or(todo != 0u)) return true;
+    if (!gr.sync_or(todo != 0u)) return true;
     if (tid == 0) {
       int go = 1;
       if ((round & 7u) == 7u && aborted(err)) {
@@ -171,7 +252,7 @@ __device__ bool gather_records(const float2* src, float2* dst, unsigned todo, un
       }
       *s_flag = go;
     }
-    __syncthreads();
+    gr.sync();
     if (!*s_flag) return false;
     __nanosleep(64);
   }
@@ -249,8 +330,14 @@ __device__ __forceinline__ float piece_count(const Geom& g, int t) {
   return (float)((a + g.wR < g.HW) ? g.wR : g.HW - a);
 }
 
-template <typename T, int VW, int LAYOUT, bool BWD, bool HOLD>
+// MODE 0: a piece waits for its unit's statistics in its slot, and the CTA
+// runs stage A and stage B in turn; MODE 1: it waits in tensor memory;
+// MODE 2: it waits in tensor memory, and stage A (warps 0-3) and stage B
+// (warps 4-7) run concurrently, handing pieces over through mbarriers.
+template <typename T, int VW, int LAYOUT, bool BWD, int MODE>
 __global__ void __launch_bounds__(kWaveThreads, kWaveCtasPerSm) wave_kernel(const __grid_constant__ KParams p) {
+  constexpr bool HOLD = MODE >= 1;
+  constexpr bool WS = MODE == 2;
   extern __shared__ __align__(128) char smem_raw[];
   char* smem =
       reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
@@ -258,11 +345,21 @@ __global__ void __launch_bounds__(kWaveThreads, kWaveCtasPerSm) wave_kernel(cons
   constexpr int NTEN = BWD ? 2 : 1;
   const int tid = threadIdx.x, nt = blockDim.x;
   const int lane = tid & 31, warp = tid >> 5, nwarps = nt >> 5;
+  // the stages' threads: the whole CTA, or (WS) warps 0-3 for stage A and
+  // warps 4-7 for stage B; tg is this thread's index in its stage
+  const int ng = WS ? nt / 2 : nt;
+  const bool is_a = !WS || tid < ng;
+  const int tg = WS && !is_a ? tid - ng : tid;
+  const Group ga{WS ? 1 : 0, ng, tg};
+  const Group gb{WS ? 2 : 0, ng, tg};
+  const int wg = tg >> 5, nwg = ng >> 5;  // warp within the stage, warps of a stage
   char* ring = smem + g.off_ring;
   float* red = reinterpret_cast<float*>(smem + g.off_red);
   float2* grp = reinterpret_cast<float2*>(smem + g.off_grp);  // per-group results of the unit
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + g.off_bar);
-  __shared__ int s_ok;
+  // outcomes of the waits, one flag per waiting site: a flag is written
+  // again only after every thread of its stage has passed another barrier
+  __shared__ int s_ok, s_ok_b, s_ok_e, s_ok_f;
   __shared__ uint32_t s_tmem;  // HOLD: base address of the CTA's tensor memory
 
   const int NC = gridDim.x, b = blockIdx.x;
@@ -279,6 +376,10 @@ __global__ void __launch_bounds__(kWaveThreads, kWaveCtasPerSm) wave_kernel(cons
   const int ahead = HOLD ? H - 1 : (S >= 3 ? 1 : 0);
   const int NCB = (int)g.wB;            // buffers of per-piece constants
   const int NRB = HOLD && H > 2 ? H : 2;  // P == 1: buffers of the CTA's own records
+  // WS: tm_full[h] completes when stage A has put a piece into hold buffer
+  // h, tm_empty[h] when stage B has written that piece out
+  uint64_t* tm_full = full + S;
+  uint64_t* tm_empty = tm_full + H;
   // shared scratch: the unit's records (P > 1: gathered; P == 1: the CTA's
   // own, NRB pieces' worth), then the CTA sums
   float2* recs = reinterpret_cast<float2*>(red);
@@ -290,9 +391,15 @@ __global__ void __launch_bounds__(kWaveThreads, kWaveCtasPerSm) wave_kernel(cons
 
   if (tid == 0) {
     for (int i = 0; i < S; ++i) mbar_init(full + i, 1);
+    if (WS)
+      for (int h = 0; h < H; ++h) {
+        mbar_init(tm_full + h, 1);
+        mbar_init(tm_empty + h, 1);
+      }
     fence_mbar_init();
   }
   if (HOLD) {
+    __syncwarp();
     if (warp == 0) tmem_alloc(&s_tmem, kWaveTmemCols);
     tmem_fence_before();
   }
@@ -352,9 +459,9 @@ __global__ void __launch_bounds__(kWaveThreads, kWaveCtasPerSm) wave_kernel(cons
   // rl, rl + rpi, ...; qe[e] is the group (within the block) of its channel
   // e.  NCHW: the piece's 16-byte vectors tid, tid + nt, ...
   const int Wv = LAYOUT == kNHWC ? nch / VW : 1;
-  const int rpi = LAYOUT == kNHWC ? nt / Wv : nt;
-  const int j = LAYOUT == kNHWC ? tid % Wv : 0;
-  const int rl = LAYOUT == kNHWC ? tid / Wv : tid;
+  const int rpi = LAYOUT == kNHWC ? ng / Wv : ng;
+  const int j = LAYOUT == kNHWC ? tg % Wv : 0;
+  const int rl = LAYOUT == kNHWC ? tg / Wv : tg;
   const bool lane_ok = LAYOUT == kNHWC ? rl < rpi : true;
   int qe[VW];
 #pragma unroll
@@ -373,7 +480,7 @@ __global__ void __launch_bounds__(kWaveThreads, kWaveCtasPerSm) wave_kernel(cons
       const Piece pc = piece_of<LAYOUT>(g, k * NC + b);
       float* cs = cstb + (k % NCB) * CST;
       if (LAYOUT == kNHWC) {
-        for (int c = tid; c < nch; c += nt) {
+        for (int c = tg; c < nch; c += ng) {
           if (p.gamma) cp_async4(cs + c, p.gamma + pc.cbase + c);
           else cs[c] = 1.0f;
           if (!BWD) {
@@ -382,18 +489,18 @@ __global__ void __launch_bounds__(kWaveThreads, kWaveCtasPerSm) wave_kernel(cons
           }
         }
         if (BWD) {
-          const int64_t gb = (int64_t)pc.n * g.G + pc.cbase / Cg;
-          for (int q = tid; q < ngrp; q += nt) {
-            cp_async4(cs + nch + q, p.mean + gb + q);
-            cp_async4(cs + nch + ngrp + q, p.rstd + gb + q);
+          const int64_t g0 = (int64_t)pc.n * g.G + pc.cbase / Cg;
+          for (int q = tg; q < ngrp; q += ng) {
+            cp_async4(cs + nch + q, p.mean + g0 + q);
+            cp_async4(cs + nch + ngrp + q, p.rstd + g0 + q);
           }
         }
       } else {
-        for (int cl = tid; cl < Cg; cl += nt) {
+        for (int cl = tg; cl < Cg; cl += ng) {
           if (p.gamma) cp_async4(cs + cl, p.gamma + (int64_t)pc.gi * Cg + cl);
           else cs[cl] = 1.0f;
         }
-        if (tid == nt - 1) {
+        if (tg == ng - 1) {
           if (BWD) {
             cp_async4(cs + Cg, p.mean + pc.u);
             cp_async4(cs + Cg + 1, p.rstd + pc.u);
@@ -407,24 +514,27 @@ __global__ void __launch_bounds__(kWaveThreads, kWaveCtasPerSm) wave_kernel(cons
     }
     cp_async_commit();
   };
-  fetch_constants(0);
+  if (is_a) fetch_constants(0);
 
-  // ---- a unit's records are read ahead, during the stage A before their
-  // stage B (when stage A runs ahead): raw words land in registers while the
-  // stage works, and are decoded into shared memory at its end
+  // ---- a unit's records are read ahead: during the stage A before their
+  // stage B (when stage A runs ahead), or (WS) by stage B during the output
+  // of its previous piece.  Raw words land in registers while the stage
+  // works, and are decoded into shared memory at its end.
   constexpr int kPre = 8;  // records per thread read ahead (at most)
-  const bool read_ahead = P > 1 && ahead >= 1 && rec_unit <= kPre * nt;
+  const bool read_ahead = P > 1 && (WS || ahead >= 1) && rec_unit <= kPre * ng;
   unsigned long long pre[kPre];
   int pre_unit = -1;       // the unit whose records sit in `recs`, or -1
   unsigned pre_todo = 0;   // of those, the ones not yet written
 
-  // ---- HOLD: thread t keeps the vectors it reduces in stage A (and writes
-  // in stage B) in tensor-memory lane 32*(warp % 4) + t % 32, T4 vectors of
-  // x then T4 of dy from column (warp / 4) * tcols of the piece's buffer
+  // ---- HOLD: thread t of a stage keeps the vectors it reduces in stage A
+  // (and writes in stage B) in tensor-memory lane 32*(warp % 4) + t % 32, T4
+  // vectors of x then T4 of dy from column 0 (WS) or (warp / 4) * tcols of
+  // the piece's buffer
   const int T4 = HOLD ? (int)g.wT : 0;
   const uint32_t tcols = 4u * NTEN * (uint32_t)T4;
-  const uint32_t bcols = tcols * (uint32_t)(nt / 128);
-  const uint32_t tthr = HOLD ? s_tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(warp >> 2) * tcols : 0u;
+  const uint32_t bcols = WS ? tcols : tcols * (uint32_t)(nt / 128);
+  const uint32_t tthr =
+      HOLD ? s_tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (WS ? 0u : (uint32_t)(warp >> 2) * tcols) : 0u;
 
   // ---- stage A of piece k: wait for its copy, reduce it, publish its records
   auto stage_a = [&](int k) -> bool {
@@ -437,20 +547,15 @@ __global__ void __launch_bounds__(kWaveThreads, kWaveCtasPerSm) wave_kernel(cons
     fetch_constants(k + 1);  // and the next piece's, for the next step
     // the records of the unit of the stage B that follows (piece k - ahead)
     const int pre_k = k - ahead;
-    const int pre_u = read_ahead && pre_k >= 0 ? piece_of<LAYOUT>(g, pre_k * NC + b).u : -1;
+    const int pre_u = !WS && read_ahead && pre_k >= 0 ? piece_of<LAYOUT>(g, pre_k * NC + b).u : -1;
     if (pre_u >= 0) {
       const float2* src = p.part + (int64_t)pre_u * rec_unit;
 #pragma unroll
       for (int i = 0; i < kPre; ++i)
-        pre[i] = tid + i * nt < rec_unit ? ld_rec_raw(src + tid + i * nt) : 0ull;
+        pre[i] = tg + i * ng < rec_unit ? ld_rec_raw(src + tg + i * ng) : 0ull;
     }
-    if (tid == 0)
-      s_ok = mbar_try_wait(full + si, parity)
-                 ? 1
-                 : (aborted(p.err) ? 0 : (wait_bar_t0(full + si, parity, p.err) ? 1 : 0));
-    __syncthreads();  // also publishes the constants to every thread
-    if (!s_ok) return false;
-    mbar_try_wait(full + si, parity);  // completed: orders this thread's reads after the copy
+    // the piece's copy (the group barrier also publishes the constants)
+    if (!group_wait(full + si, parity, p.err, &s_ok, ga)) return false;
     float2* rec_g = p.part + (int64_t)pc.u * rec_unit + pc.t * nch;
     float2* rec_s = recs + (k % NRB) * nch;  // P == 1: kept in shared memory
     const bool publish = !(p.stall_unit == pc.u && pc.t == 0);  // fault injection
@@ -480,13 +585,13 @@ __global__ void __launch_bounds__(kWaveThreads, kWaveCtasPerSm) wave_kernel(cons
         }
       };
       if constexpr (HOLD) {
-        // vectors tid + i*nt, i < T4, also go to tensor memory (zeros past the piece)
+        // vectors tg + i*ng, i < T4, also go to tensor memory (zeros past the piece)
         const uint32_t tb = tthr + (uint32_t)(k % H) * bcols;
         for (int i0 = 0; i0 < T4; i0 += 4) {
           uint32_t wx[16], wd[16];
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            const int v = tid + (i0 + u) * nt;
+            const int v = tg + (i0 + u) * ng;
             uint4 rx = make_uint4(0u, 0u, 0u, 0u), rd = rx;
             if (v < nv) {
               rx = lds16(slot + (size_t)v * 16);
@@ -502,12 +607,12 @@ __global__ void __launch_bounds__(kWaveThreads, kWaveCtasPerSm) wave_kernel(cons
         tmem_wait_st();
       } else {
 #pragma unroll 4
-        for (int v = tid; v < nv; v += nt)
+        for (int v = tg; v < nv; v += ng)
           add(lds16(slot + (size_t)v * 16),
               BWD ? lds16(slot + g.ten_stride + (size_t)v * 16) : make_uint4(0u, 0u, 0u, 0u));
       }
-      const float2 s2 = block_sum2_t0(a, c, cred);
-      if (tid == 0) {
+      const float2 s2 = group_sum2_t0(a, c, cred, ga);
+      if (tg == 0) {
         float2 r;
         if (BWD) {
           r = s2;
@@ -586,40 +691,45 @@ __global__ void __launch_bounds__(kWaveThreads, kWaveCtasPerSm) wave_kernel(cons
       // accumulators in a fixed rotation, then the lanes meet in a fixed xor
       // tree
 #pragma unroll
-      for (int q = 0; q < 2 * VW; ++q) cred[q * nt + tid] = acc[q];
-      float* ksh = cred + 2 * VW * nt;
+      for (int q = 0; q < 2 * VW; ++q) cred[q * ng + tg] = acc[q];
+      float* ksh = cred + 2 * VW * ng;
       float* sums = ksh + nch;
       if (!BWD && rl == 0 && lane_ok) {
 #pragma unroll
         for (int e = 0; e < VW; ++e) ksh[j * VW + e] = Ks[e];
       }
-      __syncthreads();
+      ga.sync();
       {
         const int nsum = 2 * VW * Wv;
         int tps = 1;
-        while (tps < 32 && 2 * tps * nsum <= nt) tps *= 2;
-        const int sidx = tid / tps, l = tid % tps;
-        const bool mine = sidx < nsum;
-        const int q = mine ? sidx / Wv : 0, jj = mine ? sidx % Wv : 0;
-        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-        if (mine) {
-          const float* src = cred + q * nt + jj;
-          int r = l;
-          for (; r + 3 * tps < rpi; r += 4 * tps) {
-            a0 += src[r * Wv];
-            a1 += src[(r + tps) * Wv];
-            a2 += src[(r + 2 * tps) * Wv];
-            a3 += src[(r + 3 * tps) * Wv];
+        while (tps < 32 && 2 * tps * nsum <= ng) tps *= 2;
+        const int l = tg % tps;
+        // with more sums than the stage has threads (tps = 1), each thread
+        // takes several; the trip count is the same for every thread
+        for (int base = 0; base < nsum * tps; base += ng) {
+          const int sidx = (base + tg) / tps;
+          const bool mine = sidx < nsum;
+          const int q = mine ? sidx / Wv : 0, jj = mine ? sidx % Wv : 0;
+          float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+          if (mine) {
+            const float* src = cred + q * ng + jj;
+            int r = l;
+            for (; r + 3 * tps < rpi; r += 4 * tps) {
+              a0 += src[r * Wv];
+              a1 += src[(r + tps) * Wv];
+              a2 += src[(r + 2 * tps) * Wv];
+              a3 += src[(r + 3 * tps) * Wv];
+            }
+            for (; r < rpi; r += tps) a0 += src[r * Wv];
           }
-          for (; r < rpi; r += tps) a0 += src[r * Wv];
+          float a = (a0 + a1) + (a2 + a3);
+          for (int off = tps / 2; off > 0; off >>= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
+          if (mine && l == 0) sums[sidx] = a;
         }
-        float a = (a0 + a1) + (a2 + a3);
-        for (int off = tps / 2; off > 0; off >>= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
-        if (mine && l == 0) sums[sidx] = a;
       }
-      __syncthreads();
+      ga.sync();
       const float n = (float)pc.len;
-      for (int c = tid; c < nch; c += nt) {
+      for (int c = tg; c < nch; c += ng) {
         const int jj = c / VW, e = c - jj * VW;
         const float sa = sums[(2 * e) * Wv + jj];
         const float sb = sums[(2 * e + 1) * Wv + jj];
@@ -634,13 +744,14 @@ __global__ void __launch_bounds__(kWaveThreads, kWaveCtasPerSm) wave_kernel(cons
         else if (publish) put_rec(rec_g + c, rr);
       }
     }
-    __syncthreads();  // the records are out; the scratch is free
+    if (HOLD) tmem_fence_before();  // the piece's tensor-memory stores (waited for) precede the barrier
+    ga.sync();  // the records are out; the scratch and the slot are free
     if (pre_u >= 0) {
       unsigned todo = 0;
 #pragma unroll
       for (int i = 0; i < kPre; ++i) {
-        if (tid + i * nt >= rec_unit) continue;
-        if (pre[i]) recs[tid + i * nt] = rec_decode(pre[i]);
+        if (tg + i * ng >= rec_unit) continue;
+        if (pre[i]) recs[tg + i * ng] = rec_decode(pre[i]);
         else todo |= 1u << i;
       }
       pre_todo = todo;
@@ -657,9 +768,9 @@ __global__ void __launch_bounds__(kWaveThreads, kWaveCtasPerSm) wave_kernel(cons
     const float* cs = cstb + (k % NCB) * CST;
     const float2* R = recs + (k % NRB) * nch;
     if (P > 1) {
-      const unsigned todo = pre_unit == pc.u ? pre_todo : record_mask(rec_unit);
+      const unsigned todo = pre_unit == pc.u ? pre_todo : record_mask(rec_unit, gb);
       pre_unit = -1;
-      if (!gather_records(p.part + (int64_t)pc.u * rec_unit, recs, todo, p.err, &s_ok))
+      if (!gather_records(p.part + (int64_t)pc.u * rec_unit, recs, todo, p.err, &s_ok_b, gb))
         return false;
       R = recs;
     }
@@ -669,7 +780,7 @@ __global__ void __launch_bounds__(kWaveThreads, kWaveCtasPerSm) wave_kernel(cons
     // parallel-axis identity over all of a group's records at once; backward:
     // c1 = sum gamma_c*S1 and c2 = sum gamma_c*S2.
     const int64_t gbase = LAYOUT == kNHWC ? (int64_t)pc.n * g.G + pc.cbase / Cg : pc.u;
-    for (int q = warp; q < ngrp; q += nwarps) {
+    for (int q = wg; q < ngrp; q += nwg) {
       const int nrow = LAYOUT == kNHWC ? Cg : 1;  // records of a piece in the group
       const float2* Rq = R + (LAYOUT == kNHWC ? q * Cg : 0);
       const int rstride = LAYOUT == kNHWC ? nch : 1;
@@ -711,7 +822,7 @@ __global__ void __launch_bounds__(kWaveThreads, kWaveCtasPerSm) wave_kernel(cons
     if (BWD && pc.t == 0 && (p.dgamma || p.dbeta)) {
       const int nchan = LAYOUT == kNHWC ? nch : Cg;
       const int64_t c0 = LAYOUT == kNHWC ? pc.cbase : (int64_t)pc.gi * Cg;
-      for (int c = tid; c < nchan; c += nt) {
+      for (int c = tg; c < nchan; c += ng) {
         float sa = 0.f, sb = 0.f;
         const int cnt_c = LAYOUT == kNHWC ? P : (int)g.wm;
         for (int t = 0; t < cnt_c; ++t) {
@@ -722,12 +833,21 @@ __global__ void __launch_bounds__(kWaveThreads, kWaveCtasPerSm) wave_kernel(cons
         p.chst[(int64_t)pc.n * g.C + c0 + c] = make_float2(sa, sb);
       }
     }
-    __syncthreads();  // the groups' values
+    gb.sync();  // the groups' values; the gathered records are read
     if (!BWD && pc.t == 0)
-      for (int q = tid; q < ngrp; q += nt) {
+      for (int q = tg; q < ngrp; q += ng) {
         p.mean[gbase + q] = grp[q].x;
         p.rstd[gbase + q] = grp[q].y;
       }
+    // WS: the records of the next piece's unit, read while this one is written
+    int nxt_u = -1;
+    if (WS && read_ahead && k + 1 < K) {
+      nxt_u = piece_of<LAYOUT>(g, (k + 1) * NC + b).u;
+      const float2* src = p.part + (int64_t)nxt_u * rec_unit;
+#pragma unroll
+      for (int i = 0; i < kPre; ++i)
+        pre[i] = tg + i * ng < rec_unit ? ld_rec_raw(src + tg + i * ng) : 0ull;
+    }
 
     // ---- the piece's output, from tensor memory (HOLD) or its slot
     if (LAYOUT == kNCHW) {
@@ -769,7 +889,7 @@ __global__ void __launch_bounds__(kWaveThreads, kWaveCtasPerSm) wave_kernel(cons
           tmem_wait_ld();
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            const int v = tid + (i0 + u) * nt;
+            const int v = tg + (i0 + u) * ng;
             if (v < nv) {
               if constexpr (BWD) put(v, get4(wx, u), get4(wd, u));
               else put(v, get4(wx, u), get4(wx, u));
@@ -778,7 +898,7 @@ __global__ void __launch_bounds__(kWaveThreads, kWaveCtasPerSm) wave_kernel(cons
         }
       } else {
 #pragma unroll 4
-        for (int v = tid; v < nv; v += nt)
+        for (int v = tg; v < nv; v += ng)
           put(v, lds16(slot + (size_t)v * 16),
               BWD ? lds16(slot + g.ten_stride + (size_t)v * 16) : make_uint4(0u, 0u, 0u, 0u));
       }
@@ -840,14 +960,24 @@ __global__ void __launch_bounds__(kWaveThreads, kWaveCtasPerSm) wave_kernel(cons
               BWD ? lds16(col + g.ten_stride + (size_t)r * rowb) : make_uint4(0u, 0u, 0u, 0u));
       }
     }
-    __syncthreads();  // the slot's reads are done; the scratch is free
+    if (nxt_u >= 0) {
+      unsigned todo = 0;
+#pragma unroll
+      for (int i = 0; i < kPre; ++i) {
+        if (tg + i * ng >= rec_unit) continue;
+        if (pre[i]) recs[tg + i * ng] = rec_decode(pre[i]);
+        else todo |= 1u << i;
+      }
+      pre_todo = todo;
+      pre_unit = nxt_u;
+    }
+    if (HOLD) tmem_fence_before();  // the piece's tensor-memory loads (waited for) precede the barrier
+    gb.sync();  // the slot's (or buffer's) reads are done; the scratch is free
     return true;
   };
 
-  // ---- the pipeline.  Stage A runs `ahead` pieces before stage B: by the
-  // time a CTA needs a unit's records, every CTA has had `ahead` steps to
-  // publish them.  A slot takes its next copy (piece k + S) once piece k is
-  // done with it: after stage A with HOLD (the piece waits in tensor
+  // ---- the pipeline.  A slot takes its next copy (piece k + S) once piece k
+  // is done with it: after stage A with HOLD (the piece waits in tensor
   // memory), after stage B without.
   auto issue_next = [&]() {
     if (tid == 0 && issued < K) {
@@ -857,30 +987,57 @@ __global__ void __launch_bounds__(kWaveThreads, kWaveCtasPerSm) wave_kernel(cons
     }
   };
   int ka = 0;  // pieces through stage A
-  bool ok = true;
-  for (; ok && ka <= ahead && ka < K; ++ka) {
-    ok = stage_a(ka);
-    if (ok && HOLD) issue_next();
-  }
-  if (!ok) --ka;  // that piece's copy may still be in flight
-  for (int k = 0; ok && k < K; ++k) {
-    if (!stage_b(k)) {
-      ok = false;
-      break;
+  if constexpr (WS) {
+    // Stage A puts piece k into hold buffer k % H once stage B has written
+    // piece k - H out of it; stage B takes piece k once stage A has put it
+    // there.  Either side gives up when the other has raised the error word.
+    if (is_a) {
+      for (int k = 0; k < K; ++k) {
+        const int h = k % H;
+        if (k >= H && !group_wait(tm_empty + h, (uint32_t)((k / H - 1) & 1), p.err, &s_ok_e, ga)) break;
+        tmem_fence_after();
+        if (!stage_a(k)) break;
+        if (tg == 0) mbar_arrive(tm_full + h);
+        issue_next();
+        ka = k + 1;
+      }
+    } else {
+      for (int k = 0; k < K; ++k) {
+        const int h = k % H;
+        if (!group_wait(tm_full + h, (uint32_t)((k / H) & 1), p.err, &s_ok_f, gb)) break;
+        tmem_fence_after();
+        if (!stage_b(k)) break;
+        if (tg == 0) mbar_arrive(tm_empty + h);
+      }
     }
-    if (!HOLD) issue_next();
-    if (ka < K) {
-      if (!stage_a(ka)) {
+  } else {
+    // Stage A runs `ahead` pieces before stage B: by the time a CTA needs a
+    // unit's records, every CTA has had `ahead` steps to publish them.
+    bool ok = true;
+    for (; ok && ka <= ahead && ka < K; ++ka) {
+      ok = stage_a(ka);
+      if (ok && HOLD) issue_next();
+    }
+    if (!ok) --ka;  // that piece's copy may still be in flight
+    for (int k = 0; ok && k < K; ++k) {
+      if (!stage_b(k)) {
         ok = false;
         break;
       }
-      if (HOLD) issue_next();
-      ++ka;
+      if (!HOLD) issue_next();
+      if (ka < K) {
+        if (!stage_a(ka)) {
+          ok = false;
+          break;
+        }
+        if (HOLD) issue_next();
+        ++ka;
+      }
     }
   }
 
   // ---- after a wait ran out: this CTA's copies still in flight land first
-  if (!ok && tid == 0)
+  if (tid == 0)
     for (int i = ka; i < issued; ++i) wait_bar_t0(full + (i % S), (uint32_t)((i / S) & 1), p.err);
   cp_async_wait_all();  // no asynchronous copy into shared memory outlives the CTA
   if (HOLD) {  // every thread's tensor-memory accesses have completed (waited for)
@@ -932,26 +1089,28 @@ __global__ void __launch_bounds__(kWaveThreads, kWaveCtasPerSm) wave_kernel(cons
 }
 
 template <typename T, int VW, int LAYOUT, bool BWD>
-const void* kernel_ptr(bool hold) {
-  return hold ? (const void*)wave_kernel<T, VW, LAYOUT, BWD, true>
-              : (const void*)wave_kernel<T, VW, LAYOUT, BWD, false>;
+const void* kernel_ptr(int mode) {
+  if (mode == 2) return (const void*)wave_kernel<T, VW, LAYOUT, BWD, 2>;
+  if (mode == 1) return (const void*)wave_kernel<T, VW, LAYOUT, BWD, 1>;
+  return (const void*)wave_kernel<T, VW, LAYOUT, BWD, 0>;
 }
 
 template <typename T>
-const void* pick(int layout, bool bwd, bool hold) {
+const void* pick(int layout, bool bwd, int mode) {
   constexpr int V = Elem<T>::VEC;
   if (layout == kNCHW)
-    return bwd ? kernel_ptr<T, V, kNCHW, true>(hold) : kernel_ptr<T, V, kNCHW, false>(hold);
-  return bwd ? kernel_ptr<T, V, kNHWC, true>(hold) : kernel_ptr<T, V, kNHWC, false>(hold);
+    return bwd ? kernel_ptr<T, V, kNCHW, true>(mode) : kernel_ptr<T, V, kNCHW, false>(mode);
+  return bwd ? kernel_ptr<T, V, kNHWC, true>(mode) : kernel_ptr<T, V, kNHWC, false>(mode);
 }
 
 }  // namespace
 
 const void* wave_kernel_ptr(const Geom& g, bool bwd) {
+  const int mode = g.wH > 0 ? (g.wWs ? 2 : 1) : 0;
   switch (g.dtype) {
-    case kF32: return pick<float>(g.layout, bwd, g.wH > 0);
-    case kF16: return pick<__half>(g.layout, bwd, g.wH > 0);
-    default: return pick<__nv_bfloat16>(g.layout, bwd, g.wH > 0);
+    case kF32: return pick<float>(g.layout, bwd, mode);
+    case kF16: return pick<__half>(g.layout, bwd, mode);
+    default: return pick<__nv_bfloat16>(g.layout, bwd, mode);
   }
 }
 

@@ -217,12 +217,13 @@ def test_f64_storage_plans(gn):
 
 
 def test_automatic_choice(gn):
-    """The automatic choice: the wave regime for the NCHW backward with units
+    """The automatic choice: the wave regime for NCHW problems with units
     of at least 4 MiB; the resident regime for channels-last forwards and
     small NCHW units when one wave of clusters covers every unit (or the
     input is tiny); the two-kernel path otherwise."""
     assert gn.plan_info(1, 112, 64, 512 * 512, 8, "nchw", "f32").regime == 3   # 8 MiB units
-    assert gn.plan_info(0, 112, 64, 512 * 512, 8, "nchw", "f32").regime == 0
+    assert gn.plan_info(0, 112, 64, 512 * 512, 8, "nchw", "f32").regime == 3
+    assert gn.plan_info(0, 16, 64, 512 * 512, 64, "nchw", "f32").regime == 0   # 1 MiB units
     assert gn.plan_info(0, 2, 32, 256, 8, "nchw", "f32").regime == 1        # 64 KB
     assert gn.plan_info(0, 512, 32, 256, 8, "nchw", "f32").regime == 0      # 4096 units
     assert gn.plan_info(0, 8, 320, 4096, 32, "nhwc", "bf16").regime == 1    # 32 clusters
@@ -250,6 +251,8 @@ def test_wave_plans(gn):
         gn.set_regime(gn.REGIME_AUTO)
     for w, d in plans:
         assert d.regime == 3 and d.launches == 1
+        assert d.hold_buffers >= 2 and d.slots >= 2  # pieces wait in tensor memory
+        assert d.smem_bytes > 114 * 1024  # one tensor-memory holder per SM
         assert 1 <= d.pieces_per_unit <= d.ctas
         assert d.ctas % d.pieces_per_unit == 0
         assert d.smem_bytes <= 227 * 1024
