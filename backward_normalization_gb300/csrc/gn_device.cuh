@@ -439,14 +439,15 @@ __device__ __forceinline__ void tmem_fence_after() {
 }
 // Warp-wide: 16 consecutive columns of this thread's lane from / to registers.
 // A load's registers are valid only after tmem_wait_ld; a store has finished
-// (its cells readable, its columns reusable) after tmem_wait_st.
+// (its cells readable, its columns reusable) after tmem_wait_st.  Neither
+// touches memory the compiler sees, so ordinary loads and stores may move
+// across them; the waits, fences and barriers keep their order (volatile).
 __device__ __forceinline__ void tmem_st16(uint32_t a, const uint32_t (&v)[16]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
       "%14, %15, %16};" ::"r"(a),
       "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
-      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
-      : "memory");
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]));
 }
 __device__ __forceinline__ void tmem_ld16(uint32_t a, uint32_t (&v)[16]) {
   asm volatile(
@@ -454,8 +455,7 @@ __device__ __forceinline__ void tmem_ld16(uint32_t a, uint32_t (&v)[16]) {
       "%15}, [%16];"
       : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
         "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
-      : "r"(a)
-      : "memory");
+      : "r"(a));
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }

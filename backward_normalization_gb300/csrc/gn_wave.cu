@@ -585,26 +585,61 @@ __global__ void __launch_bounds__(kWaveThreads, kWaveCtasPerSm) wave_kernel(cons
         }
       };
       if constexpr (HOLD) {
-        // vectors tg + i*ng, i < T4, also go to tensor memory (zeros past the piece)
+        // vectors tg + i*ng, i < T4, also go to tensor memory (zeros past the
+        // piece).  Ordinary shared-memory loads (the compiler may run them
+        // ahead), and one partial sum per vector element, so that the
+        // dependency chains stay short; the partial sums meet in element
+        // order at the end.
+        float ae[VW], ce[VW];
+#pragma unroll
+        for (int e = 0; e < VW; ++e) ae[e] = ce[e] = 0.f;
         const uint32_t tb = tthr + (uint32_t)(k % H) * bcols;
         for (int i0 = 0; i0 < T4; i0 += 4) {
           uint32_t wx[16], wd[16];
+          uint4 rx[4], rd[4];
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const int v = tg + (i0 + u) * ng;
-            uint4 rx = make_uint4(0u, 0u, 0u, 0u), rd = rx;
+            rx[u] = rd[u] = make_uint4(0u, 0u, 0u, 0u);
             if (v < nv) {
-              rx = lds16(slot + (size_t)v * 16);
-              if (BWD) rd = lds16(slot + g.ten_stride + (size_t)v * 16);
-              add(rx, rd);
+              rx[u] = *reinterpret_cast<const uint4*>(slot + (size_t)v * 16);
+              if (BWD) rd[u] = *reinterpret_cast<const uint4*>(slot + g.ten_stride + (size_t)v * 16);
             }
-            put4(wx, u, rx);
-            if (BWD) put4(wd, u, rd);
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            if (tg + (i0 + u) * ng < nv) {
+              float xv[VW];
+              Access<T, VW>::unpack(rx[u], xv);
+              if (BWD) {
+                float dv[VW];
+                Access<T, VW>::unpack(rd[u], dv);
+#pragma unroll
+                for (int e = 0; e < VW; ++e) {
+                  ae[e] += dv[e];
+                  ce[e] = fmaf(dv[e], xv[e] - mu, ce[e]);
+                }
+              } else {
+#pragma unroll
+                for (int e = 0; e < VW; ++e) {
+                  const float d = xv[e] - K0;
+                  ae[e] += d;
+                  ce[e] = fmaf(d, d, ce[e]);
+                }
+              }
+            }
+            put4(wx, u, rx[u]);
+            if (BWD) put4(wd, u, rd[u]);
           }
           tmem_st16(tb + 4u * (uint32_t)i0, wx);
           if (BWD) tmem_st16(tb + 4u * (uint32_t)(T4 + i0), wd);
         }
         tmem_wait_st();
+#pragma unroll
+        for (int e = 0; e < VW; ++e) {
+          a += ae[e];
+          c += ce[e];
+        }
       } else {
 #pragma unroll 4
         for (int v = tg; v < nv; v += ng)
@@ -881,20 +916,36 @@ __global__ void __launch_bounds__(kWaveThreads, kWaveCtasPerSm) wave_kernel(cons
         Access<T, VW>::store(o + (int64_t)v * VW, xv, pol_out);
       };
       if constexpr (HOLD) {
+        // the tensor-memory loads run one batch ahead: batch i0 + 4 is in
+        // flight while batch i0 is written (two register sets, a and b)
         const uint32_t tb = tthr + (uint32_t)(k % H) * bcols;
-        for (int i0 = 0; i0 < T4; i0 += 4) {
-          uint32_t wx[16], wd[16];
-          tmem_ld16(tb + 4u * (uint32_t)i0, wx);
-          if constexpr (BWD) tmem_ld16(tb + 4u * (uint32_t)(T4 + i0), wd);
-          tmem_wait_ld();
+        uint32_t xa[16], da[16], xb[16], db[16];
+        auto load = [&](int i0, uint32_t (&xr)[16], uint32_t (&dr)[16]) {
+          tmem_ld16(tb + 4u * (uint32_t)i0, xr);
+          if constexpr (BWD) tmem_ld16(tb + 4u * (uint32_t)(T4 + i0), dr);
+        };
+        auto write = [&](int i0, const uint32_t (&xr)[16], const uint32_t (&dr)[16]) {
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const int v = tg + (i0 + u) * ng;
             if (v < nv) {
-              if constexpr (BWD) put(v, get4(wx, u), get4(wd, u));
-              else put(v, get4(wx, u), get4(wx, u));
+              if constexpr (BWD) put(v, get4(xr, u), get4(dr, u));
+              else put(v, get4(xr, u), get4(xr, u));
             }
           }
+        };
+        load(0, xa, da);
+        tmem_wait_ld();
+        for (int i0 = 0; i0 < T4; i0 += 8) {
+          const bool nb = i0 + 4 < T4;
+          if (nb) load(i0 + 4, xb, db);
+          write(i0, xa, da);
+          tmem_wait_ld();
+          if (!nb) break;
+          const bool na = i0 + 8 < T4;
+          if (na) load(i0 + 8, xa, da);
+          write(i0 + 4, xb, db);
+          tmem_wait_ld();
         }
       } else {
 #pragma unroll 4
