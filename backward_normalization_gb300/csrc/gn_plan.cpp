@@ -387,7 +387,7 @@ int64_t wave_ctas(const Geom& g, int op, size_t smem, int sm_count, int want_per
   int nb = 0;
   if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
           cudaSuccess ||
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fn, kWaveThreads, smem) != cudaSuccess) {
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fn, g.tpb, smem) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
@@ -448,7 +448,7 @@ size_t wave_fixed_bytes(const Geom& g, int64_t P, int64_t Cb, int vec, int64_t H
   const size_t cst = (size_t)wave_cst_floats(t) * 4 * kWaveMaxSlots;  // per-piece constants (H + 1 <= max slots)
   const size_t tab = (size_t)2 * P * 4;                                 // piece counts, planes
   return a128((size_t)red * 4) + a128(tab) + a128(cst) + a128((size_t)grp * 8) +
-         a128(8 * (kWaveMaxSlots + 2 * kWaveMaxHold));
+         a128(8 * (kWaveMaxSlots + 3 * kWaveMaxHold));
 }
 
 // Threads of one stage of a wave CTA: half of it with warp specialisation.
@@ -548,7 +548,7 @@ bool plan_wave(Geom& g, int op, int sm_count) {
   if (best.P == 0) return false;
   Geom r = g;
   r.regime = kRegimeWave;
-  r.tpb = kWaveThreads;
+  r.tpb = kWaveThreads;  // (NCHW with warp specialisation: + the merge warp, below)
   r.wP = best.P;
   r.wR = best.R;
   r.wm = best.m;
@@ -557,6 +557,7 @@ bool plan_wave(Geom& g, int op, int sm_count) {
   r.wT = best.T4;
   r.wB = best.H > 0 ? best.H + 1 : best.S;  // constants live from stage A to stage B
   r.wWs = best.H > 0 && kWaveWs ? 1 : 0;
+  if (r.wWs && g.layout == kNCHW) r.tpb = kWaveThreads + 32;
   if (g.layout == kNHWC) {
     r.Cb = best.Cb;
     r.ncbu = g.C / best.Cb;
@@ -589,10 +590,12 @@ bool plan_wave(Geom& g, int op, int sm_count) {
   off += a128((size_t)2 * r.wP * 4);
   r.off_xch = off;  // per-piece constants
   off += a128((size_t)wave_cst_floats(r) * 4 * r.wB);
-  r.off_grp = off;
-  off += a128((size_t)(g.layout == kNHWC ? r.Cb / g.Cg : 1) * 8);
-  r.off_bar = off;  // slots' mbarriers, then (warp specialisation) the hold buffers' full and empty ones
-  off += a128(8 * (size_t)(r.S + 2 * r.wH));
+  r.off_grp = off;  // per-group results of a unit (NCHW merge warp: one per hold buffer)
+  off += a128((size_t)std::max<int64_t>(g.layout == kNHWC ? r.Cb / g.Cg : 1, r.wH) * 8);
+  // slots' mbarriers, then (warp specialisation) the hold buffers' full,
+  // empty and merged ones
+  r.off_bar = off;
+  off += a128(8 * (size_t)(r.S + 3 * r.wH));
   r.smem = off + 128;  // slack for aligning the dynamic shared memory base
   // a CTA that allocates tensor memory takes more than half of an SM's shared
   // memory, so that no other CTA of the kernel can share its SM (and wait

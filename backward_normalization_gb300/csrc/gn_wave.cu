@@ -335,9 +335,13 @@ __device__ __forceinline__ float piece_count(const Geom& g, int t) {
 // MODE 2: it waits in tensor memory, and stage A (warps 0-3) and stage B
 // (warps 4-7) run concurrently, handing pieces over through mbarriers.
 template <typename T, int VW, int LAYOUT, bool BWD, int MODE>
-__global__ void __launch_bounds__(kWaveThreads, kWaveCtasPerSm) wave_kernel(const __grid_constant__ KParams p) {
+__global__ void __launch_bounds__(LAYOUT == kNCHW && MODE == 2 ? kWaveThreads + 32 : kWaveThreads, kWaveCtasPerSm)
+    wave_kernel(const __grid_constant__ KParams p) {
   constexpr bool HOLD = MODE >= 1;
   constexpr bool WS = MODE == 2;
+  // WS, NCHW: a ninth warp (threads 256-287) gathers and merges each unit's
+  // records, so that stage B only writes
+  constexpr bool MW = WS && LAYOUT == kNCHW;
   extern __shared__ __align__(128) char smem_raw[];
   char* smem =
       reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
@@ -347,19 +351,20 @@ __global__ void __launch_bounds__(kWaveThreads, kWaveCtasPerSm) wave_kernel(cons
   const int lane = tid & 31, warp = tid >> 5, nwarps = nt >> 5;
   // the stages' threads: the whole CTA, or (WS) warps 0-3 for stage A and
   // warps 4-7 for stage B; tg is this thread's index in its stage
-  const int ng = WS ? nt / 2 : nt;
+  const int ng = WS ? kWaveThreads / 2 : nt;
   const bool is_a = !WS || tid < ng;
-  const int tg = WS && !is_a ? tid - ng : tid;
+  const bool is_m = MW && tid >= 2 * ng;
+  const int tg = !WS || is_a ? tid : is_m ? tid - 2 * ng : tid - ng;
   const Group ga{WS ? 1 : 0, ng, tg};
   const Group gb{WS ? 2 : 0, ng, tg};
-  const int wg = tg >> 5, nwg = ng >> 5;  // warp within the stage, warps of a stage
+  const Group gq{3, 32, tg};  // the merge warp
   char* ring = smem + g.off_ring;
   float* red = reinterpret_cast<float*>(smem + g.off_red);
   float2* grp = reinterpret_cast<float2*>(smem + g.off_grp);  // per-group results of the unit
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + g.off_bar);
   // outcomes of the waits, one flag per waiting site: a flag is written
   // again only after every thread of its stage has passed another barrier
-  __shared__ int s_ok, s_ok_b, s_ok_e, s_ok_f;
+  __shared__ int s_ok, s_ok_b, s_ok_e, s_ok_f, s_ok_m, s_ok_q, s_ok_r;
   __shared__ uint32_t s_tmem;  // HOLD: base address of the CTA's tensor memory
 
   const int NC = gridDim.x, b = blockIdx.x;
@@ -380,6 +385,7 @@ __global__ void __launch_bounds__(kWaveThreads, kWaveCtasPerSm) wave_kernel(cons
   // h, tm_empty[h] when stage B has written that piece out
   uint64_t* tm_full = full + S;
   uint64_t* tm_empty = tm_full + H;
+  uint64_t* mg_done = tm_empty + H;  // MW: the merge warp has piece k's unit statistics in grp[k % H]
   // shared scratch: the unit's records (P > 1: gathered; P == 1: the CTA's
   // own, NRB pieces' worth), then the CTA sums
   float2* recs = reinterpret_cast<float2*>(red);
@@ -395,6 +401,7 @@ __global__ void __launch_bounds__(kWaveThreads, kWaveCtasPerSm) wave_kernel(cons
       for (int h = 0; h < H; ++h) {
         mbar_init(tm_full + h, 1);
         mbar_init(tm_empty + h, 1);
+        if (MW) mbar_init(mg_done + h, 1);
       }
     fence_mbar_init();
   }
@@ -521,7 +528,7 @@ __global__ void __launch_bounds__(kWaveThreads, kWaveCtasPerSm) wave_kernel(cons
   // of its previous piece.  Raw words land in registers while the stage
   // works, and are decoded into shared memory at its end.
   constexpr int kPre = 8;  // records per thread read ahead (at most)
-  const bool read_ahead = P > 1 && (WS || ahead >= 1) && rec_unit <= kPre * ng;
+  const bool read_ahead = P > 1 && (WS || ahead >= 1) && rec_unit <= kPre * (MW ? 32 : ng);
   unsigned long long pre[kPre];
   int pre_unit = -1;       // the unit whose records sit in `recs`, or -1
   unsigned pre_todo = 0;   // of those, the ones not yet written
@@ -795,18 +802,19 @@ __global__ void __launch_bounds__(kWaveThreads, kWaveCtasPerSm) wave_kernel(cons
     return true;
   };
 
-  // ---- stage B of piece k: the unit's records (all published by now, or
-  // polled until they are), the group statistics, the piece's output
-  auto stage_b = [&](int k) -> bool {
+  // ---- the statistics of piece k's unit, by the threads of `gr`: its
+  // records (all published by now, or polled until they are), merged into
+  // the unit's per-group results at gout; the unit's first piece also writes
+  // the forward's mean and rstd or the backward's per-channel sums
+  auto merge_unit = [&](int k, const Group& gr, int* flag, float2* gout) -> bool {
     const Piece pc = piece_of<LAYOUT>(g, k * NC + b);
-    const char* slot = ring + (size_t)(k % S) * slot_bytes;  // without HOLD the piece is still there
     const float* cs = cstb + (k % NCB) * CST;
     const float2* R = recs + (k % NRB) * nch;
+    const int lane = gr.t & 31, wg = gr.t >> 5, nwg = gr.n >> 5;
     if (P > 1) {
-      const unsigned todo = pre_unit == pc.u ? pre_todo : record_mask(rec_unit, gb);
+      const unsigned todo = pre_unit == pc.u ? pre_todo : record_mask(rec_unit, gr);
       pre_unit = -1;
-      if (!gather_records(p.part + (int64_t)pc.u * rec_unit, recs, todo, p.err, &s_ok_b, gb))
-        return false;
+      if (!gather_records(p.part + (int64_t)pc.u * rec_unit, recs, todo, p.err, flag, gr)) return false;
       R = recs;
     }
     // one warp per group of the unit, over the group's records (lane l takes
@@ -836,7 +844,7 @@ __global__ void __launch_bounds__(kWaveThreads, kWaveCtasPerSm) wave_kernel(cons
           m2 += fmaf(cnt[t] * d, d, v.y);
         }
         m2 = warp_allsum(m2);
-        if (lane == 0) grp[q] = make_float2(mean, 1.0f / sqrtf(m2 / Mg + p.eps));
+        if (lane == 0) gout[q] = make_float2(mean, 1.0f / sqrtf(m2 / Mg + p.eps));
       } else {
         float c1 = 0.f, c2 = 0.f;
         for (int f = lane; f < nrec; f += 32) {
@@ -849,7 +857,7 @@ __global__ void __launch_bounds__(kWaveThreads, kWaveCtasPerSm) wave_kernel(cons
         c1 = warp_allsum(c1);
         c2 = warp_allsum(c2);
         const float r = LAYOUT == kNHWC ? cs[nch + ngrp + q] : cs[Cg + 1];
-        if (lane == 0) grp[q] = coef_from(c1, c2, g, r);
+        if (lane == 0) gout[q] = coef_from(c1, c2, g, r);
       }
     }
     // the unit's first piece also writes its per-channel sums (backward, for
@@ -857,7 +865,7 @@ __global__ void __launch_bounds__(kWaveThreads, kWaveCtasPerSm) wave_kernel(cons
     if (BWD && pc.t == 0 && (p.dgamma || p.dbeta)) {
       const int nchan = LAYOUT == kNHWC ? nch : Cg;
       const int64_t c0 = LAYOUT == kNHWC ? pc.cbase : (int64_t)pc.gi * Cg;
-      for (int c = tg; c < nchan; c += ng) {
+      for (int c = gr.t; c < nchan; c += gr.n) {
         float sa = 0.f, sb = 0.f;
         const int cnt_c = LAYOUT == kNHWC ? P : (int)g.wm;
         for (int t = 0; t < cnt_c; ++t) {
@@ -868,15 +876,26 @@ __global__ void __launch_bounds__(kWaveThreads, kWaveCtasPerSm) wave_kernel(cons
         p.chst[(int64_t)pc.n * g.C + c0 + c] = make_float2(sa, sb);
       }
     }
-    gb.sync();  // the groups' values; the gathered records are read
+    gr.sync();  // the groups' values; the gathered records are read
     if (!BWD && pc.t == 0)
-      for (int q = tg; q < ngrp; q += ng) {
-        p.mean[gbase + q] = grp[q].x;
-        p.rstd[gbase + q] = grp[q].y;
+      for (int q = gr.t; q < ngrp; q += gr.n) {
+        p.mean[gbase + q] = gout[q].x;
+        p.rstd[gbase + q] = gout[q].y;
       }
+    return true;
+  };
+
+  // ---- stage B of piece k: the unit's statistics (merged here, or by the
+  // merge warp), the piece's output
+  auto stage_b = [&](int k) -> bool {
+    const Piece pc = piece_of<LAYOUT>(g, k * NC + b);
+    const char* slot = ring + (size_t)(k % S) * slot_bytes;  // without HOLD the piece is still there
+    const float* cs = cstb + (k % NCB) * CST;
+    if (!MW && !merge_unit(k, gb, &s_ok_b, grp)) return false;
+    const float2* gres = MW ? grp + k % H : grp;  // the unit's per-group results
     // WS: the records of the next piece's unit, read while this one is written
     int nxt_u = -1;
-    if (WS && read_ahead && k + 1 < K) {
+    if (WS && !MW && read_ahead && k + 1 < K) {
       nxt_u = piece_of<LAYOUT>(g, (k + 1) * NC + b).u;
       const float2* src = p.part + (int64_t)nxt_u * rec_unit;
 #pragma unroll
@@ -891,11 +910,11 @@ __global__ void __launch_bounds__(kWaveThreads, kWaveCtasPerSm) wave_kernel(cons
       if (BWD) {
         ca = cs[Cg + 1] * gm;
         cm = cs[Cg];
-        cb = grp[0].x;
-        cd = grp[0].y;
+        cb = gres[0].x;
+        cd = gres[0].y;
       } else {
-        cm = grp[0].x;
-        ca = grp[0].y * gm;
+        cm = gres[0].x;
+        ca = gres[0].y * gm;
         cb = cs[Cg];
         cd = 0.f;
       }
@@ -959,7 +978,7 @@ __global__ void __launch_bounds__(kWaveThreads, kWaveCtasPerSm) wave_kernel(cons
       for (int e = 0; e < VW; ++e) {
         const int cl = j * VW + e;
         const float gm = cs[cl];
-        const float2 gv = grp[qe[e]];
+        const float2 gv = gres[qe[e]];
         if (BWD) {
           ca[e] = cs[nch + ngrp + qe[e]] * gm;
           cm[e] = cs[nch + qe[e]];
@@ -1052,13 +1071,43 @@ __global__ void __launch_bounds__(kWaveThreads, kWaveCtasPerSm) wave_kernel(cons
         issue_next();
         ka = k + 1;
       }
-    } else {
+    } else if (!is_m) {
       for (int k = 0; k < K; ++k) {
         const int h = k % H;
         if (!group_wait(tm_full + h, (uint32_t)((k / H) & 1), p.err, &s_ok_f, gb)) break;
+        if (MW && !group_wait(mg_done + h, (uint32_t)((k / H) & 1), p.err, &s_ok_m, gb)) break;
         tmem_fence_after();
         if (!stage_b(k)) break;
         if (tg == 0) mbar_arrive(tm_empty + h);
+      }
+    } else {
+      // the merge warp: once stage A has piece k in (and so its constants),
+      // the statistics of its unit into grp[k % H]; the records of the next
+      // piece's unit are read while it merges
+      for (int k = 0; k < K; ++k) {
+        const int h = k % H;
+        if (!group_wait(tm_full + h, (uint32_t)((k / H) & 1), p.err, &s_ok_q, gq)) break;
+        int nxt_u = -1;
+        if (read_ahead && k + 1 < K) {
+          nxt_u = piece_of<LAYOUT>(g, (k + 1) * NC + b).u;
+          const float2* src = p.part + (int64_t)nxt_u * rec_unit;
+#pragma unroll
+          for (int i = 0; i < kPre; ++i) pre[i] = tg + i * 32 < rec_unit ? ld_rec_raw(src + tg + i * 32) : 0ull;
+        }
+        if (!merge_unit(k, gq, &s_ok_r, grp + h)) break;
+        gq.sync();  // the merge has read the gathered records
+        if (tg == 0) mbar_arrive(mg_done + h);
+        if (nxt_u >= 0) {
+          unsigned todo = 0;
+#pragma unroll
+          for (int i = 0; i < kPre; ++i) {
+            if (tg + i * 32 >= rec_unit) continue;
+            if (pre[i]) recs[tg + i * 32] = rec_decode(pre[i]);
+            else todo |= 1u << i;
+          }
+          pre_todo = todo;
+          pre_unit = nxt_u;
+        }
       }
     }
   } else {
