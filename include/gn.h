@@ -243,11 +243,13 @@ GN_API int gn_set_timing_events(void* ev_begin, void* ev_mid, void* ev_end);
  * shared memory.  GN_REGIME_WAVE runs one persistent kernel (a cooperative
  * launch; 16-byte aligned fp32 / fp16 / bf16 data) that cuts every reduction
  * unit -- one (n, group) span for NCHW, one (sample, block of whole groups)
- * for NHWC -- into pieces held in the shared memory of several CTAs at once:
- * each CTA reduces its piece, publishes per-channel partial sums, waits
- * (bounded) for the unit's other pieces and writes its output from shared
- * memory, so the input is read from HBM once; it is taken where every unit
- * fits in the shared memory of the co-resident CTAs.  Every regime gives
+ * for NHWC -- into pieces held on chip by several CTAs at once: each CTA
+ * reduces its piece, publishes per-channel partial sums, waits (bounded) for
+ * the unit's other pieces and writes its output from the copy it holds
+ * (in tensor memory where the piece fits there twice, with the reduce and
+ * the output on separate warps), so the input is read from HBM once; it is
+ * taken where every unit fits on the co-resident CTAs, and chosen
+ * automatically for NCHW problems with units of at least 4 MiB.  Every regime gives
  * results within the same tolerances of the definition, each bit-identical
  * from run to run. */
 #define GN_REGIME_AUTO (-1)
