@@ -113,10 +113,16 @@ bool resident_preferred(const Geom& g, int op) {
 
 // The automatic choice of the wave regime (where its plan fits), from
 // measurements on GB300.  It reads each input once; with its pieces held in
-// tensor memory and stage A and stage B on separate warps, it wins for NCHW
-// problems whose units are large: fp32 112x64x512x512 G8, 8 MiB units, runs
-// the forward in 2.67 ms and the backward in 4.36 ms against 3.21 / 5.28 ms
-// two-kernel.  The small channels-last workloads stay with the other
+// tensor memory and stage A and stage B on separate warps, it beats the
+// two-kernel path on every NCHW problem measured from 64 MiB up, forward /
+// backward in us against two-kernel: fp32 112x64x512x512 G8 2593 / 4176
+// against 3191 / 5231; fp32 16x64x512x512 G64 (1 MiB units) 341 / 509
+// against 476 / 784; fp32 32x64x256x256 G8 173 / 302 against 244 / 402;
+// fp32 64x64x128x128 G8 (512 KiB units) 93 / 151 against 150 / 245; fp32
+// 256x64x64x64 G8 (128 KiB units) 219 / 242 against 433 / 587; bf16
+// 8x320x64x64 G32 NCHW 47 / 53 against 69 / 98; fp32 1x64x512x512 G8 (64 MiB)
+// 39 / 54 against 37 / 60.  Smaller inputs are left to the resident and
+// two-kernel paths.  The small channels-last workloads stay with the other
 // families (bf16 8x320x64x64 G32: 50 / 55 us against 29 / 38 us; bf16
 // 32x512x32x32 G32: 38 / 53 us against 32 / 38 us): with a handful of steps
 // per CTA the cooperative launch and the pipeline's fill cost more than the
@@ -124,7 +130,7 @@ bool resident_preferred(const Geom& g, int op) {
 bool wave_preferred(const Geom& g, int op) {
   (void)op;
   const int esz = dtype_size(g.dtype);
-  return g.layout == kNCHW && g.Cg * g.HW * esz >= (4ll << 20);
+  return g.layout == kNCHW && g.Cg * g.HW * esz >= (64ll << 10) && g.N * g.C * g.HW * esz >= (32ll << 20);
 }
 
 // Input that counts as tiny for the automatic choice (see plan_resident).
@@ -408,12 +414,20 @@ struct WaveCut {
 // slot lets a piece land while two are in use.
 int64_t wave_ahead(int64_t H, int64_t S) { return H > 0 ? H - 1 : (S >= 3 ? 1 : 0); }
 
-// Cost model of a wave cut, from measurements on GB300: an SM moves about
-// 45 GB/s (in + out), shared by its CTAs; every step adds about 0.4 us of work that copies do not
-// hide, a unit split over CTAs about 0.3 us more for its arrivals, and
-// unless stage A runs ahead the wait for a unit is exposed (about 1 us).  A unit whose
-// pieces straddle two steps (P not dividing the CTA count) stalls its CTAs
-// for about one piece time.
+// Cost model of a wave cut, in microseconds, fitted to measurements on
+// GB300.  t_io is a step's data at 45 GB/s per SM (in + out), shared by the
+// CTAs on it.  With pieces held in tensor memory and warp specialisation, a
+// step costs about 1.75 us plus half of t_io: the stages overlap the copies,
+// and most of a step is the chain of barriers, record exchange and merge
+// (fp32 NCHW forward, per step: 13.8 KB pieces 2.0 us, 26 KB 2.3, 32 KB 2.3,
+// 52 KB 3.0, 55 KB 3.0).  With only two hold buffers stage A runs one step
+// ahead, and every step waits for the unit's slowest CTA: about 0.4 us more,
+// plus up to 1 us as the unit spreads over all CTAs (backward: 55 KB pieces
+// over 19 CTAs 4.0 us, over 152 CTAs 5.0 us).  A unit straddling two steps
+// costs nothing measurable there.  Without hold buffers: t_io plus 0.4 us a
+// step, 0.3 us more for a unit split over CTAs, about 1 us more when the
+// wait for a unit is exposed (two slots), and a piece time more when a unit
+// straddles two steps.
 #ifndef GN_WAVE_FORCE_CB
 #define GN_WAVE_FORCE_CB 0
 #endif
@@ -421,10 +435,15 @@ int64_t wave_ahead(int64_t H, int64_t S) { return H > 0 ? H - 1 : (S >= 3 ? 1 : 
 #define GN_WAVE_FORCE_P 0
 #endif
 double wave_cost(const WaveCut& c, int64_t NC) {
-  // us at 45 GB/s per SM, shared by the CTAs on it
   const double t_io = (double)(c.slot + c.out) * kWaveCtasPerSm / 45.0e3;
-  double per_step = t_io + 0.4 + (c.P > 1 ? 0.3 : 0.0) + (wave_ahead(c.H, c.S) < 1 ? 1.0 : 0.0);
-  if (c.P > 1 && NC % c.P != 0) per_step += t_io;
+  double per_step;
+  if (c.H > 0 && kWaveWs) {
+    per_step = 1.75 + 0.5 * t_io;
+    if (c.H < 3) per_step += 0.4 + (double)std::min(c.P, NC) / (double)NC;
+  } else {
+    per_step = t_io + 0.4 + (c.P > 1 ? 0.3 : 0.0) + (wave_ahead(c.H, c.S) < 1 ? 1.0 : 0.0);
+    if (c.P > 1 && NC % c.P != 0) per_step += t_io;
+  }
   return (double)c.steps * per_step + t_io;
 }
 

@@ -382,6 +382,34 @@ def test_constant_group_gives_beta(regime):
 # The two small channels-last workloads are compared element by element in
 # full; the two large ones at sampled offsets chosen per (n, g) group and at
 # the boundaries of the plan's items or pieces (see _boundary_offsets).
+# Mid-size NCHW problems that the automatic choice gives to the wave regime,
+# with units of 2 MiB, 256 KiB and 128 KiB, and pieces per unit (32, 56) that
+# do not divide the CTA count, so units straddle two steps.  Compared in full.
+_AFFINE = dict(gamma=("normal", 1.0, 0.1), beta=("normal", 0.0, 0.1))
+MID_WAVE = [
+    ("fp32_nchw_4x64x256x256_g8", synth.WORKLOADS[3].scaled(name="mw0", N=4, H=256, W=256, **_AFFINE)),
+    ("bf16_nchw_16x64x128x128_g8", synth.WORKLOADS[3].scaled(name="mw1", dtype="bf16", N=16, H=128, W=128,
+                                                             **_AFFINE)),
+    ("fp16_nchw_8x32x256x256_g32", synth.WORKLOADS[3].scaled(name="mw2", dtype="f16", N=8, C=32, G=32,
+                                                             H=256, W=256, **_AFFINE)),
+]
+
+
+@pytest.mark.parametrize("name,w", MID_WAVE, ids=[c[0] for c in MID_WAVE])
+def test_mid_size_wave(name, w):
+    plans = [gn.plan_info(op, w.N, w.C, w.HW, w.G, w.layout, w.dtype) for op in (0, 1)]
+    assert all(d.regime == gn.REGIME_WAVE and d.hold_buffers >= 2 for d in plans)
+    inp = synth.make_inputs(w, "cpu", seed=3)
+    got = _gpu_run(inp, w)
+    _compare(got, _oracle_full(inp, w), w)
+
+
+def test_mid_size_wave_straddles():
+    w = MID_WAVE[0][1]
+    d = [gn.plan_info(op, w.N, w.C, w.HW, w.G, w.layout, w.dtype) for op in (0, 1)]
+    assert any(x.ctas % x.pieces_per_unit != 0 for x in d)
+
+
 FULL_COMPARE = {"bf16_nhwc_8x320x64x64_g32", "bf16_nhwc_32x512x32x32_g32"}
 
 
