@@ -703,20 +703,25 @@ __global__ void __launch_bounds__(LAYOUT == kNCHW && MODE == 2 ? kWaveThreads + 
       if constexpr (HOLD) {
         // rows rl + i*rpi, i < T4, of column j also go to tensor memory
         // (zeros past the piece, and for threads without a column)
+        // (ordinary shared-memory loads, which the compiler may run ahead)
         const uint32_t tb = tthr + (uint32_t)(k % H) * bcols;
         for (int i0 = 0; i0 < T4; i0 += 4) {
           uint32_t wx[16], wd[16];
+          uint4 rx[4], rd[4];
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const int r = rl + (i0 + u) * rpi;
-            uint4 rx = make_uint4(0u, 0u, 0u, 0u), rd = rx;
+            rx[u] = rd[u] = make_uint4(0u, 0u, 0u, 0u);
             if (lane_ok && r < pc.len) {
-              rx = lds16(col + (size_t)r * rowb);
-              if (BWD) rd = lds16(col + g.ten_stride + (size_t)r * rowb);
-              add(rx, rd);
+              rx[u] = *reinterpret_cast<const uint4*>(col + (size_t)r * rowb);
+              if (BWD) rd[u] = *reinterpret_cast<const uint4*>(col + g.ten_stride + (size_t)r * rowb);
             }
-            put4(wx, u, rx);
-            if (BWD) put4(wd, u, rd);
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            if (lane_ok && rl + (i0 + u) * rpi < pc.len) add(rx[u], rd[u]);
+            put4(wx, u, rx[u]);
+            if (BWD) put4(wd, u, rd[u]);
           }
           tmem_st16(tb + 4u * (uint32_t)i0, wx);
           if (BWD) tmem_st16(tb + 4u * (uint32_t)(T4 + i0), wd);
@@ -1008,20 +1013,35 @@ __global__ void __launch_bounds__(LAYOUT == kNCHW && MODE == 2 ? kWaveThreads + 
         Access<T, VW>::store(o + (int64_t)r * g.C, xv, pol_out);
       };
       if constexpr (HOLD) {
+        // the tensor-memory loads run one batch ahead, as for NCHW
         const uint32_t tb = tthr + (uint32_t)(k % H) * bcols;
-        for (int i0 = 0; i0 < T4; i0 += 4) {
-          uint32_t wx[16], wd[16];
-          tmem_ld16(tb + 4u * (uint32_t)i0, wx);
-          if constexpr (BWD) tmem_ld16(tb + 4u * (uint32_t)(T4 + i0), wd);
-          tmem_wait_ld();
+        uint32_t xa[16], da[16], xb[16], db[16];
+        auto load = [&](int i0, uint32_t (&xr)[16], uint32_t (&dr)[16]) {
+          tmem_ld16(tb + 4u * (uint32_t)i0, xr);
+          if constexpr (BWD) tmem_ld16(tb + 4u * (uint32_t)(T4 + i0), dr);
+        };
+        auto write = [&](int i0, const uint32_t (&xr)[16], const uint32_t (&dr)[16]) {
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const int r = rl + (i0 + u) * rpi;
             if (lane_ok && r < pc.len) {
-              if constexpr (BWD) put(r, get4(wx, u), get4(wd, u));
-              else put(r, get4(wx, u), get4(wx, u));
+              if constexpr (BWD) put(r, get4(xr, u), get4(dr, u));
+              else put(r, get4(xr, u), get4(xr, u));
             }
           }
+        };
+        load(0, xa, da);
+        tmem_wait_ld();
+        for (int i0 = 0; i0 < T4; i0 += 8) {
+          const bool nb = i0 + 4 < T4;
+          if (nb) load(i0 + 4, xb, db);
+          write(i0, xa, da);
+          tmem_wait_ld();
+          if (!nb) break;
+          const bool na = i0 + 8 < T4;
+          if (na) load(i0 + 8, xa, da);
+          write(i0 + 4, xb, db);
+          tmem_wait_ld();
         }
       } else if (lane_ok) {
 #pragma unroll 2
