@@ -383,8 +383,9 @@ def test_constant_group_gives_beta(regime):
 # full; the two large ones at sampled offsets chosen per (n, g) group and at
 # the boundaries of the plan's items or pieces (see _boundary_offsets).
 # Mid-size NCHW problems that the automatic choice gives to the wave regime,
-# with units of 2 MiB, 256 KiB and 128 KiB, and pieces per unit (32, 56) that
-# do not divide the CTA count, so units straddle two steps.  Compared in full.
+# with units of 2 MiB, 256 KiB, 128 KiB and 8 MiB, and pieces per unit (32,
+# 56) that do not divide the CTA count, so units straddle two steps.
+# Compared in full.
 _AFFINE = dict(gamma=("normal", 1.0, 0.1), beta=("normal", 0.0, 0.1))
 MID_WAVE = [
     ("fp32_nchw_4x64x256x256_g8", synth.WORKLOADS[3].scaled(name="mw0", N=4, H=256, W=256, **_AFFINE)),
@@ -392,6 +393,8 @@ MID_WAVE = [
                                                              **_AFFINE)),
     ("fp16_nchw_8x32x256x256_g32", synth.WORKLOADS[3].scaled(name="mw2", dtype="f16", N=8, C=32, G=32,
                                                              H=256, W=256, **_AFFINE)),
+    # 8 MiB units over every CTA: 8 pieces per CTA cycle through the hold buffers
+    ("fp32_nchw_2x32x512x512_g4", synth.WORKLOADS[3].scaled(name="mw3", N=2, C=32, G=4, **_AFFINE)),
 ]
 
 
