@@ -405,6 +405,7 @@ int64_t wave_ctas(const Geom& g, int op, size_t smem, int sm_count, int want_per
 // time in microseconds.
 struct WaveCut {
   int64_t P = 0, R = 0, m = 1, nb = 1, box = 0, Cb = 0, S = 0, steps = 0, H = 0, T4 = 0;
+  bool fwd = false;
   double cost = 0.0;
   size_t slot = 0, out = 0;
 };
@@ -423,8 +424,8 @@ int64_t wave_ahead(int64_t H, int64_t S) { return H > 0 ? H - 1 : (S >= 3 ? 1 : 
 // 52 KB 3.0, 55 KB 3.0).  With only two hold buffers stage A runs one step
 // ahead, and every step waits for the unit's slowest CTA: about 0.4 us more,
 // plus up to 1 us as the unit spreads over all CTAs (backward: 55 KB pieces
-// over 19 CTAs 4.0 us, over 152 CTAs 5.0 us).  A unit straddling two steps
-// costs nothing measurable there.  Without hold buffers: t_io plus 0.4 us a
+// over 19 CTAs 4.0 us, over 152 CTAs 5.0 us).  A unit over a small share of
+// the CTAs straddling two steps costs nothing measurable there.  Without hold buffers: t_io plus 0.4 us a
 // step, 0.3 us more for a unit split over CTAs, about 1 us more when the
 // wait for a unit is exposed (two slots), and a piece time more when a unit
 // straddles two steps.
@@ -440,6 +441,12 @@ double wave_cost(const WaveCut& c, int64_t NC) {
   if (c.H > 0 && kWaveWs) {
     per_step = 1.75 + 0.5 * t_io;
     if (c.H < 3) per_step += 0.4 + (double)std::min(c.P, NC) / (double)NC;
+    // forward: a unit over more than half of the CTAs that straddles two
+    // steps holds up the merge of most CTAs (fp32 NCHW 112x64x512x512 G8:
+    // 104 pieces per unit 4.4 us a step, 152 pieces 2.9 us).  The backward
+    // measured the other way (bf16 NCHW 32x64x512x512 G8: 104 pieces 4.05
+    // us a step for 121 KB, 152 pieces 3.24 us for 83 KB).
+    if (c.fwd && c.P > NC / 2 && NC % c.P != 0) per_step += 0.3 * t_io;
   } else {
     per_step = t_io + 0.4 + (c.P > 1 ? 0.3 : 0.0) + (wave_ahead(c.H, c.S) < 1 ? 1.0 : 0.0);
     if (c.P > 1 && NC % c.P != 0) per_step += t_io;
@@ -516,6 +523,7 @@ bool plan_wave(Geom& g, int op, int sm_count) {
     if (c.P * (g.layout == kNHWC ? c.Cb : 1) > 32 * wave_stage_threads(kWaveWs)) return;
     if (GN_WAVE_FORCE_CB > 0 && g.layout == kNHWC && c.Cb != GN_WAVE_FORCE_CB) return;
     if (GN_WAVE_FORCE_P > 0 && c.P != GN_WAVE_FORCE_P) return;
+    c.fwd = op == kFwd;
     wave_hold(g, c, nten, vec);
     const size_t fixed = wave_fixed_bytes(g, c.P, c.Cb, vec, c.H);
     if (fixed + 128 + 2 * c.slot > budget) return;
