@@ -327,6 +327,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// The same test, letting the hardware suspend the thread for up to `hint_ns`
+// nanoseconds while the phase is incomplete (fewer polls, more issue slots
+// for the other warps of the SM).
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
 // Waits for phase `parity` of `bar` to complete.  The wait is bounded: after
 // kMbarWaitLimit polls (far longer than any copy takes) it raises the error
 // word and returns false instead of hanging.

@@ -197,7 +197,9 @@ __device__ bool group_wait(uint64_t* bar, uint32_t parity, unsigned* err, int* f
     if (!mbar_try_wait(bar, parity)) {
       const uint64_t t0 = now_ns();
       for (unsigned i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity)) break;
+        // suspended for up to 2 us a test: the waiting warp leaves its issue
+        // slots to the other stage (c3 backward 4.20 -> 3.98 ms)
+        if (mbar_try_wait_hint(bar, parity, 2000u)) break;
         if ((i & 15u) == 0u) {
           if (aborted(err)) {
             go = 0;
