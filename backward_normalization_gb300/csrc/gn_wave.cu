@@ -1,6 +1,7 @@
 // gn_wave.cu -- the wave regime: one persistent kernel per op that reads its
 // input from HBM once and writes its output once, for problems whose
-// reduction units fit in the shared memory of the CTAs that share them.
+// reduction units fit on chip (shared and tensor memory) across the CTAs
+// that share them.
 //
 // Work.  A reduction unit is one (sample, group) span for NCHW -- Cg
 // contiguous channel planes -- or one (sample, block of Cb channels made of
@@ -9,8 +10,8 @@
 // consecutive segments of each plane (P = Cg*wm), for NHWC blocks of wR
 // rows.  Pieces are numbered unit-major, q = u*P + t, and CTA b of the NC
 // co-resident CTAs takes pieces q = k*NC + b for k = 0, 1, ... (its steps).
-// The plan makes P divide NC where it can, so that the pieces of a unit all
-// belong to one step and arrive together.
+// The plan picks P by a cost model fitted to measurements; a unit whose P
+// does not divide NC straddles two steps.
 //
 // Per piece: bulk (TMA) copies bring it into one of S shared-memory slots
 // (all slots are kept loading); stage A reduces the piece and writes one
@@ -30,7 +31,11 @@
 // the reduce of one piece (shared-memory reads, tensor-memory writes)
 // overlaps the output of an earlier one (tensor-memory reads, global
 // stores).  Per hold buffer an mbarrier `tm_full` tells stage B that a piece
-// is in, and `tm_empty` tells stage A that it has been written out.  Without
+// is in, and `tm_empty` tells stage A that it has been written out.  For
+// NCHW a ninth warp gathers and merges each unit's records into a result per
+// hold buffer (`mg_done`), so that stage B only writes.  Waiting threads are
+// suspended by the hardware (mbarrier try_wait with a time hint) rather than
+// spinning, which leaves issue slots to the working stage.  Without
 // hold buffers the CTA runs the stages in turn, stage A one piece ahead of
 // stage B when a third slot is free, and the piece waits in its slot.
 //
