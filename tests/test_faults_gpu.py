@@ -20,8 +20,13 @@ from tests import checks
 
 pytestmark = pytest.mark.gpu
 
-# a wave-regime problem whose units are split over several CTAs
+# wave-regime problems whose units are split over several CTAs: channels-last
+# (stage B merges), and NCHW (the merge warp merges; several pieces per CTA,
+# so stage A also waits for hold buffers)
 W = synth.WORKLOADS[2].scaled(name="fault2", N=2, H=32, W=32)
+W_NCHW = synth.WORKLOADS[3].scaled(name="fault3", N=2, H=256, W=256,
+                                   gamma=("normal", 1.0, 0.1), beta=("normal", 0.0, 0.1))
+CASES = [pytest.param(W, id="nhwc"), pytest.param(W_NCHW, id="nchw")]
 
 
 def _oracle(inp, w):
@@ -57,8 +62,8 @@ def _calls(inp, w, ws):
     return (rc_f, st_f, rc_b, st_b), dict(y=y, mean=mean, rstd=rstd, dx=dx, dgamma=dg, dbeta=db)
 
 
-def test_stalled_unit_is_reported_and_the_next_call_is_correct(wave):
-    w = W
+@pytest.mark.parametrize("w", CASES)
+def test_stalled_unit_is_reported_and_the_next_call_is_correct(wave, w):
     for op in (gn.OP_FWD, gn.OP_BWD):
         d = gn.plan_info(op, w.N, w.C, w.HW, w.G, w.layout, w.dtype)
         assert d.regime == gn.REGIME_WAVE and d.pieces_per_unit > 1
@@ -83,8 +88,8 @@ def test_stalled_unit_is_reported_and_the_next_call_is_correct(wave):
     checks.assert_param("dgamma", got["dgamma"], ref["dgamma"])
 
 
-def test_stalled_backward_is_reported(wave):
-    w = W
+@pytest.mark.parametrize("w", CASES)
+def test_stalled_backward_is_reported(wave, w):
     inp = synth.make_inputs(w, "cpu", seed=32)
     ws = gn.alloc_workspace(gn.OP_BWD, w.N, w.C, w.HW, w.G, w.layout, w.dtype)
     x, dy = inp["x"].cuda(), inp["dy"].cuda()
