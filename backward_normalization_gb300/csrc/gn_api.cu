@@ -15,7 +15,8 @@ thread_local gn::TimingEvents t_events = {nullptr, nullptr, nullptr};
 // Fault injection (test hook).  GN_FAULT_LAUNCH makes every call fail with
 // GN_ERR_CUDA after validation and before anything is enqueued, as a failed
 // launch would; GN_FAULT_STALL makes the next wave-regime call withhold one
-// arrival, so that the bounded waits on that unit run out.  The environment
+// arrival (the next flat-regime call one chunk copy), so that the bounded
+// waits on it run out.  The environment
 // variable GN_FAULT_INJECT=launch sets GN_FAULT_LAUNCH at the first call.
 std::atomic<int> g_fault{-1};  // -1: not read from the environment yet
 
@@ -110,14 +111,14 @@ __global__ void __launch_bounds__(256) ws_clear(unsigned* ws, int words) {
   for (int i = threadIdx.x; i < words; i += blockDim.x) ws[i] = 0u;
 }
 
-// Enqueues the workspace clear, then the plan's kernel(s).  The wave
-// regime's kernel clears its counters itself (behind a grid barrier of its
-// cooperative launch) and needs no separate clear.
+// Enqueues the workspace clear, then the plan's kernel(s).  The wave and
+// flat regimes' kernels clear what they use themselves (ordered by a grid
+// barrier of their cooperative launch) and need no separate clear.
 cudaError_t launch(const gn::KParams& p, cudaStream_t s, bool bwd) {
   const bool nhwc = p.g.layout == GN_LAYOUT_NHWC;
   const gn::TimingEvents& ev = gn::timing_events();
   if (ev.begin) cudaEventRecord(ev.begin, s);
-  if (p.g.regime != gn::kRegimeWave) {
+  if (p.g.regime != gn::kRegimeWave && p.g.regime != gn::kRegimeFlat) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(1, 1, 1);
     cfg.blockDim = dim3(256, 1, 1);
@@ -134,6 +135,7 @@ cudaError_t launch(const gn::KParams& p, cudaStream_t s, bool bwd) {
     case gn::kRegimeResident: return gn::launch_resident(p, s, bwd);
     case gn::kRegimePipelined: return gn::launch_nchw_pipelined(p, s, bwd);
     case gn::kRegimeWave: return gn::launch_wave(p, s, bwd);
+    case gn::kRegimeFlat: return gn::launch_flat(p, s, bwd);
     default: return nhwc ? gn::launch_nhwc(p, s, bwd) : gn::launch_nchw(p, s, bwd);
   }
 }
@@ -397,7 +399,7 @@ int gn_workspace_status(const void* workspace, void* stream) {
 
 int gn_set_regime(int regime) {
   if (regime != GN_REGIME_AUTO && regime != GN_REGIME_TWO_KERNEL && regime != GN_REGIME_RESIDENT &&
-      regime != GN_REGIME_PIPELINED && regime != GN_REGIME_WAVE)
+      regime != GN_REGIME_PIPELINED && regime != GN_REGIME_WAVE && regime != GN_REGIME_FLAT)
     return GN_ERR_INVALID;
   gn::set_regime_override(regime);
   return GN_OK;
@@ -421,13 +423,14 @@ int gn_plan_info(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout
   const gn::Geom g = gn::make_geom(op, N, C, HW, G, layout, dtype, aligned != 0);
   out->regime = g.regime;
   // the plan's kernels, plus the workspace clear that precedes every regime
-  // but the wave regime (whose kernel clears its counters itself)
-  out->launches = (g.regime == gn::kRegimeGeneric ? 2 : 1) + (g.regime == gn::kRegimeWave ? 0 : 1);
+  // but the wave and flat regimes (whose kernels clear what they use)
+  const bool self_clear = g.regime == gn::kRegimeWave || g.regime == gn::kRegimeFlat;
+  out->launches = (g.regime == gn::kRegimeGeneric ? 2 : 1) + (self_clear ? 0 : 1);
   out->vector_width = g.vw;
   out->threads = g.tpb;
-  out->ctas = g.regime == gn::kRegimeResident                                     ? g.units * g.K
-              : (g.regime == gn::kRegimePipelined || g.regime == gn::kRegimeWave) ? g.grid
-                                                                                  : g.items;
+  const bool persistent = g.regime == gn::kRegimePipelined || g.regime == gn::kRegimeWave ||
+                          g.regime == gn::kRegimeFlat;
+  out->ctas = g.regime == gn::kRegimeResident ? g.units * g.K : persistent ? g.grid : g.items;
   out->partials = g.N * g.C * (g.T + (g.l1 > 1 ? g.Tp : 0));
   out->workspace_bytes = gn::ws_layout(op, g).total;
   out->err_offset = gn::ws_layout(op, g).err;
@@ -443,6 +446,10 @@ int gn_plan_info(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout
   if (g.regime == gn::kRegimeWave) {
     out->piece_elems = g.wR;
     out->pieces_per_unit = g.wP;
+  } else if (g.regime == gn::kRegimeFlat) {
+    const int64_t R = g.N * g.HW, run = (R + g.grid - 1) / g.grid;
+    out->piece_elems = g.chunk;
+    out->pieces_per_unit = (run + g.chunk - 1) / g.chunk;
   } else if (g.regime == gn::kRegimeResident) {
     out->piece_elems = g.slice;
     out->pieces_per_unit = g.K;
@@ -458,7 +465,7 @@ int gn_plan_info(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout
   }
   if (g.regime == gn::kRegimeResident) {
     out->smem_bytes = g.smem;
-  } else if (g.regime == gn::kRegimePipelined || g.regime == gn::kRegimeWave) {
+  } else if (persistent) {
     out->smem_bytes = g.smem;
   } else {
     size_t sm = 0;

@@ -29,6 +29,8 @@ enum Regime {
   kRegimeWave = 3,      // one persistent kernel: every piece of a unit stays on
                         // chip (shared or tensor memory) until the unit's
                         // statistics are known
+  kRegimeFlat = 4,      // one cooperative kernel (channels-last): every SM holds an
+                        // equal run of rows, one grid barrier between the passes
 };
 
 // How one call is cut into "items" for the two-kernel path.  Both kernels
@@ -111,6 +113,12 @@ struct Geom {
   // per-piece constants.  wWs = 1: stage A and stage B run on separate halves
   // of the CTA (warp specialisation), handing pieces over through mbarriers.
   int64_t wP, wR, wm, wnb, wcols, wH, wT, wB, wWs;
+  // flat regime (gn_flat.cu): `grid` CTAs take equal runs of the N*HW rows,
+  // read as chunks of `chunk` rows into S slots of ten_stride bytes per
+  // tensor.  fSeg: most samples one CTA's run touches (its segments);
+  // fNgv: most groups one 16-byte column spans.
+  int64_t fSeg;
+  int fNgv;
 };
 
 // Bytes reserved per ring-slot header of the pipelined kernel (the header
@@ -266,6 +274,15 @@ constexpr int kWaveTmemCols = 512 / GN_WAVE_CTAS_PER_SM;
 static_assert(kWaveTmemCols >= 32 && (kWaveTmemCols & (kWaveTmemCols - 1)) == 0,
               "a tensor-memory allocation is a power of two of at least 32 columns");
 static_assert(kWaveThreads % 128 == 0, "whole warp quarters share the tensor-memory lanes");
+// gn_flat.cu
+const void* flat_kernel_ptr(const Geom& g, bool bwd);
+cudaError_t launch_flat(const KParams& p, cudaStream_t s, bool bwd);
+// Most ring slots of a flat-regime CTA, and the bytes its shared-memory
+// bookkeeping (mbarriers, fill counts, flags) takes after the tables.
+constexpr int kFlatMaxSlots = 32;
+constexpr size_t kFlatBookBytes = 8 * kFlatMaxSlots + 4 * 2 * kFlatMaxSlots + 16;
+// Threads of a flat-regime CTA at most (a whole number of row lanes of C/vw columns).
+constexpr int kFlatThreads = 512;
 // gn_resident.cu
 // [N*HW, C] view of an NHWC tensor for TMA, boxes of [g.chunk rows, g.Cb channels].
 cudaError_t encode_nhwc_map(CUtensorMap* map, const void* base, const Geom& g);
@@ -273,6 +290,10 @@ const void* resident_kernel_ptr(const Geom& g, bool bwd);
 cudaError_t launch_resident(const KParams& p, cudaStream_t s, bool bwd);
 // Threads of a resident CTA: the consumer warps plus one producer warp.
 inline int resident_threads(const Geom& g) { return (g.tpb + 31) / 32 * 32 + 32; }
+// Raises a kernel's dynamic shared memory limit to at least `smem` bytes on
+// the current device; remembered per (device, kernel), so that launches after
+// the first make no attribute call.
+cudaError_t prepare_smem(const void* kernel, size_t smem);
 // Sets the kernel attributes a resident launch needs (large shared memory,
 // 16-CTA clusters); idempotent.
 cudaError_t prepare_resident_kernel(const void* kernel, const Geom& g);

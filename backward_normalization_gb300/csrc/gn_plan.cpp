@@ -42,6 +42,21 @@ int64_t resident_or(const Geom& g, int op, int second, int sm_count) {
 
 void set_regime_override(int regime) { g_regime_override.store(regime); }
 
+cudaError_t prepare_smem(const void* kernel, size_t smem) {
+  static std::mutex mu;
+  static std::map<std::pair<int, const void*>, size_t> done;  // (device, kernel) -> limit set
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = done.find({dev, kernel});
+  if (it != done.end() && it->second >= smem) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  done[{dev, kernel}] = smem;
+  return cudaSuccess;
+}
+
 cudaError_t prepare_resident_kernel(const void* kernel, const Geom& g) {
   static std::mutex mu;
   static std::map<std::pair<int, const void*>, size_t> done;  // (device, kernel) -> smem set
@@ -131,6 +146,20 @@ bool wave_preferred(const Geom& g, int op) {
   (void)op;
   const int esz = dtype_size(g.dtype);
   return g.layout == kNCHW && g.Cg * g.HW * esz >= (64ll << 10) && g.N * g.C * g.HW * esz >= (32ll << 20);
+}
+
+// The automatic choice of the flat regime, from measurements on GB300 (L2
+// flushed before each call): channels-last backwards whose x and dy hold
+// 10-48 MiB together, where its one launch and minimal HBM traffic beat the
+// two-kernel path (bf16 8x320x64x64 G32: 38.6 against 41.8 us; at N = 2,
+// 26.0 against 35.1 us).  Larger backwards lose to the two-kernel path (at
+// 64 MiB, 32x512x32x32: 53 against 38 us: pass 2 reads most chunks again
+// and the merge and second barrier cost more than the saved launch), and
+// forwards lose to the resident or two-kernel path (8x320x64x64: 34.7
+// against 23.2 us resident).
+bool flat_preferred(const Geom& g, int op) {
+  const double in = 2.0 * (double)g.N * (double)g.C * (double)g.HW * dtype_size(g.dtype);
+  return op == kBwd && g.layout == kNHWC && in >= 10.0 * (1 << 20) && in <= 48.0 * (1 << 20);
 }
 
 // Input that counts as tiny for the automatic choice (see plan_resident).
@@ -391,8 +420,7 @@ int64_t wave_ctas(const Geom& g, int op, size_t smem, int sm_count, int want_per
   }
   const void* fn = wave_kernel_ptr(g, op == kBwd);
   int nb = 0;
-  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-          cudaSuccess ||
+  if (prepare_smem(fn, smem) != cudaSuccess ||
       cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fn, g.tpb, smem) != cudaSuccess) {
     cudaGetLastError();
     return 0;
@@ -636,6 +664,117 @@ bool plan_wave(Geom& g, int op, int sm_count) {
   g = r;
   return true;
 }
+
+// Co-resident CTAs of a flat-regime plan (one per SM at most); the SM count
+// when no device is visible.
+int64_t flat_ctas(const Geom& g, int op, int sm_count) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return sm_count;
+  }
+  const void* fn = flat_kernel_ptr(g, op == kBwd);
+  int nb = 0;
+  if (prepare_smem(fn, g.smem) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fn, g.tpb, g.smem) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return (int64_t)std::min(nb, 1) * sm_count;
+}
+
+// Slot bytes per tensor of a flat-regime ring, and the chunks of a run that
+// the forward keeps when the whole run fits in shared memory.
+constexpr int64_t kFlatSlotBytes = 16 << 10;
+constexpr int64_t kFlatWholeChunks = 8;
+
+// Fills the flat-regime fields of g (gn_flat.cu); false when the problem does
+// not fit the regime: dense, 16-byte aligned channels-last fp32 / fp16 / bf16
+// data of at most kFlatThreads 16-byte columns per row, and per-segment
+// tables that fit in shared memory.  One CTA per SM takes an equal run of the
+// N*HW rows.  The forward keeps its whole run in shared memory when it fits
+// (kFlatWholeChunks chunks); otherwise, and for the backward, the run streams
+// through a ring of as many kFlatSlotBytes slots (per tensor) as fit.
+bool plan_flat(Geom& g, int op, int sm_count) {
+  const int esz = dtype_size(g.dtype);
+  const int vec = 16 / esz;
+  if (g.layout != kNHWC || g.dtype == kF64 || g.vw != vec) return false;
+  const int64_t V = g.C / vec;
+  if (V > kFlatThreads) return false;
+  const int64_t R = g.N * g.HW;
+  const int64_t NB = std::min<int64_t>(sm_count, R);
+  if (NB < 1) return false;
+  const bool bwd = op == kBwd;
+  const int nten = bwd ? 2 : 1;
+  Geom r = g;
+  r.regime = kRegimeFlat;
+  r.V = V;
+  r.Wv = (int)V;
+  r.ncb = 1;
+  r.rpi = (int)std::max<int64_t>(1, kFlatThreads / V);
+  r.tpb = r.rpi * r.Wv;
+  int64_t segmax = 0, ngv = 0;
+  for (int64_t b = 0; b < NB; ++b) {
+    const int64_t a = b * R / NB, z = (b + 1) * R / NB;
+    segmax = std::max(segmax, (z - 1) / g.HW - a / g.HW + 1);
+  }
+  for (int64_t j = 0; j < V; ++j)
+    ngv = std::max(ngv, (j * vec + vec - 1) / g.Cg - j * vec / g.Cg + 1);
+  r.fSeg = segmax;
+  r.fNgv = (int)ngv;
+  const int64_t rowb = g.C * esz;
+  const int64_t rmax = cdiv(R, NB);
+  const int64_t sgn = segmax * g.G;
+  const size_t red = bwd ? (size_t)2 * vec * (r.tpb + 1) * 4 : (size_t)ngv * r.tpb * 8;
+  const size_t tab = 4 * (bwd ? (size_t)(4 * sgn + 2 * g.C) : (size_t)(2 * sgn + g.G));
+  const size_t runs = a128((size_t)(NB + 1) * 8) + a128((size_t)NB * 8);  // run table
+  const size_t fixed = a128(red) + a128(tab) + runs + a128(kFlatBookBytes) + 128;
+  if (fixed + 1024 > kSmemPerCta || tab > (32u << 10)) return false;
+  const int64_t whole = cdiv(rmax, kFlatWholeChunks);
+  const size_t whole_slot = a128((size_t)(whole * rowb));
+  int64_t chunk, S;
+  if (!bwd && fixed + (size_t)cdiv(rmax, whole) * whole_slot <= kSmemPerCta) {
+    chunk = whole;
+    S = cdiv(rmax, whole);
+  } else {
+    chunk = std::max<int64_t>(1, kFlatSlotBytes / rowb);
+    const size_t slot = a128((size_t)(chunk * rowb)) * nten;
+    S = std::min<int64_t>((int64_t)((kSmemPerCta - fixed) / slot), kFlatMaxSlots);
+    S = std::min<int64_t>(S, cdiv(rmax, chunk));
+    if (S < 2 && cdiv(rmax, chunk) > 1) return false;
+  }
+  if (chunk * rowb * nten >= (1 << 20)) return false;  // one mbarrier phase's byte count
+  r.chunk = chunk;
+  r.S = (int)S;
+  r.ten_stride = (int64_t)a128((size_t)(chunk * rowb));
+  size_t off = 0;
+  r.off_ring = off;
+  off += (size_t)S * (size_t)r.ten_stride * nten;
+  r.off_red = off;
+  off += a128(red);
+  r.off_grp = off;
+  off += a128(tab);
+  r.off_tot = off;
+  off += runs;
+  r.off_bar = off;
+  off += a128(kFlatBookBytes);
+  r.smem = off + 128;  // slack for aligning the dynamic shared memory base
+  if (r.smem > kSmemPerCta) return false;
+  // records: one per (CTA, segment) and group (forward) or channel (backward),
+  // in the workspace's partial-sum region
+  const int64_t recs = NB * segmax * (bwd ? g.C : g.G);
+  r.l1 = 1;
+  r.Tp = cdiv(recs, g.N * g.C);
+  r.T = r.Tp;
+  r.groups1 = 0;
+  r.units_fin = 0;
+  r.unit_groups = 0;
+  r.fin2 = 0;
+  r.grid = NB;
+  if (flat_ctas(r, op, sm_count) < NB) return false;
+  g = r;
+  return true;
+}
 }  // namespace
 
 int64_t plan_max_clusters(const Geom& g, int op) {
@@ -843,7 +982,11 @@ Geom plan_geom(int op, int64_t N, int64_t C, int64_t HW, int64_t G, int layout, 
     plan_pipelined(g, op, sm_count);
   } else if (ov == kRegimeWave) {
     plan_wave(g, op, sm_count);
+  } else if (ov == kRegimeFlat) {
+    plan_flat(g, op, sm_count);
   } else if (ov == kRegimeAuto && wave_preferred(g, op) && plan_wave(g, op, sm_count)) {
+    // taken
+  } else if (ov == kRegimeAuto && flat_preferred(g, op) && plan_flat(g, op, sm_count)) {
     // taken
   } else if (ov == kRegimeAuto && resident_preferred(g, op)) {
     // measured on GB300: the pipelined kernel moves the minimal traffic but is

@@ -1251,7 +1251,7 @@ cudaError_t launch_wave(const KParams& p_in, cudaStream_t s, bool bwd) {
     if (e != cudaSuccess) return e;
   }
   const void* fn = wave_kernel_ptr(g, bwd);
-  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)g.smem);
+  e = prepare_smem(fn, g.smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)g.grid, 1, 1);

@@ -199,7 +199,8 @@ def bwd_ex_raw(dy, dy_s, x, x_s, mean, rstd, gamma, N, C, HW, G, layout, dx, dx_
                            _ptr(workspace), ws_bytes, _stream(stream))
 
 
-REGIME_AUTO, REGIME_TWO_KERNEL, REGIME_RESIDENT, REGIME_PIPELINED, REGIME_WAVE = -1, 0, 1, 2, 3
+REGIME_AUTO, REGIME_TWO_KERNEL, REGIME_RESIDENT, REGIME_PIPELINED, REGIME_WAVE, REGIME_FLAT = \
+    -1, 0, 1, 2, 3, 4
 
 
 def set_regime(regime: int) -> None:

@@ -44,14 +44,14 @@ def min_bytes(w):
     return {"fwd": 2 * e, "bwd": 3 * e}
 
 
-REGIME_NAMES = {0: "two-kernel", 1: "resident", 2: "pipelined", 3: "wave"}
+REGIME_NAMES = {0: "two-kernel", 1: "resident", 2: "pipelined", 3: "wave", 4: "flat"}
 
 
 def kernel_bytes(w, fwd_regime=0, bwd_regime=0):
     """Algorithmic bytes of each kernel (what it must move at least).  The
-    two-kernel path reads its input twice by construction; the resident and
-    pipelined regimes run one kernel per op that moves the op's minimal
-    traffic."""
+    two-kernel path reads its input twice by construction; the resident,
+    pipelined, wave and flat regimes run one kernel per op that moves the op's
+    minimal traffic."""
     e = w.E * esize(w.dtype)
     kb = {}
     if fwd_regime == 0:

@@ -205,6 +205,8 @@ GN_API int gn_workspace_status(const void* workspace, void* stream);
  *                   withholds the arrival of one piece of unit 0, so the waits
  *                   on that unit run out: that call's outputs for unit 0 are
  *                   not valid and gn_workspace_status reports GN_ERR_TIMEOUT.
+ *                   On the flat regime it withholds CTA 0's first copy: the
+ *                   call's outputs are not valid and the status is the same.
  *                   The mode then returns to GN_FAULT_NONE by itself.
  * Nothing here faults the GPU: every injected failure is made on the host, or
  * is a wait that nothing satisfies and that gives up within its bound.
@@ -249,7 +251,16 @@ GN_API int gn_set_timing_events(void* ev_begin, void* ev_mid, void* ev_end);
  * (in tensor memory where the piece fits there twice, with the reduce and
  * the output on separate warps), so the input is read from HBM once; it is
  * taken where every unit fits on the co-resident CTAs, and chosen
- * automatically for NCHW problems with units of at least 4 MiB.  Every regime gives
+ * automatically for NCHW problems with units of at least 4 MiB.  GN_REGIME_FLAT
+ * runs one cooperative kernel for dense, 16-byte aligned channels-last fp32 /
+ * fp16 / bf16 data of at most 512 16-byte vectors per row: the N*HW rows are
+ * cut into equal runs, one per SM, each read by bulk copies into shared
+ * memory; every CTA writes per-group (forward) or per-channel (backward)
+ * partial sums for the samples its run touches, one grid-wide barrier
+ * separates that from the merge, and the output is written from the chunks
+ * still held (the others are read again, from L2); it is chosen
+ * automatically for channels-last backwards whose x and dy hold 10-48 MiB
+ * together.  Every regime gives
  * results within the same tolerances of the definition, each bit-identical
  * from run to run. */
 #define GN_REGIME_AUTO (-1)
@@ -257,17 +268,18 @@ GN_API int gn_set_timing_events(void* ev_begin, void* ev_mid, void* ev_end);
 #define GN_REGIME_RESIDENT 1
 #define GN_REGIME_PIPELINED 2
 #define GN_REGIME_WAVE 3
+#define GN_REGIME_FLAT 4
 
 /* Test hook, process-wide: GN_REGIME_AUTO (default) lets each call choose
  * the faster family for its shape; GN_REGIME_TWO_KERNEL forces the two-kernel
- * path; GN_REGIME_RESIDENT, GN_REGIME_PIPELINED and GN_REGIME_WAVE force that regime wherever
+ * path; GN_REGIME_RESIDENT, GN_REGIME_PIPELINED, GN_REGIME_WAVE and GN_REGIME_FLAT force that regime wherever
  * the problem fits it (else the two-kernel path runs).  Not thread-safe with respect to
  * calls in flight on other threads.  Returns a gn_status. */
 GN_API int gn_set_regime(int regime);
 
 /* What a call would run, for tests and reports (host-only, no launch). */
 typedef struct gn_plan_desc {
-  int regime;            /* GN_REGIME_TWO_KERNEL, _RESIDENT, _PIPELINED or _WAVE */
+  int regime;            /* GN_REGIME_TWO_KERNEL, _RESIDENT, _PIPELINED, _WAVE or _FLAT */
   int launches;          /* kernels one call enqueues, the workspace clear included */
   int vector_width;      /* elements per access: 16-byte vectors, or 1 (scalar path) */
   int threads;           /* threads per CTA */
@@ -285,9 +297,11 @@ typedef struct gn_plan_desc {
   int level1_items;      /* items merged per level-1 record (1: none) */
   size_t clear_bytes;    /* bytes at the start of the workspace (error word and
                             counters) that the call zero-fills before its kernels */
-  int64_t piece_elems;   /* wave regime: elements (NCHW) or rows (NHWC) per piece */
-  int64_t pieces_per_unit; /* wave regime: pieces of one reduction unit */
-  int slots;             /* resident / pipelined / wave regimes: shared-memory slots per CTA */
+  int64_t piece_elems;   /* wave regime: elements (NCHW) or rows (NHWC) per piece;
+                            flat regime: rows per chunk */
+  int64_t pieces_per_unit; /* wave regime: pieces of one reduction unit; flat
+                            regime: chunks of the longest run */
+  int slots;             /* resident / pipelined / wave / flat regimes: shared-memory slots per CTA */
   int hold_buffers;      /* wave regime: tensor-memory buffers holding reduced pieces
                             (0: a piece waits for its unit's statistics in its slot) */
 } gn_plan_desc;

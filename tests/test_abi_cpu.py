@@ -158,6 +158,12 @@ def test_regime_choice(gn):
         assert d.regime == 3 and d.launches == 1
     finally:
         gn.set_regime(gn.REGIME_AUTO)
+    gn.set_regime(gn.REGIME_FLAT)
+    try:
+        d = gn.plan_info(1, 8, 320, 4096, 32, "nhwc", "bf16")
+        assert d.regime == 4 and d.launches == 1
+    finally:
+        gn.set_regime(gn.REGIME_AUTO)
     with pytest.raises(gn.GnError):
         gn.set_regime(7)
 
@@ -204,7 +210,7 @@ def test_f64_storage_plans(gn):
     assert gn.plan_info(1, 3, 40, 99, 8, "nhwc", "f64").vector_width == 2
     assert gn.plan_info(1, 2, 3, 25, 3, "nhwc", "f64").vector_width == 1   # 3 doubles: not 16 B
     assert gn.plan_info(0, 2, 6, 63, 3, "nchw", "f64").vector_width == 1   # 63 doubles per plane
-    for reg in (gn.REGIME_RESIDENT, gn.REGIME_PIPELINED, gn.REGIME_WAVE):
+    for reg in (gn.REGIME_RESIDENT, gn.REGIME_PIPELINED, gn.REGIME_WAVE, gn.REGIME_FLAT):
         gn.set_regime(reg)
         try:
             assert gn.plan_info(1, 2, 16, 4096, 4, "nchw", "f64").regime == 0
@@ -218,9 +224,10 @@ def test_f64_storage_plans(gn):
 
 def test_automatic_choice(gn):
     """The automatic choice: the wave regime for NCHW problems of at least
-    32 MiB with units of at least 64 KiB; the resident regime for channels-last forwards and
-    small NCHW units when one wave of clusters covers every unit (or the
-    input is tiny); the two-kernel path otherwise."""
+    32 MiB with units of at least 64 KiB; the flat regime for channels-last
+    backwards of 10-48 MiB (x and dy); the resident regime for channels-last
+    forwards and small NCHW units when one wave of clusters covers every unit
+    (or the input is tiny); the two-kernel path otherwise."""
     assert gn.plan_info(1, 112, 64, 512 * 512, 8, "nchw", "f32").regime == 3   # 8 MiB units
     assert gn.plan_info(0, 112, 64, 512 * 512, 8, "nchw", "f32").regime == 3
     assert gn.plan_info(0, 16, 64, 512 * 512, 64, "nchw", "f32").regime == 3   # 1 MiB units
@@ -230,7 +237,11 @@ def test_automatic_choice(gn):
     assert gn.plan_info(0, 512, 32, 256, 8, "nchw", "f32").regime == 0      # 4096 units
     assert gn.plan_info(0, 8, 320, 4096, 32, "nhwc", "bf16").regime == 1    # 32 clusters
     assert gn.plan_info(0, 64, 320, 4096, 32, "nhwc", "bf16").regime == 0   # 256 clusters
-    assert gn.plan_info(1, 8, 320, 4096, 32, "nhwc", "bf16").regime == 0
+    assert gn.plan_info(1, 8, 320, 4096, 32, "nhwc", "bf16").regime == 4   # 40 MiB backward
+    assert gn.plan_info(1, 2, 320, 4096, 32, "nhwc", "bf16").regime == 4   # 10 MiB
+    assert gn.plan_info(1, 32, 512, 1024, 32, "nhwc", "bf16").regime == 0  # 64 MiB
+    assert gn.plan_info(1, 1, 320, 4096, 32, "nhwc", "bf16").regime != 4   # 5 MiB
+    assert gn.plan_info(1, 8, 320, 4096, 32, "nhwc", "bf16", aligned=False).regime == 0
     assert gn.plan_info(0, 1, 128, 2048 * 1024, 16, "nhwc", "f16").regime == 0
     assert gn.plan_info(0, 2, 64, 2303, 8, "nchw", "f32").regime == 0       # scalar path
     assert gn.plan_info(1, 2, 16, 4096 * 256, 4, "nchw", "f64").regime == 0  # f64 storage
@@ -263,6 +274,37 @@ def test_wave_plans(gn):
     gn.set_regime(gn.REGIME_WAVE)
     try:
         assert gn.plan_info(0, 1, 128, 2048 * 1024, 16, "nhwc", "f16").regime == 0  # too large
+    finally:
+        gn.set_regime(gn.REGIME_AUTO)
+
+
+def test_flat_plans(gn):
+    """Flat plans: one CTA per SM (at most one per row), one launch (no
+    separate workspace clear), whole row vectors per thread, and a forward
+    that holds each CTA's whole run in shared memory when it fits; only
+    dense, 16-byte aligned channels-last fp32 / fp16 / bf16 problems take it."""
+    gn.set_regime(gn.REGIME_FLAT)
+    try:
+        for N, C, HW, G, dt in ((8, 320, 4096, 32, "bf16"), (32, 512, 1024, 32, "bf16"),
+                                (4, 512, 16384, 32, "bf16"), (2, 64, 300, 8, "f32")):
+            for op in (0, 1):
+                d = gn.plan_info(op, N, C, HW, G, "nhwc", dt)
+                esz = 4 if dt == "f32" else 2
+                assert (d.regime, d.launches, d.ctas) == (4, 1, min(152, N * HW))
+                assert d.threads % (C * esz // 16) == 0 and d.threads <= 512
+                assert 1 <= d.slots <= 32 and d.smem_bytes <= 227 * 1024
+                # a chunk's copy (x, and dy) completes one mbarrier phase
+                assert d.piece_elems * C * esz * (1 + op) < 1 << 20
+        # c4's forward run (216 rows of 1 KiB) stays in shared memory: as many
+        # slots as chunks
+        d = gn.plan_info(0, 32, 512, 1024, 32, "nhwc", "bf16")
+        assert d.slots == d.pieces_per_unit
+        assert gn.plan_info(0, 7, 16, 1, 4, "nhwc", "bf16").ctas == 7  # one row per CTA
+        assert gn.plan_info(0, 2, 64, 2304, 8, "nchw", "f32").regime == 0
+        assert gn.plan_info(0, 2, 40, 99, 8, "nhwc", "f64").regime == 0
+        assert gn.plan_info(0, 2, 40, 99, 8, "nhwc", "f32", aligned=False).regime == 0
+        assert gn.plan_info(0, 3, 6, 77, 3, "nhwc", "f16").regime == 0   # rows not 16-byte vectors
+        assert gn.plan_info(1, 2, 4096, 40, 32, "nhwc", "f16").regime == 0  # 512 columns: scratch too large
     finally:
         gn.set_regime(gn.REGIME_AUTO)
 

@@ -2,9 +2,9 @@
 
 Two host-made failures: GN_FAULT_LAUNCH makes a call fail before it
 enqueues anything; GN_FAULT_STALL makes one wave-regime call withhold one
-piece's arrival, so that the waits on that unit run out (each wait is
-bounded, about 0.5 s) and the kernel returns with the workspace's error word
-set.  In both cases the caller is told (the status, or gn_workspace_status),
+piece's arrival (one flat-regime call, one chunk copy of CTA 0), so that the
+waits on it run out (each wait is bounded, about 0.5 s) and the kernel
+returns with the workspace's error word set.  In both cases the caller is told (the status, or gn_workspace_status),
 the CUDA context stays usable, and the next call is correct.
 """
 from __future__ import annotations
@@ -26,7 +26,12 @@ pytestmark = pytest.mark.gpu
 W = synth.WORKLOADS[2].scaled(name="fault2", N=2, H=32, W=32)
 W_NCHW = synth.WORKLOADS[3].scaled(name="fault3", N=2, H=256, W=256,
                                    gamma=("normal", 1.0, 0.1), beta=("normal", 0.0, 0.1))
-CASES = [pytest.param(W, id="nhwc"), pytest.param(W_NCHW, id="nchw")]
+# the flat regime: CTA 0 never gets its first chunk; the other CTAs read its
+# (missing) records and finish
+W_FLAT = synth.WORKLOADS[4].scaled(name="fault4", N=8, H=32, W=32)
+CASES = [pytest.param(W, "wave", id="nhwc"), pytest.param(W_NCHW, "wave", id="nchw"),
+         pytest.param(W_FLAT, "flat", id="flat_nhwc")]
+REG = {"wave": gn.REGIME_WAVE, "flat": gn.REGIME_FLAT}
 
 
 def _oracle(inp, w):
@@ -40,9 +45,8 @@ def _oracle(inp, w):
 
 
 @pytest.fixture
-def wave():
-    gn.set_regime(gn.REGIME_WAVE)
-    yield
+def forced():
+    yield lambda reg: gn.set_regime(REG[reg])
     gn.set_regime(gn.REGIME_AUTO)
     gn.set_fault_injection(gn.FAULT_NONE)
 
@@ -62,11 +66,12 @@ def _calls(inp, w, ws):
     return (rc_f, st_f, rc_b, st_b), dict(y=y, mean=mean, rstd=rstd, dx=dx, dgamma=dg, dbeta=db)
 
 
-@pytest.mark.parametrize("w", CASES)
-def test_stalled_unit_is_reported_and_the_next_call_is_correct(wave, w):
+@pytest.mark.parametrize("w,reg", CASES)
+def test_stalled_unit_is_reported_and_the_next_call_is_correct(forced, w, reg):
+    forced(reg)
     for op in (gn.OP_FWD, gn.OP_BWD):
         d = gn.plan_info(op, w.N, w.C, w.HW, w.G, w.layout, w.dtype)
-        assert d.regime == gn.REGIME_WAVE and d.pieces_per_unit > 1
+        assert d.regime == REG[reg] and d.pieces_per_unit > 1
     inp = synth.make_inputs(w, "cpu", seed=31)
     ws = gn.alloc_workspace(gn.OP_BWD, w.N, w.C, w.HW, w.G, w.layout, w.dtype)
     gn.set_fault_injection(gn.FAULT_STALL)  # applies to the next call only: the forward
@@ -88,8 +93,9 @@ def test_stalled_unit_is_reported_and_the_next_call_is_correct(wave, w):
     checks.assert_param("dgamma", got["dgamma"], ref["dgamma"])
 
 
-@pytest.mark.parametrize("w", CASES)
-def test_stalled_backward_is_reported(wave, w):
+@pytest.mark.parametrize("w,reg", CASES)
+def test_stalled_backward_is_reported(forced, w, reg):
+    forced(reg)
     inp = synth.make_inputs(w, "cpu", seed=32)
     ws = gn.alloc_workspace(gn.OP_BWD, w.N, w.C, w.HW, w.G, w.layout, w.dtype)
     x, dy = inp["x"].cuda(), inp["dy"].cuda()

@@ -73,7 +73,7 @@ STREAMING = [
 
 
 REGIMES = {"auto": gn.REGIME_AUTO, "two_kernel": gn.REGIME_TWO_KERNEL, "resident": gn.REGIME_RESIDENT,
-           "pipelined": gn.REGIME_PIPELINED, "wave": gn.REGIME_WAVE}
+           "pipelined": gn.REGIME_PIPELINED, "wave": gn.REGIME_WAVE, "flat": gn.REGIME_FLAT}
 
 
 @pytest.fixture(params=list(REGIMES))
@@ -413,6 +413,37 @@ def test_mid_size_wave_straddles():
     assert any(x.ctas % x.pieces_per_unit != 0 for x in d)
 
 
+# Channels-last problems on the flat regime, compared in full: runs that cut
+# samples at odd rows (fp16, 1536 rows per sample), fp32 vectors of four
+# channels with two samples in many runs, and one whose runs (441 KiB) exceed
+# shared memory, so that both passes stream through the ring and pass 2 reads
+# most chunks again.
+MID_FLAT = [
+    ("fp16_nhwc_8x320x32x48_g32", synth.WORKLOADS[2].scaled(name="mf0", dtype="f16", H=32, W=48)),
+    ("fp32_nhwc_16x256x24x24_g16", synth.WORKLOADS[4].scaled(name="mf1", dtype="f32", N=16, C=256, G=16,
+                                                             H=24, W=24)),
+    ("bf16_nhwc_4x512x128x128_g32_ring", synth.WORKLOADS[4].scaled(name="mf2", N=4, H=128, W=128)),
+    ("bf16_nhwc_300x64x1x2_g8_many_samples", synth.WORKLOADS[4].scaled(name="mf3", N=300, C=64, G=8,
+                                                                       H=1, W=2)),
+]
+
+
+@pytest.mark.parametrize("name,w", MID_FLAT, ids=[c[0] for c in MID_FLAT])
+def test_mid_size_flat(name, w):
+    gn.set_regime(gn.REGIME_FLAT)
+    try:
+        plans = [gn.plan_info(op, w.N, w.C, w.HW, w.G, w.layout, w.dtype) for op in (0, 1)]
+        assert all(d.regime == gn.REGIME_FLAT for d in plans)
+        inp = synth.make_inputs(w, "cpu", seed=4)
+        got = _gpu_run(inp, w)
+        again = _gpu_run(inp, w)
+    finally:
+        gn.set_regime(gn.REGIME_AUTO)
+    _compare(got, _oracle_full(inp, w), w)
+    for k in got:
+        assert torch.equal(got[k], again[k]), k
+
+
 FULL_COMPARE = {"bf16_nhwc_8x320x64x64_g32", "bf16_nhwc_32x512x32x32_g32"}
 
 
@@ -506,7 +537,8 @@ def _oracle_by_samples(w, inp, idx=None):
 
 FULL = ([(w, "auto") for w in synth.WORKLOADS[1:]]
         + [(synth.WORKLOADS[3], "two_kernel"), (synth.WORKLOADS[2], "resident"),
-           (synth.WORKLOADS[4], "two_kernel"), (synth.WORKLOADS[2], "two_kernel")])
+           (synth.WORKLOADS[4], "two_kernel"), (synth.WORKLOADS[2], "two_kernel"),
+           (synth.WORKLOADS[2], "flat"), (synth.WORKLOADS[4], "flat")])
 
 
 @pytest.mark.parametrize("w,reg", FULL, ids=[f"{w.name}-{r}" for w, r in FULL])
