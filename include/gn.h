@@ -251,7 +251,8 @@ GN_API int gn_set_timing_events(void* ev_begin, void* ev_mid, void* ev_end);
  * (in tensor memory where the piece fits there twice, with the reduce and
  * the output on separate warps), so the input is read from HBM once; it is
  * taken where every unit fits on the co-resident CTAs, and chosen
- * automatically for NCHW problems with units of at least 4 MiB.  GN_REGIME_FLAT
+ * automatically for NCHW problems of at least 32 MiB whose units hold at least
+ * 64 KiB.  GN_REGIME_FLAT
  * runs one cooperative kernel for dense, 16-byte aligned channels-last fp32 /
  * fp16 / bf16 data of at most 512 16-byte vectors per row: the N*HW rows are
  * cut into equal runs, one per SM, each read by bulk copies into shared
