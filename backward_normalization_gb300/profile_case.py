@@ -35,7 +35,7 @@ def main(argv=None) -> int:
     ap.add_argument("--H", type=int)
     ap.add_argument("--W", type=int)
     ap.add_argument("--calls", type=int, default=2)
-    ap.add_argument("--regime", choices=["auto", "two_kernel", "resident", "pipelined", "wave"],
+    ap.add_argument("--regime", choices=["auto", "two_kernel", "resident", "pipelined", "wave", "flat"],
                     default="auto")
     a = ap.parse_args(argv)
     if a.row_workload:
@@ -48,7 +48,7 @@ def main(argv=None) -> int:
         w = w.scaled(**over)
     gn.set_regime({"auto": gn.REGIME_AUTO, "two_kernel": gn.REGIME_TWO_KERNEL,
                    "resident": gn.REGIME_RESIDENT, "pipelined": gn.REGIME_PIPELINED,
-                   "wave": gn.REGIME_WAVE}[a.regime])
+                   "wave": gn.REGIME_WAVE, "flat": gn.REGIME_FLAT}[a.regime])
     inp = synth.make_inputs(w, "cuda", seed=0)
     x, dy, gm, bt = inp["x"], inp["dy"], inp["gamma"], inp["beta"]
     y, dx = torch.empty_like(x), torch.empty_like(x)

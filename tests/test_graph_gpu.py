@@ -1,7 +1,8 @@
 """GPU: the library's calls capture into a CUDA graph (the launch-bound small
 problems replay without per-call launch cost) and replay bit-identically to
 the eager calls, for every kernel family (two-kernel with programmatic
-dependent launch, resident clusters, the cooperative wave kernel, rows)."""
+dependent launch, resident clusters, the cooperative wave and flat kernels,
+rows)."""
 from __future__ import annotations
 
 import pytest
@@ -23,6 +24,9 @@ CASES = [
      gn.REGIME_WAVE),
     ("fp32_nchw_4x64x48x48_g8_wave", synth.WORKLOADS[3].scaled(name="g3w", N=4, H=48, W=48),
      gn.REGIME_WAVE),
+    # one cooperative launch per op with two grid barriers
+    ("bf16_nhwc_8x320x16x16_g32_flat", synth.WORKLOADS[2].scaled(name="g2f", H=16, W=16),
+     gn.REGIME_FLAT),
 ]
 
 
