@@ -533,12 +533,16 @@ RowPlan row_plan(int64_t M, int64_t N, int dtype, bool rms, bool bwd, bool align
   // 16 for small ones, whose rows are latency-bound (measured on GB300: the
   // small shapes of the benchmark table gain 2 us, e.g. LayerNorm fp32
   // 4096x1024 14.3 -> 12.3 us, RMSNorm fp16 4096x1024 10.7 -> 8.2 us)
-  const int cap = bwd || (double)M * (double)N <= 16.0 * (1 << 20) ? 16 : 32;
-  int vmax = cap / pl.vw;
-  if (vmax > 8) vmax = 8;
-  if (vmax < 1) vmax = 1;
+  // Rows too long for a team of kRowThreads at the small-problem cap take
+  // more values per thread, up to the large one (the row limit stays 256 x 32
+  // values in the forward).
+  const int cap_max = bwd ? 16 : 32;
+  const int cap = (double)M * (double)N <= 16.0 * (1 << 20) ? 16 : cap_max;
+  auto clampv = [](int v) { return v > 8 ? 8 : (v < 1 ? 1 : v); };
+  const int vmax = clampv(cap / pl.vw), vmax_hi = clampv(cap_max / pl.vw);
   int vpt = 1;
   while (vpt < vmax && vpt < pl.V) vpt <<= 1;
+  while (pow2ceil(cdiv64(pl.V, vpt)) > kRowThreads && vpt < vmax_hi) vpt <<= 1;
   pl.vpt = vpt;
   pl.tw = pow2ceil(cdiv64(pl.V, vpt));
   if (pl.tw > kRowThreads) return pl;  // rows too long to hold in one CTA's registers

@@ -115,6 +115,36 @@ def test_validation_before_any_launch(gn):
     assert _bwd(gn, ws_bytes=need - 1) == WS
 
 
+def test_row_length_limit_independent_of_problem_size(gn):
+    """LayerNorm / RMSNorm forward rows up to 256 threads x 32 values (8192
+    values, fp32 too) are planned whatever the row count (small problems take
+    fewer values per thread only where the row still fits a team); the
+    backward takes rows up to 256 x 16 values (4096); longer rows give
+    GN_ERR_UNSUPPORTED.  Checked on the host: without a device a planned call
+    goes on to its launch and fails there (GN_ERR_CUDA), an unplannable one
+    is refused before."""
+    L = gn.lib()
+    x, y, mean, rstd = 1 << 40, 2 << 40, 3 << 40, (3 << 40) + (1 << 32)
+    dx, dy, ws = 4 << 40, 5 << 40, 6 << 40
+
+    def fwd(M, N, dt, rms=False):
+        if rms:
+            return L.rms_fwd(x, M, N, dt, None, 1e-5, y, rstd, None)
+        return L.ln_fwd(x, M, N, dt, None, None, 1e-5, y, mean, rstd, None)
+
+    def bwd(M, N, dt):
+        return L.ln_bwd(dy, x, mean, rstd, None, M, N, dt, dx, None, None, ws, 1 << 30, None)
+
+    UNS = gn.GN_ERR_UNSUPPORTED
+    for M in (1, 64, 2048, 131072):
+        for dt in (1, 2):  # fp16, bf16
+            assert fwd(M, 8192, dt) != UNS and fwd(M, 8192, dt, rms=True) != UNS
+            assert fwd(M, 4096, dt) != UNS and fwd(M, 16384, dt) == UNS
+            assert bwd(M, 4096, dt) != UNS and bwd(M, 8192, dt) == UNS
+        assert fwd(M, 8192, 0) != UNS and fwd(M, 16384, 0) == UNS  # fp32
+        assert bwd(M, 4096, 0) != UNS and bwd(M, 8192, 0) == UNS
+
+
 def test_plan_vector_width_and_modes(gn):
     d = gn.plan_info(0, 1, 128, 2048 * 1024, 16, "nhwc", "f16")
     assert d.vector_width == 8 and d.launches == 3  # workspace clear + two kernels

@@ -90,6 +90,35 @@ def test_row_small_parity(w):
     _compare(_gpu(inp, w), _oracle(inp, w), w)
 
 
+# Forward rows longer than a team of 256 threads holds at a small problem's
+# 16 values per thread: the plan takes 32 values per thread (LayerNorm then
+# stages gamma and beta in shared memory).  The backward's rows stop at 4096.
+LONG_FWD = [
+    RW("ln_f16_64x8192", "ln", "f16", 64, 8192),
+    RW("rms_bf16_3x8192", "rms", "bf16", 3, 8192),
+    RW("ln_f32_16x8192", "ln", "f32", 16, 8192),
+]
+
+
+@pytest.mark.parametrize("w", LONG_FWD, ids=[w.name for w in LONG_FWD])
+def test_row_forward_long_rows(w):
+    inp = synth.make_row_inputs(w, "cpu", seed=5)
+    ro = oracle.get_row()
+    x = inp["x"].double().numpy()
+    g, b = inp["gamma"].double().numpy(), inp["beta"].double().numpy()
+    xd, gd, bd = inp["x"].cuda(), inp["gamma"].cuda(), inp["beta"].cuda()
+    if w.op == "ln":
+        y, mean, rstd = gn.ln_forward(xd, w.M, w.N, gd, bd, w.eps)
+        ry, rmean, rrstd = ro.ln_forward(x, w.M, w.N, g, b, w.eps)
+        checks.assert_stat("mean", mean, rmean)
+    else:
+        y, rstd = gn.rms_forward(xd, w.M, w.N, gd, w.eps)
+        ry, rrstd = ro.rms_forward(x, w.M, w.N, g, w.eps)
+    torch.cuda.synchronize()
+    checks.assert_out("y", y, ry, w.dtype)
+    checks.assert_stat("rstd", rstd, rrstd)
+
+
 @pytest.mark.parametrize("w", [SMALL[1], SMALL[3], SMALL[11]], ids=lambda w: w.name)
 def test_row_bit_identical_runs(w):
     inp = synth.make_row_inputs(w, "cpu", seed=1)
