@@ -529,15 +529,19 @@ RowPlan row_plan(int64_t M, int64_t N, int dtype, bool rms, bool bwd, bool align
   const int esz = dtype == kF32 ? 4 : 2;
   pl.vw = (aligned && (N * esz) % 16 == 0) ? 16 / esz : 1;  // aligned: bases and strides
   pl.V = N / pl.vw;
-  // forward: 32 values per thread for large problems (more bytes in flight),
-  // 16 for small ones, whose rows are latency-bound (measured on GB300: the
-  // small shapes of the benchmark table gain 2 us, e.g. LayerNorm fp32
-  // 4096x1024 14.3 -> 12.3 us, RMSNorm fp16 4096x1024 10.7 -> 8.2 us)
+  // forward: 32 values per thread for large problems (more bytes in flight);
+  // small ones, whose rows are latency-bound, take two 16-byte vectors per
+  // thread (16 values at 16 bits, 8 in fp32).  Measured on GB300 on the
+  // benchmark table's small shapes: one vector per thread is slower, and four
+  // too (RMSNorm fp16 4096x1024 10.7 us at four vectors, 8.2 us at two;
+  // LayerNorm fp32 4096x1024 14.3 us at eight, 12.3 at four, 10.2 at two).
   // Rows too long for a team of kRowThreads at the small-problem cap take
   // more values per thread, up to the large one (the row limit stays 256 x 32
   // values in the forward).
+  // The backward keeps 16 values per thread at every size.
+  const bool small = (double)M * (double)N <= 16.0 * (1 << 20);
   const int cap_max = bwd ? 16 : 32;
-  const int cap = (double)M * (double)N <= 16.0 * (1 << 20) ? 16 : cap_max;
+  const int cap = !small || bwd ? cap_max : (pl.vw > 1 ? 2 * pl.vw : 16);
   auto clampv = [](int v) { return v > 8 ? 8 : (v < 1 ? 1 : v); };
   const int vmax = clampv(cap / pl.vw), vmax_hi = clampv(cap_max / pl.vw);
   int vpt = 1;
